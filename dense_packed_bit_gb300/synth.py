@@ -1,0 +1,245 @@
+"""Seeded synthetic inputs shared by the CUDA path, the oracle tests and the bench.
+
+This module holds no arithmetic of the method itself (no products, no sums, no
+unpacking): it only draws numbers.  Both sides of every parity comparison take
+their inputs from here, so neither needs to trust the other's generator.
+
+Generator: SplitMix64 used as a counter-based generator (Steele, Lea and Flood,
+"Fast splittable pseudorandom number generators", OOPSLA 2014; the finaliser
+constants are Vigna's published ones).  Draw i of stream `seed` is
+``mix(seed * 2**32 + i + 1)`` where ``mix`` is the SplitMix64 output function
+applied to ``state = counter * golden_gamma``.  It is written out here with
+numpy uint64 arithmetic (which wraps mod 2**64), so every machine and numpy
+version produces the same bits.
+
+Value recipes (the shapes and distributions of the workloads on the pages):
+  * uniform fp32 on [lo, hi): fp64 ``lo + (hi-lo)*u`` rounded to fp32 (RNE),
+    with ``u = (z >> 11) * 2**-53``; a value that rounds up to ``hi`` is
+    replaced by the next fp32 below ``hi``.
+  * normal(0, sigma): Box-Muller in fp64 from two draws, rounded to fp32 or
+    to fp16 (RNE).  fp16 values are returned as their uint16 bit patterns.
+  * uniform 2-bit codes: uniformly random bytes (four iid uniform 2-bit
+    fields per byte, as the Kernel 0112 page's "random bytes" matrices).
+  * ternary codes: each 2-bit field iid with P(field=0)=0.25, P(1)=0.5,
+    P(2)=0.25 (field value = ternary value + 1), the fields of one byte
+    independent, so the byte is a random draw whose meaning does not depend
+    on the bit order inside the byte.
+"""
+from __future__ import annotations
+
+import hashlib
+from dataclasses import dataclass
+
+import numpy as np
+
+_GAMMA = np.uint64(0x9E3779B97F4A7C15)
+_M1 = np.uint64(0xBF58476D1CE4E5B9)
+_M2 = np.uint64(0x94D049BB133111EB)
+
+
+def _splitmix64(seed: int, n: int, offset: int = 0) -> np.ndarray:
+    """n consecutive SplitMix64 outputs of stream `seed`, starting at draw `offset`."""
+    base = np.uint64((int(seed) << 32) & 0xFFFFFFFFFFFFFFFF)
+    ctr = np.arange(offset + 1, offset + n + 1, dtype=np.uint64) + base
+    with np.errstate(over="ignore"):
+        z = ctr * _GAMMA
+        z = (z ^ (z >> np.uint64(30))) * _M1
+        z = (z ^ (z >> np.uint64(27))) * _M2
+        z = z ^ (z >> np.uint64(31))
+    return z
+
+
+def _unit_open0(z: np.ndarray) -> np.ndarray:
+    """uniform on [0, 1) with 53 random bits."""
+    return (z >> np.uint64(11)).astype(np.float64) * (2.0 ** -53)
+
+
+def _unit_open1(z: np.ndarray) -> np.ndarray:
+    """uniform on (0, 1] with 53 random bits (safe for log)."""
+    return ((z >> np.uint64(11)).astype(np.float64) + 1.0) * (2.0 ** -53)
+
+
+def uniform_f32(seed: int, shape, lo: float = -1.0, hi: float = 1.0) -> np.ndarray:
+    n = int(np.prod(shape))
+    u = _unit_open0(_splitmix64(seed, n))
+    v = (lo + (hi - lo) * u).astype(np.float32)
+    top = np.nextafter(np.float32(hi), np.float32(lo))
+    v = np.where(v >= np.float32(hi), top, v)
+    return v.reshape(shape)
+
+
+def normal_f64(seed: int, n: int, sigma: float = 1.0) -> np.ndarray:
+    z = _splitmix64(seed, 2 * n)
+    u1 = _unit_open1(z[0::2])
+    u2 = _unit_open0(z[1::2])
+    return sigma * np.sqrt(-2.0 * np.log(u1)) * np.cos(2.0 * np.pi * u2)
+
+
+def normal_f32(seed: int, shape, sigma: float = 1.0) -> np.ndarray:
+    n = int(np.prod(shape))
+    return normal_f64(seed, n, sigma).astype(np.float32).reshape(shape)
+
+
+def normal_f16_bits(seed: int, shape, sigma: float = 1.0) -> np.ndarray:
+    n = int(np.prod(shape))
+    return normal_f64(seed, n, sigma).astype(np.float16).view(np.uint16).reshape(shape)
+
+
+def uniform_f16_bits(seed: int, shape, lo: float, hi: float) -> np.ndarray:
+    """fp16 bit patterns of fp64 uniform[lo, hi) values rounded RNE."""
+    n = int(np.prod(shape))
+    u = _unit_open0(_splitmix64(seed, n))
+    v = (lo + (hi - lo) * u).astype(np.float16)
+    top = np.nextafter(np.float16(hi), np.float16(lo))
+    v = np.where(v >= np.float16(hi), top, v)
+    return v.view(np.uint16).reshape(shape)
+
+
+def random_bytes(seed: int, n: int) -> np.ndarray:
+    """n uniformly random bytes (8 per SplitMix64 draw, low byte first)."""
+    words = _splitmix64(seed, (n + 7) // 8)
+    out = np.empty((len(words), 8), dtype=np.uint8)
+    for b in range(8):
+        out[:, b] = ((words >> np.uint64(8 * b)) & np.uint64(0xFF)).astype(np.uint8)
+    return out.reshape(-1)[:n].copy()
+
+
+def ternary_field_bytes(seed: int, n: int) -> np.ndarray:
+    """n bytes whose four 2-bit fields are iid: 0 w.p. 1/4, 1 w.p. 1/2, 2 w.p. 1/4.
+
+    Each field uses two fresh random bits r: r=0 -> 0, r in {1,2} -> 1, r=3 -> 2.
+    """
+    rnd = random_bytes(seed, n)
+    out = np.zeros(n, dtype=np.uint8)
+    for f in range(4):
+        r = (rnd >> np.uint8(2 * f)) & np.uint8(3)
+        field = np.where(r == 0, 0, np.where(r == 3, 2, 1)).astype(np.uint8)
+        out |= field << np.uint8(2 * f)
+    return out
+
+
+def digest(*arrays) -> str:
+    """SHA-256 over the raw bytes of the given arrays (detects silent input drift)."""
+    h = hashlib.sha256()
+    for a in arrays:
+        a = np.ascontiguousarray(a)
+        h.update(str(a.dtype).encode())
+        h.update(str(a.shape).encode())
+        h.update(a.tobytes())
+    return h.hexdigest()
+
+
+# --------------------------------------------------------------------------
+# Workloads.  Each is named by what it is, with its sizes.  Seeds are fixed
+# per (workload, tensor, index) so a workload is reproducible bit for bit.
+# --------------------------------------------------------------------------
+
+def _seed(workload_id: int, tensor_id: int, index: int = 0) -> int:
+    return (workload_id * 1000 + tensor_id) * 1000 + index
+
+
+@dataclass
+class GemmCase:
+    name: str
+    transA: int
+    transB: int
+    M: int
+    N: int
+    K: int
+    A: np.ndarray  # stored (M,K) or (K,M) if transA
+    B: np.ndarray  # stored (K,N) or (N,K) if transB
+
+
+def gemm_case(name, transA, transB, M, N, K, dist, seed_base, sigma=0.02):
+    a_shape = (K, M) if transA else (M, K)
+    b_shape = (N, K) if transB else (K, N)
+    if dist == "uniform":
+        A = uniform_f32(_seed(seed_base, 1), a_shape, -1.0, 1.0)
+        B = uniform_f32(_seed(seed_base, 2), b_shape, -1.0, 1.0)
+    elif dist == "normal":
+        A = normal_f32(_seed(seed_base, 1), a_shape, sigma)
+        B = normal_f32(_seed(seed_base, 2), b_shape, sigma)
+    else:
+        raise ValueError(dist)
+    return GemmCase(name, transA, transB, M, N, K, A, B)
+
+
+def gpt2_mlp_up_64x768x3072() -> GemmCase:
+    """GPT-2-small MLP up-projection, 64 tokens: C(64x3072) = A(64x768) B(768x3072), U[-1,1)."""
+    return gemm_case("gpt2_mlp_up_m64_k768_n3072_nn", 0, 0, 64, 3072, 768, "uniform", 1)
+
+
+def square_2048(layout: str) -> GemmCase:
+    """Square 2048^3 fp32 GEMM, N(0,0.02) operands, layout 'nn' | 'nt' | 'tn'."""
+    tA, tB = {"nn": (0, 0), "nt": (0, 1), "tn": (1, 0)}[layout]
+    return gemm_case(f"square_2048_{layout}", tA, tB, 2048, 2048, 2048, "normal",
+                     2 + {"nn": 0, "nt": 10, "tn": 20}[layout])
+
+
+def training_set_8192(which: str) -> GemmCase:
+    """Training-shape products (batch 16 x seq 512 = 8192 rows, d=2048, d_ff=8192).
+
+    'fwd': C = A(8192x2048) B(2048x8192)            (NN)
+    'dA' : dA = dC(8192x8192) B^T, B stored 2048x8192 (NT: M=8192,N=2048,K=8192)
+    'dB' : dB = A^T dC, A stored 8192x2048            (TN: M=2048,N=8192,K=8192)
+    All operands N(0,0.02); A, B and dC each come from one fixed stream.
+    """
+    A = normal_f32(_seed(5, 1), (8192, 2048), 0.02)
+    B = normal_f32(_seed(5, 2), (2048, 8192), 0.02)
+    if which == "fwd":
+        return GemmCase("train_fwd_8192x8192x2048_nn", 0, 0, 8192, 8192, 2048, A, B)
+    dC = normal_f32(_seed(5, 3), (8192, 8192), 0.02)
+    if which == "dA":
+        return GemmCase("train_dA_8192x2048x8192_nt", 0, 1, 8192, 2048, 8192, dC, B)
+    if which == "dB":
+        return GemmCase("train_dB_2048x8192x8192_tn", 1, 0, 2048, 8192, 8192, A, dC)
+    raise ValueError(which)
+
+
+@dataclass
+class PackedCase:
+    name: str
+    rows: int
+    cols: int
+    codes: np.ndarray      # (rows, ceil(cols/4)) uint8
+    scales: np.ndarray     # (rows,) uint16 fp16 bits
+    codebook: np.ndarray   # (4,) float32
+    X: np.ndarray          # (M, cols) uint16 fp16 bits; M=1 for a GEMV
+
+
+CODEBOOK_2BIT = np.array([-2.0, -1.0, 0.0, 1.0], dtype=np.float32)
+# Ternary values v in {-1,0,+1} are stored as field v+1; field 3 never occurs and means 0.
+CODEBOOK_TERNARY = np.array([-1.0, 0.0, 1.0, 0.0], dtype=np.float32)
+
+
+def packed_matrix(seed_base, index, rows, cols, kind):
+    nbytes = rows * ((cols + 3) // 4)
+    if kind == "uniform2":
+        codes = random_bytes(_seed(seed_base, 1, index), nbytes)
+    elif kind == "ternary":
+        codes = ternary_field_bytes(_seed(seed_base, 1, index), nbytes)
+    else:
+        raise ValueError(kind)
+    scales = uniform_f16_bits(_seed(seed_base, 2, index), (rows,), 0.005, 0.05)
+    return codes.reshape(rows, (cols + 3) // 4), scales
+
+
+def gemv_2bit_12288x1536(index: int) -> PackedCase:
+    """One of the 64 rotated 2-bit GEMV matrices: 12288 rows x 1536 cols (4.5 MiB of codes)."""
+    codes, scales = packed_matrix(3, index, 12288, 1536, "uniform2")
+    x = normal_f16_bits(_seed(3, 3, 0), (1, 1536))
+    return PackedCase(f"gemv2_12288x1536_m{index}", 12288, 1536, codes, scales,
+                      CODEBOOK_2BIT.copy(), x)
+
+
+def ternary_encoder_layer(layer: int, proj: str) -> PackedCase:
+    """Layer `layer` (0..15) of the ternary 16-layer encoder block, M = 2 x 111 = 222 rows.
+
+    proj 'up'  : W 3072 x 768  (N=3072, K=768)
+    proj 'down': W 768 x 3072  (N=768,  K=3072)
+    """
+    rows, cols, pid = (3072, 768, 0) if proj == "up" else (768, 3072, 1)
+    codes, scales = packed_matrix(4, 2 * layer + pid, rows, cols, "ternary")
+    X = normal_f16_bits(_seed(4, 3, 2 * layer + pid), (222, cols))
+    return PackedCase(f"ternary_enc_l{layer}_{proj}", rows, cols, codes, scales,
+                      CODEBOOK_TERNARY.copy(), X)

@@ -1,0 +1,163 @@
+"""CPU oracle for the dense fp32 GEMM and the packed 2-bit GEMV / skinny GEMM.
+
+TEST INFRASTRUCTURE.  Only the tests, the smoke check and the bench's CPU
+baseline leg may import this package.  The product library never loads it and
+there is no fallback from the CUDA path to it.
+
+The arithmetic lives in ``oracle.c`` (plain C, fp64 accumulation, a scalar
+bit unpacker); this module only compiles it with gcc and marshals numpy arrays
+through ctypes.  Every function returns the value and T = sum_k |term_k|,
+the scale of the acceptance bound |y - y_ref| <= 1e-5 * T.
+
+Pins (tests/test_oracle.py): closed forms (all-ones, identity, rank-1),
+textbook small products, exact integer products against numpy int64 matmul,
+the fp16 decoder against numpy's float16 for all 65,536 patterns, the unpacker
+against a hand-written byte table and a pack/unpack round trip, and the packed
+GEMM against dense products of explicitly decoded weights.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "oracle.c")
+_LIB = os.path.join(_HERE, "liboracle.so")
+_lock = threading.Lock()
+_lib = None
+
+
+def build(force: bool = False) -> str:
+    """Compile oracle.c into oracle/liboracle.so with gcc (plain -O2, portable)."""
+    if force or not os.path.exists(_LIB) or os.path.getmtime(_LIB) < os.path.getmtime(_SRC):
+        tmp = _LIB + f".tmp{os.getpid()}"
+        subprocess.check_call(["gcc", "-O2", "-std=c11", "-fPIC", "-shared", "-pthread",
+                               "-o", tmp, _SRC, "-lm"])
+        os.replace(tmp, _LIB)
+    return _LIB
+
+
+def _load():
+    global _lib
+    with _lock:
+        if _lib is None:
+            build()
+            lib = ctypes.CDLL(_LIB)
+            P = ctypes.c_void_p
+            I64 = ctypes.c_int64
+            I = ctypes.c_int
+            lib.orc_half_to_double.argtypes = [ctypes.c_uint16]
+            lib.orc_half_to_double.restype = ctypes.c_double
+            lib.orc_unpack2.argtypes = [P, I64, I64, P]
+            lib.orc_pack2.argtypes = [P, I64, I64, P]
+            lib.orc_gemm.argtypes = [I, I, I64, I64, I64, P, I64, P, I64, P, P, I]
+            lib.orc_gemm_at.argtypes = [I, I, I64, P, I64, P, I64, I64, P, P, P, P]
+            lib.orc_packed_gemm.argtypes = [P, P, P, I64, I64, I64, P, P, P, I]
+            lib.orc_packed_gemm_at.argtypes = [P, P, P, I64, P, I64, P, P, P, P]
+            _lib = lib
+    return _lib
+
+
+def _ptr(a: np.ndarray):
+    return a.ctypes.data_as(ctypes.c_void_p)
+
+
+def default_threads() -> int:
+    return max(1, len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else os.cpu_count())
+
+
+def half_to_double(bits) -> np.ndarray:
+    lib = _load()
+    b = np.asarray(bits, dtype=np.uint16).reshape(-1)
+    return np.array([lib.orc_half_to_double(int(v)) for v in b], dtype=np.float64)
+
+
+def unpack2(codes: np.ndarray, rows: int, cols: int) -> np.ndarray:
+    lib = _load()
+    c = np.ascontiguousarray(codes, dtype=np.uint8)
+    assert c.size == rows * ((cols + 3) // 4)
+    out = np.empty((rows, cols), dtype=np.uint8)
+    lib.orc_unpack2(_ptr(c), rows, cols, _ptr(out))
+    return out
+
+
+def pack2(fields: np.ndarray) -> np.ndarray:
+    lib = _load()
+    f = np.ascontiguousarray(fields, dtype=np.uint8)
+    rows, cols = f.shape
+    out = np.empty((rows, (cols + 3) // 4), dtype=np.uint8)
+    lib.orc_pack2(_ptr(f), rows, cols, _ptr(out))
+    return out
+
+
+def gemm(transA: int, transB: int, M: int, N: int, K: int, A: np.ndarray, B: np.ndarray,
+         lda: int | None = None, ldb: int | None = None, threads: int | None = None):
+    """(C, T), both (M, N) float64, of C = op(A) op(B) from fp32 A, B (row-major)."""
+    lib = _load()
+    A = np.ascontiguousarray(A, dtype=np.float32)
+    B = np.ascontiguousarray(B, dtype=np.float32)
+    if lda is None:
+        lda = A.shape[-1]
+    if ldb is None:
+        ldb = B.shape[-1]
+    C = np.empty((M, N), dtype=np.float64)
+    T = np.empty((M, N), dtype=np.float64)
+    lib.orc_gemm(int(transA), int(transB), M, N, K, _ptr(A), lda, _ptr(B), ldb,
+                 _ptr(C), _ptr(T), threads or default_threads())
+    return C, T
+
+
+def gemm_at(transA: int, transB: int, K: int, A: np.ndarray, B: np.ndarray, ii, jj,
+            lda: int | None = None, ldb: int | None = None):
+    """(C, T) at the listed output coordinates (ii[n], jj[n])."""
+    lib = _load()
+    A = np.ascontiguousarray(A, dtype=np.float32)
+    B = np.ascontiguousarray(B, dtype=np.float32)
+    if lda is None:
+        lda = A.shape[-1]
+    if ldb is None:
+        ldb = B.shape[-1]
+    ii = np.ascontiguousarray(ii, dtype=np.int64)
+    jj = np.ascontiguousarray(jj, dtype=np.int64)
+    C = np.empty(len(ii), dtype=np.float64)
+    T = np.empty(len(ii), dtype=np.float64)
+    lib.orc_gemm_at(int(transA), int(transB), K, _ptr(A), lda, _ptr(B), ldb, len(ii),
+                    _ptr(ii), _ptr(jj), _ptr(C), _ptr(T))
+    return C, T
+
+
+def packed_gemm(codes: np.ndarray, scales: np.ndarray, X: np.ndarray, rows: int, cols: int,
+                codebook, threads: int | None = None):
+    """(Y, T), both (M, rows) float64, Y[m,r] = sum_k scale_r cb[field(r,k)] X[m,k]."""
+    lib = _load()
+    codes = np.ascontiguousarray(codes, dtype=np.uint8)
+    scales = np.ascontiguousarray(scales, dtype=np.uint16)
+    X = np.ascontiguousarray(X, dtype=np.uint16).reshape(-1, cols)
+    cb = np.ascontiguousarray(codebook, dtype=np.float32)
+    assert cb.size == 4 and scales.size == rows and codes.size == rows * ((cols + 3) // 4)
+    M = X.shape[0]
+    Y = np.empty((M, rows), dtype=np.float64)
+    T = np.empty((M, rows), dtype=np.float64)
+    lib.orc_packed_gemm(_ptr(codes), _ptr(scales), _ptr(X), M, rows, cols, _ptr(cb),
+                        _ptr(Y), _ptr(T), threads or default_threads())
+    return Y, T
+
+
+def packed_gemm_at(codes, scales, X, cols: int, codebook, mm, rr):
+    """(Y, T) at the listed coordinates (mm[n], rr[n])."""
+    lib = _load()
+    codes = np.ascontiguousarray(codes, dtype=np.uint8)
+    scales = np.ascontiguousarray(scales, dtype=np.uint16)
+    X = np.ascontiguousarray(X, dtype=np.uint16).reshape(-1, cols)
+    cb = np.ascontiguousarray(codebook, dtype=np.float32)
+    mm = np.ascontiguousarray(mm, dtype=np.int64)
+    rr = np.ascontiguousarray(rr, dtype=np.int64)
+    Y = np.empty(len(mm), dtype=np.float64)
+    T = np.empty(len(mm), dtype=np.float64)
+    lib.orc_packed_gemm_at(_ptr(codes), _ptr(scales), _ptr(X), cols, _ptr(cb), len(mm),
+                           _ptr(mm), _ptr(rr), _ptr(Y), _ptr(T))
+    return Y, T
