@@ -1,0 +1,488 @@
+#!/usr/bin/env python
+"""Benchmark of the dense fp32 GEMM and packed 2-bit GEMV / skinny GEMM path on GB300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl mm|reference]
+
+Prints ONE JSON line (rank 0).  One step is one pass of the whole hot path:
+  1. square 2048^3 fp32 GEMM in the NN, NT and TN layouts (L2 flushed first
+     by writing a 512 MiB buffer, since the 48 MiB of operands fit in L2);
+  2. the 2-bit 12,288 x 1,536 GEMV over a rotation of 64 distinct matrices
+     (288 MiB of codes, larger than the 129 MB L2), back to back, launched with
+     programmatic dependent launch (weights are static, so their loads start
+     before the wait on the previous call);
+  3. the ternary 16-layer encoder block: 16 x (222x768 -> 3072, 222x3072 -> 768).
+Each phase is timed with CUDA events on the stream the kernels run on.  The
+headline value is the 2048^3 GEMM throughput (TFLOP/s); the GEMV weight
+bandwidth (GB/s, 4,718,592 bytes of weights per call over the per-call time,
+the measure defined on the Kernel 0112 page) is reported beside it.
+
+Multi-GPU (torchrun): every rank runs the same step on its own GPU with its own
+inputs (replicas, weak scaling, no collective on the data path); times are
+max-reduced over ranks and `value` counts the work of all ranks.
+
+--impl reference times the CPU oracle (plain fp64 C triple loops) on the same
+workload on this host's cores, on a bounded sample per step.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "2048³ fp32 GEMM TFLOP/s; 2-bit 12288×1536 GEMV weight GB/s vs HBM peak"
+GEMV_WEIGHT_BYTES = 12288 * 1536 // 4           # 4,718,592
+GEMV_TOTAL_BYTES = GEMV_WEIGHT_BYTES + 12288 * 2 + 1536 * 2 + 12288 * 4
+GEMM_FLOP = 2.0 * 2048 ** 3
+TERN_FLOP_PER_LAYER = 2 * (2.0 * 222 * 3072 * 768)
+N_GEMV = 64
+N_LAYERS = 16
+WORKLOAD = ("square_2048_fp32_gemm_nn_nt_tn + gemv2bit_12288x1536_rotation64 + "
+            "ternary_encoder_16x(222x768x3072,222x3072x768)")
+
+
+def parse_args(argv=None):
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", choices=["mm", "reference"], default="mm")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--gemv-split", type=int, default=8)
+    ap.add_argument("--gemv-rows", type=int, default=4)
+    ap.add_argument("--gemv-warps", type=int, default=4)
+    ap.add_argument("--gemm-path", type=int, default=0)
+    return ap.parse_args(argv)
+
+
+# ---------------------------------------------------------------- distributed helpers
+
+def dist_env():
+    return (int(os.environ.get("RANK", "0")), int(os.environ.get("WORLD_SIZE", "1")),
+            int(os.environ.get("LOCAL_RANK", "0")))
+
+
+def dist_init(backend):
+    rank, world, _ = dist_env()
+    if world > 1:
+        import torch.distributed as dist
+        if not dist.is_initialized():
+            dist.init_process_group(backend=backend)
+    return rank, world
+
+
+def reduce_max(value: float, device=None) -> float:
+    """Max of `value` over all ranks (identity when not distributed)."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return value
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(device=None):
+    import torch.distributed as dist
+    if dist.is_available() and dist.is_initialized() and dist.get_world_size() > 1:
+        if device is not None and device.type == "cuda":
+            dist.barrier(device_ids=[device.index])
+        else:
+            dist.barrier()
+
+
+def rank_seed_offset(rank: int) -> int:
+    """Each rank draws its own inputs (weak scaling): seeds are offset per rank."""
+    return 7919 * rank
+
+
+# ---------------------------------------------------------------- clocks
+
+class ClockSampler:
+    """nvidia-smi sampled every 200 ms while the timed region runs."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu_index = gpu_index
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        fd, self.path = tempfile.mkstemp(prefix="clocks_", suffix=".csv")
+        os.close(fd)
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu_index), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except (FileNotFoundError, OSError):
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        time.sleep(0.25)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        with open(self.path) as f:
+            for line in f:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) < 9:
+                    continue
+                try:
+                    sm.append(float(parts[1]))
+                    smax.append(float(parts[2]))
+                except ValueError:
+                    continue
+                for n, v in zip(names, parts[5:9]):
+                    if v.lower() in ("active", "1", "0x1"):
+                        reasons.add(n)
+        os.unlink(self.path)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(smax) if smax else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ---------------------------------------------------------------- peaks
+
+def measured_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return d, "measured"
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0,
+            "sm_max_mhz": 2070.0}, "fallback"
+
+
+def fp32_simt_peak_tflops(sms: int, mhz: float) -> float:
+    # 128 FP32 lanes per SM, 2 flop per FMA
+    return sms * 128 * 2 * mhz * 1e6 / 1e12
+
+
+def traffic_for(kernel_key: str):
+    """DRAM bytes per launch from the committed ncu summary, if it still matches the source."""
+    p = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(p):
+        return None
+    with open(p) as f:
+        d = json.load(f)
+    e = d.get(kernel_key)
+    if not e:
+        return None
+    src = os.path.join(ROOT, e["source"])
+    if not os.path.exists(src):
+        return None
+    if hashlib.sha256(open(src, "rb").read()).hexdigest() != e["source_sha256"]:
+        return None
+    return e["dram_bytes_per_launch"]
+
+
+# ---------------------------------------------------------------- workload
+
+class Workload:
+    def __init__(self, device, rank, args):
+        import torch
+        from dense_packed_bit_gb300 import synth
+        self.dev = device
+        off = rank_seed_offset(rank)
+        self.gemm = []
+        for layout in ("nn", "nt", "tn"):
+            c = synth.square_2048(layout)
+            A, B = c.A, c.B
+            if off:
+                A = synth.normal_f32(off + 1 + len(self.gemm), A.shape, 0.02)
+                B = synth.normal_f32(off + 11 + len(self.gemm), B.shape, 0.02)
+            self.gemm.append(dict(case=c, A=torch.from_numpy(A).to(device), B=torch.from_numpy(B).to(device),
+                                  C=torch.empty((c.M, c.N), dtype=torch.float32, device=device),
+                                  hA=A, hB=B))
+        self.gemv_codes, self.gemv_scales = [], []
+        x = None
+        for i in range(N_GEMV):
+            c = synth.gemv_2bit_12288x1536(i + (off % 1000) * N_GEMV if off else i)
+            self.gemv_codes.append(torch.from_numpy(c.codes).to(device))
+            self.gemv_scales.append(torch.from_numpy(c.scales).to(device))
+            x = c.X
+            self.gemv_cb = c.codebook
+        self.gemv_x = torch.from_numpy(x.reshape(-1)).to(device)
+        self.gemv_y = torch.empty((N_GEMV, 12288), dtype=torch.float32, device=device)
+        self.tern = []
+        for layer in range(N_LAYERS):
+            for proj in ("up", "down"):
+                c = synth.ternary_encoder_layer(layer, proj)
+                self.tern.append(dict(case=c, codes=torch.from_numpy(c.codes).to(device),
+                                      scales=torch.from_numpy(c.scales).to(device),
+                                      X=torch.from_numpy(c.X).to(device),
+                                      Y=torch.empty((c.X.shape[0], c.rows), dtype=torch.float32, device=device)))
+        self.flush = torch.empty(512 * 1024 * 1024 // 4, dtype=torch.float32, device=device)
+        self.args = args
+
+    def launches_per_step(self):
+        return len(self.gemm) + N_GEMV + len(self.tern)
+
+
+def run_step(w: Workload, ev, stream):
+    """One pass of the hot path; ev: list of (start, end) event pairs per phase."""
+    import dense_packed_bit_gb300 as mm
+    a = w.args
+    w.flush.fill_(1.0)  # evict the GEMM operands from L2 (torch kernel, not timed)
+    for i, g in enumerate(w.gemm):
+        c = g["case"]
+        ev["gemm"][i][0].record(stream)
+        mm.mm_gemm_f32_ex(c.transA, c.transB, c.M, c.N, c.K, g["A"], g["A"].shape[1], g["B"], g["B"].shape[1],
+                          g["C"], c.N, stream, path=a.gemm_path)
+        ev["gemm"][i][1].record(stream)
+    ev["gemv"][0].record(stream)
+    for i in range(N_GEMV):
+        mm.mm_gemv_packed2_ex(w.gemv_codes[i], w.gemv_scales[i], w.gemv_x, w.gemv_y[i], 12288, 1536, w.gemv_cb,
+                              stream, split=a.gemv_split, rows_per_lane=a.gemv_rows, warps=a.gemv_warps,
+                              pdl=1, weights_static=1)
+    ev["gemv"][1].record(stream)
+    ev["tern"][0].record(stream)
+    for t in w.tern:
+        c = t["case"]
+        mm.mm_gemm_packed2(t["codes"], t["scales"], t["X"], t["Y"], c.X.shape[0], c.rows, c.cols, c.codebook,
+                           stream)
+    ev["tern"][1].record(stream)
+
+
+def new_events():
+    import torch
+    mk = lambda: (torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+    return {"gemm": [mk() for _ in range(3)], "gemv": mk(), "tern": mk()}
+
+
+def e2e_gemm(w: Workload, steps: int, stream):
+    """2048^3 GEMMs through the C ABI with host buffers: H2D of A and B from pinned
+    memory, the three GEMMs, D2H of C, all inside the timed region."""
+    import torch
+    import dense_packed_bit_gb300 as mm
+    host = []
+    for g in w.gemm:
+        hA = torch.from_numpy(g["hA"]).pin_memory()
+        hB = torch.from_numpy(g["hB"]).pin_memory()
+        hC = torch.empty(g["C"].shape, dtype=torch.float32).pin_memory()
+        host.append((hA, hB, hC))
+    h2d = sum(a.numel() * 4 + b.numel() * 4 for a, b, _ in host)
+    d2h = sum(c.numel() * 4 for _, _, c in host)
+
+    def once():
+        for g, (hA, hB, hC) in zip(w.gemm, host):
+            c = g["case"]
+            g["A"].copy_(hA, non_blocking=True)
+            g["B"].copy_(hB, non_blocking=True)
+            mm.mm_gemm_f32(c.transA, c.transB, c.M, c.N, c.K, g["A"], g["A"].shape[1], g["B"], g["B"].shape[1],
+                           g["C"], c.N, stream)
+            hC.copy_(g["C"], non_blocking=True)
+
+    with torch.cuda.stream(stream):
+        once()
+        torch.cuda.synchronize()
+        t0 = time.perf_counter()
+        for _ in range(steps):
+            once()
+        torch.cuda.synchronize()
+        dt = time.perf_counter() - t0
+    return {"value": 3 * GEMM_FLOP * steps / dt / 1e12, "unit": "TFLOP/s",
+            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
+
+
+# ---------------------------------------------------------------- CPU oracle baseline
+
+def cpu_oracle_sample(seconds_target: float = 15.0):
+    """Time the fp64 oracle on the 2048^3 NN/NT/TN products (all host cores)."""
+    import oracle
+    from dense_packed_bit_gb300 import synth
+    oracle.build()
+    threads = oracle.default_threads()
+    flop = 0.0
+    t0 = time.perf_counter()
+    n_done = 0
+    while True:
+        for layout in ("nn", "nt", "tn"):
+            c = synth.square_2048(layout)
+            oracle.gemm(c.transA, c.transB, c.M, c.N, c.K, c.A, c.B, threads=threads)
+            flop += GEMM_FLOP
+            n_done += 1
+        if time.perf_counter() - t0 > seconds_target or n_done >= 6:
+            break
+    dt = time.perf_counter() - t0
+    return {"value": flop / dt / 1e12, "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
+            "sample": f"{n_done} full 2048^3 products (NN, NT, TN in turn), fp64 accumulation, {dt:.1f} s"}
+
+
+# ---------------------------------------------------------------- main arms
+
+def main_reference(args):
+    rank, world, _ = dist_env()
+    if world > 1:
+        dist_init("gloo")
+        if rank != 0:
+            return 0
+    import oracle
+    from dense_packed_bit_gb300 import synth
+    oracle.build()
+    threads = oracle.default_threads()
+    # bounded sample per step: the first 128 rows of each 2048^3 product
+    rows = 128
+    cases = [synth.square_2048(l) for l in ("nn", "nt", "tn")]
+
+    def step():
+        fl = 0.0
+        for c in cases:
+            A = c.A[:, :rows].copy() if c.transA else c.A[:rows]
+            oracle.gemm(c.transA, c.transB, rows, c.N, c.K, A, c.B, threads=threads)
+            fl += 2.0 * rows * c.N * c.K
+        return fl
+
+    for _ in range(args.warmup):
+        step()
+    t0 = time.perf_counter()
+    fl = 0.0
+    for _ in range(args.steps):
+        fl += step()
+    dt = time.perf_counter() - t0
+    val = fl / dt / 1e12
+    sample = f"first {rows} rows of each 2048^3 product (NN, NT, TN) per step, fp64 oracle"
+    print(json.dumps({
+        "impl": "reference", "metric": METRIC, "value": val, "unit": "TFLOP/s", "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt / args.steps * 1e3,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": "square_2048_fp32_gemm_nn_nt_tn (row sample)", "rows_per_product": rows},
+        "cpu_baseline": {"value": val, "unit": "TFLOP/s", "cores": threads, "kind": "oracle", "sample": sample},
+        "e2e": {"value": val, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }), flush=True)
+    return 0
+
+
+def main_mm(args):
+    import torch
+    import dense_packed_bit_gb300 as mm
+    from dense_packed_bit_gb300 import build as mmbuild
+
+    rank, world, local = dist_env()
+    if rank == 0:
+        mmbuild.build()
+    dev = torch.device(f"cuda:{local}")
+    torch.cuda.set_device(dev)
+    rank, world = dist_init("nccl")
+    if world > 1:
+        barrier(dev)
+        mmbuild.build()  # other ranks pick up the library rank 0 built
+    mm.load_library()
+
+    w = Workload(dev, rank, args)
+    stream = torch.cuda.Stream(device=dev)
+    ev_steps = [new_events() for _ in range(args.steps)]
+    with torch.cuda.stream(stream):
+        for _ in range(max(3, args.warmup)):
+            run_step(w, new_events(), stream)
+        mm.mm_check_device_error(stream)
+        torch.cuda.synchronize()
+
+        clocks = ClockSampler(dev.index)
+        clocks.start()
+        barrier(dev)
+        torch.cuda.synchronize()
+        t0 = time.perf_counter()
+        for s in range(args.steps):
+            run_step(w, ev_steps[s], stream)
+        torch.cuda.synchronize()
+        barrier(dev)
+        wall = time.perf_counter() - t0
+        clk = clocks.stop()
+        mm.mm_check_device_error(stream)
+
+    gemm_ms = [[e[0].elapsed_time(e[1]) for e in ev["gemm"]] for ev in ev_steps]
+    gemv_ms = [ev["gemv"][0].elapsed_time(ev["gemv"][1]) for ev in ev_steps]
+    tern_ms = [ev["tern"][0].elapsed_time(ev["tern"][1]) for ev in ev_steps]
+    gemm_total_s = reduce_max(sum(sum(r) for r in gemm_ms) / 1e3, dev)
+    gemv_total_s = reduce_max(sum(gemv_ms) / 1e3, dev)
+    tern_total_s = reduce_max(sum(tern_ms) / 1e3, dev)
+    wall = reduce_max(wall, dev)
+
+    gemm_tflops = world * 3 * GEMM_FLOP * args.steps / gemm_total_s / 1e12
+    per_call_gemv_s = gemv_total_s / (args.steps * N_GEMV)
+    gemv_gbs = world * GEMV_WEIGHT_BYTES / per_call_gemv_s / 1e9
+    tern_tflops = world * N_LAYERS * TERN_FLOP_PER_LAYER * args.steps / tern_total_s / 1e12
+    step_ms = (gemm_total_s + gemv_total_s + tern_total_s) / args.steps * 1e3
+
+    peaks, peaks_src = measured_peaks()
+    props = torch.cuda.get_device_properties(dev)
+    sms = props.multi_processor_count
+    fp32_peak_max = fp32_simt_peak_tflops(sms, peaks.get("sm_max_mhz", 2070.0))
+    per_gemm_ms = {l: statistics.mean(r[i] for r in gemm_ms) for i, l in enumerate(("nn", "nt", "tn"))}
+    gemm_per_gpu = 3 * GEMM_FLOP * args.steps / gemm_total_s / 1e12
+    if args.gemm_path == mm.MM_GEMM_TF32X3:
+        tf32_peak = peaks["bf16_tflops"] * (1.1 / 2.25)
+        roof = {"bound": "tensor", "achieved": gemm_per_gpu, "peak": tf32_peak / 3.0, "unit": "TFLOP/s",
+                "frac": gemm_per_gpu / (tf32_peak / 3.0), "traffic": traffic_for("gemm_tf32x3"),
+                "kernel": "gemm_tf32x3", "peak_source": f"{peaks_src} bf16 x nominal tf32/bf16 ratio / 3 MMAs"}
+    else:
+        roof = {"bound": "alu", "achieved": gemm_per_gpu, "peak": fp32_peak_max, "unit": "TFLOP/s",
+                "frac": gemm_per_gpu / fp32_peak_max, "traffic": traffic_for("gemm_ffma"),
+                "kernel": "gemm_ffma_kernel",
+                "peak_source": f"{sms} SMs x 128 FP32 lanes x 2 flop x {peaks.get('sm_max_mhz', 2070.0):.0f} MHz"}
+        if clk.get("sm_mhz"):
+            roof["frac_at_sampled_clock"] = gemm_per_gpu / fp32_simt_peak_tflops(sms, clk["sm_mhz"])
+
+    out = {
+        "metric": METRIC, "value": gemm_tflops, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
+        "warmup": max(3, args.warmup), "ms_per_step": step_ms, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+        "config": {"workload": WORKLOAD, "gemm": "2048x2048x2048 fp32 NN+NT+TN, N(0,0.02)",
+                   "gemv": "12288x1536 2-bit, 64-matrix rotation (288 MiB > L2), codebook {-2,-1,0,1}",
+                   "ternary": "16 layers, M=222, up 768->3072 and down 3072->768",
+                   "l2": "512 MiB buffer written before the GEMM phase of every step; GEMV inputs exceed L2",
+                   "gemv_opts": {"split": args.gemv_split, "rows_per_lane": args.gemv_rows,
+                                 "warps": args.gemv_warps, "pdl": 1, "weights_static": 1},
+                   "gemm_path": args.gemm_path, "parallelism": f"replicas x{world}"},
+        "gemm_ms": per_gemm_ms,
+        "gemv": {"metric": "2-bit 12288x1536 GEMV weight GB/s", "value": gemv_gbs, "unit": "GB/s",
+                 "us_per_call": per_call_gemv_s * 1e6,
+                 "roofline": {"bound": "hbm", "achieved": GEMV_TOTAL_BYTES / per_call_gemv_s / 1e9,
+                              "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                              "frac": GEMV_TOTAL_BYTES / per_call_gemv_s / 1e9 / peaks["hbm_gbs"],
+                              "weight_frac": GEMV_WEIGHT_BYTES / per_call_gemv_s / 1e9 / peaks["hbm_gbs"],
+                              "traffic": traffic_for("gemv2_vec"), "peak_source": peaks_src}},
+        "ternary": {"value": tern_tflops, "unit": "TFLOP/s", "ms_per_block": tern_total_s / args.steps * 1e3},
+        "roofline": roof,
+        "clocks": clk,
+        "gpu_launches": w.launches_per_step() * args.steps,
+        "wall_s": wall,
+    }
+    if rank == 0:
+        out["e2e"] = e2e_gemm(w, max(2, args.steps // 2), stream)
+        if world == 1 and not args.no_cpu_baseline:
+            out["cpu_baseline"] = cpu_oracle_sample()
+        print(json.dumps(out), flush=True)
+    return 0
+
+
+def main(argv=None):
+    args = parse_args(argv)
+    if args.impl == "reference":
+        return main_reference(args)
+    return main_mm(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

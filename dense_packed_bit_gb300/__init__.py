@@ -1,0 +1,169 @@
+"""dense_packed_bit_gb300 -- fp32 dense GEMM and packed 2-bit GEMV / skinny GEMM on GB300.
+
+Thin ctypes binding over libmm.so (the C ABI declared in include/mm.h).  The
+functions keep the C names and argument order; tensors are torch CUDA tensors
+(only their device pointers are passed) and `stream` defaults to torch's
+current stream.  Every step of the computation runs in libmm's CUDA kernels:
+there is no CPU or PyTorch fallback, and a missing or unloadable libmm.so is
+an error.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+__all__ = [
+    "MMError", "load_library", "library_path", "mm_version", "mm_last_error",
+    "mm_gemm_f32", "mm_gemm_f32_ex", "mm_gemv_packed2", "mm_gemv_packed2_ex",
+    "mm_gemm_packed2", "mm_gemm_packed2_ex", "mm_check_device_error",
+    "MM_OK", "MM_ERR_INVALID_ARG", "MM_ERR_UNSUPPORTED", "MM_ERR_CUDA", "MM_ERR_TIMEOUT",
+    "MM_GEMM_AUTO", "MM_GEMM_FFMA", "MM_GEMM_TF32X3",
+    "MM_DEQ_AUTO", "MM_DEQ_SELECT", "MM_DEQ_AFFINE",
+]
+
+MM_OK, MM_ERR_INVALID_ARG, MM_ERR_UNSUPPORTED, MM_ERR_CUDA, MM_ERR_TIMEOUT = 0, 1, 2, 3, 4
+MM_GEMM_AUTO, MM_GEMM_FFMA, MM_GEMM_TF32X3 = 0, 1, 2
+MM_DEQ_AUTO, MM_DEQ_SELECT, MM_DEQ_AFFINE = 0, 1, 2
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+_lock = threading.Lock()
+_lib = None
+
+# symbol -> (argtypes, restype); mirrors include/mm.h
+_P, _I64, _I = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int
+
+
+class GemmOpts(ctypes.Structure):
+    _fields_ = [("path", ctypes.c_int), ("tile", ctypes.c_int), ("reserved", ctypes.c_int * 6)]
+
+
+class GemvOpts(ctypes.Structure):
+    _fields_ = [("split", ctypes.c_int), ("rows_per_lane", ctypes.c_int), ("warps", ctypes.c_int),
+                ("dequant", ctypes.c_int), ("pdl", ctypes.c_int), ("weights_static", ctypes.c_int),
+                ("reserved", ctypes.c_int * 6)]
+
+
+class GemmPacked2Opts(ctypes.Structure):
+    _fields_ = [("tile", ctypes.c_int), ("reserved", ctypes.c_int * 7)]
+
+
+SIGNATURES = {
+    "mm_version": ([], ctypes.c_int),
+    "mm_last_error": ([], ctypes.c_char_p),
+    "mm_gemm_f32": ([_I, _I, _I64, _I64, _I64, _P, _I64, _P, _I64, _P, _I64, _P], ctypes.c_int),
+    "mm_gemm_f32_ex": ([_I, _I, _I64, _I64, _I64, _P, _I64, _P, _I64, _P, _I64, _P,
+                        ctypes.POINTER(GemmOpts)], ctypes.c_int),
+    "mm_gemv_packed2": ([_P, _P, _P, _P, _I64, _I64, _P, _P], ctypes.c_int),
+    "mm_gemv_packed2_ex": ([_P, _P, _P, _P, _I64, _I64, _P, _P, ctypes.POINTER(GemvOpts)], ctypes.c_int),
+    "mm_gemm_packed2": ([_P, _P, _P, _P, _I64, _I64, _I64, _P, _P], ctypes.c_int),
+    "mm_gemm_packed2_ex": ([_P, _P, _P, _P, _I64, _I64, _I64, _P, _P, ctypes.POINTER(GemmPacked2Opts)],
+                           ctypes.c_int),
+    "mm_check_device_error": ([_P], ctypes.c_int),
+}
+
+
+class MMError(RuntimeError):
+    def __init__(self, status: int, message: str):
+        super().__init__(f"libmm status {status}: {message}")
+        self.status = status
+
+
+def library_path() -> str:
+    return os.environ.get("MM_LIBRARY", os.path.join(_PKG, "libmm.so"))
+
+
+def load_library():
+    """Load libmm.so (built by dense_packed_bit_gb300.build); raise if it is missing."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            path = library_path()
+            if not os.path.exists(path):
+                raise MMError(MM_ERR_UNSUPPORTED,
+                              f"{path} not found: build it with `python -m dense_packed_bit_gb300.build`")
+            lib = ctypes.CDLL(path)
+            for name, (argt, rest) in SIGNATURES.items():
+                fn = getattr(lib, name)
+                fn.argtypes = argt
+                fn.restype = rest
+            _lib = lib
+    return _lib
+
+
+def _ptr(t) -> int | None:
+    if t is None:
+        return None
+    if isinstance(t, int):
+        return t
+    return t.data_ptr()
+
+
+def _stream(stream):
+    if stream is None:
+        import torch
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, int):
+        return stream
+    return stream.cuda_stream
+
+
+def _codebook(cb):
+    if cb is None:
+        return None
+    vals = [float(v) for v in (cb.tolist() if hasattr(cb, "tolist") else cb)]
+    if len(vals) != 4:
+        raise ValueError("codebook needs 4 entries")
+    return (ctypes.c_float * 4)(*vals)
+
+
+def _check(status: int):
+    if status != MM_OK:
+        msg = load_library().mm_last_error()
+        raise MMError(status, msg.decode() if msg else "")
+
+
+def mm_version() -> int:
+    return load_library().mm_version()
+
+
+def mm_last_error() -> str:
+    return load_library().mm_last_error().decode()
+
+
+def mm_gemm_f32(transA, transB, M, N, K, A, lda, B, ldb, C, ldc, stream=None):
+    _check(load_library().mm_gemm_f32(int(transA), int(transB), M, N, K, _ptr(A), lda, _ptr(B), ldb,
+                                      _ptr(C), ldc, _stream(stream)))
+
+
+def mm_gemm_f32_ex(transA, transB, M, N, K, A, lda, B, ldb, C, ldc, stream=None, *, path=0, tile=0):
+    o = GemmOpts(path, tile)
+    _check(load_library().mm_gemm_f32_ex(int(transA), int(transB), M, N, K, _ptr(A), lda, _ptr(B), ldb,
+                                         _ptr(C), ldc, _stream(stream), ctypes.byref(o)))
+
+
+def mm_gemv_packed2(codes, scales, x, y, rows, cols, codebook, stream=None):
+    _check(load_library().mm_gemv_packed2(_ptr(codes), _ptr(scales), _ptr(x), _ptr(y), rows, cols,
+                                          _codebook(codebook), _stream(stream)))
+
+
+def mm_gemv_packed2_ex(codes, scales, x, y, rows, cols, codebook, stream=None, *, split=0,
+                       rows_per_lane=0, warps=0, dequant=0, pdl=0, weights_static=0):
+    o = GemvOpts(split, rows_per_lane, warps, dequant, pdl, weights_static)
+    _check(load_library().mm_gemv_packed2_ex(_ptr(codes), _ptr(scales), _ptr(x), _ptr(y), rows, cols,
+                                             _codebook(codebook), _stream(stream), ctypes.byref(o)))
+
+
+def mm_gemm_packed2(codes, scales, X, Y, M, rows, cols, codebook, stream=None):
+    _check(load_library().mm_gemm_packed2(_ptr(codes), _ptr(scales), _ptr(X), _ptr(Y), M, rows, cols,
+                                          _codebook(codebook), _stream(stream)))
+
+
+def mm_gemm_packed2_ex(codes, scales, X, Y, M, rows, cols, codebook, stream=None, *, tile=0):
+    o = GemmPacked2Opts(tile)
+    _check(load_library().mm_gemm_packed2_ex(_ptr(codes), _ptr(scales), _ptr(X), _ptr(Y), M, rows, cols,
+                                             _codebook(codebook), _stream(stream), ctypes.byref(o)))
+
+
+def mm_check_device_error(stream=None):
+    _check(load_library().mm_check_device_error(_stream(stream)))

@@ -1,0 +1,210 @@
+// mm_api.cu -- the extern "C" boundary of libmm (declared in include/mm.h).
+//
+// Argument checks, variant selection and launches on the caller's stream.
+// Every check happens before the first CUDA call, so argument errors are
+// reported the same way on machines without a GPU.
+#include "mm.h"
+#include "mm_internal.h"
+
+#include <cuda_runtime.h>
+
+#include <cmath>
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <mutex>
+#include <string>
+
+namespace {
+
+thread_local std::string t_err;
+
+mm_status fail(mm_status s, const char *fmt, ...) {
+    char buf[512];
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(buf, sizeof(buf), fmt, ap);
+    va_end(ap);
+    t_err = buf;
+    return s;
+}
+
+mm_status ok() {
+    t_err.clear();
+    return MM_OK;
+}
+
+mm_status cuda_fail(cudaError_t e, const char *what) {
+    return fail(MM_ERR_CUDA, "%s: %s (%s)", what, cudaGetErrorName(e), cudaGetErrorString(e));
+}
+
+// bytes spanned by a row-major rows x cols matrix with leading dimension ld
+uint64_t span(int64_t rows, int64_t cols, int64_t ld, int64_t elem) {
+    return (uint64_t)(((rows - 1) * ld + cols) * elem);
+}
+
+bool overlap(const void *a, uint64_t na, const void *b, uint64_t nb) {
+    const uintptr_t x = reinterpret_cast<uintptr_t>(a), y = reinterpret_cast<uintptr_t>(b);
+    return x < y + nb && y < x + na;
+}
+
+// The library holds sm_103a code only; anything else is refused up front.
+mm_status check_device() {
+    static std::mutex mu;
+    static int known[64] = {0};  // 0 unknown, 1 ok, 2 unsupported
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+    if (dev < 0 || dev >= 64) return fail(MM_ERR_UNSUPPORTED, "device ordinal %d out of range", dev);
+    std::lock_guard<std::mutex> lk(mu);
+    if (known[dev] == 0) {
+        int major = 0, minor = 0;
+        e = cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev);
+        if (e == cudaSuccess) e = cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev);
+        if (e != cudaSuccess) return cuda_fail(e, "cudaDeviceGetAttribute");
+        known[dev] = (major == 10 && minor == 3) ? 1 : 2;
+        if (known[dev] == 2) return fail(MM_ERR_UNSUPPORTED, "libmm is built for sm_103a; device %d is sm_%d%d", dev, major, minor);
+    }
+    if (known[dev] == 2) return fail(MM_ERR_UNSUPPORTED, "libmm is built for sm_103a only");
+    return MM_OK;
+}
+
+mm_status check_codebook(const float *cb) {
+    if (!cb) return fail(MM_ERR_INVALID_ARG, "codebook is NULL");
+    for (int i = 0; i < 4; ++i)
+        if (!std::isfinite(cb[i])) return fail(MM_ERR_INVALID_ARG, "codebook[%d] is not finite", i);
+    return MM_OK;
+}
+
+mm_status check_packed(const uint8_t *codes, const uint16_t *scales, const uint16_t *x, const float *y,
+                       int64_t M, int64_t rows, int64_t cols, const float *cb) {
+    if (!codes || !scales || !x || !y) return fail(MM_ERR_INVALID_ARG, "NULL pointer argument");
+    if (M < 1 || rows < 1 || cols < 1)
+        return fail(MM_ERR_INVALID_ARG, "sizes must be >= 1 (M=%lld rows=%lld cols=%lld)", (long long)M,
+                    (long long)rows, (long long)cols);
+    if (rows > ((int64_t)1 << 40) || cols > ((int64_t)1 << 40) || M > ((int64_t)1 << 31))
+        return fail(MM_ERR_INVALID_ARG, "sizes too large");
+    mm_status s = check_codebook(cb);
+    if (s != MM_OK) return s;
+    const uint64_t ybytes = (uint64_t)(M * rows * 4);
+    if (overlap(y, ybytes, codes, (uint64_t)(rows * ((cols + 3) / 4))) || overlap(y, ybytes, scales, (uint64_t)rows * 2) ||
+        overlap(y, ybytes, x, (uint64_t)(M * cols * 2)))
+        return fail(MM_ERR_INVALID_ARG, "output overlaps an input");
+    return MM_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int mm_version(void) { return 100; }
+
+const char *mm_last_error(void) { return t_err.c_str(); }
+
+mm_status mm_gemm_f32_ex(int transA, int transB, int64_t M, int64_t N, int64_t K, const float *A, int64_t lda,
+                         const float *B, int64_t ldb, float *C, int64_t ldc, mm_stream_t stream,
+                         const mm_gemm_opts *opts) {
+    if ((transA != 0 && transA != 1) || (transB != 0 && transB != 1))
+        return fail(MM_ERR_INVALID_ARG, "transA/transB must be 0 or 1");
+    if (M < 1 || N < 1 || K < 1)
+        return fail(MM_ERR_INVALID_ARG, "M, N, K must be >= 1 (got %lld, %lld, %lld)", (long long)M, (long long)N,
+                    (long long)K);
+    if (!A || !B || !C) return fail(MM_ERR_INVALID_ARG, "NULL matrix pointer");
+    const int64_t a_rows = transA ? K : M, a_cols = transA ? M : K;
+    const int64_t b_rows = transB ? N : K, b_cols = transB ? K : N;
+    if (lda < a_cols) return fail(MM_ERR_INVALID_ARG, "lda=%lld < %lld", (long long)lda, (long long)a_cols);
+    if (ldb < b_cols) return fail(MM_ERR_INVALID_ARG, "ldb=%lld < %lld", (long long)ldb, (long long)b_cols);
+    if (ldc < N) return fail(MM_ERR_INVALID_ARG, "ldc=%lld < N=%lld", (long long)ldc, (long long)N);
+    const uint64_t cb = span(M, N, ldc, 4);
+    if (overlap(C, cb, A, span(a_rows, a_cols, lda, 4)) || overlap(C, cb, B, span(b_rows, b_cols, ldb, 4)))
+        return fail(MM_ERR_INVALID_ARG, "C overlaps A or B");
+    int path = MM_GEMM_AUTO;
+    if (opts) {
+        path = opts->path;
+        if (path < MM_GEMM_AUTO || path > MM_GEMM_TF32X3) return fail(MM_ERR_INVALID_ARG, "unknown path %d", path);
+    }
+    mm_status s = check_device();
+    if (s != MM_OK) return s;
+
+    mm::GemmArgs g{transA, transB, M, N, K, A, lda, B, ldb, C, ldc};
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    cudaError_t e;
+    if (path == MM_GEMM_TF32X3) return fail(MM_ERR_UNSUPPORTED, "3xTF32 path not available in this build");
+    if (mm::gemm_ffma_supported(g)) e = mm::launch_gemm_ffma(g, opts ? opts->tile : 0, st);
+    else if (path == MM_GEMM_FFMA || path == MM_GEMM_AUTO) e = mm::launch_gemm_simple(g, st);
+    else e = cudaErrorNotSupported;
+    if (e != cudaSuccess) return cuda_fail(e, "gemm launch");
+    return ok();
+}
+
+mm_status mm_gemm_f32(int transA, int transB, int64_t M, int64_t N, int64_t K, const float *A, int64_t lda,
+                      const float *B, int64_t ldb, float *C, int64_t ldc, mm_stream_t stream) {
+    return mm_gemm_f32_ex(transA, transB, M, N, K, A, lda, B, ldb, C, ldc, stream, nullptr);
+}
+
+mm_status mm_gemv_packed2_ex(const uint8_t *codes, const uint16_t *scales, const uint16_t *x, float *y, int64_t rows,
+                             int64_t cols, const float codebook[4], mm_stream_t stream, const mm_gemv_opts *opts) {
+    mm_status s = check_packed(codes, scales, x, y, 1, rows, cols, codebook);
+    if (s != MM_OK) return s;
+    mm::GemvConfig cfg{8, 4, 4, 0, 1, 0};
+    if (opts) {
+        if (opts->split) cfg.split = opts->split;
+        if (opts->rows_per_lane) cfg.rows_per_lane = opts->rows_per_lane;
+        if (opts->warps) cfg.warps = opts->warps;
+        cfg.dequant = opts->dequant;
+        cfg.pdl = opts->pdl;
+        cfg.weights_static = opts->weights_static;
+    }
+    if (cfg.split != 4 && cfg.split != 8 && cfg.split != 16) return fail(MM_ERR_INVALID_ARG, "split must be 4, 8 or 16");
+    if (cfg.rows_per_lane != 1 && cfg.rows_per_lane != 2 && cfg.rows_per_lane != 4)
+        return fail(MM_ERR_INVALID_ARG, "rows_per_lane must be 1, 2 or 4");
+    if (cfg.warps < 1 || cfg.warps > 16) return fail(MM_ERR_INVALID_ARG, "warps must be 1..16");
+    if (cfg.pdl != 0 && cfg.pdl != 1) return fail(MM_ERR_INVALID_ARG, "pdl must be 0 or 1");
+    if (cfg.weights_static != 0 && cfg.weights_static != 1) return fail(MM_ERR_INVALID_ARG, "weights_static must be 0 or 1");
+    const bool affine = mm::codebook_is_affine(codebook);
+    if (cfg.dequant == MM_DEQ_AUTO) cfg.dequant = affine ? MM_DEQ_AFFINE : MM_DEQ_SELECT;
+    if (cfg.dequant != MM_DEQ_SELECT && cfg.dequant != MM_DEQ_AFFINE)
+        return fail(MM_ERR_INVALID_ARG, "unknown dequant %d", cfg.dequant);
+    if (cfg.dequant == MM_DEQ_AFFINE && !affine)
+        return fail(MM_ERR_INVALID_ARG, "affine decode needs codebook[c] == codebook[0] + c*(codebook[1]-codebook[0])");
+    s = check_device();
+    if (s != MM_OK) return s;
+    mm::PackedArgs a{codes, scales, x, y, 1, rows, cols, {codebook[0], codebook[1], codebook[2], codebook[3]}};
+    cudaError_t e = mm::launch_gemv_packed2(a, cfg, reinterpret_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "gemv launch");
+    return ok();
+}
+
+mm_status mm_gemv_packed2(const uint8_t *codes, const uint16_t *scales, const uint16_t *x, float *y, int64_t rows,
+                          int64_t cols, const float codebook[4], mm_stream_t stream) {
+    return mm_gemv_packed2_ex(codes, scales, x, y, rows, cols, codebook, stream, nullptr);
+}
+
+mm_status mm_gemm_packed2_ex(const uint8_t *codes, const uint16_t *scales, const uint16_t *X, float *Y, int64_t M,
+                             int64_t rows, int64_t cols, const float codebook[4], mm_stream_t stream,
+                             const mm_gemm_packed2_opts *opts) {
+    mm_status s = check_packed(codes, scales, X, Y, M, rows, cols, codebook);
+    if (s != MM_OK) return s;
+    if (opts && opts->tile < 0) return fail(MM_ERR_INVALID_ARG, "unknown tile %d", opts->tile);
+    s = check_device();
+    if (s != MM_OK) return s;
+    mm::PackedArgs a{codes, scales, X, Y, M, rows, cols, {codebook[0], codebook[1], codebook[2], codebook[3]}};
+    cudaError_t e = mm::launch_gemm_packed2(a, opts ? opts->tile : 0, reinterpret_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "packed gemm launch");
+    return ok();
+}
+
+mm_status mm_gemm_packed2(const uint8_t *codes, const uint16_t *scales, const uint16_t *X, float *Y, int64_t M,
+                          int64_t rows, int64_t cols, const float codebook[4], mm_stream_t stream) {
+    return mm_gemm_packed2_ex(codes, scales, X, Y, M, rows, cols, codebook, stream, nullptr);
+}
+
+mm_status mm_check_device_error(mm_stream_t stream) {
+    cudaError_t e;
+    const unsigned int v = mm::gemm_ffma_take_device_error(reinterpret_cast<cudaStream_t>(stream), &e);
+    if (e != cudaSuccess) return cuda_fail(e, "mm_check_device_error");
+    if (v != 0) return fail(MM_ERR_TIMEOUT, "a bounded device wait ran out in the FFMA GEMM (code %u)", v);
+    return ok();
+}
+
+}  // extern "C"

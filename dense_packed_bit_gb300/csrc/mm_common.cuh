@@ -1,0 +1,130 @@
+// mm_common.cuh -- device helpers shared by the libmm kernels (sm_103a).
+//
+// Inline PTX for mbarriers, TMA tile loads, programmatic dependent launch and
+// streaming global loads.  Every wait here is bounded by wall-clock time read
+// from %globaltimer; a wait that runs out records an error code in the calling
+// translation unit's device error word and reports failure to its caller,
+// which then returns without trapping.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace mm {
+
+// Upper bound of any single device-side wait (nanoseconds).
+constexpr unsigned long long kWaitLimitNs = 2000000000ull;  // 2 s
+
+// Error codes written to a translation unit's device error word.
+enum : unsigned int {
+    kDevErrNone = 0,
+    kDevErrWaitFull = 1,    // consumer wait for a filled pipeline stage ran out
+    kDevErrWaitEmpty = 2,   // producer wait for a drained stage ran out
+    kDevErrWaitMma = 3,     // wait for tensor-core completion ran out
+    kDevErrDrain = 4        // wait for in-flight copies after an error ran out
+};
+
+__device__ __forceinline__ uint32_t smem_u32(const void *p) {
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ unsigned long long global_ns() {
+    unsigned long long t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+
+// ---------------------------------------------------------------- mbarrier
+
+__device__ __forceinline__ void mbar_init(uint64_t *bar, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ void fence_mbar_init() {
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t *bar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)), "r"(bytes)
+                 : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint64_t *bar) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
+// Wait until the barrier phase with the given parity completes, for at most
+// kWaitLimitNs.  Returns false when the limit ran out.
+__device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const unsigned long long t0 = global_ns();
+    while (true) {
+        for (int i = 0; i < 64; ++i)
+            if (mbar_try_wait(bar, parity)) return true;
+        if (global_ns() - t0 > kWaitLimitNs) return false;
+    }
+}
+
+// ---------------------------------------------------------------- TMA
+
+// 2-D tiled bulk tensor load into this CTA's shared memory, completion
+// reported as transaction bytes on `bar`.  c0 is the innermost coordinate.
+__device__ __forceinline__ void tma_load_2d(void *smem_dst, const void *tmap, uint64_t *bar, int c0, int c1) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cta.global.tile.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%3, %4}], [%2];" ::"r"(smem_u32(smem_dst)),
+        "l"(tmap), "r"(smem_u32(bar)), "r"(c0), "r"(c1)
+        : "memory");
+}
+
+__device__ __forceinline__ void tma_prefetch_desc(const void *tmap) {
+    asm volatile("prefetch.tensormap [%0];" ::"l"(tmap) : "memory");
+}
+
+// ---------------------------------------------------------------- PDL
+
+// Block until every grid this one depends on has completed and its writes
+// are visible.  A no-op when the grid was not launched as a dependent.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
+// Allow the next dependent grid in the stream to begin launching.
+__device__ __forceinline__ void pdl_launch_dependents() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+// ---------------------------------------------------------------- loads
+
+// 16-byte read-only load that bypasses L1 allocation (streamed weights).
+__device__ __forceinline__ uint4 ld_stream_v4(const void *p) {
+    uint4 v;
+    asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                 : "l"(p));
+    return v;
+}
+
+// ---------------------------------------------------------------- packed fp32 pairs
+
+// d = a * b + c on two fp32 lanes at once (sm_100+ packed f32x2 FMA), round to nearest.
+__device__ __forceinline__ float2 ffma2(float2 a, float2 b, float2 c) {
+    unsigned long long A, B, C, D;
+    A = *reinterpret_cast<unsigned long long *>(&a);
+    B = *reinterpret_cast<unsigned long long *>(&b);
+    C = *reinterpret_cast<unsigned long long *>(&c);
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(D) : "l"(A), "l"(B), "l"(C));
+    return *reinterpret_cast<float2 *>(&D);
+}
+
+}  // namespace mm

@@ -1,0 +1,69 @@
+// mm_internal.h -- host-side interfaces between the C-ABI layer (mm_api.cu)
+// and the kernel translation units.  Not installed; not part of the ABI.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace mm {
+
+// ------------------------------------------------------------------ GEMV / packed GEMM
+
+struct PackedArgs {
+    const uint8_t *codes;
+    const uint16_t *scales;
+    const uint16_t *x;  // GEMV: cols entries; GEMM: M x cols
+    float *y;           // GEMV: rows entries; GEMM: M x rows
+    int64_t M, rows, cols;
+    float cb[4];
+};
+
+struct GemvConfig {
+    int split;          // lanes per row: 4, 8, 16
+    int rows_per_lane;  // 1, 2, 4
+    int warps;          // warps per CTA
+    int dequant;        // 1 select, 2 affine
+    int pdl;
+    int weights_static;
+};
+
+// True when cb[c] == cb[0] + c * (cb[1] - cb[0]) holds exactly in fp32 for c = 0..3.
+bool codebook_is_affine(const float cb[4]);
+
+// Vectorised path needs cols % 64 == 0, a 16-byte aligned codes pointer and
+// cols small enough for x to sit in shared memory.
+bool gemv_vec_supported(const PackedArgs &a);
+
+// Launches the GEMV.  Falls back to the bytewise kernel when the vectorised
+// path does not apply.  Returns the launch error.
+cudaError_t launch_gemv_packed2(const PackedArgs &a, const GemvConfig &cfg, cudaStream_t s);
+
+// Skinny packed GEMM (M >= 1).
+cudaError_t launch_gemm_packed2(const PackedArgs &a, int tile, cudaStream_t s);
+
+// ------------------------------------------------------------------ dense GEMM
+
+struct GemmArgs {
+    int transA, transB;
+    int64_t M, N, K;
+    const float *A;
+    int64_t lda;
+    const float *B;
+    int64_t ldb;
+    float *C;
+    int64_t ldc;
+};
+
+// Plain shared-memory tiled FFMA kernel: any sizes, strides and alignment.
+cudaError_t launch_gemm_simple(const GemmArgs &g, cudaStream_t s);
+
+// TMA-staged register-blocked FFMA kernel.  Needs 16-byte aligned A, B and
+// leading dimensions that are multiples of 4.  Returns cudaErrorNotSupported
+// when the arguments do not fit.
+bool gemm_ffma_supported(const GemmArgs &g);
+cudaError_t launch_gemm_ffma(const GemmArgs &g, int tile, cudaStream_t s);
+
+// Per translation unit device error words (read and cleared).
+unsigned int gemm_ffma_take_device_error(cudaStream_t s, cudaError_t *err);
+
+}  // namespace mm

@@ -1,0 +1,76 @@
+"""Run one hot-path kernel a few times on one workload, for profiler captures.
+
+    python -m dense_packed_bit_gb300.profile_case gemm --layout nn --size 2048 --reps 3
+    python -m dense_packed_bit_gb300.profile_case gemv --reps 3 [--split 8 --rows 4 --warps 4]
+    python -m dense_packed_bit_gb300.profile_case ternary --reps 1
+
+One warm-up launch precedes the `reps` launches.  No timing is done here:
+numbers come from the profiler or from bench.py.
+"""
+from __future__ import annotations
+
+import argparse
+import sys
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser()
+    ap.add_argument("op", choices=["gemm", "gemv", "ternary"])
+    ap.add_argument("--layout", default="nn", choices=["nn", "nt", "tn"])
+    ap.add_argument("--size", type=int, default=2048)
+    ap.add_argument("--path", type=int, default=0)
+    ap.add_argument("--reps", type=int, default=3)
+    ap.add_argument("--matrices", type=int, default=64)
+    ap.add_argument("--split", type=int, default=8)
+    ap.add_argument("--rows", type=int, default=4)
+    ap.add_argument("--warps", type=int, default=4)
+    ap.add_argument("--pdl", type=int, default=1)
+    a = ap.parse_args(argv)
+
+    import torch
+
+    import dense_packed_bit_gb300 as mm
+    from dense_packed_bit_gb300 import build, synth
+
+    build.build()
+    mm.load_library()
+    dev = torch.device("cuda:0")
+    if a.op == "gemm":
+        n = a.size
+        tA, tB = {"nn": (0, 0), "nt": (0, 1), "tn": (1, 0)}[a.layout]
+        A = torch.from_numpy(synth.normal_f32(1, (n, n), 0.02)).to(dev)
+        B = torch.from_numpy(synth.normal_f32(2, (n, n), 0.02)).to(dev)
+        C = torch.empty((n, n), dtype=torch.float32, device=dev)
+        for _ in range(1 + a.reps):
+            mm.mm_gemm_f32_ex(tA, tB, n, n, n, A, n, B, n, C, n, path=a.path)
+    elif a.op == "gemv":
+        codes, scales = [], []
+        for i in range(a.matrices):
+            c = synth.gemv_2bit_12288x1536(i)
+            codes.append(torch.from_numpy(c.codes).to(dev))
+            scales.append(torch.from_numpy(c.scales).to(dev))
+        x = torch.from_numpy(c.X.reshape(-1)).to(dev)
+        y = torch.empty((a.matrices, 12288), dtype=torch.float32, device=dev)
+        for r in range(1 + a.reps):
+            i = r % a.matrices
+            mm.mm_gemv_packed2_ex(codes[i], scales[i], x, y[i], 12288, 1536, c.codebook, split=a.split,
+                                  rows_per_lane=a.rows, warps=a.warps, pdl=a.pdl, weights_static=a.pdl)
+    else:
+        layers = []
+        for layer in range(16):
+            for proj in ("up", "down"):
+                c = synth.ternary_encoder_layer(layer, proj)
+                layers.append((c, torch.from_numpy(c.codes).to(dev), torch.from_numpy(c.scales).to(dev),
+                               torch.from_numpy(c.X).to(dev),
+                               torch.empty((c.X.shape[0], c.rows), dtype=torch.float32, device=dev)))
+        for _ in range(1 + a.reps):
+            for c, dc, ds, dX, dY in layers:
+                mm.mm_gemm_packed2(dc, ds, dX, dY, c.X.shape[0], c.rows, c.cols, c.codebook)
+    mm.mm_check_device_error()
+    torch.cuda.synchronize()
+    print("ok")
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,173 @@
+/*
+ * mm.h -- C ABI of libmm: fp32 dense GEMM and packed 2-bit GEMV / skinny GEMM
+ * on one NVIDIA GB300 (sm_103a).
+ *
+ * The two operations:
+ *
+ *  1. Dense fp32 matrix multiply  C = op(A) . op(B), C overwritten.
+ *     "I built a GPT-2 in the browser, then made it 2.6x-12.1x faster",
+ *     section "The kernel sweep": the matmul that is about 80% of a GPT-2
+ *     training step; one output cell per (row, column) walks the inner
+ *     dimension summing products.  The forward pass uses C = A.B (NN); the
+ *     backward products are dA = dC.B^T (NT) and dB = A^T.dC (TN).
+ *     "More Stumbling, This Time in the Browser", section "Four answers per
+ *     worker": rows are tokens, columns output features; edge masks cover
+ *     partial tiles; each output accumulates along the inner dimension in one
+ *     fixed order, so repeated calls give bit-identical results.
+ *
+ *  2. Packed 2-bit weights times activations:
+ *        Y[m][r] = scale_r * sum_k codebook[field(r, k)] * X[m][k]
+ *     "Kernel 0112", section "What is being measured": a 12,288 x 1,536
+ *     matrix of weights stored in 2 bits each, times a vector of 1,536
+ *     inputs; the work is dominated by reading the 4.5 MiB of weights.
+ *     The GEMV is the M = 1 case; the skinny GEMM serves a short batch of
+ *     rows ("More Stumbling...", the 16-layer ternary encoder on a 111-token
+ *     input with 2 questions).
+ *
+ * Layouts (all row-major, all pointers DEVICE memory owned by the caller):
+ *  - A: M x K (lda >= K), or K x M when transA (lda >= M).
+ *  - B: K x N (ldb >= N), or N x K when transB (ldb >= K).
+ *  - C: M x N (ldc >= N).  Leading dimensions count elements.
+ *  - codes: rows x ceil(cols/4) bytes.  Element k of a row is the 2-bit field
+ *    in byte floor(k/4), bits 2*(k mod 4) and 2*(k mod 4)+1 (little-endian
+ *    along K).  Fields of the last byte past `cols` are ignored.
+ *  - scales: rows fp16 values, passed as their uint16 bit patterns.
+ *  - x / X: fp16 bit patterns, x has cols entries, X is M x cols.
+ *  - y / Y: fp32, y has rows entries, Y is M x rows.
+ *  - codebook: 4 fp32 values in HOST memory, read during the call.
+ *
+ * Arithmetic: fp32 accumulation everywhere.  Every output satisfies
+ * |y - y_exact| <= 1e-5 * sum_k |term_k|; decoding of 2-bit fields is exact.
+ *
+ * Calls are asynchronous on `stream` (NULL = the legacy default stream); the
+ * return code covers argument checks and launch errors only.  The library
+ * keeps no pointer past a call and allocates no device memory in these calls.
+ * Operands must not overlap the output.  Not thread-safe for concurrent calls
+ * from several host threads (the last-error message is per thread; the
+ * kernel-attribute and tensor-map caches are guarded by a mutex).
+ *
+ * Device-side waits are bounded: a wait that runs out sets a device error word
+ * and the kernel returns early; mm_check_device_error() reports it as
+ * MM_ERR_TIMEOUT.  No kernel traps.
+ */
+#ifndef MM_H_
+#define MM_H_
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same type as cudaStream_t / CUstream. */
+typedef struct CUstream_st *mm_stream_t;
+
+typedef enum {
+    MM_OK = 0,
+    MM_ERR_INVALID_ARG = 1,  /* null pointer, bad size / leading dim, overlap, bad option */
+    MM_ERR_UNSUPPORTED = 2,  /* valid request this build cannot run (e.g. no sm_103 device) */
+    MM_ERR_CUDA = 3,         /* a CUDA runtime call or kernel launch failed */
+    MM_ERR_TIMEOUT = 4       /* a kernel's bounded device wait ran out (see mm_check_device_error) */
+} mm_status;
+
+/* Version of this ABI: major*10000 + minor*100 + patch. */
+int mm_version(void);
+
+/* Message for the last non-MM_OK status returned on this host thread. */
+const char *mm_last_error(void);
+
+/*
+ * Dense fp32 GEMM, C = op(A) . op(B).  M, N, K >= 1.
+ * Errors: MM_ERR_INVALID_ARG for a null pointer, a dimension < 1, a leading
+ * dimension below the stored width, or C overlapping A or B.
+ */
+mm_status mm_gemm_f32(int transA, int transB, int64_t M, int64_t N, int64_t K,
+                      const float *A, int64_t lda, const float *B, int64_t ldb,
+                      float *C, int64_t ldc, mm_stream_t stream);
+
+/*
+ * y = W . x for a packed 2-bit W (rows x cols) with per-row fp16 scale.
+ * rows, cols >= 1.  Errors: MM_ERR_INVALID_ARG for null pointers, sizes < 1,
+ * a null codebook, non-finite codebook entries, or y overlapping an input.
+ */
+mm_status mm_gemv_packed2(const uint8_t *codes, const uint16_t *scales, const uint16_t *x,
+                          float *y, int64_t rows, int64_t cols, const float codebook[4],
+                          mm_stream_t stream);
+
+/*
+ * Y = X . W^T for a packed 2-bit W (rows x cols), X (M x cols) fp16, Y (M x rows) fp32.
+ * M, rows, cols >= 1.  Errors as mm_gemv_packed2.
+ */
+mm_status mm_gemm_packed2(const uint8_t *codes, const uint16_t *scales, const uint16_t *X,
+                          float *Y, int64_t M, int64_t rows, int64_t cols,
+                          const float codebook[4], mm_stream_t stream);
+
+/*
+ * Waits for `stream`, then reads and clears the device error word set by a
+ * kernel whose bounded wait ran out.  Returns MM_OK, MM_ERR_TIMEOUT or
+ * MM_ERR_CUDA.
+ */
+mm_status mm_check_device_error(mm_stream_t stream);
+
+/* ------------------------------------------------------------------------
+ * Variant selection for sweeps and tests.  A zeroed struct means "automatic".
+ * Every variant computes the same operation to the same bound.
+ * ------------------------------------------------------------------------ */
+
+enum {
+    MM_GEMM_AUTO = 0,
+    MM_GEMM_FFMA = 1,    /* TMA-staged, register-blocked fp32 FFMA */
+    MM_GEMM_TF32X3 = 2   /* 3xTF32 split on tcgen05 tensor cores, TMEM accumulators */
+};
+
+typedef struct {
+    int path;      /* MM_GEMM_* */
+    int tile;      /* 0 = automatic, else a path-specific tile id */
+    int reserved[6];
+} mm_gemm_opts;
+
+mm_status mm_gemm_f32_ex(int transA, int transB, int64_t M, int64_t N, int64_t K,
+                         const float *A, int64_t lda, const float *B, int64_t ldb,
+                         float *C, int64_t ldc, mm_stream_t stream, const mm_gemm_opts *opts);
+
+enum {
+    MM_DEQ_AUTO = 0,
+    MM_DEQ_SELECT = 1,   /* any codebook: per-field select of the entry, fp32 FMA */
+    MM_DEQ_AFFINE = 2    /* codebook[c] = c0 + c*d exactly (and no zero entry at field 3):
+                            fields used in place as exact fp32 subnormals in packed f32x2
+                            FMAs, y = scale * (c0 * sum x + d * sum c x) */
+};
+
+typedef struct {
+    int split;           /* lanes sharing one row's dot product: 0 (auto), 4, 8, 16 */
+    int rows_per_lane;   /* rows each lane carries: 0 (auto), 1, 2, 4 */
+    int warps;           /* warps per CTA: 0 (auto), 1..16 */
+    int dequant;         /* MM_DEQ_* */
+    int pdl;             /* 1: launch with programmatic dependent launch so the
+                            kernel's prologue overlaps the previous kernel; it
+                            still waits for that kernel before reading x */
+    int weights_static;  /* 1: promise that codes and scales are not written by
+                            work queued before this call, so their loads may start
+                            before the wait on the previous kernel (needs pdl) */
+    int reserved[6];
+} mm_gemv_opts;
+
+mm_status mm_gemv_packed2_ex(const uint8_t *codes, const uint16_t *scales, const uint16_t *x,
+                             float *y, int64_t rows, int64_t cols, const float codebook[4],
+                             mm_stream_t stream, const mm_gemv_opts *opts);
+
+typedef struct {
+    int tile;       /* 0 = automatic, else a tile id */
+    int reserved[7];
+} mm_gemm_packed2_opts;
+
+mm_status mm_gemm_packed2_ex(const uint8_t *codes, const uint16_t *scales, const uint16_t *X,
+                             float *Y, int64_t M, int64_t rows, int64_t cols,
+                             const float codebook[4], mm_stream_t stream,
+                             const mm_gemm_packed2_opts *opts);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MM_H_ */

@@ -1,0 +1,148 @@
+"""The C-ABI library builds, loads and exports every symbol include/mm.h declares;
+argument checks return their status codes before any CUDA call (no GPU needed).
+
+Every call here is rejected by argument validation, so no pointer passed is
+ever dereferenced and no kernel is launched, on any machine.
+"""
+import ctypes
+import os
+import re
+
+import pytest
+
+import dense_packed_bit_gb300 as mm
+from dense_packed_bit_gb300 import build as mmbuild
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+FAKE = 0x10000  # never dereferenced: every call below fails validation first
+
+
+@pytest.fixture(scope="module")
+def lib():
+    mmbuild.build()
+    return mm.load_library()
+
+
+def header_functions():
+    src = open(os.path.join(ROOT, "include", "mm.h")).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(mm_[a-z0-9_]+)\s*\(", src)))
+
+
+def test_header_lists_the_boundary():
+    names = header_functions()
+    for n in ["mm_gemm_f32", "mm_gemv_packed2", "mm_gemm_packed2", "mm_last_error", "mm_version",
+              "mm_check_device_error", "mm_gemm_f32_ex", "mm_gemv_packed2_ex", "mm_gemm_packed2_ex"]:
+        assert n in names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for name in header_functions():
+        assert hasattr(lib, name), name
+        assert name in mm.SIGNATURES, f"binding lacks {name}"
+
+
+def test_library_has_no_oracle_symbols(lib):
+    # the product library must not carry the oracle
+    for name in ["orc_gemm", "orc_packed_gemm", "orc_unpack2"]:
+        with pytest.raises(AttributeError):
+            getattr(lib, name)
+
+
+def test_version(lib):
+    assert mm.mm_version() == 100
+
+
+def _status(fn, *args):
+    return fn(*args)
+
+
+@pytest.mark.parametrize("case", [
+    dict(tA=2), dict(M=0), dict(N=-1), dict(K=0), dict(A=None), dict(B=None), dict(C=None),
+    dict(lda=3), dict(ldb=4), dict(ldc=5), dict(tA=1, lda=7), dict(tB=1, ldb=7),
+])
+def test_gemm_argument_errors(lib, case):
+    a = dict(tA=0, tB=0, M=8, N=8, K=8, A=FAKE, lda=8, B=FAKE + 4096, ldb=8, C=FAKE + 8192, ldc=8)
+    a.update(case)
+    st = lib.mm_gemm_f32(a["tA"], a["tB"], a["M"], a["N"], a["K"], a["A"], a["lda"], a["B"], a["ldb"],
+                         a["C"], a["ldc"], None)
+    assert st == mm.MM_ERR_INVALID_ARG, lib.mm_last_error()
+    assert lib.mm_last_error()
+
+
+def test_gemm_overlap_rejected(lib):
+    # C overlapping A
+    st = lib.mm_gemm_f32(0, 0, 8, 8, 8, FAKE, 8, FAKE + 4096, 8, FAKE + 64, 8, None)
+    assert st == mm.MM_ERR_INVALID_ARG and b"overlap" in lib.mm_last_error()
+
+
+def test_gemm_bad_path_option(lib):
+    o = mm.GemmOpts(7, 0)
+    st = lib.mm_gemm_f32_ex(0, 0, 8, 8, 8, FAKE, 8, FAKE + 4096, 8, FAKE + 8192, 8, None, ctypes.byref(o))
+    assert st == mm.MM_ERR_INVALID_ARG
+
+
+def _cb(*v):
+    return (ctypes.c_float * 4)(*v)
+
+
+@pytest.mark.parametrize("case", [
+    dict(codes=None), dict(scales=None), dict(x=None), dict(y=None), dict(rows=0), dict(cols=0),
+    dict(cb=None), dict(cb=(0.0, float("nan"), 1.0, 2.0)), dict(cb=(0.0, float("inf"), 1.0, 2.0)),
+])
+def test_gemv_argument_errors(lib, case):
+    a = dict(codes=FAKE, scales=FAKE + 0x100000, x=FAKE + 0x200000, y=FAKE + 0x300000, rows=64, cols=64,
+             cb=(-2.0, -1.0, 0.0, 1.0))
+    a.update(case)
+    cb = None if a["cb"] is None else _cb(*a["cb"])
+    st = lib.mm_gemv_packed2(a["codes"], a["scales"], a["x"], a["y"], a["rows"], a["cols"], cb, None)
+    assert st == mm.MM_ERR_INVALID_ARG, lib.mm_last_error()
+
+
+def test_gemv_output_overlap_rejected(lib):
+    st = lib.mm_gemv_packed2(FAKE, FAKE + 0x100000, FAKE + 0x200000, FAKE + 8, 64, 64, _cb(-2, -1, 0, 1), None)
+    assert st == mm.MM_ERR_INVALID_ARG and b"overlap" in lib.mm_last_error()
+
+
+@pytest.mark.parametrize("opt", [dict(split=3), dict(rows_per_lane=3), dict(warps=17), dict(dequant=9),
+                                 dict(pdl=2), dict(weights_static=5)])
+def test_gemv_bad_options(lib, opt):
+    o = mm.GemvOpts(**opt)
+    st = lib.mm_gemv_packed2_ex(FAKE, FAKE + 0x100000, FAKE + 0x200000, FAKE + 0x300000, 64, 64,
+                                _cb(-2, -1, 0, 1), None, ctypes.byref(o))
+    assert st == mm.MM_ERR_INVALID_ARG
+
+
+def test_gemv_affine_decode_needs_affine_codebook(lib):
+    o = mm.GemvOpts(dequant=mm.MM_DEQ_AFFINE)
+    st = lib.mm_gemv_packed2_ex(FAKE, FAKE + 0x100000, FAKE + 0x200000, FAKE + 0x300000, 64, 64,
+                                _cb(-1, 0, 1, 0), None, ctypes.byref(o))
+    assert st == mm.MM_ERR_INVALID_ARG and b"affine" in lib.mm_last_error()
+
+
+@pytest.mark.parametrize("case", [dict(M=0), dict(rows=-3), dict(X=None), dict(cb=None)])
+def test_gemm_packed_argument_errors(lib, case):
+    a = dict(M=4, rows=64, cols=64, X=FAKE + 0x200000, cb=(-1.0, 0.0, 1.0, 0.0))
+    a.update(case)
+    cb = None if a["cb"] is None else _cb(*a["cb"])
+    st = lib.mm_gemm_packed2(FAKE, FAKE + 0x100000, a["X"], FAKE + 0x300000, a["M"], a["rows"], a["cols"],
+                             cb, None)
+    assert st == mm.MM_ERR_INVALID_ARG
+
+
+def test_python_binding_raises_with_message(lib):
+    with pytest.raises(mm.MMError) as ei:
+        mm.mm_gemm_f32(0, 0, 0, 8, 8, FAKE, 8, FAKE, 8, FAKE, 8, stream=0)
+    assert ei.value.status == mm.MM_ERR_INVALID_ARG and "M, N, K" in str(ei.value)
+
+
+def test_missing_library_fails_loudly(monkeypatch):
+    import importlib
+    monkeypatch.setenv("MM_LIBRARY", "/nonexistent/libmm.so")
+    mod = importlib.reload(mm)
+    try:
+        with pytest.raises(mm.MMError):
+            mod.load_library()
+    finally:
+        monkeypatch.delenv("MM_LIBRARY")
+        importlib.reload(mm)

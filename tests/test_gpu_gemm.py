@@ -1,0 +1,145 @@
+"""GPU parity of the dense fp32 GEMM (through the C ABI) against the fp64 oracle.
+
+Sizes span several 128 x 128 tiles with ragged tails in every dimension; the
+GPT-2 MLP up-projection (64 x 768 x 3072) and the square 2048^3 layouts are
+checked on every output; the training-shape set (8192 / 2048 / 8192) on whole
+sampled rows and columns plus random outputs.
+"""
+import numpy as np
+import pytest
+
+import dense_packed_bit_gb300 as mm
+from dense_packed_bit_gb300 import synth
+from gpu_util import check_bound, check_exact, empty_f32, to_dev, to_host
+
+pytestmark = pytest.mark.gpu
+
+LAYOUTS = {"nn": (0, 0), "nt": (0, 1), "tn": (1, 0), "tt": (1, 1)}
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    from dense_packed_bit_gb300 import build
+    build.build()
+    mm.load_library()
+
+
+def run(tA, tB, M, N, K, A, B, lda=None, ldb=None, ldc=None, path=mm.MM_GEMM_AUTO):
+    lda = lda or A.shape[1]
+    ldb = ldb or B.shape[1]
+    ldc = ldc or N
+    dA, dB = to_dev(A), to_dev(B)
+    dC = empty_f32((M, ldc))
+    mm.mm_gemm_f32_ex(tA, tB, M, N, K, dA, lda, dB, ldb, dC, ldc, path=path)
+    mm.mm_check_device_error()
+    return to_host(dC)
+
+
+def stored(tA, tB, M, N, K, seed, kind="normal"):
+    a_shape = (K, M) if tA else (M, K)
+    b_shape = (N, K) if tB else (K, N)
+    if kind == "int":
+        rng = np.random.default_rng(seed)
+        return (rng.integers(-6, 7, size=a_shape).astype(np.float32),
+                rng.integers(-6, 7, size=b_shape).astype(np.float32))
+    return synth.normal_f32(seed, a_shape, 1.0), synth.normal_f32(seed + 1, b_shape, 1.0)
+
+
+SHAPES = [(1, 1, 1), (3, 17, 5), (65, 129, 33), (127, 63, 129), (200, 300, 97), (257, 130, 1000)]
+
+
+@pytest.mark.parametrize("layout", list(LAYOUTS))
+@pytest.mark.parametrize("shape", SHAPES)
+def test_gemm_ragged_shapes(oracle, layout, shape):
+    tA, tB = LAYOUTS[layout]
+    M, N, K = shape
+    A, B = stored(tA, tB, M, N, K, seed=1000 * list(LAYOUTS).index(layout) + 7 * M + 3 * N + K)
+    C = run(tA, tB, M, N, K, A, B)
+    ref, T = oracle.gemm(tA, tB, M, N, K, A, B)
+    check_bound(C, ref, T, f"{layout} {shape}")
+
+
+@pytest.mark.parametrize("layout", list(LAYOUTS))
+def test_gemm_unaligned_leading_dims_use_general_path(oracle, layout):
+    # leading dimensions that are not a multiple of 4 floats cannot be described by TMA
+    tA, tB = LAYOUTS[layout]
+    M, N, K = 70, 45, 83
+    A, B = stored(tA, tB, M, N, K, seed=17)
+    Ap = np.zeros((A.shape[0], A.shape[1] + 3), np.float32); Ap[:, :A.shape[1]] = A
+    Bp = np.zeros((B.shape[0], B.shape[1] + 1), np.float32); Bp[:, :B.shape[1]] = B
+    C = run(tA, tB, M, N, K, Ap, Bp, lda=Ap.shape[1], ldb=Bp.shape[1], ldc=N + 5)
+    ref, T = oracle.gemm(tA, tB, M, N, K, A, B)
+    check_bound(C[:, :N], ref, T, layout)
+    assert np.all(np.isnan(C[:, N:])), "columns past N were written"
+
+
+@pytest.mark.parametrize("layout", list(LAYOUTS))
+def test_gemm_padded_ld_tma_path_and_canary(oracle, layout):
+    tA, tB = LAYOUTS[layout]
+    M, N, K = 150, 260, 70
+    A, B = stored(tA, tB, M, N, K, seed=23)
+    lda = (A.shape[1] + 3) // 4 * 4 + 4   # multiples of 4 floats: the TMA path applies
+    ldb = (B.shape[1] + 3) // 4 * 4 + 8
+    Ap = np.full((A.shape[0], lda), 7.0, np.float32); Ap[:, :A.shape[1]] = A
+    Bp = np.full((B.shape[0], ldb), -5.0, np.float32); Bp[:, :B.shape[1]] = B
+    C = run(tA, tB, M, N, K, Ap, Bp, lda=Ap.shape[1], ldb=Bp.shape[1], ldc=N + 12)
+    ref, T = oracle.gemm(tA, tB, M, N, K, A, B)
+    check_bound(C[:, :N], ref, T, layout)
+    assert np.all(np.isnan(C[:, N:])), "columns past N were written"
+
+
+@pytest.mark.parametrize("layout", ["nn", "nt", "tn"])
+def test_gemm_small_integers_bit_exact(oracle, layout):
+    # every partial sum is an integer below 2^24, so any summation order is exact
+    tA, tB = LAYOUTS[layout]
+    M, N, K = 300, 270, 513
+    A, B = stored(tA, tB, M, N, K, seed=31, kind="int")
+    ref, _ = oracle.gemm(tA, tB, M, N, K, A, B)
+    for path in (mm.MM_GEMM_AUTO, mm.MM_GEMM_FFMA):
+        check_exact(run(tA, tB, M, N, K, A, B, path=path), ref, f"{layout} path {path}")
+
+
+def test_gemm_all_ones_is_K():
+    M, N, K = 129, 257, 1000
+    C = run(0, 0, M, N, K, np.ones((M, K), np.float32), np.ones((K, N), np.float32))
+    assert np.all(C == K)
+
+
+@pytest.mark.parametrize("layout", ["nn", "nt", "tn"])
+def test_gemm_deterministic(layout):
+    tA, tB = LAYOUTS[layout]
+    M, N, K = 333, 444, 555
+    A, B = stored(tA, tB, M, N, K, seed=41)
+    c1 = run(tA, tB, M, N, K, A, B)
+    c2 = run(tA, tB, M, N, K, A, B)
+    assert np.array_equal(c1.view(np.uint32), c2.view(np.uint32))
+
+
+def test_gpt2_mlp_up_64x768x3072_all_outputs(oracle):
+    c = synth.gpt2_mlp_up_64x768x3072()
+    C = run(c.transA, c.transB, c.M, c.N, c.K, c.A, c.B)
+    ref, T = oracle.gemm(c.transA, c.transB, c.M, c.N, c.K, c.A, c.B)
+    check_bound(C, ref, T, c.name)
+
+
+@pytest.mark.parametrize("layout", ["nn", "nt", "tn"])
+def test_square_2048_all_outputs(oracle, layout):
+    c = synth.square_2048(layout)
+    C = run(c.transA, c.transB, c.M, c.N, c.K, c.A, c.B)
+    ref, T = oracle.gemm(c.transA, c.transB, c.M, c.N, c.K, c.A, c.B)
+    worst = check_bound(C, ref, T, c.name)
+    print(f"{c.name}: worst |err|/T = {worst:.3e}")
+
+
+@pytest.mark.parametrize("which", ["fwd", "dA", "dB"])
+def test_training_set_sampled(oracle, which):
+    c = synth.training_set_8192(which)
+    C = run(c.transA, c.transB, c.M, c.N, c.K, c.A, c.B)
+    rng = np.random.default_rng(7)
+    rows = [0, c.M - 1, int(rng.integers(c.M))]
+    cols = [0, c.N - 1, int(rng.integers(c.N))]
+    ii = np.concatenate([np.repeat(rows, c.N), np.tile(np.arange(c.M), len(cols)), rng.integers(0, c.M, 4000)])
+    jj = np.concatenate([np.tile(np.arange(c.N), len(rows)), np.repeat(cols, c.M), rng.integers(0, c.N, 4000)])
+    ref, T = oracle.gemm_at(c.transA, c.transB, c.K, c.A, c.B, ii, jj)
+    worst = check_bound(C[ii, jj], ref, T, c.name)
+    print(f"{c.name}: {len(ii)} outputs, worst |err|/T = {worst:.3e}")

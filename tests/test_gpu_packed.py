@@ -1,0 +1,199 @@
+"""GPU parity of the packed 2-bit GEMV and skinny GEMM (through the C ABI) against the oracle.
+
+The 2-bit 12,288 x 1,536 GEMV is checked on every output of all 64 rotated
+matrices; the ternary encoder block on every output of its first and last
+layers and sampled outputs of the rest.  Field decoding is checked bit for bit
+with one-hot activations and integer-valued activations.
+"""
+import numpy as np
+import pytest
+
+import dense_packed_bit_gb300 as mm
+from dense_packed_bit_gb300 import synth
+from gpu_util import check_bound, check_exact, empty_f32, to_dev, to_host
+
+pytestmark = pytest.mark.gpu
+
+CB2 = synth.CODEBOOK_2BIT
+CBT = synth.CODEBOOK_TERNARY
+CB_ODD = np.array([0.3, -1.7, 2.5, 0.01], np.float32)   # not affine: select decode
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    from dense_packed_bit_gb300 import build
+    build.build()
+    mm.load_library()
+
+
+def gemv(codes, scales, x, rows, cols, cb, **opts):
+    dc, ds, dx = to_dev(codes), to_dev(scales), to_dev(x.reshape(-1))
+    dy = empty_f32((rows,))
+    if opts:
+        mm.mm_gemv_packed2_ex(dc, ds, dx, dy, rows, cols, cb, **opts)
+    else:
+        mm.mm_gemv_packed2(dc, ds, dx, dy, rows, cols, cb)
+    return to_host(dy)
+
+
+def gemm_packed(codes, scales, X, M, rows, cols, cb):
+    dc, ds, dX = to_dev(codes), to_dev(scales), to_dev(X)
+    dY = empty_f32((M, rows))
+    mm.mm_gemm_packed2(dc, ds, dX, dY, M, rows, cols, cb)
+    return to_host(dY)
+
+
+def rand_case(rows, cols, M=1, seed=0, kind="uniform2"):
+    rb = (cols + 3) // 4
+    codes = (synth.random_bytes(seed, rows * rb) if kind == "uniform2"
+             else synth.ternary_field_bytes(seed, rows * rb)).reshape(rows, rb)
+    scales = synth.uniform_f16_bits(seed + 1, (rows,), 0.005, 0.05)
+    X = synth.normal_f16_bits(seed + 2, (M, cols))
+    return codes, scales, X
+
+
+# ------------------------------------------------------------------ GEMV
+
+def test_gemv_2bit_12288x1536_all_64_matrices(oracle):
+    worst = 0.0
+    for i in range(64):
+        c = synth.gemv_2bit_12288x1536(i)
+        y = gemv(c.codes, c.scales, c.X, c.rows, c.cols, c.codebook)
+        ref, T = oracle.packed_gemm(c.codes, c.scales, c.X, c.rows, c.cols, c.codebook)
+        worst = max(worst, check_bound(y, ref[0], T[0], c.name))
+    print(f"64 matrices: worst |err|/T = {worst:.3e}")
+
+
+VARIANTS = [dict(split=s, rows_per_lane=r, warps=w, dequant=d, pdl=p, weights_static=ws)
+            for s in (4, 8, 16) for r in (1, 2, 4) for w in (2, 4, 8) for d in (1, 2)
+            for (p, ws) in ((0, 0), (1, 1))]
+
+
+@pytest.mark.parametrize("v", VARIANTS, ids=lambda v: "s{split}r{rows_per_lane}w{warps}d{dequant}p{pdl}".format(**v))
+def test_gemv_variant_matrix(oracle, v):
+    rows, cols = 1000, 1536 + 256   # ragged row count; 28 chunks per row (not a multiple of S * CPL)
+    codes, scales, x = rand_case(rows, cols, seed=101)
+    y = gemv(codes, scales, x, rows, cols, CB2, **v)
+    ref, T = oracle.packed_gemm(codes, scales, x, rows, cols, CB2)
+    check_bound(y, ref[0], T[0], str(v))
+
+
+@pytest.mark.parametrize("rows,cols", [(1, 1), (1, 64), (7, 3), (33, 63), (129, 64), (65, 65), (300, 100),
+                                       (17, 4097), (5, 40000), (2, 192)])
+@pytest.mark.parametrize("cb", ["2bit", "odd"])
+def test_gemv_edge_shapes(oracle, rows, cols, cb):
+    codebook = CB2 if cb == "2bit" else CB_ODD
+    codes, scales, x = rand_case(rows, cols, seed=rows * 131 + cols)
+    y = gemv(codes, scales, x, rows, cols, codebook)
+    ref, T = oracle.packed_gemm(codes, scales, x, rows, cols, codebook)
+    check_bound(y, ref[0], T[0], f"{rows}x{cols}")
+
+
+@pytest.mark.parametrize("cols", [5, 66, 1538])
+def test_gemv_ignores_fields_past_cols(oracle, cols):
+    rows = 40
+    codes, scales, x = rand_case(rows, cols, seed=cols)
+    dirty = codes.copy()
+    dirty[:, -1] |= np.uint8((0xFF << (2 * (cols % 4))) & 0xFF)
+    y_clean = gemv(codes, scales, x, rows, cols, CB2)
+    y_dirty = gemv(dirty, scales, x, rows, cols, CB2)
+    assert np.array_equal(y_clean, y_dirty)
+
+
+@pytest.mark.parametrize("dequant", [1, 2])
+@pytest.mark.parametrize("cols", [64, 1536, 100])
+def test_gemv_one_hot_decodes_exactly(oracle, dequant, cols):
+    # x = e_k: every y_r must be exactly fp32(scale_r * cb[field(r, k)])
+    rows = 257
+    codes, scales, _ = rand_case(rows, cols, seed=5 + cols)
+    fields = oracle.unpack2(codes, rows, cols)
+    ks = sorted(set([0, 1, 15, 16, 31, cols - 1] + list(range(2, cols, max(1, cols // 37)))))
+    for k in ks:
+        if k >= cols:
+            continue
+        x = np.zeros(cols, np.uint16)
+        x[k] = 0x3C00
+        opts = dict(dequant=dequant) if cols % 64 == 0 else {}
+        y = gemv(codes, scales, x, rows, cols, CB2, **opts)
+        ref, _ = oracle.packed_gemm(codes, scales, x, rows, cols, CB2)
+        check_exact(y, ref[0], f"k={k}")
+        s = scales.view(np.float16).astype(np.float64)
+        assert np.array_equal(y.astype(np.float64), s * CB2[fields[:, k]].astype(np.float64))
+
+
+@pytest.mark.parametrize("dequant", [1, 2])
+def test_gemv_integer_activations_bit_exact(oracle, dequant):
+    rows, cols = 500, 1536
+    codes, _, _ = rand_case(rows, cols, seed=77)
+    scales = np.full(rows, 0x3C00, np.uint16)
+    rng = np.random.default_rng(3)
+    x = rng.integers(-3, 4, size=cols).astype(np.float16).view(np.uint16)
+    y = gemv(codes, scales, x, rows, cols, CB2, dequant=dequant)
+    ref, _ = oracle.packed_gemm(codes, scales, x, rows, cols, CB2)
+    check_exact(y, ref[0], "integer x")
+
+
+def test_gemv_deterministic():
+    c = synth.gemv_2bit_12288x1536(3)
+    y1 = gemv(c.codes, c.scales, c.X, c.rows, c.cols, c.codebook)
+    y2 = gemv(c.codes, c.scales, c.X, c.rows, c.cols, c.codebook)
+    assert np.array_equal(y1.view(np.uint32), y2.view(np.uint32))
+
+
+def test_gemv_zero_bound_rows_are_zero(oracle):
+    # rows of field 2 (entry 0) give T = 0, so y must be exactly 0
+    rows, cols = 64, 1536
+    codes = np.full((rows, cols // 4), 0xAA, np.uint8)
+    scales = synth.uniform_f16_bits(9, (rows,), 0.005, 0.05)
+    x = synth.normal_f16_bits(10, (cols,))
+    for d in (1, 2):
+        y = gemv(codes, scales, x, rows, cols, CB2, dequant=d)
+        assert np.all(y == 0.0)
+
+
+# ------------------------------------------------------------------ skinny GEMM
+
+@pytest.mark.parametrize("M,rows,cols", [(1, 1, 1), (3, 17, 5), (65, 129, 64), (222, 130, 100),
+                                         (7, 64, 768), (130, 33, 1537)])
+@pytest.mark.parametrize("cb", ["ternary", "2bit", "odd"])
+def test_gemm_packed_edge_shapes(oracle, M, rows, cols, cb):
+    codebook = {"ternary": CBT, "2bit": CB2, "odd": CB_ODD}[cb]
+    codes, scales, X = rand_case(rows, cols, M=M, seed=M * 1000 + rows + cols,
+                                 kind="ternary" if cb == "ternary" else "uniform2")
+    Y = gemm_packed(codes, scales, X, M, rows, cols, codebook)
+    ref, T = oracle.packed_gemm(codes, scales, X, rows, cols, codebook)
+    check_bound(Y, ref, T, f"{M}x{rows}x{cols}")
+
+
+@pytest.mark.parametrize("layer", [0, 15])
+@pytest.mark.parametrize("proj", ["up", "down"])
+def test_ternary_encoder_full_layers(oracle, layer, proj):
+    c = synth.ternary_encoder_layer(layer, proj)
+    M = c.X.shape[0]
+    Y = gemm_packed(c.codes, c.scales, c.X, M, c.rows, c.cols, c.codebook)
+    ref, T = oracle.packed_gemm(c.codes, c.scales, c.X, c.rows, c.cols, c.codebook)
+    worst = check_bound(Y, ref, T, c.name)
+    print(f"{c.name}: worst |err|/T = {worst:.3e}")
+
+
+@pytest.mark.parametrize("proj", ["up", "down"])
+def test_ternary_encoder_other_layers_sampled(oracle, proj):
+    rng = np.random.default_rng(11)
+    for layer in range(1, 15):
+        c = synth.ternary_encoder_layer(layer, proj)
+        M = c.X.shape[0]
+        Y = gemm_packed(c.codes, c.scales, c.X, M, c.rows, c.cols, c.codebook)
+        mm_i = rng.integers(0, M, 3000)
+        rr_i = rng.integers(0, c.rows, 3000)
+        ref, T = oracle.packed_gemm_at(c.codes, c.scales, c.X, c.cols, c.codebook, mm_i, rr_i)
+        check_bound(Y[mm_i, rr_i], ref, T, c.name)
+
+
+def test_gemm_packed_matches_gemv_rows(oracle):
+    # M = 1 skinny GEMM and GEMV compute the same product
+    c = synth.gemv_2bit_12288x1536(0)
+    y = gemv(c.codes, c.scales, c.X, c.rows, c.cols, c.codebook)
+    Y = gemm_packed(c.codes, c.scales, c.X, 1, c.rows, c.cols, c.codebook)
+    ref, T = oracle.packed_gemm(c.codes, c.scales, c.X, c.rows, c.cols, c.codebook)
+    check_bound(y, ref[0], T[0], "gemv")
+    check_bound(Y[0], ref[0], T[0], "gemm M=1")
