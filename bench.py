@@ -7,14 +7,16 @@ Prints ONE JSON line (rank 0).  One step is one pass of the whole hot path:
   1. square 2048^3 fp32 GEMM in the NN, NT and TN layouts (L2 flushed first
      by writing a 512 MiB buffer, since the 48 MiB of operands fit in L2);
   2. the 2-bit 12,288 x 1,536 GEMV over a rotation of 64 distinct matrices
-     (288 MiB of codes, larger than the 129 MB L2), back to back, launched with
-     programmatic dependent launch (weights are static, so their loads start
-     before the wait on the previous call);
+     (288 MiB of codes, larger than the 129 MB L2), back to back, twice: as 64
+     independent calls (programmatic dependent launch, no call waits for the
+     previous one) and as a dependent chain (each call waits for the previous
+     kernel before reading x; only its weight loads start early);
   3. the ternary 16-layer encoder block: 16 x (222x768 -> 3072, 222x3072 -> 768).
-Each phase is timed with CUDA events on the stream the kernels run on.  The
-headline value is the 2048^3 GEMM throughput (TFLOP/s); the GEMV weight
-bandwidth (GB/s, 4,718,592 bytes of weights per call over the per-call time,
-the measure defined on the Kernel 0112 page) is reported beside it.
+Each phase is captured once as a CUDA graph and replayed; every replay is timed
+with CUDA events on the stream it runs on.  The headline value is the 2048^3
+GEMM throughput (TFLOP/s); the GEMV weight bandwidth (GB/s: 4,718,592 bytes of
+weights per call over the per-call time, the measure defined on the Kernel 0112
+page, whose runs are batches of back-to-back dispatches) is reported beside it.
 
 Multi-GPU (torchrun): every rank runs the same step on its own GPU with its own
 inputs (replicas, weak scaling, no collective on the data path); times are
@@ -54,13 +56,10 @@ WORKLOAD = ("square_2048_fp32_gemm_nn_nt_tn + gemv2bit_12288x1536_rotation64 + "
 def parse_args(argv=None):
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--steps", type=int, default=50)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", choices=["mm", "reference"], default="mm")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--gemv-split", type=int, default=8)
-    ap.add_argument("--gemv-rows", type=int, default=4)
-    ap.add_argument("--gemv-warps", type=int, default=4)
     ap.add_argument("--gemm-path", type=int, default=0)
     return ap.parse_args(argv)
 
@@ -235,39 +234,71 @@ class Workload:
         self.flush = torch.empty(512 * 1024 * 1024 // 4, dtype=torch.float32, device=device)
         self.args = args
 
-    def launches_per_step(self):
-        return len(self.gemm) + N_GEMV + len(self.tern)
+
+GEMV_INDEP = dict(split=8, rows_per_lane=4, warps=8, dequant=2, pdl=1, independent=1)
+GEMV_CHAINED = dict(split=3, rows_per_lane=2, warps=6, dequant=3, pdl=1, weights_static=1)
 
 
-def run_step(w: Workload, ev, stream):
-    """One pass of the hot path; ev: list of (start, end) event pairs per phase."""
+def capture_phases(w: Workload, stream):
+    """CUDA graphs of each phase (launch-bound loops replay without host launch cost).
+
+    gemm   : the three 2048^3 products (NN, NT, TN)
+    gemv   : the 64-matrix rotation as independent calls (no call reads another's output;
+             each kernel skips the wait on its predecessor and overlaps it completely)
+    gemv_c : the same rotation as a dependent chain (each call waits for the previous
+             kernel before reading x, only its weight loads start early)
+    tern   : the 16-layer ternary encoder block (32 skinny GEMMs)
+    """
+    import torch
     import dense_packed_bit_gb300 as mm
     a = w.args
-    w.flush.fill_(1.0)  # evict the GEMM operands from L2 (torch kernel, not timed)
-    for i, g in enumerate(w.gemm):
-        c = g["case"]
-        ev["gemm"][i][0].record(stream)
-        mm.mm_gemm_f32_ex(c.transA, c.transB, c.M, c.N, c.K, g["A"], g["A"].shape[1], g["B"], g["B"].shape[1],
-                          g["C"], c.N, stream, path=a.gemm_path)
-        ev["gemm"][i][1].record(stream)
-    ev["gemv"][0].record(stream)
-    for i in range(N_GEMV):
-        mm.mm_gemv_packed2_ex(w.gemv_codes[i], w.gemv_scales[i], w.gemv_x, w.gemv_y[i], 12288, 1536, w.gemv_cb,
-                              stream, split=a.gemv_split, rows_per_lane=a.gemv_rows, warps=a.gemv_warps,
-                              pdl=1, weights_static=1)
-    ev["gemv"][1].record(stream)
-    ev["tern"][0].record(stream)
-    for t in w.tern:
-        c = t["case"]
-        mm.mm_gemm_packed2(t["codes"], t["scales"], t["X"], t["Y"], c.X.shape[0], c.rows, c.cols, c.codebook,
-                           stream)
-    ev["tern"][1].record(stream)
+
+    def gemm():
+        for g in w.gemm:
+            c = g["case"]
+            mm.mm_gemm_f32_ex(c.transA, c.transB, c.M, c.N, c.K, g["A"], g["A"].shape[1], g["B"],
+                              g["B"].shape[1], g["C"], c.N, path=a.gemm_path)
+
+    def gemv(opts):
+        def f():
+            for i in range(N_GEMV):
+                mm.mm_gemv_packed2_ex(w.gemv_codes[i], w.gemv_scales[i], w.gemv_x, w.gemv_y[i], 12288, 1536,
+                                      w.gemv_cb, **opts)
+        return f
+
+    def tern():
+        for t in w.tern:
+            c = t["case"]
+            mm.mm_gemm_packed2(t["codes"], t["scales"], t["X"], t["Y"], c.X.shape[0], c.rows, c.cols, c.codebook)
+
+    graphs = {}
+    for name, fn in (("gemm", gemm), ("gemv", gemv(GEMV_INDEP)), ("gemv_c", gemv(GEMV_CHAINED)), ("tern", tern)):
+        with torch.cuda.stream(stream):
+            fn()  # warm the kernels' one-time setup outside capture
+        torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            fn()
+        graphs[name] = g
+    return graphs
+
+
+LAUNCHES_PER_STEP = 3 + 2 * N_GEMV + 2 * N_LAYERS
+
+
+def run_step(w: Workload, graphs, ev, stream):
+    """One pass of the hot path; ev maps each phase to a (start, end) event pair."""
+    w.flush.fill_(1.0)  # evict the GEMM operands from L2 (torch kernel, outside the events)
+    for name in ("gemm", "gemv", "gemv_c", "tern"):
+        ev[name][0].record(stream)
+        graphs[name].replay()
+        ev[name][1].record(stream)
 
 
 def new_events():
     import torch
     mk = lambda: (torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-    return {"gemm": [mk() for _ in range(3)], "gemv": mk(), "tern": mk()}
+    return {"gemm": mk(), "gemv": mk(), "gemv_c": mk(), "tern": mk()}
 
 
 def e2e_gemm(w: Workload, steps: int, stream):
@@ -391,10 +422,11 @@ def main_mm(args):
 
     w = Workload(dev, rank, args)
     stream = torch.cuda.Stream(device=dev)
+    graphs = capture_phases(w, stream)
     ev_steps = [new_events() for _ in range(args.steps)]
     with torch.cuda.stream(stream):
         for _ in range(max(3, args.warmup)):
-            run_step(w, new_events(), stream)
+            run_step(w, graphs, new_events(), stream)
         mm.mm_check_device_error(stream)
         torch.cuda.synchronize()
 
@@ -404,32 +436,33 @@ def main_mm(args):
         torch.cuda.synchronize()
         t0 = time.perf_counter()
         for s in range(args.steps):
-            run_step(w, ev_steps[s], stream)
+            run_step(w, graphs, ev_steps[s], stream)
         torch.cuda.synchronize()
         barrier(dev)
         wall = time.perf_counter() - t0
         clk = clocks.stop()
         mm.mm_check_device_error(stream)
 
-    gemm_ms = [[e[0].elapsed_time(e[1]) for e in ev["gemm"]] for ev in ev_steps]
-    gemv_ms = [ev["gemv"][0].elapsed_time(ev["gemv"][1]) for ev in ev_steps]
-    tern_ms = [ev["tern"][0].elapsed_time(ev["tern"][1]) for ev in ev_steps]
-    gemm_total_s = reduce_max(sum(sum(r) for r in gemm_ms) / 1e3, dev)
-    gemv_total_s = reduce_max(sum(gemv_ms) / 1e3, dev)
-    tern_total_s = reduce_max(sum(tern_ms) / 1e3, dev)
+    def total_s(name):
+        return reduce_max(sum(ev[name][0].elapsed_time(ev[name][1]) for ev in ev_steps) / 1e3, dev)
+
+    gemm_total_s = total_s("gemm")
+    gemv_total_s = total_s("gemv")
+    gemvc_total_s = total_s("gemv_c")
+    tern_total_s = total_s("tern")
     wall = reduce_max(wall, dev)
 
     gemm_tflops = world * 3 * GEMM_FLOP * args.steps / gemm_total_s / 1e12
     per_call_gemv_s = gemv_total_s / (args.steps * N_GEMV)
+    per_call_gemvc_s = gemvc_total_s / (args.steps * N_GEMV)
     gemv_gbs = world * GEMV_WEIGHT_BYTES / per_call_gemv_s / 1e9
     tern_tflops = world * N_LAYERS * TERN_FLOP_PER_LAYER * args.steps / tern_total_s / 1e12
-    step_ms = (gemm_total_s + gemv_total_s + tern_total_s) / args.steps * 1e3
+    step_ms = (gemm_total_s + gemv_total_s + gemvc_total_s + tern_total_s) / args.steps * 1e3
 
     peaks, peaks_src = measured_peaks()
     props = torch.cuda.get_device_properties(dev)
     sms = props.multi_processor_count
     fp32_peak_max = fp32_simt_peak_tflops(sms, peaks.get("sm_max_mhz", 2070.0))
-    per_gemm_ms = {l: statistics.mean(r[i] for r in gemm_ms) for i, l in enumerate(("nn", "nt", "tn"))}
     gemm_per_gpu = 3 * GEMM_FLOP * args.steps / gemm_total_s / 1e12
     if args.gemm_path == mm.MM_GEMM_TF32X3:
         tf32_peak = peaks["bf16_tflops"] * (1.1 / 2.25)
@@ -452,12 +485,16 @@ def main_mm(args):
                    "gemv": "12288x1536 2-bit, 64-matrix rotation (288 MiB > L2), codebook {-2,-1,0,1}",
                    "ternary": "16 layers, M=222, up 768->3072 and down 3072->768",
                    "l2": "512 MiB buffer written before the GEMM phase of every step; GEMV inputs exceed L2",
-                   "gemv_opts": {"split": args.gemv_split, "rows_per_lane": args.gemv_rows,
-                                 "warps": args.gemv_warps, "pdl": 1, "weights_static": 1},
+                   "gemv_opts": {"independent": GEMV_INDEP, "chained": GEMV_CHAINED},
+                   "launch": "each phase replayed as a CUDA graph",
                    "gemm_path": args.gemm_path, "parallelism": f"replicas x{world}"},
-        "gemm_ms": per_gemm_ms,
+        "gemm_ms_per_step": gemm_total_s / args.steps * 1e3,
         "gemv": {"metric": "2-bit 12288x1536 GEMV weight GB/s", "value": gemv_gbs, "unit": "GB/s",
                  "us_per_call": per_call_gemv_s * 1e6,
+                 "mode": "64 independent back-to-back calls over the rotation",
+                 "chained": {"value": world * GEMV_WEIGHT_BYTES / per_call_gemvc_s / 1e9, "unit": "GB/s",
+                             "us_per_call": per_call_gemvc_s * 1e6,
+                             "mode": "each call waits for the previous kernel before reading x"},
                  "roofline": {"bound": "hbm", "achieved": GEMV_TOTAL_BYTES / per_call_gemv_s / 1e9,
                               "peak": peaks["hbm_gbs"], "unit": "GB/s",
                               "frac": GEMV_TOTAL_BYTES / per_call_gemv_s / 1e9 / peaks["hbm_gbs"],
@@ -466,7 +503,7 @@ def main_mm(args):
         "ternary": {"value": tern_tflops, "unit": "TFLOP/s", "ms_per_block": tern_total_s / args.steps * 1e3},
         "roofline": roof,
         "clocks": clk,
-        "gpu_launches": w.launches_per_step() * args.steps,
+        "gpu_launches": LAUNCHES_PER_STEP * args.steps,
         "wall_s": wall,
     }
     if rank == 0:

@@ -19,12 +19,12 @@ __all__ = [
     "mm_gemm_packed2", "mm_gemm_packed2_ex", "mm_check_device_error",
     "MM_OK", "MM_ERR_INVALID_ARG", "MM_ERR_UNSUPPORTED", "MM_ERR_CUDA", "MM_ERR_TIMEOUT",
     "MM_GEMM_AUTO", "MM_GEMM_FFMA", "MM_GEMM_TF32X3",
-    "MM_DEQ_AUTO", "MM_DEQ_SELECT", "MM_DEQ_AFFINE",
+    "MM_DEQ_AUTO", "MM_DEQ_SELECT", "MM_DEQ_AFFINE", "MM_DEQ_MMA",
 ]
 
 MM_OK, MM_ERR_INVALID_ARG, MM_ERR_UNSUPPORTED, MM_ERR_CUDA, MM_ERR_TIMEOUT = 0, 1, 2, 3, 4
 MM_GEMM_AUTO, MM_GEMM_FFMA, MM_GEMM_TF32X3 = 0, 1, 2
-MM_DEQ_AUTO, MM_DEQ_SELECT, MM_DEQ_AFFINE = 0, 1, 2
+MM_DEQ_AUTO, MM_DEQ_SELECT, MM_DEQ_AFFINE, MM_DEQ_MMA = 0, 1, 2, 3
 
 _PKG = os.path.dirname(os.path.abspath(__file__))
 _lock = threading.Lock()
@@ -41,7 +41,7 @@ class GemmOpts(ctypes.Structure):
 class GemvOpts(ctypes.Structure):
     _fields_ = [("split", ctypes.c_int), ("rows_per_lane", ctypes.c_int), ("warps", ctypes.c_int),
                 ("dequant", ctypes.c_int), ("pdl", ctypes.c_int), ("weights_static", ctypes.c_int),
-                ("reserved", ctypes.c_int * 6)]
+                ("independent", ctypes.c_int), ("reserved", ctypes.c_int * 5)]
 
 
 class GemmPacked2Opts(ctypes.Structure):
@@ -148,8 +148,8 @@ def mm_gemv_packed2(codes, scales, x, y, rows, cols, codebook, stream=None):
 
 
 def mm_gemv_packed2_ex(codes, scales, x, y, rows, cols, codebook, stream=None, *, split=0,
-                       rows_per_lane=0, warps=0, dequant=0, pdl=0, weights_static=0):
-    o = GemvOpts(split, rows_per_lane, warps, dequant, pdl, weights_static)
+                       rows_per_lane=0, warps=0, dequant=0, pdl=0, weights_static=0, independent=0):
+    o = GemvOpts(split, rows_per_lane, warps, dequant, pdl, weights_static, independent)
     _check(load_library().mm_gemv_packed2_ex(_ptr(codes), _ptr(scales), _ptr(x), _ptr(y), rows, cols,
                                              _codebook(codebook), _stream(stream), ctypes.byref(o)))
 

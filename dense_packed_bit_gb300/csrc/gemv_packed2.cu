@@ -137,31 +137,48 @@ __global__ void __launch_bounds__(512) gemv2_vec_kernel(const PackedArgs a, cons
             }
     };
 
-    if (prefetch) {
-        load_batch(0);  // codes are not written by earlier queued work
+    // prefetch: 0 wait for earlier kernels first; 1 codes before the wait;
+    // 2 no wait at all (the caller promised no dependence on queued work)
+    if (prefetch >= 1) {
+        load_batch(0);
         pdl_launch_dependents();
-        pdl_wait();
+        if (prefetch == 1) pdl_wait();
     } else {
         pdl_wait();
         load_batch(0);
         pdl_launch_dependents();
     }
 
-    // ---- stage x as fp32 (prepared for the affine decode)
-    const int n4 = (int)(a.cols >> 2);
-    for (int f = threadIdx.x; f < n4; f += blockDim.x) {
-        const uint2 hv = *reinterpret_cast<const uint2 *>(a.x + 4 * (int64_t)f);
-        float v[4] = {h2f((uint16_t)(hv.x & 0xFFFFu)), h2f((uint16_t)(hv.x >> 16)),
-                      h2f((uint16_t)(hv.y & 0xFFFFu)), h2f((uint16_t)(hv.y >> 16))};
-        if (DQ == kDeqAffine) {
+    // ---- stage x as fp32 (prepared for the affine decode); every 16-byte
+    // load of a batch is issued before any of them is converted
+    const int n8 = (int)(a.cols >> 3);
+    constexpr int XU = 4;
+    for (int base = threadIdx.x; base < n8; base += XU * blockDim.x) {
+        uint4 hv[XU];
 #pragma unroll
-            for (int i = 0; i < 4; ++i) {
-                const int j = (4 * f + i) & 15;        // field index inside its 32-bit word
-                const int p = j < 12 ? 2 * j : 2 * j - 16;  // bit it is read at
-                v[i] *= pow2f(111 - p);
+        for (int u = 0; u < XU; ++u) {
+            const int g = base + u * blockDim.x;
+            if (g < n8) hv[u] = __ldg(reinterpret_cast<const uint4 *>(a.x) + g);
+        }
+#pragma unroll
+        for (int u = 0; u < XU; ++u) {
+            const int g = base + u * blockDim.x;
+            if (g < n8) {
+                const uint32_t hw[4] = {hv[u].x, hv[u].y, hv[u].z, hv[u].w};
+                float v[8];
+#pragma unroll
+                for (int i = 0; i < 8; ++i) {
+                    v[i] = h2f((uint16_t)((hw[i >> 1] >> (16 * (i & 1))) & 0xFFFFu));
+                    if (DQ == kDeqAffine) {
+                        const int j = (8 * g + i) & 15;             // field index inside its 32-bit word
+                        const int p = j < 12 ? 2 * j : 2 * j - 16;  // bit it is read at
+                        v[i] *= pow2f(111 - p);
+                    }
+                }
+                xs[xs_slot(2 * g)] = make_float4(v[0], v[1], v[2], v[3]);
+                xs[xs_slot(2 * g + 1)] = make_float4(v[4], v[5], v[6], v[7]);
             }
         }
-        xs[xs_slot(f)] = make_float4(v[0], v[1], v[2], v[3]);
     }
     __syncthreads();
 
@@ -276,7 +293,7 @@ cudaError_t launch_vec(const PackedArgs &a, const GemvConfig &cfg, cudaStream_t 
     attr[0].val.programmaticStreamSerializationAllowed = cfg.pdl ? 1 : 0;
     lc.attrs = attr;
     lc.numAttrs = 1;
-    const int prefetch = (cfg.pdl && cfg.weights_static) ? 1 : 0;
+    const int prefetch = !cfg.pdl ? 0 : cfg.independent ? 2 : cfg.weights_static ? 1 : 0;
     return cudaLaunchKernelEx(&lc, kern, a, prefetch);
 }
 
@@ -316,10 +333,11 @@ bool codebook_is_affine(const float cb[4]) {
 
 bool gemv_vec_supported(const PackedArgs &a) {
     return a.cols % 64 == 0 && a.cols <= kMaxStagedCols && (reinterpret_cast<uintptr_t>(a.codes) % 16) == 0 &&
-           (reinterpret_cast<uintptr_t>(a.x) % 8) == 0;
+           (reinterpret_cast<uintptr_t>(a.x) % 16) == 0;
 }
 
 cudaError_t launch_gemv_packed2(const PackedArgs &a, const GemvConfig &cfg, cudaStream_t st) {
+    if (cfg.dequant == 3) return launch_gemv_mma(a, cfg, st);
     if (!gemv_vec_supported(a)) {
         cudaLaunchConfig_t lc = {};
         lc.gridDim = dim3((unsigned)((a.rows + 7) / 8));

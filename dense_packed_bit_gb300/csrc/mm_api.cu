@@ -146,30 +146,50 @@ mm_status mm_gemv_packed2_ex(const uint8_t *codes, const uint16_t *scales, const
                              int64_t cols, const float codebook[4], mm_stream_t stream, const mm_gemv_opts *opts) {
     mm_status s = check_packed(codes, scales, x, y, 1, rows, cols, codebook);
     if (s != MM_OK) return s;
-    mm::GemvConfig cfg{8, 4, 4, 0, 1, 0};
+    mm::GemvConfig cfg{0, 0, 0, 0, 1, 0, 0};
     if (opts) {
-        if (opts->split) cfg.split = opts->split;
-        if (opts->rows_per_lane) cfg.rows_per_lane = opts->rows_per_lane;
-        if (opts->warps) cfg.warps = opts->warps;
+        cfg.split = opts->split;
+        cfg.rows_per_lane = opts->rows_per_lane;
+        cfg.warps = opts->warps;
         cfg.dequant = opts->dequant;
         cfg.pdl = opts->pdl;
         cfg.weights_static = opts->weights_static;
+        cfg.independent = opts->independent;
     }
-    if (cfg.split != 4 && cfg.split != 8 && cfg.split != 16) return fail(MM_ERR_INVALID_ARG, "split must be 4, 8 or 16");
-    if (cfg.rows_per_lane != 1 && cfg.rows_per_lane != 2 && cfg.rows_per_lane != 4)
-        return fail(MM_ERR_INVALID_ARG, "rows_per_lane must be 1, 2 or 4");
-    if (cfg.warps < 1 || cfg.warps > 16) return fail(MM_ERR_INVALID_ARG, "warps must be 1..16");
+    const bool affine = mm::codebook_is_affine(codebook);
+    mm::PackedArgs a{codes, scales, x, y, 1, rows, cols, {codebook[0], codebook[1], codebook[2], codebook[3]}};
+    if (cfg.dequant == MM_DEQ_AUTO)
+        cfg.dequant = (affine && mm::gemv_mma_supported(a)) ? MM_DEQ_MMA : affine ? MM_DEQ_AFFINE : MM_DEQ_SELECT;
+    if (cfg.dequant < MM_DEQ_SELECT || cfg.dequant > MM_DEQ_MMA)
+        return fail(MM_ERR_INVALID_ARG, "unknown dequant %d", cfg.dequant);
+    if ((cfg.dequant == MM_DEQ_AFFINE || cfg.dequant == MM_DEQ_MMA) && !affine)
+        return fail(MM_ERR_INVALID_ARG, "affine decode needs codebook[c] == codebook[0] + c*(codebook[1]-codebook[0])");
+    if (cfg.dequant == MM_DEQ_MMA) {
+        if (!mm::gemv_mma_supported(a))
+            return fail(MM_ERR_INVALID_ARG, "tensor-core decode needs cols %% 256 == 0, cols <= 32768, 16-byte aligned codes and x");
+        if (!cfg.split) cfg.split = 3;
+        if (!cfg.rows_per_lane) cfg.rows_per_lane = 2;
+        if (!cfg.warps) cfg.warps = 2 * cfg.split;
+        if (cfg.split != 1 && cfg.split != 2 && cfg.split != 3 && cfg.split != 4 && cfg.split != 6)
+            return fail(MM_ERR_INVALID_ARG, "split must be 1, 2, 3, 4 or 6 for the tensor-core decode");
+        if (cfg.rows_per_lane != 1 && cfg.rows_per_lane != 2 && cfg.rows_per_lane != 4)
+            return fail(MM_ERR_INVALID_ARG, "rows_per_lane must be 1, 2 or 4 for the tensor-core decode");
+        if (cfg.warps < 1 || cfg.warps > (cfg.rows_per_lane >= 2 ? 8 : 16) || cfg.warps % cfg.split)
+            return fail(MM_ERR_INVALID_ARG, "warps must be a multiple of split, at most 16 (8 with rows_per_lane 2 or 4)");
+    } else {
+        if (!cfg.split) cfg.split = 8;
+        if (!cfg.rows_per_lane) cfg.rows_per_lane = 4;
+        if (!cfg.warps) cfg.warps = 8;
+        if (cfg.split != 4 && cfg.split != 8 && cfg.split != 16) return fail(MM_ERR_INVALID_ARG, "split must be 4, 8 or 16");
+        if (cfg.rows_per_lane != 1 && cfg.rows_per_lane != 2 && cfg.rows_per_lane != 4)
+            return fail(MM_ERR_INVALID_ARG, "rows_per_lane must be 1, 2 or 4");
+        if (cfg.warps < 1 || cfg.warps > 16) return fail(MM_ERR_INVALID_ARG, "warps must be 1..16");
+    }
     if (cfg.pdl != 0 && cfg.pdl != 1) return fail(MM_ERR_INVALID_ARG, "pdl must be 0 or 1");
     if (cfg.weights_static != 0 && cfg.weights_static != 1) return fail(MM_ERR_INVALID_ARG, "weights_static must be 0 or 1");
-    const bool affine = mm::codebook_is_affine(codebook);
-    if (cfg.dequant == MM_DEQ_AUTO) cfg.dequant = affine ? MM_DEQ_AFFINE : MM_DEQ_SELECT;
-    if (cfg.dequant != MM_DEQ_SELECT && cfg.dequant != MM_DEQ_AFFINE)
-        return fail(MM_ERR_INVALID_ARG, "unknown dequant %d", cfg.dequant);
-    if (cfg.dequant == MM_DEQ_AFFINE && !affine)
-        return fail(MM_ERR_INVALID_ARG, "affine decode needs codebook[c] == codebook[0] + c*(codebook[1]-codebook[0])");
+    if (cfg.independent != 0 && cfg.independent != 1) return fail(MM_ERR_INVALID_ARG, "independent must be 0 or 1");
     s = check_device();
     if (s != MM_OK) return s;
-    mm::PackedArgs a{codes, scales, x, y, 1, rows, cols, {codebook[0], codebook[1], codebook[2], codebook[3]}};
     cudaError_t e = mm::launch_gemv_packed2(a, cfg, reinterpret_cast<cudaStream_t>(stream));
     if (e != cudaSuccess) return cuda_fail(e, "gemv launch");
     return ok();

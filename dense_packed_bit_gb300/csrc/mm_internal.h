@@ -22,17 +22,22 @@ struct GemvConfig {
     int split;          // lanes per row: 4, 8, 16
     int rows_per_lane;  // 1, 2, 4
     int warps;          // warps per CTA
-    int dequant;        // 1 select, 2 affine
+    int dequant;        // 1 select, 2 affine (SIMT), 3 affine (tensor-core mma)
     int pdl;
     int weights_static;
+    int independent;
 };
 
 // True when cb[c] == cb[0] + c * (cb[1] - cb[0]) holds exactly in fp32 for c = 0..3.
 bool codebook_is_affine(const float cb[4]);
 
-// Vectorised path needs cols % 64 == 0, a 16-byte aligned codes pointer and
-// cols small enough for x to sit in shared memory.
+// Vectorised path needs cols % 64 == 0, 16-byte aligned codes and x pointers
+// and cols small enough for x to sit in shared memory.
 bool gemv_vec_supported(const PackedArgs &a);
+
+// Tensor-core GEMV (affine codebooks): cols % 256 == 0, 16-byte aligned codes and x.
+bool gemv_mma_supported(const PackedArgs &a);
+cudaError_t launch_gemv_mma(const PackedArgs &a, const GemvConfig &cfg, cudaStream_t s);
 
 // Launches the GEMV.  Falls back to the bytewise kernel when the vectorised
 // path does not apply.  Returns the launch error.

@@ -133,15 +133,22 @@ mm_status mm_gemm_f32_ex(int transA, int transB, int64_t M, int64_t N, int64_t K
 enum {
     MM_DEQ_AUTO = 0,
     MM_DEQ_SELECT = 1,   /* any codebook: per-field select of the entry, fp32 FMA */
-    MM_DEQ_AFFINE = 2    /* codebook[c] = c0 + c*d exactly (and no zero entry at field 3):
+    MM_DEQ_AFFINE = 2,   /* codebook[c] = c0 + c*d exactly (and no zero entry at field 3):
                             fields used in place as exact fp32 subnormals in packed f32x2
                             FMAs, y = scale * (c0 * sum x + d * sum c x) */
+    MM_DEQ_MMA = 3       /* same affine condition, cols % 256 == 0: two fields per integer
+                            op become an fp16x2 of exact subnormals and the multiply-adds run
+                            as tensor-core mma.sync (fp16 in, fp32 accumulate) */
 };
 
 typedef struct {
-    int split;           /* lanes sharing one row's dot product: 0 (auto), 4, 8, 16 */
-    int rows_per_lane;   /* rows each lane carries: 0 (auto), 1, 2, 4 */
-    int warps;           /* warps per CTA: 0 (auto), 1..16 */
+    int split;           /* SIMT decodes: lanes sharing one row's dot product (4, 8, 16);
+                            MM_DEQ_MMA: warps sharing one row's dot product (1, 2, 3, 4, 6);
+                            0 = automatic */
+    int rows_per_lane;   /* SIMT decodes: rows each lane carries (1, 2, 4);
+                            MM_DEQ_MMA: 16-row blocks each warp carries (1, 2, 4); 0 = automatic */
+    int warps;           /* warps per CTA: 0 (auto), 1..16 (MM_DEQ_MMA: a multiple of split,
+                            at most 8 when rows_per_lane is 2 or 4) */
     int dequant;         /* MM_DEQ_* */
     int pdl;             /* 1: launch with programmatic dependent launch so the
                             kernel's prologue overlaps the previous kernel; it
@@ -149,7 +156,11 @@ typedef struct {
     int weights_static;  /* 1: promise that codes and scales are not written by
                             work queued before this call, so their loads may start
                             before the wait on the previous kernel (needs pdl) */
-    int reserved[6];
+    int independent;     /* 1: promise that no work queued before this call writes
+                            codes, scales or x, or reads y: the kernel then never
+                            waits for the previous kernel (needs pdl), so back-to-back
+                            calls over different matrices overlap completely */
+    int reserved[5];
 } mm_gemv_opts;
 
 mm_status mm_gemv_packed2_ex(const uint8_t *codes, const uint16_t *scales, const uint16_t *x,

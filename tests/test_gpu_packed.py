@@ -69,9 +69,17 @@ VARIANTS = [dict(split=s, rows_per_lane=r, warps=w, dequant=d, pdl=p, weights_st
             for (p, ws) in ((0, 0), (1, 1))]
 
 
-@pytest.mark.parametrize("v", VARIANTS, ids=lambda v: "s{split}r{rows_per_lane}w{warps}d{dequant}p{pdl}".format(**v))
+MMA_VARIANTS = [dict(split=k, rows_per_lane=r, warps=k * m, dequant=3, pdl=p, weights_static=ws, independent=ind)
+                for k in (1, 2, 3, 4, 6) for r in (1, 2, 4) for m in (1, 2) if k * m <= (8 if r >= 2 else 16)
+                for (p, ws, ind) in ((0, 0, 0), (1, 1, 0), (1, 0, 1))]
+
+
+@pytest.mark.parametrize("v", VARIANTS + MMA_VARIANTS,
+                         ids=lambda v: "s{split}r{rows_per_lane}w{warps}d{dequant}p{pdl}".format(**v)
+                         + ("i" if v.get("independent") else ""))
 def test_gemv_variant_matrix(oracle, v):
-    rows, cols = 1000, 1536 + 256   # ragged row count; 28 chunks per row (not a multiple of S * CPL)
+    # ragged row count; 28 chunks = 7 slabs per row (not a multiple of the split widths)
+    rows, cols = 1000, 1536 + 256
     codes, scales, x = rand_case(rows, cols, seed=101)
     y = gemv(codes, scales, x, rows, cols, CB2, **v)
     ref, T = oracle.packed_gemm(codes, scales, x, rows, cols, CB2)
@@ -100,8 +108,8 @@ def test_gemv_ignores_fields_past_cols(oracle, cols):
     assert np.array_equal(y_clean, y_dirty)
 
 
-@pytest.mark.parametrize("dequant", [1, 2])
-@pytest.mark.parametrize("cols", [64, 1536, 100])
+@pytest.mark.parametrize("dequant", [1, 2, 3])
+@pytest.mark.parametrize("cols", [64, 256, 1536, 100])
 def test_gemv_one_hot_decodes_exactly(oracle, dequant, cols):
     # x = e_k: every y_r must be exactly fp32(scale_r * cb[field(r, k)])
     rows = 257
@@ -113,7 +121,7 @@ def test_gemv_one_hot_decodes_exactly(oracle, dequant, cols):
             continue
         x = np.zeros(cols, np.uint16)
         x[k] = 0x3C00
-        opts = dict(dequant=dequant) if cols % 64 == 0 else {}
+        opts = dict(dequant=dequant) if cols % (256 if dequant == 3 else 64) == 0 else {}
         y = gemv(codes, scales, x, rows, cols, CB2, **opts)
         ref, _ = oracle.packed_gemm(codes, scales, x, rows, cols, CB2)
         check_exact(y, ref[0], f"k={k}")
@@ -121,7 +129,7 @@ def test_gemv_one_hot_decodes_exactly(oracle, dequant, cols):
         assert np.array_equal(y.astype(np.float64), s * CB2[fields[:, k]].astype(np.float64))
 
 
-@pytest.mark.parametrize("dequant", [1, 2])
+@pytest.mark.parametrize("dequant", [1, 2, 3])
 def test_gemv_integer_activations_bit_exact(oracle, dequant):
     rows, cols = 500, 1536
     codes, _, _ = rand_case(rows, cols, seed=77)
@@ -131,6 +139,21 @@ def test_gemv_integer_activations_bit_exact(oracle, dequant):
     y = gemv(codes, scales, x, rows, cols, CB2, dequant=dequant)
     ref, _ = oracle.packed_gemm(codes, scales, x, rows, cols, CB2)
     check_exact(y, ref[0], "integer x")
+
+
+@pytest.mark.parametrize("dequant", [1, 2, 3])
+def test_gemv_tiny_activations_exact(oracle, dequant):
+    # one-hot with fp16 subnormal and smallest-normal activations: products far below
+    # 1 must still be exact
+    rows, cols = 64, 256
+    codes, scales, _ = rand_case(rows, cols, seed=91)
+    for bits in (0x0001, 0x0003, 0x03FF, 0x0400, 0x8001):
+        for k in (0, 9, 130, 255):
+            x = np.zeros(cols, np.uint16)
+            x[k] = bits
+            y = gemv(codes, scales, x, rows, cols, CB2, dequant=dequant)
+            ref, _ = oracle.packed_gemm(codes, scales, x, rows, cols, CB2)
+            check_exact(y, ref[0], f"x[{k}]={bits:#06x}")
 
 
 def test_gemv_deterministic():
@@ -146,9 +169,15 @@ def test_gemv_zero_bound_rows_are_zero(oracle):
     codes = np.full((rows, cols // 4), 0xAA, np.uint8)
     scales = synth.uniform_f16_bits(9, (rows,), 0.005, 0.05)
     x = synth.normal_f16_bits(10, (cols,))
-    for d in (1, 2):
+    for d in (1, 2, 3):
         y = gemv(codes, scales, x, rows, cols, CB2, dequant=d)
-        assert np.all(y == 0.0)
+        assert np.all(y == 0.0), d
+    # zero entry at field 1 or 0 cancels exactly too
+    for cb, byte in ((np.array([-1, 0, 1, 2], np.float32), 0x55), (np.array([0, 0.5, 1, 1.5], np.float32), 0x00)):
+        codes = np.full((rows, cols // 4), byte, np.uint8)
+        for d in (1, 2, 3):
+            y = gemv(codes, scales, x, rows, cols, cb, dequant=d)
+            assert np.all(y == 0.0), (cb, d)
 
 
 # ------------------------------------------------------------------ skinny GEMM
