@@ -205,11 +205,18 @@ mm_status mm_gemm_packed2_ex(const uint8_t *codes, const uint16_t *scales, const
                              const mm_gemm_packed2_opts *opts) {
     mm_status s = check_packed(codes, scales, X, Y, M, rows, cols, codebook);
     if (s != MM_OK) return s;
-    if (opts && opts->tile < 0) return fail(MM_ERR_INVALID_ARG, "unknown tile %d", opts->tile);
+    const int tile = opts ? opts->tile : 0;
+    if (tile != 0 && tile != 1 && tile != 32 && tile != 64 && tile != 128)
+        return fail(MM_ERR_INVALID_ARG, "tile must be 0 (auto), 1 (FFMA), 32, 64 or 128 (tensor cores)");
+    mm::PackedArgs a{codes, scales, X, Y, M, rows, cols, {codebook[0], codebook[1], codebook[2], codebook[3]}};
+    const bool tc_ok = mm::gemm_packed2_tc_supported(a);
+    if (tile >= 32 && !tc_ok)
+        return fail(MM_ERR_INVALID_ARG, "tensor-core tile needs fp16-exact codebook entries, cols %% 8 == 0 and 16-byte aligned X");
     s = check_device();
     if (s != MM_OK) return s;
-    mm::PackedArgs a{codes, scales, X, Y, M, rows, cols, {codebook[0], codebook[1], codebook[2], codebook[3]}};
-    cudaError_t e = mm::launch_gemm_packed2(a, opts ? opts->tile : 0, reinterpret_cast<cudaStream_t>(stream));
+    cudaError_t e;
+    if (tc_ok && tile != 1) e = mm::launch_gemm_packed2_tc(a, tile, reinterpret_cast<cudaStream_t>(stream));
+    else e = mm::launch_gemm_packed2(a, 0, reinterpret_cast<cudaStream_t>(stream));
     if (e != cudaSuccess) return cuda_fail(e, "packed gemm launch");
     return ok();
 }
@@ -224,6 +231,9 @@ mm_status mm_check_device_error(mm_stream_t stream) {
     const unsigned int v = mm::gemm_ffma_take_device_error(reinterpret_cast<cudaStream_t>(stream), &e);
     if (e != cudaSuccess) return cuda_fail(e, "mm_check_device_error");
     if (v != 0) return fail(MM_ERR_TIMEOUT, "a bounded device wait ran out in the FFMA GEMM (code %u)", v);
+    const unsigned int w = mm::gemm_packed2_tc_take_device_error(&e);
+    if (e != cudaSuccess) return cuda_fail(e, "mm_check_device_error");
+    if (w != 0) return fail(MM_ERR_TIMEOUT, "a bounded device wait ran out in the tensor-core packed GEMM (code %u)", w);
     return ok();
 }
 

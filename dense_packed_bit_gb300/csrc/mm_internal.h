@@ -43,8 +43,14 @@ cudaError_t launch_gemv_mma(const PackedArgs &a, const GemvConfig &cfg, cudaStre
 // path does not apply.  Returns the launch error.
 cudaError_t launch_gemv_packed2(const PackedArgs &a, const GemvConfig &cfg, cudaStream_t s);
 
-// Skinny packed GEMM (M >= 1).
+// Skinny packed GEMM (M >= 1), FFMA on shared-memory tiles: any shape, any codebook.
 cudaError_t launch_gemm_packed2(const PackedArgs &a, int tile, cudaStream_t s);
+
+// Skinny packed GEMM on tcgen05 tensor cores: codebook entries exact in fp16,
+// cols % 8 == 0, 16-byte aligned X.  tile = W rows per CTA (32, 64, 128) or 0.
+bool gemm_packed2_tc_supported(const PackedArgs &a);
+cudaError_t launch_gemm_packed2_tc(const PackedArgs &a, int tile, cudaStream_t s);
+unsigned int gemm_packed2_tc_take_device_error(cudaError_t *err);
 
 // ------------------------------------------------------------------ dense GEMM
 

@@ -168,7 +168,10 @@ mm_status mm_gemv_packed2_ex(const uint8_t *codes, const uint16_t *scales, const
                              mm_stream_t stream, const mm_gemv_opts *opts);
 
 typedef struct {
-    int tile;       /* 0 = automatic, else a tile id */
+    int tile;       /* 0 = automatic (tensor cores when the codebook entries are exact in
+                       fp16, cols % 8 == 0 and X is 16-byte aligned; FFMA otherwise),
+                       1 = FFMA kernel, 32 / 64 / 128 = tensor cores with that many W rows
+                       per CTA */
     int reserved[7];
 } mm_gemm_packed2_opts;
 

@@ -137,12 +137,26 @@ def test_python_binding_raises_with_message(lib):
 
 
 def test_missing_library_fails_loudly(monkeypatch):
-    import importlib
+    # a separate copy of the binding module, so the loaded library stays untouched
+    import importlib.util
+    spec = importlib.util.spec_from_file_location("mm_binding_copy", mm.__file__)
+    mod = importlib.util.module_from_spec(spec)
+    spec.loader.exec_module(mod)
     monkeypatch.setenv("MM_LIBRARY", "/nonexistent/libmm.so")
-    mod = importlib.reload(mm)
-    try:
-        with pytest.raises(mm.MMError):
-            mod.load_library()
-    finally:
-        monkeypatch.delenv("MM_LIBRARY")
-        importlib.reload(mm)
+    with pytest.raises(mod.MMError):
+        mod.load_library()
+
+
+@pytest.mark.parametrize("tile", [-1, 2, 48, 256])
+def test_gemm_packed_bad_tile(lib, tile):
+    o = mm.GemmPacked2Opts(tile)
+    st = lib.mm_gemm_packed2_ex(FAKE, FAKE + 0x100000, FAKE + 0x200000, FAKE + 0x300000, 4, 64, 64,
+                                _cb(-1, 0, 1, 0), None, ctypes.byref(o))
+    assert st == mm.MM_ERR_INVALID_ARG
+
+
+def test_gemm_packed_tensor_core_tile_needs_fp16_codebook(lib):
+    o = mm.GemmPacked2Opts(64)
+    st = lib.mm_gemm_packed2_ex(FAKE, FAKE + 0x100000, FAKE + 0x200000, FAKE + 0x300000, 4, 64, 64,
+                                _cb(0.3, -1.7, 2.5, 0.01), None, ctypes.byref(o))
+    assert st == mm.MM_ERR_INVALID_ARG and b"fp16" in lib.mm_last_error()

@@ -36,10 +36,14 @@ def gemv(codes, scales, x, rows, cols, cb, **opts):
     return to_host(dy)
 
 
-def gemm_packed(codes, scales, X, M, rows, cols, cb):
+def gemm_packed(codes, scales, X, M, rows, cols, cb, tile=None):
     dc, ds, dX = to_dev(codes), to_dev(scales), to_dev(X)
     dY = empty_f32((M, rows))
-    mm.mm_gemm_packed2(dc, ds, dX, dY, M, rows, cols, cb)
+    if tile is None:
+        mm.mm_gemm_packed2(dc, ds, dX, dY, M, rows, cols, cb)
+    else:
+        mm.mm_gemm_packed2_ex(dc, ds, dX, dY, M, rows, cols, cb, tile=tile)
+    mm.mm_check_device_error()
     return to_host(dY)
 
 
@@ -226,3 +230,39 @@ def test_gemm_packed_matches_gemv_rows(oracle):
     ref, T = oracle.packed_gemm(c.codes, c.scales, c.X, c.rows, c.cols, c.codebook)
     check_bound(y, ref[0], T[0], "gemv")
     check_bound(Y[0], ref[0], T[0], "gemm M=1")
+
+
+@pytest.mark.parametrize("tile", [1, 32, 64, 128])
+@pytest.mark.parametrize("M,rows,cols", [(1, 1, 8), (3, 33, 24), (129, 130, 136), (222, 256, 768),
+                                         (300, 65, 1536), (17, 3072, 64)])
+@pytest.mark.parametrize("cb", ["ternary", "2bit"])
+def test_gemm_packed_tile_matrix(oracle, tile, M, rows, cols, cb):
+    # tensor-core tiles (32/64/128 W rows per CTA) and the FFMA kernel (tile 1); cols not a
+    # multiple of 64 exercise the bytewise code loads and the zero-filled K tail
+    codebook = CBT if cb == "ternary" else CB2
+    codes, scales, X = rand_case(rows, cols, M=M, seed=7 * M + rows + 3 * cols,
+                                 kind="ternary" if cb == "ternary" else "uniform2")
+    Y = gemm_packed(codes, scales, X, M, rows, cols, codebook, tile=tile)
+    ref, T = oracle.packed_gemm(codes, scales, X, rows, cols, codebook)
+    check_bound(Y, ref, T, f"tile {tile} {M}x{rows}x{cols}")
+
+
+@pytest.mark.parametrize("tile", [32, 128])
+def test_gemm_packed_tensor_core_integer_exact(oracle, tile):
+    # integer activations and scale 1: every partial sum is a small integer, so exact
+    M, rows, cols = 150, 200, 512
+    codes, _, _ = rand_case(rows, cols, M=M, seed=5)
+    scales = np.full(rows, 0x3C00, np.uint16)
+    rng = np.random.default_rng(8)
+    X = rng.integers(-4, 5, size=(M, cols)).astype(np.float16).view(np.uint16)
+    Y = gemm_packed(codes, scales, X, M, rows, cols, CB2, tile=tile)
+    ref, _ = oracle.packed_gemm(codes, scales, X, rows, cols, CB2)
+    check_exact(Y, ref, f"tile {tile}")
+
+
+def test_gemm_packed_tensor_core_deterministic():
+    c = synth.ternary_encoder_layer(2, "down")
+    M = c.X.shape[0]
+    y1 = gemm_packed(c.codes, c.scales, c.X, M, c.rows, c.cols, c.codebook)
+    y2 = gemm_packed(c.codes, c.scales, c.X, M, c.rows, c.cols, c.codebook)
+    assert np.array_equal(y1.view(np.uint32), y2.view(np.uint32))
