@@ -464,11 +464,15 @@ def main_mm(args):
     sms = props.multi_processor_count
     fp32_peak_max = fp32_simt_peak_tflops(sms, peaks.get("sm_max_mhz", 2070.0))
     gemm_per_gpu = 3 * GEMM_FLOP * args.steps / gemm_total_s / 1e12
-    if args.gemm_path == mm.MM_GEMM_TF32X3:
+    if args.gemm_path in (mm.MM_GEMM_AUTO, mm.MM_GEMM_TF32X3):
+        # three tf32 MMAs per fp32 multiply-add: the fp32-equivalent tensor peak is a third of tf32's
         tf32_peak = peaks["bf16_tflops"] * (1.1 / 2.25)
         roof = {"bound": "tensor", "achieved": gemm_per_gpu, "peak": tf32_peak / 3.0, "unit": "TFLOP/s",
                 "frac": gemm_per_gpu / (tf32_peak / 3.0), "traffic": traffic_for("gemm_tf32x3"),
-                "kernel": "gemm_tf32x3", "peak_source": f"{peaks_src} bf16 x nominal tf32/bf16 ratio / 3 MMAs"}
+                "kernel": "gemm_tf32x3_kernel",
+                "peak_source": (f"{peaks_src} bf16 burst {peaks['bf16_tflops']:.0f} TFLOP/s x nominal tf32/bf16 "
+                                f"ratio 1.1/2.25, divided by the 3 MMAs of the split"),
+                "frac_of_fp32_simt_peak": gemm_per_gpu / fp32_peak_max}
     else:
         roof = {"bound": "alu", "achieved": gemm_per_gpu, "peak": fp32_peak_max, "unit": "TFLOP/s",
                 "frac": gemm_per_gpu / fp32_peak_max, "traffic": traffic_for("gemm_ffma"),

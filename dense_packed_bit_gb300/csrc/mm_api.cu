@@ -129,8 +129,11 @@ mm_status mm_gemm_f32_ex(int transA, int transB, int64_t M, int64_t N, int64_t K
     mm::GemmArgs g{transA, transB, M, N, K, A, lda, B, ldb, C, ldc};
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
     cudaError_t e;
-    if (path == MM_GEMM_TF32X3) return fail(MM_ERR_UNSUPPORTED, "3xTF32 path not available in this build");
-    if (mm::gemm_ffma_supported(g)) e = mm::launch_gemm_ffma(g, opts ? opts->tile : 0, st);
+    if (path == MM_GEMM_TF32X3 && !mm::gemm_tf32x3_supported(g))
+        return fail(MM_ERR_INVALID_ARG, "3xTF32 path needs 16-byte aligned A, B and lda, ldb multiples of 4");
+    if ((path == MM_GEMM_TF32X3 || path == MM_GEMM_AUTO) && mm::gemm_tf32x3_supported(g))
+        e = mm::launch_gemm_tf32x3(g, st);
+    else if (mm::gemm_ffma_supported(g)) e = mm::launch_gemm_ffma(g, opts ? opts->tile : 0, st);
     else if (path == MM_GEMM_FFMA || path == MM_GEMM_AUTO) e = mm::launch_gemm_simple(g, st);
     else e = cudaErrorNotSupported;
     if (e != cudaSuccess) return cuda_fail(e, "gemm launch");
@@ -234,6 +237,9 @@ mm_status mm_check_device_error(mm_stream_t stream) {
     const unsigned int w = mm::gemm_packed2_tc_take_device_error(&e);
     if (e != cudaSuccess) return cuda_fail(e, "mm_check_device_error");
     if (w != 0) return fail(MM_ERR_TIMEOUT, "a bounded device wait ran out in the tensor-core packed GEMM (code %u)", w);
+    const unsigned int z = mm::gemm_tf32x3_take_device_error(&e);
+    if (e != cudaSuccess) return cuda_fail(e, "mm_check_device_error");
+    if (z != 0) return fail(MM_ERR_TIMEOUT, "a bounded device wait ran out in the 3xTF32 GEMM (code %u)", z);
     return ok();
 }
 

@@ -115,9 +115,12 @@ mm_status mm_check_device_error(mm_stream_t stream);
  * ------------------------------------------------------------------------ */
 
 enum {
-    MM_GEMM_AUTO = 0,
-    MM_GEMM_FFMA = 1,    /* TMA-staged, register-blocked fp32 FFMA */
-    MM_GEMM_TF32X3 = 2   /* 3xTF32 split on tcgen05 tensor cores, TMEM accumulators */
+    MM_GEMM_AUTO = 0,    /* 3xTF32 when A, B are 16-byte aligned and lda, ldb are multiples
+                            of 4; the plain tiled FFMA kernel otherwise */
+    MM_GEMM_FFMA = 1,    /* TMA-staged, register-blocked fp32 FFMA (plain tiled FFMA kernel
+                            when the operands cannot be described by TMA) */
+    MM_GEMM_TF32X3 = 2   /* fp32 by the three-term tf32 split (hi*hi + hi*lo + lo*hi) on the
+                            tcgen05 tensor cores, TMEM accumulators; same operand rules as AUTO */
 };
 
 typedef struct {

@@ -48,15 +48,37 @@ def stored(tA, tB, M, N, K, seed, kind="normal"):
 SHAPES = [(1, 1, 1), (3, 17, 5), (65, 129, 33), (127, 63, 129), (200, 300, 97), (257, 130, 1000)]
 
 
+PATHS = {"auto": mm.MM_GEMM_AUTO, "ffma": mm.MM_GEMM_FFMA, "tf32x3": mm.MM_GEMM_TF32X3}
+
+
+@pytest.mark.parametrize("path", list(PATHS))
 @pytest.mark.parametrize("layout", list(LAYOUTS))
 @pytest.mark.parametrize("shape", SHAPES)
-def test_gemm_ragged_shapes(oracle, layout, shape):
+def test_gemm_ragged_shapes(oracle, layout, shape, path):
     tA, tB = LAYOUTS[layout]
     M, N, K = shape
     A, B = stored(tA, tB, M, N, K, seed=1000 * list(LAYOUTS).index(layout) + 7 * M + 3 * N + K)
-    C = run(tA, tB, M, N, K, A, B)
+    if path == "tf32x3" and (A.shape[1] % 4 or B.shape[1] % 4):
+        pytest.skip("3xTF32 path needs leading dimensions that are multiples of 4")
+    C = run(tA, tB, M, N, K, A, B, path=PATHS[path])
     ref, T = oracle.gemm(tA, tB, M, N, K, A, B)
-    check_bound(C, ref, T, f"{layout} {shape}")
+    check_bound(C, ref, T, f"{layout} {shape} {path}")
+
+
+@pytest.mark.parametrize("layout", list(LAYOUTS))
+@pytest.mark.parametrize("shape", [(128, 128, 32), (256, 384, 64), (130, 260, 100), (384, 128, 1000),
+                                   (64, 3072, 768)])
+def test_gemm_tf32x3_tiles(oracle, layout, shape):
+    # whole tiles, ragged tiles and K tails on the tensor-core path
+    tA, tB = LAYOUTS[layout]
+    M, N, K = shape
+    A, B = stored(tA, tB, M, N, K, seed=17 + M + N + K)
+    Ap = np.zeros((A.shape[0], (A.shape[1] + 3) // 4 * 4), np.float32); Ap[:, :A.shape[1]] = A
+    Bp = np.zeros((B.shape[0], (B.shape[1] + 3) // 4 * 4), np.float32); Bp[:, :B.shape[1]] = B
+    C = run(tA, tB, M, N, K, Ap, Bp, lda=Ap.shape[1], ldb=Bp.shape[1], path=mm.MM_GEMM_TF32X3)
+    ref, T = oracle.gemm(tA, tB, M, N, K, A, B)
+    worst = check_bound(C, ref, T, f"{layout} {shape}")
+    print(f"tf32x3 {layout} {shape}: worst |err|/T = {worst:.3e}")
 
 
 @pytest.mark.parametrize("layout", list(LAYOUTS))
@@ -92,10 +114,12 @@ def test_gemm_padded_ld_tma_path_and_canary(oracle, layout):
 def test_gemm_small_integers_bit_exact(oracle, layout):
     # every partial sum is an integer below 2^24, so any summation order is exact
     tA, tB = LAYOUTS[layout]
-    M, N, K = 300, 270, 513
+    M, N, K = 300, 272, 516
     A, B = stored(tA, tB, M, N, K, seed=31, kind="int")
     ref, _ = oracle.gemm(tA, tB, M, N, K, A, B)
-    for path in (mm.MM_GEMM_AUTO, mm.MM_GEMM_FFMA):
+    for path in (mm.MM_GEMM_AUTO, mm.MM_GEMM_FFMA, mm.MM_GEMM_TF32X3):
+        if path == mm.MM_GEMM_TF32X3 and (A.shape[1] % 4 or B.shape[1] % 4):
+            continue
         check_exact(run(tA, tB, M, N, K, A, B, path=path), ref, f"{layout} path {path}")
 
 
@@ -105,14 +129,25 @@ def test_gemm_all_ones_is_K():
     assert np.all(C == K)
 
 
+@pytest.mark.parametrize("path", ["ffma", "tf32x3"])
 @pytest.mark.parametrize("layout", ["nn", "nt", "tn"])
-def test_gemm_deterministic(layout):
+def test_gemm_deterministic(layout, path):
     tA, tB = LAYOUTS[layout]
-    M, N, K = 333, 444, 555
+    M, N, K = 332, 444, 556
     A, B = stored(tA, tB, M, N, K, seed=41)
-    c1 = run(tA, tB, M, N, K, A, B)
-    c2 = run(tA, tB, M, N, K, A, B)
+    c1 = run(tA, tB, M, N, K, A, B, path=PATHS[path])
+    c2 = run(tA, tB, M, N, K, A, B, path=PATHS[path])
     assert np.array_equal(c1.view(np.uint32), c2.view(np.uint32))
+
+
+def test_gemm_tf32x3_all_ones_and_identity():
+    M = N = K = 256
+    C = run(0, 0, M, N, K, np.ones((M, K), np.float32), np.ones((K, N), np.float32), path=mm.MM_GEMM_TF32X3)
+    assert np.all(C == K)
+    X = synth.normal_f32(3, (M, K), 1.0)
+    C = run(0, 0, M, N, K, X, np.eye(K, dtype=np.float32), path=mm.MM_GEMM_TF32X3)
+    # x = hi + lo with lo's tf32 rounding dropped: relative error below 2^-21
+    assert np.all(np.abs(C - X) <= 2.0 ** -20 * np.abs(X))
 
 
 def test_gpt2_mlp_up_64x768x3072_all_outputs(oracle):
@@ -122,19 +157,21 @@ def test_gpt2_mlp_up_64x768x3072_all_outputs(oracle):
     check_bound(C, ref, T, c.name)
 
 
+@pytest.mark.parametrize("path", ["ffma", "tf32x3"])
 @pytest.mark.parametrize("layout", ["nn", "nt", "tn"])
-def test_square_2048_all_outputs(oracle, layout):
+def test_square_2048_all_outputs(oracle, layout, path):
     c = synth.square_2048(layout)
-    C = run(c.transA, c.transB, c.M, c.N, c.K, c.A, c.B)
+    C = run(c.transA, c.transB, c.M, c.N, c.K, c.A, c.B, path=PATHS[path])
     ref, T = oracle.gemm(c.transA, c.transB, c.M, c.N, c.K, c.A, c.B)
     worst = check_bound(C, ref, T, c.name)
-    print(f"{c.name}: worst |err|/T = {worst:.3e}")
+    print(f"{c.name} {path}: worst |err|/T = {worst:.3e}")
 
 
+@pytest.mark.parametrize("path", ["ffma", "tf32x3"])
 @pytest.mark.parametrize("which", ["fwd", "dA", "dB"])
-def test_training_set_sampled(oracle, which):
+def test_training_set_sampled(oracle, which, path):
     c = synth.training_set_8192(which)
-    C = run(c.transA, c.transB, c.M, c.N, c.K, c.A, c.B)
+    C = run(c.transA, c.transB, c.M, c.N, c.K, c.A, c.B, path=PATHS[path])
     rng = np.random.default_rng(7)
     rows = [0, c.M - 1, int(rng.integers(c.M))]
     cols = [0, c.N - 1, int(rng.integers(c.N))]
