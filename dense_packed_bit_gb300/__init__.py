@@ -45,7 +45,7 @@ class GemvOpts(ctypes.Structure):
 
 
 class GemmPacked2Opts(ctypes.Structure):
-    _fields_ = [("tile", ctypes.c_int), ("reserved", ctypes.c_int * 7)]
+    _fields_ = [("tile", ctypes.c_int), ("splitk", ctypes.c_int), ("reserved", ctypes.c_int * 6)]
 
 
 SIGNATURES = {
@@ -159,8 +159,8 @@ def mm_gemm_packed2(codes, scales, X, Y, M, rows, cols, codebook, stream=None):
                                           _codebook(codebook), _stream(stream)))
 
 
-def mm_gemm_packed2_ex(codes, scales, X, Y, M, rows, cols, codebook, stream=None, *, tile=0):
-    o = GemmPacked2Opts(tile)
+def mm_gemm_packed2_ex(codes, scales, X, Y, M, rows, cols, codebook, stream=None, *, tile=0, splitk=0):
+    o = GemmPacked2Opts(tile, splitk)
     _check(load_library().mm_gemm_packed2_ex(_ptr(codes), _ptr(scales), _ptr(X), _ptr(Y), M, rows, cols,
                                              _codebook(codebook), _stream(stream), ctypes.byref(o)))
 

@@ -209,8 +209,11 @@ mm_status mm_gemm_packed2_ex(const uint8_t *codes, const uint16_t *scales, const
     mm_status s = check_packed(codes, scales, X, Y, M, rows, cols, codebook);
     if (s != MM_OK) return s;
     const int tile = opts ? opts->tile : 0;
+    const int splitk = opts ? opts->splitk : 0;
     if (tile != 0 && tile != 1 && tile != 32 && tile != 64 && tile != 128)
         return fail(MM_ERR_INVALID_ARG, "tile must be 0 (auto), 1 (FFMA), 32, 64 or 128 (tensor cores)");
+    if (splitk != 0 && splitk != 1 && splitk != 2 && splitk != 4 && splitk != 8)
+        return fail(MM_ERR_INVALID_ARG, "splitk must be 0 (auto), 1, 2, 4 or 8");
     mm::PackedArgs a{codes, scales, X, Y, M, rows, cols, {codebook[0], codebook[1], codebook[2], codebook[3]}};
     const bool tc_ok = mm::gemm_packed2_tc_supported(a);
     if (tile >= 32 && !tc_ok)
@@ -218,7 +221,7 @@ mm_status mm_gemm_packed2_ex(const uint8_t *codes, const uint16_t *scales, const
     s = check_device();
     if (s != MM_OK) return s;
     cudaError_t e;
-    if (tc_ok && tile != 1) e = mm::launch_gemm_packed2_tc(a, tile, reinterpret_cast<cudaStream_t>(stream));
+    if (tc_ok && tile != 1) e = mm::launch_gemm_packed2_tc(a, tile, splitk, reinterpret_cast<cudaStream_t>(stream));
     else e = mm::launch_gemm_packed2(a, 0, reinterpret_cast<cudaStream_t>(stream));
     if (e != cudaSuccess) return cuda_fail(e, "packed gemm launch");
     return ok();

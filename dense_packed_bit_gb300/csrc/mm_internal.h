@@ -47,9 +47,10 @@ cudaError_t launch_gemv_packed2(const PackedArgs &a, const GemvConfig &cfg, cuda
 cudaError_t launch_gemm_packed2(const PackedArgs &a, int tile, cudaStream_t s);
 
 // Skinny packed GEMM on tcgen05 tensor cores: codebook entries exact in fp16,
-// cols % 8 == 0, 16-byte aligned X.  tile = W rows per CTA (32, 64, 128) or 0.
+// cols % 8 == 0, 16-byte aligned X.  tile = W rows per CTA (32, 64, 128) or 0;
+// splitk = CTAs of a cluster sharing K (1, 2, 4, 8) or 0 for automatic.
 bool gemm_packed2_tc_supported(const PackedArgs &a);
-cudaError_t launch_gemm_packed2_tc(const PackedArgs &a, int tile, cudaStream_t s);
+cudaError_t launch_gemm_packed2_tc(const PackedArgs &a, int tile, int splitk, cudaStream_t s);
 unsigned int gemm_packed2_tc_take_device_error(cudaError_t *err);
 
 // ------------------------------------------------------------------ dense GEMM

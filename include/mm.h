@@ -175,7 +175,10 @@ typedef struct {
                        fp16, cols % 8 == 0 and X is 16-byte aligned; FFMA otherwise),
                        1 = FFMA kernel, 32 / 64 / 128 = tensor cores with that many W rows
                        per CTA */
-    int reserved[7];
+    int splitk;     /* tensor cores: CTAs of one thread-block cluster that split K and add
+                       their partial tiles through distributed shared memory in rank
+                       order: 0 (auto), 1, 2, 4, 8 */
+    int reserved[6];
 } mm_gemm_packed2_opts;
 
 mm_status mm_gemm_packed2_ex(const uint8_t *codes, const uint16_t *scales, const uint16_t *X,

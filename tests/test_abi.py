@@ -160,3 +160,11 @@ def test_gemm_packed_tensor_core_tile_needs_fp16_codebook(lib):
     st = lib.mm_gemm_packed2_ex(FAKE, FAKE + 0x100000, FAKE + 0x200000, FAKE + 0x300000, 4, 64, 64,
                                 _cb(0.3, -1.7, 2.5, 0.01), None, ctypes.byref(o))
     assert st == mm.MM_ERR_INVALID_ARG and b"fp16" in lib.mm_last_error()
+
+
+@pytest.mark.parametrize("splitk", [-1, 3, 16])
+def test_gemm_packed_bad_splitk(lib, splitk):
+    o = mm.GemmPacked2Opts(0, splitk)
+    st = lib.mm_gemm_packed2_ex(FAKE, FAKE + 0x100000, FAKE + 0x200000, FAKE + 0x300000, 4, 64, 64,
+                                _cb(-1, 0, 1, 0), None, ctypes.byref(o))
+    assert st == mm.MM_ERR_INVALID_ARG

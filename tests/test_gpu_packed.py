@@ -36,13 +36,13 @@ def gemv(codes, scales, x, rows, cols, cb, **opts):
     return to_host(dy)
 
 
-def gemm_packed(codes, scales, X, M, rows, cols, cb, tile=None):
+def gemm_packed(codes, scales, X, M, rows, cols, cb, tile=None, splitk=0):
     dc, ds, dX = to_dev(codes), to_dev(scales), to_dev(X)
     dY = empty_f32((M, rows))
-    if tile is None:
+    if tile is None and not splitk:
         mm.mm_gemm_packed2(dc, ds, dX, dY, M, rows, cols, cb)
     else:
-        mm.mm_gemm_packed2_ex(dc, ds, dX, dY, M, rows, cols, cb, tile=tile)
+        mm.mm_gemm_packed2_ex(dc, ds, dX, dY, M, rows, cols, cb, tile=tile or 0, splitk=splitk)
     mm.mm_check_device_error()
     return to_host(dY)
 
@@ -266,3 +266,15 @@ def test_gemm_packed_tensor_core_deterministic():
     y1 = gemm_packed(c.codes, c.scales, c.X, M, c.rows, c.cols, c.codebook)
     y2 = gemm_packed(c.codes, c.scales, c.X, M, c.rows, c.cols, c.codebook)
     assert np.array_equal(y1.view(np.uint32), y2.view(np.uint32))
+
+
+@pytest.mark.parametrize("splitk", [1, 2, 4, 8])
+@pytest.mark.parametrize("tile", [32, 64, 128])
+@pytest.mark.parametrize("M,rows,cols", [(222, 768, 3072), (5, 40, 640), (130, 200, 1000)])
+def test_gemm_packed_cluster_splitk(oracle, splitk, tile, M, rows, cols):
+    # K split over a cluster, partial tiles summed through distributed shared memory;
+    # 1000 columns: 16 k-tiles of 64 with a ragged last one, uneven shares for 8 ranks
+    codes, scales, X = rand_case(rows, cols, M=M, seed=splitk * 100 + tile + M, kind="ternary")
+    Y = gemm_packed(codes, scales, X, M, rows, cols, CBT, tile=tile, splitk=splitk)
+    ref, T = oracle.packed_gemm(codes, scales, X, rows, cols, CBT)
+    check_bound(Y, ref, T, f"splitk {splitk} tile {tile}")
