@@ -179,20 +179,18 @@ def fp32_simt_peak_tflops(sms: int, mhz: float) -> float:
 
 def traffic_for(kernel_key: str):
     """DRAM bytes per launch from the committed ncu summary, if it still matches the source."""
-    p = os.path.join(ROOT, "profiles", "traffic.json")
+    p = os.path.join(ROOT, "profiles", "traffic.txt")
     if not os.path.exists(p):
         return None
-    with open(p) as f:
-        d = json.load(f)
-    e = d.get(kernel_key)
-    if not e:
-        return None
-    src = os.path.join(ROOT, e["source"])
-    if not os.path.exists(src):
-        return None
-    if hashlib.sha256(open(src, "rb").read()).hexdigest() != e["source_sha256"]:
-        return None
-    return e["dram_bytes_per_launch"]
+    for line in open(p):
+        parts = line.split()
+        if not parts or parts[0].startswith("#") or parts[0] != kernel_key:
+            continue
+        src = os.path.join(ROOT, parts[1])
+        if not os.path.exists(src) or hashlib.sha256(open(src, "rb").read()).hexdigest() != parts[2]:
+            return None
+        return int(parts[3])
+    return None
 
 
 # ---------------------------------------------------------------- workload

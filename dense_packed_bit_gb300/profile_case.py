@@ -1,7 +1,7 @@
 """Run one hot-path kernel a few times on one workload, for profiler captures.
 
     python -m dense_packed_bit_gb300.profile_case gemm --layout nn --size 2048 --reps 3
-    python -m dense_packed_bit_gb300.profile_case gemv --reps 3 [--split 8 --rows 4 --warps 4]
+    python -m dense_packed_bit_gb300.profile_case gemv --reps 3 [--split 8 --rows 4 --warps 8 --dequant 2 --independent 1]
     python -m dense_packed_bit_gb300.profile_case ternary --reps 1
 
 One warm-up launch precedes the `reps` launches.  No timing is done here:
@@ -25,6 +25,8 @@ def main(argv=None):
     ap.add_argument("--rows", type=int, default=4)
     ap.add_argument("--warps", type=int, default=4)
     ap.add_argument("--pdl", type=int, default=1)
+    ap.add_argument("--dequant", type=int, default=0)
+    ap.add_argument("--independent", type=int, default=0)
     a = ap.parse_args(argv)
 
     import torch
@@ -54,7 +56,8 @@ def main(argv=None):
         for r in range(1 + a.reps):
             i = r % a.matrices
             mm.mm_gemv_packed2_ex(codes[i], scales[i], x, y[i], 12288, 1536, c.codebook, split=a.split,
-                                  rows_per_lane=a.rows, warps=a.warps, pdl=a.pdl, weights_static=a.pdl)
+                                  rows_per_lane=a.rows, warps=a.warps, dequant=a.dequant, pdl=a.pdl,
+                                  weights_static=a.pdl and not a.independent, independent=a.independent)
     else:
         layers = []
         for layer in range(16):
