@@ -41,7 +41,7 @@ class GemmOpts(ctypes.Structure):
 class GemvOpts(ctypes.Structure):
     _fields_ = [("split", ctypes.c_int), ("rows_per_lane", ctypes.c_int), ("warps", ctypes.c_int),
                 ("dequant", ctypes.c_int), ("pdl", ctypes.c_int), ("weights_static", ctypes.c_int),
-                ("independent", ctypes.c_int), ("reserved", ctypes.c_int * 5)]
+                ("independent", ctypes.c_int), ("staging", ctypes.c_int), ("reserved", ctypes.c_int * 4)]
 
 
 class GemmPacked2Opts(ctypes.Structure):
@@ -148,8 +148,8 @@ def mm_gemv_packed2(codes, scales, x, y, rows, cols, codebook, stream=None):
 
 
 def mm_gemv_packed2_ex(codes, scales, x, y, rows, cols, codebook, stream=None, *, split=0,
-                       rows_per_lane=0, warps=0, dequant=0, pdl=0, weights_static=0, independent=0):
-    o = GemvOpts(split, rows_per_lane, warps, dequant, pdl, weights_static, independent)
+                       rows_per_lane=0, warps=0, dequant=0, pdl=0, weights_static=0, independent=0, staging=0):
+    o = GemvOpts(split, rows_per_lane, warps, dequant, pdl, weights_static, independent, staging)
     _check(load_library().mm_gemv_packed2_ex(_ptr(codes), _ptr(scales), _ptr(x), _ptr(y), rows, cols,
                                              _codebook(codebook), _stream(stream), ctypes.byref(o)))
 

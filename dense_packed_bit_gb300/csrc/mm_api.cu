@@ -149,7 +149,7 @@ mm_status mm_gemv_packed2_ex(const uint8_t *codes, const uint16_t *scales, const
                              int64_t cols, const float codebook[4], mm_stream_t stream, const mm_gemv_opts *opts) {
     mm_status s = check_packed(codes, scales, x, y, 1, rows, cols, codebook);
     if (s != MM_OK) return s;
-    mm::GemvConfig cfg{0, 0, 0, 0, 1, 0, 0};
+    mm::GemvConfig cfg{0, 0, 0, 0, 1, 0, 0, -1, 0};
     if (opts) {
         cfg.split = opts->split;
         cfg.rows_per_lane = opts->rows_per_lane;
@@ -158,6 +158,7 @@ mm_status mm_gemv_packed2_ex(const uint8_t *codes, const uint16_t *scales, const
         cfg.pdl = opts->pdl;
         cfg.weights_static = opts->weights_static;
         cfg.independent = opts->independent;
+        cfg.staging = opts->staging;
     }
     const bool affine = mm::codebook_is_affine(codebook);
     mm::PackedArgs a{codes, scales, x, y, 1, rows, cols, {codebook[0], codebook[1], codebook[2], codebook[3]}};
@@ -167,7 +168,19 @@ mm_status mm_gemv_packed2_ex(const uint8_t *codes, const uint16_t *scales, const
         return fail(MM_ERR_INVALID_ARG, "unknown dequant %d", cfg.dequant);
     if ((cfg.dequant == MM_DEQ_AFFINE || cfg.dequant == MM_DEQ_MMA) && !affine)
         return fail(MM_ERR_INVALID_ARG, "affine decode needs codebook[c] == codebook[0] + c*(codebook[1]-codebook[0])");
-    if (cfg.dequant == MM_DEQ_MMA) {
+    if (cfg.staging < 0) cfg.staging = (cfg.dequant == MM_DEQ_MMA && !cfg.split && !cfg.warps &&
+                                        mm::gemv_tma_supported(a)) ? 1 : 0;
+    if (cfg.staging != 0 && cfg.staging != 1) return fail(MM_ERR_INVALID_ARG, "staging must be 0 or 1");
+    if (cfg.staging && (cfg.dequant != MM_DEQ_MMA || !mm::gemv_tma_supported(a)))
+        return fail(MM_ERR_INVALID_ARG, "staging needs the tensor-core decode, cols %% 512 == 0, cols <= 4096 and 16-byte aligned codes and x");
+    if (cfg.dequant == MM_DEQ_MMA && cfg.staging) {
+        // one warp per 256-field slab fixes split and warps; rows_per_lane counts the 64-row
+        // blocks a CTA streams (automatic: 4 for independent calls, 1 otherwise)
+        if (cfg.split || cfg.warps) return fail(MM_ERR_INVALID_ARG, "split and warps are fixed by staging");
+        if (cfg.rows_per_lane < 0 || cfg.rows_per_lane > 64)
+            return fail(MM_ERR_INVALID_ARG, "rows_per_lane (64-row blocks per CTA) must be 0..64 with staging");
+        cfg.blocks_per_cta = cfg.rows_per_lane ? cfg.rows_per_lane : (cfg.independent ? 4 : 1);
+    } else if (cfg.dequant == MM_DEQ_MMA) {
         if (!mm::gemv_mma_supported(a))
             return fail(MM_ERR_INVALID_ARG, "tensor-core decode needs cols %% 256 == 0, cols <= 32768, 16-byte aligned codes and x");
         if (!cfg.split) cfg.split = 3;
@@ -243,6 +256,9 @@ mm_status mm_check_device_error(mm_stream_t stream) {
     const unsigned int z = mm::gemm_tf32x3_take_device_error(&e);
     if (e != cudaSuccess) return cuda_fail(e, "mm_check_device_error");
     if (z != 0) return fail(MM_ERR_TIMEOUT, "a bounded device wait ran out in the 3xTF32 GEMM (code %u)", z);
+    const unsigned int q = mm::gemv_tma_take_device_error(&e);
+    if (e != cudaSuccess) return cuda_fail(e, "mm_check_device_error");
+    if (q != 0) return fail(MM_ERR_TIMEOUT, "a bounded device wait ran out in the staged GEMV (code %u)", q);
     return ok();
 }
 

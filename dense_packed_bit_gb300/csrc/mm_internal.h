@@ -26,6 +26,8 @@ struct GemvConfig {
     int pdl;
     int weights_static;
     int independent;
+    int staging;        // tensor-core decode: 1 = codes brought to shared memory by TMA
+    int blocks_per_cta; // staging: 64-row blocks each CTA streams through its TMA ring
 };
 
 // True when cb[c] == cb[0] + c * (cb[1] - cb[0]) holds exactly in fp32 for c = 0..3.
@@ -38,6 +40,12 @@ bool gemv_vec_supported(const PackedArgs &a);
 // Tensor-core GEMV (affine codebooks): cols % 256 == 0, 16-byte aligned codes and x.
 bool gemv_mma_supported(const PackedArgs &a);
 cudaError_t launch_gemv_mma(const PackedArgs &a, const GemvConfig &cfg, cudaStream_t s);
+
+// Tensor-core GEMV with each CTA's 64 code rows staged in shared memory by TMA:
+// cols % 512 == 0, cols <= 4096, 16-byte aligned codes and x.
+bool gemv_tma_supported(const PackedArgs &a);
+cudaError_t launch_gemv_tma(const PackedArgs &a, const GemvConfig &cfg, cudaStream_t s);
+unsigned int gemv_tma_take_device_error(cudaError_t *err);
 
 // Launches the GEMV.  Falls back to the bytewise kernel when the vectorised
 // path does not apply.  Returns the launch error.

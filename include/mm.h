@@ -163,7 +163,13 @@ typedef struct {
                             codes, scales or x, or reads y: the kernel then never
                             waits for the previous kernel (needs pdl), so back-to-back
                             calls over different matrices overlap completely */
-    int reserved[5];
+    int staging;         /* MM_DEQ_MMA only: 1 = code rows arrive in shared memory by TMA,
+                            64-row blocks through a 2-deep ring per CTA, one warp per
+                            256-field slab (cols % 512 == 0, cols <= 4096; split and warps
+                            must be 0, rows_per_lane = 64-row blocks per CTA, 0 = 4 for
+                            independent calls, 1 otherwise); 0 = per-warp register loads.
+                            The call without options stages whenever the shape allows it. */
+    int reserved[4];
 } mm_gemv_opts;
 
 mm_status mm_gemv_packed2_ex(const uint8_t *codes, const uint16_t *scales, const uint16_t *x,
