@@ -19,12 +19,12 @@ __all__ = [
     "mm_gemm_packed2", "mm_gemm_packed2_ex", "mm_check_device_error",
     "MM_OK", "MM_ERR_INVALID_ARG", "MM_ERR_UNSUPPORTED", "MM_ERR_CUDA", "MM_ERR_TIMEOUT",
     "MM_GEMM_AUTO", "MM_GEMM_FFMA", "MM_GEMM_TF32X3",
-    "MM_DEQ_AUTO", "MM_DEQ_SELECT", "MM_DEQ_AFFINE", "MM_DEQ_MMA",
+    "MM_DEQ_AUTO", "MM_DEQ_SELECT", "MM_DEQ_AFFINE", "MM_DEQ_MMA", "MM_DEQ_FP8", "MM_DEQ_TC",
 ]
 
 MM_OK, MM_ERR_INVALID_ARG, MM_ERR_UNSUPPORTED, MM_ERR_CUDA, MM_ERR_TIMEOUT = 0, 1, 2, 3, 4
 MM_GEMM_AUTO, MM_GEMM_FFMA, MM_GEMM_TF32X3 = 0, 1, 2
-MM_DEQ_AUTO, MM_DEQ_SELECT, MM_DEQ_AFFINE, MM_DEQ_MMA = 0, 1, 2, 3
+MM_DEQ_AUTO, MM_DEQ_SELECT, MM_DEQ_AFFINE, MM_DEQ_MMA, MM_DEQ_FP8, MM_DEQ_TC = 0, 1, 2, 3, 4, 5
 
 _PKG = os.path.dirname(os.path.abspath(__file__))
 _lock = threading.Lock()

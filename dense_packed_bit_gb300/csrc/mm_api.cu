@@ -162,18 +162,39 @@ mm_status mm_gemv_packed2_ex(const uint8_t *codes, const uint16_t *scales, const
     }
     const bool affine = mm::codebook_is_affine(codebook);
     mm::PackedArgs a{codes, scales, x, y, 1, rows, cols, {codebook[0], codebook[1], codebook[2], codebook[3]}};
+    // automatic decode, by measurement on GB300 (12,288 x 1,536): calls promised independent
+    // are bound by issue throughput, where the SIMT affine decode is fastest; otherwise each
+    // call's latency matters and the fp16 tensor-core decode is fastest
     if (cfg.dequant == MM_DEQ_AUTO)
-        cfg.dequant = (affine && mm::gemv_mma_supported(a)) ? MM_DEQ_MMA : affine ? MM_DEQ_AFFINE : MM_DEQ_SELECT;
-    if (cfg.dequant < MM_DEQ_SELECT || cfg.dequant > MM_DEQ_MMA)
+        cfg.dequant = !affine ? MM_DEQ_SELECT
+                      : (!cfg.independent && mm::gemv_mma_supported(a)) ? MM_DEQ_MMA : MM_DEQ_AFFINE;
+    if (cfg.dequant < MM_DEQ_SELECT || cfg.dequant > MM_DEQ_TC)
         return fail(MM_ERR_INVALID_ARG, "unknown dequant %d", cfg.dequant);
-    if ((cfg.dequant == MM_DEQ_AFFINE || cfg.dequant == MM_DEQ_MMA) && !affine)
+    if (cfg.dequant != MM_DEQ_SELECT && !affine)
         return fail(MM_ERR_INVALID_ARG, "affine decode needs codebook[c] == codebook[0] + c*(codebook[1]-codebook[0])");
-    if (cfg.staging < 0) cfg.staging = (cfg.dequant == MM_DEQ_MMA && !cfg.split && !cfg.warps &&
-                                        mm::gemv_tma_supported(a)) ? 1 : 0;
+    if (cfg.staging < 0) cfg.staging = 0;  // staging is chosen explicitly (it measured slower)
     if (cfg.staging != 0 && cfg.staging != 1) return fail(MM_ERR_INVALID_ARG, "staging must be 0 or 1");
-    if (cfg.staging && (cfg.dequant != MM_DEQ_MMA || !mm::gemv_tma_supported(a)))
+    if (cfg.staging && cfg.dequant < MM_DEQ_FP8 && (cfg.dequant != MM_DEQ_MMA || !mm::gemv_tma_supported(a)))
         return fail(MM_ERR_INVALID_ARG, "staging needs the tensor-core decode, cols %% 512 == 0, cols <= 4096 and 16-byte aligned codes and x");
-    if (cfg.dequant == MM_DEQ_MMA && cfg.staging) {
+    if (cfg.dequant == MM_DEQ_TC) {
+        // 127 rows per tile and CTA-wide roles fix split and warps; rows_per_lane counts the
+        // tiles a CTA multiplies (automatic: 1)
+        if (!mm::gemv_tc_supported(a))
+            return fail(MM_ERR_INVALID_ARG, "tcgen05 decode needs cols %% 512 == 0, cols <= 8192 and 16-byte aligned codes and x");
+        if (cfg.split || cfg.warps) return fail(MM_ERR_INVALID_ARG, "split and warps are fixed by the tcgen05 decode");
+        if (cfg.rows_per_lane < 0 || cfg.rows_per_lane > 64)
+            return fail(MM_ERR_INVALID_ARG, "rows_per_lane (127-row tiles per CTA) must be 0..64 with the tcgen05 decode");
+        cfg.blocks_per_cta = cfg.rows_per_lane ? cfg.rows_per_lane : 1;
+    } else if (cfg.dequant == MM_DEQ_FP8) {
+        // one warp per 256-field slab, code rows always staged by TMA; rows_per_lane counts
+        // the 64-row blocks a CTA streams (automatic: 2 for independent calls, 1 otherwise)
+        if (!mm::gemv_fp8_supported(a))
+            return fail(MM_ERR_INVALID_ARG, "fp8 decode needs cols %% 512 == 0, cols <= 4096 and 16-byte aligned codes and x");
+        if (cfg.split || cfg.warps) return fail(MM_ERR_INVALID_ARG, "split and warps are fixed by the fp8 decode");
+        if (cfg.rows_per_lane < 0 || cfg.rows_per_lane > 64)
+            return fail(MM_ERR_INVALID_ARG, "rows_per_lane (64-row blocks per CTA) must be 0..64 with the fp8 decode");
+        cfg.blocks_per_cta = cfg.rows_per_lane ? cfg.rows_per_lane : (cfg.independent ? 2 : 1);
+    } else if (cfg.dequant == MM_DEQ_MMA && cfg.staging) {
         // one warp per 256-field slab fixes split and warps; rows_per_lane counts the 64-row
         // blocks a CTA streams (automatic: 4 for independent calls, 1 otherwise)
         if (cfg.split || cfg.warps) return fail(MM_ERR_INVALID_ARG, "split and warps are fixed by staging");
@@ -259,6 +280,12 @@ mm_status mm_check_device_error(mm_stream_t stream) {
     const unsigned int q = mm::gemv_tma_take_device_error(&e);
     if (e != cudaSuccess) return cuda_fail(e, "mm_check_device_error");
     if (q != 0) return fail(MM_ERR_TIMEOUT, "a bounded device wait ran out in the staged GEMV (code %u)", q);
+    const unsigned int f = mm::gemv_fp8_take_device_error(&e);
+    if (e != cudaSuccess) return cuda_fail(e, "mm_check_device_error");
+    if (f != 0) return fail(MM_ERR_TIMEOUT, "a bounded device wait ran out in the fp8 GEMV (code %u)", f);
+    const unsigned int u = mm::gemv_tc_take_device_error(&e);
+    if (e != cudaSuccess) return cuda_fail(e, "mm_check_device_error");
+    if (u != 0) return fail(MM_ERR_TIMEOUT, "a bounded device wait ran out in the tcgen05 GEMV (code %u)", u);
     return ok();
 }
 

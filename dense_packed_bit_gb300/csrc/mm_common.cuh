@@ -77,6 +77,31 @@ __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity) {
     }
 }
 
+// try_wait that lets the hardware suspend the thread for up to `suspend_ns` while the
+// phase is incomplete (it resumes as soon as the phase completes), so waiting warps
+// take no issue slots from the warps that compute.
+__device__ __forceinline__ bool mbar_try_wait_suspend(uint64_t *bar, uint32_t parity, uint32_t suspend_ns) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity), "r"(suspend_ns)
+        : "memory");
+    return ok != 0;
+}
+
+// mbar_wait built on suspending tries: for waits that are long compared with the
+// work of the other warps on the SM (whole tiles streaming in from HBM).
+__device__ __forceinline__ bool mbar_wait_sleep(uint64_t *bar, uint32_t parity) {
+    if (mbar_try_wait_suspend(bar, parity, 100000u)) return true;
+    const unsigned long long t0 = global_ns();
+    while (!mbar_try_wait_suspend(bar, parity, 100000u))
+        if (global_ns() - t0 > kWaitLimitNs) return false;
+    return true;
+}
+
 // Named barrier over `nthreads` threads (a multiple of 32), id 1..15 (0 is __syncthreads).
 __device__ __forceinline__ void bar_sync(int id, int nthreads) {
     asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
@@ -121,6 +146,14 @@ __device__ __forceinline__ void tma_load_2d(void *smem_dst, const void *tmap, ui
         " [%0], [%1, {%3, %4}], [%2];" ::"r"(smem_u32(smem_dst)),
         "l"(tmap), "r"(smem_u32(bar)), "r"(c0), "r"(c1)
         : "memory");
+}
+
+// 1-D bulk copy of `bytes` (a multiple of 16; both addresses 16-byte aligned) from
+// global into this CTA's shared memory, completion reported on `bar`.
+__device__ __forceinline__ void bulk_load(void *smem_dst, const void *gsrc, uint32_t bytes, uint64_t *bar) {
+    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
+                 ::"r"(smem_u32(smem_dst)), "l"(gsrc), "r"(bytes), "r"(smem_u32(bar))
+                 : "memory");
 }
 
 __device__ __forceinline__ void tma_prefetch_desc(const void *tmap) {

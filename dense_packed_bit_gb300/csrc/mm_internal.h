@@ -27,7 +27,7 @@ struct GemvConfig {
     int weights_static;
     int independent;
     int staging;        // tensor-core decode: 1 = codes brought to shared memory by TMA
-    int blocks_per_cta; // staging: 64-row blocks each CTA streams through its TMA ring
+    int blocks_per_cta; // staging and fp8 decode: 64-row blocks each CTA streams through its TMA ring
 };
 
 // True when cb[c] == cb[0] + c * (cb[1] - cb[0]) holds exactly in fp32 for c = 0..3.
@@ -46,6 +46,12 @@ cudaError_t launch_gemv_mma(const PackedArgs &a, const GemvConfig &cfg, cudaStre
 bool gemv_tma_supported(const PackedArgs &a);
 cudaError_t launch_gemv_tma(const PackedArgs &a, const GemvConfig &cfg, cudaStream_t s);
 unsigned int gemv_tma_take_device_error(cudaError_t *err);
+bool gemv_fp8_supported(const PackedArgs &a);
+cudaError_t launch_gemv_fp8(const PackedArgs &a, const GemvConfig &cfg, cudaStream_t s);
+unsigned int gemv_fp8_take_device_error(cudaError_t *err);
+bool gemv_tc_supported(const PackedArgs &a);
+cudaError_t launch_gemv_tc(const PackedArgs &a, const GemvConfig &cfg, cudaStream_t s);
+unsigned int gemv_tc_take_device_error(cudaError_t *err);
 
 // Launches the GEMV.  Falls back to the bytewise kernel when the vectorised
 // path does not apply.  Returns the launch error.

@@ -134,14 +134,28 @@ mm_status mm_gemm_f32_ex(int transA, int transB, int64_t M, int64_t N, int64_t K
                          float *C, int64_t ldc, mm_stream_t stream, const mm_gemm_opts *opts);
 
 enum {
-    MM_DEQ_AUTO = 0,
+    MM_DEQ_AUTO = 0,     /* MM_DEQ_MMA for calls not promised independent (cols % 256 == 0),
+                            MM_DEQ_AFFINE for independent calls, MM_DEQ_SELECT when the
+                            codebook is not affine: the fastest measured on GB300 */
     MM_DEQ_SELECT = 1,   /* any codebook: per-field select of the entry, fp32 FMA */
     MM_DEQ_AFFINE = 2,   /* codebook[c] = c0 + c*d exactly (and no zero entry at field 3):
                             fields used in place as exact fp32 subnormals in packed f32x2
                             FMAs, y = scale * (c0 * sum x + d * sum c x) */
-    MM_DEQ_MMA = 3       /* same affine condition, cols % 256 == 0: two fields per integer
-                            op become an fp16x2 of exact subnormals and the multiply-adds run
-                            as tensor-core mma.sync (fp16 in, fp32 accumulate) */
+    MM_DEQ_MMA = 3,      /* same affine condition, cols % 256 == 0: two fields per integer
+                            op become an fp16x2 (1 + c 2^(p-10)) from which one fp16x2
+                            subtraction leaves c 2^(p-10) exactly; the multiply-adds run as
+                            tensor-core mma.sync (fp16 in, fp32 accumulate) */
+    MM_DEQ_FP8 = 4,      /* same affine condition, cols % 512 == 0, cols <= 4096, 16-byte
+                            aligned codes and x: one AND turns four fields into exact e4m3
+                            operands, x is split exactly into e5m2 pieces, and the
+                            multiply-adds run as mma.sync m16n8k32 (fp8 in, fp32 accumulate);
+                            code rows are staged by TMA, one warp per 256-field slab */
+    MM_DEQ_TC = 5        /* same affine condition, cols % 512 == 0, cols <= 8192, 16-byte
+                            aligned codes and x: the e4m3 field bytes are written to tensor
+                            memory as the A operand of tcgen05.mma kind::f8f6f4 (M = 128,
+                            K = 32), x as exact e5m2 pieces is the B operand in shared memory,
+                            fp32 accumulation in tensor memory; 127 rows per tile, the 128th
+                            lane forms sum x with the same MMAs */
 };
 
 typedef struct {
@@ -149,9 +163,13 @@ typedef struct {
                             MM_DEQ_MMA: warps sharing one row's dot product (1, 2, 3, 4, 6);
                             0 = automatic */
     int rows_per_lane;   /* SIMT decodes: rows each lane carries (1, 2, 4);
-                            MM_DEQ_MMA: 16-row blocks each warp carries (1, 2, 4); 0 = automatic */
+                            MM_DEQ_MMA: 16-row blocks each warp carries (1, 2, 4);
+                            MM_DEQ_FP8: 64-row blocks each CTA streams (1..64);
+                            MM_DEQ_TC: 127-row tiles each CTA multiplies (1..64);
+                            0 = automatic */
     int warps;           /* warps per CTA: 0 (auto), 1..16 (MM_DEQ_MMA: a multiple of split,
-                            at most 8 when rows_per_lane is 2 or 4) */
+                            at most 8 when rows_per_lane is 2 or 4; MM_DEQ_FP8 and
+                            MM_DEQ_TC: must be 0, like split) */
     int dequant;         /* MM_DEQ_* */
     int pdl;             /* 1: launch with programmatic dependent launch so the
                             kernel's prologue overlaps the previous kernel; it
@@ -167,8 +185,7 @@ typedef struct {
                             64-row blocks through a 2-deep ring per CTA, one warp per
                             256-field slab (cols % 512 == 0, cols <= 4096; split and warps
                             must be 0, rows_per_lane = 64-row blocks per CTA, 0 = 4 for
-                            independent calls, 1 otherwise); 0 = per-warp register loads.
-                            The call without options stages whenever the shape allows it. */
+                            independent calls, 1 otherwise); 0 = per-warp register loads. */
     int reserved[4];
 } mm_gemv_opts;
 

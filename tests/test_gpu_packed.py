@@ -112,7 +112,7 @@ def test_gemv_ignores_fields_past_cols(oracle, cols):
     assert np.array_equal(y_clean, y_dirty)
 
 
-@pytest.mark.parametrize("dequant", [1, 2, 3])
+@pytest.mark.parametrize("dequant", [1, 2, 3, 4, 5])
 @pytest.mark.parametrize("cols", [64, 256, 1536, 100])
 def test_gemv_one_hot_decodes_exactly(oracle, dequant, cols):
     # x = e_k: every y_r must be exactly fp32(scale_r * cb[field(r, k)])
@@ -125,7 +125,7 @@ def test_gemv_one_hot_decodes_exactly(oracle, dequant, cols):
             continue
         x = np.zeros(cols, np.uint16)
         x[k] = 0x3C00
-        opts = dict(dequant=dequant) if cols % (256 if dequant == 3 else 64) == 0 else {}
+        opts = dict(dequant=dequant) if cols % {3: 256, 4: 512, 5: 512}.get(dequant, 64) == 0 else {}
         y = gemv(codes, scales, x, rows, cols, CB2, **opts)
         ref, _ = oracle.packed_gemm(codes, scales, x, rows, cols, CB2)
         check_exact(y, ref[0], f"k={k}")
@@ -173,13 +173,13 @@ def test_gemv_zero_bound_rows_are_zero(oracle):
     codes = np.full((rows, cols // 4), 0xAA, np.uint8)
     scales = synth.uniform_f16_bits(9, (rows,), 0.005, 0.05)
     x = synth.normal_f16_bits(10, (cols,))
-    for d in (1, 2, 3):
+    for d in (1, 2, 3, 4, 5):
         y = gemv(codes, scales, x, rows, cols, CB2, dequant=d)
         assert np.all(y == 0.0), d
     # zero entry at field 1 or 0 cancels exactly too
     for cb, byte in ((np.array([-1, 0, 1, 2], np.float32), 0x55), (np.array([0, 0.5, 1, 1.5], np.float32), 0x00)):
         codes = np.full((rows, cols // 4), byte, np.uint8)
-        for d in (1, 2, 3):
+        for d in (1, 2, 3, 4, 5):
             y = gemv(codes, scales, x, rows, cols, cb, dequant=d)
             assert np.all(y == 0.0), (cb, d)
 
@@ -309,3 +309,105 @@ def test_gemv_tma_staging_exactness(oracle):
     zero = np.full((rows, cols // 4), 0xAA, np.uint8)
     xn = synth.normal_f16_bits(12, (cols,))
     assert np.all(gemv(zero, scales, xn, rows, cols, CB2, dequant=3, staging=1) == 0.0)
+
+
+# ------------------------------------------------------------------ fp8 tensor-core decode
+
+FP8_MODES = [dict(pdl=0), dict(pdl=1, weights_static=1), dict(pdl=1, independent=1)]
+
+
+@pytest.mark.parametrize("rows", [1, 63, 64, 65, 1000, 1100])
+@pytest.mark.parametrize("cols", [512, 1024, 1536, 4096])
+@pytest.mark.parametrize("mode", FP8_MODES, ids=["serial", "chained", "independent"])
+@pytest.mark.parametrize("blocks", [0, 1, 3, 8])
+def test_gemv_fp8(oracle, rows, cols, mode, blocks):
+    # codes as e4m3 operands, x as exact e5m2 pieces, mma.sync m16n8k32; 64-row blocks
+    # through the TMA ring (0 = automatic count), ragged last CTAs and blocks
+    codes, scales, x = rand_case(rows, cols, seed=rows * 11 + cols)
+    y = gemv(codes, scales, x, rows, cols, CB2, dequant=4, rows_per_lane=blocks, **mode)
+    ref, T = oracle.packed_gemm(codes, scales, x, rows, cols, CB2)
+    check_bound(y, ref[0], T[0], f"{rows}x{cols} {mode} blocks {blocks}")
+
+
+@pytest.mark.parametrize("rows", [1, 126, 127, 128, 254, 255, 1000, 1100])
+@pytest.mark.parametrize("cols", [512, 1024, 1536, 4096, 8192])
+@pytest.mark.parametrize("mode", FP8_MODES, ids=["serial", "chained", "independent"])
+@pytest.mark.parametrize("tiles", [0, 1, 2, 5])
+def test_gemv_tcgen05(oracle, rows, cols, mode, tiles):
+    # e4m3 code bytes in tensor memory x e5m2 pieces of x, tcgen05.mma; 127-row tiles
+    # (the 128th lane forms sum x), several tiles per CTA, ragged last tiles
+    codes, scales, x = rand_case(rows, cols, seed=rows * 13 + cols)
+    y = gemv(codes, scales, x, rows, cols, CB2, dequant=5, rows_per_lane=tiles, **mode)
+    ref, T = oracle.packed_gemm(codes, scales, x, rows, cols, CB2)
+    check_bound(y, ref[0], T[0], f"{rows}x{cols} {mode} tiles {tiles}")
+
+
+def _fp16_values(bits):
+    return np.array(bits, np.uint16).view(np.float16).astype(np.float64)
+
+
+@pytest.mark.parametrize("dequant", [4, 5])
+def test_gemv_fp8_one_hot_every_window(oracle, dequant):
+    # x = v e_k for values on both sides of the 2^-6 window boundary, subnormals, the
+    # largest finite fp16 and negative values: y_r must be exactly fp32(scale_r * cb * v)
+    rows, cols = 130, 1536
+    codes, scales, _ = rand_case(rows, cols, seed=14)
+    fields = oracle.unpack2(codes, rows, cols)
+    s = scales.view(np.float16).astype(np.float64)
+    values = [0x3C00, 0x2400, 0x23FF, 0x0001, 0x0155, 0x03FF, 0x0400, 0x7BFF, 0xFBFF, 0x8001, 0xC4D3, 0x1234]
+    for k in (0, 1, 2, 3, 4, 15, 16, 63, 64, 255, 256, 511, 777, 1535):
+        for bits in values:
+            x = np.zeros(cols, np.uint16)
+            x[k] = bits
+            y = gemv(codes, scales, x, rows, cols, CB2, dequant=dequant)
+            expect = (s * CB2[fields[:, k]].astype(np.float64) * _fp16_values([bits])[0]).astype(np.float32)
+            assert np.array_equal(y, expect), (k, hex(bits))
+
+
+@pytest.mark.parametrize("dequant", [4, 5])
+def test_gemv_fp8_integer_activations_bit_exact(oracle, dequant):
+    rows, cols = 500, 1536
+    codes, _, _ = rand_case(rows, cols, seed=78)
+    scales = np.full(rows, 0x3C00, np.uint16)
+    rng = np.random.default_rng(4)
+    x = rng.integers(-3, 4, size=cols).astype(np.float16).view(np.uint16)
+    y = gemv(codes, scales, x, rows, cols, CB2, dequant=dequant)
+    ref, _ = oracle.packed_gemm(codes, scales, x, rows, cols, CB2)
+    check_exact(y, ref[0], "integer x")
+
+
+@pytest.mark.parametrize("dequant", [4, 5])
+def test_gemv_fp8_wide_dynamic_range(oracle, dequant):
+    # activations spread over every fp16 binade, subnormals included, both signs
+    rows, cols = 257, 2048
+    codes, scales, _ = rand_case(rows, cols, seed=21)
+    rng = np.random.default_rng(21)
+    x = rng.integers(0, 0x7C00, size=cols).astype(np.uint16) | (rng.integers(0, 2, size=cols) << 15).astype(np.uint16)
+    y = gemv(codes, scales, x, rows, cols, CB2, dequant=dequant)
+    ref, T = oracle.packed_gemm(codes, scales, x, rows, cols, CB2)
+    check_bound(y, ref[0], T[0], "wide range")
+
+
+@pytest.mark.parametrize("cb,zero_code", [(CB2, 2), (np.array([-1, 0, 1, 2], np.float32), 1),
+                                          (np.array([0, 0.5, 1, 1.5], np.float32), 0)])
+@pytest.mark.parametrize("dequant", [4, 5])
+def test_gemv_fp8_zero_rows_at_every_position(oracle, cb, zero_code, dequant):
+    # rows whose fields all hold the zero entry sit at every position of the 16-row MMA
+    # blocks, between random rows: their outputs must be exactly 0
+    rows, cols = 200, 1536
+    codes, scales, x = rand_case(rows, cols, seed=30 + zero_code)
+    zero_rows = [r for r in range(rows) if r % 3 == 0]
+    codes[zero_rows, :] = np.uint8(zero_code * 0x55)
+    for x_ in (x, synth.normal_f16_bits(31, (cols,))):
+        y = gemv(codes, scales, x_, rows, cols, cb, dequant=dequant)
+        assert np.all(y[zero_rows] == 0.0)
+        ref, T = oracle.packed_gemm(codes, scales, x_, rows, cols, cb)
+        check_bound(y, ref[0], T[0], "zero rows")
+
+
+@pytest.mark.parametrize("dequant", [4, 5])
+def test_gemv_fp8_deterministic(dequant):
+    c = synth.gemv_2bit_12288x1536(5)
+    y1 = gemv(c.codes, c.scales, c.X, c.rows, c.cols, c.codebook, dequant=dequant, pdl=1, independent=1)
+    y2 = gemv(c.codes, c.scales, c.X, c.rows, c.cols, c.codebook, dequant=dequant, rows_per_lane=3)
+    assert np.array_equal(y1.view(np.uint32), y2.view(np.uint32))
