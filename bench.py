@@ -233,7 +233,7 @@ class Workload:
         self.args = args
 
 
-GEMV_INDEP = dict(split=8, rows_per_lane=4, warps=8, dequant=2, pdl=1, independent=1)
+GEMV_INDEP = dict(dequant=2, staging=1, rows_per_lane=3, pdl=1, independent=1)
 GEMV_CHAINED = dict(split=3, rows_per_lane=2, warps=6, dequant=3, pdl=1, weights_static=1)
 GEMV_INDEP_STREAMS = 2  # independent calls alternate between two streams inside the graph
 

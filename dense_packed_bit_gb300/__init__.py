@@ -148,7 +148,7 @@ def mm_gemv_packed2(codes, scales, x, y, rows, cols, codebook, stream=None):
 
 
 def mm_gemv_packed2_ex(codes, scales, x, y, rows, cols, codebook, stream=None, *, split=0,
-                       rows_per_lane=0, warps=0, dequant=0, pdl=0, weights_static=0, independent=0, staging=0):
+                       rows_per_lane=0, warps=0, dequant=0, pdl=0, weights_static=0, independent=0, staging=-1):
     o = GemvOpts(split, rows_per_lane, warps, dequant, pdl, weights_static, independent, staging)
     _check(load_library().mm_gemv_packed2_ex(_ptr(codes), _ptr(scales), _ptr(x), _ptr(y), rows, cols,
                                              _codebook(codebook), _stream(stream), ctypes.byref(o)))

@@ -338,6 +338,7 @@ bool gemv_vec_supported(const PackedArgs &a) {
 
 cudaError_t launch_gemv_packed2(const PackedArgs &a, const GemvConfig &cfg, cudaStream_t st) {
     if (cfg.dequant == 5) return launch_gemv_tc(a, cfg, st);
+    if (cfg.dequant == kDeqAffine && cfg.staging) return launch_gemv_rows(a, cfg, st);
     if (cfg.dequant == 4) return launch_gemv_fp8(a, cfg, st);
     if (cfg.dequant == 3) return cfg.staging ? launch_gemv_tma(a, cfg, st) : launch_gemv_mma(a, cfg, st);
     if (!gemv_vec_supported(a)) {

@@ -172,10 +172,16 @@ mm_status mm_gemv_packed2_ex(const uint8_t *codes, const uint16_t *scales, const
         return fail(MM_ERR_INVALID_ARG, "unknown dequant %d", cfg.dequant);
     if (cfg.dequant != MM_DEQ_SELECT && !affine)
         return fail(MM_ERR_INVALID_ARG, "affine decode needs codebook[c] == codebook[0] + c*(codebook[1]-codebook[0])");
-    if (cfg.staging < 0) cfg.staging = 0;  // staging is chosen explicitly (it measured slower)
+    // automatic staging: the TMA-staged affine kernel is the fastest measured for independent
+    // calls; the staged tensor-core decode measured slower than register loads
+    if (cfg.staging < 0)
+        cfg.staging = (cfg.dequant == MM_DEQ_AFFINE && cfg.independent && !cfg.split && !cfg.warps &&
+                       mm::gemv_rows_supported(a)) ? 1 : 0;
     if (cfg.staging != 0 && cfg.staging != 1) return fail(MM_ERR_INVALID_ARG, "staging must be 0 or 1");
-    if (cfg.staging && cfg.dequant < MM_DEQ_FP8 && (cfg.dequant != MM_DEQ_MMA || !mm::gemv_tma_supported(a)))
-        return fail(MM_ERR_INVALID_ARG, "staging needs the tensor-core decode, cols %% 512 == 0, cols <= 4096 and 16-byte aligned codes and x");
+    if (cfg.staging && cfg.dequant < MM_DEQ_FP8 &&
+        !(cfg.dequant == MM_DEQ_MMA && mm::gemv_tma_supported(a)) &&
+        !(cfg.dequant == MM_DEQ_AFFINE && mm::gemv_rows_supported(a)))
+        return fail(MM_ERR_INVALID_ARG, "staging needs the affine or tensor-core decode, cols %% 512 == 0, cols <= 4096 and 16-byte aligned codes and x");
     if (cfg.dequant == MM_DEQ_TC) {
         // 127 rows per tile and CTA-wide roles fix split and warps; rows_per_lane counts the
         // tiles a CTA multiplies (automatic: 1)
@@ -194,6 +200,13 @@ mm_status mm_gemv_packed2_ex(const uint8_t *codes, const uint16_t *scales, const
         if (cfg.rows_per_lane < 0 || cfg.rows_per_lane > 64)
             return fail(MM_ERR_INVALID_ARG, "rows_per_lane (64-row blocks per CTA) must be 0..64 with the fp8 decode");
         cfg.blocks_per_cta = cfg.rows_per_lane ? cfg.rows_per_lane : (cfg.independent ? 2 : 1);
+    } else if (cfg.dequant == MM_DEQ_AFFINE && cfg.staging) {
+        // one lane per row of 128-row TMA blocks, eight warps splitting K; rows_per_lane counts
+        // the blocks a CTA streams (automatic: 2 for independent calls, 1 otherwise)
+        if (cfg.split || cfg.warps) return fail(MM_ERR_INVALID_ARG, "split and warps are fixed by staging");
+        if (cfg.rows_per_lane < 0 || cfg.rows_per_lane > 64)
+            return fail(MM_ERR_INVALID_ARG, "rows_per_lane (128-row blocks per CTA) must be 0..64 with staging");
+        cfg.blocks_per_cta = cfg.rows_per_lane ? cfg.rows_per_lane : (cfg.independent ? 3 : 1);
     } else if (cfg.dequant == MM_DEQ_MMA && cfg.staging) {
         // one warp per 256-field slab fixes split and warps; rows_per_lane counts the 64-row
         // blocks a CTA streams (automatic: 4 for independent calls, 1 otherwise)
@@ -283,6 +296,9 @@ mm_status mm_check_device_error(mm_stream_t stream) {
     const unsigned int f = mm::gemv_fp8_take_device_error(&e);
     if (e != cudaSuccess) return cuda_fail(e, "mm_check_device_error");
     if (f != 0) return fail(MM_ERR_TIMEOUT, "a bounded device wait ran out in the fp8 GEMV (code %u)", f);
+    const unsigned int v2 = mm::gemv_rows_take_device_error(&e);
+    if (e != cudaSuccess) return cuda_fail(e, "mm_check_device_error");
+    if (v2 != 0) return fail(MM_ERR_TIMEOUT, "a bounded device wait ran out in the staged affine GEMV (code %u)", v2);
     const unsigned int u = mm::gemv_tc_take_device_error(&e);
     if (e != cudaSuccess) return cuda_fail(e, "mm_check_device_error");
     if (u != 0) return fail(MM_ERR_TIMEOUT, "a bounded device wait ran out in the tcgen05 GEMV (code %u)", u);

@@ -49,6 +49,9 @@ unsigned int gemv_tma_take_device_error(cudaError_t *err);
 bool gemv_fp8_supported(const PackedArgs &a);
 cudaError_t launch_gemv_fp8(const PackedArgs &a, const GemvConfig &cfg, cudaStream_t s);
 unsigned int gemv_fp8_take_device_error(cudaError_t *err);
+bool gemv_rows_supported(const PackedArgs &a);
+cudaError_t launch_gemv_rows(const PackedArgs &a, const GemvConfig &cfg, cudaStream_t s);
+unsigned int gemv_rows_take_device_error(cudaError_t *err);
 bool gemv_tc_supported(const PackedArgs &a);
 cudaError_t launch_gemv_tc(const PackedArgs &a, const GemvConfig &cfg, cudaStream_t s);
 unsigned int gemv_tc_take_device_error(cudaError_t *err);

@@ -2,6 +2,7 @@
 
     python -m dense_packed_bit_gb300.profile_case gemm --layout nn --size 2048 --reps 3
     python -m dense_packed_bit_gb300.profile_case gemv --reps 3 [--split 8 --rows 4 --warps 8 --dequant 2 --independent 1]
+    python -m dense_packed_bit_gb300.profile_case gemv --reps 3 --split 0 --rows 1 --warps 0 --dequant 2 --staging 1
     python -m dense_packed_bit_gb300.profile_case ternary --reps 1
 
 One warm-up launch precedes the `reps` launches.  No timing is done here:
@@ -27,6 +28,7 @@ def main(argv=None):
     ap.add_argument("--pdl", type=int, default=1)
     ap.add_argument("--dequant", type=int, default=0)
     ap.add_argument("--independent", type=int, default=0)
+    ap.add_argument("--staging", type=int, default=0)
     a = ap.parse_args(argv)
 
     import torch
@@ -57,7 +59,8 @@ def main(argv=None):
             i = r % a.matrices
             mm.mm_gemv_packed2_ex(codes[i], scales[i], x, y[i], 12288, 1536, c.codebook, split=a.split,
                                   rows_per_lane=a.rows, warps=a.warps, dequant=a.dequant, pdl=a.pdl,
-                                  weights_static=a.pdl and not a.independent, independent=a.independent)
+                                  weights_static=a.pdl and not a.independent, independent=a.independent,
+                                  staging=a.staging)
     else:
         layers = []
         for layer in range(16):

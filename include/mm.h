@@ -135,8 +135,9 @@ mm_status mm_gemm_f32_ex(int transA, int transB, int64_t M, int64_t N, int64_t K
 
 enum {
     MM_DEQ_AUTO = 0,     /* MM_DEQ_MMA for calls not promised independent (cols % 256 == 0),
-                            MM_DEQ_AFFINE for independent calls, MM_DEQ_SELECT when the
-                            codebook is not affine: the fastest measured on GB300 */
+                            MM_DEQ_AFFINE (TMA-staged when the shape allows) for independent
+                            calls, MM_DEQ_SELECT when the codebook is not affine: the fastest
+                            measured on GB300 */
     MM_DEQ_SELECT = 1,   /* any codebook: per-field select of the entry, fp32 FMA */
     MM_DEQ_AFFINE = 2,   /* codebook[c] = c0 + c*d exactly (and no zero entry at field 3):
                             fields used in place as exact fp32 subnormals in packed f32x2
@@ -181,11 +182,16 @@ typedef struct {
                             codes, scales or x, or reads y: the kernel then never
                             waits for the previous kernel (needs pdl), so back-to-back
                             calls over different matrices overlap completely */
-    int staging;         /* MM_DEQ_MMA only: 1 = code rows arrive in shared memory by TMA,
-                            64-row blocks through a 2-deep ring per CTA, one warp per
-                            256-field slab (cols % 512 == 0, cols <= 4096; split and warps
-                            must be 0, rows_per_lane = 64-row blocks per CTA, 0 = 4 for
-                            independent calls, 1 otherwise); 0 = per-warp register loads. */
+    int staging;         /* MM_DEQ_MMA and MM_DEQ_AFFINE: 1 = code rows arrive in shared
+                            memory by TMA (cols % 512 == 0, cols <= 4096; split and warps must
+                            be 0).  MM_DEQ_MMA: 64-row blocks through a 2-deep ring per CTA,
+                            one warp per 256-field slab, rows_per_lane = 64-row blocks per CTA
+                            (0 = 4 for independent calls, 1 otherwise).  MM_DEQ_AFFINE:
+                            128-row blocks, one lane per row, eight warps splitting K,
+                            rows_per_lane = 128-row blocks per CTA (0 = 3 for independent
+                            calls, 1 otherwise).  0 = per-warp register loads; negative =
+                            automatic (staged for independent affine calls when the shape
+                            allows, the default without options). */
     int reserved[4];
 } mm_gemv_opts;
 

@@ -170,8 +170,9 @@ def test_gemm_packed_bad_splitk(lib, splitk):
     assert st == mm.MM_ERR_INVALID_ARG
 
 
-@pytest.mark.parametrize("opt", [dict(dequant=3, staging=2), dict(dequant=2, staging=1),
-                                 dict(dequant=3, staging=1, split=2), dict(dequant=3, staging=1, rows_per_lane=65)])
+@pytest.mark.parametrize("opt", [dict(dequant=3, staging=2), dict(dequant=1, staging=1),
+                                 dict(dequant=3, staging=1, split=2), dict(dequant=3, staging=1, rows_per_lane=65),
+                                 dict(dequant=2, staging=1, warps=4), dict(dequant=2, staging=1, rows_per_lane=65)])
 def test_gemv_bad_staging(lib, opt):
     o = mm.GemvOpts(**opt)
     st = lib.mm_gemv_packed2_ex(FAKE, FAKE + 0x100000, FAKE + 0x200000, FAKE + 0x300000, 64, 1536,

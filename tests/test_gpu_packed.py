@@ -285,16 +285,19 @@ def test_gemm_packed_cluster_splitk(oracle, splitk, tile, M, rows, cols):
 @pytest.mark.parametrize("mode", [dict(pdl=0), dict(pdl=1, weights_static=1), dict(pdl=1, independent=1)],
                          ids=["serial", "chained", "independent"])
 @pytest.mark.parametrize("blocks", [0, 1, 3, 8])
-def test_gemv_tma_staging(oracle, rows, cols, mode, blocks):
-    # 64-row blocks streamed through a TMA ring (blocks per CTA: 0 = automatic), one warp per
-    # 256-field slab, tensor-core decode; ragged row counts leave partial last CTAs and blocks
+@pytest.mark.parametrize("dequant", [2, 3])
+def test_gemv_tma_staging(oracle, rows, cols, mode, blocks, dequant):
+    # code rows streamed through a TMA ring (blocks per CTA: 0 = automatic): 64-row blocks and one
+    # warp per 256-field slab (tensor-core decode), or 128-row blocks and one lane per row (SIMT
+    # affine decode); ragged row counts leave partial last CTAs and blocks
     codes, scales, x = rand_case(rows, cols, seed=rows * 7 + cols)
-    y = gemv(codes, scales, x, rows, cols, CB2, dequant=3, staging=1, rows_per_lane=blocks, **mode)
+    y = gemv(codes, scales, x, rows, cols, CB2, dequant=dequant, staging=1, rows_per_lane=blocks, **mode)
     ref, T = oracle.packed_gemm(codes, scales, x, rows, cols, CB2)
     check_bound(y, ref[0], T[0], f"{rows}x{cols} {mode}")
 
 
-def test_gemv_tma_staging_exactness(oracle):
+@pytest.mark.parametrize("dequant", [2, 3])
+def test_gemv_tma_staging_exactness(oracle, dequant):
     rows, cols = 130, 1536
     codes, scales, _ = rand_case(rows, cols, seed=4)
     fields = oracle.unpack2(codes, rows, cols)
@@ -303,12 +306,15 @@ def test_gemv_tma_staging_exactness(oracle):
         for bits in (0x3C00, 0x0001, 0xC400):
             x = np.zeros(cols, np.uint16)
             x[k] = bits
-            y = gemv(codes, scales, x, rows, cols, CB2, dequant=3, staging=1)
+            y = gemv(codes, scales, x, rows, cols, CB2, dequant=dequant, staging=1)
             xv = float(np.array([bits], np.uint16).view(np.float16)[0])
             assert np.array_equal(y.astype(np.float64), s * CB2[fields[:, k]].astype(np.float64) * xv), (k, bits)
     zero = np.full((rows, cols // 4), 0xAA, np.uint8)
     xn = synth.normal_f16_bits(12, (cols,))
-    assert np.all(gemv(zero, scales, xn, rows, cols, CB2, dequant=3, staging=1) == 0.0)
+    assert np.all(gemv(zero, scales, xn, rows, cols, CB2, dequant=dequant, staging=1) == 0.0)
+    for cb, byte in ((np.array([-1, 0, 1, 2], np.float32), 0x55), (np.array([0, 0.5, 1, 1.5], np.float32), 0x00)):
+        zr = np.full((rows, cols // 4), byte, np.uint8)
+        assert np.all(gemv(zr, scales, xn, rows, cols, cb, dequant=dequant, staging=1) == 0.0)
 
 
 # ------------------------------------------------------------------ fp8 tensor-core decode
