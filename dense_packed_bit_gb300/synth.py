@@ -28,6 +28,7 @@ Value recipes (the shapes and distributions of the workloads on the pages):
 from __future__ import annotations
 
 import hashlib
+import math
 from dataclasses import dataclass
 
 import numpy as np
@@ -212,16 +213,48 @@ CODEBOOK_2BIT = np.array([-2.0, -1.0, 0.0, 1.0], dtype=np.float32)
 CODEBOOK_TERNARY = np.array([-1.0, 0.0, 1.0, 0.0], dtype=np.float32)
 
 
+def _normal_ppf(p: float) -> float:
+    """Standard normal quantile by bisection on the CDF 0.5 erfc(-x / sqrt 2) (|error| < 1e-15)."""
+    lo, hi = -40.0, 40.0
+    for _ in range(200):
+        mid = 0.5 * (lo + hi)
+        if 0.5 * math.erfc(-mid / math.sqrt(2.0)) < p:
+            lo = mid
+        else:
+            hi = mid
+    return 0.5 * (lo + hi)
+
+
+def normal_quantile_codebook() -> np.ndarray:
+    """16-entry 4-bit codebook of normal-quantile levels with an exact zero (NF4-style).
+
+    Codes 0..6 are negative, code 7 is 0, codes 8..15 are positive: level i of a
+    side of n levels is the standard-normal quantile at 0.5 + 0.48 i / n, and each
+    side is divided by its largest level, so the table runs from -1 to 1.  None of
+    the non-trivial levels is exact in fp16.
+    """
+    neg = [-_normal_ppf(0.5 + 0.48 * i / 7) for i in range(1, 8)]
+    pos = [_normal_ppf(0.5 + 0.48 * i / 8) for i in range(1, 9)]
+    neg = [v / -neg[-1] for v in neg]
+    pos = [v / pos[-1] for v in pos]
+    return np.array(sorted(neg) + [0.0] + pos, dtype=np.float32)
+
+
+CODEBOOK_NQ4 = normal_quantile_codebook()
+
+
 def packed_matrix(seed_base, index, rows, cols, kind):
-    nbytes = rows * ((cols + 3) // 4)
-    if kind == "uniform2":
+    """Codes (rows x packed bytes) and fp16 scales; kind 'uniform4' packs 4-bit fields."""
+    rb = (cols + 1) // 2 if kind == "uniform4" else (cols + 3) // 4
+    nbytes = rows * rb
+    if kind in ("uniform2", "uniform4"):
         codes = random_bytes(_seed(seed_base, 1, index), nbytes)
     elif kind == "ternary":
         codes = ternary_field_bytes(_seed(seed_base, 1, index), nbytes)
     else:
         raise ValueError(kind)
     scales = uniform_f16_bits(_seed(seed_base, 2, index), (rows,), 0.005, 0.05)
-    return codes.reshape(rows, (cols + 3) // 4), scales
+    return codes.reshape(rows, rb), scales
 
 
 def gemv_2bit_12288x1536(index: int) -> PackedCase:
@@ -230,6 +263,15 @@ def gemv_2bit_12288x1536(index: int) -> PackedCase:
     x = normal_f16_bits(_seed(3, 3, 0), (1, 1536))
     return PackedCase(f"gemv2_12288x1536_m{index}", 12288, 1536, codes, scales,
                       CODEBOOK_2BIT.copy(), x)
+
+
+def gemv_4bit_12288x1536(index: int) -> PackedCase:
+    """One of the 64 rotated 4-bit GEMV matrices: 12288 rows x 1536 cols (9 MiB of codes),
+    fields uniform in 0..15 (two per byte), normal-quantile codebook."""
+    codes, scales = packed_matrix(5, index, 12288, 1536, "uniform4")
+    x = normal_f16_bits(_seed(5, 3, 0), (1, 1536))
+    return PackedCase(f"gemv4_12288x1536_m{index}", 12288, 1536, codes, scales,
+                      CODEBOOK_NQ4.copy(), x)
 
 
 def ternary_encoder_layer(layer: int, proj: str) -> PackedCase:

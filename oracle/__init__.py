@@ -58,6 +58,10 @@ def _load():
             lib.orc_gemm_at.argtypes = [I, I, I64, P, I64, P, I64, I64, P, P, P, P]
             lib.orc_packed_gemm.argtypes = [P, P, P, I64, I64, I64, P, P, P, I]
             lib.orc_packed_gemm_at.argtypes = [P, P, P, I64, P, I64, P, P, P, P]
+            lib.orc_unpack4.argtypes = [P, I64, I64, P]
+            lib.orc_pack4.argtypes = [P, I64, I64, P]
+            lib.orc_packed4_gemm.argtypes = [P, P, P, I64, I64, I64, P, P, P, I]
+            lib.orc_packed4_gemm_at.argtypes = [P, P, P, I64, P, I64, P, P, P, P]
             _lib = lib
     return _lib
 
@@ -160,4 +164,57 @@ def packed_gemm_at(codes, scales, X, cols: int, codebook, mm, rr):
     T = np.empty(len(mm), dtype=np.float64)
     lib.orc_packed_gemm_at(_ptr(codes), _ptr(scales), _ptr(X), cols, _ptr(cb), len(mm),
                            _ptr(mm), _ptr(rr), _ptr(Y), _ptr(T))
+    return Y, T
+
+
+def unpack4(codes: np.ndarray, rows: int, cols: int) -> np.ndarray:
+    """(rows, cols) uint8 4-bit fields of packed rows of ceil(cols/2) bytes (low nibble first)."""
+    lib = _load()
+    c = np.ascontiguousarray(codes, dtype=np.uint8)
+    assert c.size == rows * ((cols + 1) // 2)
+    out = np.empty((rows, cols), dtype=np.uint8)
+    lib.orc_unpack4(_ptr(c), rows, cols, _ptr(out))
+    return out
+
+
+def pack4(fields: np.ndarray) -> np.ndarray:
+    lib = _load()
+    f = np.ascontiguousarray(fields, dtype=np.uint8)
+    rows, cols = f.shape
+    out = np.empty((rows, (cols + 1) // 2), dtype=np.uint8)
+    lib.orc_pack4(_ptr(f), rows, cols, _ptr(out))
+    return out
+
+
+def packed4_gemm(codes: np.ndarray, scales: np.ndarray, X: np.ndarray, rows: int, cols: int,
+                 codebook, threads: int | None = None):
+    """(Y, T), both (M, rows) float64, Y[m,r] = sum_k scale_r cb[field4(r,k)] X[m,k] (16-entry cb)."""
+    lib = _load()
+    codes = np.ascontiguousarray(codes, dtype=np.uint8)
+    scales = np.ascontiguousarray(scales, dtype=np.uint16)
+    X = np.ascontiguousarray(X, dtype=np.uint16).reshape(-1, cols)
+    cb = np.ascontiguousarray(codebook, dtype=np.float32)
+    assert cb.size == 16 and scales.size == rows and codes.size == rows * ((cols + 1) // 2)
+    M = X.shape[0]
+    Y = np.empty((M, rows), dtype=np.float64)
+    T = np.empty((M, rows), dtype=np.float64)
+    lib.orc_packed4_gemm(_ptr(codes), _ptr(scales), _ptr(X), M, rows, cols, _ptr(cb),
+                         _ptr(Y), _ptr(T), threads or default_threads())
+    return Y, T
+
+
+def packed4_gemm_at(codes, scales, X, cols: int, codebook, mm, rr):
+    """(Y, T) of the 4-bit form at the listed coordinates (mm[n], rr[n])."""
+    lib = _load()
+    codes = np.ascontiguousarray(codes, dtype=np.uint8)
+    scales = np.ascontiguousarray(scales, dtype=np.uint16)
+    X = np.ascontiguousarray(X, dtype=np.uint16).reshape(-1, cols)
+    cb = np.ascontiguousarray(codebook, dtype=np.float32)
+    assert cb.size == 16
+    mm = np.ascontiguousarray(mm, dtype=np.int64)
+    rr = np.ascontiguousarray(rr, dtype=np.int64)
+    Y = np.empty(len(mm), dtype=np.float64)
+    T = np.empty(len(mm), dtype=np.float64)
+    lib.orc_packed4_gemm_at(_ptr(codes), _ptr(scales), _ptr(X), cols, _ptr(cb), len(mm),
+                            _ptr(mm), _ptr(rr), _ptr(Y), _ptr(T))
     return Y, T

@@ -30,6 +30,12 @@
  *    ceil(cols/4) bytes and unused high fields of its last byte are ignored.
  *  - a field selects one of 4 codebook entries; the per-row fp16 scale
  *    multiplies the entry.
+ *  - 4-bit codes (the 16-entry codebook of "Kernel 0112", section "What the
+ *    kernel costs in a whole token": the 4-bit weight-reading kernels, and of
+ *    "More Stumbling, This Time in the Browser": the packed NF4 path): element
+ *    k of a packed row is in byte floor(k/2), bits 4*(k mod 2)..4*(k mod 2)+3
+ *    (low nibble first, little-endian along K like the 2-bit codes); a row has
+ *    ceil(cols/2) bytes; the field selects one of 16 codebook entries.
  *
  * Loop nesting: each output's sum runs over k = 0..K-1 in increasing order.
  * The nesting of the i/j loops only changes which output is visited when, not
@@ -85,6 +91,43 @@ void orc_pack2(const uint8_t *fields, int64_t rows, int64_t cols, uint8_t *codes
             uint8_t v = fields[r * cols + k] & 3;
             codes[r * rb + k / 4] |= (uint8_t)(v << (2 * (k % 4)));
         }
+}
+
+/* 4-bit field of element k of one packed row: byte floor(k/2), low nibble first */
+int orc_code4(const uint8_t *row, int64_t k) {
+    uint8_t byte = row[k / 2];
+    int shift = 4 * (int)(k % 2);
+    return (byte >> shift) & 15;
+}
+
+int64_t orc_row_bytes4(int64_t cols) { return (cols + 1) / 2; }
+
+/* out[r*cols + k] = 4-bit field of element (r, k) */
+void orc_unpack4(const uint8_t *codes, int64_t rows, int64_t cols, uint8_t *out) {
+    int64_t rb = orc_row_bytes4(cols);
+    for (int64_t r = 0; r < rows; ++r)
+        for (int64_t k = 0; k < cols; ++k)
+            out[r * cols + k] = (uint8_t)orc_code4(codes + r * rb, k);
+}
+
+/* inverse of orc_unpack4; fields must be in 0..15; an odd row's unused high nibble is 0 */
+void orc_pack4(const uint8_t *fields, int64_t rows, int64_t cols, uint8_t *codes) {
+    int64_t rb = orc_row_bytes4(cols);
+    memset(codes, 0, (size_t)(rows * rb));
+    for (int64_t r = 0; r < rows; ++r)
+        for (int64_t k = 0; k < cols; ++k) {
+            uint8_t v = fields[r * cols + k] & 15;
+            codes[r * rb + k / 2] |= (uint8_t)(v << (4 * (k % 2)));
+        }
+}
+
+/* field of element k of a packed row with `bits` bits per field (2 or 4) */
+static int packed_code(const uint8_t *row, int64_t k, int bits) {
+    return bits == 4 ? orc_code4(row, k) : orc_code2(row, k);
+}
+
+static int64_t packed_row_bytes(int64_t cols, int bits) {
+    return bits == 4 ? orc_row_bytes4(cols) : orc_row_bytes(cols);
 }
 
 /* ------------------------------------------------------------------------ */
@@ -183,10 +226,10 @@ void orc_gemm_at(int transA, int transB, int64_t K,
 }
 
 /* ------------------------------------------------------------------------ */
-/* Packed 2-bit weights:                                                    */
+/* Packed 2-bit (or 4-bit) weights:                                         */
 /*   Y[m][r] = sum_k scale_r * codebook[field(r,k)] * X[m][k]               */
-/* codes: rows x ceil(cols/4) bytes; scales: rows fp16; X: M x cols fp16.   */
-/* A GEMV is the M = 1 case.                                                */
+/* codes: rows x ceil(cols/4) bytes (4-bit: ceil(cols/2)); scales: rows fp16; */
+/* X: M x cols fp16.  A GEMV is the M = 1 case.                             */
 /* ------------------------------------------------------------------------ */
 
 typedef struct {
@@ -197,17 +240,18 @@ typedef struct {
     const float *codebook;
     double *Y, *T;
     int64_t m0, m1;
+    int bits;
 } packed_job;
 
 static void packed_rows(const packed_job *g) {
-    int64_t rb = orc_row_bytes(g->cols);
+    int64_t rb = packed_row_bytes(g->cols, g->bits);
     for (int64_t m = g->m0; m < g->m1; ++m) {
         for (int64_t r = 0; r < g->rows; ++r) {
             const uint8_t *row = g->codes + r * rb;
             double s = orc_half_to_double(g->scales[r]);
             double acc = 0.0, abs_acc = 0.0;
             for (int64_t k = 0; k < g->cols; ++k) {
-                double w = (double)g->codebook[orc_code2(row, k)];
+                double w = (double)g->codebook[packed_code(row, k, g->bits)];
                 double x = orc_half_to_double(g->X[m * g->cols + k]);
                 double p = s * w * x;
                 acc += p;
@@ -226,20 +270,20 @@ static void *packed_thread(void *arg) {
 
 /* Y and T are M x rows, row-major.  Threads split the M rows of X when M > 1,
  * otherwise the weight rows. */
-void orc_packed_gemm(const uint8_t *codes, const uint16_t *scales, const uint16_t *X,
-                     int64_t M, int64_t rows, int64_t cols, const float *codebook,
-                     double *Y, double *T, int nthreads) {
+static void packed_gemm_bits(const uint8_t *codes, const uint16_t *scales, const uint16_t *X,
+                             int64_t M, int64_t rows, int64_t cols, const float *codebook,
+                             double *Y, double *T, int nthreads, int bits) {
     if (nthreads < 1) nthreads = 1;
     if (M == 1) {
         /* split weight rows: each thread sees a slice of the matrix */
         if (nthreads > rows) nthreads = (int)(rows > 0 ? rows : 1);
         packed_job *jobs = (packed_job *)calloc((size_t)nthreads, sizeof(packed_job));
         pthread_t *th = (pthread_t *)calloc((size_t)nthreads, sizeof(pthread_t));
-        int64_t rb = orc_row_bytes(cols);
+        int64_t rb = packed_row_bytes(cols, bits);
         for (int t = 0; t < nthreads; ++t) {
             int64_t r0 = rows * t / nthreads, r1 = rows * (t + 1) / nthreads;
             packed_job g = {codes + r0 * rb, scales + r0, X, 1, r1 - r0, cols, codebook,
-                            Y + r0, T + r0, 0, 1};
+                            Y + r0, T + r0, 0, 1, bits};
             jobs[t] = g;
         }
         for (int t = 1; t < nthreads; ++t) pthread_create(&th[t], NULL, packed_thread, &jobs[t]);
@@ -254,7 +298,7 @@ void orc_packed_gemm(const uint8_t *codes, const uint16_t *scales, const uint16_
     pthread_t *th = (pthread_t *)calloc((size_t)nthreads, sizeof(pthread_t));
     for (int t = 0; t < nthreads; ++t) {
         packed_job g = {codes, scales, X, M, rows, cols, codebook, Y, T,
-                        M * t / nthreads, M * (t + 1) / nthreads};
+                        M * t / nthreads, M * (t + 1) / nthreads, bits};
         jobs[t] = g;
     }
     for (int t = 1; t < nthreads; ++t) pthread_create(&th[t], NULL, packed_thread, &jobs[t]);
@@ -264,17 +308,30 @@ void orc_packed_gemm(const uint8_t *codes, const uint16_t *scales, const uint16_
     free(th);
 }
 
+void orc_packed_gemm(const uint8_t *codes, const uint16_t *scales, const uint16_t *X,
+                     int64_t M, int64_t rows, int64_t cols, const float *codebook,
+                     double *Y, double *T, int nthreads) {
+    packed_gemm_bits(codes, scales, X, M, rows, cols, codebook, Y, T, nthreads, 2);
+}
+
+/* 4-bit codes, 16-entry codebook */
+void orc_packed4_gemm(const uint8_t *codes, const uint16_t *scales, const uint16_t *X,
+                      int64_t M, int64_t rows, int64_t cols, const float *codebook,
+                      double *Y, double *T, int nthreads) {
+    packed_gemm_bits(codes, scales, X, M, rows, cols, codebook, Y, T, nthreads, 4);
+}
+
 /* Selected outputs only: Y[n] = Y(mm[n], rr[n]). */
-void orc_packed_gemm_at(const uint8_t *codes, const uint16_t *scales, const uint16_t *X,
-                        int64_t cols, const float *codebook,
-                        int64_t n, const int64_t *mm, const int64_t *rr, double *Y, double *T) {
-    int64_t rb = orc_row_bytes(cols);
+static void packed_gemm_at_bits(const uint8_t *codes, const uint16_t *scales, const uint16_t *X,
+                                int64_t cols, const float *codebook, int64_t n, const int64_t *mm,
+                                const int64_t *rr, double *Y, double *T, int bits) {
+    int64_t rb = packed_row_bytes(cols, bits);
     for (int64_t q = 0; q < n; ++q) {
         const uint8_t *row = codes + rr[q] * rb;
         double s = orc_half_to_double(scales[rr[q]]);
         double acc = 0.0, abs_acc = 0.0;
         for (int64_t k = 0; k < cols; ++k) {
-            double p = s * (double)codebook[orc_code2(row, k)] *
+            double p = s * (double)codebook[packed_code(row, k, bits)] *
                        orc_half_to_double(X[mm[q] * cols + k]);
             acc += p;
             abs_acc += fabs(p);
@@ -282,4 +339,16 @@ void orc_packed_gemm_at(const uint8_t *codes, const uint16_t *scales, const uint
         Y[q] = acc;
         T[q] = abs_acc;
     }
+}
+
+void orc_packed_gemm_at(const uint8_t *codes, const uint16_t *scales, const uint16_t *X,
+                        int64_t cols, const float *codebook,
+                        int64_t n, const int64_t *mm, const int64_t *rr, double *Y, double *T) {
+    packed_gemm_at_bits(codes, scales, X, cols, codebook, n, mm, rr, Y, T, 2);
+}
+
+void orc_packed4_gemm_at(const uint8_t *codes, const uint16_t *scales, const uint16_t *X,
+                         int64_t cols, const float *codebook,
+                         int64_t n, const int64_t *mm, const int64_t *rr, double *Y, double *T) {
+    packed_gemm_at_bits(codes, scales, X, cols, codebook, n, mm, rr, Y, T, 4);
 }

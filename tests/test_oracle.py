@@ -214,8 +214,8 @@ def test_gemm_fp32_products_exact(oracle):
 
 # ---------------------------------------------------------------- packed
 
-def _packed_hand():
-    lines = read_golden("packed_2x6_hand.txt")
+def _packed_hand(name="packed_2x6_hand.txt"):
+    lines = read_golden(name)
     d, cur = {}, None
     for ln in lines:
         tok = ln.split()
@@ -302,3 +302,121 @@ def test_packed_ternary_codebook(oracle):
                               synth.CODEBOOK_TERNARY)
     assert y[0].tolist() == [-1 * 1 + 0 * 2 + 1 * 3 + -1 * 4, 0.0]
     assert T[0].tolist() == [1 + 0 + 3 + 4, 0.0]
+
+
+# ---------------------------------------------------------------- 4-bit form
+
+def test_unpack4_hand_table(oracle):
+    for ln in read_golden("unpack4_bytes.txt"):
+        parts = ln.split()
+        byte = int(parts[0], 16)
+        want = [int(v) for v in parts[1:3]]
+        got = oracle.unpack4(np.array([byte], np.uint8), 1, 2)[0].tolist()
+        assert got == want, (hex(byte), got, want)
+
+
+def test_pack4_unpack4_roundtrip_all_bytes(oracle):
+    allb = np.arange(256, dtype=np.uint8).reshape(32, 8)       # 32 rows x 16 cols
+    fields = oracle.unpack4(allb, 32, 16)
+    assert fields.max() <= 15
+    assert np.array_equal(oracle.pack4(fields), allb)
+
+
+@pytest.mark.parametrize("rows,cols", [(1, 1), (3, 5), (7, 63), (5, 64), (2, 131)])
+def test_unpack4_pack4_roundtrip_ragged(oracle, rows, cols):
+    rng = np.random.default_rng(rows * 999 + cols)
+    fields = rng.integers(0, 16, size=(rows, cols), dtype=np.uint8)
+    packed = oracle.pack4(fields)
+    assert packed.shape == (rows, (cols + 1) // 2)
+    assert np.array_equal(oracle.unpack4(packed, rows, cols), fields)
+    dirty = packed.copy()
+    if cols % 2:
+        dirty[:, -1] |= np.uint8(0xF0)   # the unused high nibble is ignored
+    assert np.array_equal(oracle.unpack4(dirty, rows, cols), fields)
+
+
+def test_packed4_hand_2x5(oracle):
+    d = _packed_hand("packed4_2x5_hand.txt")
+    cols = int(d["cols"][0])
+    cb = np.array([float(v) for v in d["codebook"]], np.float32)
+    codes = np.array([[int(v, 16) for v in row] for row in d["codes"]], np.uint8)
+    scales = np.array([int(v, 16) for v in d["scales_fp16"][0]], np.uint16)
+    x = np.array([int(v, 16) for v in d["x_fp16"][0]], np.uint16)
+    y, T = oracle.packed4_gemm(codes, scales, x, 2, cols, cb)
+    assert y[0].tolist() == [float(v) for v in d["y"][0]]
+    assert T[0].tolist() == [float(v) for v in d["T"][0]]
+    ys, Ts = oracle.packed4_gemm_at(codes, scales, x, cols, cb, [0, 0], [1, 0])
+    assert ys.tolist() == [y[0, 1], y[0, 0]] and Ts.tolist() == [T[0, 1], T[0, 0]]
+
+
+@pytest.mark.parametrize("M,rows,cols", [(1, 37, 64), (1, 9, 1537), (4, 33, 771), (3, 1, 1)])
+def test_packed4_equals_dense_on_decoded_weights(oracle, M, rows, cols):
+    # dyadic codebook (c - 7) / 4: entry x fp16 scale is exact in fp32, so the dense
+    # oracle on the decoded weights must give the same sums
+    seed = M * 7919 + rows * 13 + cols
+    codes = synth.random_bytes(seed, rows * ((cols + 1) // 2)).reshape(rows, -1)
+    scales = synth.uniform_f16_bits(seed + 1, (rows,), 0.005, 0.05)
+    X = synth.normal_f16_bits(seed + 2, (M, cols))
+    cb = ((np.arange(16) - 7) / 4.0).astype(np.float32)
+    Y, T = oracle.packed4_gemm(codes, scales, X, rows, cols, cb, threads=2)
+    fields = oracle.unpack4(codes, rows, cols)
+    W = (cb[fields] * scales.view(np.float16).astype(np.float32)[:, None]).astype(np.float32)
+    Xf = X.view(np.float16).astype(np.float32)
+    C, TC = oracle.gemm(0, 1, M, rows, cols, Xf, W)
+    assert np.array_equal(Y, C)
+    assert np.array_equal(T, TC)
+
+
+def test_packed4_constant_field_rows(oracle):
+    # a row whose fields are all c gives y = scale * cb[c] * sum_k x_k
+    rows, cols = 16, 30
+    codes = np.array([[c * 0x11] * 15 for c in range(16)], np.uint8)
+    scales = np.full(rows, 0x3800, np.uint16)                          # 0.5
+    x = (np.arange(cols) - 11).astype(np.float16).view(np.uint16)      # exact small ints
+    cb = ((np.arange(16) - 7) / 8.0).astype(np.float32)
+    y, T = oracle.packed4_gemm(codes, scales, x, rows, cols, cb)
+    sx = float(np.sum(np.arange(cols) - 11))
+    sax = float(np.sum(np.abs(np.arange(cols) - 11)))
+    assert y[0].tolist() == [0.5 * float(cb[c]) * sx for c in range(16)]
+    assert T[0].tolist() == [abs(0.5 * float(cb[c])) * sax for c in range(16)]
+
+
+def test_packed4_one_hot_reads_single_field(oracle):
+    table = [ln.split() for ln in read_golden("unpack4_bytes.txt")]
+    codes = np.array([[int(t[0], 16)] for t in table], np.uint8)
+    rows = len(table)
+    scales = np.full(rows, 0x3400, np.uint16)   # 0.25
+    cb = synth.CODEBOOK_NQ4
+    for k in range(2):
+        x = np.zeros(2, np.uint16); x[k] = 0x3C00
+        y, _ = oracle.packed4_gemm(codes, scales, x, rows, 2, cb)
+        assert y[0].tolist() == [0.25 * float(cb[int(t[1 + k])]) for t in table]
+
+
+def test_packed4_agrees_with_packed2_on_small_fields(oracle):
+    # fields below 4 stored in 4 bits, with the 2-bit codebook in entries 0..3, give the
+    # 2-bit sums of the same fields (cross-format check of the nibble and field readings)
+    rows, cols = 23, 301
+    rng = np.random.default_rng(5)
+    fields = rng.integers(0, 4, size=(rows, cols), dtype=np.uint8)
+    scales = synth.uniform_f16_bits(6, (rows,), 0.005, 0.05)
+    x = synth.normal_f16_bits(7, (cols,))
+    cb4 = np.concatenate([synth.CODEBOOK_2BIT, np.full(12, 99.0, np.float32)])
+    y4, T4 = oracle.packed4_gemm(oracle.pack4(fields), scales, x, rows, cols, cb4)
+    y2, T2 = oracle.packed_gemm(oracle.pack2(fields), scales, x, rows, cols, synth.CODEBOOK_2BIT)
+    assert np.array_equal(y4, y2) and np.array_equal(T4, T2)
+
+
+def test_normal_quantile_codebook():
+    # the quantile function against textbook values of the standard normal
+    assert synth._normal_ppf(0.5) == pytest.approx(0.0, abs=1e-14)
+    assert synth._normal_ppf(0.975) == pytest.approx(1.959963984540054, abs=1e-12)
+    assert synth._normal_ppf(0.8413447460685429) == pytest.approx(1.0, abs=1e-12)   # Phi(1)
+    assert synth._normal_ppf(0.02) == pytest.approx(-synth._normal_ppf(0.98), abs=1e-12)
+    cb = synth.CODEBOOK_NQ4
+    assert cb.dtype == np.float32 and cb.size == 16
+    assert np.all(np.diff(cb) > 0)
+    assert cb[0] == -1.0 and cb[7] == 0.0 and cb[15] == 1.0
+    top = synth._normal_ppf(0.98)
+    for i in range(1, 9):
+        assert cb[7 + i] == np.float32(synth._normal_ppf(0.5 + 0.48 * i / 8) / top)
