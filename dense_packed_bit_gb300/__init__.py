@@ -1,4 +1,5 @@
-"""dense_packed_bit_gb300 -- fp32 dense GEMM and packed 2-bit GEMV / skinny GEMM on GB300.
+"""dense_packed_bit_gb300 -- fp32 dense GEMM, packed 2-bit GEMV / skinny GEMM and packed
+4-bit GEMV on GB300.
 
 Thin ctypes binding over libmm.so (the C ABI declared in include/mm.h).  The
 functions keep the C names and argument order; tensors are torch CUDA tensors
@@ -16,7 +17,8 @@ import threading
 __all__ = [
     "MMError", "load_library", "library_path", "mm_version", "mm_last_error",
     "mm_gemm_f32", "mm_gemm_f32_ex", "mm_gemv_packed2", "mm_gemv_packed2_ex",
-    "mm_gemm_packed2", "mm_gemm_packed2_ex", "mm_check_device_error",
+    "mm_gemm_packed2", "mm_gemm_packed2_ex", "mm_gemv_packed4", "mm_gemv_packed4_ex",
+    "mm_check_device_error",
     "MM_OK", "MM_ERR_INVALID_ARG", "MM_ERR_UNSUPPORTED", "MM_ERR_CUDA", "MM_ERR_TIMEOUT",
     "MM_GEMM_AUTO", "MM_GEMM_FFMA", "MM_GEMM_TF32X3",
     "MM_DEQ_AUTO", "MM_DEQ_SELECT", "MM_DEQ_AFFINE", "MM_DEQ_MMA", "MM_DEQ_FP8", "MM_DEQ_TC",
@@ -48,6 +50,11 @@ class GemmPacked2Opts(ctypes.Structure):
     _fields_ = [("tile", ctypes.c_int), ("splitk", ctypes.c_int), ("reserved", ctypes.c_int * 6)]
 
 
+class Gemv4Opts(ctypes.Structure):
+    _fields_ = [("blocks", ctypes.c_int), ("pdl", ctypes.c_int), ("weights_static", ctypes.c_int),
+                ("independent", ctypes.c_int), ("staging", ctypes.c_int), ("reserved", ctypes.c_int * 3)]
+
+
 SIGNATURES = {
     "mm_version": ([], ctypes.c_int),
     "mm_last_error": ([], ctypes.c_char_p),
@@ -57,6 +64,8 @@ SIGNATURES = {
     "mm_gemv_packed2": ([_P, _P, _P, _P, _I64, _I64, _P, _P], ctypes.c_int),
     "mm_gemv_packed2_ex": ([_P, _P, _P, _P, _I64, _I64, _P, _P, ctypes.POINTER(GemvOpts)], ctypes.c_int),
     "mm_gemm_packed2": ([_P, _P, _P, _P, _I64, _I64, _I64, _P, _P], ctypes.c_int),
+    "mm_gemv_packed4": ([_P, _P, _P, _P, _I64, _I64, _P, _P], ctypes.c_int),
+    "mm_gemv_packed4_ex": ([_P, _P, _P, _P, _I64, _I64, _P, _P, ctypes.POINTER(Gemv4Opts)], ctypes.c_int),
     "mm_gemm_packed2_ex": ([_P, _P, _P, _P, _I64, _I64, _I64, _P, _P, ctypes.POINTER(GemmPacked2Opts)],
                            ctypes.c_int),
     "mm_check_device_error": ([_P], ctypes.c_int),
@@ -108,13 +117,13 @@ def _stream(stream):
     return stream.cuda_stream
 
 
-def _codebook(cb):
+def _codebook(cb, n=4):
     if cb is None:
         return None
     vals = [float(v) for v in (cb.tolist() if hasattr(cb, "tolist") else cb)]
-    if len(vals) != 4:
-        raise ValueError("codebook needs 4 entries")
-    return (ctypes.c_float * 4)(*vals)
+    if len(vals) != n:
+        raise ValueError(f"codebook needs {n} entries")
+    return (ctypes.c_float * n)(*vals)
 
 
 def _check(status: int):
@@ -167,3 +176,15 @@ def mm_gemm_packed2_ex(codes, scales, X, Y, M, rows, cols, codebook, stream=None
 
 def mm_check_device_error(stream=None):
     _check(load_library().mm_check_device_error(_stream(stream)))
+
+
+def mm_gemv_packed4(codes, scales, x, y, rows, cols, codebook, stream=None):
+    _check(load_library().mm_gemv_packed4(_ptr(codes), _ptr(scales), _ptr(x), _ptr(y), rows, cols,
+                                          _codebook(codebook, 16), _stream(stream)))
+
+
+def mm_gemv_packed4_ex(codes, scales, x, y, rows, cols, codebook, stream=None, *, blocks=0, pdl=0,
+                       weights_static=0, independent=0, staging=-1):
+    o = Gemv4Opts(blocks, pdl, weights_static, independent, staging)
+    _check(load_library().mm_gemv_packed4_ex(_ptr(codes), _ptr(scales), _ptr(x), _ptr(y), rows, cols,
+                                             _codebook(codebook, 16), _stream(stream), ctypes.byref(o)))

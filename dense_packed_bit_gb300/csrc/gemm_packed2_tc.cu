@@ -113,7 +113,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     constexpr int TMEM_COLS = BN < 32 ? 32 : BN;
 
     extern __shared__ uint8_t smem_raw[];
-    uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint8_t *smem = smem_aligned<1024>(smem_raw);
     uint64_t *full = reinterpret_cast<uint64_t *>(smem + STAGES * L::STAGE_BYTES);
     uint64_t *done = full + STAGES;
     uint64_t *last = done + STAGES;

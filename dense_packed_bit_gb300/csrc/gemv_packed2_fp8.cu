@@ -152,7 +152,7 @@ __global__ void __launch_bounds__(512) gemv2_fp8_kernel(const __grid_constant__ 
                                                         const int prefetch, const int nblk, const int ring) {
     extern __shared__ uint8_t smem_raw[];
     __shared__ int s_fail;  // set by any thread whose bounded wait ran out; read after a barrier
-    uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint8_t *smem = smem_aligned<1024>(smem_raw);
     const int cols = (int)a.cols;
     const int KW = blockDim.x >> 5;  // warps = 256-field slabs
     const int nbox = cols >> 9;      // 128-byte boxes per row

@@ -73,7 +73,7 @@ __global__ void __launch_bounds__(NTHREADS) gemv2_rows_kernel(const __grid_const
                                                               const int ring) {
     extern __shared__ uint8_t smem_raw[];
     __shared__ int s_fail;  // set by a thread whose bounded wait ran out; read after a barrier
-    uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint8_t *smem = smem_aligned<1024>(smem_raw);
     constexpr int cols = 512 * CPW;
     constexpr int nbox = CPW;     // 128-byte boxes per row
     constexpr int stage_bytes = nbox * BOX;

@@ -193,7 +193,7 @@ __global__ void __launch_bounds__(NTHREADS) gemv2_tc_kernel(const __grid_constan
                                                            const int prefetch, const int tiles_per_cta,
                                                            const int bring) {
     extern __shared__ uint8_t smem_raw[];
-    uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint8_t *smem = smem_aligned<1024>(smem_raw);
     const int cols = (int)a.cols;
     const int nbox = cols >> 9;    // code boxes per tile
     const int nst = cols >> 7;     // 128-field stages per tile

@@ -44,7 +44,7 @@ constexpr int RING = 2;                              // 64-row blocks in flight 
 __global__ void __launch_bounds__(512) gemv2_tma_kernel(const __grid_constant__ CUtensorMap tmC, const PackedArgs a,
                                                         const int prefetch, const int nblk) {
     extern __shared__ uint8_t smem_raw[];
-    uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint8_t *smem = smem_aligned<1024>(smem_raw);
     const int KW = blockDim.x >> 5;       // warps = 256-field slabs = cols / 256
     const int nbox = (int)(a.cols >> 9);  // 128-byte boxes per row
     const int stage_bytes = nbox * BOX;

@@ -69,9 +69,9 @@ mm_status check_device() {
     return MM_OK;
 }
 
-mm_status check_codebook(const float *cb) {
+mm_status check_codebook(const float *cb, int n = 4) {
     if (!cb) return fail(MM_ERR_INVALID_ARG, "codebook is NULL");
-    for (int i = 0; i < 4; ++i)
+    for (int i = 0; i < n; ++i)
         if (!std::isfinite(cb[i])) return fail(MM_ERR_INVALID_ARG, "codebook[%d] is not finite", i);
     return MM_OK;
 }
@@ -89,6 +89,21 @@ mm_status check_packed(const uint8_t *codes, const uint16_t *scales, const uint1
     const uint64_t ybytes = (uint64_t)(M * rows * 4);
     if (overlap(y, ybytes, codes, (uint64_t)(rows * ((cols + 3) / 4))) || overlap(y, ybytes, scales, (uint64_t)rows * 2) ||
         overlap(y, ybytes, x, (uint64_t)(M * cols * 2)))
+        return fail(MM_ERR_INVALID_ARG, "output overlaps an input");
+    return MM_OK;
+}
+
+mm_status check_packed4(const uint8_t *codes, const uint16_t *scales, const uint16_t *x, const float *y,
+                        int64_t rows, int64_t cols, const float *cb) {
+    if (!codes || !scales || !x || !y) return fail(MM_ERR_INVALID_ARG, "NULL pointer argument");
+    if (rows < 1 || cols < 1)
+        return fail(MM_ERR_INVALID_ARG, "sizes must be >= 1 (rows=%lld cols=%lld)", (long long)rows, (long long)cols);
+    if (rows > ((int64_t)1 << 40) || cols > ((int64_t)1 << 40)) return fail(MM_ERR_INVALID_ARG, "sizes too large");
+    mm_status s = check_codebook(cb, 16);
+    if (s != MM_OK) return s;
+    const uint64_t ybytes = (uint64_t)(rows * 4);
+    if (overlap(y, ybytes, codes, (uint64_t)(rows * ((cols + 1) / 2))) || overlap(y, ybytes, scales, (uint64_t)rows * 2) ||
+        overlap(y, ybytes, x, (uint64_t)(cols * 2)))
         return fail(MM_ERR_INVALID_ARG, "output overlaps an input");
     return MM_OK;
 }
@@ -279,6 +294,42 @@ mm_status mm_gemm_packed2(const uint8_t *codes, const uint16_t *scales, const ui
     return mm_gemm_packed2_ex(codes, scales, X, Y, M, rows, cols, codebook, stream, nullptr);
 }
 
+mm_status mm_gemv_packed4_ex(const uint8_t *codes, const uint16_t *scales, const uint16_t *x, float *y, int64_t rows,
+                             int64_t cols, const float codebook[16], mm_stream_t stream, const mm_gemv4_opts *opts) {
+    mm_status s = check_packed4(codes, scales, x, y, rows, cols, codebook);
+    if (s != MM_OK) return s;
+    mm::Gemv4Config cfg{1, 0, 0, -1, 0};
+    if (opts) {
+        cfg.pdl = opts->pdl;
+        cfg.weights_static = opts->weights_static;
+        cfg.independent = opts->independent;
+        cfg.staging = opts->staging;
+        cfg.blocks_per_cta = opts->blocks;
+    }
+    mm::Packed4Args a{codes, scales, x, y, rows, cols, {}};
+    for (int i = 0; i < 16; ++i) a.cb[i] = codebook[i];
+    if (cfg.staging < 0) cfg.staging = mm::gemv4_lut_supported(a) ? 1 : 0;
+    if (cfg.staging != 0 && cfg.staging != 1) return fail(MM_ERR_INVALID_ARG, "staging must be -1, 0 or 1");
+    if (cfg.staging && !mm::gemv4_lut_supported(a))
+        return fail(MM_ERR_INVALID_ARG, "the staged 4-bit kernel needs cols %% 256 == 0, cols <= 4096 and 16-byte aligned codes and x");
+    if (cfg.blocks_per_cta < 0 || cfg.blocks_per_cta > 64)
+        return fail(MM_ERR_INVALID_ARG, "blocks (64-row blocks per CTA) must be 0..64");
+    if (cfg.staging && !cfg.blocks_per_cta) cfg.blocks_per_cta = cfg.independent ? 2 : 1;
+    if (cfg.pdl != 0 && cfg.pdl != 1) return fail(MM_ERR_INVALID_ARG, "pdl must be 0 or 1");
+    if (cfg.weights_static != 0 && cfg.weights_static != 1) return fail(MM_ERR_INVALID_ARG, "weights_static must be 0 or 1");
+    if (cfg.independent != 0 && cfg.independent != 1) return fail(MM_ERR_INVALID_ARG, "independent must be 0 or 1");
+    s = check_device();
+    if (s != MM_OK) return s;
+    cudaError_t e = mm::launch_gemv_packed4(a, cfg, reinterpret_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "gemv4 launch");
+    return ok();
+}
+
+mm_status mm_gemv_packed4(const uint8_t *codes, const uint16_t *scales, const uint16_t *x, float *y, int64_t rows,
+                          int64_t cols, const float codebook[16], mm_stream_t stream) {
+    return mm_gemv_packed4_ex(codes, scales, x, y, rows, cols, codebook, stream, nullptr);
+}
+
 mm_status mm_check_device_error(mm_stream_t stream) {
     cudaError_t e;
     const unsigned int v = mm::gemm_ffma_take_device_error(reinterpret_cast<cudaStream_t>(stream), &e);
@@ -299,6 +350,9 @@ mm_status mm_check_device_error(mm_stream_t stream) {
     const unsigned int v2 = mm::gemv_rows_take_device_error(&e);
     if (e != cudaSuccess) return cuda_fail(e, "mm_check_device_error");
     if (v2 != 0) return fail(MM_ERR_TIMEOUT, "a bounded device wait ran out in the staged affine GEMV (code %u)", v2);
+    const unsigned int u4 = mm::gemv4_take_device_error(&e);
+    if (e != cudaSuccess) return cuda_fail(e, "mm_check_device_error");
+    if (u4 != 0) return fail(MM_ERR_TIMEOUT, "a bounded device wait ran out in the 4-bit GEMV (code %u)", u4);
     const unsigned int u = mm::gemv_tc_take_device_error(&e);
     if (e != cudaSuccess) return cuda_fail(e, "mm_check_device_error");
     if (u != 0) return fail(MM_ERR_TIMEOUT, "a bounded device wait ran out in the tcgen05 GEMV (code %u)", u);

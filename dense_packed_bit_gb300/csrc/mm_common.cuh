@@ -28,6 +28,16 @@ __device__ __forceinline__ uint32_t smem_u32(const void *p) {
     return static_cast<uint32_t>(__cvta_generic_to_shared(p));
 }
 
+// The dynamic shared-memory base rounded up to ALIGN bytes.  The result is formed
+// by pointer arithmetic on the shared array itself (not by a round trip through an
+// integer), so the compiler still knows every pointer derived from it addresses
+// shared memory and emits shared loads and stores with 32-bit addresses.
+template <int ALIGN>
+__device__ __forceinline__ uint8_t *smem_aligned(uint8_t *raw) {
+    const uint32_t a = smem_u32(raw);
+    return raw + ((ALIGN - (a & (ALIGN - 1))) & (ALIGN - 1));
+}
+
 __device__ __forceinline__ unsigned long long global_ns() {
     unsigned long long t;
     asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));

@@ -30,6 +30,28 @@ struct GemvConfig {
     int blocks_per_cta; // staging and fp8 decode: 64-row blocks each CTA streams through its TMA ring
 };
 
+// 4-bit packed GEMV: codes rows x ceil(cols/2) bytes (low nibble first), 16-entry codebook.
+struct Packed4Args {
+    const uint8_t *codes;
+    const uint16_t *scales;
+    const uint16_t *x;
+    float *y;
+    int64_t rows, cols;
+    float cb[16];
+};
+
+struct Gemv4Config {
+    int pdl;
+    int weights_static;
+    int independent;
+    int staging;         // 1 = TMA-staged table decode, 0 = generic kernel
+    int blocks_per_cta;  // staging: 64-row blocks each CTA streams through its TMA ring
+};
+
+bool gemv4_lut_supported(const Packed4Args &a);
+cudaError_t launch_gemv_packed4(const Packed4Args &a, const Gemv4Config &cfg, cudaStream_t s);
+unsigned int gemv4_take_device_error(cudaError_t *err);
+
 // True when cb[c] == cb[0] + c * (cb[1] - cb[0]) holds exactly in fp32 for c = 0..3.
 bool codebook_is_affine(const float cb[4]);
 

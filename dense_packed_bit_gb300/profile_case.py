@@ -3,6 +3,7 @@
     python -m dense_packed_bit_gb300.profile_case gemm --layout nn --size 2048 --reps 3
     python -m dense_packed_bit_gb300.profile_case gemv --reps 3 [--split 8 --rows 4 --warps 8 --dequant 2 --independent 1]
     python -m dense_packed_bit_gb300.profile_case gemv --reps 3 --split 0 --rows 1 --warps 0 --dequant 2 --staging 1
+    python -m dense_packed_bit_gb300.profile_case gemv4 --reps 3 [--staging 1 --independent 1]
     python -m dense_packed_bit_gb300.profile_case ternary --reps 1
 
 One warm-up launch precedes the `reps` launches.  No timing is done here:
@@ -16,7 +17,7 @@ import sys
 
 def main(argv=None):
     ap = argparse.ArgumentParser()
-    ap.add_argument("op", choices=["gemm", "gemv", "ternary"])
+    ap.add_argument("op", choices=["gemm", "gemv", "gemv4", "ternary"])
     ap.add_argument("--layout", default="nn", choices=["nn", "nt", "tn"])
     ap.add_argument("--size", type=int, default=2048)
     ap.add_argument("--path", type=int, default=0)
@@ -61,6 +62,18 @@ def main(argv=None):
                                   rows_per_lane=a.rows, warps=a.warps, dequant=a.dequant, pdl=a.pdl,
                                   weights_static=a.pdl and not a.independent, independent=a.independent,
                                   staging=a.staging)
+    elif a.op == "gemv4":
+        codes, scales = [], []
+        for i in range(a.matrices):
+            c = synth.gemv_4bit_12288x1536(i)
+            codes.append(torch.from_numpy(c.codes).to(dev))
+            scales.append(torch.from_numpy(c.scales).to(dev))
+        x = torch.from_numpy(c.X.reshape(-1)).to(dev)
+        y = torch.empty((a.matrices, 12288), dtype=torch.float32, device=dev)
+        for r in range(1 + a.reps):
+            i = r % a.matrices
+            mm.mm_gemv_packed4_ex(codes[i], scales[i], x, y[i], 12288, 1536, c.codebook, pdl=a.pdl,
+                                  independent=a.independent, staging=a.staging if a.staging else -1)
     else:
         layers = []
         for layer in range(16):

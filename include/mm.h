@@ -24,6 +24,11 @@
  *     rows ("More Stumbling...", the 16-layer ternary encoder on a 111-token
  *     input with 2 questions).
  *
+ *  3. Packed 4-bit weights times a vector (GEMV), the same formula with a
+ *     16-entry codebook: "Kernel 0112", section "What the kernel costs in a
+ *     whole token" (the model's 4-bit weight-reading kernels, the fastest the
+ *     pages measure) and "More Stumbling..." (the packed NF4 path).
+ *
  * Layouts (all row-major, all pointers DEVICE memory owned by the caller):
  *  - A: M x K (lda >= K), or K x M when transA (lda >= M).
  *  - B: K x N (ldb >= N), or N x K when transB (ldb >= K).
@@ -34,7 +39,11 @@
  *  - scales: rows fp16 values, passed as their uint16 bit patterns.
  *  - x / X: fp16 bit patterns, x has cols entries, X is M x cols.
  *  - y / Y: fp32, y has rows entries, Y is M x rows.
- *  - codebook: 4 fp32 values in HOST memory, read during the call.
+ *  - 4-bit codes: rows x ceil(cols/2) bytes; element k of a row is the field in
+ *    byte floor(k/2), bits 4*(k mod 2)..4*(k mod 2)+3 (low nibble first).  The
+ *    pages give no bit order; this is the 2-bit convention carried over.
+ *  - codebook: 4 (2-bit) or 16 (4-bit) fp32 values in HOST memory, read
+ *    during the call; every entry must be finite.
  *
  * Arithmetic: fp32 accumulation everywhere.  Every output satisfies
  * |y - y_exact| <= 1e-5 * sum_k |term_k|; decoding of 2-bit fields is exact.
@@ -42,9 +51,11 @@
  * Calls are asynchronous on `stream` (NULL = the legacy default stream); the
  * return code covers argument checks and launch errors only.  The library
  * keeps no pointer past a call and allocates no device memory in these calls.
- * Operands must not overlap the output.  Not thread-safe for concurrent calls
- * from several host threads (the last-error message is per thread; the
- * kernel-attribute and tensor-map caches are guarded by a mutex).
+ * Operands must not overlap the output.  Calls from several host threads may
+ * run concurrently: the library's shared state is one-time setup (kernel
+ * attributes, the device check, the driver entry point that encodes tensor
+ * maps) done under std::call_once or a mutex; tensor maps are encoded on the
+ * host in each call; the last-error message is per thread.
  *
  * Device-side waits are bounded: a wait that runs out sets a device error word
  * and the kernel returns early; mm_check_device_error() reports it as
@@ -214,6 +225,37 @@ mm_status mm_gemm_packed2_ex(const uint8_t *codes, const uint16_t *scales, const
                              float *Y, int64_t M, int64_t rows, int64_t cols,
                              const float codebook[4], mm_stream_t stream,
                              const mm_gemm_packed2_opts *opts);
+
+/* ------------------------------------------------------------------ 4-bit GEMV */
+
+/* y[r] = scale_r * sum_k codebook[field4(r, k)] * x[k], r < rows, k < cols.
+ * codes: rows x ceil(cols/2) bytes (low nibble first); scales: rows fp16; x: cols
+ * fp16; y: rows fp32; codebook: 16 fp32 values in host memory (any finite values,
+ * for example a normal-quantile (NF4-style) table).  fp32 products and
+ * accumulation, |y - y_exact| <= 1e-5 * sum_k |term_k|; decoding is exact.
+ * Errors: MM_ERR_INVALID_ARG for NULL pointers, sizes < 1, a non-finite codebook
+ * entry or an output overlapping an input; MM_ERR_UNSUPPORTED on a device other
+ * than sm_103; MM_ERR_CUDA for launch failures. */
+mm_status mm_gemv_packed4(const uint8_t *codes, const uint16_t *scales, const uint16_t *x, float *y,
+                          int64_t rows, int64_t cols, const float codebook[16], mm_stream_t stream);
+
+typedef struct {
+    int blocks;          /* staged kernel: 64-row blocks each CTA streams (1..64; 0 = 2 for
+                            independent calls, 1 otherwise) */
+    int pdl;             /* as in mm_gemv_opts */
+    int weights_static;  /* as in mm_gemv_opts */
+    int independent;     /* as in mm_gemv_opts */
+    int staging;         /* 1: code rows arrive in shared memory by TMA and each code byte
+                            indexes a shared-memory table of its two fields' fp32 entries
+                            (cols % 256 == 0, cols <= 4096, 16-byte aligned codes and x);
+                            0: the generic kernel (any shape); negative: automatic (1 when
+                            the shape allows, the default without options) */
+    int reserved[3];
+} mm_gemv4_opts;
+
+mm_status mm_gemv_packed4_ex(const uint8_t *codes, const uint16_t *scales, const uint16_t *x, float *y,
+                             int64_t rows, int64_t cols, const float codebook[16], mm_stream_t stream,
+                             const mm_gemv4_opts *opts);
 
 #ifdef __cplusplus
 }

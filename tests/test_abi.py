@@ -178,3 +178,40 @@ def test_gemv_bad_staging(lib, opt):
     st = lib.mm_gemv_packed2_ex(FAKE, FAKE + 0x100000, FAKE + 0x200000, FAKE + 0x300000, 64, 1536,
                                 _cb(-2, -1, 0, 1), None, ctypes.byref(o))
     assert st == mm.MM_ERR_INVALID_ARG
+
+
+def _cb16(*vals):
+    v = list(vals) + [0.0] * (16 - len(vals))
+    return (ctypes.c_float * 16)(*v)
+
+
+def test_header_lists_the_4bit_boundary():
+    names = header_functions()
+    assert "mm_gemv_packed4" in names and "mm_gemv_packed4_ex" in names
+
+
+@pytest.mark.parametrize("case", [
+    dict(codes=None), dict(scales=None), dict(x=None), dict(y=None), dict(rows=0), dict(cols=-3),
+    dict(cb="nan"), dict(cb=None), dict(y="overlap"),
+])
+def test_gemv4_argument_errors(lib, case):
+    a = dict(codes=FAKE, scales=FAKE + 0x100000, x=FAKE + 0x200000, y=FAKE + 0x300000, rows=64, cols=1536,
+             cb=_cb16(*range(16)))
+    a.update(case)
+    if a["cb"] == "nan":
+        a["cb"] = _cb16(*([0.0] * 12 + [float("nan")]))
+    if a["y"] == "overlap":
+        a["y"] = FAKE + 64
+    st = lib.mm_gemv_packed4(a["codes"], a["scales"], a["x"], a["y"], a["rows"], a["cols"], a["cb"], None)
+    assert st == mm.MM_ERR_INVALID_ARG, lib.mm_last_error()
+    assert lib.mm_last_error()
+
+
+@pytest.mark.parametrize("opt", [dict(staging=1, cols=1000), dict(staging=1, cols=8192), dict(staging=2),
+                                 dict(blocks=65), dict(blocks=-1), dict(pdl=2), dict(independent=3)])
+def test_gemv4_bad_options(lib, opt):
+    cols = opt.pop("cols", 1536)
+    o = mm.Gemv4Opts(**opt)
+    st = lib.mm_gemv_packed4_ex(FAKE, FAKE + 0x100000, FAKE + 0x200000, FAKE + 0x300000, 64, cols,
+                                _cb16(*range(16)), None, ctypes.byref(o))
+    assert st == mm.MM_ERR_INVALID_ARG, lib.mm_last_error()
