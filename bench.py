@@ -45,12 +45,14 @@ sys.path.insert(0, ROOT)
 METRIC = "2048³ fp32 GEMM TFLOP/s; 2-bit 12288×1536 GEMV weight GB/s vs HBM peak"
 GEMV_WEIGHT_BYTES = 12288 * 1536 // 4           # 4,718,592
 GEMV_TOTAL_BYTES = GEMV_WEIGHT_BYTES + 12288 * 2 + 1536 * 2 + 12288 * 4
+GEMV4_WEIGHT_BYTES = 12288 * 1536 // 2          # 9,437,184
+GEMV4_TOTAL_BYTES = GEMV4_WEIGHT_BYTES + 12288 * 2 + 1536 * 2 + 12288 * 4
 GEMM_FLOP = 2.0 * 2048 ** 3
 TERN_FLOP_PER_LAYER = 2 * (2.0 * 222 * 3072 * 768)
 N_GEMV = 64
 N_LAYERS = 16
 WORKLOAD = ("square_2048_fp32_gemm_nn_nt_tn + gemv2bit_12288x1536_rotation64 + "
-            "ternary_encoder_16x(222x768x3072,222x3072x768)")
+            "ternary_encoder_16x(222x768x3072,222x3072x768) + gemv4bit_12288x1536_rotation64")
 
 
 def parse_args(argv=None):
@@ -221,6 +223,15 @@ class Workload:
             self.gemv_cb = c.codebook
         self.gemv_x = torch.from_numpy(x.reshape(-1)).to(device)
         self.gemv_y = torch.empty((N_GEMV, 12288), dtype=torch.float32, device=device)
+        self.gemv4_codes, self.gemv4_scales = [], []
+        for i in range(N_GEMV):
+            c = synth.gemv_4bit_12288x1536(i + (off % 1000) * N_GEMV if off else i)
+            self.gemv4_codes.append(torch.from_numpy(c.codes).to(device))
+            self.gemv4_scales.append(torch.from_numpy(c.scales).to(device))
+            x4 = c.X
+            self.gemv4_cb = c.codebook
+        self.gemv4_x = torch.from_numpy(x4.reshape(-1)).to(device)
+        self.gemv4_y = torch.empty((N_GEMV, 12288), dtype=torch.float32, device=device)
         self.tern = []
         for layer in range(N_LAYERS):
             for proj in ("up", "down"):
@@ -236,6 +247,7 @@ class Workload:
 GEMV_INDEP = dict(dequant=2, staging=1, rows_per_lane=3, pdl=1, independent=1)
 GEMV_CHAINED = dict(split=3, rows_per_lane=2, warps=6, dequant=3, pdl=1, weights_static=1)
 GEMV_INDEP_STREAMS = 2  # independent calls alternate between two streams inside the graph
+GEMV4_INDEP = dict(staging=1, blocks=1, pdl=1, independent=1)
 
 
 def capture_phases(w: Workload, stream):
@@ -248,6 +260,7 @@ def capture_phases(w: Workload, stream):
     gemv_c : the same rotation as a dependent chain (each call waits for the previous
              kernel before reading x, only its weight loads start early)
     tern   : the 16-layer ternary encoder block (32 skinny GEMMs)
+    gemv4  : the 64-matrix rotation of 4-bit matrices as independent calls over two streams
     """
     import torch
     import dense_packed_bit_gb300 as mm
@@ -274,6 +287,15 @@ def capture_phases(w: Workload, stream):
                 cur.wait_stream(side)
         return f
 
+    def gemv4():
+        cur = torch.cuda.current_stream()
+        side.wait_stream(cur)
+        for i in range(N_GEMV):
+            st = side if i % 2 else cur
+            mm.mm_gemv_packed4_ex(w.gemv4_codes[i], w.gemv4_scales[i], w.gemv4_x, w.gemv4_y[i], 12288, 1536,
+                                  w.gemv4_cb, st, **GEMV4_INDEP)
+        cur.wait_stream(side)
+
     def tern():
         for t in w.tern:
             c = t["case"]
@@ -281,7 +303,7 @@ def capture_phases(w: Workload, stream):
 
     graphs = {}
     for name, fn in (("gemm", gemm), ("gemv", gemv(GEMV_INDEP, GEMV_INDEP_STREAMS)), ("gemv_c", gemv(GEMV_CHAINED)),
-                     ("tern", tern)):
+                     ("tern", tern), ("gemv4", gemv4)):
         with torch.cuda.stream(stream):
             fn()  # warm the kernels' one-time setup outside capture
         torch.cuda.synchronize()
@@ -292,13 +314,13 @@ def capture_phases(w: Workload, stream):
     return graphs
 
 
-LAUNCHES_PER_STEP = 3 + 2 * N_GEMV + 2 * N_LAYERS
+LAUNCHES_PER_STEP = 3 + 3 * N_GEMV + 2 * N_LAYERS
 
 
 def run_step(w: Workload, graphs, ev, stream):
     """One pass of the hot path; ev maps each phase to a (start, end) event pair."""
     w.flush.fill_(1.0)  # evict the GEMM operands from L2 (torch kernel, outside the events)
-    for name in ("gemm", "gemv", "gemv_c", "tern"):
+    for name in ("gemm", "gemv", "gemv_c", "tern", "gemv4"):
         ev[name][0].record(stream)
         graphs[name].replay()
         ev[name][1].record(stream)
@@ -307,7 +329,7 @@ def run_step(w: Workload, graphs, ev, stream):
 def new_events():
     import torch
     mk = lambda: (torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-    return {"gemm": mk(), "gemv": mk(), "gemv_c": mk(), "tern": mk()}
+    return {"gemm": mk(), "gemv": mk(), "gemv_c": mk(), "tern": mk(), "gemv4": mk()}
 
 
 def e2e_gemm(w: Workload, steps: int, stream):
@@ -459,6 +481,7 @@ def main_mm(args):
     gemv_total_s = total_s("gemv")
     gemvc_total_s = total_s("gemv_c")
     tern_total_s = total_s("tern")
+    gemv4_total_s = total_s("gemv4")
     wall = reduce_max(wall, dev)
 
     gemm_tflops = world * 3 * GEMM_FLOP * args.steps / gemm_total_s / 1e12
@@ -466,7 +489,8 @@ def main_mm(args):
     per_call_gemvc_s = gemvc_total_s / (args.steps * N_GEMV)
     gemv_gbs = world * GEMV_WEIGHT_BYTES / per_call_gemv_s / 1e9
     tern_tflops = world * N_LAYERS * TERN_FLOP_PER_LAYER * args.steps / tern_total_s / 1e12
-    step_ms = (gemm_total_s + gemv_total_s + gemvc_total_s + tern_total_s) / args.steps * 1e3
+    per_call_gemv4_s = gemv4_total_s / (args.steps * N_GEMV)
+    step_ms = (gemm_total_s + gemv_total_s + gemvc_total_s + tern_total_s + gemv4_total_s) / args.steps * 1e3
 
     peaks, peaks_src = measured_peaks()
     props = torch.cuda.get_device_properties(dev)
@@ -515,6 +539,15 @@ def main_mm(args):
                               "weight_frac": GEMV_WEIGHT_BYTES / per_call_gemv_s / 1e9 / peaks["hbm_gbs"],
                               "traffic": traffic_for("gemv2_vec"), "peak_source": peaks_src}},
         "ternary": {"value": tern_tflops, "unit": "TFLOP/s", "ms_per_block": tern_total_s / args.steps * 1e3},
+        "gemv4": {"metric": "4-bit 12288x1536 GEMV weight GB/s (normal-quantile 16-entry codebook)",
+                  "value": world * GEMV4_WEIGHT_BYTES / per_call_gemv4_s / 1e9, "unit": "GB/s",
+                  "us_per_call": per_call_gemv4_s * 1e6,
+                  "mode": "64 independent back-to-back calls over the rotation, two streams",
+                  "opts": GEMV4_INDEP,
+                  "roofline": {"bound": "hbm", "achieved": GEMV4_TOTAL_BYTES / per_call_gemv4_s / 1e9,
+                               "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                               "frac": GEMV4_TOTAL_BYTES / per_call_gemv4_s / 1e9 / peaks["hbm_gbs"],
+                               "traffic": traffic_for("gemv4_lut"), "peak_source": peaks_src}},
         "roofline": roof,
         "clocks": clk,
         "gpu_launches": LAUNCHES_PER_STEP * args.steps,

@@ -74,26 +74,28 @@ __global__ void __launch_bounds__(256) gemv4_generic_kernel(const Packed4Args a)
 
 constexpr int ROWS = 64;          // rows per block: one TMA box height
 constexpr int BOX = 128 * ROWS;   // bytes of one 128-byte-wide box of 64 rows
-constexpr int NWARPS = 8, NTHREADS = 32 * NWARPS;
+constexpr int NWARPS_MAX = 16;
 constexpr int RPL = ROWS / 32;    // rows per lane
-constexpr int LUT_BYTES = 256 * 16 * 8;
 
-// CPW = boxes per row = cols / 256 (each warp takes one 16-byte chunk of every box).
-template <int CPW>
-__global__ void __launch_bounds__(NTHREADS) gemv4_lut_kernel(const __grid_constant__ CUtensorMap tmC,
+// CPW = boxes per row = cols / 256; NW warps, warp w takes the 16-byte chunks c = w, w + NW, ...
+// of every row (chunk c is chunk c % 8 of box c / 8), CPW * 8 / NW of them.
+template <int CPW, int NW>
+__global__ void __launch_bounds__(32 * NW) gemv4_lut_kernel(const __grid_constant__ CUtensorMap tmC,
                                                              const Packed4Args a, const int prefetch, const int nblk,
                                                              const int ring) {
     extern __shared__ uint8_t smem_raw[];
+    // the byte table lives in static shared memory: its address is a link-time constant, so
+    // a lookup needs only the byte offset in a register (base folded into the load)
+    __shared__ __align__(128) float2 lut[256 * 16];  // [byte][lane % 16]
     __shared__ int s_fail;  // set by a thread whose bounded wait ran out; read after a barrier
     __shared__ float cbs[16];
     uint8_t *smem = smem_aligned<1024>(smem_raw);
     constexpr int cols = 256 * CPW;
     constexpr int stage_bytes = CPW * BOX;
     uint8_t *tiles = smem;                                                         // [ring][CPW][64 rows][128 B]
-    float2 *lut = reinterpret_cast<float2 *>(smem + (size_t)ring * stage_bytes);  // [256 bytes][16 lanes]
-    float4 *xs = reinterpret_cast<float4 *>(reinterpret_cast<uint8_t *>(lut) + LUT_BYTES);  // cols floats
-    float *red = reinterpret_cast<float *>(xs + cols / 4);                                   // [NWARPS][ROWS]
-    uint64_t *full = reinterpret_cast<uint64_t *>(red + NWARPS * ROWS);
+    float4 *xs = reinterpret_cast<float4 *>(smem + (size_t)ring * stage_bytes);  // cols floats
+    float *red = reinterpret_cast<float *>(xs + cols / 4);                                   // [NW][ROWS]
+    uint64_t *full = reinterpret_cast<uint64_t *>(red + NW * ROWS);
 
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int blk0 = blockIdx.x * nblk;
@@ -132,12 +134,12 @@ __global__ void __launch_bounds__(NTHREADS) gemv4_lut_kernel(const __grid_consta
     }
 
     // ---- byte -> (entry of the low field, entry of the high field), one copy per half-warp lane
-    for (int e = threadIdx.x; e < 256 * 16; e += NTHREADS) {
+    for (int e = threadIdx.x; e < 256 * 16; e += 32 * NW) {
         const int b = e >> 4;
         lut[e] = make_float2(cbs[b & 15], cbs[b >> 4]);
     }
     // ---- x -> fp32 in shared memory
-    for (int g = threadIdx.x; g < cols / 8; g += NTHREADS) {
+    for (int g = threadIdx.x; g < cols / 8; g += 32 * NW) {
         const uint4 hv = __ldg(reinterpret_cast<const uint4 *>(a.x) + g);
         const uint32_t hw[4] = {hv.x, hv.y, hv.z, hv.w};
         float v[8];
@@ -148,7 +150,8 @@ __global__ void __launch_bounds__(NTHREADS) gemv4_lut_kernel(const __grid_consta
     }
     __syncthreads();
 
-    const float2 *lut_lane = lut + (lane & 15);
+    const uint32_t lane_off = (uint32_t)(lane & 15) * 8u;  // byte offset of this lane's copy of an entry
+    const uint8_t *lut_bytes = reinterpret_cast<const uint8_t *>(lut);
     bool ok = true;
     int waited = 0;
     for (int i = 0; i < my_blocks && ok; ++i) {
@@ -167,13 +170,14 @@ __global__ void __launch_bounds__(NTHREADS) gemv4_lut_kernel(const __grid_consta
 #pragma unroll
         for (int j = 0; j < RPL; ++j) acc[j][0] = acc[j][1] = make_float2(0.f, 0.f);
 #pragma unroll
-        for (int m = 0; m < CPW; ++m) {
-            // chunk m * 8 + warp: 16 bytes = 32 fields of rows lane + 32 j (row % 8 == lane % 8)
-            const uint8_t *bp = tile + m * BOX + ((warp ^ (lane & 7)) << 4);
+        for (int m = 0; m < CPW * 8 / NW; ++m) {
+            // chunk c = warp + NW m: 16 bytes = 32 fields of rows lane + 32 j (row % 8 == lane % 8)
+            const int c = warp + NW * m;
+            const uint8_t *bp = tile + (c >> 3) * BOX + (((c & 7) ^ (lane & 7)) << 4);
             uint4 q[RPL];
 #pragma unroll
             for (int j = 0; j < RPL; ++j) q[j] = *reinterpret_cast<const uint4 *>(bp + (lane + 32 * j) * 128);
-            const float4 *xp = xs + (m * 8 + warp) * 8;
+            const float4 *xp = xs + c * 8;
 #pragma unroll
             for (int wd = 0; wd < 4; ++wd) {
                 const float4 xa = xp[2 * wd], xb = xp[2 * wd + 1];  // fields 8 wd .. 8 wd + 7 of the chunk
@@ -183,8 +187,14 @@ __global__ void __launch_bounds__(NTHREADS) gemv4_lut_kernel(const __grid_consta
 #pragma unroll
                 for (int j = 0; j < RPL; ++j) {
                     const uint32_t w = wd == 0 ? q[j].x : wd == 1 ? q[j].y : wd == 2 ? q[j].z : q[j].w;
+                    // byte k of w times 128 (the entry stride), or'ed with the lane's offset: bits 7..14
+                    // hold the byte and bits 3..6 the lane, so the sum is a bitwise or
 #pragma unroll
-                    for (int k = 0; k < 4; ++k) e[j][k] = lut_lane[((w >> (8 * k)) & 0xFFu) * 16];
+                    for (int k = 0; k < 4; ++k) {
+                        const uint32_t sh = k == 0 ? (w << 7) : (w >> (8 * k - 7));
+                        const uint32_t off = (sh & 0x7F80u) | lane_off;
+                        e[j][k] = *reinterpret_cast<const float2 *>(lut_bytes + off);
+                    }
                 }
 #pragma unroll
                 for (int j = 0; j < RPL; ++j)
@@ -202,7 +212,7 @@ __global__ void __launch_bounds__(NTHREADS) gemv4_lut_kernel(const __grid_consta
         if (leader && i + ring < my_blocks) issue(i + ring);
         if (threadIdx.x < ROWS) {
             float s = red[threadIdx.x];
-            for (int k = 1; k < NWARPS; ++k) s += red[k * ROWS + threadIdx.x];
+            for (int k = 1; k < NW; ++k) s += red[k * ROWS + threadIdx.x];
             if (row < a.rows) a.y[row] = scl * s;
         }
         __syncthreads();  // the next block may overwrite the partial sums
@@ -215,15 +225,26 @@ __global__ void __launch_bounds__(NTHREADS) gemv4_lut_kernel(const __grid_consta
     }
 }
 
+// dynamic shared memory (the 32 KiB byte table is static)
 size_t lut_smem_bytes(int64_t cols, int ring) {
-    return 1024 + (size_t)ring * (size_t)(cols / 256) * BOX + LUT_BYTES + (size_t)cols * 4 + NWARPS * ROWS * 4 +
+    return 1024 + (size_t)ring * (size_t)(cols / 256) * BOX + (size_t)cols * 4 + NWARPS_MAX * ROWS * 4 +
            (size_t)ring * 8;
 }
 
+// 16 warps when the chunks split evenly over them (an even number of boxes), else 8
 template <int CPW>
 cudaError_t launch_lut(cudaLaunchConfig_t &lc, const CUtensorMap &tm, const Packed4Args &a, int prefetch, int nblk,
                        int ring) {
-    return cudaLaunchKernelEx(&lc, gemv4_lut_kernel<CPW>, tm, a, prefetch, nblk, ring);
+    static std::once_flag once;
+    static cudaError_t attr_err = cudaSuccess;
+    constexpr int NW = (CPW % 2 == 0) ? 16 : 8;
+    std::call_once(once, [&] {
+        attr_err = cudaFuncSetAttribute(gemv4_lut_kernel<CPW, NW>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                        160 * 1024);
+    });
+    if (attr_err != cudaSuccess) return attr_err;
+    lc.blockDim = dim3(32 * NW);
+    return cudaLaunchKernelEx(&lc, gemv4_lut_kernel<CPW, NW>, tm, a, prefetch, nblk, ring);
 }
 
 }  // namespace
@@ -252,29 +273,12 @@ cudaError_t launch_gemv_packed4(const Packed4Args &a, const Gemv4Config &cfg, cu
     cudaError_t e = make_tmap_2d(&tm, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, a.codes, (uint64_t)rowbytes, (uint64_t)a.rows,
                                  (uint64_t)rowbytes, 128, ROWS, CU_TENSOR_MAP_SWIZZLE_128B);
     if (e != cudaSuccess) return e;
-    static std::once_flag once;
-    static cudaError_t attr_err = cudaSuccess;
-    std::call_once(once, [&] {
-        const void *fns[16] = {(const void *)gemv4_lut_kernel<1>,  (const void *)gemv4_lut_kernel<2>,
-                               (const void *)gemv4_lut_kernel<3>,  (const void *)gemv4_lut_kernel<4>,
-                               (const void *)gemv4_lut_kernel<5>,  (const void *)gemv4_lut_kernel<6>,
-                               (const void *)gemv4_lut_kernel<7>,  (const void *)gemv4_lut_kernel<8>,
-                               (const void *)gemv4_lut_kernel<9>,  (const void *)gemv4_lut_kernel<10>,
-                               (const void *)gemv4_lut_kernel<11>, (const void *)gemv4_lut_kernel<12>,
-                               (const void *)gemv4_lut_kernel<13>, (const void *)gemv4_lut_kernel<14>,
-                               (const void *)gemv4_lut_kernel<15>, (const void *)gemv4_lut_kernel<16>};
-        for (const void *f : fns)
-            if (attr_err == cudaSuccess)
-                attr_err = cudaFuncSetAttribute(f, cudaFuncAttributeMaxDynamicSharedMemorySize, 200 * 1024);
-    });
-    if (attr_err != cudaSuccess) return attr_err;
     const int nblk = cfg.blocks_per_cta > 0 ? cfg.blocks_per_cta : 1;
     int ring = nblk >= 2 ? 2 : 1;
-    if (lut_smem_bytes(a.cols, ring) > 200 * 1024) ring = 1;
+    if (lut_smem_bytes(a.cols, ring) > 160 * 1024) ring = 1;
     const int64_t nrowblk = (a.rows + ROWS - 1) / ROWS;
     cudaLaunchConfig_t lc = {};
     lc.gridDim = dim3((unsigned)((nrowblk + nblk - 1) / nblk));
-    lc.blockDim = dim3(NTHREADS);
     lc.dynamicSmemBytes = lut_smem_bytes(a.cols, ring);
     lc.stream = st;
     lc.attrs = attr;

@@ -3,7 +3,7 @@
     python -m dense_packed_bit_gb300.profile_case gemm --layout nn --size 2048 --reps 3
     python -m dense_packed_bit_gb300.profile_case gemv --reps 3 [--split 8 --rows 4 --warps 8 --dequant 2 --independent 1]
     python -m dense_packed_bit_gb300.profile_case gemv --reps 3 --split 0 --rows 1 --warps 0 --dequant 2 --staging 1
-    python -m dense_packed_bit_gb300.profile_case gemv4 --reps 3 [--staging 1 --independent 1]
+    python -m dense_packed_bit_gb300.profile_case gemv4 --reps 3 [--staging 1 --rows 1 --independent 1]
     python -m dense_packed_bit_gb300.profile_case ternary --reps 1
 
 One warm-up launch precedes the `reps` launches.  No timing is done here:
@@ -73,7 +73,8 @@ def main(argv=None):
         for r in range(1 + a.reps):
             i = r % a.matrices
             mm.mm_gemv_packed4_ex(codes[i], scales[i], x, y[i], 12288, 1536, c.codebook, pdl=a.pdl,
-                                  independent=a.independent, staging=a.staging if a.staging else -1)
+                                  independent=a.independent, staging=a.staging if a.staging else -1,
+                                  blocks=a.rows if a.staging else 0)
     else:
         layers = []
         for layer in range(16):
