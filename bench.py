@@ -537,7 +537,7 @@ def main_mm(args):
                               "peak": peaks["hbm_gbs"], "unit": "GB/s",
                               "frac": GEMV_TOTAL_BYTES / per_call_gemv_s / 1e9 / peaks["hbm_gbs"],
                               "weight_frac": GEMV_WEIGHT_BYTES / per_call_gemv_s / 1e9 / peaks["hbm_gbs"],
-                              "traffic": traffic_for("gemv2_vec"), "peak_source": peaks_src}},
+                              "traffic": traffic_for("gemv2_rows"), "peak_source": peaks_src}},
         "ternary": {"value": tern_tflops, "unit": "TFLOP/s", "ms_per_block": tern_total_s / args.steps * 1e3},
         "gemv4": {"metric": "4-bit 12288x1536 GEMV weight GB/s (normal-quantile 16-entry codebook)",
                   "value": world * GEMV4_WEIGHT_BYTES / per_call_gemv4_s / 1e9, "unit": "GB/s",
