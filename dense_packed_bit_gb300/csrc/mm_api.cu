@@ -138,6 +138,9 @@ mm_status mm_gemm_f32_ex(int transA, int transB, int64_t M, int64_t N, int64_t K
         path = opts->path;
         if (path < MM_GEMM_AUTO || path > MM_GEMM_TF32X3) return fail(MM_ERR_INVALID_ARG, "unknown path %d", path);
     }
+    const int tile = opts ? opts->tile : 0;
+    if ((path == MM_GEMM_TF32X3 || path == MM_GEMM_AUTO) && (tile < 0 || tile > 2))
+        return fail(MM_ERR_INVALID_ARG, "3xTF32 tile must be 0 (automatic), 1 (two-stage) or 2 (warp-specialised)");
     mm_status s = check_device();
     if (s != MM_OK) return s;
 
@@ -147,7 +150,7 @@ mm_status mm_gemm_f32_ex(int transA, int transB, int64_t M, int64_t N, int64_t K
     if (path == MM_GEMM_TF32X3 && !mm::gemm_tf32x3_supported(g))
         return fail(MM_ERR_INVALID_ARG, "3xTF32 path needs 16-byte aligned A, B and lda, ldb multiples of 4");
     if ((path == MM_GEMM_TF32X3 || path == MM_GEMM_AUTO) && mm::gemm_tf32x3_supported(g))
-        e = mm::launch_gemm_tf32x3(g, st);
+        e = tile == 1 ? mm::launch_gemm_tf32x3(g, st) : mm::launch_gemm_tf32x3_ws(g, st);
     else if (mm::gemm_ffma_supported(g)) e = mm::launch_gemm_ffma(g, opts ? opts->tile : 0, st);
     else if (path == MM_GEMM_FFMA || path == MM_GEMM_AUTO) e = mm::launch_gemm_simple(g, st);
     else e = cudaErrorNotSupported;
@@ -341,6 +344,9 @@ mm_status mm_check_device_error(mm_stream_t stream) {
     const unsigned int z = mm::gemm_tf32x3_take_device_error(&e);
     if (e != cudaSuccess) return cuda_fail(e, "mm_check_device_error");
     if (z != 0) return fail(MM_ERR_TIMEOUT, "a bounded device wait ran out in the 3xTF32 GEMM (code %u)", z);
+    const unsigned int zw = mm::gemm_tf32x3_ws_take_device_error(&e);
+    if (e != cudaSuccess) return cuda_fail(e, "mm_check_device_error");
+    if (zw != 0) return fail(MM_ERR_TIMEOUT, "a bounded device wait ran out in the warp-specialised 3xTF32 GEMM (code %u)", zw);
     const unsigned int q = mm::gemv_tma_take_device_error(&e);
     if (e != cudaSuccess) return cuda_fail(e, "mm_check_device_error");
     if (q != 0) return fail(MM_ERR_TIMEOUT, "a bounded device wait ran out in the staged GEMV (code %u)", q);

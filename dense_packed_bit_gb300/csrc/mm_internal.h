@@ -114,12 +114,17 @@ cudaError_t launch_gemm_simple(const GemmArgs &g, cudaStream_t s);
 bool gemm_ffma_supported(const GemmArgs &g);
 cudaError_t launch_gemm_ffma(const GemmArgs &g, int tile, cudaStream_t s);
 
-// 3xTF32 tcgen05 kernel: same operand requirements as the FFMA TMA kernel.
+// 3xTF32 tcgen05 kernels: same operand requirements as the FFMA TMA kernel.
+// launch_gemm_tf32x3: one 128 x 128 tile per CTA, two stages, all threads split
+// and wait together; launch_gemm_tf32x3_ws: persistent, warp-specialised,
+// 128 x 256 tiles, raw tiles used as the hi operands.
 bool gemm_tf32x3_supported(const GemmArgs &g);
 cudaError_t launch_gemm_tf32x3(const GemmArgs &g, cudaStream_t s);
+cudaError_t launch_gemm_tf32x3_ws(const GemmArgs &g, cudaStream_t s);
 
 // Per translation unit device error words (read and cleared).
 unsigned int gemm_ffma_take_device_error(cudaStream_t s, cudaError_t *err);
 unsigned int gemm_tf32x3_take_device_error(cudaError_t *err);
+unsigned int gemm_tf32x3_ws_take_device_error(cudaError_t *err);
 
 }  // namespace mm

@@ -66,6 +66,24 @@ __device__ __forceinline__ uint64_t sdesc_kmajor_sw128(uint32_t smem_addr) {
     return d;
 }
 
+// Swizzle-mode codes of the shared-memory descriptor (bits 61-63).
+constexpr uint32_t kSdescSw128 = 2, kSdescSw64 = 4, kSdescSw32 = 6;
+
+// General shared-memory matrix descriptor: start address, leading and stride
+// byte offsets, swizzle mode.  For a K-major swizzled operand the stride byte
+// offset is the distance between 8-row groups along M/N and the leading one is
+// unused (encoded as 16 bytes).
+__device__ __forceinline__ uint64_t sdesc_make(uint32_t smem_addr, uint32_t lbo_bytes, uint32_t sbo_bytes,
+                                               uint32_t swizzle) {
+    uint64_t d = 0;
+    d |= (uint64_t)((smem_addr & 0x3FFFFu) >> 4);
+    d |= (uint64_t)((lbo_bytes >> 4) & 0x3FFFu) << 16;
+    d |= (uint64_t)((sbo_bytes >> 4) & 0x3FFFu) << 32;
+    d |= (uint64_t)1 << 46;
+    d |= (uint64_t)swizzle << 61;
+    return d;
+}
+
 // Instruction descriptor: D format in bits 4-5 (1 = f32), A and B formats in
 // bits 7-9 and 10-12 (kind::f16: 0 = f16, 1 = bf16; kind::tf32: 2 = tf32),
 // A / B major-ness in bits 15 / 16 (0 = K-major), N >> 3 in bits 17-22,
@@ -75,6 +93,7 @@ __host__ __device__ constexpr uint32_t make_idesc(uint32_t a_fmt, uint32_t b_fmt
 }
 
 constexpr uint32_t kFmtF16 = 0, kFmtBF16 = 1, kFmtTF32 = 2;
+
 
 // ---------------------------------------------------------------- MMA
 

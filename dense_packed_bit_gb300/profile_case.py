@@ -21,6 +21,7 @@ def main(argv=None):
     ap.add_argument("--layout", default="nn", choices=["nn", "nt", "tn"])
     ap.add_argument("--size", type=int, default=2048)
     ap.add_argument("--path", type=int, default=0)
+    ap.add_argument("--tile", type=int, default=0)
     ap.add_argument("--reps", type=int, default=3)
     ap.add_argument("--matrices", type=int, default=64)
     ap.add_argument("--split", type=int, default=8)
@@ -47,7 +48,7 @@ def main(argv=None):
         B = torch.from_numpy(synth.normal_f32(2, (n, n), 0.02)).to(dev)
         C = torch.empty((n, n), dtype=torch.float32, device=dev)
         for _ in range(1 + a.reps):
-            mm.mm_gemm_f32_ex(tA, tB, n, n, n, A, n, B, n, C, n, path=a.path)
+            mm.mm_gemm_f32_ex(tA, tB, n, n, n, A, n, B, n, C, n, path=a.path, tile=a.tile)
     elif a.op == "gemv":
         codes, scales = [], []
         for i in range(a.matrices):

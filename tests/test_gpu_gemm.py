@@ -24,13 +24,15 @@ def _lib():
     mm.load_library()
 
 
-def run(tA, tB, M, N, K, A, B, lda=None, ldb=None, ldc=None, path=mm.MM_GEMM_AUTO):
+def run(tA, tB, M, N, K, A, B, lda=None, ldb=None, ldc=None, path=mm.MM_GEMM_AUTO, tile=0):
+    if isinstance(path, tuple):
+        path, tile = path
     lda = lda or A.shape[1]
     ldb = ldb or B.shape[1]
     ldc = ldc or N
     dA, dB = to_dev(A), to_dev(B)
     dC = empty_f32((M, ldc))
-    mm.mm_gemm_f32_ex(tA, tB, M, N, K, dA, lda, dB, ldb, dC, ldc, path=path)
+    mm.mm_gemm_f32_ex(tA, tB, M, N, K, dA, lda, dB, ldb, dC, ldc, path=path, tile=tile)
     mm.mm_check_device_error()
     return to_host(dC)
 
@@ -48,7 +50,11 @@ def stored(tA, tB, M, N, K, seed, kind="normal"):
 SHAPES = [(1, 1, 1), (3, 17, 5), (65, 129, 33), (127, 63, 129), (200, 300, 97), (257, 130, 1000)]
 
 
-PATHS = {"auto": mm.MM_GEMM_AUTO, "ffma": mm.MM_GEMM_FFMA, "tf32x3": mm.MM_GEMM_TF32X3}
+# (path, tile): the 3xTF32 path has two kernels, the persistent warp-specialised one
+# (tile 2, the automatic choice) and the two-stage one (tile 1)
+PATHS = {"auto": (mm.MM_GEMM_AUTO, 0), "ffma": (mm.MM_GEMM_FFMA, 0), "tf32x3": (mm.MM_GEMM_TF32X3, 2),
+         "tf32x3_2stage": (mm.MM_GEMM_TF32X3, 1)}
+TC_PATHS = ("tf32x3", "tf32x3_2stage")
 
 
 @pytest.mark.parametrize("path", list(PATHS))
@@ -58,27 +64,28 @@ def test_gemm_ragged_shapes(oracle, layout, shape, path):
     tA, tB = LAYOUTS[layout]
     M, N, K = shape
     A, B = stored(tA, tB, M, N, K, seed=1000 * list(LAYOUTS).index(layout) + 7 * M + 3 * N + K)
-    if path == "tf32x3" and (A.shape[1] % 4 or B.shape[1] % 4):
+    if path in TC_PATHS and (A.shape[1] % 4 or B.shape[1] % 4):
         pytest.skip("3xTF32 path needs leading dimensions that are multiples of 4")
     C = run(tA, tB, M, N, K, A, B, path=PATHS[path])
     ref, T = oracle.gemm(tA, tB, M, N, K, A, B)
     check_bound(C, ref, T, f"{layout} {shape} {path}")
 
 
+@pytest.mark.parametrize("tile", [1, 2])
 @pytest.mark.parametrize("layout", list(LAYOUTS))
-@pytest.mark.parametrize("shape", [(128, 128, 32), (256, 384, 64), (130, 260, 100), (384, 128, 1000),
-                                   (64, 3072, 768)])
-def test_gemm_tf32x3_tiles(oracle, layout, shape):
+@pytest.mark.parametrize("shape", [(5, 7, 3), (128, 128, 32), (128, 256, 16), (256, 384, 64), (130, 260, 100),
+                                   (384, 128, 1000), (64, 3072, 768), (2000, 2900, 72)])
+def test_gemm_tf32x3_tiles(oracle, layout, shape, tile):
     # whole tiles, ragged tiles and K tails on the tensor-core path
     tA, tB = LAYOUTS[layout]
     M, N, K = shape
     A, B = stored(tA, tB, M, N, K, seed=17 + M + N + K)
     Ap = np.zeros((A.shape[0], (A.shape[1] + 3) // 4 * 4), np.float32); Ap[:, :A.shape[1]] = A
     Bp = np.zeros((B.shape[0], (B.shape[1] + 3) // 4 * 4), np.float32); Bp[:, :B.shape[1]] = B
-    C = run(tA, tB, M, N, K, Ap, Bp, lda=Ap.shape[1], ldb=Bp.shape[1], path=mm.MM_GEMM_TF32X3)
+    C = run(tA, tB, M, N, K, Ap, Bp, lda=Ap.shape[1], ldb=Bp.shape[1], path=mm.MM_GEMM_TF32X3, tile=tile)
     ref, T = oracle.gemm(tA, tB, M, N, K, A, B)
-    worst = check_bound(C, ref, T, f"{layout} {shape}")
-    print(f"tf32x3 {layout} {shape}: worst |err|/T = {worst:.3e}")
+    worst = check_bound(C, ref, T, f"{layout} {shape} tile {tile}")
+    print(f"tf32x3 tile {tile} {layout} {shape}: worst |err|/T = {worst:.3e}")
 
 
 @pytest.mark.parametrize("layout", list(LAYOUTS))
@@ -117,8 +124,8 @@ def test_gemm_small_integers_bit_exact(oracle, layout):
     M, N, K = 300, 272, 516
     A, B = stored(tA, tB, M, N, K, seed=31, kind="int")
     ref, _ = oracle.gemm(tA, tB, M, N, K, A, B)
-    for path in (mm.MM_GEMM_AUTO, mm.MM_GEMM_FFMA, mm.MM_GEMM_TF32X3):
-        if path == mm.MM_GEMM_TF32X3 and (A.shape[1] % 4 or B.shape[1] % 4):
+    for path in PATHS.values():
+        if path[0] == mm.MM_GEMM_TF32X3 and (A.shape[1] % 4 or B.shape[1] % 4):
             continue
         check_exact(run(tA, tB, M, N, K, A, B, path=path), ref, f"{layout} path {path}")
 
@@ -129,7 +136,7 @@ def test_gemm_all_ones_is_K():
     assert np.all(C == K)
 
 
-@pytest.mark.parametrize("path", ["ffma", "tf32x3"])
+@pytest.mark.parametrize("path", ["ffma", "tf32x3", "tf32x3_2stage"])
 @pytest.mark.parametrize("layout", ["nn", "nt", "tn"])
 def test_gemm_deterministic(layout, path):
     tA, tB = LAYOUTS[layout]
@@ -140,12 +147,14 @@ def test_gemm_deterministic(layout, path):
     assert np.array_equal(c1.view(np.uint32), c2.view(np.uint32))
 
 
-def test_gemm_tf32x3_all_ones_and_identity():
+@pytest.mark.parametrize("tile", [1, 2])
+def test_gemm_tf32x3_all_ones_and_identity(tile):
     M = N = K = 256
-    C = run(0, 0, M, N, K, np.ones((M, K), np.float32), np.ones((K, N), np.float32), path=mm.MM_GEMM_TF32X3)
+    C = run(0, 0, M, N, K, np.ones((M, K), np.float32), np.ones((K, N), np.float32), path=mm.MM_GEMM_TF32X3,
+            tile=tile)
     assert np.all(C == K)
     X = synth.normal_f32(3, (M, K), 1.0)
-    C = run(0, 0, M, N, K, X, np.eye(K, dtype=np.float32), path=mm.MM_GEMM_TF32X3)
+    C = run(0, 0, M, N, K, X, np.eye(K, dtype=np.float32), path=mm.MM_GEMM_TF32X3, tile=tile)
     # x = hi + lo with lo's tf32 rounding dropped: relative error below 2^-21
     assert np.all(np.abs(C - X) <= 2.0 ** -20 * np.abs(X))
 
@@ -157,7 +166,7 @@ def test_gpt2_mlp_up_64x768x3072_all_outputs(oracle):
     check_bound(C, ref, T, c.name)
 
 
-@pytest.mark.parametrize("path", ["ffma", "tf32x3"])
+@pytest.mark.parametrize("path", ["ffma", "tf32x3", "tf32x3_2stage"])
 @pytest.mark.parametrize("layout", ["nn", "nt", "tn"])
 def test_square_2048_all_outputs(oracle, layout, path):
     c = synth.square_2048(layout)
