@@ -58,7 +58,7 @@ WORKLOAD = ("square_2048_fp32_gemm_nn_nt_tn + gemv2bit_12288x1536_rotation64 + "
 def parse_args(argv=None):
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--steps", type=int, default=400)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", choices=["mm", "reference"], default="mm")
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -110,7 +110,7 @@ def rank_seed_offset(rank: int) -> int:
 # ---------------------------------------------------------------- clocks
 
 class ClockSampler:
-    """nvidia-smi sampled every 200 ms while the timed region runs."""
+    """nvidia-smi sampled every 100 ms while the timed region runs."""
 
     FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
@@ -127,7 +127,7 @@ class ClockSampler:
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", "-i", str(self.gpu_index), f"--query-gpu={self.FIELDS}",
-                 "--format=csv,noheader,nounits", "-lms", "200"],
+                 "--format=csv,noheader,nounits", "-lms", "100"],
                 stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
         except (FileNotFoundError, OSError):
             self.proc = None
@@ -501,8 +501,8 @@ def main_mm(args):
         # three tf32 MMAs per fp32 multiply-add: the fp32-equivalent tensor peak is a third of tf32's
         tf32_peak = peaks["bf16_tflops"] * (1.1 / 2.25)
         roof = {"bound": "tensor", "achieved": gemm_per_gpu, "peak": tf32_peak / 3.0, "unit": "TFLOP/s",
-                "frac": gemm_per_gpu / (tf32_peak / 3.0), "traffic": traffic_for("gemm_tf32x3"),
-                "kernel": "gemm_tf32x3_kernel",
+                "frac": gemm_per_gpu / (tf32_peak / 3.0), "traffic": traffic_for("gemm_tf32x3_ws"),
+                "kernel": "gemm_tf32x3_ws_kernel",
                 "peak_source": (f"{peaks_src} bf16 burst {peaks['bf16_tflops']:.0f} TFLOP/s x nominal tf32/bf16 "
                                 f"ratio 1.1/2.25, divided by the 3 MMAs of the split"),
                 "frac_of_fp32_simt_peak": gemm_per_gpu / fp32_peak_max}

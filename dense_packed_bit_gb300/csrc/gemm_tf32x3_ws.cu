@@ -17,17 +17,25 @@
 // its hi and lo tiles transposed (4 conflict-free column reads, one 16-byte
 // conflict-free store per tile).
 //
-// Roles (one CTA per SM, persistent over 128 x 256 output tiles):
+// Roles (one CTA per SM, persistent over output tiles of 128 x 256 per CTA,
+// or 256 x 256 per pair of CTAs):
 //   warp 0      one thread issues the TMA loads of each 16-deep k-slab of
 //               op(A) (128 x 16) and op(B) (256 x 16) into a ring of 3 or
 //               4 stages (as many as fit in shared memory);
 //   warp 1      one thread issues 2 x 3 tcgen05.mma kind::tf32 (M = 128,
 //               N = 256, K = 8) per slab into one of two TMEM accumulators
 //               and commits each slab to the barrier that frees its stage;
+//               with CTA pairs (cta_group::2, a cluster of 2) the even CTA's
+//               thread issues M = 256 MMAs over both CTAs' tiles -- each CTA
+//               holds its 128 rows of op(A) and 128 of the 256 rows of op(B)
+//               -- and its commits arrive on the barriers of both CTAs;
 //   warps 2-5   compute lo = a - a_hi for each landed slab (and transpose
 //               M/N-contiguous operands into the K-major layout);
 //   warps 6-9   drain a finished accumulator (tcgen05.ld) into C with edge
 //               masks while the MMAs of the next tile run in the other one.
+// In a pair, the lo-pass and epilogue warps of both CTAs report to the even
+// CTA's barriers (one arrival per warp, after fence.proxy.async for the lo
+// tiles the peer's tensor core reads).
 // Every wait is bounded; a wait that runs out records an error, raises a CTA
 // flag that the other roles poll, and the CTA drains its copies and MMAs,
 // frees its TMEM and returns.
@@ -45,28 +53,31 @@ __device__ unsigned int g_tf32ws_err;
 namespace {
 
 constexpr int BM = 128, BN = 256, BK = 16, NACC = 2;
-constexpr int A_BYTES = BM * BK * 4;          // 8 KiB: one 128 x 16 fp32 tile
-constexpr int B_BYTES = BN * BK * 4;          // 16 KiB: one 256 x 16 fp32 tile
-constexpr int RAW_BYTES = A_BYTES + B_BYTES;  // bytes TMA brings per stage
-constexpr int WARP_TMA = 0, WARP_MMA = 1, WARP_CONV0 = 2, NCONV = 128, WARP_EPI0 = 6, NEPI = 128;
+constexpr int A_BYTES = BM * BK * 4;          // 8 KiB: one CTA's 128 x 16 fp32 A tile
+constexpr int WARP_TMA = 0, WARP_MMA = 1, WARP_CONV0 = 2, NCONV = 128, WARP_EPI0 = 6;
 constexpr int NTHREADS = 320;
 constexpr int TMEM_COLS = NACC * BN;          // 512: the whole tensor memory of the SM
 constexpr int SMEM_LIMIT = 227 * 1024;
+constexpr int MAX_STAGES = 6;
 
-// Shared-memory plan of one stage.  A K-contiguous operand keeps raw (= hi) and
-// lo tiles; an M/N-contiguous one keeps its raw [k][m] tile plus K-major hi and lo.
-template <bool A_KC, bool B_KC>
+// Shared-memory plan of one stage of one CTA.  CG CTAs share a tile of
+// (128 CG) x 256: each holds 128 rows of op(A) and 256 / CG rows of op(B).  A
+// K-contiguous operand keeps raw (= hi) and lo tiles; an M/N-contiguous one
+// keeps its raw [k][m] tile plus K-major hi and lo.
+template <bool A_KC, bool B_KC, int CG>
 struct Plan {
+    static constexpr int BNC = BN / CG;                 // B rows held by one CTA
+    static constexpr int B_BYTES = BNC * BK * 4;
+    static constexpr int RAW_BYTES = A_BYTES + B_BYTES;  // bytes TMA brings per stage
     static constexpr int A_REGION = (A_KC ? 2 : 3) * A_BYTES;
     static constexpr int B_REGION = (B_KC ? 2 : 3) * B_BYTES;
     static constexpr int STAGE_BYTES = A_REGION + B_REGION;
     static constexpr int RAW_A = 0, HI_A = A_KC ? 0 : A_BYTES, LO_A = A_KC ? A_BYTES : 2 * A_BYTES;
     static constexpr int RAW_B = A_REGION, HI_B = A_REGION + (B_KC ? 0 : B_BYTES),
                          LO_B = A_REGION + (B_KC ? B_BYTES : 2 * B_BYTES);
-    static constexpr int NBARS_MAX = 3 * 4 + 2 * NACC + 1;
-    static constexpr int FIXED = NBARS_MAX * 8 + 16 + 1024;
+    static constexpr int FIXED = (3 * MAX_STAGES + 2 * NACC + 1) * 8 + 16 + 1024;
     static constexpr int S_FIT = (SMEM_LIMIT - FIXED) / STAGE_BYTES;
-    static constexpr int STAGES = S_FIT < 4 ? S_FIT : 4;
+    static constexpr int STAGES = S_FIT < MAX_STAGES ? S_FIT : MAX_STAGES;
     static constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + (3 * STAGES + 2 * NACC + 1) * 8 + 16 + 1024;
     static_assert(STAGES >= 3, "at least three stages");
     static_assert(SMEM_BYTES <= SMEM_LIMIT, "shared memory");
@@ -120,44 +131,62 @@ __device__ __forceinline__ void split_transpose(const uint8_t *raw, uint8_t *hi,
     }
 }
 
+// Record an error and raise the abort flag of this CTA and, in a pair, of its peer.
+template <int CG>
 __device__ __forceinline__ void fail(volatile int *abort_flag, unsigned int code) {
     atomicExch(&g_tf32ws_err, code);
     *abort_flag = 1;
+    if constexpr (CG == 2)
+        st_cluster_u32(cluster_map(smem_u32(const_cast<int *>(abort_flag)), cluster_ctarank() ^ 1u), 1u);
 }
 
-template <bool A_KC, bool B_KC>
+// One arrival on the barrier at `bar`'s offset in CTA 0 of the pair (or this CTA).
+template <int CG>
+__device__ __forceinline__ void arrive_leader(uint64_t *bar) {
+    if constexpr (CG == 2) mbar_arrive_cluster(cluster_map(smem_u32(bar), 0));
+    else mbar_arrive(bar);
+}
+
+template <bool A_KC, bool B_KC, int CG>
 __global__ void __launch_bounds__(NTHREADS, 1)
     gemm_tf32x3_ws_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                           const WsParams p) {
-    using P = Plan<A_KC, B_KC>;
-    constexpr int STAGES = P::STAGES, STAGE_BYTES = P::STAGE_BYTES;
+    using P = Plan<A_KC, B_KC, CG>;
+    constexpr int STAGES = P::STAGES, STAGE_BYTES = P::STAGE_BYTES, BNC = P::BNC;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = smem_aligned<1024>(smem_raw);
-    uint64_t *full = reinterpret_cast<uint64_t *>(smem + STAGES * STAGE_BYTES);  // TMA -> lo pass
-    uint64_t *conv = full + STAGES;                                              // lo pass -> MMA
-    uint64_t *empty = conv + STAGES;                                             // MMA -> TMA
-    uint64_t *accf = empty + STAGES;                                             // MMA -> epilogue
-    uint64_t *acce = accf + NACC;                                                // epilogue -> MMA
+    uint64_t *full = reinterpret_cast<uint64_t *>(smem + STAGES * STAGE_BYTES);  // TMA -> lo pass (own CTA)
+    uint64_t *conv = full + STAGES;    // lo passes -> MMA (CTA 0's, one arrival per lo-pass warp of the pair)
+    uint64_t *empty = conv + STAGES;   // MMA -> TMA (every CTA's, by commit)
+    uint64_t *accf = empty + STAGES;   // MMA -> epilogue (every CTA's, by commit)
+    uint64_t *acce = accf + NACC;      // epilogues -> MMA (CTA 0's, one arrival per epilogue warp of the pair)
     uint64_t *last = acce + NACC;
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(last + 1);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int KT = (p.K + BK - 1) / BK;
+    const uint32_t rank = CG == 2 ? cluster_ctarank() : 0u;
+    const int cid = blockIdx.x / CG, ncl = gridDim.x / CG;
 
     if (warp == WARP_MMA) {
-        tmem_alloc(tmem_slot, TMEM_COLS);
-        tmem_relinquish();
+        if constexpr (CG == 2) {
+            tmem_alloc_pair(tmem_slot, TMEM_COLS);
+            tmem_relinquish_pair();
+        } else {
+            tmem_alloc(tmem_slot, TMEM_COLS);
+            tmem_relinquish();
+        }
     }
     if (threadIdx.x == 0) {
         for (int s = 0; s < STAGES; ++s) {
             mbar_init(&full[s], 1);
-            mbar_init(&conv[s], NCONV);
+            mbar_init(&conv[s], 4 * CG);
             mbar_init(&empty[s], 1);
         }
         for (int b = 0; b < NACC; ++b) {
             mbar_init(&accf[b], 1);
-            mbar_init(&acce[b], NEPI);
+            mbar_init(&acce[b], 4 * CG);
         }
         mbar_init(last, 1);
         *abort_flag = 0;
@@ -166,7 +195,8 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         tma_prefetch_desc(&tmB);
     }
     tc_fence_before_sync();
-    __syncthreads();
+    if constexpr (CG == 2) cluster_sync();
+    else __syncthreads();
     tc_fence_after_sync();
     const uint32_t tmem = *tmem_slot;
 
@@ -174,24 +204,25 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         if (lane == 0) {
             int it = 0;  // slabs issued so far (ring position)
             bool stop = false;
-            for (int t = blockIdx.x; t < p.tiles && !stop; t += gridDim.x) {
-                const int m0 = (t % p.tiles_m) * BM, n0 = (t / p.tiles_m) * BN;
+            for (int t = cid; t < p.tiles && !stop; t += ncl) {
+                const int m0 = (t % p.tiles_m) * (BM * CG) + BM * (int)rank;
+                const int nb = (t / p.tiles_m) * BN + BNC * (int)rank;
                 for (int kt = 0; kt < KT; ++kt) {
                     const int s = it % STAGES;
                     const uint32_t use = it / STAGES;
                     if (*abort_flag) { stop = true; break; }
                     if (use > 0 && !mbar_wait(&empty[s], (use - 1) & 1)) {
-                        fail(abort_flag, kDevErrWaitEmpty);
+                        fail<CG>(abort_flag, kDevErrWaitEmpty);
                         stop = true;
                         break;
                     }
                     uint8_t *st = smem + s * STAGE_BYTES;
-                    mbar_arrive_expect_tx(&full[s], RAW_BYTES);
+                    mbar_arrive_expect_tx(&full[s], P::RAW_BYTES);
                     const int k0 = kt * BK;
                     if (A_KC) tma_load_2d(st + P::RAW_A, &tmA, &full[s], k0, m0);
                     else tma_load_2d(st + P::RAW_A, &tmA, &full[s], m0, k0);
-                    if (B_KC) tma_load_2d(st + P::RAW_B, &tmB, &full[s], k0, n0);
-                    else tma_load_2d(st + P::RAW_B, &tmB, &full[s], n0, k0);
+                    if (B_KC) tma_load_2d(st + P::RAW_B, &tmB, &full[s], k0, nb);
+                    else tma_load_2d(st + P::RAW_B, &tmB, &full[s], nb, k0);
                     ++it;
                 }
             }
@@ -205,16 +236,17 @@ __global__ void __launch_bounds__(NTHREADS, 1)
             }
         }
     } else if (warp == WARP_MMA) {
-        if (lane == 0) {
-            constexpr uint32_t idesc = make_idesc(kFmtTF32, kFmtTF32, BN, BM);
+        if (lane == 0 && rank == 0) {
+            constexpr uint32_t idesc = make_idesc(kFmtTF32, kFmtTF32, BN, BM * CG);
+            constexpr uint16_t all = (uint16_t)((1u << CG) - 1u);
             int it = 0, tc = 0;
             bool stop = false;
-            for (int t = blockIdx.x; t < p.tiles && !stop; t += gridDim.x, ++tc) {
+            for (int t = cid; t < p.tiles && !stop; t += ncl, ++tc) {
                 const int b = tc % NACC;
                 const uint32_t ause = tc / NACC;
                 if (*abort_flag) break;
                 if (ause > 0 && !mbar_wait(&acce[b], (ause - 1) & 1)) {
-                    fail(abort_flag, kDevErrWaitEmpty);
+                    fail<CG>(abort_flag, kDevErrWaitEmpty);
                     break;
                 }
                 tc_fence_after_sync();
@@ -224,7 +256,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                     const uint32_t use = it / STAGES;
                     if (*abort_flag) { stop = true; break; }
                     if (!mbar_wait(&conv[s], use & 1)) {
-                        fail(abort_flag, kDevErrWaitFull);
+                        fail<CG>(abort_flag, kDevErrWaitFull);
                         stop = true;
                         break;
                     }
@@ -238,16 +270,28 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                         const uint64_t al = sdesc_make(st + P::LO_A + o, 16, 512, kSdescSw64);
                         const uint64_t bh = sdesc_make(st + P::HI_B + o, 16, 512, kSdescSw64);
                         const uint64_t bl = sdesc_make(st + P::LO_B + o, 16, 512, kSdescSw64);
-                        umma_tf32(d, ah, bh, idesc, (kt > 0 || ks > 0) ? 1u : 0u);
-                        umma_tf32(d, ah, bl, idesc, 1u);
-                        umma_tf32(d, al, bh, idesc, 1u);
+                        const uint32_t acc0 = (kt > 0 || ks > 0) ? 1u : 0u;
+                        if constexpr (CG == 2) {
+                            umma_tf32_pair(d, ah, bh, idesc, acc0);
+                            umma_tf32_pair(d, ah, bl, idesc, 1u);
+                            umma_tf32_pair(d, al, bh, idesc, 1u);
+                        } else {
+                            umma_tf32(d, ah, bh, idesc, acc0);
+                            umma_tf32(d, ah, bl, idesc, 1u);
+                            umma_tf32(d, al, bh, idesc, 1u);
+                        }
                     }
-                    umma_commit(&empty[s]);
+                    if constexpr (CG == 2) umma_commit_pair(&empty[s], all);
+                    else umma_commit(&empty[s]);
                 }
-                if (!stop) umma_commit(&accf[b]);
+                if (!stop) {
+                    if constexpr (CG == 2) umma_commit_pair(&accf[b], all);
+                    else umma_commit(&accf[b]);
+                }
             }
             // every MMA issued must be complete before the tensor memory is freed
-            umma_commit(last);
+            if constexpr (CG == 2) umma_commit_pair(last, 1);
+            else umma_commit(last);
             if (!mbar_wait(last, 0)) atomicExch(&g_tf32ws_err, kDevErrWaitMma);
         }
     } else if (warp < WARP_EPI0) {
@@ -255,40 +299,41 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         const int ct = threadIdx.x - 32 * WARP_CONV0;
         int it = 0;
         bool stop = false;
-        for (int t = blockIdx.x; t < p.tiles && !stop; t += gridDim.x) {
+        for (int t = cid; t < p.tiles && !stop; t += ncl) {
             for (int kt = 0; kt < KT; ++kt, ++it) {
                 const int s = it % STAGES;
                 const uint32_t use = it / STAGES;
                 if (*abort_flag) { stop = true; break; }
                 if (!mbar_wait(&full[s], use & 1)) {
-                    fail(abort_flag, kDevErrWaitFull);
+                    fail<CG>(abort_flag, kDevErrWaitFull);
                     stop = true;
                     break;
                 }
                 uint8_t *st = smem + s * STAGE_BYTES;
                 if (A_KC) lo_in_place_layout<A_BYTES>(st + P::RAW_A, st + P::LO_A, ct);
                 else split_transpose<BM>(st + P::RAW_A, st + P::HI_A, st + P::LO_A, ct);
-                if (B_KC) lo_in_place_layout<B_BYTES>(st + P::RAW_B, st + P::LO_B, ct);
-                else split_transpose<BN>(st + P::RAW_B, st + P::HI_B, st + P::LO_B, ct);
+                if (B_KC) lo_in_place_layout<P::B_BYTES>(st + P::RAW_B, st + P::LO_B, ct);
+                else split_transpose<BNC>(st + P::RAW_B, st + P::HI_B, st + P::LO_B, ct);
                 fence_proxy_async_smem();
-                mbar_arrive(&conv[s]);
+                __syncwarp();
+                if (lane == 0) arrive_leader<CG>(&conv[s]);
             }
         }
     } else {
-        // epilogue: warp w reads TMEM lanes 32 (w % 4) .. 32 (w % 4) + 31
+        // epilogue: warp w reads TMEM lanes 32 (w % 4) .. 32 (w % 4) + 31 of this CTA
         const int q = warp & 3;
         const bool vec_ok = (p.ldc % 4 == 0) && ((reinterpret_cast<uintptr_t>(p.C) & 15) == 0);
         int tc = 0;
-        for (int t = blockIdx.x; t < p.tiles; t += gridDim.x, ++tc) {
+        for (int t = cid; t < p.tiles; t += ncl, ++tc) {
             const int b = tc % NACC;
             const uint32_t ause = tc / NACC;
             if (*abort_flag) break;
             if (!mbar_wait_sleep(&accf[b], ause & 1)) {
-                fail(abort_flag, kDevErrWaitMma);
+                fail<CG>(abort_flag, kDevErrWaitMma);
                 break;
             }
             tc_fence_after_sync();
-            const int m0 = (t % p.tiles_m) * BM, n0 = (t / p.tiles_m) * BN;
+            const int m0 = (t % p.tiles_m) * (BM * CG) + BM * (int)rank, n0 = (t / p.tiles_m) * BN;
             const int row = m0 + 32 * q + lane;
             const uint32_t base = tmem + (uint32_t)(b * BN) + ((uint32_t)(32 * q) << 16);
             float *crow = p.C + (int64_t)row * p.ldc + n0;
@@ -309,34 +354,49 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                 }
             }
             tc_fence_before_sync();
-            mbar_arrive(&acce[b]);
+            __syncwarp();
+            if (lane == 0) arrive_leader<CG>(&acce[b]);
         }
     }
 
     tc_fence_before_sync();
-    __syncthreads();
+    if constexpr (CG == 2) cluster_sync();
+    else __syncthreads();
     tc_fence_after_sync();
-    if (warp == WARP_MMA) tmem_dealloc(tmem, TMEM_COLS);
+    if (warp == WARP_MMA) {
+        if constexpr (CG == 2) tmem_dealloc_pair(tmem, TMEM_COLS);
+        else tmem_dealloc(tmem, TMEM_COLS);
+    }
 }
 
-template <bool A_KC, bool B_KC>
+template <bool A_KC, bool B_KC, int CG>
 cudaError_t launch_ws(const CUtensorMap &ta, const CUtensorMap &tb, const WsParams &p, int grid, cudaStream_t s) {
-    auto kern = gemm_tf32x3_ws_kernel<A_KC, B_KC>;
-    constexpr int smem = Plan<A_KC, B_KC>::SMEM_BYTES;
+    auto kern = gemm_tf32x3_ws_kernel<A_KC, B_KC, CG>;
+    constexpr int smem = Plan<A_KC, B_KC, CG>::SMEM_BYTES;
     static std::once_flag once;
     static cudaError_t attr_err = cudaSuccess;
     std::call_once(once, [&] {
         attr_err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     });
     if (attr_err != cudaSuccess) return attr_err;
-    kern<<<grid, NTHREADS, smem, s>>>(ta, tb, p);
-    return cudaGetLastError();
+    cudaLaunchConfig_t lc = {};
+    lc.gridDim = dim3((unsigned)grid);
+    lc.blockDim = dim3(NTHREADS);
+    lc.dynamicSmemBytes = smem;
+    lc.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = CG;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    lc.attrs = attr;
+    lc.numAttrs = CG == 2 ? 1 : 0;
+    return cudaLaunchKernelEx(&lc, kern, ta, tb, p);
 }
 
-}  // namespace
-
-cudaError_t launch_gemm_tf32x3_ws(const GemmArgs &g, cudaStream_t s) {
-    if (!gemm_tf32x3_supported(g)) return cudaErrorNotSupported;
+template <int CG>
+cudaError_t launch_ws_cg(const GemmArgs &g, cudaStream_t s) {
+    constexpr int BNC = BN / CG;
     CUtensorMap ta, tb;
     cudaError_t e;
     // K-contiguous operands: 16 x rows boxes, 64-byte swizzle (the MMA operand layout);
@@ -349,23 +409,31 @@ cudaError_t launch_gemm_tf32x3_ws(const GemmArgs &g, cudaStream_t s) {
                          CU_TENSOR_MAP_SWIZZLE_NONE);
     if (e != cudaSuccess) return e;
     if (g.transB)
-        e = make_tmap_2d(&tb, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, g.B, g.K, g.N, g.ldb * 4, BK, BN,
+        e = make_tmap_2d(&tb, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, g.B, g.K, g.N, g.ldb * 4, BK, BNC,
                          CU_TENSOR_MAP_SWIZZLE_64B);
     else
-        e = make_tmap_2d(&tb, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, g.B, g.N, g.K, g.ldb * 4, BN, BK,
+        e = make_tmap_2d(&tb, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, g.B, g.N, g.K, g.ldb * 4, BNC, BK,
                          CU_TENSOR_MAP_SWIZZLE_NONE);
     if (e != cudaSuccess) return e;
     int dev = 0, sms = 0;
     e = cudaGetDevice(&dev);
     if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
     if (e != cudaSuccess) return e;
-    const int tiles_m = (int)((g.M + BM - 1) / BM), tiles_n = (int)((g.N + BN - 1) / BN);
+    const int tiles_m = (int)((g.M + BM * CG - 1) / (BM * CG)), tiles_n = (int)((g.N + BN - 1) / BN);
     WsParams p{(int)g.M, (int)g.N, (int)g.K, tiles_m, tiles_m * tiles_n, g.C, g.ldc};
-    const int grid = p.tiles < sms ? p.tiles : sms;
-    if (!g.transA && !g.transB) return launch_ws<true, false>(ta, tb, p, grid, s);
-    if (!g.transA && g.transB) return launch_ws<true, true>(ta, tb, p, grid, s);
-    if (g.transA && !g.transB) return launch_ws<false, false>(ta, tb, p, grid, s);
-    return launch_ws<false, true>(ta, tb, p, grid, s);
+    const int units = sms / CG;
+    const int grid = CG * (p.tiles < units ? p.tiles : units);
+    if (!g.transA && !g.transB) return launch_ws<true, false, CG>(ta, tb, p, grid, s);
+    if (!g.transA && g.transB) return launch_ws<true, true, CG>(ta, tb, p, grid, s);
+    if (g.transA && !g.transB) return launch_ws<false, false, CG>(ta, tb, p, grid, s);
+    return launch_ws<false, true, CG>(ta, tb, p, grid, s);
+}
+
+}  // namespace
+
+cudaError_t launch_gemm_tf32x3_ws(const GemmArgs &g, int pair, cudaStream_t s) {
+    if (!gemm_tf32x3_supported(g)) return cudaErrorNotSupported;
+    return pair ? launch_ws_cg<2>(g, s) : launch_ws_cg<1>(g, s);
 }
 
 unsigned int gemm_tf32x3_ws_take_device_error(cudaError_t *err) {

@@ -139,8 +139,9 @@ mm_status mm_gemm_f32_ex(int transA, int transB, int64_t M, int64_t N, int64_t K
         if (path < MM_GEMM_AUTO || path > MM_GEMM_TF32X3) return fail(MM_ERR_INVALID_ARG, "unknown path %d", path);
     }
     const int tile = opts ? opts->tile : 0;
-    if ((path == MM_GEMM_TF32X3 || path == MM_GEMM_AUTO) && (tile < 0 || tile > 2))
-        return fail(MM_ERR_INVALID_ARG, "3xTF32 tile must be 0 (automatic), 1 (two-stage) or 2 (warp-specialised)");
+    if ((path == MM_GEMM_TF32X3 || path == MM_GEMM_AUTO) && (tile < 0 || tile > 3))
+        return fail(MM_ERR_INVALID_ARG,
+                    "3xTF32 tile must be 0 (automatic), 1 (two-stage), 2 (warp-specialised) or 3 (CTA pairs)");
     mm_status s = check_device();
     if (s != MM_OK) return s;
 
@@ -150,7 +151,9 @@ mm_status mm_gemm_f32_ex(int transA, int transB, int64_t M, int64_t N, int64_t K
     if (path == MM_GEMM_TF32X3 && !mm::gemm_tf32x3_supported(g))
         return fail(MM_ERR_INVALID_ARG, "3xTF32 path needs 16-byte aligned A, B and lda, ldb multiples of 4");
     if ((path == MM_GEMM_TF32X3 || path == MM_GEMM_AUTO) && mm::gemm_tf32x3_supported(g))
-        e = tile == 1 ? mm::launch_gemm_tf32x3(g, st) : mm::launch_gemm_tf32x3_ws(g, st);
+        // automatic: CTA pairs (256-row tiles) once M fills them, one CTA per 128-row tile below that
+        e = tile == 1 ? mm::launch_gemm_tf32x3(g, st)
+                      : mm::launch_gemm_tf32x3_ws(g, (tile == 3 || (tile == 0 && M > 128)) ? 1 : 0, st);
     else if (mm::gemm_ffma_supported(g)) e = mm::launch_gemm_ffma(g, opts ? opts->tile : 0, st);
     else if (path == MM_GEMM_FFMA || path == MM_GEMM_AUTO) e = mm::launch_gemm_simple(g, st);
     else e = cudaErrorNotSupported;

@@ -137,6 +137,19 @@ __device__ __forceinline__ uint32_t cluster_map(uint32_t smem_addr, uint32_t ran
     return r;
 }
 
+// Arrive on the mbarrier at a shared::cluster address (this CTA's or a peer's)
+// with the instruction's default semantics.  Shared-memory operands written
+// before it for a peer's tensor-core MMA are first made visible to the async
+// proxy (fence.proxy.async); an explicit cluster-scope release here measured
+// about twice as slow for the whole GEMM pipeline on GB300.
+__device__ __forceinline__ void mbar_arrive_cluster(uint32_t cluster_addr) {
+    asm volatile("mbarrier.arrive.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr) : "memory");
+}
+
+__device__ __forceinline__ void st_cluster_u32(uint32_t cluster_addr, uint32_t v) {
+    asm volatile("st.shared::cluster.u32 [%0], %1;" ::"r"(cluster_addr), "r"(v) : "memory");
+}
+
 __device__ __forceinline__ float4 ld_cluster_v4(uint32_t addr) {
     float4 v;
     asm volatile("ld.shared::cluster.v4.f32 {%0, %1, %2, %3}, [%4];"

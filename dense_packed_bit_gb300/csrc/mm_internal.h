@@ -117,10 +117,11 @@ cudaError_t launch_gemm_ffma(const GemmArgs &g, int tile, cudaStream_t s);
 // 3xTF32 tcgen05 kernels: same operand requirements as the FFMA TMA kernel.
 // launch_gemm_tf32x3: one 128 x 128 tile per CTA, two stages, all threads split
 // and wait together; launch_gemm_tf32x3_ws: persistent, warp-specialised,
-// 128 x 256 tiles, raw tiles used as the hi operands.
+// raw tiles used as the hi operands, 128 x 256 tiles per CTA (pair = 0) or
+// 256 x 256 tiles per pair of CTAs sharing each MMA (pair = 1).
 bool gemm_tf32x3_supported(const GemmArgs &g);
 cudaError_t launch_gemm_tf32x3(const GemmArgs &g, cudaStream_t s);
-cudaError_t launch_gemm_tf32x3_ws(const GemmArgs &g, cudaStream_t s);
+cudaError_t launch_gemm_tf32x3_ws(const GemmArgs &g, int pair, cudaStream_t s);
 
 // Per translation unit device error words (read and cleared).
 unsigned int gemm_ffma_take_device_error(cudaStream_t s, cudaError_t *err);

@@ -139,7 +139,9 @@ typedef struct {
     int tile;      /* 0 = automatic, else a path-specific tile id.  3xTF32 (MM_GEMM_AUTO
                       or MM_GEMM_TF32X3 with TMA-describable operands): 1 = one 128 x 128
                       tile per CTA, two stages; 2 = persistent warp-specialised kernel,
-                      128 x 256 tiles (the automatic choice).  Other values are refused. */
+                      128 x 256 tiles; 3 = the same with pairs of CTAs (a cluster of 2)
+                      sharing 256 x 256 tiles.  Automatic: 3 when M > 128, else 2.
+                      Other values are refused. */
     int reserved[6];
 } mm_gemm_opts;
 

@@ -82,7 +82,7 @@ def test_gemm_bad_path_option(lib):
     assert st == mm.MM_ERR_INVALID_ARG
 
 
-@pytest.mark.parametrize("path,tile", [(0, 3), (2, -1), (2, 7)])
+@pytest.mark.parametrize("path,tile", [(0, 4), (2, -1), (2, 7)])
 def test_gemm_bad_tf32x3_tile(lib, path, tile):
     o = mm.GemmOpts(path, tile)
     st = lib.mm_gemm_f32_ex(0, 0, 8, 8, 8, FAKE, 8, FAKE + 4096, 8, FAKE + 8192, 8, None, ctypes.byref(o))

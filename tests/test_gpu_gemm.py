@@ -53,8 +53,8 @@ SHAPES = [(1, 1, 1), (3, 17, 5), (65, 129, 33), (127, 63, 129), (200, 300, 97), 
 # (path, tile): the 3xTF32 path has two kernels, the persistent warp-specialised one
 # (tile 2, the automatic choice) and the two-stage one (tile 1)
 PATHS = {"auto": (mm.MM_GEMM_AUTO, 0), "ffma": (mm.MM_GEMM_FFMA, 0), "tf32x3": (mm.MM_GEMM_TF32X3, 2),
-         "tf32x3_2stage": (mm.MM_GEMM_TF32X3, 1)}
-TC_PATHS = ("tf32x3", "tf32x3_2stage")
+         "tf32x3_2stage": (mm.MM_GEMM_TF32X3, 1), "tf32x3_pair": (mm.MM_GEMM_TF32X3, 3)}
+TC_PATHS = ("tf32x3", "tf32x3_2stage", "tf32x3_pair")
 
 
 @pytest.mark.parametrize("path", list(PATHS))
@@ -71,7 +71,7 @@ def test_gemm_ragged_shapes(oracle, layout, shape, path):
     check_bound(C, ref, T, f"{layout} {shape} {path}")
 
 
-@pytest.mark.parametrize("tile", [1, 2])
+@pytest.mark.parametrize("tile", [1, 2, 3])
 @pytest.mark.parametrize("layout", list(LAYOUTS))
 @pytest.mark.parametrize("shape", [(5, 7, 3), (128, 128, 32), (128, 256, 16), (256, 384, 64), (130, 260, 100),
                                    (384, 128, 1000), (64, 3072, 768), (2000, 2900, 72)])
@@ -136,7 +136,7 @@ def test_gemm_all_ones_is_K():
     assert np.all(C == K)
 
 
-@pytest.mark.parametrize("path", ["ffma", "tf32x3", "tf32x3_2stage"])
+@pytest.mark.parametrize("path", ["ffma", "tf32x3", "tf32x3_2stage", "tf32x3_pair"])
 @pytest.mark.parametrize("layout", ["nn", "nt", "tn"])
 def test_gemm_deterministic(layout, path):
     tA, tB = LAYOUTS[layout]
@@ -147,7 +147,7 @@ def test_gemm_deterministic(layout, path):
     assert np.array_equal(c1.view(np.uint32), c2.view(np.uint32))
 
 
-@pytest.mark.parametrize("tile", [1, 2])
+@pytest.mark.parametrize("tile", [1, 2, 3])
 def test_gemm_tf32x3_all_ones_and_identity(tile):
     M = N = K = 256
     C = run(0, 0, M, N, K, np.ones((M, K), np.float32), np.ones((K, N), np.float32), path=mm.MM_GEMM_TF32X3,
@@ -166,7 +166,7 @@ def test_gpt2_mlp_up_64x768x3072_all_outputs(oracle):
     check_bound(C, ref, T, c.name)
 
 
-@pytest.mark.parametrize("path", ["ffma", "tf32x3", "tf32x3_2stage"])
+@pytest.mark.parametrize("path", ["ffma", "tf32x3", "tf32x3_2stage", "tf32x3_pair"])
 @pytest.mark.parametrize("layout", ["nn", "nt", "tn"])
 def test_square_2048_all_outputs(oracle, layout, path):
     c = synth.square_2048(layout)
@@ -176,7 +176,7 @@ def test_square_2048_all_outputs(oracle, layout, path):
     print(f"{c.name} {path}: worst |err|/T = {worst:.3e}")
 
 
-@pytest.mark.parametrize("path", ["ffma", "tf32x3"])
+@pytest.mark.parametrize("path", ["ffma", "tf32x3", "tf32x3_pair"])
 @pytest.mark.parametrize("which", ["fwd", "dA", "dB"])
 def test_training_set_sampled(oracle, which, path):
     c = synth.training_set_8192(which)
