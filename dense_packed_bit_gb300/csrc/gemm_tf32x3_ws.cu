@@ -52,21 +52,25 @@ __device__ unsigned int g_tf32ws_err;
 
 namespace {
 
-constexpr int BM = 128, BN = 256, BK = 16, NACC = 2;
+constexpr int BM = 128, BK = 16, NACC = 2;
+constexpr int ACC_COLS = 256;                 // TMEM columns per accumulator (N of a tile <= 256)
 constexpr int A_BYTES = BM * BK * 4;          // 8 KiB: one CTA's 128 x 16 fp32 A tile
 constexpr int WARP_TMA = 0, WARP_MMA = 1, WARP_CONV0 = 2, NCONV = 128, WARP_EPI0 = 6;
 constexpr int NTHREADS = 320;
-constexpr int TMEM_COLS = NACC * BN;          // 512: the whole tensor memory of the SM
+constexpr int TMEM_COLS = NACC * ACC_COLS;    // 512: the whole tensor memory of the SM
 constexpr int SMEM_LIMIT = 227 * 1024;
 constexpr int MAX_STAGES = 6;
 
 // Shared-memory plan of one stage of one CTA.  CG CTAs share a tile of
-// (128 CG) x 256: each holds 128 rows of op(A) and 256 / CG rows of op(B).  A
+// (128 CG) x BN: each holds 128 rows of op(A) and BN / CG rows of op(B).  A
 // K-contiguous operand keeps raw (= hi) and lo tiles; an M/N-contiguous one
-// keeps its raw [k][m] tile plus K-major hi and lo.
-template <bool A_KC, bool B_KC, int CG>
+// keeps its raw [k][m] tile plus K-major hi and lo.  Every tile is a multiple
+// of 512 bytes, the period of the 64-byte swizzle.
+template <bool A_KC, bool B_KC, int CG, int BN>
 struct Plan {
     static constexpr int BNC = BN / CG;                 // B rows held by one CTA
+    static_assert(BN % 16 == 0 && BNC % 8 == 0 && BN <= ACC_COLS, "MMA N: a multiple of 16, at most 256");
+    static_assert((BNC * BK * 4) % 512 == 0, "tiles keep the swizzle period");
     static constexpr int B_BYTES = BNC * BK * 4;
     static constexpr int RAW_BYTES = A_BYTES + B_BYTES;  // bytes TMA brings per stage
     static constexpr int A_REGION = (A_KC ? 2 : 3) * A_BYTES;
@@ -101,13 +105,14 @@ __device__ __forceinline__ float4 lo_part4(float4 v) {
 // K-contiguous operand: the lo tile at the same (swizzled) offsets as the raw tile.
 template <int BYTES>
 __device__ __forceinline__ void lo_in_place_layout(const uint8_t *raw, uint8_t *lo, int ct) {
-    constexpr int R = BYTES / (16 * NCONV);
-    static_assert(BYTES % (16 * NCONV) == 0, "whole float4 rounds");
+    constexpr int N4 = BYTES / 16, R = (N4 + NCONV - 1) / NCONV;
     float4 v[R];
 #pragma unroll
-    for (int i = 0; i < R; ++i) v[i] = *reinterpret_cast<const float4 *>(raw + (ct + i * NCONV) * 16);
+    for (int i = 0; i < R; ++i)
+        if (N4 % NCONV == 0 || ct + i * NCONV < N4) v[i] = *reinterpret_cast<const float4 *>(raw + (ct + i * NCONV) * 16);
 #pragma unroll
-    for (int i = 0; i < R; ++i) *reinterpret_cast<float4 *>(lo + (ct + i * NCONV) * 16) = lo_part4(v[i]);
+    for (int i = 0; i < R; ++i)
+        if (N4 % NCONV == 0 || ct + i * NCONV < N4) *reinterpret_cast<float4 *>(lo + (ct + i * NCONV) * 16) = lo_part4(v[i]);
 }
 
 // M/N-contiguous operand: raw [k][r] (BK rows of ROWS fp32, unswizzled) -> K-major
@@ -117,11 +122,11 @@ __device__ __forceinline__ void lo_in_place_layout(const uint8_t *raw, uint8_t *
 template <int ROWS>
 __device__ __forceinline__ void split_transpose(const uint8_t *raw, uint8_t *hi, uint8_t *lo, int ct) {
     const float *src = reinterpret_cast<const float *>(raw);
-    constexpr int TASKS = ROWS * (BK / 4);
-    static_assert(TASKS % NCONV == 0, "whole rounds");
+    constexpr int TASKS = ROWS * (BK / 4), R = (TASKS + NCONV - 1) / NCONV;
 #pragma unroll
-    for (int i = 0; i < TASKS / NCONV; ++i) {
+    for (int i = 0; i < R; ++i) {
         const int idx = ct + i * NCONV;
+        if (TASKS % NCONV != 0 && idx >= TASKS) break;
         const int r = idx % ROWS, c = idx / ROWS;
         const float4 v = make_float4(src[(4 * c + 0) * ROWS + r], src[(4 * c + 1) * ROWS + r],
                                      src[(4 * c + 2) * ROWS + r], src[(4 * c + 3) * ROWS + r]);
@@ -147,11 +152,11 @@ __device__ __forceinline__ void arrive_leader(uint64_t *bar) {
     else mbar_arrive(bar);
 }
 
-template <bool A_KC, bool B_KC, int CG>
+template <bool A_KC, bool B_KC, int CG, int BN>
 __global__ void __launch_bounds__(NTHREADS, 1)
     gemm_tf32x3_ws_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                           const WsParams p) {
-    using P = Plan<A_KC, B_KC, CG>;
+    using P = Plan<A_KC, B_KC, CG, BN>;
     constexpr int STAGES = P::STAGES, STAGE_BYTES = P::STAGE_BYTES, BNC = P::BNC;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = smem_aligned<1024>(smem_raw);
@@ -250,7 +255,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                     break;
                 }
                 tc_fence_after_sync();
-                const uint32_t d = tmem + (uint32_t)(b * BN);
+                const uint32_t d = tmem + (uint32_t)(b * ACC_COLS);
                 for (int kt = 0; kt < KT; ++kt, ++it) {
                     const int s = it % STAGES;
                     const uint32_t use = it / STAGES;
@@ -335,21 +340,23 @@ __global__ void __launch_bounds__(NTHREADS, 1)
             tc_fence_after_sync();
             const int m0 = (t % p.tiles_m) * (BM * CG) + BM * (int)rank, n0 = (t / p.tiles_m) * BN;
             const int row = m0 + 32 * q + lane;
-            const uint32_t base = tmem + (uint32_t)(b * BN) + ((uint32_t)(32 * q) << 16);
+            const uint32_t base = tmem + (uint32_t)(b * ACC_COLS) + ((uint32_t)(32 * q) << 16);
             float *crow = p.C + (int64_t)row * p.ldc + n0;
 #pragma unroll 1
             for (int c0 = 0; c0 < BN; c0 += 32) {
                 float v[32];
                 tmem_ld32(base + (uint32_t)c0, v);
+                // columns of this chunk inside the tile (the last chunk of a 240-wide tile has 16)
+                const int w = BN - c0 < 32 ? BN - c0 : 32;
                 if (row < p.M && n0 + c0 < p.N) {
-                    if (vec_ok && n0 + c0 + 32 <= p.N) {
+                    if (vec_ok && w == 32 && n0 + c0 + 32 <= p.N) {
 #pragma unroll
                         for (int j = 0; j < 32; j += 4)
                             *reinterpret_cast<float4 *>(crow + c0 + j) = make_float4(v[j], v[j + 1], v[j + 2], v[j + 3]);
                     } else {
 #pragma unroll
                         for (int j = 0; j < 32; ++j)
-                            if (n0 + c0 + j < p.N) crow[c0 + j] = v[j];
+                            if (j < w && n0 + c0 + j < p.N) crow[c0 + j] = v[j];
                     }
                 }
             }
@@ -369,10 +376,10 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     }
 }
 
-template <bool A_KC, bool B_KC, int CG>
+template <bool A_KC, bool B_KC, int CG, int BN>
 cudaError_t launch_ws(const CUtensorMap &ta, const CUtensorMap &tb, const WsParams &p, int grid, cudaStream_t s) {
-    auto kern = gemm_tf32x3_ws_kernel<A_KC, B_KC, CG>;
-    constexpr int smem = Plan<A_KC, B_KC, CG>::SMEM_BYTES;
+    auto kern = gemm_tf32x3_ws_kernel<A_KC, B_KC, CG, BN>;
+    constexpr int smem = Plan<A_KC, B_KC, CG, BN>::SMEM_BYTES;
     static std::once_flag once;
     static cudaError_t attr_err = cudaSuccess;
     std::call_once(once, [&] {
@@ -394,8 +401,8 @@ cudaError_t launch_ws(const CUtensorMap &ta, const CUtensorMap &tb, const WsPara
     return cudaLaunchKernelEx(&lc, kern, ta, tb, p);
 }
 
-template <int CG>
-cudaError_t launch_ws_cg(const GemmArgs &g, cudaStream_t s) {
+template <int CG, int BN>
+cudaError_t launch_ws_cg(const GemmArgs &g, int sms, cudaStream_t s) {
     constexpr int BNC = BN / CG;
     CUtensorMap ta, tb;
     cudaError_t e;
@@ -415,25 +422,27 @@ cudaError_t launch_ws_cg(const GemmArgs &g, cudaStream_t s) {
         e = make_tmap_2d(&tb, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, g.B, g.N, g.K, g.ldb * 4, BNC, BK,
                          CU_TENSOR_MAP_SWIZZLE_NONE);
     if (e != cudaSuccess) return e;
-    int dev = 0, sms = 0;
-    e = cudaGetDevice(&dev);
-    if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-    if (e != cudaSuccess) return e;
     const int tiles_m = (int)((g.M + BM * CG - 1) / (BM * CG)), tiles_n = (int)((g.N + BN - 1) / BN);
     WsParams p{(int)g.M, (int)g.N, (int)g.K, tiles_m, tiles_m * tiles_n, g.C, g.ldc};
     const int units = sms / CG;
     const int grid = CG * (p.tiles < units ? p.tiles : units);
-    if (!g.transA && !g.transB) return launch_ws<true, false, CG>(ta, tb, p, grid, s);
-    if (!g.transA && g.transB) return launch_ws<true, true, CG>(ta, tb, p, grid, s);
-    if (g.transA && !g.transB) return launch_ws<false, false, CG>(ta, tb, p, grid, s);
-    return launch_ws<false, true, CG>(ta, tb, p, grid, s);
+    if (!g.transA && !g.transB) return launch_ws<true, false, CG, BN>(ta, tb, p, grid, s);
+    if (!g.transA && g.transB) return launch_ws<true, true, CG, BN>(ta, tb, p, grid, s);
+    if (g.transA && !g.transB) return launch_ws<false, false, CG, BN>(ta, tb, p, grid, s);
+    return launch_ws<false, true, CG, BN>(ta, tb, p, grid, s);
 }
 
 }  // namespace
 
 cudaError_t launch_gemm_tf32x3_ws(const GemmArgs &g, int pair, cudaStream_t s) {
     if (!gemm_tf32x3_supported(g)) return cudaErrorNotSupported;
-    return pair ? launch_ws_cg<2>(g, s) : launch_ws_cg<1>(g, s);
+    int dev = 0, sms = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    if (e != cudaSuccess) return e;
+    // 256 columns per tile: a 240-wide pair tile (72 tiles of a 2048^2 output on 76
+    // pairs instead of 64) measured no faster on GB300, the MMA time not shrinking with N
+    return pair ? launch_ws_cg<2, 256>(g, sms, s) : launch_ws_cg<1, 256>(g, sms, s);
 }
 
 unsigned int gemm_tf32x3_ws_take_device_error(cudaError_t *err) {

@@ -74,8 +74,9 @@ def test_gemm_ragged_shapes(oracle, layout, shape, path):
 @pytest.mark.parametrize("tile", [1, 2, 3])
 @pytest.mark.parametrize("layout", list(LAYOUTS))
 @pytest.mark.parametrize("shape", [(5, 7, 3), (128, 128, 32), (128, 256, 16), (256, 384, 64), (130, 260, 100),
-                                   (384, 128, 1000), (64, 3072, 768), (2000, 2900, 72)])
+                                   (384, 128, 1000), (64, 3072, 768), (2000, 2900, 72), (19456, 256, 24)])
 def test_gemm_tf32x3_tiles(oracle, layout, shape, tile):
+    # 19456 x 256: 76 pair tiles, every pair of the GPU busy at once
     # whole tiles, ragged tiles and K tails on the tensor-core path
     tA, tB = LAYOUTS[layout]
     M, N, K = shape
