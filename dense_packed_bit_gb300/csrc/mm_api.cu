@@ -278,19 +278,34 @@ mm_status mm_gemm_packed2_ex(const uint8_t *codes, const uint16_t *scales, const
     if (s != MM_OK) return s;
     const int tile = opts ? opts->tile : 0;
     const int splitk = opts ? opts->splitk : 0;
-    if (tile != 0 && tile != 1 && tile != 32 && tile != 64 && tile != 128)
-        return fail(MM_ERR_INVALID_ARG, "tile must be 0 (auto), 1 (FFMA), 32, 64 or 128 (tensor cores)");
-    if (splitk != 0 && splitk != 1 && splitk != 2 && splitk != 4 && splitk != 8)
-        return fail(MM_ERR_INVALID_ARG, "splitk must be 0 (auto), 1, 2, 4 or 8");
+    const int pdl = opts ? opts->pdl : 0, weights_static = opts ? opts->weights_static : 0;
+    if (tile != 0 && tile != 1 && tile != 2 && tile != 32 && tile != 64 && tile != 128)
+        return fail(MM_ERR_INVALID_ARG, "tile must be 0 (auto), 1 (FFMA), 2, 32, 64 or 128 (tensor cores)");
+    if (splitk != 0 && splitk != 1 && splitk != 2 && splitk != 4 && splitk != 8 && !(splitk == 16 && tile == 2))
+        return fail(MM_ERR_INVALID_ARG, "splitk must be 0 (auto), 1, 2, 4 or 8 (or 16 with tile 2)");
+    if ((pdl != 0 && pdl != 1) || (weights_static != 0 && weights_static != 1) || (weights_static && !pdl))
+        return fail(MM_ERR_INVALID_ARG, "pdl and weights_static must be 0 or 1, weights_static only with pdl");
     mm::PackedArgs a{codes, scales, X, Y, M, rows, cols, {codebook[0], codebook[1], codebook[2], codebook[3]}};
     const bool tc_ok = mm::gemm_packed2_tc_supported(a);
+    const bool tcw_ok = mm::gemm_packed2_tcw_supported(a);
     if (tile >= 32 && !tc_ok)
         return fail(MM_ERR_INVALID_ARG, "tensor-core tile needs fp16-exact codebook entries, cols %% 8 == 0 and 16-byte aligned X");
+    if (tile == 2 && !tcw_ok)
+        return fail(MM_ERR_INVALID_ARG,
+                    "tile 2 needs fp16-exact codebook entries, cols %% 64 == 0 and 16-byte aligned codes and X");
+    if (tile == 2 && splitk && !mm::gemm_packed2_tcw_fits(M, cols, splitk))
+        return fail(MM_ERR_INVALID_ARG,
+                    "tile 2: splitk must leave each CTA 1 to 8 of the cols / 64 atoms, within shared memory with X");
     s = check_device();
     if (s != MM_OK) return s;
     cudaError_t e;
-    if (tc_ok && tile != 1) e = mm::launch_gemm_packed2_tc(a, tile, splitk, reinterpret_cast<cudaStream_t>(stream));
-    else e = mm::launch_gemm_packed2(a, 0, reinterpret_cast<cudaStream_t>(stream));
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    // automatic: the pipelined kernel (tile 32 / 64 / 128) measured faster than tile 2 on the
+    // ternary encoder shapes, whose cluster reduction of 128 x 224 partial tiles costs more
+    // than the split saves
+    if (tile == 2) e = mm::launch_gemm_packed2_tcw(a, splitk, pdl, weights_static, st);
+    else if (tc_ok && tile != 1) e = mm::launch_gemm_packed2_tc(a, tile, splitk, st);
+    else e = mm::launch_gemm_packed2(a, 0, st);
     if (e != cudaSuccess) return cuda_fail(e, "packed gemm launch");
     return ok();
 }
@@ -350,6 +365,9 @@ mm_status mm_check_device_error(mm_stream_t stream) {
     const unsigned int zw = mm::gemm_tf32x3_ws_take_device_error(&e);
     if (e != cudaSuccess) return cuda_fail(e, "mm_check_device_error");
     if (zw != 0) return fail(MM_ERR_TIMEOUT, "a bounded device wait ran out in the warp-specialised 3xTF32 GEMM (code %u)", zw);
+    const unsigned int tw = mm::gemm_packed2_tcw_take_device_error(&e);
+    if (e != cudaSuccess) return cuda_fail(e, "mm_check_device_error");
+    if (tw != 0) return fail(MM_ERR_TIMEOUT, "a bounded device wait ran out in the tensor-core packed GEMM, tile 2 (code %u)", tw);
     const unsigned int q = mm::gemv_tma_take_device_error(&e);
     if (e != cudaSuccess) return cuda_fail(e, "mm_check_device_error");
     if (q != 0) return fail(MM_ERR_TIMEOUT, "a bounded device wait ran out in the staged GEMV (code %u)", q);

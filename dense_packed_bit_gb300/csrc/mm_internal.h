@@ -92,6 +92,15 @@ bool gemm_packed2_tc_supported(const PackedArgs &a);
 cudaError_t launch_gemm_packed2_tc(const PackedArgs &a, int tile, int splitk, cudaStream_t s);
 unsigned int gemm_packed2_tc_take_device_error(cudaError_t *err);
 
+// Skinny packed GEMM with the decoded weights as the MMA's A operand (128 W rows
+// per CTA) and the tokens as its N (up to 256): fp16-exact codebook, cols % 64 == 0,
+// 16-byte aligned codes and X; K split over a cluster of `splitk` CTAs (0 = auto).
+int gemm_packed2_tcw_split(int64_t M, int64_t rows, int64_t cols, int sms);
+bool gemm_packed2_tcw_fits(int64_t M, int64_t cols, int splitk);  // a share of K fits one CTA
+bool gemm_packed2_tcw_supported(const PackedArgs &a);
+cudaError_t launch_gemm_packed2_tcw(const PackedArgs &a, int splitk, int pdl, int weights_static, cudaStream_t s);
+unsigned int gemm_packed2_tcw_take_device_error(cudaError_t *err);
+
 // ------------------------------------------------------------------ dense GEMM
 
 struct GemmArgs {

@@ -4,7 +4,7 @@
     python -m dense_packed_bit_gb300.profile_case gemv --reps 3 [--split 8 --rows 4 --warps 8 --dequant 2 --independent 1]
     python -m dense_packed_bit_gb300.profile_case gemv --reps 3 --split 0 --rows 1 --warps 0 --dequant 2 --staging 1
     python -m dense_packed_bit_gb300.profile_case gemv4 --reps 3 [--staging 1 --rows 1 --independent 1]
-    python -m dense_packed_bit_gb300.profile_case ternary --reps 1
+    python -m dense_packed_bit_gb300.profile_case ternary --reps 1 [--tile 2] [--pdl 2: pdl + static weights]
 
 One warm-up launch precedes the `reps` launches.  No timing is done here:
 numbers come from the profiler or from bench.py.
@@ -86,7 +86,11 @@ def main(argv=None):
                                torch.empty((c.X.shape[0], c.rows), dtype=torch.float32, device=dev)))
         for _ in range(1 + a.reps):
             for c, dc, ds, dX, dY in layers:
-                mm.mm_gemm_packed2(dc, ds, dX, dY, c.X.shape[0], c.rows, c.cols, c.codebook)
+                if a.tile or a.pdl == 2:
+                    mm.mm_gemm_packed2_ex(dc, ds, dX, dY, c.X.shape[0], c.rows, c.cols, c.codebook, tile=a.tile,
+                                          pdl=int(a.pdl == 2), weights_static=int(a.pdl == 2))
+                else:
+                    mm.mm_gemm_packed2(dc, ds, dX, dY, c.X.shape[0], c.rows, c.cols, c.codebook)
     mm.mm_check_device_error()
     torch.cuda.synchronize()
     print("ok")

@@ -154,7 +154,7 @@ def test_missing_library_fails_loudly(monkeypatch):
         mod.load_library()
 
 
-@pytest.mark.parametrize("tile", [-1, 2, 48, 256])
+@pytest.mark.parametrize("tile", [-1, 3, 48, 256])
 def test_gemm_packed_bad_tile(lib, tile):
     o = mm.GemmPacked2Opts(tile)
     st = lib.mm_gemm_packed2_ex(FAKE, FAKE + 0x100000, FAKE + 0x200000, FAKE + 0x300000, 4, 64, 64,
@@ -167,6 +167,18 @@ def test_gemm_packed_tensor_core_tile_needs_fp16_codebook(lib):
     st = lib.mm_gemm_packed2_ex(FAKE, FAKE + 0x100000, FAKE + 0x200000, FAKE + 0x300000, 4, 64, 64,
                                 _cb(0.3, -1.7, 2.5, 0.01), None, ctypes.byref(o))
     assert st == mm.MM_ERR_INVALID_ARG and b"fp16" in lib.mm_last_error()
+
+
+@pytest.mark.parametrize("opt", [dict(tile=2, cols=100), dict(tile=2, splitk=16, cols=640),
+                                 dict(tile=2, splitk=1, cols=1024), dict(pdl=2), dict(pdl=0, weights_static=1),
+                                 dict(tile=64, splitk=16)])
+def test_gemm_packed_tile2_bad_options(lib, opt):
+    # tile 2 needs cols % 64 == 0 and 1 to 8 atoms of 64 per CTA; weights_static needs pdl
+    cols = opt.pop("cols", 640)
+    o = mm.GemmPacked2Opts(**opt)
+    st = lib.mm_gemm_packed2_ex(FAKE, FAKE + 0x100000, FAKE + 0x200000, FAKE + 0x300000, 4, 64, cols,
+                                _cb(-1, 0, 1, 0), None, ctypes.byref(o))
+    assert st == mm.MM_ERR_INVALID_ARG, lib.mm_last_error()
 
 
 @pytest.mark.parametrize("splitk", [-1, 3, 16])

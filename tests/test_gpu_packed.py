@@ -36,13 +36,13 @@ def gemv(codes, scales, x, rows, cols, cb, **opts):
     return to_host(dy)
 
 
-def gemm_packed(codes, scales, X, M, rows, cols, cb, tile=None, splitk=0):
+def gemm_packed(codes, scales, X, M, rows, cols, cb, tile=None, splitk=0, **opts):
     dc, ds, dX = to_dev(codes), to_dev(scales), to_dev(X)
     dY = empty_f32((M, rows))
-    if tile is None and not splitk:
+    if tile is None and not splitk and not opts:
         mm.mm_gemm_packed2(dc, ds, dX, dY, M, rows, cols, cb)
     else:
-        mm.mm_gemm_packed2_ex(dc, ds, dX, dY, M, rows, cols, cb, tile=tile or 0, splitk=splitk)
+        mm.mm_gemm_packed2_ex(dc, ds, dX, dY, M, rows, cols, cb, tile=tile or 0, splitk=splitk, **opts)
     mm.mm_check_device_error()
     return to_host(dY)
 
@@ -278,6 +278,104 @@ def test_gemm_packed_cluster_splitk(oracle, splitk, tile, M, rows, cols):
     Y = gemm_packed(codes, scales, X, M, rows, cols, CBT, tile=tile, splitk=splitk)
     ref, T = oracle.packed_gemm(codes, scales, X, rows, cols, CBT)
     check_bound(Y, ref, T, f"splitk {splitk} tile {tile}")
+
+
+# ------------------------------------------------------------------ tile 2: W rows as the MMA's M
+
+TILE2_SHAPES = [(1, 1, 64), (3, 33, 64), (129, 130, 192), (222, 256, 768), (300, 65, 1536), (17, 3072, 64),
+                (222, 3072, 768), (222, 768, 3072), (257, 200, 640), (512, 100, 128)]
+
+
+@pytest.mark.parametrize("M,rows,cols", TILE2_SHAPES)
+@pytest.mark.parametrize("cb", ["ternary", "2bit"])
+def test_gemm_packed_tile2_auto_split(oracle, M, rows, cols, cb):
+    # ragged feature tiles (rows not a multiple of 128), ragged and multiple token tiles
+    # (M > 256), the automatic split of K over a cluster
+    codebook = CBT if cb == "ternary" else CB2
+    codes, scales, X = rand_case(rows, cols, M=M, seed=11 * M + rows + 5 * cols,
+                                 kind="ternary" if cb == "ternary" else "uniform2")
+    Y = gemm_packed(codes, scales, X, M, rows, cols, codebook, tile=2)
+    ref, T = oracle.packed_gemm(codes, scales, X, rows, cols, codebook)
+    check_bound(Y, ref, T, f"tile 2 {M}x{rows}x{cols}")
+
+
+@pytest.mark.parametrize("splitk", [1, 2, 4, 8, 16])
+@pytest.mark.parametrize("M,rows,cols", [(222, 300, 512), (40, 128, 1024), (222, 768, 3072), (5, 17, 1600)])
+def test_gemm_packed_tile2_cluster_splitk(oracle, splitk, M, rows, cols):
+    # every cluster size; 1600 columns: 25 atoms, uneven shares; shares of more than
+    # 8 atoms are refused
+    atoms = cols // 64
+    if splitk > atoms or -(-atoms // splitk) > 8 or (M > 128 and -(-atoms // splitk) > 4):
+        pytest.skip("share does not fit one CTA")
+    codes, scales, X = rand_case(rows, cols, M=M, seed=splitk * 31 + M + rows, kind="ternary")
+    Y = gemm_packed(codes, scales, X, M, rows, cols, CBT, tile=2, splitk=splitk)
+    ref, T = oracle.packed_gemm(codes, scales, X, rows, cols, CBT)
+    check_bound(Y, ref, T, f"tile 2 splitk {splitk} {M}x{rows}x{cols}")
+
+
+@pytest.mark.parametrize("splitk", [2, 4])
+def test_gemm_packed_tile2_integer_exact(oracle, splitk):
+    # integer activations, scale 1, integer codebook: exact in any summation order
+    M, rows, cols = 150, 200, 512
+    codes, _, _ = rand_case(rows, cols, M=M, seed=5)
+    scales = np.full(rows, 0x3C00, np.uint16)
+    rng = np.random.default_rng(8)
+    X = rng.integers(-4, 5, size=(M, cols)).astype(np.float16).view(np.uint16)
+    Y = gemm_packed(codes, scales, X, M, rows, cols, CB2, tile=2, splitk=splitk)
+    ref, _ = oracle.packed_gemm(codes, scales, X, rows, cols, CB2)
+    check_exact(Y, ref, f"tile 2 splitk {splitk}")
+
+
+def test_gemm_packed_tile2_deterministic():
+    c = synth.ternary_encoder_layer(3, "down")
+    M = c.X.shape[0]
+    y1 = gemm_packed(c.codes, c.scales, c.X, M, c.rows, c.cols, c.codebook, tile=2)
+    y2 = gemm_packed(c.codes, c.scales, c.X, M, c.rows, c.cols, c.codebook, tile=2)
+    assert np.array_equal(y1.view(np.uint32), y2.view(np.uint32))
+
+
+@pytest.mark.parametrize("weights_static", [0, 1])
+def test_gemm_packed_tile2_pdl_waits_before_writing_and_reading(oracle, weights_static):
+    # Back-to-back calls with programmatic dependent launch on one stream.
+    # Call 2 writes its Y over the bytes of call 1's X (write after read), and call 3
+    # reads as X the bytes call 2 wrote (read after write).  Integer activations, an
+    # integer codebook and scale 1 make every Y an integer below 2^11, whose fp32 bits
+    # read as two finite fp16 values, so the oracle can follow the chain exactly.
+    import torch
+    M, rows, cols = 222, 768, 1024
+    rng = np.random.default_rng(21)
+    cb = CB2
+    ones = np.full(rows, 0x3C00, np.uint16)
+    codes = [rand_case(rows, cols, M=1, seed=40 + i)[0] for i in range(3)]
+    X1 = rng.integers(-2, 3, size=(M, cols)).astype(np.float16).view(np.uint16)
+    X2 = rng.integers(-2, 3, size=(M, cols)).astype(np.float16).view(np.uint16)
+    dev = torch.device("cuda:0")
+    buf = torch.zeros(M * rows * 4, dtype=torch.uint8, device=dev)   # holds X1, then Y2, read as X3
+    buf[: X1.nbytes].copy_(torch.from_numpy(X1.view(np.uint8).reshape(-1)))
+    dX1 = buf[: X1.nbytes].view(torch.int16).view(M, cols)
+    dY2 = buf.view(torch.float32).view(M, rows)
+    dX3 = buf.view(torch.int16).view(M, 2 * rows)                     # cols of call 3 = 2 * rows
+    codes3 = rand_case(rows, 2 * rows, M=1, seed=43)[0]
+    dc = [to_dev(codes[0]), to_dev(codes[1]), to_dev(codes3)]
+    ds = to_dev(ones)
+    dX2 = to_dev(X2)
+    dY1 = empty_f32((M, rows))
+    dY3 = empty_f32((M, rows))
+    opts = dict(tile=2, pdl=1, weights_static=weights_static)
+    for _ in range(3):
+        buf[: X1.nbytes].copy_(torch.from_numpy(X1.view(np.uint8).reshape(-1)))
+        mm.mm_gemm_packed2_ex(dc[0], ds, dX1, dY1, M, rows, cols, cb, **opts)
+        mm.mm_gemm_packed2_ex(dc[1], ds, dX2, dY2, M, rows, cols, cb, **opts)
+        mm.mm_gemm_packed2_ex(dc[2], ds, dX3, dY3, M, rows, 2 * rows, cb, **opts)
+        mm.mm_check_device_error()
+        ref1, _ = oracle.packed_gemm(codes[0], ones, X1, rows, cols, cb)
+        ref2, _ = oracle.packed_gemm(codes[1], ones, X2, rows, cols, cb)
+        check_exact(to_host(dY1), ref1, "call 1 read X1 before call 2 overwrote it")
+        check_exact(to_host(dY2), ref2, "call 2")
+        X3 = ref2.astype(np.float32).view(np.uint16).reshape(M, 2 * rows)
+        assert np.all(np.isfinite(X3.view(np.float16)))
+        ref3, T3 = oracle.packed_gemm(codes3, ones, X3, rows, 2 * rows, cb)
+        check_bound(to_host(dY3), ref3, T3, "call 3 read call 2's Y")
 
 
 @pytest.mark.parametrize("rows", [1, 63, 64, 65, 1000, 1100])
