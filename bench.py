@@ -245,7 +245,7 @@ class Workload:
 
 
 GEMV_INDEP = dict(dequant=2, staging=1, rows_per_lane=3, pdl=1, independent=1)
-GEMV_CHAINED = dict(split=3, rows_per_lane=2, warps=6, dequant=3, pdl=1, weights_static=1)
+GEMV_CHAINED = dict(dequant=2, staging=1, rows_per_lane=1, pdl=1, weights_static=1)
 GEMV_INDEP_STREAMS = 2  # independent calls alternate between two streams inside the graph
 GEMV4_INDEP = dict(staging=1, blocks=1, pdl=1, independent=1)
 

@@ -148,7 +148,6 @@ __global__ void __launch_bounds__(NTHREADS, 1)
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int f0 = blockIdx.x * FM, t0 = blockIdx.y * p.ntok;
-    if (p.pdl) pdl_launch_dependents();
 
     // byte -> fp16 codebook entries of its 4 fields, in K order
     for (int b = tid; b < 256; b += NTHREADS) {
@@ -186,6 +185,9 @@ __global__ void __launch_bounds__(NTHREADS, 1)
             mbar_arrive_expect_tx(bar_c, (uint32_t)(p.kcmax * FM * 16));  // the whole box
             tma_load_2d(sC, &tmC, bar_c, a0 * 16, f0);
             pdl_wait();  // X may be the previous kernel's output
+            // the next call may launch once this one has passed its wait (not before: a chain
+            // of calls would otherwise park every later call's CTAs on the SMs)
+            if (p.pdl) pdl_launch_dependents();
             mbar_arrive_expect_tx(bar_x, (uint32_t)(kc * p.ntok * 128));
             for (int a = 0; a < kc; ++a) tma_load_2d(sX + a * p.ntok * 128, &tmX, bar_x, (a0 + a) * KATOM, t0);
             // both copies must land before this CTA's shared memory is released

@@ -141,8 +141,10 @@ __global__ void __launch_bounds__(512) gemv2_vec_kernel(const PackedArgs a, cons
     // 2 no wait at all (the caller promised no dependence on queued work)
     if (prefetch >= 1) {
         load_batch(0);
-        pdl_launch_dependents();
+        // chained calls: the next call may launch only once this one has passed its wait,
+        // so at most one call runs ahead (its weight loads) instead of a queue of parked ones
         if (prefetch == 1) pdl_wait();
+        pdl_launch_dependents();
     } else {
         pdl_wait();
         load_batch(0);

@@ -193,11 +193,13 @@ __global__ void __launch_bounds__(512) gemv2_fp8_kernel(const __grid_constant__ 
             for (int i = 0; i < first; ++i) issue(i);
             if (prefetch == 2) issue_x();
         }
-        pdl_launch_dependents();
+        // chained calls: the next call may launch only once this one has passed its wait,
+        // so at most one call runs ahead (its weight loads) instead of a queue of parked ones
         if (prefetch == 1) {
             pdl_wait();
             if (leader) issue_x();
         }
+        pdl_launch_dependents();
     } else {
         pdl_wait();
         if (leader) {

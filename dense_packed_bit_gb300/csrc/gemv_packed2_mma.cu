@@ -85,8 +85,10 @@ __global__ void __launch_bounds__(RB == 1 ? 512 : 256) gemv2_mma_kernel(const Pa
 
     if (prefetch >= 1) {
         load(s_begin);
-        pdl_launch_dependents();
+        // chained calls: the next call may launch only once this one has passed its wait,
+        // so at most one call runs ahead (its weight loads) instead of a queue of parked ones
         if (prefetch == 1) pdl_wait();
+        pdl_launch_dependents();
     } else {
         pdl_wait();
         load(s_begin);

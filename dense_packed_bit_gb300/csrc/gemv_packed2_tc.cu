@@ -265,11 +265,13 @@ __global__ void __launch_bounds__(NTHREADS) gemv2_tc_kernel(const __grid_constan
             for (; issued_boxes < min(bring, total_boxes); ++issued_boxes) issue_box(issued_boxes);
             if (prefetch == 2) issue_x();
         }
-        pdl_launch_dependents();
+        // chained calls: the next call may launch only once this one has passed its wait,
+        // so at most one call runs ahead (its weight loads) instead of a queue of parked ones
         if (prefetch == 1) {
             pdl_wait();
             if (warp == PRODUCER_WARP && lane == 0) issue_x();
         }
+        pdl_launch_dependents();
     } else {
         pdl_wait();
         if (warp == PRODUCER_WARP && lane == 0) {

@@ -75,8 +75,10 @@ __global__ void __launch_bounds__(512) gemv2_tma_kernel(const __grid_constant__ 
     };
     if (prefetch >= 1) {
         issue_first();
-        pdl_launch_dependents();
+        // chained calls: the next call may launch only once this one has passed its wait,
+        // so at most one call runs ahead (its weight loads) instead of a queue of parked ones
         if (prefetch == 1) pdl_wait();
+        pdl_launch_dependents();
     } else {
         pdl_wait();
         issue_first();

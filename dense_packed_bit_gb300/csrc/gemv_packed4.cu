@@ -122,8 +122,10 @@ __global__ void __launch_bounds__(32 * NW) gemv4_lut_kernel(const __grid_constan
             tma_prefetch_desc(&tmC);
             for (int i = 0; i < first; ++i) issue(i);
         }
-        pdl_launch_dependents();
+        // chained calls: the next call may launch only once this one has passed its wait,
+        // so at most one call runs ahead (its weight loads) instead of a queue of parked ones
         if (prefetch == 1) pdl_wait();
+        pdl_launch_dependents();
     } else {
         pdl_wait();
         if (leader) {

@@ -183,21 +183,19 @@ mm_status mm_gemv_packed2_ex(const uint8_t *codes, const uint16_t *scales, const
     }
     const bool affine = mm::codebook_is_affine(codebook);
     mm::PackedArgs a{codes, scales, x, y, 1, rows, cols, {codebook[0], codebook[1], codebook[2], codebook[3]}};
-    // automatic decode, by measurement on GB300 (12,288 x 1,536): calls promised independent
-    // are bound by issue throughput, where the SIMT affine decode is fastest; otherwise each
-    // call's latency matters and the fp16 tensor-core decode is fastest
-    if (cfg.dequant == MM_DEQ_AUTO)
-        cfg.dequant = !affine ? MM_DEQ_SELECT
-                      : (!cfg.independent && mm::gemv_mma_supported(a)) ? MM_DEQ_MMA : MM_DEQ_AFFINE;
+    // automatic decode, by measurement on GB300 (12,288 x 1,536): the SIMT affine decode is the
+    // fastest both for independent calls (bound by issue throughput) and for chained ones
+    if (cfg.dequant == MM_DEQ_AUTO) cfg.dequant = affine ? MM_DEQ_AFFINE : MM_DEQ_SELECT;
     if (cfg.dequant < MM_DEQ_SELECT || cfg.dequant > MM_DEQ_TC)
         return fail(MM_ERR_INVALID_ARG, "unknown dequant %d", cfg.dequant);
     if (cfg.dequant != MM_DEQ_SELECT && !affine)
         return fail(MM_ERR_INVALID_ARG, "affine decode needs codebook[c] == codebook[0] + c*(codebook[1]-codebook[0])");
-    // automatic staging: the TMA-staged affine kernel is the fastest measured for independent
-    // calls; the staged tensor-core decode measured slower than register loads
+    // automatic staging: the TMA-staged affine kernel is the fastest measured, for independent
+    // calls (three 128-row blocks per CTA) and chained ones (one block per CTA, its weights
+    // loaded before the wait on the previous kernel when they are promised static); the staged
+    // tensor-core decode measured slower than register loads
     if (cfg.staging < 0)
-        cfg.staging = (cfg.dequant == MM_DEQ_AFFINE && cfg.independent && !cfg.split && !cfg.warps &&
-                       mm::gemv_rows_supported(a)) ? 1 : 0;
+        cfg.staging = (cfg.dequant == MM_DEQ_AFFINE && !cfg.split && !cfg.warps && mm::gemv_rows_supported(a)) ? 1 : 0;
     if (cfg.staging != 0 && cfg.staging != 1) return fail(MM_ERR_INVALID_ARG, "staging must be 0 or 1");
     if (cfg.staging && cfg.dequant < MM_DEQ_FP8 &&
         !(cfg.dequant == MM_DEQ_MMA && mm::gemv_tma_supported(a)) &&

@@ -150,10 +150,9 @@ mm_status mm_gemm_f32_ex(int transA, int transB, int64_t M, int64_t N, int64_t K
                          float *C, int64_t ldc, mm_stream_t stream, const mm_gemm_opts *opts);
 
 enum {
-    MM_DEQ_AUTO = 0,     /* MM_DEQ_MMA for calls not promised independent (cols % 256 == 0),
-                            MM_DEQ_AFFINE (TMA-staged when the shape allows) for independent
-                            calls, MM_DEQ_SELECT when the codebook is not affine: the fastest
-                            measured on GB300 */
+    MM_DEQ_AUTO = 0,     /* MM_DEQ_AFFINE (TMA-staged when the shape allows), MM_DEQ_SELECT
+                            when the codebook is not affine: the fastest measured on GB300 for
+                            independent and for chained calls */
     MM_DEQ_SELECT = 1,   /* any codebook: per-field select of the entry, fp32 FMA */
     MM_DEQ_AFFINE = 2,   /* codebook[c] = c0 + c*d exactly (and no zero entry at field 3):
                             fields used in place as exact fp32 subnormals in packed f32x2
@@ -206,8 +205,8 @@ typedef struct {
                             128-row blocks, one lane per row, eight warps splitting K,
                             rows_per_lane = 128-row blocks per CTA (0 = 3 for independent
                             calls, 1 otherwise).  0 = per-warp register loads; negative =
-                            automatic (staged for independent affine calls when the shape
-                            allows, the default without options). */
+                            automatic (staged for affine calls when the shape allows, the
+                            default without options). */
     int reserved[4];
 } mm_gemv_opts;
 
