@@ -11,7 +11,9 @@ Prints ONE JSON line (rank 0).  One step is one pass of the whole hot path:
      independent calls (programmatic dependent launch, no call waits for the
      previous one) and as a dependent chain (each call waits for the previous
      kernel before reading x; only its weight loads start early);
-  3. the ternary 16-layer encoder block: 16 x (222x768 -> 3072, 222x3072 -> 768).
+  3. the ternary 16-layer encoder block: 16 x (222x768 -> 3072, 222x3072 -> 768);
+  4. the 4-bit 12,288 x 1,536 GEMV and the transposed 2-bit 1,536 x 12,288 GEMV,
+     each over a 64-matrix rotation of independent calls.
 Each phase is captured once as a CUDA graph and replayed; every replay is timed
 with CUDA events on the stream it runs on.  The headline value is the 2048^3
 GEMM throughput (TFLOP/s); the GEMV weight bandwidth (GB/s: 4,718,592 bytes of
@@ -47,12 +49,14 @@ GEMV_WEIGHT_BYTES = 12288 * 1536 // 4           # 4,718,592
 GEMV_TOTAL_BYTES = GEMV_WEIGHT_BYTES + 12288 * 2 + 1536 * 2 + 12288 * 4
 GEMV4_WEIGHT_BYTES = 12288 * 1536 // 2          # 9,437,184
 GEMV4_TOTAL_BYTES = GEMV4_WEIGHT_BYTES + 12288 * 2 + 1536 * 2 + 12288 * 4
+GEMVT_TOTAL_BYTES = GEMV_WEIGHT_BYTES + 1536 * 2 + 12288 * 2 + 1536 * 4   # 1536 x 12288: same weight bytes
 GEMM_FLOP = 2.0 * 2048 ** 3
 TERN_FLOP_PER_LAYER = 2 * (2.0 * 222 * 3072 * 768)
 N_GEMV = 64
 N_LAYERS = 16
 WORKLOAD = ("square_2048_fp32_gemm_nn_nt_tn + gemv2bit_12288x1536_rotation64 + "
-            "ternary_encoder_16x(222x768x3072,222x3072x768) + gemv4bit_12288x1536_rotation64")
+            "ternary_encoder_16x(222x768x3072,222x3072x768) + gemv4bit_12288x1536_rotation64 + "
+            "gemv2bit_1536x12288_rotation64")
 
 
 def parse_args(argv=None):
@@ -232,6 +236,14 @@ class Workload:
             self.gemv4_cb = c.codebook
         self.gemv4_x = torch.from_numpy(x4.reshape(-1)).to(device)
         self.gemv4_y = torch.empty((N_GEMV, 12288), dtype=torch.float32, device=device)
+        self.gemvt_codes, self.gemvt_scales = [], []
+        for i in range(N_GEMV):
+            c = synth.gemv_2bit_1536x12288(i + (off % 1000) * N_GEMV if off else i)
+            self.gemvt_codes.append(torch.from_numpy(c.codes).to(device))
+            self.gemvt_scales.append(torch.from_numpy(c.scales).to(device))
+            xt = c.X
+        self.gemvt_x = torch.from_numpy(xt.reshape(-1)).to(device)
+        self.gemvt_y = torch.empty((N_GEMV, 1536), dtype=torch.float32, device=device)
         self.tern = []
         for layer in range(N_LAYERS):
             for proj in ("up", "down"):
@@ -248,6 +260,7 @@ GEMV_INDEP = dict(dequant=2, staging=1, rows_per_lane=3, pdl=1, independent=1)
 GEMV_CHAINED = dict(dequant=2, staging=1, rows_per_lane=1, pdl=1, weights_static=1)
 GEMV_INDEP_STREAMS = 2  # independent calls alternate between two streams inside the graph
 GEMV4_INDEP = dict(staging=1, blocks=1, pdl=1, independent=1)
+GEMVT_INDEP = dict(pdl=1, independent=1)  # automatic decode and shape for 1536 x 12288
 
 
 def capture_phases(w: Workload, stream):
@@ -296,6 +309,15 @@ def capture_phases(w: Workload, stream):
                                   w.gemv4_cb, st, **GEMV4_INDEP)
         cur.wait_stream(side)
 
+    def gemvt():
+        cur = torch.cuda.current_stream()
+        side.wait_stream(cur)
+        for i in range(N_GEMV):
+            st = side if i % 2 else cur
+            mm.mm_gemv_packed2_ex(w.gemvt_codes[i], w.gemvt_scales[i], w.gemvt_x, w.gemvt_y[i], 1536, 12288,
+                                  w.gemv_cb, st, **GEMVT_INDEP)
+        cur.wait_stream(side)
+
     def tern():
         for t in w.tern:
             c = t["case"]
@@ -303,7 +325,7 @@ def capture_phases(w: Workload, stream):
 
     graphs = {}
     for name, fn in (("gemm", gemm), ("gemv", gemv(GEMV_INDEP, GEMV_INDEP_STREAMS)), ("gemv_c", gemv(GEMV_CHAINED)),
-                     ("tern", tern), ("gemv4", gemv4)):
+                     ("tern", tern), ("gemv4", gemv4), ("gemvt", gemvt)):
         with torch.cuda.stream(stream):
             fn()  # warm the kernels' one-time setup outside capture
         torch.cuda.synchronize()
@@ -314,13 +336,13 @@ def capture_phases(w: Workload, stream):
     return graphs
 
 
-LAUNCHES_PER_STEP = 3 + 3 * N_GEMV + 2 * N_LAYERS
+LAUNCHES_PER_STEP = 3 + 4 * N_GEMV + 2 * N_LAYERS
 
 
 def run_step(w: Workload, graphs, ev, stream):
     """One pass of the hot path; ev maps each phase to a (start, end) event pair."""
     w.flush.fill_(1.0)  # evict the GEMM operands from L2 (torch kernel, outside the events)
-    for name in ("gemm", "gemv", "gemv_c", "tern", "gemv4"):
+    for name in ("gemm", "gemv", "gemv_c", "tern", "gemv4", "gemvt"):
         ev[name][0].record(stream)
         graphs[name].replay()
         ev[name][1].record(stream)
@@ -329,7 +351,7 @@ def run_step(w: Workload, graphs, ev, stream):
 def new_events():
     import torch
     mk = lambda: (torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-    return {"gemm": mk(), "gemv": mk(), "gemv_c": mk(), "tern": mk(), "gemv4": mk()}
+    return {"gemm": mk(), "gemv": mk(), "gemv_c": mk(), "tern": mk(), "gemv4": mk(), "gemvt": mk()}
 
 
 def e2e_gemm(w: Workload, steps: int, stream):
@@ -482,6 +504,7 @@ def main_mm(args):
     gemvc_total_s = total_s("gemv_c")
     tern_total_s = total_s("tern")
     gemv4_total_s = total_s("gemv4")
+    gemvt_total_s = total_s("gemvt")
     wall = reduce_max(wall, dev)
 
     gemm_tflops = world * 3 * GEMM_FLOP * args.steps / gemm_total_s / 1e12
@@ -490,7 +513,8 @@ def main_mm(args):
     gemv_gbs = world * GEMV_WEIGHT_BYTES / per_call_gemv_s / 1e9
     tern_tflops = world * N_LAYERS * TERN_FLOP_PER_LAYER * args.steps / tern_total_s / 1e12
     per_call_gemv4_s = gemv4_total_s / (args.steps * N_GEMV)
-    step_ms = (gemm_total_s + gemv_total_s + gemvc_total_s + tern_total_s + gemv4_total_s) / args.steps * 1e3
+    per_call_gemvt_s = gemvt_total_s / (args.steps * N_GEMV)
+    step_ms = (gemm_total_s + gemv_total_s + gemvc_total_s + tern_total_s + gemv4_total_s + gemvt_total_s) / args.steps * 1e3
 
     peaks, peaks_src = measured_peaks()
     props = torch.cuda.get_device_properties(dev)
@@ -521,6 +545,7 @@ def main_mm(args):
         "config": {"workload": WORKLOAD, "gemm": "2048x2048x2048 fp32 NN+NT+TN, N(0,0.02)",
                    "gemv": "12288x1536 2-bit, 64-matrix rotation (288 MiB > L2), codebook {-2,-1,0,1}",
                    "ternary": "16 layers, M=222, up 768->3072 and down 3072->768",
+                   "gemv_t": "1536x12288 2-bit, 64-matrix rotation (288 MiB > L2)",
                    "l2": "512 MiB buffer written before the GEMM phase of every step; GEMV inputs exceed L2",
                    "gemv_opts": {"independent": GEMV_INDEP, "independent_streams": GEMV_INDEP_STREAMS,
                                  "chained": GEMV_CHAINED},
@@ -548,6 +573,15 @@ def main_mm(args):
                                "peak": peaks["hbm_gbs"], "unit": "GB/s",
                                "frac": GEMV4_TOTAL_BYTES / per_call_gemv4_s / 1e9 / peaks["hbm_gbs"],
                                "traffic": traffic_for("gemv4_lut"), "peak_source": peaks_src}},
+        "gemv_t": {"metric": "2-bit 1536x12288 GEMV weight GB/s (transposed shape)",
+                   "value": world * GEMV_WEIGHT_BYTES / per_call_gemvt_s / 1e9, "unit": "GB/s",
+                   "us_per_call": per_call_gemvt_s * 1e6,
+                   "mode": "64 independent back-to-back calls over the rotation, two streams",
+                   "opts": GEMVT_INDEP,
+                   "roofline": {"bound": "hbm", "achieved": GEMVT_TOTAL_BYTES / per_call_gemvt_s / 1e9,
+                                "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                                "frac": GEMVT_TOTAL_BYTES / per_call_gemvt_s / 1e9 / peaks["hbm_gbs"],
+                                "traffic": None, "peak_source": peaks_src}},
         "roofline": roof,
         "clocks": clk,
         "gpu_launches": LAUNCHES_PER_STEP * args.steps,

@@ -265,6 +265,15 @@ def gemv_2bit_12288x1536(index: int) -> PackedCase:
                       CODEBOOK_2BIT.copy(), x)
 
 
+def gemv_2bit_1536x12288(index: int) -> PackedCase:
+    """The transposed shape (the pages' kernel 0113): 1536 rows x 12288 cols of 2-bit codes,
+    4.5 MiB per matrix like the 12288 x 1536 one; same value distributions."""
+    codes, scales = packed_matrix(6, index, 1536, 12288, "uniform2")
+    x = normal_f16_bits(_seed(6, 3, 0), (1, 12288))
+    return PackedCase(f"gemv2_1536x12288_m{index}", 1536, 12288, codes, scales,
+                      CODEBOOK_2BIT.copy(), x)
+
+
 def gemv_4bit_12288x1536(index: int) -> PackedCase:
     """One of the 64 rotated 4-bit GEMV matrices: 12288 rows x 1536 cols (9 MiB of codes),
     fields uniform in 0..15 (two per byte), normal-quantile codebook."""

@@ -280,6 +280,22 @@ def test_gemm_packed_cluster_splitk(oracle, splitk, tile, M, rows, cols):
     check_bound(Y, ref, T, f"splitk {splitk} tile {tile}")
 
 
+# ------------------------------------------------------------------ transposed shape (1,536 x 12,288)
+
+@pytest.mark.parametrize("mode", [dict(), dict(pdl=1, independent=1), dict(pdl=1, weights_static=1),
+                                  dict(dequant=2, staging=0, split=16, rows_per_lane=4, warps=8),
+                                  dict(dequant=3, split=4, rows_per_lane=2, warps=4),
+                                  dict(dequant=1, split=16, rows_per_lane=1, warps=4)])
+def test_gemv_transposed_1536x12288(oracle, mode):
+    # the pages' transposed kernel shape: few rows, 12,288 fields each; automatic and explicit
+    # decodes, every output of two rotated matrices
+    for i in (0, 63):
+        c = synth.gemv_2bit_1536x12288(i)
+        y = gemv(c.codes, c.scales, c.X, c.rows, c.cols, c.codebook, **mode)
+        ref, T = oracle.packed_gemm(c.codes, c.scales, c.X, c.rows, c.cols, c.codebook)
+        check_bound(y, ref[0], T[0], f"{c.name} {mode}")
+
+
 # ------------------------------------------------------------------ tile 2: W rows as the MMA's M
 
 TILE2_SHAPES = [(1, 1, 64), (3, 33, 64), (129, 130, 192), (222, 256, 768), (300, 65, 1536), (17, 3072, 64),
