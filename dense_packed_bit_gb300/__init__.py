@@ -70,6 +70,9 @@ SIGNATURES = {
     "mm_gemm_packed2_ex": ([_P, _P, _P, _P, _I64, _I64, _I64, _P, _P, ctypes.POINTER(GemmPacked2Opts)],
                            ctypes.c_int),
     "mm_check_device_error": ([_P], ctypes.c_int),
+    "mm_gemm_f32_splitk_workspace": ([_I64, _I64, _I64, _I, ctypes.POINTER(ctypes.c_int64)], ctypes.c_int),
+    "mm_gemm_f32_splitk": ([_I, _I, _I64, _I64, _I64, _P, _I64, _P, _I64, _P, _I64, _I, _P, _I64, _P],
+                           ctypes.c_int),
 }
 
 
@@ -150,6 +153,20 @@ def mm_gemm_f32_ex(transA, transB, M, N, K, A, lda, B, ldb, C, ldc, stream=None,
     o = GemmOpts(path, tile)
     _check(load_library().mm_gemm_f32_ex(int(transA), int(transB), M, N, K, _ptr(A), lda, _ptr(B), ldb,
                                          _ptr(C), ldc, _stream(stream), ctypes.byref(o)))
+
+
+def mm_gemm_f32_splitk_workspace(M, N, K, splitk=0) -> int:
+    """Floats of workspace mm_gemm_f32_splitk needs for these sizes and split (0 = automatic)."""
+    out = ctypes.c_int64(0)
+    _check(load_library().mm_gemm_f32_splitk_workspace(M, N, K, splitk, ctypes.byref(out)))
+    return out.value
+
+
+def mm_gemm_f32_splitk(transA, transB, M, N, K, A, lda, B, ldb, C, ldc, splitk, workspace, workspace_floats,
+                       stream=None):
+    _check(load_library().mm_gemm_f32_splitk(int(transA), int(transB), M, N, K, _ptr(A), lda, _ptr(B), ldb,
+                                             _ptr(C), ldc, int(splitk), _ptr(workspace), int(workspace_floats),
+                                             _stream(stream)))
 
 
 def mm_gemv_packed2(codes, scales, x, y, rows, cols, codebook, stream=None):

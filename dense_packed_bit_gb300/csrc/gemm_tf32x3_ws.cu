@@ -89,10 +89,26 @@ struct Plan {
 
 struct WsParams {
     int M, N, K;
-    int tiles_m, tiles;
+    int tiles_m, tiles;  // tiles = output tiles x ksplit work units
+    int ksplit;          // K slices per output tile (1: no split)
     float *C;
     int64_t ldc;
+    float *ws;           // ksplit > 1: slice s of every output tile goes to ws + s M N (row-major, ld N)
 };
+
+// Work unit t: output tile t / ksplit, K slice t % ksplit (slabs [kt0, kt1)).
+struct Unit {
+    int mn, s, kt0, kt1;
+};
+
+__device__ __forceinline__ Unit unit_of(int t, const WsParams &p, int KT) {
+    Unit u;
+    u.s = t % p.ksplit;
+    u.mn = t / p.ksplit;
+    u.kt0 = (int)((int64_t)u.s * KT / p.ksplit);
+    u.kt1 = (int)((int64_t)(u.s + 1) * KT / p.ksplit);
+    return u;
+}
 
 __device__ __forceinline__ float lo_part(float a) {
     return __fsub_rn(a, __uint_as_float(__float_as_uint(a) & 0xFFFFE000u));
@@ -210,9 +226,10 @@ __global__ void __launch_bounds__(NTHREADS, 1)
             int it = 0;  // slabs issued so far (ring position)
             bool stop = false;
             for (int t = cid; t < p.tiles && !stop; t += ncl) {
-                const int m0 = (t % p.tiles_m) * (BM * CG) + BM * (int)rank;
-                const int nb = (t / p.tiles_m) * BN + BNC * (int)rank;
-                for (int kt = 0; kt < KT; ++kt) {
+                const Unit u = unit_of(t, p, KT);
+                const int m0 = (u.mn % p.tiles_m) * (BM * CG) + BM * (int)rank;
+                const int nb = (u.mn / p.tiles_m) * BN + BNC * (int)rank;
+                for (int kt = u.kt0; kt < u.kt1; ++kt) {
                     const int s = it % STAGES;
                     const uint32_t use = it / STAGES;
                     if (*abort_flag) { stop = true; break; }
@@ -256,7 +273,8 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                 }
                 tc_fence_after_sync();
                 const uint32_t d = tmem + (uint32_t)(b * ACC_COLS);
-                for (int kt = 0; kt < KT; ++kt, ++it) {
+                const Unit u = unit_of(t, p, KT);
+                for (int kt = u.kt0; kt < u.kt1; ++kt, ++it) {
                     const int s = it % STAGES;
                     const uint32_t use = it / STAGES;
                     if (*abort_flag) { stop = true; break; }
@@ -275,7 +293,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                         const uint64_t al = sdesc_make(st + P::LO_A + o, 16, 512, kSdescSw64);
                         const uint64_t bh = sdesc_make(st + P::HI_B + o, 16, 512, kSdescSw64);
                         const uint64_t bl = sdesc_make(st + P::LO_B + o, 16, 512, kSdescSw64);
-                        const uint32_t acc0 = (kt > 0 || ks > 0) ? 1u : 0u;
+                        const uint32_t acc0 = (kt > u.kt0 || ks > 0) ? 1u : 0u;
                         if constexpr (CG == 2) {
                             umma_tf32_pair(d, ah, bh, idesc, acc0);
                             umma_tf32_pair(d, ah, bl, idesc, 1u);
@@ -305,7 +323,8 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         int it = 0;
         bool stop = false;
         for (int t = cid; t < p.tiles && !stop; t += ncl) {
-            for (int kt = 0; kt < KT; ++kt, ++it) {
+            const Unit u = unit_of(t, p, KT);
+            for (int kt = u.kt0; kt < u.kt1; ++kt, ++it) {
                 const int s = it % STAGES;
                 const uint32_t use = it / STAGES;
                 if (*abort_flag) { stop = true; break; }
@@ -327,7 +346,6 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     } else {
         // epilogue: warp w reads TMEM lanes 32 (w % 4) .. 32 (w % 4) + 31 of this CTA
         const int q = warp & 3;
-        const bool vec_ok = (p.ldc % 4 == 0) && ((reinterpret_cast<uintptr_t>(p.C) & 15) == 0);
         int tc = 0;
         for (int t = cid; t < p.tiles; t += ncl, ++tc) {
             const int b = tc % NACC;
@@ -338,10 +356,15 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                 break;
             }
             tc_fence_after_sync();
-            const int m0 = (t % p.tiles_m) * (BM * CG) + BM * (int)rank, n0 = (t / p.tiles_m) * BN;
+            const Unit u = unit_of(t, p, KT);
+            const int m0 = (u.mn % p.tiles_m) * (BM * CG) + BM * (int)rank, n0 = (u.mn / p.tiles_m) * BN;
             const int row = m0 + 32 * q + lane;
             const uint32_t base = tmem + (uint32_t)(b * ACC_COLS) + ((uint32_t)(32 * q) << 16);
-            float *crow = p.C + (int64_t)row * p.ldc + n0;
+            // the output, or this K slice's part of the workspace
+            float *out = p.ws ? p.ws + (int64_t)u.s * p.M * p.N : p.C;
+            const int64_t ld = p.ws ? (int64_t)p.N : p.ldc;
+            const bool vec = (ld % 4 == 0) && ((reinterpret_cast<uintptr_t>(out) & 15) == 0);
+            float *crow = out + (int64_t)row * ld + n0;
 #pragma unroll 1
             for (int c0 = 0; c0 < BN; c0 += 32) {
                 float v[32];
@@ -349,7 +372,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                 // columns of this chunk inside the tile (the last chunk of a 240-wide tile has 16)
                 const int w = BN - c0 < 32 ? BN - c0 : 32;
                 if (row < p.M && n0 + c0 < p.N) {
-                    if (vec_ok && w == 32 && n0 + c0 + 32 <= p.N) {
+                    if (vec && w == 32 && n0 + c0 + 32 <= p.N) {
 #pragma unroll
                         for (int j = 0; j < 32; j += 4)
                             *reinterpret_cast<float4 *>(crow + c0 + j) = make_float4(v[j], v[j + 1], v[j + 2], v[j + 3]);
@@ -401,8 +424,38 @@ cudaError_t launch_ws(const CUtensorMap &ta, const CUtensorMap &tb, const WsPara
     return cudaLaunchKernelEx(&lc, kern, ta, tb, p);
 }
 
+// C = sum over the ksplit slices of the workspace, added in slice order (bit-reproducible).
+__global__ void __launch_bounds__(256) splitk_reduce_kernel(const float *__restrict__ ws, float *__restrict__ C,
+                                                            int64_t ldc, int M, int N, int ksplit) {
+    const int64_t MN = (int64_t)M * N;
+    const int64_t step = (int64_t)gridDim.x * blockDim.x;
+    const bool vec = (N % 4 == 0) && (ldc % 4 == 0) && ((reinterpret_cast<uintptr_t>(C) & 15) == 0) &&
+                     ((reinterpret_cast<uintptr_t>(ws) & 15) == 0);
+    if (vec) {
+        const float4 *w4 = reinterpret_cast<const float4 *>(ws);
+        for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < MN / 4; i += step) {
+            float4 acc = w4[i];
+            for (int s = 1; s < ksplit; ++s) {
+                const float4 v = w4[(int64_t)s * (MN / 4) + i];
+                acc.x += v.x;
+                acc.y += v.y;
+                acc.z += v.z;
+                acc.w += v.w;
+            }
+            const int64_t row = (4 * i) / N, col = (4 * i) % N;
+            *reinterpret_cast<float4 *>(C + row * ldc + col) = acc;
+        }
+    } else {
+        for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < MN; i += step) {
+            float acc = ws[i];
+            for (int s = 1; s < ksplit; ++s) acc += ws[(int64_t)s * MN + i];
+            C[(i / N) * ldc + i % N] = acc;
+        }
+    }
+}
+
 template <int CG, int BN>
-cudaError_t launch_ws_cg(const GemmArgs &g, int sms, cudaStream_t s) {
+cudaError_t launch_ws_cg(const GemmArgs &g, int sms, int ksplit, float *ws, cudaStream_t s) {
     constexpr int BNC = BN / CG;
     CUtensorMap ta, tb;
     cudaError_t e;
@@ -423,26 +476,56 @@ cudaError_t launch_ws_cg(const GemmArgs &g, int sms, cudaStream_t s) {
                          CU_TENSOR_MAP_SWIZZLE_NONE);
     if (e != cudaSuccess) return e;
     const int tiles_m = (int)((g.M + BM * CG - 1) / (BM * CG)), tiles_n = (int)((g.N + BN - 1) / BN);
-    WsParams p{(int)g.M, (int)g.N, (int)g.K, tiles_m, tiles_m * tiles_n, g.C, g.ldc};
+    if (ksplit < 2) ws = nullptr;
+    WsParams p{(int)g.M, (int)g.N, (int)g.K, tiles_m, tiles_m * tiles_n * (ws ? ksplit : 1), ws ? ksplit : 1,
+               g.C, g.ldc, ws};
     const int units = sms / CG;
     const int grid = CG * (p.tiles < units ? p.tiles : units);
-    if (!g.transA && !g.transB) return launch_ws<true, false, CG, BN>(ta, tb, p, grid, s);
-    if (!g.transA && g.transB) return launch_ws<true, true, CG, BN>(ta, tb, p, grid, s);
-    if (g.transA && !g.transB) return launch_ws<false, false, CG, BN>(ta, tb, p, grid, s);
-    return launch_ws<false, true, CG, BN>(ta, tb, p, grid, s);
+    if (!g.transA && !g.transB) e = launch_ws<true, false, CG, BN>(ta, tb, p, grid, s);
+    else if (!g.transA && g.transB) e = launch_ws<true, true, CG, BN>(ta, tb, p, grid, s);
+    else if (g.transA && !g.transB) e = launch_ws<false, false, CG, BN>(ta, tb, p, grid, s);
+    else e = launch_ws<false, true, CG, BN>(ta, tb, p, grid, s);
+    if (e != cudaSuccess || !ws) return e;
+    const int64_t work = (g.M * g.N + 3) / 4;
+    const int64_t blocks = (work + 255) / 256;
+    splitk_reduce_kernel<<<(unsigned)(blocks < 4 * sms ? blocks : 4 * sms), 256, 0, s>>>(ws, g.C, g.ldc, (int)g.M,
+                                                                                        (int)g.N, ksplit);
+    return cudaGetLastError();
 }
 
 }  // namespace
 
-cudaError_t launch_gemm_tf32x3_ws(const GemmArgs &g, int pair, cudaStream_t s) {
-    if (!gemm_tf32x3_supported(g)) return cudaErrorNotSupported;
-    int dev = 0, sms = 0;
+static cudaError_t sm_count(int *sms) {
+    int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
-    if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    if (e == cudaSuccess) e = cudaDeviceGetAttribute(sms, cudaDevAttrMultiProcessorCount, dev);
+    return e;
+}
+
+cudaError_t launch_gemm_tf32x3_ws(const GemmArgs &g, int pair, cudaStream_t s) {
+    return launch_gemm_tf32x3_ws_splitk(g, pair, 1, nullptr, s);
+}
+
+cudaError_t launch_gemm_tf32x3_ws_splitk(const GemmArgs &g, int pair, int ksplit, float *ws, cudaStream_t s) {
+    if (!gemm_tf32x3_supported(g)) return cudaErrorNotSupported;
+    int sms = 0;
+    cudaError_t e = sm_count(&sms);
     if (e != cudaSuccess) return e;
     // 256 columns per tile: a 240-wide pair tile (72 tiles of a 2048^2 output on 76
     // pairs instead of 64) measured no faster on GB300, the MMA time not shrinking with N
-    return pair ? launch_ws_cg<2, 256>(g, sms, s) : launch_ws_cg<1, 256>(g, sms, s);
+    return pair ? launch_ws_cg<2, 256>(g, sms, ksplit, ws, s) : launch_ws_cg<1, 256>(g, sms, ksplit, ws, s);
+}
+
+// Automatic K split: as many slices as keep every tile's slices within one wave of the
+// persistent grid, at least 4 slabs of 16 per slice, at most 16 slices.
+int gemm_splitk_auto(int64_t M, int64_t N, int64_t K, int pair, int sms) {
+    const int cg = pair ? 2 : 1;
+    const int64_t tiles = ((M + 128 * cg - 1) / (128 * cg)) * ((N + 255) / 256);
+    const int64_t kt = (K + BK - 1) / BK;
+    int64_t s = (sms / cg) / tiles;
+    if (s > kt / 4) s = kt / 4;
+    if (s > 16) s = 16;
+    return s < 1 ? 1 : (int)s;
 }
 
 unsigned int gemm_tf32x3_ws_take_device_error(cudaError_t *err) {

@@ -166,6 +166,87 @@ mm_status mm_gemm_f32(int transA, int transB, int64_t M, int64_t N, int64_t K, c
     return mm_gemm_f32_ex(transA, transB, M, N, K, A, lda, B, ldb, C, ldc, stream, nullptr);
 }
 
+}  // extern "C"
+
+namespace {
+
+// The split a split-K call uses: `splitk` itself when given, else the automatic choice for
+// the tile shape the call runs (CTA pairs when M > 128).
+mm_status resolve_splitk(int64_t M, int64_t N, int64_t K, int splitk, int *out) {
+    if (splitk < 0 || splitk > 16) return fail(MM_ERR_INVALID_ARG, "splitk must be 0 (automatic) or 1..16");
+    if (splitk) {
+        *out = (int)(splitk > (K + 15) / 16 ? (K + 15) / 16 : splitk);
+        return MM_OK;
+    }
+    mm_status s = check_device();
+    if (s != MM_OK) return s;
+    int dev = 0, sms = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaDeviceGetAttribute");
+    *out = mm::gemm_splitk_auto(M, N, K, M > 128 ? 1 : 0, sms);
+    return MM_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+mm_status mm_gemm_f32_splitk_workspace(int64_t M, int64_t N, int64_t K, int splitk, int64_t *floats) {
+    if (!floats) return fail(MM_ERR_INVALID_ARG, "floats is NULL");
+    if (M < 1 || N < 1 || K < 1) return fail(MM_ERR_INVALID_ARG, "M, N, K must be >= 1");
+    int sk = 1;
+    mm_status s = resolve_splitk(M, N, K, splitk, &sk);
+    if (s != MM_OK) return s;
+    *floats = sk > 1 ? (int64_t)sk * M * N : 0;
+    return ok();
+}
+
+mm_status mm_gemm_f32_splitk(int transA, int transB, int64_t M, int64_t N, int64_t K, const float *A, int64_t lda,
+                             const float *B, int64_t ldb, float *C, int64_t ldc, int splitk, float *workspace,
+                             int64_t workspace_floats, mm_stream_t stream) {
+    if ((transA != 0 && transA != 1) || (transB != 0 && transB != 1))
+        return fail(MM_ERR_INVALID_ARG, "transA/transB must be 0 or 1");
+    if (M < 1 || N < 1 || K < 1)
+        return fail(MM_ERR_INVALID_ARG, "M, N, K must be >= 1 (got %lld, %lld, %lld)", (long long)M, (long long)N,
+                    (long long)K);
+    if (!A || !B || !C) return fail(MM_ERR_INVALID_ARG, "NULL matrix pointer");
+    const int64_t a_rows = transA ? K : M, a_cols = transA ? M : K;
+    const int64_t b_rows = transB ? N : K, b_cols = transB ? K : N;
+    if (lda < a_cols) return fail(MM_ERR_INVALID_ARG, "lda=%lld < %lld", (long long)lda, (long long)a_cols);
+    if (ldb < b_cols) return fail(MM_ERR_INVALID_ARG, "ldb=%lld < %lld", (long long)ldb, (long long)b_cols);
+    if (ldc < N) return fail(MM_ERR_INVALID_ARG, "ldc=%lld < N=%lld", (long long)ldc, (long long)N);
+    const uint64_t cb = span(M, N, ldc, 4);
+    if (overlap(C, cb, A, span(a_rows, a_cols, lda, 4)) || overlap(C, cb, B, span(b_rows, b_cols, ldb, 4)))
+        return fail(MM_ERR_INVALID_ARG, "C overlaps A or B");
+    if (splitk < 0 || splitk > 16) return fail(MM_ERR_INVALID_ARG, "splitk must be 0 (automatic) or 1..16");
+    if (workspace_floats < 0) return fail(MM_ERR_INVALID_ARG, "workspace_floats < 0");
+    if (workspace && (reinterpret_cast<uintptr_t>(workspace) & 15))
+        return fail(MM_ERR_INVALID_ARG, "workspace must be 16-byte aligned");
+    if (workspace) {
+        const uint64_t wb = (uint64_t)workspace_floats * 4;
+        if (overlap(workspace, wb, A, span(a_rows, a_cols, lda, 4)) || overlap(workspace, wb, B, span(b_rows, b_cols, ldb, 4)) ||
+            overlap(workspace, wb, C, cb))
+            return fail(MM_ERR_INVALID_ARG, "workspace overlaps A, B or C");
+    }
+    int sk = 1;
+    mm_status s = resolve_splitk(M, N, K, splitk, &sk);
+    if (s != MM_OK) return s;
+    if (sk > 1 && (!workspace || workspace_floats < (int64_t)sk * M * N))
+        return fail(MM_ERR_INVALID_ARG, "workspace of %lld floats needed for %d K slices",
+                    (long long)((int64_t)sk * M * N), sk);
+    s = check_device();
+    if (s != MM_OK) return s;
+    mm::GemmArgs g{transA, transB, M, N, K, A, lda, B, ldb, C, ldc};
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    cudaError_t e;
+    // operands TMA cannot describe take the unsplit general kernel (the workspace is unused)
+    if (mm::gemm_tf32x3_supported(g)) e = mm::launch_gemm_tf32x3_ws_splitk(g, M > 128 ? 1 : 0, sk, workspace, st);
+    else e = mm::launch_gemm_simple(g, st);
+    if (e != cudaSuccess) return cuda_fail(e, "gemm launch");
+    return ok();
+}
+
 mm_status mm_gemv_packed2_ex(const uint8_t *codes, const uint16_t *scales, const uint16_t *x, float *y, int64_t rows,
                              int64_t cols, const float codebook[4], mm_stream_t stream, const mm_gemv_opts *opts) {
     mm_status s = check_packed(codes, scales, x, y, 1, rows, cols, codebook);

@@ -131,6 +131,10 @@ cudaError_t launch_gemm_ffma(const GemmArgs &g, int tile, cudaStream_t s);
 bool gemm_tf32x3_supported(const GemmArgs &g);
 cudaError_t launch_gemm_tf32x3(const GemmArgs &g, cudaStream_t s);
 cudaError_t launch_gemm_tf32x3_ws(const GemmArgs &g, int pair, cudaStream_t s);
+// Split-K form: ksplit slices per output tile computed into ws (ksplit * M * N floats,
+// 16-byte aligned), then summed in slice order into C by a second kernel.
+cudaError_t launch_gemm_tf32x3_ws_splitk(const GemmArgs &g, int pair, int ksplit, float *ws, cudaStream_t s);
+int gemm_splitk_auto(int64_t M, int64_t N, int64_t K, int pair, int sms);
 
 // Per translation unit device error words (read and cleared).
 unsigned int gemm_ffma_take_device_error(cudaStream_t s, cudaError_t *err);

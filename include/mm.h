@@ -120,6 +120,30 @@ mm_status mm_gemm_packed2(const uint8_t *codes, const uint16_t *scales, const ui
  */
 mm_status mm_check_device_error(mm_stream_t stream);
 
+/*
+ * Split-K form of mm_gemm_f32 for products with few output tiles (short M and N,
+ * long K: the GPT-2 MLP shapes at small batch).  K is cut into `splitk` slices
+ * (0 = automatic, 1..16); every slice of every output tile is computed by its own
+ * CTA into `workspace`, then a second kernel adds the slices in slice order into C
+ * (the result is bit-reproducible run to run; it may differ from mm_gemm_f32 in
+ * the last bits, by summation order).  Same bound |C - C_exact| <= 1e-5 sum|a b|.
+ *
+ * workspace: caller-owned device memory, 16-byte aligned, at least the number of
+ * floats mm_gemm_f32_splitk_workspace reports for the same M, N, K, splitk
+ * (splitk * M * N once the split is resolved; 0 when it resolves to 1, and
+ * NULL is then accepted).  It must not overlap A, B or C; its contents on entry
+ * do not matter.  Operands TMA cannot describe (A or B not 16-byte aligned, lda
+ * or ldb not a multiple of 4) run the unsplit general kernel and leave the
+ * workspace untouched.
+ * Errors: as mm_gemm_f32, plus MM_ERR_INVALID_ARG for splitk outside 0..16, a
+ * misaligned, overlapping or too small workspace.
+ */
+mm_status mm_gemm_f32_splitk_workspace(int64_t M, int64_t N, int64_t K, int splitk, int64_t *floats);
+mm_status mm_gemm_f32_splitk(int transA, int transB, int64_t M, int64_t N, int64_t K,
+                             const float *A, int64_t lda, const float *B, int64_t ldb,
+                             float *C, int64_t ldc, int splitk, float *workspace,
+                             int64_t workspace_floats, mm_stream_t stream);
+
 /* ------------------------------------------------------------------------
  * Variant selection for sweeps and tests.  A zeroed struct means "automatic".
  * Every variant computes the same operation to the same bound.

@@ -89,6 +89,30 @@ def test_gemm_bad_tf32x3_tile(lib, path, tile):
     assert st == mm.MM_ERR_INVALID_ARG and b"tile" in lib.mm_last_error()
 
 
+def test_gemm_splitk_workspace_size(lib):
+    out = ctypes.c_int64(-1)
+    assert lib.mm_gemm_f32_splitk_workspace(64, 3072, 768, 4, ctypes.byref(out)) == mm.MM_OK
+    assert out.value == 4 * 64 * 3072
+    assert lib.mm_gemm_f32_splitk_workspace(64, 3072, 768, 1, ctypes.byref(out)) == mm.MM_OK and out.value == 0
+    # a split is capped at one slice per 16-deep slab of K
+    assert lib.mm_gemm_f32_splitk_workspace(8, 8, 20, 16, ctypes.byref(out)) == mm.MM_OK and out.value == 2 * 64
+    assert lib.mm_gemm_f32_splitk_workspace(64, 3072, 768, 17, ctypes.byref(out)) == mm.MM_ERR_INVALID_ARG
+    assert lib.mm_gemm_f32_splitk_workspace(0, 3072, 768, 2, ctypes.byref(out)) == mm.MM_ERR_INVALID_ARG
+    assert lib.mm_gemm_f32_splitk_workspace(8, 8, 8, 2, None) == mm.MM_ERR_INVALID_ARG
+
+
+@pytest.mark.parametrize("case", [dict(splitk=17), dict(splitk=-1), dict(ws=FAKE + 0x100004),
+                                  dict(ws_floats=4 * 64 * 64 - 1), dict(ws=None), dict(ws=FAKE + 64),
+                                  dict(ws_floats=-5), dict(ldc=10)])
+def test_gemm_splitk_argument_errors(lib, case):
+    a = dict(M=64, N=64, K=256, A=FAKE, B=FAKE + 0x20000, C=FAKE + 0x40000, ldc=64, splitk=4,
+             ws=FAKE + 0x100000, ws_floats=4 * 64 * 64)
+    a.update(case)
+    st = lib.mm_gemm_f32_splitk(0, 0, a["M"], a["N"], a["K"], a["A"], a["K"], a["B"], a["N"], a["C"], a["ldc"],
+                                a["splitk"], a["ws"], a["ws_floats"], None)
+    assert st == mm.MM_ERR_INVALID_ARG, lib.mm_last_error()
+
+
 def _cb(*v):
     return (ctypes.c_float * 4)(*v)
 

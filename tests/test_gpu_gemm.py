@@ -190,3 +190,64 @@ def test_training_set_sampled(oracle, which, path):
     ref, T = oracle.gemm_at(c.transA, c.transB, c.K, c.A, c.B, ii, jj)
     worst = check_bound(C[ii, jj], ref, T, c.name)
     print(f"{c.name}: {len(ii)} outputs, worst |err|/T = {worst:.3e}")
+
+
+# ------------------------------------------------------------------ split-K with a workspace
+
+def run_splitk(tA, tB, M, N, K, A, B, splitk, lda=None, ldb=None, ldc=None, fill=float("nan")):
+    import torch
+    lda = lda or A.shape[1]
+    ldb = ldb or B.shape[1]
+    ldc = ldc or N
+    dA, dB = to_dev(A), to_dev(B)
+    dC = empty_f32((M, ldc))
+    n = mm.mm_gemm_f32_splitk_workspace(M, N, K, splitk)
+    ws = torch.full((max(n, 1),), fill, dtype=torch.float32, device=dA.device)  # contents must not matter
+    mm.mm_gemm_f32_splitk(tA, tB, M, N, K, dA, lda, dB, ldb, dC, ldc, splitk, ws if n else None, n)
+    mm.mm_check_device_error()
+    return to_host(dC)
+
+
+def test_gpt2_mlp_up_splitk_auto_all_outputs(oracle):
+    # 64 x 768 x 3072: 12 output tiles, split automatically over the SMs
+    c = synth.gpt2_mlp_up_64x768x3072()
+    assert mm.mm_gemm_f32_splitk_workspace(c.M, c.N, c.K, 0) > 0
+    C = run_splitk(c.transA, c.transB, c.M, c.N, c.K, c.A, c.B, 0)
+    ref, T = oracle.gemm(c.transA, c.transB, c.M, c.N, c.K, c.A, c.B)
+    check_bound(C, ref, T, c.name + " split-K")
+
+
+@pytest.mark.parametrize("splitk", [1, 2, 3, 5, 16])
+@pytest.mark.parametrize("layout", list(LAYOUTS))
+@pytest.mark.parametrize("shape", [(64, 3072, 768), (100, 300, 500), (300, 260, 1000), (5, 7, 40)])
+def test_gemm_splitk_parity(oracle, splitk, layout, shape):
+    # single CTAs (M <= 128) and CTA pairs (M > 128), ragged tiles, K tails, uneven slices
+    tA, tB = LAYOUTS[layout]
+    M, N, K = shape
+    A, B = stored(tA, tB, M, N, K, seed=900 + M + N + K)
+    Ap = np.zeros((A.shape[0], (A.shape[1] + 3) // 4 * 4), np.float32); Ap[:, :A.shape[1]] = A
+    Bp = np.zeros((B.shape[0], (B.shape[1] + 3) // 4 * 4), np.float32); Bp[:, :B.shape[1]] = B
+    C = run_splitk(tA, tB, M, N, K, Ap, Bp, splitk, lda=Ap.shape[1], ldb=Bp.shape[1], ldc=N + 3)
+    ref, T = oracle.gemm(tA, tB, M, N, K, A, B)
+    check_bound(C[:, :N], ref, T, f"split {splitk} {layout} {shape}")
+    assert np.all(np.isnan(C[:, N:])), "columns past N were written"
+
+
+def test_gemm_splitk_deterministic_and_integer_exact(oracle):
+    M, N, K = 96, 520, 1536
+    A, B = stored(0, 0, M, N, K, seed=77, kind="int")
+    ref, _ = oracle.gemm(0, 0, M, N, K, A, B)
+    c1 = run_splitk(0, 0, M, N, K, A, B, 7)
+    c2 = run_splitk(0, 0, M, N, K, A, B, 7, fill=123.0)
+    check_exact(c1, ref, "split-K integers")
+    assert np.array_equal(c1.view(np.uint32), c2.view(np.uint32))
+
+
+def test_gemm_splitk_unaligned_operands_take_general_path(oracle):
+    # lda not a multiple of 4: no TMA, no split; the workspace is not needed
+    M, N, K = 70, 45, 83
+    A, B = stored(0, 0, M, N, K, seed=5)
+    Ap = np.zeros((M, K + 3), np.float32); Ap[:, :K] = A
+    C = run_splitk(0, 0, M, N, K, Ap, B, 4, lda=K + 3)
+    ref, T = oracle.gemm(0, 0, M, N, K, A, B)
+    check_bound(C, ref, T, "general path")
