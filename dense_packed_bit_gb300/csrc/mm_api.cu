@@ -247,6 +247,37 @@ mm_status mm_gemm_f32_splitk(int transA, int transB, int64_t M, int64_t N, int64
     return ok();
 }
 
+mm_status mm_gemm_f32_splitk_noalloc(int transA, int transB, int64_t M, int64_t N, int64_t K, const float *A,
+                                     int64_t lda, const float *B, int64_t ldb, float *C, int64_t ldc, int splitk,
+                                     mm_stream_t stream) {
+    static_assert(mm::kSplitkStaticFloats == MM_SPLITK_NOALLOC_MAX_FLOATS, "the header states the scratch size");
+    // the cheap checks first, so that bad arguments never reach a CUDA call
+    if ((transA != 0 && transA != 1) || (transB != 0 && transB != 1))
+        return fail(MM_ERR_INVALID_ARG, "transA/transB must be 0 or 1");
+    if (M < 1 || N < 1 || K < 1)
+        return fail(MM_ERR_INVALID_ARG, "M, N, K must be >= 1 (got %lld, %lld, %lld)", (long long)M, (long long)N,
+                    (long long)K);
+    if (!A || !B || !C) return fail(MM_ERR_INVALID_ARG, "NULL matrix pointer");
+    if (splitk < 0 || splitk > 16) return fail(MM_ERR_INVALID_ARG, "splitk must be 0 (automatic) or 1..16");
+    int64_t need = 0;
+    mm_status s = mm_gemm_f32_splitk_workspace(M, N, K, splitk, &need);
+    if (s != MM_OK) return s;
+    if (need > mm::kSplitkStaticFloats)
+        return fail(MM_ERR_INVALID_ARG,
+                    "split-K of %lld x %lld needs %lld floats of scratch; the library's static scratch holds %lld "
+                    "(pass a smaller splitk, or a workspace to mm_gemm_f32_splitk)",
+                    (long long)M, (long long)N, (long long)need, (long long)mm::kSplitkStaticFloats);
+    float *scratch = nullptr;
+    int64_t cap = 0;
+    if (need > 0) {
+        s = check_device();
+        if (s != MM_OK) return s;
+        const cudaError_t e = mm::splitk_static_scratch(&scratch, &cap);
+        if (e != cudaSuccess) return cuda_fail(e, "cudaGetSymbolAddress of the split-K scratch");
+    }
+    return mm_gemm_f32_splitk(transA, transB, M, N, K, A, lda, B, ldb, C, ldc, splitk, scratch, cap, stream);
+}
+
 mm_status mm_gemv_packed2_ex(const uint8_t *codes, const uint16_t *scales, const uint16_t *x, float *y, int64_t rows,
                              int64_t cols, const float codebook[4], mm_stream_t stream, const mm_gemv_opts *opts) {
     mm_status s = check_packed(codes, scales, x, y, 1, rows, cols, codebook);

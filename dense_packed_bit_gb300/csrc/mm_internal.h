@@ -136,6 +136,11 @@ cudaError_t launch_gemm_tf32x3_ws(const GemmArgs &g, int pair, cudaStream_t s);
 cudaError_t launch_gemm_tf32x3_ws_splitk(const GemmArgs &g, int pair, int ksplit, float *ws, cudaStream_t s);
 int gemm_splitk_auto(int64_t M, int64_t N, int64_t K, int pair, int sms);
 
+// The static scratch of the split-K entry point that allocates nothing: its device
+// address on the current device (looked up on the first call per device) and size.
+constexpr int64_t kSplitkStaticFloats = 4194304;  // 16 MiB; mm.h states the same limit
+cudaError_t splitk_static_scratch(float **ptr, int64_t *floats);
+
 // Per translation unit device error words (read and cleared).
 unsigned int gemm_ffma_take_device_error(cudaStream_t s, cudaError_t *err);
 unsigned int gemm_tf32x3_take_device_error(cudaError_t *err);

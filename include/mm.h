@@ -144,6 +144,32 @@ mm_status mm_gemm_f32_splitk(int transA, int transB, int64_t M, int64_t N, int64
                              float *C, int64_t ldc, int splitk, float *workspace,
                              int64_t workspace_floats, mm_stream_t stream);
 
+/*
+ * mm_gemm_f32_splitk with no workspace argument and no allocation: the partial
+ * tiles go to a scratch array of MM_SPLITK_NOALLOC_MAX_FLOATS floats (16 MiB)
+ * that the library holds in device memory of every GPU that loads it, until the
+ * process exits.  The pages have no counterpart: this is for callers that cannot
+ * call cudaMalloc or hand over a workspace where they multiply (device memory
+ * owned by another allocator, such as a framework's caching pool that has
+ * reserved what it manages; paths where cudaMalloc's device-wide synchronisation
+ * is not acceptable).  Nothing here calls cudaMalloc, cudaFree or any
+ * allocating routine.
+ *
+ * Same arguments, result and errors as mm_gemm_f32_splitk, plus
+ * MM_ERR_INVALID_ARG when the resolved split needs more than
+ * MM_SPLITK_NOALLOC_MAX_FLOATS floats (splitk * M * N).  The first call on a
+ * device looks up the array's device address (cudaGetSymbolAddress, with that
+ * device current); make that first call before any stream capture.  Every call
+ * shares the one array and leaves its partial tiles there; no part of it has to
+ * start at zero (each call writes all it reads).  Calls whose kernels overlap on
+ * the GPU (on different streams, or from different threads) race on the array
+ * and may return wrong results: serialise them.
+ */
+#define MM_SPLITK_NOALLOC_MAX_FLOATS 4194304
+mm_status mm_gemm_f32_splitk_noalloc(int transA, int transB, int64_t M, int64_t N, int64_t K,
+                                     const float *A, int64_t lda, const float *B, int64_t ldb,
+                                     float *C, int64_t ldc, int splitk, mm_stream_t stream);
+
 /* ------------------------------------------------------------------------
  * Variant selection for sweeps and tests.  A zeroed struct means "automatic".
  * Every variant computes the same operation to the same bound.

@@ -113,6 +113,16 @@ def test_gemm_splitk_argument_errors(lib, case):
     assert st == mm.MM_ERR_INVALID_ARG, lib.mm_last_error()
 
 
+def test_gemm_splitk_noalloc_rejects_oversized_split(lib):
+    # 16 slices of 1024 x 1024 need 16 Mi floats, more than the static scratch holds
+    assert mm.MM_SPLITK_NOALLOC_MAX_FLOATS == 4194304
+    st = lib.mm_gemm_f32_splitk_noalloc(0, 0, 1024, 1024, 4096, FAKE, 4096, FAKE + 0x1000000, 1024,
+                                        FAKE + 0x2000000, 1024, 16, None)
+    assert st == mm.MM_ERR_INVALID_ARG and b"static scratch" in lib.mm_last_error()
+    st = lib.mm_gemm_f32_splitk_noalloc(0, 0, 8, 8, 64, None, 64, FAKE, 8, FAKE + 0x10000, 8, 2, None)
+    assert st == mm.MM_ERR_INVALID_ARG
+
+
 def _cb(*v):
     return (ctypes.c_float * 4)(*v)
 

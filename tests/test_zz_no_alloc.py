@@ -1,0 +1,62 @@
+"""The split-K GEMM entry point that allocates nothing, against the one that takes a workspace.
+
+mm_gemm_f32_splitk_noalloc is for callers that cannot call cudaMalloc or hand
+over a workspace where they multiply (their device memory belongs to another
+allocator, or cudaMalloc's device-wide synchronisation is not acceptable there):
+its partial tiles go to a scratch array the library holds in device memory.
+Two calls in a row, with different shapes, layouts and splits, so that the
+second call also shows that what the first left in the shared scratch does not
+leak into its result.  This file sorts last, so a run that stops at the first
+failure has run every other test first; it also passes alone in a fresh process,
+where its first call sets the scratch up.
+"""
+import numpy as np
+import pytest
+
+import dense_packed_bit_gb300 as mm
+from dense_packed_bit_gb300 import synth
+from gpu_util import check_bound, empty_f32, to_dev, to_host
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    from dense_packed_bit_gb300 import build
+    build.build()
+    mm.load_library()
+
+
+def _stored(tA, tB, M, N, K, seed):
+    A = synth.normal_f32(seed, (K, M) if tA else (M, K), 1.0)
+    B = synth.normal_f32(seed + 1, (N, K) if tB else (K, N), 1.0)
+    return A, B
+
+
+def test_noalloc_splitk_matches_workspace_entry_two_calls(oracle):
+    import torch
+    calls = [  # (transA, transB, M, N, K, splitk): the GPT-2 MLP up-projection with the automatic
+               # split, then a transposed product with an uneven explicit split
+        (0, 0, 64, 3072, 768, 0),
+        (1, 0, 96, 520, 1536, 7),
+    ]
+    for i, (tA, tB, M, N, K, splitk) in enumerate(calls):
+        A, B = _stored(tA, tB, M, N, K, seed=4100 + 10 * i)
+        dA, dB = to_dev(A), to_dev(B)
+        need = mm.mm_gemm_f32_splitk_workspace(M, N, K, splitk)
+        assert 0 < need <= mm.MM_SPLITK_NOALLOC_MAX_FLOATS
+
+        c_noalloc = empty_f32((M, N))
+        mm.mm_gemm_f32_splitk_noalloc(tA, tB, M, N, K, dA, A.shape[1], dB, B.shape[1], c_noalloc, N, splitk)
+        mm.mm_check_device_error()
+
+        ws = torch.full((need,), float("nan"), dtype=torch.float32, device=dA.device)
+        c_ws = empty_f32((M, N))
+        mm.mm_gemm_f32_splitk(tA, tB, M, N, K, dA, A.shape[1], dB, B.shape[1], c_ws, N, splitk, ws, need)
+        mm.mm_check_device_error()
+
+        ref, T = oracle.gemm(tA, tB, M, N, K, A, B)
+        got, want = to_host(c_noalloc), to_host(c_ws)
+        # the tolerance of every GEMM test, between the two entry points and against the oracle
+        check_bound(got, want.astype(np.float64), T, f"call {i}: static scratch vs workspace")
+        check_bound(got, ref, T, f"call {i}: static scratch vs oracle")
