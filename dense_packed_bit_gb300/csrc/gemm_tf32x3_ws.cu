@@ -79,10 +79,10 @@ struct Plan {
     static constexpr int RAW_A = 0, HI_A = A_KC ? 0 : A_BYTES, LO_A = A_KC ? A_BYTES : 2 * A_BYTES;
     static constexpr int RAW_B = A_REGION, HI_B = A_REGION + (B_KC ? 0 : B_BYTES),
                          LO_B = A_REGION + (B_KC ? B_BYTES : 2 * B_BYTES);
-    static constexpr int FIXED = (3 * MAX_STAGES + 2 * NACC + 1) * 8 + 16 + 1024;
+    static constexpr int FIXED = (3 * MAX_STAGES + 2 * NACC + 2) * 8 + 16 + 1024;
     static constexpr int S_FIT = (SMEM_LIMIT - FIXED) / STAGE_BYTES;
     static constexpr int STAGES = S_FIT < MAX_STAGES ? S_FIT : MAX_STAGES;
-    static constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + (3 * STAGES + 2 * NACC + 1) * 8 + 16 + 1024;
+    static constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + (3 * STAGES + 2 * NACC + 2) * 8 + 16 + 1024;
     static_assert(STAGES >= 3, "at least three stages");
     static_assert(SMEM_BYTES <= SMEM_LIMIT, "shared memory");
 };
@@ -94,6 +94,12 @@ struct WsParams {
     float *C;
     int64_t ldc;
     float *ws;           // ksplit > 1: slice s of every output tile goes to ws + s M N (row-major, ld N)
+    // stream-K: unit c (a CTA, or a pair) takes slabs [c sk_w, (c + 1) sk_w) of the tiles' K
+    // ranges laid end to end; a tile's segment that starts its K range adds the other
+    // segments' partial tiles (slot of their unit, in K order) once their flags are set
+    int sk, sk_w, sk_total;
+    float *sk_slots;        // [unit][rank][128][BN] fp32
+    unsigned int *sk_flags; // [unit][rank], zeroed before the launch
 };
 
 // Work unit t: output tile t / ksplit, K slice t % ksplit (slabs [kt0, kt1)).
@@ -108,6 +114,29 @@ __device__ __forceinline__ Unit unit_of(int t, const WsParams &p, int KT) {
     u.kt0 = (int)((int64_t)u.s * KT / p.ksplit);
     u.kt1 = (int)((int64_t)(u.s + 1) * KT / p.ksplit);
     return u;
+}
+
+// The work of unit `cid` as a sequence of segments, identical for every role: work units
+// cid, cid + ncl, ... or, with stream-K, the pieces of its slab range cut at tile boundaries.
+template <bool SK>
+__device__ __forceinline__ int seg_begin(const WsParams &p, int cid) { return SK ? cid * p.sk_w : cid; }
+
+template <bool SK>
+__device__ __forceinline__ bool seg_next(const WsParams &p, int KT, int cid, int ncl, int &cur, Unit &u) {
+    if (!SK) {
+        if (cur >= p.tiles) return false;
+        u = unit_of(cur, p, KT);
+        cur += ncl;
+        return true;
+    }
+    const int r1 = min((cid + 1) * p.sk_w, p.sk_total);
+    if (cur >= r1) return false;
+    u.mn = cur / KT;
+    u.kt0 = cur - u.mn * KT;
+    u.kt1 = min(KT, u.kt0 + (r1 - cur));
+    u.s = 0;
+    cur += u.kt1 - u.kt0;
+    return true;
 }
 
 __device__ __forceinline__ float lo_part(float a) {
@@ -168,7 +197,24 @@ __device__ __forceinline__ void arrive_leader(uint64_t *bar) {
     else mbar_arrive(bar);
 }
 
-template <bool A_KC, bool B_KC, int CG, int BN>
+// Stream-K flags in global memory: set with release, polled with acquire (device scope),
+// the wait bounded like every other wait here.
+__device__ __forceinline__ void flag_set(unsigned int *f) {
+    asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(f), "r"(1u) : "memory");
+}
+
+__device__ __forceinline__ bool flag_wait(const unsigned int *f) {
+    const unsigned long long t0 = global_ns();
+    while (true) {
+        unsigned int v;
+        asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(f) : "memory");
+        if (v) return true;
+        if (global_ns() - t0 > kWaitLimitNs) return false;
+        __nanosleep(64);
+    }
+}
+
+template <bool A_KC, bool B_KC, int CG, int BN, bool SK>
 __global__ void __launch_bounds__(NTHREADS, 1)
     gemm_tf32x3_ws_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                           const WsParams p) {
@@ -182,7 +228,8 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     uint64_t *accf = empty + STAGES;   // MMA -> epilogue (every CTA's, by commit)
     uint64_t *acce = accf + NACC;      // epilogues -> MMA (CTA 0's, one arrival per epilogue warp of the pair)
     uint64_t *last = acce + NACC;
-    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(last + 1);
+    uint64_t *epi = last + 1;          // the 128 epilogue threads of this CTA (stream-K slot hand-off)
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(epi + 1);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -210,6 +257,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
             mbar_init(&acce[b], 4 * CG);
         }
         mbar_init(last, 1);
+        mbar_init(epi, 128);
         *abort_flag = 0;
         fence_mbar_init();
         tma_prefetch_desc(&tmA);
@@ -225,8 +273,9 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         if (lane == 0) {
             int it = 0;  // slabs issued so far (ring position)
             bool stop = false;
-            for (int t = cid; t < p.tiles && !stop; t += ncl) {
-                const Unit u = unit_of(t, p, KT);
+            int cur = seg_begin<SK>(p, cid);
+            Unit u;
+            while (!stop && seg_next<SK>(p, KT, cid, ncl, cur, u)) {
                 const int m0 = (u.mn % p.tiles_m) * (BM * CG) + BM * (int)rank;
                 const int nb = (u.mn / p.tiles_m) * BN + BNC * (int)rank;
                 for (int kt = u.kt0; kt < u.kt1; ++kt) {
@@ -263,7 +312,9 @@ __global__ void __launch_bounds__(NTHREADS, 1)
             constexpr uint16_t all = (uint16_t)((1u << CG) - 1u);
             int it = 0, tc = 0;
             bool stop = false;
-            for (int t = cid; t < p.tiles && !stop; t += ncl, ++tc) {
+            int cur = seg_begin<SK>(p, cid);
+            Unit u;
+            for (; !stop && seg_next<SK>(p, KT, cid, ncl, cur, u); ++tc) {
                 const int b = tc % NACC;
                 const uint32_t ause = tc / NACC;
                 if (*abort_flag) break;
@@ -273,7 +324,6 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                 }
                 tc_fence_after_sync();
                 const uint32_t d = tmem + (uint32_t)(b * ACC_COLS);
-                const Unit u = unit_of(t, p, KT);
                 for (int kt = u.kt0; kt < u.kt1; ++kt, ++it) {
                     const int s = it % STAGES;
                     const uint32_t use = it / STAGES;
@@ -322,8 +372,9 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         const int ct = threadIdx.x - 32 * WARP_CONV0;
         int it = 0;
         bool stop = false;
-        for (int t = cid; t < p.tiles && !stop; t += ncl) {
-            const Unit u = unit_of(t, p, KT);
+        int cur = seg_begin<SK>(p, cid);
+        Unit u;
+        while (!stop && seg_next<SK>(p, KT, cid, ncl, cur, u)) {
             for (int kt = u.kt0; kt < u.kt1; ++kt, ++it) {
                 const int s = it % STAGES;
                 const uint32_t use = it / STAGES;
@@ -346,8 +397,17 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     } else {
         // epilogue: warp w reads TMEM lanes 32 (w % 4) .. 32 (w % 4) + 31 of this CTA
         const int q = warp & 3;
+        const int et = threadIdx.x - 32 * WARP_EPI0;  // 0..127
+        uint32_t epi_phase = 0;
+        auto epi_sync = [&] {  // all 128 epilogue threads, bounded
+            mbar_arrive(epi);
+            if (!mbar_wait(epi, epi_phase & 1)) fail<CG>(abort_flag, kDevErrWaitFull);
+            ++epi_phase;
+        };
         int tc = 0;
-        for (int t = cid; t < p.tiles; t += ncl, ++tc) {
+        int cur = seg_begin<SK>(p, cid);
+        Unit u;
+        for (; seg_next<SK>(p, KT, cid, ncl, cur, u); ++tc) {
             const int b = tc % NACC;
             const uint32_t ause = tc / NACC;
             if (*abort_flag) break;
@@ -356,19 +416,56 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                 break;
             }
             tc_fence_after_sync();
-            const Unit u = unit_of(t, p, KT);
             const int m0 = (u.mn % p.tiles_m) * (BM * CG) + BM * (int)rank, n0 = (u.mn / p.tiles_m) * BN;
-            const int row = m0 + 32 * q + lane;
+
             const uint32_t base = tmem + (uint32_t)(b * ACC_COLS) + ((uint32_t)(32 * q) << 16);
-            // the output, or this K slice's part of the workspace
-            float *out = p.ws ? p.ws + (int64_t)u.s * p.M * p.N : p.C;
-            const int64_t ld = p.ws ? (int64_t)p.N : p.ldc;
+            // stream-K: a segment that does not start its tile's K range leaves its partial tile
+            // in its unit's slot; the one that starts it adds the later segments' slots in K order
+            const bool sk_part = SK && u.kt0 > 0;
+            const bool sk_fix = SK && u.kt0 == 0 && u.kt1 < KT;
+            int c_last = cid;
+            if (sk_fix) {
+                c_last = ((u.mn + 1) * KT - 1) / p.sk_w;
+                bool ok = true;
+                if (et == 0)
+                    for (int c = cid + 1; c <= c_last && ok; ++c)
+                        ok = flag_wait(p.sk_flags + c * CG + rank);
+                if (!ok) fail<CG>(abort_flag, kDevErrWaitFull);
+                epi_sync();  // every slot to be read is complete
+            }
+            // the output, this K slice's part of the workspace, or this unit's stream-K slot.  Each
+            // thread stores its own row (a warp instruction touches 32 rows): staging 32 x 32
+            // blocks through shared memory for row-coalesced stores measured slower on GB300
+            // (2048^3: 76 against 68 us), four times the store instructions costing more
+            const int lrow = 32 * q + lane, row = m0 + lrow;
+            float *out = sk_part ? p.sk_slots + ((int64_t)cid * CG + rank) * BM * BN
+                         : p.ws  ? p.ws + (int64_t)u.s * p.M * p.N : p.C;
+            const int64_t ld = sk_part ? (int64_t)BN : p.ws ? (int64_t)p.N : p.ldc;
             const bool vec = (ld % 4 == 0) && ((reinterpret_cast<uintptr_t>(out) & 15) == 0);
-            float *crow = out + (int64_t)row * ld + n0;
+            float *crow = sk_part ? out + (int64_t)lrow * BN : out + (int64_t)row * ld + n0;
 #pragma unroll 1
             for (int c0 = 0; c0 < BN; c0 += 32) {
                 float v[32];
                 tmem_ld32(base + (uint32_t)c0, v);
+                if (sk_part) {
+                    // the whole 128 x BN partial tile, unmasked: the slot is private to this unit
+#pragma unroll
+                    for (int j = 0; j < 32; j += 4)
+                        *reinterpret_cast<float4 *>(crow + c0 + j) = make_float4(v[j], v[j + 1], v[j + 2], v[j + 3]);
+                    continue;
+                }
+                for (int c = cid + 1; c <= c_last; ++c) {
+                    const float4 *src = reinterpret_cast<const float4 *>(
+                        p.sk_slots + ((int64_t)c * CG + rank) * BM * BN + (int64_t)lrow * BN + c0);
+#pragma unroll
+                    for (int j = 0; j < 8; ++j) {
+                        const float4 a = __ldcg(src + j);
+                        v[4 * j] += a.x;
+                        v[4 * j + 1] += a.y;
+                        v[4 * j + 2] += a.z;
+                        v[4 * j + 3] += a.w;
+                    }
+                }
                 // columns of this chunk inside the tile (the last chunk of a 240-wide tile has 16)
                 const int w = BN - c0 < 32 ? BN - c0 : 32;
                 if (row < p.M && n0 + c0 < p.N) {
@@ -382,6 +479,12 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                             if (j < w && n0 + c0 + j < p.N) crow[c0 + j] = v[j];
                     }
                 }
+            }
+            if (sk_part) {
+                // the slot's stores are visible device-wide before its flag is
+                __threadfence();
+                epi_sync();
+                if (et == 0) flag_set(p.sk_flags + cid * CG + rank);
             }
             tc_fence_before_sync();
             __syncwarp();
@@ -399,9 +502,9 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     }
 }
 
-template <bool A_KC, bool B_KC, int CG, int BN>
-cudaError_t launch_ws(const CUtensorMap &ta, const CUtensorMap &tb, const WsParams &p, int grid, cudaStream_t s) {
-    auto kern = gemm_tf32x3_ws_kernel<A_KC, B_KC, CG, BN>;
+template <bool A_KC, bool B_KC, int CG, int BN, bool SK>
+cudaError_t launch_ws1(const CUtensorMap &ta, const CUtensorMap &tb, const WsParams &p, int grid, cudaStream_t s) {
+    auto kern = gemm_tf32x3_ws_kernel<A_KC, B_KC, CG, BN, SK>;
     constexpr int smem = Plan<A_KC, B_KC, CG, BN>::SMEM_BYTES;
     static std::once_flag once;
     static cudaError_t attr_err = cudaSuccess;
@@ -454,6 +557,12 @@ __global__ void __launch_bounds__(256) splitk_reduce_kernel(const float *__restr
     }
 }
 
+template <bool A_KC, bool B_KC, int CG, int BN>
+cudaError_t launch_ws(const CUtensorMap &ta, const CUtensorMap &tb, const WsParams &p, int grid, cudaStream_t s) {
+    return p.sk ? launch_ws1<A_KC, B_KC, CG, BN, true>(ta, tb, p, grid, s)
+                : launch_ws1<A_KC, B_KC, CG, BN, false>(ta, tb, p, grid, s);
+}
+
 template <int CG, int BN>
 cudaError_t launch_ws_cg(const GemmArgs &g, int sms, int ksplit, float *ws, cudaStream_t s) {
     constexpr int BNC = BN / CG;
@@ -476,11 +585,26 @@ cudaError_t launch_ws_cg(const GemmArgs &g, int sms, int ksplit, float *ws, cuda
                          CU_TENSOR_MAP_SWIZZLE_NONE);
     if (e != cudaSuccess) return e;
     const int tiles_m = (int)((g.M + BM * CG - 1) / (BM * CG)), tiles_n = (int)((g.N + BN - 1) / BN);
+    const bool sk = ksplit == kStreamK && ws;
+    float *const sk_ws = ws;
     if (ksplit < 2) ws = nullptr;
     WsParams p{(int)g.M, (int)g.N, (int)g.K, tiles_m, tiles_m * tiles_n * (ws ? ksplit : 1), ws ? ksplit : 1,
-               g.C, g.ldc, ws};
+               g.C, g.ldc, ws, 0, 0, 0, nullptr, nullptr};
     const int units = sms / CG;
-    const int grid = CG * (p.tiles < units ? p.tiles : units);
+    int grid = CG * (p.tiles < units ? p.tiles : units);
+    if (sk) {
+        const int KT = (int)((g.K + BK - 1) / BK);
+        p.sk = 1;
+        p.sk_total = tiles_m * tiles_n * KT;
+        p.sk_w = (p.sk_total + units - 1) / units;
+        const int used = (p.sk_total + p.sk_w - 1) / p.sk_w;
+        p.sk_slots = sk_ws;
+        p.sk_flags = reinterpret_cast<unsigned int *>(sk_ws + (int64_t)used * CG * BM * BN);
+        e = cudaMemsetAsync(p.sk_flags, 0, (size_t)used * CG * sizeof(unsigned int), s);
+        if (e != cudaSuccess) return e;
+        grid = CG * used;
+        ws = nullptr;  // no second kernel
+    }
     if (!g.transA && !g.transB) e = launch_ws<true, false, CG, BN>(ta, tb, p, grid, s);
     else if (!g.transA && g.transB) e = launch_ws<true, true, CG, BN>(ta, tb, p, grid, s);
     else if (g.transA && !g.transB) e = launch_ws<false, false, CG, BN>(ta, tb, p, grid, s);
@@ -516,16 +640,42 @@ cudaError_t launch_gemm_tf32x3_ws_splitk(const GemmArgs &g, int pair, int ksplit
     return pair ? launch_ws_cg<2, 256>(g, sms, ksplit, ws, s) : launch_ws_cg<1, 256>(g, sms, ksplit, ws, s);
 }
 
-// Automatic K split: as many slices as keep every tile's slices within one wave of the
-// persistent grid, at least 4 slabs of 16 per slice, at most 16 slices.
+// Automatic K split.  Tiles that leave more than half of the persistent grid idle: split-K,
+// as many slices as keep every tile's slices within one wave, at least 4 slabs of 16 per
+// slice, at most 16.  Several waves of tiles with a costly partial last wave: stream-K.
 int gemm_splitk_auto(int64_t M, int64_t N, int64_t K, int pair, int sms) {
     const int cg = pair ? 2 : 1;
     const int64_t tiles = ((M + 128 * cg - 1) / (128 * cg)) * ((N + 255) / 256);
     const int64_t kt = (K + BK - 1) / BK;
-    int64_t s = (sms / cg) / tiles;
-    if (s > kt / 4) s = kt / 4;
-    if (s > 16) s = 16;
-    return s < 1 ? 1 : (int)s;
+    const int64_t units = sms / cg;
+    if (tiles >= units) {
+        // stream-K when the last wave is partial enough to cost more than 5% (4 waves' worth of
+        // units for 256 pair tiles on 76 pairs: +12% measured), and each unit keeps 8 slabs
+        const int64_t waves = (tiles + units - 1) / units;
+        return (waves * units * 100 > tiles * 105 && tiles * kt >= 8 * units) ? kStreamK : 1;
+    }
+    int64_t s = units / tiles;
+    if (s >= 2) {
+        if (s > kt / 4) s = kt / 4;
+        if (s > 16) s = 16;
+        return s < 1 ? 1 : (int)s;
+    }
+    // between half a wave and a wave (64 pair tiles of 2048^3 on 76 pairs): no split; stream-K
+    // measured slower there, all 152 SMs running each slab ~11% slower than 128
+    return 1;
+}
+
+// Workspace floats of a split: split-K slices, or the stream-K slots and flags.
+int64_t gemm_splitk_workspace_floats(int64_t M, int64_t N, int64_t K, int pair, int split, int sms) {
+    if (split >= 2) return (int64_t)split * M * N;
+    if (split != kStreamK) return 0;
+    const int cg = pair ? 2 : 1;
+    const int64_t tiles = ((M + 128 * cg - 1) / (128 * cg)) * ((N + 255) / 256);
+    const int64_t total = tiles * ((K + BK - 1) / BK);
+    const int64_t units = sms / cg;
+    const int64_t w = (total + units - 1) / units;
+    const int64_t used = (total + w - 1) / w;
+    return used * cg * BM * 256 + (used * cg + 3) / 4 * 4;  // slots, then one flag word per CTA
 }
 
 unsigned int gemm_tf32x3_ws_take_device_error(cudaError_t *err) {

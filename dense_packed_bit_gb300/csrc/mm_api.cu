@@ -170,12 +170,16 @@ mm_status mm_gemm_f32(int transA, int transB, int64_t M, int64_t N, int64_t K, c
 
 namespace {
 
-// The split a split-K call uses: `splitk` itself when given, else the automatic choice for
-// the tile shape the call runs (CTA pairs when M > 128).
-mm_status resolve_splitk(int64_t M, int64_t N, int64_t K, int splitk, int *out) {
-    if (splitk < 0 || splitk > 16) return fail(MM_ERR_INVALID_ARG, "splitk must be 0 (automatic) or 1..16");
-    if (splitk) {
+// The split a split-K call uses and the workspace it needs: `splitk` itself when given (1..16
+// slices, -1 stream-K), else the automatic choice for the tile shape the call runs (CTA pairs
+// when M > 128).  Stream-K sizes depend on the SM count, so they query the device.
+mm_status resolve_splitk(int64_t M, int64_t N, int64_t K, int splitk, int *out, int64_t *floats) {
+    if (splitk < -1 || splitk > 16)
+        return fail(MM_ERR_INVALID_ARG, "splitk must be 0 (automatic), 1..16 (slices) or -1 (stream-K)");
+    const int pair = M > 128 ? 1 : 0;
+    if (splitk > 0) {
         *out = (int)(splitk > (K + 15) / 16 ? (K + 15) / 16 : splitk);
+        *floats = mm::gemm_splitk_workspace_floats(M, N, K, pair, *out, 0);
         return MM_OK;
     }
     mm_status s = check_device();
@@ -184,7 +188,8 @@ mm_status resolve_splitk(int64_t M, int64_t N, int64_t K, int splitk, int *out) 
     cudaError_t e = cudaGetDevice(&dev);
     if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
     if (e != cudaSuccess) return cuda_fail(e, "cudaDeviceGetAttribute");
-    *out = mm::gemm_splitk_auto(M, N, K, M > 128 ? 1 : 0, sms);
+    *out = splitk == mm::kStreamK ? mm::kStreamK : mm::gemm_splitk_auto(M, N, K, pair, sms);
+    *floats = mm::gemm_splitk_workspace_floats(M, N, K, pair, *out, sms);
     return MM_OK;
 }
 
@@ -196,9 +201,8 @@ mm_status mm_gemm_f32_splitk_workspace(int64_t M, int64_t N, int64_t K, int spli
     if (!floats) return fail(MM_ERR_INVALID_ARG, "floats is NULL");
     if (M < 1 || N < 1 || K < 1) return fail(MM_ERR_INVALID_ARG, "M, N, K must be >= 1");
     int sk = 1;
-    mm_status s = resolve_splitk(M, N, K, splitk, &sk);
+    mm_status s = resolve_splitk(M, N, K, splitk, &sk, floats);
     if (s != MM_OK) return s;
-    *floats = sk > 1 ? (int64_t)sk * M * N : 0;
     return ok();
 }
 
@@ -219,7 +223,8 @@ mm_status mm_gemm_f32_splitk(int transA, int transB, int64_t M, int64_t N, int64
     const uint64_t cb = span(M, N, ldc, 4);
     if (overlap(C, cb, A, span(a_rows, a_cols, lda, 4)) || overlap(C, cb, B, span(b_rows, b_cols, ldb, 4)))
         return fail(MM_ERR_INVALID_ARG, "C overlaps A or B");
-    if (splitk < 0 || splitk > 16) return fail(MM_ERR_INVALID_ARG, "splitk must be 0 (automatic) or 1..16");
+    if (splitk < -1 || splitk > 16)
+        return fail(MM_ERR_INVALID_ARG, "splitk must be 0 (automatic), 1..16 (slices) or -1 (stream-K)");
     if (workspace_floats < 0) return fail(MM_ERR_INVALID_ARG, "workspace_floats < 0");
     if (workspace && (reinterpret_cast<uintptr_t>(workspace) & 15))
         return fail(MM_ERR_INVALID_ARG, "workspace must be 16-byte aligned");
@@ -230,11 +235,12 @@ mm_status mm_gemm_f32_splitk(int transA, int transB, int64_t M, int64_t N, int64
             return fail(MM_ERR_INVALID_ARG, "workspace overlaps A, B or C");
     }
     int sk = 1;
-    mm_status s = resolve_splitk(M, N, K, splitk, &sk);
+    int64_t need = 0;
+    mm_status s = resolve_splitk(M, N, K, splitk, &sk, &need);
     if (s != MM_OK) return s;
-    if (sk > 1 && (!workspace || workspace_floats < (int64_t)sk * M * N))
-        return fail(MM_ERR_INVALID_ARG, "workspace of %lld floats needed for %d K slices",
-                    (long long)((int64_t)sk * M * N), sk);
+    if (need > 0 && (!workspace || workspace_floats < need))
+        return fail(MM_ERR_INVALID_ARG, "workspace of %lld floats needed (%s)", (long long)need,
+                    sk == mm::kStreamK ? "stream-K" : "K slices");
     s = check_device();
     if (s != MM_OK) return s;
     mm::GemmArgs g{transA, transB, M, N, K, A, lda, B, ldb, C, ldc};
@@ -262,6 +268,11 @@ mm_status mm_gemm_f32_splitk_noalloc(int transA, int transB, int64_t M, int64_t 
     int64_t need = 0;
     mm_status s = mm_gemm_f32_splitk_workspace(M, N, K, splitk, &need);
     if (s != MM_OK) return s;
+    if (!splitk && need > mm::kSplitkStaticFloats) {
+        // the automatic split does not fit the scratch (stream-K of a large product): no split
+        splitk = 1;
+        need = 0;
+    }
     if (need > mm::kSplitkStaticFloats)
         return fail(MM_ERR_INVALID_ARG,
                     "split-K of %lld x %lld needs %lld floats of scratch; the library's static scratch holds %lld "

@@ -133,8 +133,11 @@ cudaError_t launch_gemm_tf32x3(const GemmArgs &g, cudaStream_t s);
 cudaError_t launch_gemm_tf32x3_ws(const GemmArgs &g, int pair, cudaStream_t s);
 // Split-K form: ksplit slices per output tile computed into ws (ksplit * M * N floats,
 // 16-byte aligned), then summed in slice order into C by a second kernel.
+// ksplit == kStreamK: stream-K instead, ws holding the units' partial-tile slots and flags.
+constexpr int kStreamK = -1;
 cudaError_t launch_gemm_tf32x3_ws_splitk(const GemmArgs &g, int pair, int ksplit, float *ws, cudaStream_t s);
 int gemm_splitk_auto(int64_t M, int64_t N, int64_t K, int pair, int sms);
+int64_t gemm_splitk_workspace_floats(int64_t M, int64_t N, int64_t K, int pair, int split, int sms);
 
 // The static scratch of the split-K entry point that allocates nothing: its device
 // address on the current device (looked up on the first call per device) and size.

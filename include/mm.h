@@ -121,21 +121,28 @@ mm_status mm_gemm_packed2(const uint8_t *codes, const uint16_t *scales, const ui
 mm_status mm_check_device_error(mm_stream_t stream);
 
 /*
- * Split-K form of mm_gemm_f32 for products with few output tiles (short M and N,
- * long K: the GPT-2 MLP shapes at small batch).  K is cut into `splitk` slices
- * (0 = automatic, 1..16); every slice of every output tile is computed by its own
- * CTA into `workspace`, then a second kernel adds the slices in slice order into C
- * (the result is bit-reproducible run to run; it may differ from mm_gemm_f32 in
- * the last bits, by summation order).  Same bound |C - C_exact| <= 1e-5 sum|a b|.
+ * Split-K form of mm_gemm_f32 for products with fewer output tiles than the GPU
+ * has SMs (short M and N, long K: the GPT-2 MLP shapes at small batch; or a
+ * last partial wave, such as 2048^3 on CTA pairs).  splitk = 1..16: K is cut into
+ * that many slices, every slice of every output tile is computed by its own CTA
+ * into `workspace`, then a second kernel adds the slices in slice order into C.
+ * splitk = -1: stream-K -- the tiles' K ranges, laid end to end, are cut evenly
+ * over the SMs; the CTA holding the start of a tile's K range adds the partial
+ * tiles the other CTAs leave in the workspace (in K order, after their flags).
+ * splitk = 0: automatic (no split when the tiles fill the GPU, stream-K when they
+ * fill more than half of it, split slices otherwise).  Results are
+ * bit-reproducible run to run; they may differ from mm_gemm_f32 in the last bits,
+ * by summation order.  Same bound |C - C_exact| <= 1e-5 sum|a b|.
  *
  * workspace: caller-owned device memory, 16-byte aligned, at least the number of
  * floats mm_gemm_f32_splitk_workspace reports for the same M, N, K, splitk
- * (splitk * M * N once the split is resolved; 0 when it resolves to 1, and
- * NULL is then accepted).  It must not overlap A, B or C; its contents on entry
- * do not matter.  Operands TMA cannot describe (A or B not 16-byte aligned, lda
+ * (splitk * M * N for slices; one 128 x 256 partial tile per CTA plus a flag
+ * word for stream-K; 0 when the split resolves to 1, and NULL is then
+ * accepted).  It must not overlap A, B or C; its contents on entry do not
+ * matter.  Calls sharing one workspace must not overlap on the GPU.  Operands TMA cannot describe (A or B not 16-byte aligned, lda
  * or ldb not a multiple of 4) run the unsplit general kernel and leave the
  * workspace untouched.
- * Errors: as mm_gemm_f32, plus MM_ERR_INVALID_ARG for splitk outside 0..16, a
+ * Errors: as mm_gemm_f32, plus MM_ERR_INVALID_ARG for splitk outside -1..16, a
  * misaligned, overlapping or too small workspace.
  */
 mm_status mm_gemm_f32_splitk_workspace(int64_t M, int64_t N, int64_t K, int splitk, int64_t *floats);
@@ -156,8 +163,9 @@ mm_status mm_gemm_f32_splitk(int transA, int transB, int64_t M, int64_t N, int64
  * allocating routine.
  *
  * Same arguments, result and errors as mm_gemm_f32_splitk, plus
- * MM_ERR_INVALID_ARG when the resolved split needs more than
- * MM_SPLITK_NOALLOC_MAX_FLOATS floats (splitk * M * N).  The first call on a
+ * MM_ERR_INVALID_ARG when a given split needs more than
+ * MM_SPLITK_NOALLOC_MAX_FLOATS floats (splitk * M * N); an automatic split
+ * that would need more is replaced by no split.  splitk = -1 is refused.  The first call on a
  * device looks up the array's device address (cudaGetSymbolAddress, with that
  * device current); make that first call before any stream capture.  Every call
  * shares the one array and leaves its partial tiles there; no part of it has to

@@ -101,7 +101,7 @@ def test_gemm_splitk_workspace_size(lib):
     assert lib.mm_gemm_f32_splitk_workspace(8, 8, 8, 2, None) == mm.MM_ERR_INVALID_ARG
 
 
-@pytest.mark.parametrize("case", [dict(splitk=17), dict(splitk=-1), dict(ws=FAKE + 0x100004),
+@pytest.mark.parametrize("case", [dict(splitk=17), dict(splitk=-2), dict(ws=FAKE + 0x100004),
                                   dict(ws_floats=4 * 64 * 64 - 1), dict(ws=None), dict(ws=FAKE + 64),
                                   dict(ws_floats=-5), dict(ldc=10)])
 def test_gemm_splitk_argument_errors(lib, case):

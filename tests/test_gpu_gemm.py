@@ -251,3 +251,40 @@ def test_gemm_splitk_unaligned_operands_take_general_path(oracle):
     C = run_splitk(0, 0, M, N, K, Ap, B, 4, lda=K + 3)
     ref, T = oracle.gemm(0, 0, M, N, K, A, B)
     check_bound(C, ref, T, "general path")
+
+
+@pytest.mark.parametrize("layout", ["nn", "nt", "tn"])
+def test_square_2048_stream_k_auto_all_outputs(oracle, layout):
+    # 64 pair tiles on 76 pairs: the automatic split is stream-K
+    c = synth.square_2048(layout)
+    C = run_splitk(c.transA, c.transB, c.M, c.N, c.K, c.A, c.B, 0)
+    ref, T = oracle.gemm(c.transA, c.transB, c.M, c.N, c.K, c.A, c.B)
+    worst = check_bound(C, ref, T, c.name + " stream-K")
+    print(f"{c.name} stream-K: worst |err|/T = {worst:.3e}")
+
+
+@pytest.mark.parametrize("layout", list(LAYOUTS))
+@pytest.mark.parametrize("shape", [(300, 2000, 1000), (100, 3000, 2000), (2000, 2900, 72), (129, 257, 33),
+                                   (19456, 256, 24), (64, 300, 4096)])
+def test_gemm_stream_k_parity(oracle, layout, shape):
+    # stream-K forced: tiles fewer and more than the units, one- and multi-segment tiles,
+    # short K (a unit spanning several whole tiles), single CTAs and pairs
+    tA, tB = LAYOUTS[layout]
+    M, N, K = shape
+    A, B = stored(tA, tB, M, N, K, seed=1300 + M + N + K)
+    Ap = np.zeros((A.shape[0], (A.shape[1] + 3) // 4 * 4), np.float32); Ap[:, :A.shape[1]] = A
+    Bp = np.zeros((B.shape[0], (B.shape[1] + 3) // 4 * 4), np.float32); Bp[:, :B.shape[1]] = B
+    C = run_splitk(tA, tB, M, N, K, Ap, Bp, -1, lda=Ap.shape[1], ldb=Bp.shape[1], ldc=N + 2)
+    ref, T = oracle.gemm(tA, tB, M, N, K, A, B)
+    check_bound(C[:, :N], ref, T, f"stream-K {layout} {shape}")
+    assert np.all(np.isnan(C[:, N:])), "columns past N were written"
+
+
+def test_gemm_stream_k_deterministic_and_integer_exact(oracle):
+    M, N, K = 700, 900, 2000
+    A, B = stored(0, 1, M, N, K, seed=91, kind="int")
+    ref, _ = oracle.gemm(0, 1, M, N, K, A, B)
+    c1 = run_splitk(0, 1, M, N, K, A, B, -1)
+    c2 = run_splitk(0, 1, M, N, K, A, B, -1, fill=-7.0)
+    check_exact(c1, ref, "stream-K integers")
+    assert np.array_equal(c1.view(np.uint32), c2.view(np.uint32))

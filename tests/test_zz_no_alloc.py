@@ -60,3 +60,22 @@ def test_noalloc_splitk_matches_workspace_entry_two_calls(oracle):
         # the tolerance of every GEMM test, between the two entry points and against the oracle
         check_bound(got, want.astype(np.float64), T, f"call {i}: static scratch vs workspace")
         check_bound(got, ref, T, f"call {i}: static scratch vs oracle")
+
+
+def test_noalloc_automatic_split_falls_back_when_scratch_is_small(oracle):
+    # 4096^3: the automatic split (stream-K, 256 pair tiles on 76 pairs) needs more than the
+    # static scratch; the entry point then runs the product unsplit instead of refusing it
+    M = N = K = 4096
+    assert mm.mm_gemm_f32_splitk_workspace(M, N, K, 0) > mm.MM_SPLITK_NOALLOC_MAX_FLOATS
+    A = synth.normal_f32(4300, (M, K), 0.02)
+    B = synth.normal_f32(4301, (K, N), 0.02)
+    dA, dB = to_dev(A), to_dev(B)
+    C = empty_f32((M, N))
+    mm.mm_gemm_f32_splitk_noalloc(0, 0, M, N, K, dA, K, dB, N, C, N, 0)
+    mm.mm_check_device_error()
+    got = to_host(C)
+    rng = np.random.default_rng(3)
+    ii = np.concatenate([np.repeat([0, M - 1], N), rng.integers(0, M, 3000)])
+    jj = np.concatenate([np.tile(np.arange(N), 2), rng.integers(0, N, 3000)])
+    ref, T = oracle.gemm_at(0, 0, K, A, B, ii, jj)
+    check_bound(got[ii, jj], ref, T, "4096^3 through the static-scratch entry point")
