@@ -60,6 +60,7 @@ constexpr int NTHREADS = 320;
 constexpr int TMEM_COLS = NACC * ACC_COLS;    // 512: the whole tensor memory of the SM
 constexpr int SMEM_LIMIT = 227 * 1024;
 constexpr int MAX_STAGES = 6;
+constexpr int EPI_TMA_BYTES = 4 * 32 * 128;   // CTA pairs: a 32 x 32 fp32 block per epilogue warp for TMA stores
 
 // Shared-memory plan of one stage of one CTA.  CG CTAs share a tile of
 // (128 CG) x BN: each holds 128 rows of op(A) and BN / CG rows of op(B).  A
@@ -79,10 +80,11 @@ struct Plan {
     static constexpr int RAW_A = 0, HI_A = A_KC ? 0 : A_BYTES, LO_A = A_KC ? A_BYTES : 2 * A_BYTES;
     static constexpr int RAW_B = A_REGION, HI_B = A_REGION + (B_KC ? 0 : B_BYTES),
                          LO_B = A_REGION + (B_KC ? B_BYTES : 2 * B_BYTES);
-    static constexpr int FIXED = (3 * MAX_STAGES + 2 * NACC + 2) * 8 + 16 + 1024;
+    static constexpr int EPI = CG == 2 ? EPI_TMA_BYTES : 0;
+    static constexpr int FIXED = EPI + (3 * MAX_STAGES + 2 * NACC + 2) * 8 + 16 + 1024;
     static constexpr int S_FIT = (SMEM_LIMIT - FIXED) / STAGE_BYTES;
     static constexpr int STAGES = S_FIT < MAX_STAGES ? S_FIT : MAX_STAGES;
-    static constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + (3 * STAGES + 2 * NACC + 2) * 8 + 16 + 1024;
+    static constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + EPI + (3 * STAGES + 2 * NACC + 2) * 8 + 16 + 1024;
     static_assert(STAGES >= 3, "at least three stages");
     static_assert(SMEM_BYTES <= SMEM_LIMIT, "shared memory");
 };
@@ -100,6 +102,7 @@ struct WsParams {
     int sk, sk_w, sk_total;
     float *sk_slots;        // [unit][rank][128][BN] fp32
     unsigned int *sk_flags; // [unit][rank], zeroed before the launch
+    int c_tma;              // CTA pairs: C is stored through shared memory by TMA (tmC valid)
 };
 
 // Work unit t: output tile t / ksplit, K slice t % ksplit (slabs [kt0, kt1)).
@@ -217,12 +220,13 @@ __device__ __forceinline__ bool flag_wait(const unsigned int *f) {
 template <bool A_KC, bool B_KC, int CG, int BN, bool SK>
 __global__ void __launch_bounds__(NTHREADS, 1)
     gemm_tf32x3_ws_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-                          const WsParams p) {
+                          const __grid_constant__ CUtensorMap tmC, const WsParams p) {
     using P = Plan<A_KC, B_KC, CG, BN>;
     constexpr int STAGES = P::STAGES, STAGE_BYTES = P::STAGE_BYTES, BNC = P::BNC;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = smem_aligned<1024>(smem_raw);
-    uint64_t *full = reinterpret_cast<uint64_t *>(smem + STAGES * STAGE_BYTES);  // TMA -> lo pass (own CTA)
+    uint8_t *epi_stage = smem + STAGES * STAGE_BYTES;  // CTA pairs: [4 warps][32 rows][128 B], 128-byte swizzled
+    uint64_t *full = reinterpret_cast<uint64_t *>(smem + STAGES * STAGE_BYTES + P::EPI);  // TMA -> lo pass
     uint64_t *conv = full + STAGES;    // lo passes -> MMA (CTA 0's, one arrival per lo-pass warp of the pair)
     uint64_t *empty = conv + STAGES;   // MMA -> TMA (every CTA's, by commit)
     uint64_t *accf = empty + STAGES;   // MMA -> epilogue (every CTA's, by commit)
@@ -466,6 +470,24 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                         v[4 * j + 3] += a.w;
                     }
                 }
+                if (CG == 2 && p.c_tma && !p.ws) {
+                    // the warp's 32 x 32 block to its swizzled staging buffer (16-byte chunk k of
+                    // row i at k ^ (i % 8), conflict-free), then one TMA store that clips at M, N
+                    uint8_t *stg = epi_stage + q * 4096;
+                    if (lane == 0) bulk_wait_read_all();  // the previous block has left the buffer
+                    __syncwarp();
+#pragma unroll
+                    for (int k = 0; k < 8; ++k)
+                        *reinterpret_cast<float4 *>(stg + lane * 128 + ((k ^ (lane & 7)) << 4)) =
+                            make_float4(v[4 * k], v[4 * k + 1], v[4 * k + 2], v[4 * k + 3]);
+                    fence_proxy_async_smem();
+                    __syncwarp();
+                    if (lane == 0 && m0 + 32 * q < p.M && n0 + c0 < p.N) {
+                        tma_store_2d(&tmC, stg, n0 + c0, m0 + 32 * q);
+                        bulk_commit();
+                    }
+                    continue;
+                }
                 // columns of this chunk inside the tile (the last chunk of a 240-wide tile has 16)
                 const int w = BN - c0 < 32 ? BN - c0 : 32;
                 if (row < p.M && n0 + c0 < p.N) {
@@ -490,6 +512,8 @@ __global__ void __launch_bounds__(NTHREADS, 1)
             __syncwarp();
             if (lane == 0) arrive_leader<CG>(&acce[b]);
         }
+        // TMA stores of C complete before the CTA's shared memory is released
+        if (CG == 2 && lane == 0) bulk_wait_all();
     }
 
     tc_fence_before_sync();
@@ -503,7 +527,8 @@ __global__ void __launch_bounds__(NTHREADS, 1)
 }
 
 template <bool A_KC, bool B_KC, int CG, int BN, bool SK>
-cudaError_t launch_ws1(const CUtensorMap &ta, const CUtensorMap &tb, const WsParams &p, int grid, cudaStream_t s) {
+cudaError_t launch_ws1(const CUtensorMap &ta, const CUtensorMap &tb, const CUtensorMap &tc, const WsParams &p,
+                       int grid, cudaStream_t s) {
     auto kern = gemm_tf32x3_ws_kernel<A_KC, B_KC, CG, BN, SK>;
     constexpr int smem = Plan<A_KC, B_KC, CG, BN>::SMEM_BYTES;
     static std::once_flag once;
@@ -524,7 +549,7 @@ cudaError_t launch_ws1(const CUtensorMap &ta, const CUtensorMap &tb, const WsPar
     attr[0].val.clusterDim.z = 1;
     lc.attrs = attr;
     lc.numAttrs = CG == 2 ? 1 : 0;
-    return cudaLaunchKernelEx(&lc, kern, ta, tb, p);
+    return cudaLaunchKernelEx(&lc, kern, ta, tb, tc, p);
 }
 
 // C = sum over the ksplit slices of the workspace, added in slice order (bit-reproducible).
@@ -558,9 +583,10 @@ __global__ void __launch_bounds__(256) splitk_reduce_kernel(const float *__restr
 }
 
 template <bool A_KC, bool B_KC, int CG, int BN>
-cudaError_t launch_ws(const CUtensorMap &ta, const CUtensorMap &tb, const WsParams &p, int grid, cudaStream_t s) {
-    return p.sk ? launch_ws1<A_KC, B_KC, CG, BN, true>(ta, tb, p, grid, s)
-                : launch_ws1<A_KC, B_KC, CG, BN, false>(ta, tb, p, grid, s);
+cudaError_t launch_ws(const CUtensorMap &ta, const CUtensorMap &tb, const CUtensorMap &tc, const WsParams &p, int grid,
+                      cudaStream_t s) {
+    return p.sk ? launch_ws1<A_KC, B_KC, CG, BN, true>(ta, tb, tc, p, grid, s)
+                : launch_ws1<A_KC, B_KC, CG, BN, false>(ta, tb, tc, p, grid, s);
 }
 
 template <int CG, int BN>
@@ -589,7 +615,13 @@ cudaError_t launch_ws_cg(const GemmArgs &g, int sms, int ksplit, float *ws, cuda
     float *const sk_ws = ws;
     if (ksplit < 2) ws = nullptr;
     WsParams p{(int)g.M, (int)g.N, (int)g.K, tiles_m, tiles_m * tiles_n * (ws ? ksplit : 1), ws ? ksplit : 1,
-               g.C, g.ldc, ws, 0, 0, 0, nullptr, nullptr};
+               g.C, g.ldc, ws, 0, 0, 0, nullptr, nullptr, 0};
+    // C through TMA stores (CTA pairs): 16-byte aligned C, ldc a multiple of 4
+    CUtensorMap tc = ta;
+    if (CG == 2 && (reinterpret_cast<uintptr_t>(g.C) & 15) == 0 && g.ldc % 4 == 0 &&
+        make_tmap_2d(&tc, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, g.C, g.N, g.M, g.ldc * 4, 32, 32,
+                     CU_TENSOR_MAP_SWIZZLE_128B) == cudaSuccess)
+        p.c_tma = 1;
     const int units = sms / CG;
     int grid = CG * (p.tiles < units ? p.tiles : units);
     if (sk) {
@@ -605,10 +637,10 @@ cudaError_t launch_ws_cg(const GemmArgs &g, int sms, int ksplit, float *ws, cuda
         grid = CG * used;
         ws = nullptr;  // no second kernel
     }
-    if (!g.transA && !g.transB) e = launch_ws<true, false, CG, BN>(ta, tb, p, grid, s);
-    else if (!g.transA && g.transB) e = launch_ws<true, true, CG, BN>(ta, tb, p, grid, s);
-    else if (g.transA && !g.transB) e = launch_ws<false, false, CG, BN>(ta, tb, p, grid, s);
-    else e = launch_ws<false, true, CG, BN>(ta, tb, p, grid, s);
+    if (!g.transA && !g.transB) e = launch_ws<true, false, CG, BN>(ta, tb, tc, p, grid, s);
+    else if (!g.transA && g.transB) e = launch_ws<true, true, CG, BN>(ta, tb, tc, p, grid, s);
+    else if (g.transA && !g.transB) e = launch_ws<false, false, CG, BN>(ta, tb, tc, p, grid, s);
+    else e = launch_ws<false, true, CG, BN>(ta, tb, tc, p, grid, s);
     if (e != cudaSuccess || !ws) return e;
     const int64_t work = (g.M * g.N + 3) / 4;
     const int64_t blocks = (work + 255) / 256;
