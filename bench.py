@@ -13,7 +13,9 @@ Prints ONE JSON line (rank 0).  One step is one pass of the whole hot path:
      kernel before reading x; only its weight loads start early);
   3. the ternary 16-layer encoder block: 16 x (222x768 -> 3072, 222x3072 -> 768);
   4. the 4-bit 12,288 x 1,536 GEMV and the transposed 2-bit 1,536 x 12,288 GEMV,
-     each over a 64-matrix rotation of independent calls.
+     each over a 64-matrix rotation of independent calls;
+  5. the training-shape set: 8192 x 8192 x 2048 forward and its two backward
+     products, through the split entry point (automatic split, one workspace).
 Each phase is captured once as a CUDA graph and replayed; every replay is timed
 with CUDA events on the stream it runs on.  The headline value is the 2048^3
 GEMM throughput (TFLOP/s); the GEMV weight bandwidth (GB/s: 4,718,592 bytes of
@@ -51,12 +53,13 @@ GEMV4_WEIGHT_BYTES = 12288 * 1536 // 2          # 9,437,184
 GEMV4_TOTAL_BYTES = GEMV4_WEIGHT_BYTES + 12288 * 2 + 1536 * 2 + 12288 * 4
 GEMVT_TOTAL_BYTES = GEMV_WEIGHT_BYTES + 1536 * 2 + 12288 * 2 + 1536 * 4   # 1536 x 12288: same weight bytes
 GEMM_FLOP = 2.0 * 2048 ** 3
+TRAIN_FLOP = 3 * 2.0 * 8192 * 8192 * 2048  # forward + the two backward products, 274.9 GFLOP each
 TERN_FLOP_PER_LAYER = 2 * (2.0 * 222 * 3072 * 768)
 N_GEMV = 64
 N_LAYERS = 16
 WORKLOAD = ("square_2048_fp32_gemm_nn_nt_tn + gemv2bit_12288x1536_rotation64 + "
             "ternary_encoder_16x(222x768x3072,222x3072x768) + gemv4bit_12288x1536_rotation64 + "
-            "gemv2bit_1536x12288_rotation64")
+            "gemv2bit_1536x12288_rotation64 + training_set_8192x2048x8192_fwd_dA_dB")
 
 
 def parse_args(argv=None):
@@ -252,6 +255,24 @@ class Workload:
                                       scales=torch.from_numpy(c.scales).to(device),
                                       X=torch.from_numpy(c.X).to(device),
                                       Y=torch.empty((c.X.shape[0], c.rows), dtype=torch.float32, device=device)))
+        # training-shape set: forward C = A B, dA = dC B^T, dB = A^T dC (N(0, 0.02)), through the
+        # split entry point with its automatic choice and one shared workspace
+        self.train = []
+        for which in ("fwd", "dA", "dB"):
+            c = synth.training_set_8192(which)
+            self.train.append(c)
+        tA = torch.from_numpy(self.train[0].A if not off else synth.normal_f32(off + 21, (8192, 2048), 0.02)).to(device)
+        tB = torch.from_numpy(self.train[0].B if not off else synth.normal_f32(off + 22, (2048, 8192), 0.02)).to(device)
+        tdC = torch.from_numpy(self.train[1].A if not off else synth.normal_f32(off + 23, (8192, 8192), 0.02)).to(device)
+        import dense_packed_bit_gb300 as mm
+        self.train_ops = []
+        need = 0
+        for c, (a, b) in zip(self.train, ((tA, tB), (tdC, tB), (tA, tdC))):
+            out = torch.empty((c.M, c.N), dtype=torch.float32, device=device)
+            self.train_ops.append((c, a, b, out))
+            need = max(need, mm.mm_gemm_f32_splitk_workspace(c.M, c.N, c.K, 0))
+        self.train_ws = torch.empty(max(need, 4), dtype=torch.float32, device=device)
+        self.train_ws_floats = need
         self.flush = torch.empty(512 * 1024 * 1024 // 4, dtype=torch.float32, device=device)
         self.args = args
 
@@ -318,6 +339,11 @@ def capture_phases(w: Workload, stream):
                                   w.gemv_cb, st, **GEMVT_INDEP)
         cur.wait_stream(side)
 
+    def train():
+        for c, a, b, out in w.train_ops:
+            mm.mm_gemm_f32_splitk(c.transA, c.transB, c.M, c.N, c.K, a, a.shape[1], b, b.shape[1], out, c.N, 0,
+                                  w.train_ws, w.train_ws_floats)
+
     def tern():
         for t in w.tern:
             c = t["case"]
@@ -325,7 +351,7 @@ def capture_phases(w: Workload, stream):
 
     graphs = {}
     for name, fn in (("gemm", gemm), ("gemv", gemv(GEMV_INDEP, GEMV_INDEP_STREAMS)), ("gemv_c", gemv(GEMV_CHAINED)),
-                     ("tern", tern), ("gemv4", gemv4), ("gemvt", gemvt)):
+                     ("tern", tern), ("gemv4", gemv4), ("gemvt", gemvt), ("train", train)):
         with torch.cuda.stream(stream):
             fn()  # warm the kernels' one-time setup outside capture
         torch.cuda.synchronize()
@@ -336,13 +362,13 @@ def capture_phases(w: Workload, stream):
     return graphs
 
 
-LAUNCHES_PER_STEP = 3 + 4 * N_GEMV + 2 * N_LAYERS
+LAUNCHES_PER_STEP = 3 + 4 * N_GEMV + 2 * N_LAYERS + 3  # + the training set's 3 GEMM kernels
 
 
 def run_step(w: Workload, graphs, ev, stream):
     """One pass of the hot path; ev maps each phase to a (start, end) event pair."""
     w.flush.fill_(1.0)  # evict the GEMM operands from L2 (torch kernel, outside the events)
-    for name in ("gemm", "gemv", "gemv_c", "tern", "gemv4", "gemvt"):
+    for name in ("gemm", "gemv", "gemv_c", "tern", "gemv4", "gemvt", "train"):
         ev[name][0].record(stream)
         graphs[name].replay()
         ev[name][1].record(stream)
@@ -351,7 +377,7 @@ def run_step(w: Workload, graphs, ev, stream):
 def new_events():
     import torch
     mk = lambda: (torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-    return {"gemm": mk(), "gemv": mk(), "gemv_c": mk(), "tern": mk(), "gemv4": mk(), "gemvt": mk()}
+    return {"gemm": mk(), "gemv": mk(), "gemv_c": mk(), "tern": mk(), "gemv4": mk(), "gemvt": mk(), "train": mk()}
 
 
 def e2e_gemm(w: Workload, steps: int, stream):
@@ -505,6 +531,7 @@ def main_mm(args):
     tern_total_s = total_s("tern")
     gemv4_total_s = total_s("gemv4")
     gemvt_total_s = total_s("gemvt")
+    train_total_s = total_s("train")
     wall = reduce_max(wall, dev)
 
     gemm_tflops = world * 3 * GEMM_FLOP * args.steps / gemm_total_s / 1e12
@@ -514,7 +541,8 @@ def main_mm(args):
     tern_tflops = world * N_LAYERS * TERN_FLOP_PER_LAYER * args.steps / tern_total_s / 1e12
     per_call_gemv4_s = gemv4_total_s / (args.steps * N_GEMV)
     per_call_gemvt_s = gemvt_total_s / (args.steps * N_GEMV)
-    step_ms = (gemm_total_s + gemv_total_s + gemvc_total_s + tern_total_s + gemv4_total_s + gemvt_total_s) / args.steps * 1e3
+    step_ms = (gemm_total_s + gemv_total_s + gemvc_total_s + tern_total_s + gemv4_total_s + gemvt_total_s +
+               train_total_s) / args.steps * 1e3
 
     peaks, peaks_src = measured_peaks()
     props = torch.cuda.get_device_properties(dev)
@@ -546,6 +574,7 @@ def main_mm(args):
                    "gemv": "12288x1536 2-bit, 64-matrix rotation (288 MiB > L2), codebook {-2,-1,0,1}",
                    "ternary": "16 layers, M=222, up 768->3072 and down 3072->768",
                    "gemv_t": "1536x12288 2-bit, 64-matrix rotation (288 MiB > L2)",
+                   "training_set": "8192x8192x2048 NN, dA=dC.B^T 8192x2048x8192, dB=A^T.dC 2048x8192x8192, N(0,0.02)",
                    "l2": "512 MiB buffer written before the GEMM phase of every step; GEMV inputs exceed L2",
                    "gemv_opts": {"independent": GEMV_INDEP, "independent_streams": GEMV_INDEP_STREAMS,
                                  "chained": GEMV_CHAINED},
@@ -582,6 +611,10 @@ def main_mm(args):
                                 "peak": peaks["hbm_gbs"], "unit": "GB/s",
                                 "frac": GEMVT_TOTAL_BYTES / per_call_gemvt_s / 1e9 / peaks["hbm_gbs"],
                                 "traffic": None, "peak_source": peaks_src}},
+        "training_set": {"metric": "fp32 GEMM TFLOP/s, 8192x8192x2048 forward + dA (NT) + dB (TN)",
+                         "value": world * TRAIN_FLOP * args.steps / train_total_s / 1e12, "unit": "TFLOP/s",
+                         "ms_per_set": train_total_s / args.steps * 1e3,
+                         "path": "mm_gemm_f32_splitk, automatic split (plain for the forward product, stream-K for dA and dB)"},
         "roofline": roof,
         "clocks": clk,
         "gpu_launches": LAUNCHES_PER_STEP * args.steps,
