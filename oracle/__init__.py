@@ -13,7 +13,10 @@ Pins (tests/test_oracle.py): closed forms (all-ones, identity, rank-1),
 textbook small products, exact integer products against numpy int64 matmul,
 the fp16 decoder against numpy's float16 for all 65,536 patterns, the unpacker
 against a hand-written byte table and a pack/unpack round trip, and the packed
-GEMM against dense products of explicitly decoded weights.
+GEMM against dense products of explicitly decoded weights; the GELU of the fused
+epilogue (gelu_tanh, gemm_bias_act) against its odd-part identity, the
+library's normal CDF (z Phi(z), which the tanh form approximates) and special
+values, and the bias broadcast on a zero product.
 """
 from __future__ import annotations
 
@@ -113,6 +116,30 @@ def gemm(transA: int, transB: int, M: int, N: int, K: int, A: np.ndarray, B: np.
     lib.orc_gemm(int(transA), int(transB), M, N, K, _ptr(A), lda, _ptr(B), ldb,
                  _ptr(C), _ptr(T), threads or default_threads())
     return C, T
+
+
+def gelu_tanh(z) -> np.ndarray:
+    """GELU in the tanh form GPT-2 uses, in fp64:
+    gelu(z) = z/2 (1 + tanh(sqrt(2/pi) (z + 0.044715 z^3))).
+    The pages name GPT-2's training step but print no activation; this is the
+    published GPT-2 definition, written out plainly."""
+    z = np.asarray(z, dtype=np.float64)
+    return 0.5 * z * (1.0 + np.tanh(np.sqrt(2.0 / np.pi) * (z + 0.044715 * z * z * z)))
+
+
+def gemm_bias_act(transA: int, transB: int, M: int, N: int, K: int, A: np.ndarray, B: np.ndarray,
+                  bias=None, act: int = 0, lda: int | None = None, ldb: int | None = None):
+    """(Y, T, Z) of Y = act(op(A) op(B) + bias) in fp64: bias has N entries (one per output
+    column, broadcast over the rows) or is None; act 0 is the identity, 1 is gelu_tanh.
+    Z is the pre-activation op(A) op(B) + bias; T = sum_k |a b| + |bias| bounds the
+    error the GEMM and the bias add may make."""
+    C, T = gemm(transA, transB, M, N, K, A, B, lda, ldb)
+    if bias is not None:
+        b = np.asarray(bias, dtype=np.float32).astype(np.float64).reshape(1, N)
+        C = C + b
+        T = T + np.abs(b)
+    Y = gelu_tanh(C) if act == 1 else C
+    return Y, T, C
 
 
 def gemm_at(transA: int, transB: int, K: int, A: np.ndarray, B: np.ndarray, ii, jj,

@@ -420,3 +420,52 @@ def test_normal_quantile_codebook():
     top = synth._normal_ppf(0.98)
     for i in range(1, 9):
         assert cb[7 + i] == np.float32(synth._normal_ppf(0.5 + 0.48 * i / 8) / top)
+
+
+# ------------------------------------------------------------------ bias + GELU epilogue
+
+def test_gelu_tanh_odd_part_is_identity(oracle):
+    # gelu(z) - gelu(-z) = z/2 (1 + t) + z/2 (1 - t) = z for the tanh form, any constants
+    z = np.linspace(-9.0, 9.0, 1001)
+    assert np.allclose(oracle.gelu_tanh(z) - oracle.gelu_tanh(-z), z, rtol=0, atol=1e-14)
+
+
+def test_gelu_tanh_matches_erf_form(oracle):
+    # the tanh form approximates z Phi(z) (Phi from the library's normal CDF) to within
+    # about 5e-4 everywhere; a wrong constant (sqrt(2/pi), 0.044715) or a dropped cubic
+    # term misses by far more
+    from scipy.special import ndtr
+    z = np.linspace(-8.0, 8.0, 4001)
+    exact = z * ndtr(z)
+    d = np.abs(oracle.gelu_tanh(z) - exact)
+    assert d.max() < 1e-3 and d.max() > 1e-5
+    wrong_cubic = 0.5 * z * (1 + np.tanh(np.sqrt(2 / np.pi) * z))
+    assert np.abs(wrong_cubic - exact).max() > 5e-3
+
+
+def test_gelu_tanh_special_values(oracle):
+    g = oracle.gelu_tanh(np.array([0.0, 10.0, -10.0, 30.0]))
+    assert g[0] == 0.0 and g[1] == 10.0 and g[2] == 0.0 and g[3] == 30.0
+    h = 1e-6  # slope 1/2 at the origin
+    assert abs((oracle.gelu_tanh(h) - oracle.gelu_tanh(-h)) / (2 * h) - 0.5) < 1e-9
+
+
+def test_gemm_bias_broadcasts_over_rows(oracle):
+    # zero product: every row is the bias vector (one entry per output column)
+    M, N, K = 5, 7, 3
+    A = np.zeros((M, K), np.float32)
+    B = np.ones((K, N), np.float32)
+    bias = np.arange(N, dtype=np.float32) - 3.0
+    Y, T, Z = oracle.gemm_bias_act(0, 0, M, N, K, A, B, bias, act=0)
+    assert np.array_equal(Y, np.tile(bias.astype(np.float64), (M, 1)))
+    assert np.array_equal(T, np.tile(np.abs(bias).astype(np.float64), (M, 1)))
+    Y1, _, _ = oracle.gemm_bias_act(0, 0, M, N, K, A, B, bias, act=1)
+    assert np.array_equal(Y1, oracle.gelu_tanh(np.tile(bias.astype(np.float64), (M, 1))))
+
+
+def test_gemm_bias_act_without_bias_is_gemm(oracle):
+    A = synth.normal_f32(5, (33, 17), 1.0)
+    B = synth.normal_f32(6, (17, 21), 1.0)
+    C, T = oracle.gemm(0, 0, 33, 21, 17, A, B)
+    Y, T2, Z = oracle.gemm_bias_act(0, 0, 33, 21, 17, A, B, None, act=0)
+    assert np.array_equal(Y, C) and np.array_equal(T2, T) and np.array_equal(Z, C)
