@@ -54,6 +54,8 @@ GEMV4_TOTAL_BYTES = GEMV4_WEIGHT_BYTES + 12288 * 2 + 1536 * 2 + 12288 * 4
 GEMVT_TOTAL_BYTES = GEMV_WEIGHT_BYTES + 1536 * 2 + 12288 * 2 + 1536 * 4   # 1536 x 12288: same weight bytes
 GEMM_FLOP = 2.0 * 2048 ** 3
 TRAIN_FLOP = 3 * 2.0 * 8192 * 8192 * 2048  # forward + the two backward products, 274.9 GFLOP each
+MLP_M, MLP_N, MLP_K = 8192, 3072, 768  # GPT-2 small MLP up-projection, 8 x 1024 tokens
+MLP_FLOP = 2.0 * MLP_M * MLP_N * MLP_K  # 38.7 GFLOP (the bias and GELU are O(MN), not counted)
 TERN_FLOP_PER_LAYER = 2 * (2.0 * 222 * 3072 * 768)
 N_GEMV = 64
 N_LAYERS = 16
@@ -273,6 +275,11 @@ class Workload:
             need = max(need, mm.mm_gemm_f32_splitk_workspace(c.M, c.N, c.K, 0))
         self.train_ws = torch.empty(max(need, 4), dtype=torch.float32, device=device)
         self.train_ws_floats = need
+        # GPT-2 small's MLP up-projection with its bias and GELU fused, 8 sequences of 1024 tokens
+        self.mlp_x = torch.from_numpy(synth.normal_f32(off + 31, (MLP_M, MLP_K), 1.0)).to(device)
+        self.mlp_w = torch.from_numpy(synth.normal_f32(off + 32, (MLP_K, MLP_N), 0.02)).to(device)
+        self.mlp_b = torch.from_numpy(synth.normal_f32(off + 33, (MLP_N,), 0.02)).to(device)
+        self.mlp_y = torch.empty((MLP_M, MLP_N), dtype=torch.float32, device=device)
         self.flush = torch.empty(512 * 1024 * 1024 // 4, dtype=torch.float32, device=device)
         self.args = args
 
@@ -344,6 +351,10 @@ def capture_phases(w: Workload, stream):
             mm.mm_gemm_f32_splitk(c.transA, c.transB, c.M, c.N, c.K, a, a.shape[1], b, b.shape[1], out, c.N, 0,
                                   w.train_ws, w.train_ws_floats)
 
+    def mlp():
+        mm.mm_gemm_f32_bias_act(0, 0, MLP_M, MLP_N, MLP_K, w.mlp_x, MLP_K, w.mlp_w, MLP_N, w.mlp_b,
+                                mm.MM_ACT_GELU_TANH, w.mlp_y, MLP_N)
+
     def tern():
         for t in w.tern:
             c = t["case"]
@@ -351,7 +362,7 @@ def capture_phases(w: Workload, stream):
 
     graphs = {}
     for name, fn in (("gemm", gemm), ("gemv", gemv(GEMV_INDEP, GEMV_INDEP_STREAMS)), ("gemv_c", gemv(GEMV_CHAINED)),
-                     ("tern", tern), ("gemv4", gemv4), ("gemvt", gemvt), ("train", train)):
+                     ("tern", tern), ("gemv4", gemv4), ("gemvt", gemvt), ("train", train), ("mlp", mlp)):
         with torch.cuda.stream(stream):
             fn()  # warm the kernels' one-time setup outside capture
         torch.cuda.synchronize()
@@ -362,13 +373,16 @@ def capture_phases(w: Workload, stream):
     return graphs
 
 
-LAUNCHES_PER_STEP = 3 + 4 * N_GEMV + 2 * N_LAYERS + 3  # + the training set's 3 GEMM kernels
+LAUNCHES_PER_STEP = 3 + 4 * N_GEMV + 2 * N_LAYERS + 3 + 1  # + the training set's 3 GEMMs + the MLP GEMM
+
+
+PHASES = ("gemm", "gemv", "gemv_c", "tern", "gemv4", "gemvt", "train", "mlp")
 
 
 def run_step(w: Workload, graphs, ev, stream):
     """One pass of the hot path; ev maps each phase to a (start, end) event pair."""
     w.flush.fill_(1.0)  # evict the GEMM operands from L2 (torch kernel, outside the events)
-    for name in ("gemm", "gemv", "gemv_c", "tern", "gemv4", "gemvt", "train"):
+    for name in PHASES:
         ev[name][0].record(stream)
         graphs[name].replay()
         ev[name][1].record(stream)
@@ -377,7 +391,7 @@ def run_step(w: Workload, graphs, ev, stream):
 def new_events():
     import torch
     mk = lambda: (torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-    return {"gemm": mk(), "gemv": mk(), "gemv_c": mk(), "tern": mk(), "gemv4": mk(), "gemvt": mk(), "train": mk()}
+    return {name: mk() for name in PHASES}
 
 
 def e2e_gemm(w: Workload, steps: int, stream):
@@ -532,6 +546,7 @@ def main_mm(args):
     gemv4_total_s = total_s("gemv4")
     gemvt_total_s = total_s("gemvt")
     train_total_s = total_s("train")
+    mlp_total_s = total_s("mlp")
     wall = reduce_max(wall, dev)
 
     gemm_tflops = world * 3 * GEMM_FLOP * args.steps / gemm_total_s / 1e12
@@ -542,7 +557,7 @@ def main_mm(args):
     per_call_gemv4_s = gemv4_total_s / (args.steps * N_GEMV)
     per_call_gemvt_s = gemvt_total_s / (args.steps * N_GEMV)
     step_ms = (gemm_total_s + gemv_total_s + gemvc_total_s + tern_total_s + gemv4_total_s + gemvt_total_s +
-               train_total_s) / args.steps * 1e3
+               train_total_s + mlp_total_s) / args.steps * 1e3
 
     peaks, peaks_src = measured_peaks()
     props = torch.cuda.get_device_properties(dev)
@@ -615,6 +630,11 @@ def main_mm(args):
                          "value": world * TRAIN_FLOP * args.steps / train_total_s / 1e12, "unit": "TFLOP/s",
                          "ms_per_set": train_total_s / args.steps * 1e3,
                          "path": "mm_gemm_f32_splitk, automatic split (plain for the forward product, stream-K for dA and dB)"},
+        "gpt2_mlp_up": {"metric": "fp32 GEMM TFLOP/s with bias + GELU (tanh form) fused in the epilogue",
+                        "value": world * MLP_FLOP * args.steps / mlp_total_s / 1e12, "unit": "TFLOP/s",
+                        "us_per_call": mlp_total_s / args.steps * 1e6,
+                        "shape": f"{MLP_M}x{MLP_N}x{MLP_K} NN (8 x 1024 tokens, 768 -> 3072), N(0,1) x N(0,0.02)",
+                        "path": "mm_gemm_f32_bias_act"},
         "roofline": roof,
         "clocks": clk,
         "gpu_launches": LAUNCHES_PER_STEP * args.steps,

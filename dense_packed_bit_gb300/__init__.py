@@ -19,7 +19,7 @@ __all__ = [
     "mm_gemm_f32", "mm_gemm_f32_ex", "mm_gemv_packed2", "mm_gemv_packed2_ex",
     "mm_gemm_packed2", "mm_gemm_packed2_ex", "mm_gemv_packed4", "mm_gemv_packed4_ex",
     "mm_check_device_error", "mm_gemm_f32_splitk", "mm_gemm_f32_splitk_workspace", "mm_gemm_f32_splitk_noalloc",
-    "MM_SPLITK_NOALLOC_MAX_FLOATS",
+    "MM_SPLITK_NOALLOC_MAX_FLOATS", "mm_gemm_f32_bias_act", "MM_ACT_NONE", "MM_ACT_GELU_TANH",
     "MM_OK", "MM_ERR_INVALID_ARG", "MM_ERR_UNSUPPORTED", "MM_ERR_CUDA", "MM_ERR_TIMEOUT",
     "MM_GEMM_AUTO", "MM_GEMM_FFMA", "MM_GEMM_TF32X3",
     "MM_DEQ_AUTO", "MM_DEQ_SELECT", "MM_DEQ_AFFINE", "MM_DEQ_MMA", "MM_DEQ_FP8", "MM_DEQ_TC",
@@ -29,6 +29,7 @@ MM_OK, MM_ERR_INVALID_ARG, MM_ERR_UNSUPPORTED, MM_ERR_CUDA, MM_ERR_TIMEOUT = 0, 
 MM_GEMM_AUTO, MM_GEMM_FFMA, MM_GEMM_TF32X3 = 0, 1, 2
 MM_DEQ_AUTO, MM_DEQ_SELECT, MM_DEQ_AFFINE, MM_DEQ_MMA, MM_DEQ_FP8, MM_DEQ_TC = 0, 1, 2, 3, 4, 5
 MM_SPLITK_NOALLOC_MAX_FLOATS = 4194304  # floats of the static split-K scratch (16 MiB), as in mm.h
+MM_ACT_NONE, MM_ACT_GELU_TANH = 0, 1
 
 _PKG = os.path.dirname(os.path.abspath(__file__))
 _lock = threading.Lock()
@@ -77,6 +78,7 @@ SIGNATURES = {
                            ctypes.c_int),
     "mm_gemm_f32_splitk_noalloc": ([_I, _I, _I64, _I64, _I64, _P, _I64, _P, _I64, _P, _I64, _I, _P],
                                    ctypes.c_int),
+    "mm_gemm_f32_bias_act": ([_I, _I, _I64, _I64, _I64, _P, _I64, _P, _I64, _P, _I, _P, _I64, _P], ctypes.c_int),
 }
 
 
@@ -171,6 +173,12 @@ def mm_gemm_f32_splitk(transA, transB, M, N, K, A, lda, B, ldb, C, ldc, splitk, 
     _check(load_library().mm_gemm_f32_splitk(int(transA), int(transB), M, N, K, _ptr(A), lda, _ptr(B), ldb,
                                              _ptr(C), ldc, int(splitk), _ptr(workspace), int(workspace_floats),
                                              _stream(stream)))
+
+
+def mm_gemm_f32_bias_act(transA, transB, M, N, K, A, lda, B, ldb, bias, act, C, ldc, stream=None):
+    """C = act(op(A) op(B) + bias): GPT-2's linear layer (bias per column) and GELU (act=1)."""
+    _check(load_library().mm_gemm_f32_bias_act(int(transA), int(transB), M, N, K, _ptr(A), lda, _ptr(B), ldb,
+                                               _ptr(bias), int(act), _ptr(C), ldc, _stream(stream)))
 
 
 def mm_gemm_f32_splitk_noalloc(transA, transB, M, N, K, A, lda, B, ldb, C, ldc, splitk=0, stream=None):

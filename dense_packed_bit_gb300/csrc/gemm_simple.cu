@@ -7,7 +7,9 @@
 // thread accumulates a small block of outputs in registers from them (here
 // 64 x 64 tiles, 4 x 4 per thread).  Partial tiles are masked at the edges
 // ("More Stumbling, This Time in the Browser", section "Four answers per
-// worker": the edge masks).  Every output sums k in increasing order.
+// worker": the edge masks).  Every output sums k in increasing order.  The
+// optional epilogue adds a per-column bias and applies GELU (GPT-2's linear
+// layer and MLP activation).
 #include "mm_common.cuh"
 #include "mm_internal.h"
 
@@ -62,7 +64,10 @@ __global__ void __launch_bounds__(256) gemm_simple_kernel(const GemmArgs g) {
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
             const int64_t n = n0 + tn * 4 + j;
-            if (n < g.N) g.C[m * g.ldc + n] = acc[i][j];
+            if (n >= g.N) continue;
+            float z = acc[i][j];
+            if (g.bias) z += g.bias[n];
+            g.C[m * g.ldc + n] = g.act ? gelu_tanh_f(z) : z;
         }
     }
 }

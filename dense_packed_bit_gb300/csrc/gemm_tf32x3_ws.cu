@@ -103,6 +103,8 @@ struct WsParams {
     float *sk_slots;        // [unit][rank][128][BN] fp32
     unsigned int *sk_flags; // [unit][rank], zeroed before the launch
     int c_tma;              // CTA pairs: C is stored through shared memory by TMA (tmC valid)
+    const float *bias;      // epilogue of C: + bias[column] (null: none), then GELU when act
+    int act;
 };
 
 // Work unit t: output tile t / ksplit, K slice t % ksplit (slabs [kt0, kt1)).
@@ -450,6 +452,9 @@ __global__ void __launch_bounds__(NTHREADS, 1)
 #pragma unroll 1
             for (int c0 = 0; c0 < BN; c0 += 32) {
                 float v[32];
+                // bias of this chunk's 32 columns, one per lane, loaded while TMEM is read
+                float bl = 0.0f;
+                if (SK == 0 && p.bias && !p.ws && n0 + c0 + lane < p.N) bl = __ldg(p.bias + n0 + c0 + lane);
                 tmem_ld32(base + (uint32_t)c0, v);
                 if (sk_part) {
                     // the whole 128 x BN partial tile, unmasked: the slot is private to this unit
@@ -470,6 +475,17 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                         v[4 * j + 3] += a.w;
                     }
                 }
+                // columns of this chunk inside the tile (the last chunk of a 240-wide tile has 16)
+                const int w = BN - c0 < 32 ? BN - c0 : 32;
+                if (SK == 0 && !p.ws) {  // bias and act are never set with split-K or stream-K
+                    if (p.act) {
+#pragma unroll
+                        for (int j = 0; j < 32; ++j) v[j] = gelu_tanh_f(v[j] + __shfl_sync(0xffffffffu, bl, j));
+                    } else if (p.bias) {
+#pragma unroll
+                        for (int j = 0; j < 32; ++j) v[j] += __shfl_sync(0xffffffffu, bl, j);
+                    }
+                }
                 if (CG == 2 && p.c_tma && !p.ws) {
                     // the warp's 32 x 32 block to its swizzled staging buffer (16-byte chunk k of
                     // row i at k ^ (i % 8), conflict-free), then one TMA store that clips at M, N
@@ -488,8 +504,6 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                     }
                     continue;
                 }
-                // columns of this chunk inside the tile (the last chunk of a 240-wide tile has 16)
-                const int w = BN - c0 < 32 ? BN - c0 : 32;
                 if (row < p.M && n0 + c0 < p.N) {
                     if (vec && w == 32 && n0 + c0 + 32 <= p.N) {
 #pragma unroll
@@ -615,7 +629,7 @@ cudaError_t launch_ws_cg(const GemmArgs &g, int sms, int ksplit, float *ws, cuda
     float *const sk_ws = ws;
     if (ksplit < 2) ws = nullptr;
     WsParams p{(int)g.M, (int)g.N, (int)g.K, tiles_m, tiles_m * tiles_n * (ws ? ksplit : 1), ws ? ksplit : 1,
-               g.C, g.ldc, ws, 0, 0, 0, nullptr, nullptr, 0};
+               g.C, g.ldc, ws, 0, 0, 0, nullptr, nullptr, 0, g.bias, g.act};
     // C through TMA stores (CTA pairs): 16-byte aligned C, ldc a multiple of 4
     CUtensorMap tc = ta;
     if (CG == 2 && (reinterpret_cast<uintptr_t>(g.C) & 15) == 0 && g.ldc % 4 == 0 &&

@@ -253,6 +253,38 @@ mm_status mm_gemm_f32_splitk(int transA, int transB, int64_t M, int64_t N, int64
     return ok();
 }
 
+mm_status mm_gemm_f32_bias_act(int transA, int transB, int64_t M, int64_t N, int64_t K, const float *A, int64_t lda,
+                               const float *B, int64_t ldb, const float *bias, int act, float *C, int64_t ldc,
+                               mm_stream_t stream) {
+    if ((transA != 0 && transA != 1) || (transB != 0 && transB != 1))
+        return fail(MM_ERR_INVALID_ARG, "transA/transB must be 0 or 1");
+    if (M < 1 || N < 1 || K < 1)
+        return fail(MM_ERR_INVALID_ARG, "M, N, K must be >= 1 (got %lld, %lld, %lld)", (long long)M, (long long)N,
+                    (long long)K);
+    if (!A || !B || !C) return fail(MM_ERR_INVALID_ARG, "NULL matrix pointer");
+    if (act != MM_ACT_NONE && act != MM_ACT_GELU_TANH) return fail(MM_ERR_INVALID_ARG, "unknown act %d", act);
+    const int64_t a_rows = transA ? K : M, a_cols = transA ? M : K;
+    const int64_t b_rows = transB ? N : K, b_cols = transB ? K : N;
+    if (lda < a_cols) return fail(MM_ERR_INVALID_ARG, "lda=%lld < %lld", (long long)lda, (long long)a_cols);
+    if (ldb < b_cols) return fail(MM_ERR_INVALID_ARG, "ldb=%lld < %lld", (long long)ldb, (long long)b_cols);
+    if (ldc < N) return fail(MM_ERR_INVALID_ARG, "ldc=%lld < N=%lld", (long long)ldc, (long long)N);
+    const uint64_t cb = span(M, N, ldc, 4);
+    if (overlap(C, cb, A, span(a_rows, a_cols, lda, 4)) || overlap(C, cb, B, span(b_rows, b_cols, ldb, 4)))
+        return fail(MM_ERR_INVALID_ARG, "C overlaps A or B");
+    if (bias && overlap(C, cb, bias, (uint64_t)N * 4)) return fail(MM_ERR_INVALID_ARG, "C overlaps bias");
+    mm_status s = check_device();
+    if (s != MM_OK) return s;
+    mm::GemmArgs g{transA, transB, M, N, K, A, lda, B, ldb, C, ldc};
+    g.bias = bias;
+    g.act = act;
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    // the warp-specialised 3xTF32 kernel when TMA can describe the operands, else the plain tiled one
+    cudaError_t e = mm::gemm_tf32x3_supported(g) ? mm::launch_gemm_tf32x3_ws(g, M > 128 ? 1 : 0, st)
+                                                 : mm::launch_gemm_simple(g, st);
+    if (e != cudaSuccess) return cuda_fail(e, "gemm launch");
+    return ok();
+}
+
 mm_status mm_gemm_f32_splitk_noalloc(int transA, int transB, int64_t M, int64_t N, int64_t K, const float *A,
                                      int64_t lda, const float *B, int64_t ldb, float *C, int64_t ldc, int splitk,
                                      mm_stream_t stream) {

@@ -112,7 +112,21 @@ struct GemmArgs {
     int64_t ldb;
     float *C;
     int64_t ldc;
+    // epilogue (the warp-specialised and the plain tiled kernels): C = act(op(A) op(B) + bias),
+    // bias one fp32 per column of C or null, act 0 = none, 1 = GELU (tanh form)
+    const float *bias = nullptr;
+    int act = 0;
 };
+
+// GELU in the tanh form GPT-2 uses: z/2 (1 + tanh(u)), u = sqrt(2/pi) (z + 0.044715 z^3).
+// Since (1 + tanh(u)) / 2 = 1 / (1 + e^(-2u)), it is z / (1 + e^(-2u)): one exponential and
+// one division, no branch, so that a thread's 32 outputs evaluate side by side.  Relative
+// error a few ulp where e^(-2u) is moderate; the exponent is capped at 80 so the divisor
+// stays below 2^126 (z e^-80 < 2e-35 |z| is the result's size beyond the cap).
+__device__ __forceinline__ float gelu_tanh_f(float z) {
+    const float u = 0.7978845608028654f * (z + 0.044715f * z * z * z);
+    return __fdividef(z, 1.0f + __expf(fminf(-2.0f * u, 80.0f)));
+}
 
 // Plain shared-memory tiled FFMA kernel: any sizes, strides and alignment.
 cudaError_t launch_gemm_simple(const GemmArgs &g, cudaStream_t s);

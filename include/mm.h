@@ -121,6 +121,24 @@ mm_status mm_gemm_packed2(const uint8_t *codes, const uint16_t *scales, const ui
 mm_status mm_check_device_error(mm_stream_t stream);
 
 /*
+ * GPT-2's linear layer with its MLP activation fused into the GEMM epilogue:
+ *     C = act(op(A) . op(B) + bias),   bias[n] added to column n of every row.
+ * bias: N fp32 values in device memory, or NULL for none.  act: MM_ACT_NONE or
+ * MM_ACT_GELU_TANH, gelu(z) = z/2 (1 + tanh(sqrt(2/pi) (z + 0.044715 z^3))) (the
+ * pages name GPT-2's step but print no activation; this is GPT-2's own).  Same
+ * layouts as mm_gemm_f32; |C - C_exact| <= 1.13e-5 (sum_k |a b| + |bias|) +
+ * 2^-20 (1 + |z|), z the exact pre-activation (1.13 bounds gelu's slope).  The
+ * 3xTF32 tensor-core kernel runs when A, B, C and their leading dimensions are
+ * 16-byte aligned, the general kernel otherwise.  Errors: as mm_gemm_f32, plus
+ * MM_ERR_INVALID_ARG for an unknown act or C overlapping bias.
+ */
+enum { MM_ACT_NONE = 0, MM_ACT_GELU_TANH = 1 };
+mm_status mm_gemm_f32_bias_act(int transA, int transB, int64_t M, int64_t N, int64_t K,
+                               const float *A, int64_t lda, const float *B, int64_t ldb,
+                               const float *bias, int act, float *C, int64_t ldc,
+                               mm_stream_t stream);
+
+/*
  * Split-K form of mm_gemm_f32 for products with fewer output tiles than the GPU
  * has SMs (short M and N, long K: the GPT-2 MLP shapes at small batch; or a
  * last partial wave, such as 2048^3 on CTA pairs).  splitk = 1..16: K is cut into

@@ -268,3 +268,17 @@ def test_gemv4_bad_options(lib, opt):
     st = lib.mm_gemv_packed4_ex(FAKE, FAKE + 0x100000, FAKE + 0x200000, FAKE + 0x300000, 64, cols,
                                 _cb16(*range(16)), None, ctypes.byref(o))
     assert st == mm.MM_ERR_INVALID_ARG, lib.mm_last_error()
+
+
+@pytest.mark.parametrize("case", [dict(act=2), dict(act=-1), dict(bias=FAKE + 0x40000 + 4 * 64 * 10),
+                                  dict(bias=FAKE + 0x40000 - 8), dict(C=None), dict(K=0), dict(tA=2),
+                                  dict(ldc=63)])
+def test_gemm_bias_act_argument_errors(lib, case):
+    # an unknown activation, a bias overlapping C, and the plain GEMM's own checks
+    a = dict(tA=0, M=64, N=64, K=256, A=FAKE, B=FAKE + 0x20000, C=FAKE + 0x40000, ldc=64,
+             bias=FAKE + 0x80000, act=1)
+    a.update(case)
+    st = lib.mm_gemm_f32_bias_act(a["tA"], 0, a["M"], a["N"], a["K"], a["A"], a["K"], a["B"], a["N"],
+                                  a["bias"], a["act"], a["C"], a["ldc"], None)
+    assert st == mm.MM_ERR_INVALID_ARG, lib.mm_last_error()
+    assert mm.MM_ACT_NONE == 0 and mm.MM_ACT_GELU_TANH == 1
