@@ -289,6 +289,9 @@ GEMV_CHAINED = dict(dequant=2, staging=1, rows_per_lane=1, pdl=1, weights_static
 GEMV_INDEP_STREAMS = 2  # independent calls alternate between two streams inside the graph
 GEMV4_INDEP = dict(staging=1, blocks=1, pdl=1, independent=1)
 GEMVT_INDEP = dict(pdl=1, independent=1)  # automatic decode and shape for 1536 x 12288
+# encoder layers run as a dependent chain: each product waits for the previous kernel before
+# reading X or writing Y; its weights are loaded and decoded before that wait
+TERN_OPTS = dict(pdl=1, weights_static=1)
 
 
 def capture_phases(w: Workload, stream):
@@ -358,7 +361,8 @@ def capture_phases(w: Workload, stream):
     def tern():
         for t in w.tern:
             c = t["case"]
-            mm.mm_gemm_packed2(t["codes"], t["scales"], t["X"], t["Y"], c.X.shape[0], c.rows, c.cols, c.codebook)
+            mm.mm_gemm_packed2_ex(t["codes"], t["scales"], t["X"], t["Y"], c.X.shape[0], c.rows, c.cols, c.codebook,
+                                  **TERN_OPTS)
 
     graphs = {}
     for name, fn in (("gemm", gemm), ("gemv", gemv(GEMV_INDEP, GEMV_INDEP_STREAMS)), ("gemv_c", gemv(GEMV_CHAINED)),
@@ -587,7 +591,7 @@ def main_mm(args):
         "vs_baseline": None, "dtype": "f32", "data": "synthetic",
         "config": {"workload": WORKLOAD, "gemm": "2048x2048x2048 fp32 NN+NT+TN, N(0,0.02)",
                    "gemv": "12288x1536 2-bit, 64-matrix rotation (288 MiB > L2), codebook {-2,-1,0,1}",
-                   "ternary": "16 layers, M=222, up 768->3072 and down 3072->768",
+                   "ternary": "16 layers, M=222, up 768->3072 and down 3072->768, a dependent chain with PDL",
                    "gemv_t": "1536x12288 2-bit, 64-matrix rotation (288 MiB > L2)",
                    "training_set": "8192x8192x2048 NN, dA=dC.B^T 8192x2048x8192, dB=A^T.dC 2048x8192x8192, N(0,0.02)",
                    "l2": "512 MiB buffer written before the GEMM phase of every step; GEMV inputs exceed L2",
@@ -607,7 +611,15 @@ def main_mm(args):
                               "frac": GEMV_TOTAL_BYTES / per_call_gemv_s / 1e9 / peaks["hbm_gbs"],
                               "weight_frac": GEMV_WEIGHT_BYTES / per_call_gemv_s / 1e9 / peaks["hbm_gbs"],
                               "traffic": traffic_for("gemv2_rows"), "peak_source": peaks_src}},
-        "ternary": {"value": tern_tflops, "unit": "TFLOP/s", "ms_per_block": tern_total_s / args.steps * 1e3},
+        "ternary": {"value": tern_tflops, "unit": "TFLOP/s", "ms_per_block": tern_total_s / args.steps * 1e3,
+                    "us_per_product": tern_total_s / args.steps / (2 * N_LAYERS) * 1e6,
+                    "kernel": "gemm_packed2_tcr_kernel (automatic token tile and cluster split)", "opts": TERN_OPTS,
+                    "roofline": {"bound": "tensor", "achieved": tern_tflops / world,
+                                 "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
+                                 "frac": tern_tflops / world / peaks["bf16_tflops"],
+                                 "peak_source": f"{peaks_src} bf16 burst (fp16 runs at the bf16 rate)",
+                                 "note": "1 GFLOP products: latency bound (MMA issue chain, stage hand-offs, "
+                                         "cluster reduction), not tensor-throughput bound"}},
         "gemv4": {"metric": "4-bit 12288x1536 GEMV weight GB/s (normal-quantile 16-entry codebook)",
                   "value": world * GEMV4_WEIGHT_BYTES / per_call_gemv4_s / 1e9, "unit": "GB/s",
                   "us_per_call": per_call_gemv4_s * 1e6,

@@ -51,7 +51,7 @@ class GemvOpts(ctypes.Structure):
 
 class GemmPacked2Opts(ctypes.Structure):
     _fields_ = [("tile", ctypes.c_int), ("splitk", ctypes.c_int), ("pdl", ctypes.c_int),
-                ("weights_static", ctypes.c_int), ("reserved", ctypes.c_int * 4)]
+                ("weights_static", ctypes.c_int), ("ntok", ctypes.c_int), ("reserved", ctypes.c_int * 3)]
 
 
 class Gemv4Opts(ctypes.Structure):
@@ -206,8 +206,8 @@ def mm_gemm_packed2(codes, scales, X, Y, M, rows, cols, codebook, stream=None):
 
 
 def mm_gemm_packed2_ex(codes, scales, X, Y, M, rows, cols, codebook, stream=None, *, tile=0, splitk=0, pdl=0,
-                       weights_static=0):
-    o = GemmPacked2Opts(tile, splitk, pdl, weights_static)
+                       weights_static=0, ntok=0):
+    o = GemmPacked2Opts(tile, splitk, pdl, weights_static, ntok)
     _check(load_library().mm_gemm_packed2_ex(_ptr(codes), _ptr(scales), _ptr(X), _ptr(Y), M, rows, cols,
                                              _codebook(codebook), _stream(stream), ctypes.byref(o)))
 

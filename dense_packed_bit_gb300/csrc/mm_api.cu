@@ -454,8 +454,11 @@ mm_status mm_gemm_packed2_ex(const uint8_t *codes, const uint16_t *scales, const
     const int tile = opts ? opts->tile : 0;
     const int splitk = opts ? opts->splitk : 0;
     const int pdl = opts ? opts->pdl : 0, weights_static = opts ? opts->weights_static : 0;
-    if (tile != 0 && tile != 1 && tile != 2 && tile != 32 && tile != 64 && tile != 128)
-        return fail(MM_ERR_INVALID_ARG, "tile must be 0 (auto), 1 (FFMA), 2, 32, 64 or 128 (tensor cores)");
+    const int ntok = opts ? opts->ntok : 0;
+    if (tile != 0 && tile != 1 && tile != 2 && tile != 3 && tile != 32 && tile != 64 && tile != 128)
+        return fail(MM_ERR_INVALID_ARG, "tile must be 0 (auto), 1 (FFMA), 2, 3, 32, 64 or 128 (tensor cores)");
+    if (ntok != 0 && (tile != 3 || ntok < 16 || ntok > 256 || ntok % 16 != 0))
+        return fail(MM_ERR_INVALID_ARG, "ntok (tokens per tile) is 0 or, with tile 3, a multiple of 16 in 16..256");
     if (splitk != 0 && splitk != 1 && splitk != 2 && splitk != 4 && splitk != 8 && !(splitk == 16 && tile == 2))
         return fail(MM_ERR_INVALID_ARG, "splitk must be 0 (auto), 1, 2, 4 or 8 (or 16 with tile 2)");
     if ((pdl != 0 && pdl != 1) || (weights_static != 0 && weights_static != 1) || (weights_static && !pdl))
@@ -468,6 +471,11 @@ mm_status mm_gemm_packed2_ex(const uint8_t *codes, const uint16_t *scales, const
     if (tile == 2 && !tcw_ok)
         return fail(MM_ERR_INVALID_ARG,
                     "tile 2 needs fp16-exact codebook entries, cols %% 64 == 0 and 16-byte aligned codes and X");
+    if (tile == 3 && !mm::gemm_packed2_tcr_supported(a))
+        return fail(MM_ERR_INVALID_ARG,
+                    "tile 3 needs fp16-exact codebook entries, cols %% 64 == 0 and 16-byte aligned codes and X");
+    if (tile == 3 && splitk > cols / 64)
+        return fail(MM_ERR_INVALID_ARG, "tile 3: splitk must not exceed the cols / 64 atoms");
     if (tile == 2 && splitk && !mm::gemm_packed2_tcw_fits(M, cols, splitk))
         return fail(MM_ERR_INVALID_ARG,
                     "tile 2: splitk must leave each CTA 1 to 8 of the cols / 64 atoms, within shared memory with X");
@@ -475,10 +483,13 @@ mm_status mm_gemm_packed2_ex(const uint8_t *codes, const uint16_t *scales, const
     if (s != MM_OK) return s;
     cudaError_t e;
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
-    // automatic: the pipelined kernel (tile 32 / 64 / 128) measured faster than tile 2 on the
-    // ternary encoder shapes, whose cluster reduction of 128 x 224 partial tiles costs more
-    // than the split saves
+    // automatic: tile 3 (decoded weights in tensor memory) measured fastest on the ternary
+    // encoder shapes (7.9 / 10.4 us per up / down product against 10.4 / 15.3 for the
+    // pipelined W-as-N kernel and 13.1 / 16.4 for tile 2); the W-as-N kernel covers the
+    // shapes tile 3 does not take (cols % 64 != 0, unaligned codes)
+    const bool tcr_auto = tile == 0 && mm::gemm_packed2_tcr_supported(a);
     if (tile == 2) e = mm::launch_gemm_packed2_tcw(a, splitk, pdl, weights_static, st);
+    else if (tile == 3 || tcr_auto) e = mm::launch_gemm_packed2_tcr(a, ntok, splitk, pdl, weights_static, st);
     else if (tc_ok && tile != 1) e = mm::launch_gemm_packed2_tc(a, tile, splitk, st);
     else e = mm::launch_gemm_packed2(a, 0, st);
     if (e != cudaSuccess) return cuda_fail(e, "packed gemm launch");
@@ -543,6 +554,9 @@ mm_status mm_check_device_error(mm_stream_t stream) {
     const unsigned int tw = mm::gemm_packed2_tcw_take_device_error(&e);
     if (e != cudaSuccess) return cuda_fail(e, "mm_check_device_error");
     if (tw != 0) return fail(MM_ERR_TIMEOUT, "a bounded device wait ran out in the tensor-core packed GEMM, tile 2 (code %u)", tw);
+    const unsigned int tr = mm::gemm_packed2_tcr_take_device_error(&e);
+    if (e != cudaSuccess) return cuda_fail(e, "mm_check_device_error");
+    if (tr != 0) return fail(MM_ERR_TIMEOUT, "a bounded device wait ran out in the tensor-core packed GEMM, tile 3 (code %u)", tr);
     const unsigned int q = mm::gemv_tma_take_device_error(&e);
     if (e != cudaSuccess) return cuda_fail(e, "mm_check_device_error");
     if (q != 0) return fail(MM_ERR_TIMEOUT, "a bounded device wait ran out in the staged GEMV (code %u)", q);

@@ -101,6 +101,17 @@ bool gemm_packed2_tcw_supported(const PackedArgs &a);
 cudaError_t launch_gemm_packed2_tcw(const PackedArgs &a, int splitk, int pdl, int weights_static, cudaStream_t s);
 unsigned int gemm_packed2_tcw_take_device_error(cudaError_t *err);
 
+// Tile 3: decoded weights in tensor memory as the MMA's A (128 features per CTA as
+// M), ntok tokens as N, a pipelined ring over K atoms, K split over a (1, 1, S)
+// cluster (S = 1, 2, 4, 8).  fp16-exact codebook, cols % 64 == 0, 16-byte aligned
+// codes and X.  ntok = 0 / splitk = 0: automatic (gemm_packed2_tcr_shape).
+bool gemm_packed2_tcr_supported(const PackedArgs &a);
+// capacity[i]: CTAs the GPU holds at once in clusters of 2^i
+void gemm_packed2_tcr_shape(int64_t M, int64_t rows, int64_t cols, const int capacity[4], int *ntok, int *splitk);
+cudaError_t launch_gemm_packed2_tcr(const PackedArgs &a, int ntok, int splitk, int pdl, int weights_static,
+                                    cudaStream_t s);
+unsigned int gemm_packed2_tcr_take_device_error(cudaError_t *err);
+
 // ------------------------------------------------------------------ dense GEMM
 
 struct GemmArgs {

@@ -291,25 +291,33 @@ mm_status mm_gemv_packed2_ex(const uint8_t *codes, const uint16_t *scales, const
                              mm_stream_t stream, const mm_gemv_opts *opts);
 
 typedef struct {
-    int tile;       /* 0 = automatic (tensor cores with W rows as the MMA's N when the
-                       codebook entries are exact in fp16, cols % 8 == 0 and X is 16-byte
-                       aligned, else FFMA), 1 = FFMA kernel,
+    int tile;       /* 0 = automatic (tile 3 when the codebook entries are exact in fp16,
+                       cols % 64 == 0 and codes and X are 16-byte aligned; else tensor
+                       cores with W rows as the MMA's N when the entries are exact in
+                       fp16, cols % 8 == 0 and X is 16-byte aligned; else FFMA),
+                       1 = FFMA kernel,
                        2 = tensor cores with 128 W rows per CTA as the MMA's M and up to
                        256 rows of X as its N, each CTA's share of K resident at once
                        (fp16-exact codebook, cols % 64 == 0, 16-byte aligned codes and
-                       X), 32 / 64 / 128 = tensor cores with that many W rows per CTA as
-                       the MMA's N, X rows as its M, a pipelined ring over K */
+                       X), 3 = tensor cores with 128 W rows per CTA decoded into tensor
+                       memory as the MMA's A, ntok rows of X as its N, a pipelined ring
+                       over K (same requirements as 2), 32 / 64 / 128 = tensor cores with
+                       that many W rows per CTA as the MMA's N, X rows as its M, a
+                       pipelined ring over K */
     int splitk;     /* tensor cores: CTAs of one thread-block cluster that split K and add
                        their partial tiles through distributed shared memory in rank
-                       order: 0 (auto), 1, 2, 4, 8; tile 2 also 16 */
-    int pdl;        /* tile 2: 1 = launch with
+                       order: 0 (auto), 1, 2, 4, 8; tile 2 also 16; tile 3 at most
+                       cols / 64 */
+    int pdl;        /* tiles 2 and 3 (and 0 when it picks 3): 1 = launch with
                        programmatic dependent launch; the kernel's prologue overlaps the
                        previous kernel, and it still waits for that kernel before reading
                        X or writing Y */
     int weights_static; /* 1 (needs pdl): promise that codes and scales are not written by
                        work queued before this call, so they may be loaded and decoded
                        before that wait */
-    int reserved[4];
+    int ntok;       /* tile 3: rows of X per CTA (the MMA's N), a multiple of 16 in
+                       16..256; 0 = automatic */
+    int reserved[3];
 } mm_gemm_packed2_opts;
 
 mm_status mm_gemm_packed2_ex(const uint8_t *codes, const uint16_t *scales, const uint16_t *X,

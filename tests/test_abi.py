@@ -188,7 +188,7 @@ def test_missing_library_fails_loudly(monkeypatch):
         mod.load_library()
 
 
-@pytest.mark.parametrize("tile", [-1, 3, 48, 256])
+@pytest.mark.parametrize("tile", [-1, 4, 48, 256])
 def test_gemm_packed_bad_tile(lib, tile):
     o = mm.GemmPacked2Opts(tile)
     st = lib.mm_gemm_packed2_ex(FAKE, FAKE + 0x100000, FAKE + 0x200000, FAKE + 0x300000, 4, 64, 64,
@@ -205,7 +205,10 @@ def test_gemm_packed_tensor_core_tile_needs_fp16_codebook(lib):
 
 @pytest.mark.parametrize("opt", [dict(tile=2, cols=100), dict(tile=2, splitk=16, cols=640),
                                  dict(tile=2, splitk=1, cols=1024), dict(pdl=2), dict(pdl=0, weights_static=1),
-                                 dict(tile=64, splitk=16)])
+                                 dict(tile=64, splitk=16), dict(tile=3, cols=100), dict(tile=3, splitk=16),
+                                 dict(tile=3, splitk=16, cols=64 * 8), dict(tile=3, ntok=8), dict(tile=3, ntok=272),
+                                 dict(tile=3, ntok=40), dict(tile=2, ntok=64), dict(ntok=64),
+                                 dict(tile=3, splitk=8, cols=64 * 4)])
 def test_gemm_packed_tile2_bad_options(lib, opt):
     # tile 2 needs cols % 64 == 0 and 1 to 8 atoms of 64 per CTA; weights_static needs pdl
     cols = opt.pop("cols", 640)

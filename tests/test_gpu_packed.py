@@ -350,8 +350,75 @@ def test_gemm_packed_tile2_deterministic():
     assert np.array_equal(y1.view(np.uint32), y2.view(np.uint32))
 
 
+# ------------------------------------------------------------------ tile 3: decoded weights in TMEM
+
+CB_ODD16 = np.array([0.375, -1.75, 2.5, 0.0078125], np.float32)  # four distinct fp16-exact entries
+
+
+@pytest.mark.parametrize("M,rows,cols", TILE2_SHAPES)
+@pytest.mark.parametrize("cb", ["ternary", "2bit", "odd16"])
+def test_gemm_packed_tile3_auto(oracle, M, rows, cols, cb):
+    # the automatic token tile and split; every code value decoded through prmt (odd16:
+    # four distinct entries, so a swapped field or a wrong byte of an entry shows)
+    codebook = {"ternary": CBT, "2bit": CB2, "odd16": CB_ODD16}[cb]
+    codes, scales, X = rand_case(rows, cols, M=M, seed=13 * M + rows + 7 * cols,
+                                 kind="ternary" if cb == "ternary" else "uniform2")
+    Y = gemm_packed(codes, scales, X, M, rows, cols, codebook, tile=3)
+    ref, T = oracle.packed_gemm(codes, scales, X, rows, cols, codebook)
+    check_bound(Y, ref, T, f"tile 3 {M}x{rows}x{cols} {cb}")
+
+
+@pytest.mark.parametrize("ntok", [16, 48, 64, 112, 224, 256])
+@pytest.mark.parametrize("splitk", [1, 2, 4, 8])
+@pytest.mark.parametrize("M,rows,cols", [(222, 300, 1024), (5, 17, 1600), (130, 129, 640)])
+def test_gemm_packed_tile3_token_tiles_and_splits(oracle, ntok, splitk, M, rows, cols):
+    # explicit token tiles (one, several, a ragged last one) and cluster sizes; 1600
+    # columns: 25 atoms, uneven shares; 640: 10 atoms, a ring shallower than 8 for 8 ranks
+    if splitk > cols // 64:
+        pytest.skip("more ranks than atoms")
+    codes, scales, X = rand_case(rows, cols, M=M, seed=ntok + 17 * splitk + M, kind="uniform2")
+    Y = gemm_packed(codes, scales, X, M, rows, cols, CB_ODD16, tile=3, splitk=splitk, ntok=ntok)
+    ref, T = oracle.packed_gemm(codes, scales, X, rows, cols, CB_ODD16)
+    check_bound(Y, ref, T, f"tile 3 ntok {ntok} splitk {splitk} {M}x{rows}x{cols}")
+
+
+@pytest.mark.parametrize("splitk", [1, 4])
+def test_gemm_packed_tile3_integer_exact(oracle, splitk):
+    # integer activations, scale 1, integer codebook: exact in any summation order
+    M, rows, cols = 150, 200, 512
+    codes, _, _ = rand_case(rows, cols, M=M, seed=6)
+    scales = np.full(rows, 0x3C00, np.uint16)
+    rng = np.random.default_rng(9)
+    X = rng.integers(-4, 5, size=(M, cols)).astype(np.float16).view(np.uint16)
+    Y = gemm_packed(codes, scales, X, M, rows, cols, CB2, tile=3, splitk=splitk)
+    ref, _ = oracle.packed_gemm(codes, scales, X, rows, cols, CB2)
+    check_exact(Y, ref, f"tile 3 splitk {splitk}")
+
+
+def test_gemm_packed_tile3_one_hot_decode_exact(oracle):
+    # X one-hot in K: Y[t][r] = scale_r cb[field(r, k_t)] exactly, every field of every
+    # row position of the atom, all four codes, through every lane of the tensor memory
+    M, rows, cols = 64, 256, 64
+    codes, scales, _ = rand_case(rows, cols, M=1, seed=77)
+    X = np.zeros((M, cols), np.float16)
+    X[np.arange(M), np.arange(M) % cols] = 1.0
+    X = X.view(np.uint16)
+    Y = gemm_packed(codes, scales, X, M, rows, cols, CB_ODD16, tile=3, ntok=64)
+    ref, _ = oracle.packed_gemm(codes, scales, X, rows, cols, CB_ODD16)
+    check_exact(Y, ref.astype(np.float32).astype(np.float64), "tile 3 one-hot")
+
+
+def test_gemm_packed_tile3_deterministic():
+    c = synth.ternary_encoder_layer(5, "down")
+    M = c.X.shape[0]
+    y1 = gemm_packed(c.codes, c.scales, c.X, M, c.rows, c.cols, c.codebook, tile=3)
+    y2 = gemm_packed(c.codes, c.scales, c.X, M, c.rows, c.cols, c.codebook, tile=3)
+    assert np.array_equal(y1.view(np.uint32), y2.view(np.uint32))
+
+
+@pytest.mark.parametrize("tile", [2, 3])
 @pytest.mark.parametrize("weights_static", [0, 1])
-def test_gemm_packed_tile2_pdl_waits_before_writing_and_reading(oracle, weights_static):
+def test_gemm_packed_tile2_pdl_waits_before_writing_and_reading(oracle, weights_static, tile):
     # Back-to-back calls with programmatic dependent launch on one stream.
     # Call 2 writes its Y over the bytes of call 1's X (write after read), and call 3
     # reads as X the bytes call 2 wrote (read after write).  Integer activations, an
@@ -377,7 +444,7 @@ def test_gemm_packed_tile2_pdl_waits_before_writing_and_reading(oracle, weights_
     dX2 = to_dev(X2)
     dY1 = empty_f32((M, rows))
     dY3 = empty_f32((M, rows))
-    opts = dict(tile=2, pdl=1, weights_static=weights_static)
+    opts = dict(tile=tile, pdl=1, weights_static=weights_static)
     for _ in range(3):
         buf[: X1.nbytes].copy_(torch.from_numpy(X1.view(np.uint8).reshape(-1)))
         mm.mm_gemm_packed2_ex(dc[0], ds, dX1, dY1, M, rows, cols, cb, **opts)
