@@ -618,6 +618,8 @@ def main_mm(args):
                                  "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
                                  "frac": tern_tflops / world / peaks["bf16_tflops"],
                                  "peak_source": f"{peaks_src} bf16 burst (fp16 runs at the bf16 rate)",
+                                 "traffic": {"up": traffic_for("gemm_packed2_tcr_up"),
+                                             "down": traffic_for("gemm_packed2_tcr_down")},
                                  "note": "1 GFLOP products: latency bound (MMA issue chain, stage hand-offs, "
                                          "cluster reduction), not tensor-throughput bound"}},
         "gemv4": {"metric": "4-bit 12288x1536 GEMV weight GB/s (normal-quantile 16-entry codebook)",

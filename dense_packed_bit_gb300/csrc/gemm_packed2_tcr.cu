@@ -22,7 +22,8 @@
 //     stage's 32 TMEM columns: the thread of TMEM lane f owns weight row f, the
 //     two warps of a lane quarter take one half of the atom each, and column c
 //     of a stage holds the fp16 pair of K positions 2c (low half) and 2c + 1.
-//     The store of one atom completes while the next one is decoded;
+//     Two atoms' stores are waited for at once, and the next atom is decoded
+//     while they complete;
 //   * one thread issues the atom's 4 MMAs (K = 16), A from TMEM and B from
 //     shared memory, and commits them to the barrier that frees the stage.
 // Only X passes through shared memory; the decoded weights go straight from
@@ -289,11 +290,14 @@ __global__ void __launch_bounds__(NTHREADS, 1)
 #pragma unroll
         for (int u = 0; u < PREF; ++u) pre[u] = load_codes(u);
         if (h == 0) sscale[f] = real ? h2f(p.scales[f0 + f]) : 0.f;
-        uint32_t rb[2][16];  // decoded atoms, alternating: one is stored while the next is decoded
+        // decoded atoms in four register buffers: two atoms' TMEM stores are in flight per wait,
+        // and the next atom is decoded while they complete
+        uint32_t rb[4][16];
         decode_word(pre[0].x, p.lo4, p.hi4, rb[0]);
         decode_word(pre[0].y, p.lo4, p.hi4, rb[0] + 8);
         pre[0] = load_codes(PREF);
         bool bad = false;
+        int s_prev = 0;  // stage of the stored atom not yet announced
         for (int i0 = 0; i0 < kc && !bad; i0 += PREF) {
 #pragma unroll
             for (int u = 0; u < PREF; ++u) {
@@ -307,17 +311,25 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                     break;
                 }
                 tc_fence_after_sync();
-                tmem_st16(tmem + lane_addr + (uint32_t)(ACC_COLS + 32 * s + 16 * h), rb[u & 1]);
+                tmem_st16(tmem + lane_addr + (uint32_t)(ACC_COLS + 32 * s + 16 * h), rb[u]);
                 if (i + 1 < kc) {
+                    // buffer (u + 1) % 4 was last stored two atoms ago, before the previous wait
                     const uint2 c = pre[(u + 1) % PREF];
-                    decode_word(c.x, p.lo4, p.hi4, rb[(u + 1) & 1]);
-                    decode_word(c.y, p.lo4, p.hi4, rb[(u + 1) & 1] + 8);
+                    decode_word(c.x, p.lo4, p.hi4, rb[(u + 1) % 4]);
+                    decode_word(c.y, p.lo4, p.hi4, rb[(u + 1) % 4] + 8);
                     pre[(u + 1) % PREF] = load_codes(i + 1 + PREF);
                 }
-                tmem_wait_st();
-                tc_fence_before_sync();
-                __syncwarp();
-                if (lane == 0) mbar_arrive(&afull[s]);
+                if ((u & 1) || i == kc - 1) {
+                    tmem_wait_st();
+                    tc_fence_before_sync();
+                    __syncwarp();
+                    if (lane == 0) {
+                        if (u & 1) mbar_arrive(&afull[s_prev]);
+                        mbar_arrive(&afull[s]);
+                    }
+                } else {
+                    s_prev = s;
+                }
             }
         }
         bar_sync(1, NDEC);  // the scales are in shared memory
