@@ -222,14 +222,21 @@ class Workload:
             self.gemm.append(dict(case=c, A=torch.from_numpy(A).to(device), B=torch.from_numpy(B).to(device),
                                   C=torch.empty((c.M, c.N), dtype=torch.float32, device=device),
                                   hA=A, hB=B))
+        # the rotation as one contiguous [64, 12288, 384] buffer: the per-call phases take views,
+        # the batched phase the whole buffer
+        self.gemv_codes_all = torch.empty((N_GEMV, 12288, 384), dtype=torch.uint8, device=device)
+        self.gemv_scales_all = torch.empty((N_GEMV, 12288), dtype=torch.int16, device=device)
         self.gemv_codes, self.gemv_scales = [], []
         x = None
         for i in range(N_GEMV):
             c = synth.gemv_2bit_12288x1536(i + (off % 1000) * N_GEMV if off else i)
-            self.gemv_codes.append(torch.from_numpy(c.codes).to(device))
-            self.gemv_scales.append(torch.from_numpy(c.scales).to(device))
+            self.gemv_codes_all[i].copy_(torch.from_numpy(c.codes))
+            self.gemv_scales_all[i].copy_(torch.from_numpy(c.scales.view("int16")))
+            self.gemv_codes.append(self.gemv_codes_all[i])
+            self.gemv_scales.append(self.gemv_scales_all[i])
             x = c.X
             self.gemv_cb = c.codebook
+        self.gemv_yb = torch.empty((N_GEMV, 12288), dtype=torch.float32, device=device)
         self.gemv_x = torch.from_numpy(x.reshape(-1)).to(device)
         self.gemv_y = torch.empty((N_GEMV, 12288), dtype=torch.float32, device=device)
         self.gemv4_codes, self.gemv4_scales = [], []
@@ -331,6 +338,10 @@ def capture_phases(w: Workload, stream):
                 cur.wait_stream(side)
         return f
 
+    def gemv_batched():
+        mm.mm_gemv_packed2_strided_batched(w.gemv_codes_all, 12288 * 384, w.gemv_scales_all, 12288, w.gemv_x, 0,
+                                           w.gemv_yb, 12288, N_GEMV, 12288, 1536, w.gemv_cb)
+
     def gemv4():
         cur = torch.cuda.current_stream()
         side.wait_stream(cur)
@@ -366,7 +377,8 @@ def capture_phases(w: Workload, stream):
 
     graphs = {}
     for name, fn in (("gemm", gemm), ("gemv", gemv(GEMV_INDEP, GEMV_INDEP_STREAMS)), ("gemv_c", gemv(GEMV_CHAINED)),
-                     ("tern", tern), ("gemv4", gemv4), ("gemvt", gemvt), ("train", train), ("mlp", mlp)):
+                     ("tern", tern), ("gemv4", gemv4), ("gemvt", gemvt), ("train", train), ("mlp", mlp),
+                     ("gemv_b", gemv_batched)):
         with torch.cuda.stream(stream):
             fn()  # warm the kernels' one-time setup outside capture
         torch.cuda.synchronize()
@@ -377,10 +389,10 @@ def capture_phases(w: Workload, stream):
     return graphs
 
 
-LAUNCHES_PER_STEP = 3 + 4 * N_GEMV + 2 * N_LAYERS + 3 + 1  # + the training set's 3 GEMMs + the MLP GEMM
+LAUNCHES_PER_STEP = 3 + 4 * N_GEMV + 2 * N_LAYERS + 3 + 1 + 1  # + training set, MLP GEMM, batched GEMV
 
 
-PHASES = ("gemm", "gemv", "gemv_c", "tern", "gemv4", "gemvt", "train", "mlp")
+PHASES = ("gemm", "gemv", "gemv_c", "tern", "gemv4", "gemvt", "train", "mlp", "gemv_b")
 
 
 def run_step(w: Workload, graphs, ev, stream):
@@ -551,6 +563,8 @@ def main_mm(args):
     gemvt_total_s = total_s("gemvt")
     train_total_s = total_s("train")
     mlp_total_s = total_s("mlp")
+    gemvb_total_s = total_s("gemv_b")
+    per_mat_gemvb_s = gemvb_total_s / (args.steps * N_GEMV)
     wall = reduce_max(wall, dev)
 
     gemm_tflops = world * 3 * GEMM_FLOP * args.steps / gemm_total_s / 1e12
@@ -561,7 +575,7 @@ def main_mm(args):
     per_call_gemv4_s = gemv4_total_s / (args.steps * N_GEMV)
     per_call_gemvt_s = gemvt_total_s / (args.steps * N_GEMV)
     step_ms = (gemm_total_s + gemv_total_s + gemvc_total_s + tern_total_s + gemv4_total_s + gemvt_total_s +
-               train_total_s + mlp_total_s) / args.steps * 1e3
+               train_total_s + mlp_total_s + gemvb_total_s) / args.steps * 1e3
 
     peaks, peaks_src = measured_peaks()
     props = torch.cuda.get_device_properties(dev)
@@ -610,7 +624,16 @@ def main_mm(args):
                               "peak": peaks["hbm_gbs"], "unit": "GB/s",
                               "frac": GEMV_TOTAL_BYTES / per_call_gemv_s / 1e9 / peaks["hbm_gbs"],
                               "weight_frac": GEMV_WEIGHT_BYTES / per_call_gemv_s / 1e9 / peaks["hbm_gbs"],
-                              "traffic": traffic_for("gemv2_rows"), "peak_source": peaks_src}},
+                              "traffic": traffic_for("gemv2_rows"), "peak_source": peaks_src},
+                 "batched": {"value": world * GEMV_WEIGHT_BYTES / per_mat_gemvb_s / 1e9, "unit": "GB/s",
+                             "us_per_matrix": per_mat_gemvb_s * 1e6,
+                             "mode": "the 64-matrix rotation (288 MiB) as one mm_gemv_packed2_strided_batched "
+                                     "launch per step, one shared x",
+                             "roofline": {"bound": "hbm", "achieved": GEMV_TOTAL_BYTES / per_mat_gemvb_s / 1e9,
+                                          "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                                          "frac": GEMV_TOTAL_BYTES / per_mat_gemvb_s / 1e9 / peaks["hbm_gbs"],
+                                          "weight_frac": GEMV_WEIGHT_BYTES / per_mat_gemvb_s / 1e9 / peaks["hbm_gbs"],
+                                          "traffic": None, "peak_source": peaks_src}}},
         "ternary": {"value": tern_tflops, "unit": "TFLOP/s", "ms_per_block": tern_total_s / args.steps * 1e3,
                     "us_per_product": tern_total_s / args.steps / (2 * N_LAYERS) * 1e6,
                     "kernel": "gemm_packed2_tcr_kernel (automatic token tile and cluster split)", "opts": TERN_OPTS,

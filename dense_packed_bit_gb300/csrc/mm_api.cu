@@ -446,6 +446,45 @@ mm_status mm_gemv_packed2(const uint8_t *codes, const uint16_t *scales, const ui
     return mm_gemv_packed2_ex(codes, scales, x, y, rows, cols, codebook, stream, nullptr);
 }
 
+mm_status mm_gemv_packed2_strided_batched(const uint8_t *codes, int64_t codes_stride, const uint16_t *scales,
+                                          int64_t scales_stride, const uint16_t *x, int64_t x_stride, float *y,
+                                          int64_t y_stride, int64_t batch, int64_t rows, int64_t cols,
+                                          const float codebook[4], mm_stream_t stream) {
+    if (batch < 1) return fail(MM_ERR_INVALID_ARG, "batch must be >= 1 (got %lld)", (long long)batch);
+    mm_status s = check_packed(codes, scales, x, y, 1, rows, cols, codebook);
+    if (s != MM_OK) return s;
+    const int64_t rowbytes = (cols + 3) / 4;
+    if (batch > 1 && (codes_stride < rows * rowbytes || scales_stride < rows || y_stride < rows ||
+                      (x_stride != 0 && x_stride < cols)))
+        return fail(MM_ERR_INVALID_ARG, "strides must cover one matrix (codes_stride >= rows * ceil(cols/4) bytes, "
+                                        "scales_stride >= rows, y_stride >= rows, x_stride 0 or >= cols)");
+    if (codes_stride < 0 || scales_stride < 0 || x_stride < 0 || y_stride < 0)
+        return fail(MM_ERR_INVALID_ARG, "strides must be >= 0");
+    const int64_t nb = batch - 1;
+    const uint64_t ybytes = (uint64_t)(nb * y_stride + rows) * 4;
+    if (overlap(y, ybytes, codes, (uint64_t)(nb * codes_stride + rows * rowbytes)) ||
+        overlap(y, ybytes, scales, (uint64_t)(nb * scales_stride + rows) * 2) ||
+        overlap(y, ybytes, x, (uint64_t)(nb * x_stride + cols) * 2))
+        return fail(MM_ERR_INVALID_ARG, "an output overlaps an input");
+    s = check_device();
+    if (s != MM_OK) return s;
+    mm::PackedBatch p{codes, codes_stride, scales, scales_stride, x, x_stride, y, y_stride, batch, rows, cols,
+                      {codebook[0], codebook[1], codebook[2], codebook[3]}};
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    if (mm::gemv_batched_supported(p)) {
+        const cudaError_t e = mm::launch_gemv_batched(p, st);
+        if (e != cudaSuccess) return cuda_fail(e, "batched gemv launch");
+        return ok();
+    }
+    // shapes the one-launch kernel does not take: one call per matrix
+    for (int64_t b = 0; b < batch; ++b) {
+        s = mm_gemv_packed2_ex(codes + b * codes_stride, scales + b * scales_stride, x + b * x_stride,
+                               y + b * y_stride, rows, cols, codebook, stream, nullptr);
+        if (s != MM_OK) return s;
+    }
+    return ok();
+}
+
 mm_status mm_gemm_packed2_ex(const uint8_t *codes, const uint16_t *scales, const uint16_t *X, float *Y, int64_t M,
                              int64_t rows, int64_t cols, const float codebook[4], mm_stream_t stream,
                              const mm_gemm_packed2_opts *opts) {

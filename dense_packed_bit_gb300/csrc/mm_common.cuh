@@ -175,6 +175,15 @@ __device__ __forceinline__ void tma_load_2d(void *smem_dst, const void *tmap, ui
         : "memory");
 }
 
+// 3-D form of tma_load_2d (c2: the outermost coordinate, e.g. the matrix of a batch).
+__device__ __forceinline__ void tma_load_3d(void *smem_dst, const void *tmap, uint64_t *bar, int c0, int c1, int c2) {
+    asm volatile(
+        "cp.async.bulk.tensor.3d.shared::cta.global.tile.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%3, %4, %5}], [%2];" ::"r"(smem_u32(smem_dst)),
+        "l"(tmap), "r"(smem_u32(bar)), "r"(c0), "r"(c1), "r"(c2)
+        : "memory");
+}
+
 // 2-D tiled bulk tensor store from this CTA's shared memory (the box in the tensor map's
 // layout and swizzle) to global memory; parts of the box outside the tensor are not
 // written.  Completion is tracked by the issuing thread's bulk async-groups.

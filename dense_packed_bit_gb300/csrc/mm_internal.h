@@ -55,6 +55,26 @@ unsigned int gemv4_take_device_error(cudaError_t *err);
 // True when cb[c] == cb[0] + c * (cb[1] - cb[0]) holds exactly in fp32 for c = 0..3.
 bool codebook_is_affine(const float cb[4]);
 
+// A strided batch of 2-bit GEMVs: matrix b's codes at codes + b codes_stride (bytes), its
+// scales, x and y at b times the matching stride in entries (x_stride 0: one x for all).
+struct PackedBatch {
+    const uint8_t *codes;
+    int64_t codes_stride;
+    const uint16_t *scales;
+    int64_t scales_stride;
+    const uint16_t *x;
+    int64_t x_stride;
+    float *y;
+    int64_t y_stride;
+    int64_t batch, rows, cols;
+    float cb[4];
+};
+// One launch over the whole batch (staged SIMT affine decode): cols % 512 == 0,
+// cols <= 4096, 16-byte aligned codes (and codes_stride) and x (x_stride % 8 == 0),
+// an affine codebook.
+bool gemv_batched_supported(const PackedBatch &p);
+cudaError_t launch_gemv_batched(const PackedBatch &p, cudaStream_t s);
+
 // Vectorised path needs cols % 64 == 0, 16-byte aligned codes and x pointers
 // and cols small enough for x to sit in shared memory.
 bool gemv_vec_supported(const PackedArgs &a);

@@ -325,6 +325,26 @@ mm_status mm_gemm_packed2_ex(const uint8_t *codes, const uint16_t *scales, const
                              const float codebook[4], mm_stream_t stream,
                              const mm_gemm_packed2_opts *opts);
 
+/*
+ * A strided batch of 2-bit GEMVs, y_b = mm_gemv_packed2(W_b, x_b) for b < batch:
+ * matrix b's codes at codes + b * codes_stride (bytes), its scales at scales +
+ * b * scales_stride, its x at x + b * x_stride (x_stride 0: one x for every matrix)
+ * and its y at y + b * y_stride (entries).  With an affine codebook, cols % 512 ==
+ * 0, cols <= 4096, 16-byte aligned codes and x, codes_stride % 16 == 0 and
+ * x_stride % 8 == 0 the whole batch runs in one launch (a persistent grid streaming
+ * 128-row blocks of every matrix), and each y_b equals bit for bit the staged
+ * single call's; other shapes run one call per matrix.  Same tolerance as
+ * mm_gemv_packed2.  Errors: as mm_gemv_packed2, plus MM_ERR_INVALID_ARG for batch
+ * < 1, a negative stride, strides that do not cover one matrix (batch > 1), or any
+ * y overlapping any input.
+ */
+mm_status mm_gemv_packed2_strided_batched(const uint8_t *codes, int64_t codes_stride,
+                                          const uint16_t *scales, int64_t scales_stride,
+                                          const uint16_t *x, int64_t x_stride, float *y,
+                                          int64_t y_stride, int64_t batch, int64_t rows,
+                                          int64_t cols, const float codebook[4],
+                                          mm_stream_t stream);
+
 /* ------------------------------------------------------------------ 4-bit GEMV */
 
 /* y[r] = scale_r * sum_k codebook[field4(r, k)] * x[k], r < rows, k < cols.

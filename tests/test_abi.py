@@ -285,3 +285,17 @@ def test_gemm_bias_act_argument_errors(lib, case):
                                   a["bias"], a["act"], a["C"], a["ldc"], None)
     assert st == mm.MM_ERR_INVALID_ARG, lib.mm_last_error()
     assert mm.MM_ACT_NONE == 0 and mm.MM_ACT_GELU_TANH == 1
+
+
+@pytest.mark.parametrize("case", [dict(batch=0), dict(codes_stride=100), dict(scales_stride=10), dict(y_stride=10),
+                                  dict(x_stride=5), dict(x_stride=-64), dict(y=FAKE + 0x400),
+                                  dict(y=FAKE + 0x200000 + 16), dict(codes=None)])
+def test_gemv_batched_argument_errors(lib, case):
+    # batch >= 1; strides cover one matrix (or are 0 for a shared x); no y over any input
+    a = dict(codes=FAKE, codes_stride=64 * 16, scales=FAKE + 0x100000, scales_stride=64, x=FAKE + 0x200000,
+             x_stride=64, y=FAKE + 0x300000, y_stride=64, batch=3, rows=64, cols=64)
+    a.update(case)
+    st = lib.mm_gemv_packed2_strided_batched(a["codes"], a["codes_stride"], a["scales"], a["scales_stride"], a["x"],
+                                             a["x_stride"], a["y"], a["y_stride"], a["batch"], a["rows"], a["cols"],
+                                             _cb(-2, -1, 0, 1), None)
+    assert st == mm.MM_ERR_INVALID_ARG, lib.mm_last_error()

@@ -1,0 +1,86 @@
+"""GPU parity of the strided batch of 2-bit GEMVs (one launch for the whole batch).
+
+Every output of every matrix against the oracle, and bit for bit against one
+staged call per matrix (the batched kernel runs the same arithmetic in the same
+order); shared and per-matrix x, padded strides, ragged row blocks, CTAs that
+span many small matrices, and the per-matrix fallback for shapes the one-launch
+kernel does not take.
+"""
+import numpy as np
+import pytest
+
+import dense_packed_bit_gb300 as mm
+from dense_packed_bit_gb300 import synth
+from gpu_util import check_bound, empty_f32, to_dev, to_host
+
+pytestmark = pytest.mark.gpu
+
+CB2 = synth.CODEBOOK_2BIT
+CB_ODD = np.array([0.3, -1.7, 2.5, 0.01], np.float32)
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    from dense_packed_bit_gb300 import build
+    build.build()
+    mm.load_library()
+
+
+def make_batch(batch, rows, cols, seed, shared_x, pad_rows=0):
+    rb = (cols + 3) // 4
+    codes = synth.random_bytes(seed, batch * (rows + pad_rows) * rb).reshape(batch, rows + pad_rows, rb)
+    scales = synth.uniform_f16_bits(seed + 1, (batch, rows + pad_rows), 0.005, 0.05)
+    nx = 1 if shared_x else batch
+    x = synth.normal_f16_bits(seed + 2, (nx, cols))
+    return codes, scales, x
+
+
+def run_batched(codes, scales, x, rows, cols, cb, shared_x):
+    batch, rtot, rb = codes.shape
+    dc, ds, dx = to_dev(codes), to_dev(scales), to_dev(x)
+    dy = empty_f32((batch, rtot))
+    mm.mm_gemv_packed2_strided_batched(dc, rtot * rb, ds, rtot, dx, 0 if shared_x else cols, dy, rtot, batch, rows,
+                                       cols, cb)
+    mm.mm_check_device_error()
+    return to_host(dy)
+
+
+@pytest.mark.parametrize("shared_x", [True, False])
+@pytest.mark.parametrize("batch,rows,cols,pad", [(8, 12288, 1536, 0), (3, 1000, 512, 24), (1, 129, 4096, 0),
+                                                 (200, 65, 1024, 0), (37, 300, 2048, 4)])
+def test_batched_gemv_parity_and_bitwise_equal_to_single_calls(oracle, batch, rows, cols, pad, shared_x):
+    codes, scales, x = make_batch(batch, rows, cols, seed=batch + rows + cols, shared_x=shared_x, pad_rows=pad)
+    y = run_batched(codes, scales, x, rows, cols, CB2, shared_x)
+    for b in range(batch):
+        xb = x[0 if shared_x else b]
+        ref, T = oracle.packed_gemm(codes[b, :rows], scales[b, :rows], xb.reshape(1, cols), rows, cols, CB2)
+        check_bound(y[b, :rows], ref[0], T[0], f"matrix {b}")
+        assert np.all(np.isnan(y[b, rows:])), "write into the padding rows of y"
+    # the same arithmetic as one staged call per matrix
+    for b in sorted({0, batch // 2, batch - 1}):
+        dc, ds = to_dev(np.ascontiguousarray(codes[b, :rows])), to_dev(np.ascontiguousarray(scales[b, :rows]))
+        dx = to_dev(np.ascontiguousarray(x[0 if shared_x else b]))
+        dy = empty_f32((rows,))
+        mm.mm_gemv_packed2_ex(dc, ds, dx, dy, rows, cols, CB2, dequant=2, staging=1)
+        assert np.array_equal(to_host(dy).view(np.uint32), y[b, :rows].view(np.uint32)), f"matrix {b} not bitwise equal"
+
+
+@pytest.mark.parametrize("cb,cols", [("odd", 1536), ("2bit", 1000), ("2bit", 8192)])
+def test_batched_gemv_fallback_shapes(oracle, cb, cols):
+    # a non-affine codebook, cols not a multiple of 512, cols above 4096: one call per matrix
+    codebook = CB_ODD if cb == "odd" else CB2
+    batch, rows = 4, 333
+    codes, scales, x = make_batch(batch, rows, cols, seed=cols, shared_x=False)
+    y = run_batched(codes, scales, x, rows, cols, codebook, False)
+    for b in range(batch):
+        ref, T = oracle.packed_gemm(codes[b], scales[b], x[b].reshape(1, cols), rows, cols, codebook)
+        check_bound(y[b], ref[0], T[0], f"{cb} {cols} matrix {b}")
+
+
+def test_batched_gemv_zero_entry_rows_exact(oracle):
+    # rows whose fields all hold the zero entry (code 2 of {-2,-1,0,1}) give exactly 0
+    batch, rows, cols = 5, 256, 1536
+    codes, scales, x = make_batch(batch, rows, cols, seed=3, shared_x=True)
+    codes[:, ::7, :] = 0xAA  # every field = 2
+    y = run_batched(codes, scales, x, rows, cols, CB2, True)
+    assert np.all(y[:, ::7] == 0.0)
