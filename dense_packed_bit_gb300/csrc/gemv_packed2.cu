@@ -13,9 +13,10 @@
 //    in flight at once across the 152 SMs; S consecutive lanes read one row's
 //    consecutive 16-byte chunks, so one warp instruction covers full 128-byte
 //    lines of 32/S rows.
-//  * x (fp16) is staged once per CTA in shared memory as fp32 in a layout
-//    XOR-swizzled by chunk, so the S lanes of a row group read S different
-//    chunks without bank conflicts.
+//  * x (fp16) is staged once per CTA in shared memory (fp32 for the select
+//    decode, fp16 as it is for the affine one) in a layout XOR-swizzled by
+//    chunk, so the S lanes of a row group read S different chunks without
+//    bank conflicts.
 //  * split-K partial sums reduced with __shfl_xor_sync in a fixed order (no
 //    atomics): a given variant is bit-reproducible run to run.
 //  * the per-row fp16 scale is applied once to the fp32 sum.
@@ -24,19 +25,15 @@
 //  * select: field -> codebook entry by two predicated selects, fp32 FMA.
 //    Any codebook.
 //  * affine: when codebook[c] == c0 + c*d exactly, sum_k cb[c_k] x_k is
-//    evaluated as c0 * sum_k x_k + d * sum_k c_k x_k.  The field c sitting at
-//    bit p of a 32-bit code word is used in place: the word masked to those two
-//    bits, read as an fp32 bit pattern, is the exact value c * 2^(p-149) (a
-//    subnormal, or for p = 22 and c >= 2 the smallest normals, where the bit
-//    pattern is still linear in c).  Multiplying by x_k * 2^(111-p), prepared
-//    once per CTA, gives c_k * x_k * 2^-38 exactly, with no shift, convert or
-//    select per field.  Fields at bits 24..30 are first moved down by one shift
-//    of the word.  Pairs of fields go through the packed f32x2 FMA.  Decoding
-//    stays exact: one-hot x returns scale_r * cb[field] bit for bit.
-//    sum_k x_k is accumulated by every lane with the same pairs, order and
-//    shuffle tree as sum_k c_k x_k (constant field-1 operands, no integer
-//    work), so when every field of a row is the codebook's zero entry c_z in
-//    {0, 1, 2}, d * sum c x is exactly -c0 * sum x and the row returns 0.
+//    evaluated as c0 * sum_k x_k + d * sum_k c_k x_k, the fields used in place
+//    as fp16 subnormals against fp16 x with the mixed-precision FMA, one LOP3
+//    per two fields (gemv_mixed.cuh; exact products).  Decoding stays exact:
+//    one-hot x returns scale_r * cb[field] bit for bit.  sum_k x_k is
+//    accumulated by every lane with the same FMAs (every field 1), classes,
+//    order and shuffle tree as sum_k c_k x_k, so when every field of a row is
+//    the codebook's zero entry c_z in {0, 1, 2}, d * sum c x is exactly
+//    -c0 * sum x and the row returns 0.
+#include "gemv_mixed.cuh"
 #include "mm_common.cuh"
 #include "mm_internal.h"
 
@@ -53,41 +50,8 @@ __device__ __forceinline__ float h2f(uint16_t h) { return __half2float(__ushort_
 // 64 fields is 16 float4s; its slots are XOR-permuted by (chunk & 7).
 __device__ __forceinline__ int xs_slot(int f) { return f ^ ((f >> 4) & 7); }
 
-// exact power of two 2^e for -126 <= e <= 127
-__device__ __forceinline__ float pow2f(int e) { return __int_as_float((127 + e) << 23); }
-
-__device__ __forceinline__ float2 field_pair(uint32_t w, uint32_t m0, uint32_t m1) {
-    return make_float2(__uint_as_float(w & m0), __uint_as_float(w & m1));
-}
-
-// 16 fields of one code word against 16 prepared x values (affine decode).
-__device__ __forceinline__ float2 affine_word(uint32_t w, const float4 &x0, const float4 &x1, const float4 &x2,
-                                              const float4 &x3, float2 acc) {
-    acc = ffma2(field_pair(w, 0x3u, 0xCu), make_float2(x0.x, x0.y), acc);
-    acc = ffma2(field_pair(w, 0x30u, 0xC0u), make_float2(x0.z, x0.w), acc);
-    acc = ffma2(field_pair(w, 0x300u, 0xC00u), make_float2(x1.x, x1.y), acc);
-    acc = ffma2(field_pair(w, 0x3000u, 0xC000u), make_float2(x1.z, x1.w), acc);
-    acc = ffma2(field_pair(w, 0x30000u, 0xC0000u), make_float2(x2.x, x2.y), acc);
-    acc = ffma2(field_pair(w, 0x300000u, 0xC00000u), make_float2(x2.z, x2.w), acc);
-    const uint32_t h = w >> 16;  // fields 12..15 now at bits 8..15
-    acc = ffma2(field_pair(h, 0x300u, 0xC00u), make_float2(x3.x, x3.y), acc);
-    acc = ffma2(field_pair(h, 0x3000u, 0xC000u), make_float2(x3.z, x3.w), acc);
-    return acc;
-}
-
-// sum of the same 16 prepared x values, as affine_word with every field = 1
-__device__ __forceinline__ float2 affine_ones(const float4 &x0, const float4 &x1, const float4 &x2, const float4 &x3,
-                                              float2 acc) {
-    acc = ffma2(field_pair(0xFFFFFFFFu, 0x1u, 0x4u), make_float2(x0.x, x0.y), acc);
-    acc = ffma2(field_pair(0xFFFFFFFFu, 0x10u, 0x40u), make_float2(x0.z, x0.w), acc);
-    acc = ffma2(field_pair(0xFFFFFFFFu, 0x100u, 0x400u), make_float2(x1.x, x1.y), acc);
-    acc = ffma2(field_pair(0xFFFFFFFFu, 0x1000u, 0x4000u), make_float2(x1.z, x1.w), acc);
-    acc = ffma2(field_pair(0xFFFFFFFFu, 0x10000u, 0x40000u), make_float2(x2.x, x2.y), acc);
-    acc = ffma2(field_pair(0xFFFFFFFFu, 0x100000u, 0x400000u), make_float2(x2.z, x2.w), acc);
-    acc = ffma2(field_pair(0xFFFFFFFFu, 0x100u, 0x400u), make_float2(x3.x, x3.y), acc);
-    acc = ffma2(field_pair(0xFFFFFFFFu, 0x1000u, 0x4000u), make_float2(x3.z, x3.w), acc);
-    return acc;
-}
+// the same for the affine decode's fp16 x: a chunk of 64 fields is 8 slots of 16 bytes
+__device__ __forceinline__ int xs16_slot(int g) { return g ^ ((g >> 3) & 7); }
 
 __device__ __forceinline__ float cb_select(uint32_t c, float c0, float c1, float c2, float c3) {
     const float lo = (c & 1u) ? c1 : c0;
@@ -151,8 +115,8 @@ __global__ void __launch_bounds__(512) gemv2_vec_kernel(const PackedArgs a, cons
         pdl_launch_dependents();
     }
 
-    // ---- stage x as fp32 (prepared for the affine decode); every 16-byte
-    // load of a batch is issued before any of them is converted
+    // ---- stage x: the select decode takes fp32 values, the affine decode the fp16 values as they
+    // are; every 16-byte load of a batch is issued before any of them is stored
     const int n8 = (int)(a.cols >> 3);
     constexpr int XU = 4;
     for (int base = threadIdx.x; base < n8; base += XU * blockDim.x) {
@@ -166,29 +130,34 @@ __global__ void __launch_bounds__(512) gemv2_vec_kernel(const PackedArgs a, cons
         for (int u = 0; u < XU; ++u) {
             const int g = base + u * blockDim.x;
             if (g < n8) {
-                const uint32_t hw[4] = {hv[u].x, hv[u].y, hv[u].z, hv[u].w};
-                float v[8];
+                if (DQ == kDeqAffine) {
+                    reinterpret_cast<uint4 *>(xs)[xs16_slot(g)] = hv[u];
+                } else {
+                    const uint32_t hw[4] = {hv[u].x, hv[u].y, hv[u].z, hv[u].w};
+                    float v[8];
 #pragma unroll
-                for (int i = 0; i < 8; ++i) {
-                    v[i] = h2f((uint16_t)((hw[i >> 1] >> (16 * (i & 1))) & 0xFFFFu));
-                    if (DQ == kDeqAffine) {
-                        const int j = (8 * g + i) & 15;             // field index inside its 32-bit word
-                        const int p = j < 12 ? 2 * j : 2 * j - 16;  // bit it is read at
-                        v[i] *= pow2f(111 - p);
-                    }
+                    for (int i = 0; i < 8; ++i) v[i] = h2f((uint16_t)((hw[i >> 1] >> (16 * (i & 1))) & 0xFFFFu));
+                    xs[xs_slot(2 * g)] = make_float4(v[0], v[1], v[2], v[3]);
+                    xs[xs_slot(2 * g + 1)] = make_float4(v[4], v[5], v[6], v[7]);
                 }
-                xs[xs_slot(2 * g)] = make_float4(v[0], v[1], v[2], v[3]);
-                xs[xs_slot(2 * g + 1)] = make_float4(v[4], v[5], v[6], v[7]);
             }
         }
     }
     __syncthreads();
 
     // ---- multiply
-    float2 acc[R];
+    float2 acc[R];      // select decode
+    float accm[R][5];   // affine decode: five classes per row (gemv_mixed.cuh)
+    float accx[5];      // affine: this lane's sum of x, same classes and order as accm
 #pragma unroll
-    for (int r = 0; r < R; ++r) acc[r] = make_float2(0.f, 0.f);
-    float2 acc_x = make_float2(0.f, 0.f);  // affine: this lane's sum of x, same order as acc
+    for (int r = 0; r < R; ++r) {
+        acc[r] = make_float2(0.f, 0.f);
+#pragma unroll
+        for (int k = 0; k < 5; ++k) accm[r][k] = 0.f;
+    }
+#pragma unroll
+    for (int k = 0; k < 5; ++k) accx[k] = 0.f;
+    const uint4 *xs16 = reinterpret_cast<const uint4 *>(xs);
 
     for (int c0 = 0; c0 < nc; c0 += S * CPL) {
         if (c0 > 0) load_batch(c0);
@@ -198,19 +167,26 @@ __global__ void __launch_bounds__(512) gemv2_vec_kernel(const PackedArgs a, cons
             if (c < nc) {
 #pragma unroll
                 for (int u = 0; u < 4; ++u) {
-                    const int f = 16 * c + 4 * u;
-                    const float4 x0 = xs[xs_slot(f + 0)];
-                    const float4 x1 = xs[xs_slot(f + 1)];
-                    const float4 x2 = xs[xs_slot(f + 2)];
-                    const float4 x3 = xs[xs_slot(f + 3)];
-                    if (DQ == kDeqAffine) acc_x = affine_ones(x0, x1, x2, x3, acc_x);
+                    if (DQ == kDeqAffine) {
+                        const uint4 xa = xs16[xs16_slot(8 * c + 2 * u)], xb = xs16[xs16_slot(8 * c + 2 * u + 1)];
+                        const uint32_t X[8] = {xa.x, xa.y, xa.z, xa.w, xb.x, xb.y, xb.z, xb.w};
+                        word_mixed(0x55555555u, X, accx);
 #pragma unroll
-                    for (int r = 0; r < R; ++r) {
-                        const uint32_t w = u == 0 ? q[r][t].x : u == 1 ? q[r][t].y : u == 2 ? q[r][t].z : q[r][t].w;
-                        if (DQ == kDeqAffine)
-                            acc[r] = affine_word(w, x0, x1, x2, x3, acc[r]);
-                        else
+                        for (int r = 0; r < R; ++r) {
+                            const uint32_t w = u == 0 ? q[r][t].x : u == 1 ? q[r][t].y : u == 2 ? q[r][t].z : q[r][t].w;
+                            word_mixed(w, X, accm[r]);
+                        }
+                    } else {
+                        const int f = 16 * c + 4 * u;
+                        const float4 x0 = xs[xs_slot(f + 0)];
+                        const float4 x1 = xs[xs_slot(f + 1)];
+                        const float4 x2 = xs[xs_slot(f + 2)];
+                        const float4 x3 = xs[xs_slot(f + 3)];
+#pragma unroll
+                        for (int r = 0; r < R; ++r) {
+                            const uint32_t w = u == 0 ? q[r][t].x : u == 1 ? q[r][t].y : u == 2 ? q[r][t].z : q[r][t].w;
                             acc[r] = select_word(w, x0, x1, x2, x3, acc[r], a);
+                        }
                     }
                 }
             }
@@ -221,12 +197,13 @@ __global__ void __launch_bounds__(512) gemv2_vec_kernel(const PackedArgs a, cons
     float s[R];
 #pragma unroll
     for (int r = 0; r < R; ++r) {
-        s[r] = acc[r].x + acc[r].y;
+        s[r] = DQ == kDeqAffine ? mixed_total(accm[r]) : acc[r].x + acc[r].y;
 #pragma unroll
         for (int off = S / 2; off > 0; off >>= 1) s[r] += __shfl_xor_sync(0xffffffffu, s[r], off);
     }
-    float sx = acc_x.x + acc_x.y;
+    float sx = 0.f;
     if (DQ == kDeqAffine) {
+        sx = mixed_total(accx);
 #pragma unroll
         for (int off = S / 2; off > 0; off >>= 1) sx += __shfl_xor_sync(0xffffffffu, sx, off);
     }
@@ -237,9 +214,9 @@ __global__ void __launch_bounds__(512) gemv2_vec_kernel(const PackedArgs a, cons
             const float scale = h2f(a.scales[row]);
             float v;
             if (DQ == kDeqAffine) {
-                // products with the exact powers of two are exact; no contraction into an fma
+                // no contraction into an fma: a row of zero-entry fields gives exactly 0
                 const float c0 = a.cb[0], d = a.cb[1] - a.cb[0];
-                v = __fadd_rn(__fmul_rn(c0, sx * 274877906944.0f), __fmul_rn(d, s[r] * 274877906944.0f));
+                v = __fadd_rn(__fmul_rn(c0, sx), __fmul_rn(d, s[r]));
             } else {
                 v = s[r];
             }
