@@ -633,7 +633,7 @@ def main_mm(args):
                                           "peak": peaks["hbm_gbs"], "unit": "GB/s",
                                           "frac": GEMV_TOTAL_BYTES / per_mat_gemvb_s / 1e9 / peaks["hbm_gbs"],
                                           "weight_frac": GEMV_WEIGHT_BYTES / per_mat_gemvb_s / 1e9 / peaks["hbm_gbs"],
-                                          "traffic": None, "peak_source": peaks_src}}},
+                                          "traffic": traffic_for("gemv2_batched"), "peak_source": peaks_src}}},
         "ternary": {"value": tern_tflops, "unit": "TFLOP/s", "ms_per_block": tern_total_s / args.steps * 1e3,
                     "us_per_product": tern_total_s / args.steps / (2 * N_LAYERS) * 1e6,
                     "kernel": "gemm_packed2_tcr_kernel (automatic token tile and cluster split)", "opts": TERN_OPTS,

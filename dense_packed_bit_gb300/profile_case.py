@@ -5,6 +5,7 @@
     python -m dense_packed_bit_gb300.profile_case gemv --reps 3 --split 0 --rows 1 --warps 0 --dequant 2 --staging 1
     python -m dense_packed_bit_gb300.profile_case gemv4 --reps 3 [--staging 1 --rows 1 --independent 1]
     python -m dense_packed_bit_gb300.profile_case ternary --reps 1 [--tile 2] [--pdl 2: pdl + static weights]
+    python -m dense_packed_bit_gb300.profile_case gemv_batched --reps 2 --matrices 16
 
 One warm-up launch precedes the `reps` launches.  No timing is done here:
 numbers come from the profiler or from bench.py.
@@ -17,7 +18,7 @@ import sys
 
 def main(argv=None):
     ap = argparse.ArgumentParser()
-    ap.add_argument("op", choices=["gemm", "gemv", "gemv4", "ternary"])
+    ap.add_argument("op", choices=["gemm", "gemv", "gemv4", "ternary", "gemv_batched"])
     ap.add_argument("--layout", default="nn", choices=["nn", "nt", "tn"])
     ap.add_argument("--size", type=int, default=2048)
     ap.add_argument("--path", type=int, default=0)
@@ -76,6 +77,19 @@ def main(argv=None):
             mm.mm_gemv_packed4_ex(codes[i], scales[i], x, y[i], 12288, 1536, c.codebook, pdl=a.pdl,
                                   independent=a.independent, staging=a.staging if a.staging else -1,
                                   blocks=a.rows if a.staging else 0)
+    elif a.op == "gemv_batched":
+        n = a.matrices
+        codes = torch.empty((n, 12288, 384), dtype=torch.uint8, device=dev)
+        scales = torch.empty((n, 12288), dtype=torch.int16, device=dev)
+        for i in range(n):
+            c = synth.gemv_2bit_12288x1536(i)
+            codes[i].copy_(torch.from_numpy(c.codes))
+            scales[i].copy_(torch.from_numpy(c.scales.view("int16")))
+        x = torch.from_numpy(c.X.reshape(-1)).to(dev)
+        y = torch.empty((n, 12288), dtype=torch.float32, device=dev)
+        for _ in range(1 + a.reps):
+            mm.mm_gemv_packed2_strided_batched(codes, 12288 * 384, scales, 12288, x, 0, y, 12288, n, 12288, 1536,
+                                               c.codebook)
     else:
         layers = []
         for layer in range(16):
