@@ -287,6 +287,8 @@ class Workload:
         self.mlp_w = torch.from_numpy(synth.normal_f32(off + 32, (MLP_K, MLP_N), 0.02)).to(device)
         self.mlp_b = torch.from_numpy(synth.normal_f32(off + 33, (MLP_N,), 0.02)).to(device)
         self.mlp_y = torch.empty((MLP_M, MLP_N), dtype=torch.float32, device=device)
+        self.mlp_ws_floats = mm.mm_gemm_f32_splitk_workspace(MLP_M, MLP_N, MLP_K, 0)
+        self.mlp_ws = torch.empty(max(self.mlp_ws_floats, 4), dtype=torch.float32, device=device)
         self.flush = torch.empty(512 * 1024 * 1024 // 4, dtype=torch.float32, device=device)
         self.args = args
 
@@ -366,8 +368,8 @@ def capture_phases(w: Workload, stream):
                                   w.train_ws, w.train_ws_floats)
 
     def mlp():
-        mm.mm_gemm_f32_bias_act(0, 0, MLP_M, MLP_N, MLP_K, w.mlp_x, MLP_K, w.mlp_w, MLP_N, w.mlp_b,
-                                mm.MM_ACT_GELU_TANH, w.mlp_y, MLP_N)
+        mm.mm_gemm_f32_bias_act_splitk(0, 0, MLP_M, MLP_N, MLP_K, w.mlp_x, MLP_K, w.mlp_w, MLP_N, w.mlp_b,
+                                       mm.MM_ACT_GELU_TANH, w.mlp_y, MLP_N, 0, w.mlp_ws, w.mlp_ws_floats)
 
     def tern():
         for t in w.tern:
@@ -671,7 +673,7 @@ def main_mm(args):
                         "value": world * MLP_FLOP * args.steps / mlp_total_s / 1e12, "unit": "TFLOP/s",
                         "us_per_call": mlp_total_s / args.steps * 1e6,
                         "shape": f"{MLP_M}x{MLP_N}x{MLP_K} NN (8 x 1024 tokens, 768 -> 3072), N(0,1) x N(0,0.02)",
-                        "path": "mm_gemm_f32_bias_act"},
+                        "path": "mm_gemm_f32_bias_act_splitk, automatic split (stream-K: 384 pair tiles on 76 pairs)"},
         "roofline": roof,
         "clocks": clk,
         "gpu_launches": LAUNCHES_PER_STEP * args.steps,

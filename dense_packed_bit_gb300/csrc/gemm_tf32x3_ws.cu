@@ -454,7 +454,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                 float v[32];
                 // bias of this chunk's 32 columns, one per lane, loaded while TMEM is read
                 float bl = 0.0f;
-                if (SK == 0 && p.bias && !p.ws && n0 + c0 + lane < p.N) bl = __ldg(p.bias + n0 + c0 + lane);
+                if (p.bias && !p.ws && n0 + c0 + lane < p.N) bl = __ldg(p.bias + n0 + c0 + lane);
                 tmem_ld32(base + (uint32_t)c0, v);
                 if (sk_part) {
                     // the whole 128 x BN partial tile, unmasked: the slot is private to this unit
@@ -477,7 +477,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                 }
                 // columns of this chunk inside the tile (the last chunk of a 240-wide tile has 16)
                 const int w = BN - c0 < 32 ? BN - c0 : 32;
-                if (SK == 0 && !p.ws) {  // bias and act are never set with split-K or stream-K
+                if (!p.ws) {  // K slices: the reduce kernel applies bias and act; stream-K: the fixup writes C
                     if (p.act) {
 #pragma unroll
                         for (int j = 0; j < 32; ++j) v[j] = gelu_tanh_f(v[j] + __shfl_sync(0xffffffffu, bl, j));
@@ -568,7 +568,13 @@ cudaError_t launch_ws1(const CUtensorMap &ta, const CUtensorMap &tb, const CUten
 
 // C = sum over the ksplit slices of the workspace, added in slice order (bit-reproducible).
 __global__ void __launch_bounds__(256) splitk_reduce_kernel(const float *__restrict__ ws, float *__restrict__ C,
-                                                            int64_t ldc, int M, int N, int ksplit) {
+                                                            int64_t ldc, int M, int N, int ksplit,
+                                                            const float *__restrict__ bias, int act) {
+    // the sum of the slices in slice order, then the layer's bias and activation when given
+    auto fin = [&](float z, int64_t col) {
+        if (bias) z += __ldg(bias + col);
+        return act ? gelu_tanh_f(z) : z;
+    };
     const int64_t MN = (int64_t)M * N;
     const int64_t step = (int64_t)gridDim.x * blockDim.x;
     const bool vec = (N % 4 == 0) && (ldc % 4 == 0) && ((reinterpret_cast<uintptr_t>(C) & 15) == 0) &&
@@ -585,13 +591,14 @@ __global__ void __launch_bounds__(256) splitk_reduce_kernel(const float *__restr
                 acc.w += v.w;
             }
             const int64_t row = (4 * i) / N, col = (4 * i) % N;
+            if (bias || act) acc = make_float4(fin(acc.x, col), fin(acc.y, col + 1), fin(acc.z, col + 2), fin(acc.w, col + 3));
             *reinterpret_cast<float4 *>(C + row * ldc + col) = acc;
         }
     } else {
         for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < MN; i += step) {
             float acc = ws[i];
             for (int s = 1; s < ksplit; ++s) acc += ws[(int64_t)s * MN + i];
-            C[(i / N) * ldc + i % N] = acc;
+            C[(i / N) * ldc + i % N] = (bias || act) ? fin(acc, i % N) : acc;
         }
     }
 }
@@ -659,7 +666,7 @@ cudaError_t launch_ws_cg(const GemmArgs &g, int sms, int ksplit, float *ws, cuda
     const int64_t work = (g.M * g.N + 3) / 4;
     const int64_t blocks = (work + 255) / 256;
     splitk_reduce_kernel<<<(unsigned)(blocks < 4 * sms ? blocks : 4 * sms), 256, 0, s>>>(ws, g.C, g.ldc, (int)g.M,
-                                                                                        (int)g.N, ksplit);
+                                                                                        (int)g.N, ksplit, g.bias, g.act);
     return cudaGetLastError();
 }
 
@@ -696,9 +703,11 @@ int gemm_splitk_auto(int64_t M, int64_t N, int64_t K, int pair, int sms) {
     const int64_t units = sms / cg;
     if (tiles >= units) {
         // stream-K when the last wave is partial enough to cost more than 5% (4 waves' worth of
-        // units for 256 pair tiles on 76 pairs: +12% measured), and each unit keeps 8 slabs
+        // units for 256 pair tiles on 76 pairs: +12% measured), each unit keeps 8 slabs, and a
+        // tile has at least 64 slabs (K >= 1024): with 48 (8192 x 3072 x 768, 384 pair tiles)
+        // the fixups measured slower than the partial last wave (154 against 149 us)
         const int64_t waves = (tiles + units - 1) / units;
-        return (waves * units * 100 > tiles * 105 && tiles * kt >= 8 * units) ? kStreamK : 1;
+        return (waves * units * 100 > tiles * 105 && tiles * kt >= 8 * units && kt >= 64) ? kStreamK : 1;
     }
     int64_t s = units / tiles;
     if (s >= 2) {

@@ -206,9 +206,14 @@ mm_status mm_gemm_f32_splitk_workspace(int64_t M, int64_t N, int64_t K, int spli
     return ok();
 }
 
-mm_status mm_gemm_f32_splitk(int transA, int transB, int64_t M, int64_t N, int64_t K, const float *A, int64_t lda,
-                             const float *B, int64_t ldb, float *C, int64_t ldc, int splitk, float *workspace,
-                             int64_t workspace_floats, mm_stream_t stream) {
+}  // extern "C"
+
+namespace {
+
+// the split GEMM of mm_gemm_f32_splitk, with the linear layer's bias and activation
+mm_status gemm_splitk_impl(int transA, int transB, int64_t M, int64_t N, int64_t K, const float *A, int64_t lda,
+                           const float *B, int64_t ldb, const float *bias, int act, float *C, int64_t ldc, int splitk,
+                           float *workspace, int64_t workspace_floats, mm_stream_t stream) {
     if ((transA != 0 && transA != 1) || (transB != 0 && transB != 1))
         return fail(MM_ERR_INVALID_ARG, "transA/transB must be 0 or 1");
     if (M < 1 || N < 1 || K < 1)
@@ -223,6 +228,8 @@ mm_status mm_gemm_f32_splitk(int transA, int transB, int64_t M, int64_t N, int64
     const uint64_t cb = span(M, N, ldc, 4);
     if (overlap(C, cb, A, span(a_rows, a_cols, lda, 4)) || overlap(C, cb, B, span(b_rows, b_cols, ldb, 4)))
         return fail(MM_ERR_INVALID_ARG, "C overlaps A or B");
+    if (act != MM_ACT_NONE && act != MM_ACT_GELU_TANH) return fail(MM_ERR_INVALID_ARG, "unknown act %d", act);
+    if (bias && overlap(C, cb, bias, (uint64_t)N * 4)) return fail(MM_ERR_INVALID_ARG, "C overlaps bias");
     if (splitk < -1 || splitk > 16)
         return fail(MM_ERR_INVALID_ARG, "splitk must be 0 (automatic), 1..16 (slices) or -1 (stream-K)");
     if (workspace_floats < 0) return fail(MM_ERR_INVALID_ARG, "workspace_floats < 0");
@@ -244,6 +251,8 @@ mm_status mm_gemm_f32_splitk(int transA, int transB, int64_t M, int64_t N, int64
     s = check_device();
     if (s != MM_OK) return s;
     mm::GemmArgs g{transA, transB, M, N, K, A, lda, B, ldb, C, ldc};
+    g.bias = bias;
+    g.act = act;
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
     cudaError_t e;
     // operands TMA cannot describe take the unsplit general kernel (the workspace is unused)
@@ -251,6 +260,25 @@ mm_status mm_gemm_f32_splitk(int transA, int transB, int64_t M, int64_t N, int64
     else e = mm::launch_gemm_simple(g, st);
     if (e != cudaSuccess) return cuda_fail(e, "gemm launch");
     return ok();
+}
+
+}  // namespace
+
+extern "C" {
+
+mm_status mm_gemm_f32_splitk(int transA, int transB, int64_t M, int64_t N, int64_t K, const float *A, int64_t lda,
+                             const float *B, int64_t ldb, float *C, int64_t ldc, int splitk, float *workspace,
+                             int64_t workspace_floats, mm_stream_t stream) {
+    return gemm_splitk_impl(transA, transB, M, N, K, A, lda, B, ldb, nullptr, MM_ACT_NONE, C, ldc, splitk, workspace,
+                            workspace_floats, stream);
+}
+
+mm_status mm_gemm_f32_bias_act_splitk(int transA, int transB, int64_t M, int64_t N, int64_t K, const float *A,
+                                      int64_t lda, const float *B, int64_t ldb, const float *bias, int act, float *C,
+                                      int64_t ldc, int splitk, float *workspace, int64_t workspace_floats,
+                                      mm_stream_t stream) {
+    return gemm_splitk_impl(transA, transB, M, N, K, A, lda, B, ldb, bias, act, C, ldc, splitk, workspace,
+                            workspace_floats, stream);
 }
 
 mm_status mm_gemm_f32_bias_act(int transA, int transB, int64_t M, int64_t N, int64_t K, const float *A, int64_t lda,

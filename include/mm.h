@@ -139,6 +139,19 @@ mm_status mm_gemm_f32_bias_act(int transA, int transB, int64_t M, int64_t N, int
                                mm_stream_t stream);
 
 /*
+ * mm_gemm_f32_bias_act with the split of mm_gemm_f32_splitk (same splitk values and
+ * workspace, sized by mm_gemm_f32_splitk_workspace): K slices add up in the reduce
+ * kernel, which then applies bias and act; with stream-K the segment that completes
+ * a tile applies them.  Same bound as mm_gemm_f32_bias_act.  Errors: the union of
+ * both calls' errors.
+ */
+mm_status mm_gemm_f32_bias_act_splitk(int transA, int transB, int64_t M, int64_t N, int64_t K,
+                                      const float *A, int64_t lda, const float *B, int64_t ldb,
+                                      const float *bias, int act, float *C, int64_t ldc, int splitk,
+                                      float *workspace, int64_t workspace_floats,
+                                      mm_stream_t stream);
+
+/*
  * Split-K form of mm_gemm_f32 for products with fewer output tiles than the GPU
  * has SMs (short M and N, long K: the GPT-2 MLP shapes at small batch; or a
  * last partial wave, such as 2048^3 on CTA pairs).  splitk = 1..16: K is cut into

@@ -299,3 +299,14 @@ def test_gemv_batched_argument_errors(lib, case):
                                              a["x_stride"], a["y"], a["y_stride"], a["batch"], a["rows"], a["cols"],
                                              _cb(-2, -1, 0, 1), None)
     assert st == mm.MM_ERR_INVALID_ARG, lib.mm_last_error()
+
+
+@pytest.mark.parametrize("case", [dict(act=3), dict(bias=FAKE + 0x40000), dict(splitk=17), dict(splitk=-2),
+                                  dict(ws=None, splitk=4), dict(ws_floats=10, splitk=4)])
+def test_gemm_bias_act_splitk_argument_errors(lib, case):
+    a = dict(M=64, N=64, K=256, A=FAKE, B=FAKE + 0x20000, C=FAKE + 0x40000, bias=FAKE + 0x80000, act=1, splitk=4,
+             ws=FAKE + 0x100000, ws_floats=4 * 64 * 64)
+    a.update(case)
+    st = lib.mm_gemm_f32_bias_act_splitk(0, 0, a["M"], a["N"], a["K"], a["A"], a["K"], a["B"], a["N"], a["bias"],
+                                         a["act"], a["C"], a["N"], a["splitk"], a["ws"], a["ws_floats"], None)
+    assert st == mm.MM_ERR_INVALID_ARG, lib.mm_last_error()

@@ -116,3 +116,47 @@ def test_bias_act_identity_is_plain_gemm_and_deterministic():
     db = to_dev(b)
     r = [run(0, 0, M, N, K, A, B, b, 1) for _ in range(2)]
     assert np.array_equal(r[0], r[1])
+
+
+# ------------------------------------------------------------------ with the K split
+
+def run_split(tA, tB, M, N, K, A, B, bias, act, splitk):
+    dA, dB = to_dev(A), to_dev(B)
+    dbias = None if bias is None else to_dev(bias)
+    dC = empty_f32((M, N))
+    need = mm.mm_gemm_f32_splitk_workspace(M, N, K, splitk)
+    ws = empty_f32((max(need, 4),), 0.0)
+    mm.mm_gemm_f32_bias_act_splitk(tA, tB, M, N, K, dA, A.shape[1], dB, B.shape[1], dbias, act, dC, N, splitk, ws,
+                                   need)
+    mm.mm_check_device_error()
+    return to_host(dC)
+
+
+@pytest.mark.parametrize("act", [0, 1])
+@pytest.mark.parametrize("splitk", [0, 1, 3, 16, -1])
+@pytest.mark.parametrize("layout", ["nn", "nt", "tn"])
+@pytest.mark.parametrize("shape", [(64, 3072, 768), (300, 2000, 1000), (129, 257, 33), (2000, 2900, 72)])
+def test_bias_act_split_parity(oracle, shape, layout, splitk, act):
+    # K slices (bias and act applied by the reduce kernel), stream-K (applied by the segment that
+    # completes a tile), the automatic choice, and no split
+    tA, tB = LAYOUTS[layout]
+    M, N, K = shape
+    A, B = operands(tA, tB, M, N, K, seed=7 * M + N + K + 100 * act)
+    bias = synth.normal_f32(5 + N, (N,), 1.0)
+    got = run_split(tA, tB, M, N, K, A, B, bias, act, splitk)
+    Y, T, Z = oracle.gemm_bias_act(tA, tB, M, N, K, A, B, bias, act)
+    check(got, Y, T, Z, f"{layout} {shape} splitk {splitk} act {act}")
+
+
+def test_bias_act_split_gpt2_mlp_up_sampled(oracle):
+    # the 8192 x 3072 x 768 MLP up-projection with its automatic split, sampled rows and columns
+    M, N, K = 8192, 3072, 768
+    A, B = operands(0, 0, M, N, K, seed=91)
+    bias = synth.normal_f32(92, (N,), 1.0)
+    got = run_split(0, 0, M, N, K, A, B, bias, 1, 0)
+    rows = np.array([0, 127, 128, 255, 256, 4095, 8191])
+    cols = np.array([0, 255, 256, 1535, 3071])
+    Yr, Tr, Zr = oracle.gemm_bias_act(0, 0, len(rows), N, K, A[rows], B, bias, 1)
+    check(got[rows], Yr, Tr, Zr, "sampled rows")
+    Yc, Tc, Zc = oracle.gemm_bias_act(0, 0, M, len(cols), K, A, B[:, cols], bias[cols], 1)
+    check(got[:, cols], Yc, Tc, Zc, "sampled columns")
