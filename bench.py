@@ -664,7 +664,7 @@ def main_mm(args):
                    "roofline": {"bound": "hbm", "achieved": GEMVT_TOTAL_BYTES / per_call_gemvt_s / 1e9,
                                 "peak": peaks["hbm_gbs"], "unit": "GB/s",
                                 "frac": GEMVT_TOTAL_BYTES / per_call_gemvt_s / 1e9 / peaks["hbm_gbs"],
-                                "traffic": None, "peak_source": peaks_src}},
+                                "traffic": traffic_for("gemv2_vec_t"), "peak_source": peaks_src}},
         "training_set": {"metric": "fp32 GEMM TFLOP/s, 8192x8192x2048 forward + dA (NT) + dB (TN)",
                          "value": world * TRAIN_FLOP * args.steps / train_total_s / 1e12, "unit": "TFLOP/s",
                          "ms_per_set": train_total_s / args.steps * 1e3,

@@ -6,6 +6,7 @@
     python -m dense_packed_bit_gb300.profile_case gemv4 --reps 3 [--staging 1 --rows 1 --independent 1]
     python -m dense_packed_bit_gb300.profile_case ternary --reps 1 [--tile 2] [--pdl 2: pdl + static weights]
     python -m dense_packed_bit_gb300.profile_case gemv_batched --reps 2 --matrices 16
+    python -m dense_packed_bit_gb300.profile_case gemv_t --reps 3 --matrices 8   (1,536 x 12,288, automatic)
 
 One warm-up launch precedes the `reps` launches.  No timing is done here:
 numbers come from the profiler or from bench.py.
@@ -18,7 +19,7 @@ import sys
 
 def main(argv=None):
     ap = argparse.ArgumentParser()
-    ap.add_argument("op", choices=["gemm", "gemv", "gemv4", "ternary", "gemv_batched"])
+    ap.add_argument("op", choices=["gemm", "gemv", "gemv4", "ternary", "gemv_batched", "gemv_t"])
     ap.add_argument("--layout", default="nn", choices=["nn", "nt", "tn"])
     ap.add_argument("--size", type=int, default=2048)
     ap.add_argument("--path", type=int, default=0)
@@ -64,6 +65,17 @@ def main(argv=None):
                                   rows_per_lane=a.rows, warps=a.warps, dequant=a.dequant, pdl=a.pdl,
                                   weights_static=a.pdl and not a.independent, independent=a.independent,
                                   staging=a.staging)
+    elif a.op == "gemv_t":
+        codes, scales = [], []
+        for i in range(a.matrices):
+            c = synth.gemv_2bit_1536x12288(i)
+            codes.append(torch.from_numpy(c.codes).to(dev))
+            scales.append(torch.from_numpy(c.scales).to(dev))
+        x = torch.from_numpy(c.X.reshape(-1)).to(dev)
+        y = torch.empty((a.matrices, 1536), dtype=torch.float32, device=dev)
+        for r in range(1 + a.reps):
+            i = r % a.matrices
+            mm.mm_gemv_packed2_ex(codes[i], scales[i], x, y[i], 1536, 12288, c.codebook, pdl=1, independent=1)
     elif a.op == "gemv4":
         codes, scales = [], []
         for i in range(a.matrices):
