@@ -20,7 +20,7 @@ __all__ = [
     "mm_gemm_packed2", "mm_gemm_packed2_ex", "mm_gemv_packed4", "mm_gemv_packed4_ex",
     "mm_check_device_error", "mm_gemm_f32_splitk", "mm_gemm_f32_splitk_workspace", "mm_gemm_f32_splitk_noalloc",
     "MM_SPLITK_NOALLOC_MAX_FLOATS", "mm_gemm_f32_bias_act", "MM_ACT_NONE", "MM_ACT_GELU_TANH",
-    "mm_gemv_packed2_strided_batched", "mm_gemm_f32_bias_act_splitk",
+    "mm_gemv_packed2_strided_batched", "mm_gemm_f32_bias_act_splitk", "mm_gemm_f32_split_plan",
     "MM_OK", "MM_ERR_INVALID_ARG", "MM_ERR_UNSUPPORTED", "MM_ERR_CUDA", "MM_ERR_TIMEOUT",
     "MM_GEMM_AUTO", "MM_GEMM_FFMA", "MM_GEMM_TF32X3",
     "MM_DEQ_AUTO", "MM_DEQ_SELECT", "MM_DEQ_AFFINE", "MM_DEQ_MMA", "MM_DEQ_FP8", "MM_DEQ_TC",
@@ -80,6 +80,7 @@ SIGNATURES = {
     "mm_gemm_f32_splitk_noalloc": ([_I, _I, _I64, _I64, _I64, _P, _I64, _P, _I64, _P, _I64, _I, _P],
                                    ctypes.c_int),
     "mm_gemm_f32_bias_act": ([_I, _I, _I64, _I64, _I64, _P, _I64, _P, _I64, _P, _I, _P, _I64, _P], ctypes.c_int),
+    "mm_gemm_f32_split_plan": ([_I64, _I64, _I64, _I, _P, _P], ctypes.c_int),
     "mm_gemm_f32_bias_act_splitk": ([_I, _I, _I64, _I64, _I64, _P, _I64, _P, _I64, _P, _I, _P, _I64, _I, _P, _I64,
                                      _P], ctypes.c_int),
     "mm_gemv_packed2_strided_batched": ([_P, _I64, _P, _I64, _P, _I64, _P, _I64, _I64, _I64, _I64, _P, _P],
@@ -178,6 +179,14 @@ def mm_gemm_f32_splitk(transA, transB, M, N, K, A, lda, B, ldb, C, ldc, splitk, 
     _check(load_library().mm_gemm_f32_splitk(int(transA), int(transB), M, N, K, _ptr(A), lda, _ptr(B), ldb,
                                              _ptr(C), ldc, int(splitk), _ptr(workspace), int(workspace_floats),
                                              _stream(stream)))
+
+
+def mm_gemm_f32_split_plan(M, N, K, sms):
+    """(splitk, workspace_floats) of the automatic split on a GPU with `sms` SMs; no device needed."""
+    sk = ctypes.c_int(0)
+    fl = ctypes.c_int64(0)
+    _check(load_library().mm_gemm_f32_split_plan(M, N, K, int(sms), ctypes.byref(sk), ctypes.byref(fl)))
+    return sk.value, fl.value
 
 
 def mm_gemm_f32_bias_act_splitk(transA, transB, M, N, K, A, lda, B, ldb, bias, act, C, ldc, splitk=0,

@@ -197,6 +197,17 @@ mm_status resolve_splitk(int64_t M, int64_t N, int64_t K, int splitk, int *out, 
 
 extern "C" {
 
+mm_status mm_gemm_f32_split_plan(int64_t M, int64_t N, int64_t K, int sms, int *splitk,
+                                 int64_t *workspace_floats) {
+    if (!splitk || !workspace_floats) return fail(MM_ERR_INVALID_ARG, "NULL output");
+    if (M < 1 || N < 1 || K < 1) return fail(MM_ERR_INVALID_ARG, "M, N, K must be >= 1");
+    if (sms < 2) return fail(MM_ERR_INVALID_ARG, "sms must be >= 2 (got %d)", sms);
+    const int pair = M > 128 ? 1 : 0;
+    *splitk = mm::gemm_splitk_auto(M, N, K, pair, sms);
+    *workspace_floats = mm::gemm_splitk_workspace_floats(M, N, K, pair, *splitk, sms);
+    return ok();
+}
+
 mm_status mm_gemm_f32_splitk_workspace(int64_t M, int64_t N, int64_t K, int splitk, int64_t *floats) {
     if (!floats) return fail(MM_ERR_INVALID_ARG, "floats is NULL");
     if (M < 1 || N < 1 || K < 1) return fail(MM_ERR_INVALID_ARG, "M, N, K must be >= 1");

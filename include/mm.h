@@ -177,6 +177,16 @@ mm_status mm_gemm_f32_bias_act_splitk(int transA, int transB, int64_t M, int64_t
  * misaligned, overlapping or too small workspace.
  */
 mm_status mm_gemm_f32_splitk_workspace(int64_t M, int64_t N, int64_t K, int splitk, int64_t *floats);
+
+/*
+ * The split mm_gemm_f32_splitk takes automatically (splitk = 0) for an M x N x K
+ * product on a GPU with `sms` SMs, and the workspace floats it needs, without
+ * touching any device: *splitk = 1 (no split), 2..16 (K slices) or -1 (stream-K).
+ * For sizing workspaces ahead of time on a known GPU (152 SMs on a GB300).
+ * Errors: MM_ERR_INVALID_ARG for sizes < 1, sms < 2 or NULL outputs.
+ */
+mm_status mm_gemm_f32_split_plan(int64_t M, int64_t N, int64_t K, int sms, int *splitk,
+                                 int64_t *workspace_floats);
 mm_status mm_gemm_f32_splitk(int transA, int transB, int64_t M, int64_t N, int64_t K,
                              const float *A, int64_t lda, const float *B, int64_t ldb,
                              float *C, int64_t ldc, int splitk, float *workspace,

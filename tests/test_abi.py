@@ -310,3 +310,35 @@ def test_gemm_bias_act_splitk_argument_errors(lib, case):
     st = lib.mm_gemm_f32_bias_act_splitk(0, 0, a["M"], a["N"], a["K"], a["A"], a["K"], a["B"], a["N"], a["bias"],
                                          a["act"], a["C"], a["N"], a["splitk"], a["ws"], a["ws_floats"], None)
     assert st == mm.MM_ERR_INVALID_ARG, lib.mm_last_error()
+
+
+# ------------------------------------------------------------------ the automatic GEMM split (host logic, no GPU)
+
+@pytest.mark.parametrize("shape,split,floats", [
+    # GPT-2 MLP up-projection 8192 x 3072 x 768: 384 pair tiles on 76 pairs (a partial 6th wave) but
+    # only 48 slabs of 16 per tile, where stream-K measured slower: no split
+    ((8192, 3072, 768), 1, 0),
+    # training-shape dA / dB and 4096^3: 256 pair tiles = 3.4 waves, 256-512 slabs per tile: stream-K,
+    # one 128 x 256 partial tile per CTA of the 76 units (2 x 76 x 32768 floats) + 152 flag words
+    ((8192, 2048, 8192), -1, 2 * 76 * 32768 + 152),
+    ((2048, 8192, 8192), -1, 2 * 76 * 32768 + 152),
+    ((4096, 4096, 4096), -1, 2 * 76 * 32768 + 152),
+    # training-shape forward 8192 x 8192 x 2048: 1024 pair tiles, 14 waves of 76 lose < 5%: no split
+    ((8192, 8192, 2048), 1, 0),
+    # 2048^3: 64 pair tiles, between half a wave and a wave: no split
+    ((2048, 2048, 2048), 1, 0),
+    # GPT-2 MLP up-projection at 64 tokens: 12 single-CTA tiles on 152 SMs -> 12 K slices of 64
+    ((64, 3072, 768), 12, 12 * 64 * 3072),
+    # 2 tiles: 76 slices would be too thin, capped at K / 64 = 8 slices
+    ((100, 300, 500), 8, 8 * 100 * 300),
+])
+def test_gemm_split_plan(shape, split, floats):
+    mm.load_library()
+    assert mm.mm_gemm_f32_split_plan(*shape, 152) == (split, floats)
+
+
+def test_gemm_split_plan_argument_errors(lib):
+    sk, fl = ctypes.c_int(0), ctypes.c_int64(0)
+    assert lib.mm_gemm_f32_split_plan(0, 8, 8, 152, ctypes.byref(sk), ctypes.byref(fl)) == mm.MM_ERR_INVALID_ARG
+    assert lib.mm_gemm_f32_split_plan(8, 8, 8, 1, ctypes.byref(sk), ctypes.byref(fl)) == mm.MM_ERR_INVALID_ARG
+    assert lib.mm_gemm_f32_split_plan(8, 8, 8, 152, None, ctypes.byref(fl)) == mm.MM_ERR_INVALID_ARG
