@@ -76,7 +76,7 @@ typedef struct CUstream_st *mm_stream_t;
 typedef enum {
     MM_OK = 0,
     MM_ERR_INVALID_ARG = 1,  /* null pointer, bad size / leading dim, overlap, bad option */
-    MM_ERR_UNSUPPORTED = 2,  /* valid request this build cannot run (e.g. no sm_103 device) */
+    MM_ERR_UNSUPPORTED = 2,  /* valid request the library cannot run here (e.g. no sm_103 device) */
     MM_ERR_CUDA = 3,         /* a CUDA runtime call or kernel launch failed */
     MM_ERR_TIMEOUT = 4       /* a kernel's bounded device wait ran out (see mm_check_device_error) */
 } mm_status;
