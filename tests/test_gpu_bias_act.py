@@ -160,3 +160,20 @@ def test_bias_act_split_gpt2_mlp_up_sampled(oracle):
     check(got[rows], Yr, Tr, Zr, "sampled rows")
     Yc, Tc, Zc = oracle.gemm_bias_act(0, 0, M, len(cols), K, A, B[:, cols], bias[cols], 1)
     check(got[:, cols], Yc, Tc, Zc, "sampled columns")
+
+
+@pytest.mark.parametrize("layout", ["nn", "nt", "tn"])
+def test_bias_act_padded_leading_dims(oracle, layout):
+    # padded lda / ldb (multiples of 4: the tensor-core path) and a padded C whose pad stays untouched
+    tA, tB = LAYOUTS[layout]
+    M, N, K = 300, 260, 96
+    A, B = operands(tA, tB, M, N, K, seed=33, lda=(M if tA else K) + 8, ldb=(K if tB else N) + 4)
+    bias = synth.normal_f32(34, (N,), 1.0)
+    dA, dB, db = to_dev(A), to_dev(B), to_dev(bias)
+    dC = empty_f32((M, N + 12))
+    mm.mm_gemm_f32_bias_act(tA, tB, M, N, K, dA, A.shape[1], dB, B.shape[1], db, 1, dC, N + 12)
+    mm.mm_check_device_error()
+    got = to_host(dC)
+    Y, T, Z = oracle.gemm_bias_act(tA, tB, M, N, K, A, B, bias, 1, lda=A.shape[1], ldb=B.shape[1])
+    check(got[:, :N], Y, T, Z, f"{layout} padded")
+    assert np.all(np.isnan(got[:, N:])), "write into the padding of C"

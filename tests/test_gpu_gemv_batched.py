@@ -84,3 +84,26 @@ def test_batched_gemv_zero_entry_rows_exact(oracle):
     codes[:, ::7, :] = 0xAA  # every field = 2
     y = run_batched(codes, scales, x, rows, cols, CB2, True)
     assert np.all(y[:, ::7] == 0.0)
+
+
+def test_batched_gemv_single_matrix_and_unaligned_stride_fallback(oracle):
+    # batch 1 runs the one-launch kernel; a codes stride that is not a multiple of 16 bytes
+    # (one extra byte per matrix) takes one call per matrix
+    rows, cols = 200, 1536
+    rb = cols // 4
+    codes, scales, x = make_batch(1, rows, cols, seed=61, shared_x=True)
+    y = run_batched(codes, scales, x, rows, cols, CB2, True)
+    ref, T = oracle.packed_gemm(codes[0], scales[0], x.reshape(1, cols), rows, cols, CB2)
+    check_bound(y[0], ref[0], T[0], "batch 1")
+    batch = 3
+    flat = synth.random_bytes(62, batch * (rows * rb + 1))
+    sc = synth.uniform_f16_bits(63, (batch, rows), 0.005, 0.05)
+    dflat, dsc, dx = to_dev(flat), to_dev(sc), to_dev(x[0])
+    dy = empty_f32((batch, rows))
+    mm.mm_gemv_packed2_strided_batched(dflat, rows * rb + 1, dsc, rows, dx, 0, dy, rows, batch, rows, cols, CB2)
+    mm.mm_check_device_error()
+    yh = to_host(dy)
+    for b in range(batch):
+        cb_ = flat[b * (rows * rb + 1): b * (rows * rb + 1) + rows * rb].reshape(rows, rb)
+        ref, T = oracle.packed_gemm(cb_, sc[b], x[0].reshape(1, cols), rows, cols, CB2)
+        check_bound(yh[b], ref[0], T[0], f"unaligned stride, matrix {b}")
