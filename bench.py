@@ -111,9 +111,13 @@ def barrier(device=None):
             dist.barrier()
 
 
-def rank_seed_offset(rank: int) -> int:
-    """Each rank draws its own inputs (weak scaling): seeds are offset per rank."""
-    return 7919 * rank
+def rank_replica(rank: int) -> int:
+    """Each rank draws its own inputs (weak scaling): rank r runs replica r of every workload,
+    whose random streams share no draw with any other replica's."""
+    from dense_packed_bit_gb300 import synth
+    if not 0 <= rank < synth.MAX_REPLICAS:
+        raise ValueError(f"rank {rank}: the input recipes hold {synth.MAX_REPLICAS} replicas")
+    return rank
 
 
 # ---------------------------------------------------------------- clocks
@@ -211,14 +215,11 @@ class Workload:
         import torch
         from dense_packed_bit_gb300 import synth
         self.dev = device
-        off = rank_seed_offset(rank)
+        rep = rank_replica(rank)
         self.gemm = []
         for layout in ("nn", "nt", "tn"):
-            c = synth.square_2048(layout)
+            c = synth.square_2048(layout, replica=rep)
             A, B = c.A, c.B
-            if off:
-                A = synth.normal_f32(off + 1 + len(self.gemm), A.shape, 0.02)
-                B = synth.normal_f32(off + 11 + len(self.gemm), B.shape, 0.02)
             self.gemm.append(dict(case=c, A=torch.from_numpy(A).to(device), B=torch.from_numpy(B).to(device),
                                   C=torch.empty((c.M, c.N), dtype=torch.float32, device=device),
                                   hA=A, hB=B))
@@ -229,7 +230,7 @@ class Workload:
         self.gemv_codes, self.gemv_scales = [], []
         x = None
         for i in range(N_GEMV):
-            c = synth.gemv_2bit_12288x1536(i + (off % 1000) * N_GEMV if off else i)
+            c = synth.gemv_2bit_12288x1536(i, replica=rep)
             self.gemv_codes_all[i].copy_(torch.from_numpy(c.codes))
             self.gemv_scales_all[i].copy_(torch.from_numpy(c.scales.view("int16")))
             self.gemv_codes.append(self.gemv_codes_all[i])
@@ -241,7 +242,7 @@ class Workload:
         self.gemv_y = torch.empty((N_GEMV, 12288), dtype=torch.float32, device=device)
         self.gemv4_codes, self.gemv4_scales = [], []
         for i in range(N_GEMV):
-            c = synth.gemv_4bit_12288x1536(i + (off % 1000) * N_GEMV if off else i)
+            c = synth.gemv_4bit_12288x1536(i, replica=rep)
             self.gemv4_codes.append(torch.from_numpy(c.codes).to(device))
             self.gemv4_scales.append(torch.from_numpy(c.scales).to(device))
             x4 = c.X
@@ -250,7 +251,7 @@ class Workload:
         self.gemv4_y = torch.empty((N_GEMV, 12288), dtype=torch.float32, device=device)
         self.gemvt_codes, self.gemvt_scales = [], []
         for i in range(N_GEMV):
-            c = synth.gemv_2bit_1536x12288(i + (off % 1000) * N_GEMV if off else i)
+            c = synth.gemv_2bit_1536x12288(i, replica=rep)
             self.gemvt_codes.append(torch.from_numpy(c.codes).to(device))
             self.gemvt_scales.append(torch.from_numpy(c.scales).to(device))
             xt = c.X
@@ -259,7 +260,7 @@ class Workload:
         self.tern = []
         for layer in range(N_LAYERS):
             for proj in ("up", "down"):
-                c = synth.ternary_encoder_layer(layer, proj)
+                c = synth.ternary_encoder_layer(layer, proj, replica=rep)
                 self.tern.append(dict(case=c, codes=torch.from_numpy(c.codes).to(device),
                                       scales=torch.from_numpy(c.scales).to(device),
                                       X=torch.from_numpy(c.X).to(device),
@@ -268,11 +269,11 @@ class Workload:
         # split entry point with its automatic choice and one shared workspace
         self.train = []
         for which in ("fwd", "dA", "dB"):
-            c = synth.training_set_8192(which)
+            c = synth.training_set_8192(which, replica=rep)
             self.train.append(c)
-        tA = torch.from_numpy(self.train[0].A if not off else synth.normal_f32(off + 21, (8192, 2048), 0.02)).to(device)
-        tB = torch.from_numpy(self.train[0].B if not off else synth.normal_f32(off + 22, (2048, 8192), 0.02)).to(device)
-        tdC = torch.from_numpy(self.train[1].A if not off else synth.normal_f32(off + 23, (8192, 8192), 0.02)).to(device)
+        tA = torch.from_numpy(self.train[0].A).to(device)
+        tB = torch.from_numpy(self.train[0].B).to(device)
+        tdC = torch.from_numpy(self.train[1].A).to(device)
         import dense_packed_bit_gb300 as mm
         self.train_ops = []
         need = 0
@@ -283,9 +284,11 @@ class Workload:
         self.train_ws = torch.empty(max(need, 4), dtype=torch.float32, device=device)
         self.train_ws_floats = need
         # GPT-2 small's MLP up-projection with its bias and GELU fused, 8 sequences of 1024 tokens
-        self.mlp_x = torch.from_numpy(synth.normal_f32(off + 31, (MLP_M, MLP_K), 1.0)).to(device)
-        self.mlp_w = torch.from_numpy(synth.normal_f32(off + 32, (MLP_K, MLP_N), 0.02)).to(device)
-        self.mlp_b = torch.from_numpy(synth.normal_f32(off + 33, (MLP_N,), 0.02)).to(device)
+        mlp = synth.gpt2_mlp_bias_gelu_8192x768x3072(replica=rep)
+        assert (mlp.M, mlp.N, mlp.K) == (MLP_M, MLP_N, MLP_K)
+        self.mlp_x = torch.from_numpy(mlp.A).to(device)
+        self.mlp_w = torch.from_numpy(mlp.B).to(device)
+        self.mlp_b = torch.from_numpy(mlp.bias).to(device)
         self.mlp_y = torch.empty((MLP_M, MLP_N), dtype=torch.float32, device=device)
         self.mlp_ws_floats = mm.mm_gemm_f32_splitk_workspace(MLP_M, MLP_N, MLP_K, 0)
         self.mlp_ws = torch.empty(max(self.mlp_ws_floats, 4), dtype=torch.float32, device=device)

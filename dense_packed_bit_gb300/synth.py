@@ -135,13 +135,22 @@ def digest(*arrays) -> str:
 # per (workload, tensor, index) so a workload is reproducible bit for bit.
 # Workload ids: 1 GPT-2 MLP up-projection, 2 / 12 / 22 square 2048^3 NN / NT /
 # TN, 3 2-bit GEMV rotation, 4 ternary encoder block, 5 4-bit GEMV rotation,
-# 6 transposed 2-bit GEMV rotation, 7 training-shape set.  tensor_id and index
-# stay below 1000, and no stream draws 2**32 numbers, so no two tensors of any
-# workloads share a draw.
+# 6 transposed 2-bit GEMV rotation, 7 training-shape set, 8 GPT-2 MLP
+# up-projection with bias.  `replica` gives every data-parallel replica (one
+# per GPU) its own draws of the same workload; replica 0 is the single-GPU
+# workload.  Every field of the seed is range-checked, and no stream draws
+# 2**32 numbers, so no two tensors of any workloads or replicas share a draw.
 # --------------------------------------------------------------------------
 
-def _seed(workload_id: int, tensor_id: int, index: int = 0) -> int:
-    return (workload_id * 1000 + tensor_id) * 1000 + index
+MAX_REPLICAS = 40
+
+
+def _seed(workload_id: int, tensor_id: int, index: int = 0, replica: int = 0) -> int:
+    if not (0 < workload_id < 100 and 0 < tensor_id < 1000 and 0 <= index < 1000
+            and 0 <= replica < MAX_REPLICAS):
+        raise ValueError(f"seed field out of range: workload {workload_id}, tensor {tensor_id}, "
+                         f"index {index}, replica {replica}")
+    return ((replica * 100 + workload_id) * 1000 + tensor_id) * 1000 + index
 
 
 @dataclass
@@ -154,17 +163,18 @@ class GemmCase:
     K: int
     A: np.ndarray  # stored (M,K) or (K,M) if transA
     B: np.ndarray  # stored (K,N) or (N,K) if transB
+    bias: np.ndarray | None = None  # (N,) fp32, one per output column, for a linear layer
 
 
-def gemm_case(name, transA, transB, M, N, K, dist, seed_base, sigma=0.02):
+def gemm_case(name, transA, transB, M, N, K, dist, seed_base, sigma=0.02, replica=0):
     a_shape = (K, M) if transA else (M, K)
     b_shape = (N, K) if transB else (K, N)
     if dist == "uniform":
-        A = uniform_f32(_seed(seed_base, 1), a_shape, -1.0, 1.0)
-        B = uniform_f32(_seed(seed_base, 2), b_shape, -1.0, 1.0)
+        A = uniform_f32(_seed(seed_base, 1, 0, replica), a_shape, -1.0, 1.0)
+        B = uniform_f32(_seed(seed_base, 2, 0, replica), b_shape, -1.0, 1.0)
     elif dist == "normal":
-        A = normal_f32(_seed(seed_base, 1), a_shape, sigma)
-        B = normal_f32(_seed(seed_base, 2), b_shape, sigma)
+        A = normal_f32(_seed(seed_base, 1, 0, replica), a_shape, sigma)
+        B = normal_f32(_seed(seed_base, 2, 0, replica), b_shape, sigma)
     else:
         raise ValueError(dist)
     return GemmCase(name, transA, transB, M, N, K, A, B)
@@ -175,14 +185,26 @@ def gpt2_mlp_up_64x768x3072() -> GemmCase:
     return gemm_case("gpt2_mlp_up_m64_k768_n3072_nn", 0, 0, 64, 3072, 768, "uniform", 1)
 
 
-def square_2048(layout: str) -> GemmCase:
+def square_2048(layout: str, replica: int = 0) -> GemmCase:
     """Square 2048^3 fp32 GEMM, N(0,0.02) operands, layout 'nn' | 'nt' | 'tn'."""
     tA, tB = {"nn": (0, 0), "nt": (0, 1), "tn": (1, 0)}[layout]
     return gemm_case(f"square_2048_{layout}", tA, tB, 2048, 2048, 2048, "normal",
-                     2 + {"nn": 0, "nt": 10, "tn": 20}[layout])
+                     2 + {"nn": 0, "nt": 10, "tn": 20}[layout], replica=replica)
 
 
-def training_set_8192(which: str) -> GemmCase:
+def gpt2_mlp_bias_gelu_8192x768x3072(replica: int = 0) -> GemmCase:
+    """GPT-2-small MLP up-projection of 8 sequences of 1,024 tokens, with its bias.
+
+    X 8192 x 768 N(0, 1) (the layer-normed activations), W 768 x 3072 N(0, 0.02),
+    bias 3072 N(0, 0.02); NN.  The GELU that follows has no inputs of its own.
+    """
+    X = normal_f32(_seed(8, 1, 0, replica), (8192, 768), 1.0)
+    W = normal_f32(_seed(8, 2, 0, replica), (768, 3072), 0.02)
+    bias = normal_f32(_seed(8, 3, 0, replica), (3072,), 0.02)
+    return GemmCase("gpt2_mlp_up_bias_gelu_m8192_k768_n3072_nn", 0, 0, 8192, 3072, 768, X, W, bias)
+
+
+def training_set_8192(which: str, replica: int = 0) -> GemmCase:
     """Training-shape products (batch 16 x seq 512 = 8192 rows, d=2048, d_ff=8192).
 
     'fwd': C = A(8192x2048) B(2048x8192)            (NN)
@@ -190,11 +212,11 @@ def training_set_8192(which: str) -> GemmCase:
     'dB' : dB = A^T dC, A stored 8192x2048            (TN: M=2048,N=8192,K=8192)
     All operands N(0,0.02); A, B and dC each come from one fixed stream.
     """
-    A = normal_f32(_seed(7, 1), (8192, 2048), 0.02)
-    B = normal_f32(_seed(7, 2), (2048, 8192), 0.02)
+    A = normal_f32(_seed(7, 1, 0, replica), (8192, 2048), 0.02)
+    B = normal_f32(_seed(7, 2, 0, replica), (2048, 8192), 0.02)
     if which == "fwd":
         return GemmCase("train_fwd_8192x8192x2048_nn", 0, 0, 8192, 8192, 2048, A, B)
-    dC = normal_f32(_seed(7, 3), (8192, 8192), 0.02)
+    dC = normal_f32(_seed(7, 3, 0, replica), (8192, 8192), 0.02)
     if which == "dA":
         return GemmCase("train_dA_8192x2048x8192_nt", 0, 1, 8192, 2048, 8192, dC, B)
     if which == "dB":
@@ -248,54 +270,54 @@ def normal_quantile_codebook() -> np.ndarray:
 CODEBOOK_NQ4 = normal_quantile_codebook()
 
 
-def packed_matrix(seed_base, index, rows, cols, kind):
+def packed_matrix(seed_base, index, rows, cols, kind, replica=0):
     """Codes (rows x packed bytes) and fp16 scales; kind 'uniform4' packs 4-bit fields."""
     rb = (cols + 1) // 2 if kind == "uniform4" else (cols + 3) // 4
     nbytes = rows * rb
     if kind in ("uniform2", "uniform4"):
-        codes = random_bytes(_seed(seed_base, 1, index), nbytes)
+        codes = random_bytes(_seed(seed_base, 1, index, replica), nbytes)
     elif kind == "ternary":
-        codes = ternary_field_bytes(_seed(seed_base, 1, index), nbytes)
+        codes = ternary_field_bytes(_seed(seed_base, 1, index, replica), nbytes)
     else:
         raise ValueError(kind)
-    scales = uniform_f16_bits(_seed(seed_base, 2, index), (rows,), 0.005, 0.05)
+    scales = uniform_f16_bits(_seed(seed_base, 2, index, replica), (rows,), 0.005, 0.05)
     return codes.reshape(rows, rb), scales
 
 
-def gemv_2bit_12288x1536(index: int) -> PackedCase:
+def gemv_2bit_12288x1536(index: int, replica: int = 0) -> PackedCase:
     """One of the 64 rotated 2-bit GEMV matrices: 12288 rows x 1536 cols (4.5 MiB of codes)."""
-    codes, scales = packed_matrix(3, index, 12288, 1536, "uniform2")
-    x = normal_f16_bits(_seed(3, 3, 0), (1, 1536))
+    codes, scales = packed_matrix(3, index, 12288, 1536, "uniform2", replica)
+    x = normal_f16_bits(_seed(3, 3, 0, replica), (1, 1536))
     return PackedCase(f"gemv2_12288x1536_m{index}", 12288, 1536, codes, scales,
                       CODEBOOK_2BIT.copy(), x)
 
 
-def gemv_2bit_1536x12288(index: int) -> PackedCase:
+def gemv_2bit_1536x12288(index: int, replica: int = 0) -> PackedCase:
     """The transposed shape (the pages' kernel 0113): 1536 rows x 12288 cols of 2-bit codes,
     4.5 MiB per matrix like the 12288 x 1536 one; same value distributions."""
-    codes, scales = packed_matrix(6, index, 1536, 12288, "uniform2")
-    x = normal_f16_bits(_seed(6, 3, 0), (1, 12288))
+    codes, scales = packed_matrix(6, index, 1536, 12288, "uniform2", replica)
+    x = normal_f16_bits(_seed(6, 3, 0, replica), (1, 12288))
     return PackedCase(f"gemv2_1536x12288_m{index}", 1536, 12288, codes, scales,
                       CODEBOOK_2BIT.copy(), x)
 
 
-def gemv_4bit_12288x1536(index: int) -> PackedCase:
+def gemv_4bit_12288x1536(index: int, replica: int = 0) -> PackedCase:
     """One of the 64 rotated 4-bit GEMV matrices: 12288 rows x 1536 cols (9 MiB of codes),
     fields uniform in 0..15 (two per byte), normal-quantile codebook."""
-    codes, scales = packed_matrix(5, index, 12288, 1536, "uniform4")
-    x = normal_f16_bits(_seed(5, 3, 0), (1, 1536))
+    codes, scales = packed_matrix(5, index, 12288, 1536, "uniform4", replica)
+    x = normal_f16_bits(_seed(5, 3, 0, replica), (1, 1536))
     return PackedCase(f"gemv4_12288x1536_m{index}", 12288, 1536, codes, scales,
                       CODEBOOK_NQ4.copy(), x)
 
 
-def ternary_encoder_layer(layer: int, proj: str) -> PackedCase:
+def ternary_encoder_layer(layer: int, proj: str, replica: int = 0) -> PackedCase:
     """Layer `layer` (0..15) of the ternary 16-layer encoder block, M = 2 x 111 = 222 rows.
 
     proj 'up'  : W 3072 x 768  (N=3072, K=768)
     proj 'down': W 768 x 3072  (N=768,  K=3072)
     """
     rows, cols, pid = (3072, 768, 0) if proj == "up" else (768, 3072, 1)
-    codes, scales = packed_matrix(4, 2 * layer + pid, rows, cols, "ternary")
-    X = normal_f16_bits(_seed(4, 3, 2 * layer + pid), (222, cols))
+    codes, scales = packed_matrix(4, 2 * layer + pid, rows, cols, "ternary", replica)
+    X = normal_f16_bits(_seed(4, 3, 2 * layer + pid, replica), (222, cols))
     return PackedCase(f"ternary_enc_l{layer}_{proj}", rows, cols, codes, scales,
                       CODEBOOK_TERNARY.copy(), X)

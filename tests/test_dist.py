@@ -30,7 +30,7 @@ def _worker(rank, world, port, out_q):
     r, w = bench.dist_init("gloo")
     bench.barrier()
     mx = bench.reduce_max(float(10 + 5 * r))
-    out_q.put((r, w, mx, bench.rank_seed_offset(r)))
+    out_q.put((r, w, mx, bench.rank_replica(r)))
     import torch.distributed as dist
     dist.destroy_process_group()
 

@@ -52,26 +52,33 @@ class _Recorder:
                             lambda s, nb: self._out(s, "ternary", (nb + 7) // 8, (nb,), np.uint8))
 
 
-def _all_workloads(rec):
-    """Every workload recipe with the index ranges the bench and the tests use."""
+def _all_workloads(rec, replicas=(0,)):
+    """Every workload recipe with the index ranges the bench and the tests use.
+
+    Workload names carry the replica, so that a stream shared between two
+    replicas counts as shared between two workloads.
+    """
     out = {}
 
     def run(name, fn):
         rec.workload = name
         out.setdefault(name, []).append(fn())
 
-    run("gpt2_mlp_up", synth.gpt2_mlp_up_64x768x3072)
-    for layout in ("nn", "nt", "tn"):
-        run(f"square_2048_{layout}", lambda: synth.square_2048(layout))
-    for i in range(64):
-        run("gemv2_rotation", lambda: synth.gemv_2bit_12288x1536(i))
-        run("gemv2_t_rotation", lambda: synth.gemv_2bit_1536x12288(i))
-        run("gemv4_rotation", lambda: synth.gemv_4bit_12288x1536(i))
-    for layer in range(16):
-        for proj in ("up", "down"):
-            run("ternary_encoder", lambda: synth.ternary_encoder_layer(layer, proj))
-    for which in ("fwd", "dA", "dB"):
-        run("training_set", lambda: synth.training_set_8192(which))
+    for r in replicas:
+        sfx = f"@{r}" if r else ""
+        run("gpt2_mlp_up" + sfx, synth.gpt2_mlp_up_64x768x3072)  # a parity case: replica 0 only
+        run("gpt2_mlp_bias" + sfx, lambda: synth.gpt2_mlp_bias_gelu_8192x768x3072(replica=r))
+        for layout in ("nn", "nt", "tn"):
+            run(f"square_2048_{layout}" + sfx, lambda: synth.square_2048(layout, replica=r))
+        for i in range(64):
+            run("gemv2_rotation" + sfx, lambda: synth.gemv_2bit_12288x1536(i, replica=r))
+            run("gemv2_t_rotation" + sfx, lambda: synth.gemv_2bit_1536x12288(i, replica=r))
+            run("gemv4_rotation" + sfx, lambda: synth.gemv_4bit_12288x1536(i, replica=r))
+        for layer in range(16):
+            for proj in ("up", "down"):
+                run("ternary_encoder" + sfx, lambda: synth.ternary_encoder_layer(layer, proj, replica=r))
+        for which in ("fwd", "dA", "dB"):
+            run("training_set" + sfx, lambda: synth.training_set_8192(which, replica=r))
     return out
 
 
@@ -83,6 +90,17 @@ def recorded(monkeypatch):
     return rec, cases
 
 
+def _shared_streams(rec, ignore=()):
+    by_seed = {}
+    for workload, seed, kind, draws, shape in rec.calls:
+        if workload in ignore:
+            continue
+        assert 0 <= seed < 2 ** 32, (workload, seed)
+        assert draws < 2 ** 32, (workload, seed, draws)
+        by_seed.setdefault(seed, set()).add((workload, kind, draws, shape))
+    return {s: v for s, v in by_seed.items() if len(v) > 1}
+
+
 def test_workload_streams_are_disjoint(recorded):
     """No two tensors of any workloads share a random stream.
 
@@ -92,13 +110,32 @@ def test_workload_streams_are_disjoint(recorded):
     GEMV rotation, the training set's A and B reused by dA and dB).
     """
     rec, _ = recorded
-    by_seed = {}
-    for workload, seed, kind, draws, shape in rec.calls:
-        assert 0 <= seed < 2 ** 32, (workload, seed)
-        assert draws < 2 ** 32, (workload, seed, draws)
-        by_seed.setdefault(seed, set()).add((workload, kind, draws, shape))
-    shared = {s: v for s, v in by_seed.items() if len(v) > 1}
+    shared = _shared_streams(rec)
     assert not shared, f"streams drawn by more than one tensor: {shared}"
+
+
+def test_replica_streams_are_disjoint(monkeypatch):
+    """Eight data-parallel replicas (one per GPU of a node, weak scaling) plus the
+    highest replica the seed layout holds draw no stream twice."""
+    rec = _Recorder()
+    rec.install(monkeypatch)
+    _all_workloads(rec, replicas=tuple(range(8)) + (synth.MAX_REPLICAS - 1,))
+    # the 64 x 768 MLP case is a parity case drawn once, outside the replicas
+    ignore = {f"gpt2_mlp_up@{r}" for r in range(1, synth.MAX_REPLICAS)}
+    shared = _shared_streams(rec, ignore)
+    assert not shared, f"streams drawn by more than one tensor: {shared}"
+
+
+@pytest.mark.parametrize("args", [(0, 1, 0, 0), (100, 1, 0, 0), (3, 0, 0, 0), (3, 1000, 0, 0),
+                                  (3, 1, -1, 0), (3, 1, 1000, 0), (3, 1, 0, -1), (3, 1, 0, synth.MAX_REPLICAS)])
+def test_seed_fields_range_checked(args):
+    with pytest.raises(ValueError):
+        synth._seed(*args)
+
+
+def test_seed_layout_largest_fits():
+    assert synth._seed(99, 999, 999, synth.MAX_REPLICAS - 1) < 2 ** 32
+    assert synth._seed(3, 1, 5, 0) == 3001005          # replica 0 keeps the single-GPU seeds
 
 
 def test_workload_stream_count(recorded):
@@ -115,6 +152,7 @@ def test_workload_stream_count(recorded):
     assert len(seeds[("ternary_encoder", "ternary")]) == 32
     assert len(seeds[("ternary_encoder", "normal16")]) == 32
     assert len(seeds[("training_set", "normal")]) == 3    # A, B, dC
+    assert len(seeds[("gpt2_mlp_bias", "normal")]) == 3   # X, W, bias
 
 
 def test_packed_workload_shapes(recorded):
@@ -164,6 +202,10 @@ def test_gemm_workload_layouts(recorded):
     assert [(c.transA, c.transB) for c in sq] == [(0, 0), (0, 1), (1, 0)]
     mlp = cases["gpt2_mlp_up"][0]
     assert (mlp.M, mlp.N, mlp.K, mlp.transA, mlp.transB) == (64, 3072, 768, 0, 0)
+    assert mlp.bias is None
+    lin = cases["gpt2_mlp_bias"][0]
+    assert (lin.M, lin.N, lin.K, lin.transA, lin.transB) == (8192, 3072, 768, 0, 0)
+    assert lin.bias.shape == (3072,) and lin.bias.dtype == np.float32
 
 
 # ---------------------------------------------------------------- real values
