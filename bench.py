@@ -267,10 +267,7 @@ class Workload:
                                       Y=torch.empty((c.X.shape[0], c.rows), dtype=torch.float32, device=device)))
         # training-shape set: forward C = A B, dA = dC B^T, dB = A^T dC (N(0, 0.02)), through the
         # split entry point with its automatic choice and one shared workspace
-        self.train = []
-        for which in ("fwd", "dA", "dB"):
-            c = synth.training_set_8192(which, replica=rep)
-            self.train.append(c)
+        self.train = list(synth.training_set_8192_all(replica=rep))
         tA = torch.from_numpy(self.train[0].A).to(device)
         tB = torch.from_numpy(self.train[0].B).to(device)
         tdC = torch.from_numpy(self.train[1].A).to(device)

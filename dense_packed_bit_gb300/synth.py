@@ -10,7 +10,11 @@ constants are Vigna's published ones).  Draw i of stream `seed` is
 ``mix(seed * 2**32 + i + 1)`` where ``mix`` is the SplitMix64 output function
 applied to ``state = counter * golden_gamma``.  It is written out here with
 numpy uint64 arithmetic (which wraps mod 2**64), so every machine and numpy
-version produces the same bits.
+version produces the same integer draws, hence the same codes, bytes and
+uniform values.  Normals pass through numpy's log and cos, whose last bit may
+differ between platforms before the rounding to fp32 / fp16; nothing stored
+depends on them, since every comparison recomputes its expected values from
+the inputs of the run.
 
 Value recipes (the shapes and distributions of the workloads on the pages):
   * uniform fp32 on [lo, hi): fp64 ``lo + (hi-lo)*u`` rounded to fp32 (RNE),
@@ -38,16 +42,37 @@ _M1 = np.uint64(0xBF58476D1CE4E5B9)
 _M2 = np.uint64(0x94D049BB133111EB)
 
 
+# Draws are made in chunks of this many numbers, so that the temporaries of each
+# elementwise step stay in the CPU's caches; every step is elementwise, so the
+# chunking changes no value.
+_CHUNK = 1 << 18
+
+
+def _splitmix64_into(seed: int, out: np.ndarray, offset: int = 0) -> None:
+    """Fill the 1-D uint64 array `out` with draws offset, offset+1, ... of stream `seed`."""
+    base = np.uint64((int(seed) << 32) & 0xFFFFFFFFFFFFFFFF)
+    tmp = np.empty(min(len(out), _CHUNK), dtype=np.uint64)
+    with np.errstate(over="ignore"):
+        for s in range(0, len(out), _CHUNK):
+            z = out[s:s + _CHUNK]
+            t = tmp[:len(z)]
+            np.add(np.arange(offset + s + 1, offset + s + len(z) + 1, dtype=np.uint64), base, out=z)
+            np.multiply(z, _GAMMA, out=z)
+            np.right_shift(z, np.uint64(30), out=t)
+            np.bitwise_xor(z, t, out=z)
+            np.multiply(z, _M1, out=z)
+            np.right_shift(z, np.uint64(27), out=t)
+            np.bitwise_xor(z, t, out=z)
+            np.multiply(z, _M2, out=z)
+            np.right_shift(z, np.uint64(31), out=t)
+            np.bitwise_xor(z, t, out=z)
+
+
 def _splitmix64(seed: int, n: int, offset: int = 0) -> np.ndarray:
     """n consecutive SplitMix64 outputs of stream `seed`, starting at draw `offset`."""
-    base = np.uint64((int(seed) << 32) & 0xFFFFFFFFFFFFFFFF)
-    ctr = np.arange(offset + 1, offset + n + 1, dtype=np.uint64) + base
-    with np.errstate(over="ignore"):
-        z = ctr * _GAMMA
-        z = (z ^ (z >> np.uint64(30))) * _M1
-        z = (z ^ (z >> np.uint64(27))) * _M2
-        z = z ^ (z >> np.uint64(31))
-    return z
+    out = np.empty(n, dtype=np.uint64)
+    _splitmix64_into(seed, out, offset)
+    return out
 
 
 def _unit_open0(z: np.ndarray) -> np.ndarray:
@@ -69,21 +94,34 @@ def uniform_f32(seed: int, shape, lo: float = -1.0, hi: float = 1.0) -> np.ndarr
     return v.reshape(shape)
 
 
+def _normal_into(seed: int, out: np.ndarray, sigma: float) -> None:
+    """Box-Muller normals (value i from draws 2i, 2i+1) rounded to out's dtype, chunk by chunk."""
+    z = np.empty(min(2 * len(out), 2 * _CHUNK), dtype=np.uint64)
+    for s in range(0, len(out), _CHUNK):
+        o = out[s:s + _CHUNK]
+        zc = z[:2 * len(o)]
+        _splitmix64_into(seed, zc, 2 * s)
+        u1 = _unit_open1(zc[0::2])
+        u2 = _unit_open0(zc[1::2])
+        o[:] = sigma * np.sqrt(-2.0 * np.log(u1)) * np.cos(2.0 * np.pi * u2)
+
+
 def normal_f64(seed: int, n: int, sigma: float = 1.0) -> np.ndarray:
-    z = _splitmix64(seed, 2 * n)
-    u1 = _unit_open1(z[0::2])
-    u2 = _unit_open0(z[1::2])
-    return sigma * np.sqrt(-2.0 * np.log(u1)) * np.cos(2.0 * np.pi * u2)
+    out = np.empty(n, dtype=np.float64)
+    _normal_into(seed, out, sigma)
+    return out
 
 
 def normal_f32(seed: int, shape, sigma: float = 1.0) -> np.ndarray:
-    n = int(np.prod(shape))
-    return normal_f64(seed, n, sigma).astype(np.float32).reshape(shape)
+    out = np.empty(int(np.prod(shape)), dtype=np.float32)
+    _normal_into(seed, out, sigma)
+    return out.reshape(shape)
 
 
 def normal_f16_bits(seed: int, shape, sigma: float = 1.0) -> np.ndarray:
-    n = int(np.prod(shape))
-    return normal_f64(seed, n, sigma).astype(np.float16).view(np.uint16).reshape(shape)
+    out = np.empty(int(np.prod(shape)), dtype=np.float16)
+    _normal_into(seed, out, sigma)
+    return out.view(np.uint16).reshape(shape)
 
 
 def uniform_f16_bits(seed: int, shape, lo: float, hi: float) -> np.ndarray:
@@ -99,10 +137,8 @@ def uniform_f16_bits(seed: int, shape, lo: float, hi: float) -> np.ndarray:
 def random_bytes(seed: int, n: int) -> np.ndarray:
     """n uniformly random bytes (8 per SplitMix64 draw, low byte first)."""
     words = _splitmix64(seed, (n + 7) // 8)
-    out = np.empty((len(words), 8), dtype=np.uint8)
-    for b in range(8):
-        out[:, b] = ((words >> np.uint64(8 * b)) & np.uint64(0xFF)).astype(np.uint8)
-    return out.reshape(-1)[:n].copy()
+    # the little-endian representation of a word lists its bytes low byte first
+    return words.astype("<u8", copy=False).view(np.uint8)[:n].copy()
 
 
 def ternary_field_bytes(seed: int, n: int) -> np.ndarray:
@@ -204,24 +240,43 @@ def gpt2_mlp_bias_gelu_8192x768x3072(replica: int = 0) -> GemmCase:
     return GemmCase("gpt2_mlp_up_bias_gelu_m8192_k768_n3072_nn", 0, 0, 8192, 3072, 768, X, W, bias)
 
 
+_TRAINING_PRODUCTS = {
+    # which: (name, transA, transB, M, N, K, stored A, stored B)
+    "fwd": ("train_fwd_8192x8192x2048_nn", 0, 0, 8192, 8192, 2048, "A", "B"),
+    "dA": ("train_dA_8192x2048x8192_nt", 0, 1, 8192, 2048, 8192, "dC", "B"),
+    "dB": ("train_dB_2048x8192x8192_tn", 1, 0, 2048, 8192, 8192, "A", "dC"),
+}
+_TRAINING_TENSORS = {"A": (1, (8192, 2048)), "B": (2, (2048, 8192)), "dC": (3, (8192, 8192))}
+
+
+def _training_tensor(name: str, replica: int) -> np.ndarray:
+    tensor_id, shape = _TRAINING_TENSORS[name]
+    return normal_f32(_seed(7, tensor_id, 0, replica), shape, 0.02)
+
+
 def training_set_8192(which: str, replica: int = 0) -> GemmCase:
     """Training-shape products (batch 16 x seq 512 = 8192 rows, d=2048, d_ff=8192).
 
     'fwd': C = A(8192x2048) B(2048x8192)            (NN)
     'dA' : dA = dC(8192x8192) B^T, B stored 2048x8192 (NT: M=8192,N=2048,K=8192)
     'dB' : dB = A^T dC, A stored 8192x2048            (TN: M=2048,N=8192,K=8192)
-    All operands N(0,0.02); A, B and dC each come from one fixed stream.
+    All operands N(0,0.02); A, B and dC each come from one fixed stream.  Only the
+    two tensors the product reads are drawn.
     """
-    A = normal_f32(_seed(7, 1, 0, replica), (8192, 2048), 0.02)
-    B = normal_f32(_seed(7, 2, 0, replica), (2048, 8192), 0.02)
-    if which == "fwd":
-        return GemmCase("train_fwd_8192x8192x2048_nn", 0, 0, 8192, 8192, 2048, A, B)
-    dC = normal_f32(_seed(7, 3, 0, replica), (8192, 8192), 0.02)
-    if which == "dA":
-        return GemmCase("train_dA_8192x2048x8192_nt", 0, 1, 8192, 2048, 8192, dC, B)
-    if which == "dB":
-        return GemmCase("train_dB_2048x8192x8192_tn", 1, 0, 2048, 8192, 8192, A, dC)
-    raise ValueError(which)
+    if which not in _TRAINING_PRODUCTS:
+        raise ValueError(which)
+    name, tA, tB, M, N, K, a, b = _TRAINING_PRODUCTS[which]
+    return GemmCase(name, tA, tB, M, N, K, _training_tensor(a, replica), _training_tensor(b, replica))
+
+
+def training_set_8192_all(replica: int = 0) -> tuple:
+    """The three products (fwd, dA, dB) of training_set_8192, sharing one draw of A, B and dC."""
+    t = {name: _training_tensor(name, replica) for name in _TRAINING_TENSORS}
+    out = []
+    for which in ("fwd", "dA", "dB"):
+        name, tA, tB, M, N, K, a, b = _TRAINING_PRODUCTS[which]
+        out.append(GemmCase(name, tA, tB, M, N, K, t[a], t[b]))
+    return tuple(out)
 
 
 @dataclass

@@ -20,7 +20,7 @@ class _Recorder:
 
     Generating the full-size workloads (the training set alone is 100 M values) would
     take far too long for a CPU test; the recipes' shapes and seeds are what is
-    checked, so zero-filled arrays of the right shape and dtype suffice.
+    checked, so read-only zero views of the right shape and dtype suffice.
     """
 
     def __init__(self):
@@ -30,7 +30,7 @@ class _Recorder:
         self.workload = None
 
     def _out(self, seed, kind, draws, shape, dtype):
-        a = np.zeros(shape, dtype=dtype)
+        a = np.broadcast_to(np.zeros((), dtype=dtype), shape)  # right shape, no memory
         self.calls.append((self.workload, int(seed), kind, int(draws), tuple(np.shape(a))))
         self.seed_of[id(a)] = int(seed)
         self._keep.append(a)
@@ -79,6 +79,7 @@ def _all_workloads(rec, replicas=(0,)):
                 run("ternary_encoder" + sfx, lambda: synth.ternary_encoder_layer(layer, proj, replica=r))
         for which in ("fwd", "dA", "dB"):
             run("training_set" + sfx, lambda: synth.training_set_8192(which, replica=r))
+        run("training_set_all" + sfx, lambda: synth.training_set_8192_all(replica=r))
     return out
 
 
@@ -95,6 +96,8 @@ def _shared_streams(rec, ignore=()):
     for workload, seed, kind, draws, shape in rec.calls:
         if workload in ignore:
             continue
+        # the bench's one-draw form of the training set is the same workload as its per-product form
+        workload = workload.replace("training_set_all", "training_set")
         assert 0 <= seed < 2 ** 32, (workload, seed)
         assert draws < 2 ** 32, (workload, seed, draws)
         by_seed.setdefault(seed, set()).add((workload, kind, draws, shape))
@@ -112,6 +115,23 @@ def test_workload_streams_are_disjoint(recorded):
     rec, _ = recorded
     shared = _shared_streams(rec)
     assert not shared, f"streams drawn by more than one tensor: {shared}"
+
+
+def test_training_set_all_shares_one_draw(recorded):
+    """The one-draw form hands out the same A, B and dC to the three products, and they are
+    the tensors the per-product form draws."""
+    rec, cases = recorded
+    fwd, dA, dB = cases["training_set_all"][0]
+    assert dA.B is fwd.B and dB.A is fwd.A and dA.A is dB.B
+    drawn = [c for c in rec.calls if c[0] == "training_set_all"]
+    assert len(drawn) == 3 and len({c[1] for c in drawn}) == 3
+    s = rec.seed_of
+    for one, per in zip((fwd, dA, dB), cases["training_set"]):
+        assert (one.name, one.transA, one.transB, one.M, one.N, one.K) == \
+            (per.name, per.transA, per.transB, per.M, per.N, per.K)
+        assert (s[id(one.A)], s[id(one.B)]) == (s[id(per.A)], s[id(per.B)])
+    per_product = [c for c in rec.calls if c[0] == "training_set"]
+    assert len(per_product) == 6                 # each product draws only the two tensors it reads
 
 
 def test_replica_streams_are_disjoint(monkeypatch):
@@ -294,6 +314,26 @@ def test_normal_recipe_moments():
     assert abs((z > 0).mean() - 0.5) < 6 * 0.5 / math.sqrt(n)
     # the sigma argument scales the same draws
     assert np.allclose(synth.normal_f64(11, 1000, 0.02), 0.02 * z[:1000], rtol=1e-15, atol=0)
+
+
+def test_normal_chunk_boundaries():
+    """Normal value i comes from draws 2i and 2i+1 of its stream, on both sides of the
+    generator's internal chunk boundaries, and the fp32 / fp16 forms are the fp64 value
+    rounded to nearest even."""
+    ch = synth._CHUNK
+    n = 2 * ch + 5
+    z = synth.normal_f64(21, n, 0.5)
+    for i in (0, 1, ch - 1, ch, ch + 1, 2 * ch, n - 1):
+        d = synth._splitmix64(21, 2, offset=2 * i)
+        u1 = (float(d[0] >> np.uint64(11)) + 1.0) * 2.0 ** -53
+        u2 = float(d[1] >> np.uint64(11)) * 2.0 ** -53
+        want = 0.5 * math.sqrt(-2.0 * math.log(u1)) * math.cos(2.0 * math.pi * u2)
+        assert abs(z[i] - want) <= 4e-16 * 3.0, (i, z[i], want)
+    assert np.array_equal(synth.normal_f32(21, (n,), 0.5), z.astype(np.float32))
+    assert np.array_equal(synth.normal_f16_bits(21, (n,), 0.5), z.astype(np.float16).view(np.uint16))
+    w = synth._splitmix64(8, n)
+    assert np.array_equal(w[ch - 2:ch + 2], synth._splitmix64(8, 4, offset=ch - 2))
+    assert synth._splitmix64(8, 0).shape == (0,) and synth.normal_f32(8, (0, 3)).shape == (0, 3)
 
 
 def test_streams_are_counter_windows():
