@@ -21,6 +21,7 @@ __all__ = [
     "mm_check_device_error", "mm_gemm_f32_splitk", "mm_gemm_f32_splitk_workspace", "mm_gemm_f32_splitk_noalloc",
     "MM_SPLITK_NOALLOC_MAX_FLOATS", "mm_gemm_f32_bias_act", "MM_ACT_NONE", "MM_ACT_GELU_TANH",
     "mm_gemv_packed2_strided_batched", "mm_gemm_f32_bias_act_splitk", "mm_gemm_f32_split_plan",
+    "mm_probe_bounded_wait",
     "MM_OK", "MM_ERR_INVALID_ARG", "MM_ERR_UNSUPPORTED", "MM_ERR_CUDA", "MM_ERR_TIMEOUT",
     "MM_GEMM_AUTO", "MM_GEMM_FFMA", "MM_GEMM_TF32X3",
     "MM_DEQ_AUTO", "MM_DEQ_SELECT", "MM_DEQ_AFFINE", "MM_DEQ_MMA", "MM_DEQ_FP8", "MM_DEQ_TC",
@@ -85,6 +86,7 @@ SIGNATURES = {
                                      _P], ctypes.c_int),
     "mm_gemv_packed2_strided_batched": ([_P, _I64, _P, _I64, _P, _I64, _P, _I64, _I64, _I64, _I64, _P, _P],
                                         ctypes.c_int),
+    "mm_probe_bounded_wait": ([_I, ctypes.c_uint64, _P, _P], ctypes.c_int),
 }
 
 
@@ -244,6 +246,12 @@ def mm_gemm_packed2_ex(codes, scales, X, Y, M, rows, cols, codebook, stream=None
 
 def mm_check_device_error(stream=None):
     _check(load_library().mm_check_device_error(_stream(stream)))
+
+
+def mm_probe_bounded_wait(arrive, limit_ns, out=None, stream=None):
+    """One bounded device wait that completes (arrive=1) or runs out after limit_ns (arrive=0);
+    out: None or a device int64 tensor of 2 receiving (completed, ns waited)."""
+    _check(load_library().mm_probe_bounded_wait(int(arrive), int(limit_ns), _ptr(out), _stream(stream)))
 
 
 def mm_gemv_packed4(codes, scales, x, y, rows, cols, codebook, stream=None):

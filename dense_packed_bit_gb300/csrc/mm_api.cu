@@ -650,6 +650,23 @@ mm_status mm_check_device_error(mm_stream_t stream) {
     const unsigned int u = mm::gemv_tc_take_device_error(&e);
     if (e != cudaSuccess) return cuda_fail(e, "mm_check_device_error");
     if (u != 0) return fail(MM_ERR_TIMEOUT, "a bounded device wait ran out in the tcgen05 GEMV (code %u)", u);
+    const unsigned int pr = mm::wait_probe_take_device_error(&e);
+    if (e != cudaSuccess) return cuda_fail(e, "mm_check_device_error");
+    if (pr != 0) return fail(MM_ERR_TIMEOUT, "the failure-detection probe's bounded wait ran out (code %u)", pr);
+    return ok();
+}
+
+mm_status mm_probe_bounded_wait(int arrive, uint64_t limit_ns, uint64_t *out, mm_stream_t stream) {
+    if (arrive != 0 && arrive != 1) return fail(MM_ERR_INVALID_ARG, "arrive must be 0 or 1");
+    if (limit_ns < 1000 || limit_ns > 100000000)
+        return fail(MM_ERR_INVALID_ARG, "limit_ns must be 1,000 .. 100,000,000 (1 us .. 0.1 s)");
+    if (out && (reinterpret_cast<uintptr_t>(out) & 7)) return fail(MM_ERR_INVALID_ARG, "out must be 8-byte aligned");
+    mm_status s = check_device();
+    if (s != MM_OK) return s;
+    cudaError_t e = mm::launch_wait_probe(arrive, (unsigned long long)limit_ns,
+                                          reinterpret_cast<unsigned long long *>(out),
+                                          reinterpret_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "wait probe launch");
     return ok();
 }
 

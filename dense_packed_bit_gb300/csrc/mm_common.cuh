@@ -21,7 +21,8 @@ enum : unsigned int {
     kDevErrWaitFull = 1,    // consumer wait for a filled pipeline stage ran out
     kDevErrWaitEmpty = 2,   // producer wait for a drained stage ran out
     kDevErrWaitMma = 3,     // wait for tensor-core completion ran out
-    kDevErrDrain = 4        // wait for in-flight copies after an error ran out
+    kDevErrDrain = 4,       // wait for in-flight copies after an error ran out
+    kDevErrProbe = 5        // the failure-detection probe's wait ran out (as asked)
 };
 
 __device__ __forceinline__ uint32_t smem_u32(const void *p) {
@@ -76,15 +77,20 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
 }
 
 // Wait until the barrier phase with the given parity completes, for at most
-// kWaitLimitNs.  Returns false when the limit ran out.
-__device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity) {
+// limit_ns.  Returns false when the limit ran out.
+__device__ __forceinline__ bool mbar_wait_limit(uint64_t *bar, uint32_t parity, unsigned long long limit_ns) {
     if (mbar_try_wait(bar, parity)) return true;
     const unsigned long long t0 = global_ns();
     while (true) {
         for (int i = 0; i < 64; ++i)
             if (mbar_try_wait(bar, parity)) return true;
-        if (global_ns() - t0 > kWaitLimitNs) return false;
+        if (global_ns() - t0 > limit_ns) return false;
     }
+}
+
+// mbar_wait_limit with the kernels' limit, kWaitLimitNs.
+__device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity) {
+    return mbar_wait_limit(bar, parity, kWaitLimitNs);
 }
 
 // try_wait that lets the hardware suspend the thread for up to `suspend_ns` while the

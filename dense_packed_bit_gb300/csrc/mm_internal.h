@@ -194,4 +194,9 @@ unsigned int gemm_ffma_take_device_error(cudaStream_t s, cudaError_t *err);
 unsigned int gemm_tf32x3_take_device_error(cudaError_t *err);
 unsigned int gemm_tf32x3_ws_take_device_error(cudaError_t *err);
 
+// Failure-detection probe (wait_probe.cu): one bounded mbarrier wait with a caller-chosen
+// limit, arriving first or never; out (device, may be null) receives {completed, ns waited}.
+cudaError_t launch_wait_probe(int arrive, unsigned long long limit_ns, unsigned long long *out, cudaStream_t s);
+unsigned int wait_probe_take_device_error(cudaError_t *err);
+
 }  // namespace mm

@@ -121,6 +121,25 @@ mm_status mm_gemm_packed2(const uint8_t *codes, const uint16_t *scales, const ui
 mm_status mm_check_device_error(mm_stream_t stream);
 
 /*
+ * Failure-detection probe: exercises the path by which a kernel's bounded
+ * device wait reports that it ran out, without breaking any computing kernel.
+ * One warp initialises an mbarrier expecting one arrival and waits on its first
+ * phase through the wait helper every pipelined kernel uses, with the limit
+ * limit_ns in place of the kernels' 2 s.  arrive = 1: the warp arrives first and
+ * the wait completes at once.  arrive = 0: nothing can complete the phase, so
+ * the wait runs out after limit_ns; the kernel records the timeout in its device
+ * error word and returns, and the next mm_check_device_error reports
+ * MM_ERR_TIMEOUT and clears the word.  The context stays usable.
+ * out: NULL, or 2 uint64 in device memory, 8-byte aligned, written by the kernel:
+ * out[0] = 1 if the wait completed, 0 if it ran out; out[1] = the nanoseconds it
+ * waited (%globaltimer).  limit_ns: 1,000 .. 100,000,000 (1 us .. 0.1 s).
+ * Asynchronous on `stream`.  Errors: MM_ERR_INVALID_ARG for arrive not 0 / 1, a
+ * limit out of range or a misaligned out; MM_ERR_UNSUPPORTED without an sm_103
+ * device; MM_ERR_CUDA if the launch fails.
+ */
+mm_status mm_probe_bounded_wait(int arrive, uint64_t limit_ns, uint64_t *out, mm_stream_t stream);
+
+/*
  * GPT-2's linear layer with its MLP activation fused into the GEMM epilogue:
  *     C = act(op(A) . op(B) + bias),   bias[n] added to column n of every row.
  * bias: N fp32 values in device memory, or NULL for none.  act: MM_ACT_NONE or

@@ -342,3 +342,12 @@ def test_gemm_split_plan_argument_errors(lib):
     assert lib.mm_gemm_f32_split_plan(0, 8, 8, 152, ctypes.byref(sk), ctypes.byref(fl)) == mm.MM_ERR_INVALID_ARG
     assert lib.mm_gemm_f32_split_plan(8, 8, 8, 1, ctypes.byref(sk), ctypes.byref(fl)) == mm.MM_ERR_INVALID_ARG
     assert lib.mm_gemm_f32_split_plan(8, 8, 8, 152, None, ctypes.byref(fl)) == mm.MM_ERR_INVALID_ARG
+
+
+@pytest.mark.parametrize("arrive,limit,out", [(2, 10000, None), (-1, 10000, None), (0, 999, None),
+                                              (0, 100000001, None), (1, 0, None), (0, 2 ** 63, None),
+                                              (0, 10000, FAKE + 4)])
+def test_probe_bounded_wait_argument_errors(lib, arrive, limit, out):
+    # arrive 0 / 1; limit 1 us .. 0.1 s, so the probe can never hold a GPU long; out 8-byte aligned
+    st = lib.mm_probe_bounded_wait(arrive, limit, out, None)
+    assert st == mm.MM_ERR_INVALID_ARG, lib.mm_last_error()
