@@ -216,11 +216,18 @@ class Workload:
         from dense_packed_bit_gb300 import synth
         self.dev = device
         rep = rank_replica(rank)
+        # SHA-256 of every workload's inputs as drawn (codes, scales, activations, operands), so
+        # that a change of the inputs shows in the report
+        sha = {k: synth.Digest() for k in ("square_2048", "gemv2_rotation64", "gemv4_rotation64",
+                                           "gemv2_t_rotation64", "ternary_encoder", "training_set",
+                                           "gpt2_mlp_bias_gelu")}
         self.gemm = []
         for layout in ("nn", "nt", "tn"):
             c = synth.square_2048(layout, replica=rep)
             A, B = c.A, c.B
-            self.gemm.append(dict(case=c, A=torch.from_numpy(A).to(device), B=torch.from_numpy(B).to(device),
+            sha["square_2048"].update(A, B)
+            self.gemm.append(dict(case=c, layout=layout, A=torch.from_numpy(A).to(device),
+                                  B=torch.from_numpy(B).to(device),
                                   C=torch.empty((c.M, c.N), dtype=torch.float32, device=device),
                                   hA=A, hB=B))
         # the rotation as one contiguous [64, 12288, 384] buffer: the per-call phases take views,
@@ -231,6 +238,7 @@ class Workload:
         x = None
         for i in range(N_GEMV):
             c = synth.gemv_2bit_12288x1536(i, replica=rep)
+            sha["gemv2_rotation64"].update(c.codes, c.scales)
             self.gemv_codes_all[i].copy_(torch.from_numpy(c.codes))
             self.gemv_scales_all[i].copy_(torch.from_numpy(c.scales.view("int16")))
             self.gemv_codes.append(self.gemv_codes_all[i])
@@ -238,29 +246,35 @@ class Workload:
             x = c.X
             self.gemv_cb = c.codebook
         self.gemv_yb = torch.empty((N_GEMV, 12288), dtype=torch.float32, device=device)
+        sha["gemv2_rotation64"].update(x)
         self.gemv_x = torch.from_numpy(x.reshape(-1)).to(device)
         self.gemv_y = torch.empty((N_GEMV, 12288), dtype=torch.float32, device=device)
         self.gemv4_codes, self.gemv4_scales = [], []
         for i in range(N_GEMV):
             c = synth.gemv_4bit_12288x1536(i, replica=rep)
+            sha["gemv4_rotation64"].update(c.codes, c.scales)
             self.gemv4_codes.append(torch.from_numpy(c.codes).to(device))
             self.gemv4_scales.append(torch.from_numpy(c.scales).to(device))
             x4 = c.X
             self.gemv4_cb = c.codebook
+        sha["gemv4_rotation64"].update(x4)
         self.gemv4_x = torch.from_numpy(x4.reshape(-1)).to(device)
         self.gemv4_y = torch.empty((N_GEMV, 12288), dtype=torch.float32, device=device)
         self.gemvt_codes, self.gemvt_scales = [], []
         for i in range(N_GEMV):
             c = synth.gemv_2bit_1536x12288(i, replica=rep)
+            sha["gemv2_t_rotation64"].update(c.codes, c.scales)
             self.gemvt_codes.append(torch.from_numpy(c.codes).to(device))
             self.gemvt_scales.append(torch.from_numpy(c.scales).to(device))
             xt = c.X
+        sha["gemv2_t_rotation64"].update(xt)
         self.gemvt_x = torch.from_numpy(xt.reshape(-1)).to(device)
         self.gemvt_y = torch.empty((N_GEMV, 1536), dtype=torch.float32, device=device)
         self.tern = []
         for layer in range(N_LAYERS):
             for proj in ("up", "down"):
                 c = synth.ternary_encoder_layer(layer, proj, replica=rep)
+                sha["ternary_encoder"].update(c.codes, c.scales, c.X)
                 self.tern.append(dict(case=c, codes=torch.from_numpy(c.codes).to(device),
                                       scales=torch.from_numpy(c.scales).to(device),
                                       X=torch.from_numpy(c.X).to(device),
@@ -268,6 +282,7 @@ class Workload:
         # training-shape set: forward C = A B, dA = dC B^T, dB = A^T dC (N(0, 0.02)), through the
         # split entry point with its automatic choice and one shared workspace
         self.train = list(synth.training_set_8192_all(replica=rep))
+        sha["training_set"].update(self.train[0].A, self.train[0].B, self.train[1].A)  # A, B, dC
         tA = torch.from_numpy(self.train[0].A).to(device)
         tB = torch.from_numpy(self.train[0].B).to(device)
         tdC = torch.from_numpy(self.train[1].A).to(device)
@@ -282,6 +297,8 @@ class Workload:
         self.train_ws_floats = need
         # GPT-2 small's MLP up-projection with its bias and GELU fused, 8 sequences of 1024 tokens
         mlp = synth.gpt2_mlp_bias_gelu_8192x768x3072(replica=rep)
+        sha["gpt2_mlp_bias_gelu"].update(mlp.A, mlp.B, mlp.bias)
+        self.inputs_sha256 = {k: d.hexdigest() for k, d in sha.items()}
         assert (mlp.M, mlp.N, mlp.K) == (MLP_M, MLP_N, MLP_K)
         self.mlp_x = torch.from_numpy(mlp.A).to(device)
         self.mlp_w = torch.from_numpy(mlp.B).to(device)
@@ -449,8 +466,29 @@ def e2e_gemm(w: Workload, steps: int, stream):
 
 # ---------------------------------------------------------------- CPU oracle baseline
 
-def cpu_oracle_sample(seconds_target: float = 15.0):
-    """Time the fp64 oracle on the 2048^3 NN/NT/TN products (all host cores)."""
+PARITY_TOL = 1e-5  # |C - C_exact| <= 1e-5 * sum_k |a_ik b_kj|, the bound of every GEMM parity test
+
+
+def parity_ratio(got, ref, T) -> float:
+    """max over outputs of |got - ref| / T, with T = sum_k |term_k| per output (inf for a
+    non-finite output, or for an error where T = 0)."""
+    got = np.asarray(got, dtype=np.float64)
+    ref = np.asarray(ref, dtype=np.float64)
+    T = np.asarray(T, dtype=np.float64)
+    if got.shape != ref.shape or not np.all(np.isfinite(got)):
+        return float("inf")
+    err = np.abs(got - ref)
+    with np.errstate(divide="ignore", invalid="ignore"):
+        r = np.where(T > 0, err / T, np.where(err > 0, np.inf, 0.0))
+    return float(r.max()) if r.size else 0.0
+
+
+def cpu_oracle_sample(seconds_target: float = 15.0, gpu_gemm=None):
+    """Time the fp64 oracle on the 2048^3 NN/NT/TN products (all host cores).
+
+    gpu_gemm: None, or {layout: the GPU's C for that product, on the host}; each is then
+    compared with the oracle's product, every output, and the worst |err| / sum|terms| is
+    reported beside the timing."""
     import oracle
     from dense_packed_bit_gb300 import synth
     oracle.build()
@@ -458,17 +496,26 @@ def cpu_oracle_sample(seconds_target: float = 15.0):
     flop = 0.0
     t0 = time.perf_counter()
     n_done = 0
+    parity = {}
     while True:
         for layout in ("nn", "nt", "tn"):
             c = synth.square_2048(layout)
-            oracle.gemm(c.transA, c.transB, c.M, c.N, c.K, c.A, c.B, threads=threads)
+            ref, T = oracle.gemm(c.transA, c.transB, c.M, c.N, c.K, c.A, c.B, threads=threads)
             flop += GEMM_FLOP
             n_done += 1
+            if gpu_gemm is not None and layout in gpu_gemm and layout not in parity:
+                parity[layout] = parity_ratio(gpu_gemm[layout], ref, T)
         if time.perf_counter() - t0 > seconds_target or n_done >= 6:
             break
     dt = time.perf_counter() - t0
-    return {"value": flop / dt / 1e12, "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
-            "sample": f"{n_done} full 2048^3 products (NN, NT, TN in turn), fp64 accumulation, {dt:.1f} s"}
+    out = {"value": flop / dt / 1e12, "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
+           "sample": f"{n_done} full 2048^3 products (NN, NT, TN in turn), fp64 accumulation, {dt:.1f} s"}
+    if gpu_gemm is not None:
+        out["parity"] = {"what": "max over all 2048^2 outputs of |C_gpu - C_oracle| / sum_k |a_ik b_kj|, "
+                                 "the bench's own products (mm_gemm_f32, the last e2e step)",
+                         "tol": PARITY_TOL, "square_2048": parity,
+                         "ok": bool(parity) and all(v <= PARITY_TOL for v in parity.values())}
+    return out
 
 
 # ---------------------------------------------------------------- main arms
@@ -682,7 +729,13 @@ def main_mm(args):
     if rank == 0:
         out["e2e"] = e2e_gemm(w, max(2, args.steps // 2), stream)
         if world == 1 and not args.no_cpu_baseline:
-            out["cpu_baseline"] = cpu_oracle_sample()
+            try:
+                gpu_gemm = {g["layout"]: g["C"].cpu().numpy() for g in w.gemm}
+            except Exception as e:  # the parity check is a report item: it must not cost the line
+                print(f"bench: GEMM outputs not read back for the parity check: {e}", file=sys.stderr)
+                gpu_gemm = None
+            out["cpu_baseline"] = cpu_oracle_sample(gpu_gemm=gpu_gemm)
+        out["inputs_sha256"] = w.inputs_sha256
         print(json.dumps(out), flush=True)
     return 0
 

@@ -155,15 +155,27 @@ def ternary_field_bytes(seed: int, n: int) -> np.ndarray:
     return out
 
 
+class Digest:
+    """SHA-256 over arrays given one at a time: each array's dtype, shape and raw bytes."""
+
+    def __init__(self):
+        self._h = hashlib.sha256()
+
+    def update(self, *arrays) -> "Digest":
+        for a in arrays:
+            a = np.ascontiguousarray(a)
+            self._h.update(str(a.dtype).encode())
+            self._h.update(str(a.shape).encode())
+            self._h.update(memoryview(a.reshape(-1)).cast("B"))  # the bytes, without a copy
+        return self
+
+    def hexdigest(self) -> str:
+        return self._h.hexdigest()
+
+
 def digest(*arrays) -> str:
     """SHA-256 over the raw bytes of the given arrays (detects silent input drift)."""
-    h = hashlib.sha256()
-    for a in arrays:
-        a = np.ascontiguousarray(a)
-        h.update(str(a.dtype).encode())
-        h.update(str(a.shape).encode())
-        h.update(a.tobytes())
-    return h.hexdigest()
+    return Digest().update(*arrays).hexdigest()
 
 
 # --------------------------------------------------------------------------
