@@ -469,6 +469,36 @@ def e2e_gemm(w: Workload, steps: int, stream):
 PARITY_TOL = 1e-5  # |C - C_exact| <= 1e-5 * sum_k |a_ik b_kj|, the bound of every GEMM parity test
 
 
+def cpu_model() -> str:
+    """The host CPU's model name (lscpu, else /proc/cpuinfo, else the machine type)."""
+    try:
+        r = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10)
+        for line in r.stdout.splitlines():
+            k, _, v = line.partition(":")
+            if k.strip() == "Model name" and v.strip():
+                return v.strip()
+    except (OSError, subprocess.SubprocessError):
+        pass
+    try:
+        with open("/proc/cpuinfo") as f:
+            for line in f:
+                k, _, v = line.partition(":")
+                if k.strip() in ("model name", "Model") and v.strip():
+                    return v.strip()
+    except OSError:
+        pass
+    import platform
+    return platform.machine() or "unknown"
+
+
+def phase_stats(times_ms) -> dict:
+    """Mean, median, min and max of one phase's per-step times (ms)."""
+    t = sorted(float(x) for x in times_ms)
+    if not t:
+        return {}
+    return {"ms_mean": sum(t) / len(t), "ms_median": statistics.median(t), "ms_min": t[0], "ms_max": t[-1]}
+
+
 def parity_ratio(got, ref, T) -> float:
     """max over outputs of |got - ref| / T, with T = sum_k |term_k| per output (inf for a
     non-finite output, or for an error where T = 0)."""
@@ -508,8 +538,17 @@ def cpu_oracle_sample(seconds_target: float = 15.0, gpu_gemm=None):
         if time.perf_counter() - t0 > seconds_target or n_done >= 6:
             break
     dt = time.perf_counter() - t0
+    # one core: the first 128 rows of the NN product
+    c = synth.square_2048("nn")
+    rows1 = min(128, c.M)
+    t1 = time.perf_counter()
+    oracle.gemm(c.transA, c.transB, rows1, c.N, c.K, c.A[:rows1], c.B, threads=1)
+    dt1 = time.perf_counter() - t1
     out = {"value": flop / dt / 1e12, "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
-           "sample": f"{n_done} full 2048^3 products (NN, NT, TN in turn), fp64 accumulation, {dt:.1f} s"}
+           "sample": f"{n_done} full 2048^3 products (NN, NT, TN in turn), fp64 accumulation, {dt:.1f} s",
+           "cpu_model": cpu_model(),
+           "value_1thread": 2.0 * rows1 * c.N * c.K / dt1 / 1e12,
+           "sample_1thread": f"the first {rows1} rows of the NN product on one core, {dt1:.2f} s"}
     if gpu_gemm is not None:
         out["parity"] = {"what": "max over all 2048^2 outputs of |C_gpu - C_oracle| / sum_k |a_ik b_kj|, "
                                  "the bench's own products (mm_gemm_f32, the last e2e step)",
@@ -603,6 +642,9 @@ def main_mm(args):
 
     def total_s(name):
         return reduce_max(sum(ev[name][0].elapsed_time(ev[name][1]) for ev in ev_steps) / 1e3, dev)
+
+    # per-phase spread over the timed steps on this rank (the headline figures use the totals)
+    phases = {name: phase_stats([ev[name][0].elapsed_time(ev[name][1]) for ev in ev_steps]) for name in PHASES}
 
     gemm_total_s = total_s("gemm")
     gemv_total_s = total_s("gemv")
@@ -722,6 +764,7 @@ def main_mm(args):
                         "shape": f"{MLP_M}x{MLP_N}x{MLP_K} NN (8 x 1024 tokens, 768 -> 3072), N(0,1) x N(0,0.02)",
                         "path": "mm_gemm_f32_bias_act_splitk, automatic split (stream-K: 384 pair tiles on 76 pairs)"},
         "roofline": roof,
+        "phases": phases,
         "clocks": clk,
         "gpu_launches": LAUNCHES_PER_STEP * args.steps,
         "wall_s": wall,

@@ -66,3 +66,21 @@ def test_digest_incremental_equals_whole():
     assert synth.Digest().update(a).update(b).hexdigest() == synth.digest(a, b)
     assert synth.digest(a, b) != synth.digest(b, a)
     assert synth.digest(a) != synth.digest(a.reshape(5, 4))          # the shape is hashed too
+
+
+def test_phase_stats():
+    st = bench.phase_stats([3.0, 1.0, 2.0, 10.0])
+    assert st == {"ms_mean": 4.0, "ms_median": 2.5, "ms_min": 1.0, "ms_max": 10.0}
+    assert bench.phase_stats([]) == {}
+
+
+def test_cpu_model_is_a_string():
+    m = bench.cpu_model()
+    assert isinstance(m, str) and m
+
+
+def test_cpu_baseline_one_core_figure(monkeypatch):
+    monkeypatch.setattr(synth, "square_2048", _small_square)
+    res = bench.cpu_oracle_sample(seconds_target=0.0)
+    assert res["value_1thread"] > 0 and "one core" in res["sample_1thread"]
+    assert isinstance(res["cpu_model"], str)
