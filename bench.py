@@ -595,7 +595,8 @@ def main_reference(args):
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt / args.steps * 1e3,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
         "config": {"workload": "square_2048_fp32_gemm_nn_nt_tn (row sample)", "rows_per_product": rows},
-        "cpu_baseline": {"value": val, "unit": "TFLOP/s", "cores": threads, "kind": "oracle", "sample": sample},
+        "cpu_baseline": {"value": val, "unit": "TFLOP/s", "cores": threads, "kind": "oracle", "sample": sample,
+                         "cpu_model": cpu_model()},
         "e2e": {"value": val, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }), flush=True)
     return 0

@@ -84,3 +84,10 @@ def test_cpu_baseline_one_core_figure(monkeypatch):
     res = bench.cpu_oracle_sample(seconds_target=0.0)
     assert res["value_1thread"] > 0 and "one core" in res["sample_1thread"]
     assert isinstance(res["cpu_model"], str)
+
+
+def test_rank_replica_bounds():
+    assert [bench.rank_replica(r) for r in range(8)] == list(range(8))
+    for bad in (-1, synth.MAX_REPLICAS):
+        with pytest.raises(ValueError):
+            bench.rank_replica(bad)
