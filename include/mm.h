@@ -189,9 +189,9 @@ mm_status mm_gemm_f32_bias_act_splitk(int transA, int transB, int64_t M, int64_t
  * (splitk * M * N for slices; one 128 x 256 partial tile per CTA plus a flag
  * word for stream-K; 0 when the split resolves to 1, and NULL is then
  * accepted).  It must not overlap A, B or C; its contents on entry do not
- * matter.  Calls sharing one workspace must not overlap on the GPU.  Operands TMA cannot describe (A or B not 16-byte aligned, lda
- * or ldb not a multiple of 4) run the unsplit general kernel and leave the
- * workspace untouched.
+ * matter.  Calls sharing one workspace must not overlap on the GPU.  Operands
+ * TMA cannot describe (A or B not 16-byte aligned, lda or ldb not a multiple
+ * of 4) run the unsplit general kernel and leave the workspace untouched.
  * Errors: as mm_gemm_f32, plus MM_ERR_INVALID_ARG for splitk outside -1..16, a
  * misaligned, overlapping or too small workspace.
  */
