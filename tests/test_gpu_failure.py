@@ -63,6 +63,7 @@ def test_timeout_on_a_side_stream():
     import torch
     s = torch.cuda.Stream()
     out = _out()
+    s.wait_stream(torch.cuda.current_stream())  # the fill of `out` comes before the probe's write
     with torch.cuda.stream(s):
         mm.mm_probe_bounded_wait(0, MS, out, stream=s)
     _timeout_reported(stream=s)
