@@ -61,6 +61,22 @@ def test_cpu_baseline_reports_parity_of_given_outputs(monkeypatch):
     assert "parity" not in bench.cpu_oracle_sample(seconds_target=0.0)
 
 
+def test_cpu_baseline_sample_is_bounded(monkeypatch):
+    # with no time bound reached, the sample stops at its product cap, in whole NN/NT/TN rounds,
+    # and draws each product's inputs once (before timing), not once per product
+    drawn = []
+
+    def counting(layout, replica=0):
+        drawn.append(layout)
+        return _small_square(layout, replica)
+
+    monkeypatch.setattr(synth, "square_2048", counting)
+    res = bench.cpu_oracle_sample(seconds_target=1e9)
+    assert bench.CPU_SAMPLE_MAX_PRODUCTS % 3 == 0
+    assert res["sample"].startswith(f"{bench.CPU_SAMPLE_MAX_PRODUCTS} full")
+    assert sorted(drawn) == ["nn", "nt", "tn"]
+
+
 def test_digest_incremental_equals_whole():
     a, b = synth.uniform_f32(3, (4, 5)), synth.random_bytes(4, 33)
     assert synth.Digest().update(a).update(b).hexdigest() == synth.digest(a, b)
