@@ -228,8 +228,10 @@ mm_status mm_gemm_f32_splitk(int transA, int transB, int64_t M, int64_t N, int64
  * that would need more is replaced by no split.  splitk = -1 is refused.  The first call on a
  * device looks up the array's device address (cudaGetSymbolAddress, with that
  * device current); make that first call before any stream capture.  Every call
- * shares the one array and leaves its partial tiles there; no part of it has to
- * start at zero (each call writes all it reads).  Calls whose kernels overlap on
+ * shares the one array and leaves its partial tiles there.  The caller clears
+ * nothing: a call writes every partial tile before reading it, and when the
+ * automatic split is stream-K the call itself zeroes (cudaMemsetAsync on
+ * `stream`) the hand-over flags it keeps in the array.  Calls whose kernels overlap on
  * the GPU (on different streams, or from different threads) race on the array
  * and may return wrong results: serialise them.
  */
