@@ -4,13 +4,16 @@
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl mm|reference]
 
 Prints ONE JSON line (rank 0).  One step is one pass of the whole hot path:
+  0. the GPT-2-small MLP up-projection at 64 tokens, 64 x 768 x 3072 fp32 NN,
+     one mm_gemm_f32 call with L2 flushed before it;
   1. square 2048^3 fp32 GEMM in the NN, NT and TN layouts (L2 flushed first
      by writing a 512 MiB buffer, since the 48 MiB of operands fit in L2);
   2. the 2-bit 12,288 x 1,536 GEMV over a rotation of 64 distinct matrices
      (288 MiB of codes, larger than the 129 MB L2), back to back, twice: as 64
      independent calls (programmatic dependent launch, no call waits for the
-     previous one) and as a dependent chain (each call waits for the previous
-     kernel before reading x; only its weight loads start early);
+     previous one) and as a dependent chain (call i+1 reads as its x the first
+     3 KB that call i wrote, so it waits for call i before reading x; only its
+     weight loads start early);
   3. the ternary 16-layer encoder block: 16 x (222x768 -> 3072, 222x3072 -> 768);
   4. the 4-bit 12,288 x 1,536 GEMV and the transposed 2-bit 1,536 x 12,288 GEMV,
      each over a 64-matrix rotation of independent calls;
@@ -56,10 +59,13 @@ GEMM_FLOP = 2.0 * 2048 ** 3
 TRAIN_FLOP = 3 * 2.0 * 8192 * 8192 * 2048  # forward + the two backward products, 274.9 GFLOP each
 MLP_M, MLP_N, MLP_K = 8192, 3072, 768  # GPT-2 small MLP up-projection, 8 x 1024 tokens
 MLP_FLOP = 2.0 * MLP_M * MLP_N * MLP_K  # 38.7 GFLOP (the bias and GELU are O(MN), not counted)
+C1_M, C1_N, C1_K = 64, 3072, 768  # GPT-2 small MLP up-projection at 64 tokens, one call
+C1_FLOP = 2.0 * C1_M * C1_N * C1_K  # 302 MFLOP
+C1_BYTES = 4 * (C1_M * C1_K + C1_K * C1_N + C1_M * C1_N)  # 10.42 MB: A and B read once, C written
 TERN_FLOP_PER_LAYER = 2 * (2.0 * 222 * 3072 * 768)
 N_GEMV = 64
 N_LAYERS = 16
-WORKLOAD = ("square_2048_fp32_gemm_nn_nt_tn + gemv2bit_12288x1536_rotation64 + "
+WORKLOAD = ("gpt2_mlp_up_64x768x3072_fp32_nn + square_2048_fp32_gemm_nn_nt_tn + gemv2bit_12288x1536_rotation64 + "
             "ternary_encoder_16x(222x768x3072,222x3072x768) + gemv4bit_12288x1536_rotation64 + "
             "gemv2bit_1536x12288_rotation64 + training_set_8192x2048x8192_fwd_dA_dB")
 
@@ -218,9 +224,14 @@ class Workload:
         rep = rank_replica(rank)
         # SHA-256 of every workload's inputs as drawn (codes, scales, activations, operands), so
         # that a change of the inputs shows in the report
-        sha = {k: synth.Digest() for k in ("square_2048", "gemv2_rotation64", "gemv4_rotation64",
+        sha = {k: synth.Digest() for k in ("gpt2_mlp_up_64", "square_2048", "gemv2_rotation64", "gemv4_rotation64",
                                            "gemv2_t_rotation64", "ternary_encoder", "training_set",
                                            "gpt2_mlp_bias_gelu")}
+        c1 = synth.gpt2_mlp_up_64x768x3072(replica=rep)
+        assert (c1.M, c1.N, c1.K) == (C1_M, C1_N, C1_K)
+        sha["gpt2_mlp_up_64"].update(c1.A, c1.B)
+        self.c1 = dict(case=c1, A=torch.from_numpy(c1.A).to(device), B=torch.from_numpy(c1.B).to(device),
+                       C=torch.empty((C1_M, C1_N), dtype=torch.float32, device=device))
         self.gemm = []
         for layout in ("nn", "nt", "tn"):
             c = synth.square_2048(layout, replica=rep)
@@ -249,6 +260,7 @@ class Workload:
         sha["gemv2_rotation64"].update(x)
         self.gemv_x = torch.from_numpy(x.reshape(-1)).to(device)
         self.gemv_y = torch.empty((N_GEMV, 12288), dtype=torch.float32, device=device)
+        self.gemv_yc = torch.zeros((N_GEMV, 12288), dtype=torch.float32, device=device)  # the chain's outputs
         self.gemv4_codes, self.gemv4_scales = [], []
         for i in range(N_GEMV):
             c = synth.gemv_4bit_12288x1536(i, replica=rep)
@@ -300,6 +312,7 @@ class Workload:
         sha["gpt2_mlp_bias_gelu"].update(mlp.A, mlp.B, mlp.bias)
         self.inputs_sha256 = {k: d.hexdigest() for k, d in sha.items()}
         assert (mlp.M, mlp.N, mlp.K) == (MLP_M, MLP_N, MLP_K)
+        self.mlp_case = mlp
         self.mlp_x = torch.from_numpy(mlp.A).to(device)
         self.mlp_w = torch.from_numpy(mlp.B).to(device)
         self.mlp_b = torch.from_numpy(mlp.bias).to(device)
@@ -357,6 +370,18 @@ def capture_phases(w: Workload, stream):
                 cur.wait_stream(side)
         return f
 
+    def gemv_chain():
+        # a dependent chain: call 0 reads the workload's x, call i+1 reads as its 1,536 fp16
+        # activations the first 3,072 bytes (768 fp32 outputs) that call i wrote
+        for i in range(N_GEMV):
+            x = w.gemv_x if i == 0 else w.gemv_yc[i - 1][:768].view(torch.int16)
+            mm.mm_gemv_packed2_ex(w.gemv_codes[i], w.gemv_scales[i], x, w.gemv_yc[i], 12288, 1536, w.gemv_cb,
+                                  **GEMV_CHAINED)
+
+    def c1():
+        g = w.c1
+        mm.mm_gemm_f32(0, 0, C1_M, C1_N, C1_K, g["A"], C1_K, g["B"], C1_N, g["C"], C1_N)
+
     def gemv_batched():
         mm.mm_gemv_packed2_strided_batched(w.gemv_codes_all, 12288 * 384, w.gemv_scales_all, 12288, w.gemv_x, 0,
                                            w.gemv_yb, 12288, N_GEMV, 12288, 1536, w.gemv_cb)
@@ -395,7 +420,7 @@ def capture_phases(w: Workload, stream):
                                   **TERN_OPTS)
 
     graphs = {}
-    for name, fn in (("gemm", gemm), ("gemv", gemv(GEMV_INDEP, GEMV_INDEP_STREAMS)), ("gemv_c", gemv(GEMV_CHAINED)),
+    for name, fn in (("c1", c1), ("gemm", gemm), ("gemv", gemv(GEMV_INDEP, GEMV_INDEP_STREAMS)), ("gemv_c", gemv_chain),
                      ("tern", tern), ("gemv4", gemv4), ("gemvt", gemvt), ("train", train), ("mlp", mlp),
                      ("gemv_b", gemv_batched)):
         with torch.cuda.stream(stream):
@@ -408,16 +433,18 @@ def capture_phases(w: Workload, stream):
     return graphs
 
 
-LAUNCHES_PER_STEP = 3 + 4 * N_GEMV + 2 * N_LAYERS + 3 + 1 + 1  # + training set, MLP GEMM, batched GEMV
+LAUNCHES_PER_STEP = 1 + 3 + 4 * N_GEMV + 2 * N_LAYERS + 3 + 1 + 1  # C1, 2048^3, GEMVs, encoder, training set, MLP, batched
 
 
-PHASES = ("gemm", "gemv", "gemv_c", "tern", "gemv4", "gemvt", "train", "mlp", "gemv_b")
+PHASES = ("c1", "gemm", "gemv", "gemv_c", "tern", "gemv4", "gemvt", "train", "mlp", "gemv_b")
+L2_COLD = ("c1", "gemm")  # phases whose operands fit in L2: a 512 MiB write evicts them first
 
 
 def run_step(w: Workload, graphs, ev, stream):
     """One pass of the hot path; ev maps each phase to a (start, end) event pair."""
-    w.flush.fill_(1.0)  # evict the GEMM operands from L2 (torch kernel, outside the events)
     for name in PHASES:
+        if name in L2_COLD:
+            w.flush.fill_(1.0)  # evict the operands from L2 (torch kernel, outside the events)
         ev[name][0].record(stream)
         graphs[name].replay()
         ev[name][1].record(stream)
@@ -560,6 +587,118 @@ def cpu_oracle_sample(seconds_target: float = 15.0, gpu_gemm=None):
     return out
 
 
+def _sample_coords(rng, M, N, n_lines=2, n_random=2000):
+    """Whole first / last / random rows and columns plus random outputs of an M x N result."""
+    rows = [0, M - 1] + [int(v) for v in rng.integers(0, M, n_lines)]
+    cols = [0, N - 1] + [int(v) for v in rng.integers(0, N, n_lines)]
+    ii = np.concatenate([np.repeat(rows, N), np.tile(np.arange(M), len(cols)), rng.integers(0, M, n_random)])
+    jj = np.concatenate([np.tile(np.arange(N), len(rows)), np.repeat(cols, M), rng.integers(0, N, n_random)])
+    return ii, jj
+
+
+def bench_parity(w) -> dict:
+    """The outputs the timed phases left on the GPU (the last replay of each), compared with the
+    fp64 oracle on the host: worst |y - y_ref| / sum_k |term_k| per workload, against 1e-5.
+
+    c1, gemv (64 independent calls), gemv_b (the batched launch), gemv4, gemv_t: every output.
+    gemv_c (the dependent chain): call 0 on the workload's x, and each later call whose x, the
+    bits of the previous call's first 768 outputs read as fp16, holds only finite values.
+    ternary: every output of layers 0 and 15, 2,000 sampled outputs of the other products.
+    training_set: 4 whole rows and 4 whole columns and 2,000 random outputs per product.
+    gpt2_mlp_up (bias + GELU): the first and last 64 rows, against its own bound
+    1.13e-5 T + 2^-20 (1 + |z|), reported as a fraction of that bound.
+    """
+    import oracle
+    oracle.build()
+    rng = np.random.default_rng(2026)
+    out = {}
+    t0 = time.perf_counter()
+    c = w.c1["case"]
+    ref, T = oracle.gemm(c.transA, c.transB, c.M, c.N, c.K, c.A, c.B)
+    out["gpt2_mlp_up_64"] = {"worst": parity_ratio(w.c1["C"].cpu().numpy(), ref, T), "outputs": ref.size}
+
+    codes = w.gemv_codes_all.cpu().numpy()
+    scales = w.gemv_scales_all.cpu().numpy().view(np.uint16)
+    x = w.gemv_x.cpu().numpy().view(np.uint16)
+    y, yb, yc = w.gemv_y.cpu().numpy(), w.gemv_yb.cpu().numpy(), w.gemv_yc.cpu().numpy()
+    worst = worst_b = 0.0
+    chain_worst, chain_checked = 0.0, 0
+    for i in range(N_GEMV):
+        ref, T = oracle.packed_gemm(codes[i], scales[i], x, 12288, 1536, w.gemv_cb)
+        worst = max(worst, parity_ratio(y[i], ref[0], T[0]))
+        worst_b = max(worst_b, parity_ratio(yb[i], ref[0], T[0]))
+        xi = x if i == 0 else yc[i - 1][:768].view(np.uint16)
+        if i == 0:
+            chain_worst, chain_checked = parity_ratio(yc[0], ref[0], T[0]), 1
+        elif np.all(np.isfinite(xi.view(np.float16))):
+            rc, Tc = oracle.packed_gemm(codes[i], scales[i], xi, 12288, 1536, w.gemv_cb)
+            chain_worst = max(chain_worst, parity_ratio(yc[i], rc[0], Tc[0]))
+            chain_checked += 1
+    out["gemv2_rotation64"] = {"worst": worst, "outputs": N_GEMV * 12288}
+    out["gemv2_batched"] = {"worst": worst_b, "outputs": N_GEMV * 12288}
+    out["gemv2_chain"] = {"worst": chain_worst, "calls_checked": chain_checked,
+                          "note": "later calls read the previous call's fp32 bits as fp16; calls whose x "
+                                  "holds inf or NaN patterns are not compared"}
+
+    worst = 0.0
+    x4 = w.gemv4_x.cpu().numpy().view(np.uint16)
+    y4 = w.gemv4_y.cpu().numpy()
+    for i in range(N_GEMV):
+        ref, T = oracle.packed4_gemm(w.gemv4_codes[i].cpu().numpy(), w.gemv4_scales[i].cpu().numpy().view(np.uint16),
+                                     x4, 12288, 1536, w.gemv4_cb)
+        worst = max(worst, parity_ratio(y4[i], ref[0], T[0]))
+    out["gemv4_rotation64"] = {"worst": worst, "outputs": N_GEMV * 12288}
+
+    worst = 0.0
+    xt = w.gemvt_x.cpu().numpy().view(np.uint16)
+    yt = w.gemvt_y.cpu().numpy()
+    for i in range(N_GEMV):
+        ref, T = oracle.packed_gemm(w.gemvt_codes[i].cpu().numpy(), w.gemvt_scales[i].cpu().numpy().view(np.uint16),
+                                    xt, 1536, 12288, w.gemv_cb)
+        worst = max(worst, parity_ratio(yt[i], ref[0], T[0]))
+    out["gemv2_t_rotation64"] = {"worst": worst, "outputs": N_GEMV * 1536}
+
+    worst, n_out = 0.0, 0
+    for j, t in enumerate(w.tern):
+        c = t["case"]
+        Y = t["Y"].cpu().numpy()
+        if j // 2 in (0, N_LAYERS - 1):
+            ref, T = oracle.packed_gemm(c.codes, c.scales, c.X, c.rows, c.cols, c.codebook)
+            worst = max(worst, parity_ratio(Y, ref, T))
+            n_out += Y.size
+        else:
+            mi = rng.integers(0, Y.shape[0], 2000)
+            ri = rng.integers(0, Y.shape[1], 2000)
+            ref, T = oracle.packed_gemm_at(c.codes, c.scales, c.X, c.cols, c.codebook, mi, ri)
+            worst = max(worst, parity_ratio(Y[mi, ri], ref, T))
+            n_out += len(mi)
+    out["ternary_encoder"] = {"worst": worst, "outputs": n_out}
+
+    worst, n_out = 0.0, 0
+    for c, _, _, o in w.train_ops:
+        ii, jj = _sample_coords(rng, c.M, c.N)
+        ref, T = oracle.gemm_at(c.transA, c.transB, c.K, c.A, c.B, ii, jj)
+        C = o.cpu().numpy()
+        worst = max(worst, parity_ratio(C[ii, jj], ref, T))
+        n_out += len(ii)
+    out["training_set"] = {"worst": worst, "outputs": n_out}
+
+    # bias + GELU: its bound is 1.13e-5 T + 2^-20 (1 + |z|); the ratio is err / that bound, scaled by
+    # 1e-5 so that it compares with the same tolerance as the others
+    mlp = w.mlp_case
+    Ym = w.mlp_y.cpu().numpy()
+    worst = 0.0
+    for r0 in (0, MLP_M - 64):
+        ref, T, Z = oracle.gemm_bias_act(0, 0, 64, MLP_N, MLP_K, mlp.A[r0:r0 + 64], mlp.B, mlp.bias, 1)
+        bound = 1.13 * T + 2.0 ** -20 * (1.0 + np.abs(Z)) / PARITY_TOL
+        worst = max(worst, parity_ratio(Ym[r0:r0 + 64], ref, bound))
+    out["gpt2_mlp_up_bias_gelu"] = {"worst": worst, "outputs": 128 * MLP_N,
+                                    "note": "|err| / (1.13 T + 2^-20 (1 + |z|) / 1e-5)"}
+    ok = all(v["worst"] <= PARITY_TOL for v in out.values())
+    return {"what": "max |y_gpu - y_oracle| / sum_k |term_k| over the outputs the timed phases left, per workload",
+            "tol": PARITY_TOL, "ok": bool(ok), "workloads": out, "seconds": time.perf_counter() - t0}
+
+
 # ---------------------------------------------------------------- main arms
 
 def main_reference(args):
@@ -651,6 +790,7 @@ def main_mm(args):
     # per-phase spread over the timed steps on this rank (the headline figures use the totals)
     phases = {name: phase_stats([ev[name][0].elapsed_time(ev[name][1]) for ev in ev_steps]) for name in PHASES}
 
+    c1_total_s = total_s("c1")
     gemm_total_s = total_s("gemm")
     gemv_total_s = total_s("gemv")
     gemvc_total_s = total_s("gemv_c")
@@ -670,7 +810,7 @@ def main_mm(args):
     tern_tflops = world * N_LAYERS * TERN_FLOP_PER_LAYER * args.steps / tern_total_s / 1e12
     per_call_gemv4_s = gemv4_total_s / (args.steps * N_GEMV)
     per_call_gemvt_s = gemvt_total_s / (args.steps * N_GEMV)
-    step_ms = (gemm_total_s + gemv_total_s + gemvc_total_s + tern_total_s + gemv4_total_s + gemvt_total_s +
+    step_ms = (c1_total_s + gemm_total_s + gemv_total_s + gemvc_total_s + tern_total_s + gemv4_total_s + gemvt_total_s +
                train_total_s + mlp_total_s + gemvb_total_s) / args.steps * 1e3
 
     peaks, peaks_src = measured_peaks()
@@ -687,6 +827,14 @@ def main_mm(args):
                 "peak_source": (f"{peaks_src} bf16 burst {peaks['bf16_tflops']:.0f} TFLOP/s x nominal tf32/bf16 "
                                 f"ratio 1.1/2.25, divided by the 3 MMAs of the split"),
                 "frac_of_fp32_simt_peak": gemm_per_gpu / fp32_peak_max}
+        if clk.get("sm_mhz"):
+            # the tensor peak scales with the SM clock: the measured bf16 burst ran at the clock
+            # MEASURED_PEAKS records under load, this kernel at the clock sampled during the run
+            ref_mhz = peaks.get("clocks_under_load", {}).get("sm_mhz_median") or peaks.get("sm_max_mhz", 2070.0)
+            roof["frac_at_sampled_clock"] = gemm_per_gpu / (tf32_peak / 3.0 * clk["sm_mhz"] / ref_mhz)
+            roof["sampled_clock_note"] = (f"peak rescaled from the {ref_mhz:.0f} MHz of the bf16 measurement to the "
+                                          f"{clk['sm_mhz']:.0f} MHz sampled here")
+        roof["ncu_tensor_active"] = "85.4% of cycles on the SMs holding a tile (profiles/gemm_tf32x3_ws_pair_square2048_nn.md)"
     else:
         roof = {"bound": "alu", "achieved": gemm_per_gpu, "peak": fp32_peak_max, "unit": "TFLOP/s",
                 "frac": gemm_per_gpu / fp32_peak_max, "traffic": traffic_for("gemm_ffma"),
@@ -699,17 +847,30 @@ def main_mm(args):
         "metric": METRIC, "value": gemm_tflops, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
         "warmup": max(3, args.warmup), "ms_per_step": step_ms, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f32", "data": "synthetic",
-        "config": {"workload": WORKLOAD, "gemm": "2048x2048x2048 fp32 NN+NT+TN, N(0,0.02)",
+        "config": {"workload": WORKLOAD, "gpt2_mlp_up_64": "64x768x3072 fp32 NN, U[-1,1), one mm_gemm_f32 call",
+                   "gemm": "2048x2048x2048 fp32 NN+NT+TN, N(0,0.02)",
                    "gemv": "12288x1536 2-bit, 64-matrix rotation (288 MiB > L2), codebook {-2,-1,0,1}",
                    "ternary": "16 layers, M=222, up 768->3072 and down 3072->768, a dependent chain with PDL",
                    "gemv_t": "1536x12288 2-bit, 64-matrix rotation (288 MiB > L2)",
                    "training_set": "8192x8192x2048 NN, dA=dC.B^T 8192x2048x8192, dB=A^T.dC 2048x8192x8192, N(0,0.02)",
-                   "l2": "512 MiB buffer written before the GEMM phase of every step; GEMV inputs exceed L2",
+                   "l2": "512 MiB buffer written before the 64x768x3072 and the 2048^3 phases of every step; "
+                         "GEMV rotations exceed L2",
                    "gemv_opts": {"independent": GEMV_INDEP, "independent_streams": GEMV_INDEP_STREAMS,
-                                 "chained": GEMV_CHAINED},
+                                 "chained": GEMV_CHAINED,
+                                 "chain": "call i+1 reads as x the first 768 fp32 outputs of call i, as fp16 bits"},
                    "launch": "each phase replayed as a CUDA graph",
                    "gemm_path": args.gemm_path, "parallelism": f"replicas x{world}"},
         "gemm_ms_per_step": gemm_total_s / args.steps * 1e3,
+        "gpt2_mlp_up_64": {"metric": "fp32 GEMM TFLOP/s, 64 x 768 x 3072 NN (one mm_gemm_f32 call, L2 flushed)",
+                           "value": world * C1_FLOP * args.steps / c1_total_s / 1e12, "unit": "TFLOP/s",
+                           "us_per_call": c1_total_s / args.steps * 1e6,
+                           "roofline": {"bound": "hbm", "achieved": C1_BYTES / (c1_total_s / args.steps) / 1e9,
+                                        "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                                        "frac": C1_BYTES / (c1_total_s / args.steps) / 1e9 / peaks["hbm_gbs"],
+                                        "floor_us": C1_BYTES / peaks["hbm_gbs"] / 1e3, "traffic": None,
+                                        "peak_source": peaks_src,
+                                        "note": "302 MFLOP over 10.42 MB (A, B read once, C written): 29 flop per "
+                                                "byte, below the 3xTF32 ridge, so HBM bounds it"}},
         "gemv": {"metric": "2-bit 12288x1536 GEMV weight GB/s", "value": gemv_gbs, "unit": "GB/s",
                  "us_per_call": per_call_gemv_s * 1e6,
                  "mode": "64 independent back-to-back calls over the rotation",
@@ -783,6 +944,15 @@ def main_mm(args):
                 print(f"bench: GEMM outputs not read back for the parity check: {e}", file=sys.stderr)
                 gpu_gemm = None
             out["cpu_baseline"] = cpu_oracle_sample(gpu_gemm=gpu_gemm)
+            try:
+                bp = bench_parity(w)
+                out["cpu_baseline"]["parity"]["workloads"] = bp["workloads"]
+                out["cpu_baseline"]["parity"]["ok"] = bool(out["cpu_baseline"]["parity"]["ok"] and bp["ok"])
+                out["cpu_baseline"]["parity"]["what"] += ("; and per workload, the outputs the timed phases left "
+                                                          "(see workloads)")
+                out["cpu_baseline"]["parity"]["seconds_workloads"] = bp["seconds"]
+            except Exception as e:  # a report item: it must not cost the line
+                print(f"bench: workload parity not computed: {e}", file=sys.stderr)
         out["inputs_sha256"] = w.inputs_sha256
         print(json.dumps(out), flush=True)
     return 0

@@ -228,9 +228,9 @@ def gemm_case(name, transA, transB, M, N, K, dist, seed_base, sigma=0.02, replic
     return GemmCase(name, transA, transB, M, N, K, A, B)
 
 
-def gpt2_mlp_up_64x768x3072() -> GemmCase:
+def gpt2_mlp_up_64x768x3072(replica: int = 0) -> GemmCase:
     """GPT-2-small MLP up-projection, 64 tokens: C(64x3072) = A(64x768) B(768x3072), U[-1,1)."""
-    return gemm_case("gpt2_mlp_up_m64_k768_n3072_nn", 0, 0, 64, 3072, 768, "uniform", 1)
+    return gemm_case("gpt2_mlp_up_m64_k768_n3072_nn", 0, 0, 64, 3072, 768, "uniform", 1, replica=replica)
 
 
 def square_2048(layout: str, replica: int = 0) -> GemmCase:

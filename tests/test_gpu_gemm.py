@@ -288,3 +288,45 @@ def test_gemm_stream_k_deterministic_and_integer_exact(oracle):
     c2 = run_splitk(0, 1, M, N, K, A, B, -1, fill=-7.0)
     check_exact(c1, ref, "stream-K integers")
     assert np.array_equal(c1.view(np.uint32), c2.view(np.uint32))
+
+
+def test_training_set_through_the_bench_split_path(oracle):
+    # The training-shape set exactly as the bench times it: mm_gemm_f32_splitk with the
+    # automatic split (splitk = 0) and one workspace sized for the largest of the three
+    # products.  On a 152-SM GB300 that is no split for the forward product and stream-K
+    # for dA (8192 x 2048 x 8192) and dB (2048 x 8192 x 8192), whose tiles are each added
+    # up from several K segments through the workspace flags.  Checked: whole first, last
+    # and random rows and columns, every output of the first, a middle and the last
+    # 256 x 256 tile, and random outputs.
+    import torch
+    cases = synth.training_set_8192_all()
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    plans = [mm.mm_gemm_f32_split_plan(c.M, c.N, c.K, sms)[0] for c in cases]
+    if sms == 152:
+        assert plans == [1, -1, -1], plans
+    need = max(mm.mm_gemm_f32_splitk_workspace(c.M, c.N, c.K, 0) for c in cases)
+    dev = torch.device("cuda:0")
+    ws = torch.full((max(need, 4),), float("nan"), dtype=torch.float32, device=dev)
+    dA = to_dev(cases[0].A)
+    dB = to_dev(cases[0].B)
+    ddC = to_dev(cases[1].A)
+    rng = np.random.default_rng(11)
+    for n, (c, (a, b)) in enumerate(zip(cases, ((dA, dB), (ddC, dB), (dA, ddC)))):
+        out = empty_f32((c.M, c.N))
+        mm.mm_gemm_f32_splitk(c.transA, c.transB, c.M, c.N, c.K, a, a.shape[1], b, b.shape[1], out, c.N, 0,
+                              ws, need)
+        mm.mm_check_device_error()
+        C = to_host(out)
+        rows = [0, c.M - 1, int(rng.integers(c.M))]
+        cols = [0, c.N - 1, int(rng.integers(c.N))]
+        blocks = []
+        for (r0, c0) in ((0, 0), ((c.M // 512) * 256, (c.N // 512) * 256), (c.M - 256, c.N - 256)):
+            bi, bj = np.meshgrid(np.arange(r0, r0 + 256), np.arange(c0, c0 + 256), indexing="ij")
+            blocks.append((bi.reshape(-1), bj.reshape(-1)))
+        ii = np.concatenate([np.repeat(rows, c.N), np.tile(np.arange(c.M), len(cols))] + [b[0] for b in blocks]
+                            + [rng.integers(0, c.M, 4000)])
+        jj = np.concatenate([np.tile(np.arange(c.N), len(rows)), np.repeat(cols, c.M)] + [b[1] for b in blocks]
+                            + [rng.integers(0, c.N, 4000)])
+        ref, T = oracle.gemm_at(c.transA, c.transB, c.K, c.A, c.B, ii, jj)
+        worst = check_bound(C[ii, jj], ref, T, c.name + " bench split path")
+        print(f"{c.name} (split {plans[n]}): {len(ii)} outputs, worst |err|/T = {worst:.3e}")

@@ -66,7 +66,7 @@ def _all_workloads(rec, replicas=(0,)):
 
     for r in replicas:
         sfx = f"@{r}" if r else ""
-        run("gpt2_mlp_up" + sfx, synth.gpt2_mlp_up_64x768x3072)  # a parity case: replica 0 only
+        run("gpt2_mlp_up" + sfx, lambda: synth.gpt2_mlp_up_64x768x3072(replica=r))
         run("gpt2_mlp_bias" + sfx, lambda: synth.gpt2_mlp_bias_gelu_8192x768x3072(replica=r))
         for layout in ("nn", "nt", "tn"):
             run(f"square_2048_{layout}" + sfx, lambda: synth.square_2048(layout, replica=r))
@@ -140,9 +140,7 @@ def test_replica_streams_are_disjoint(monkeypatch):
     rec = _Recorder()
     rec.install(monkeypatch)
     _all_workloads(rec, replicas=tuple(range(8)) + (synth.MAX_REPLICAS - 1,))
-    # the 64 x 768 MLP case is a parity case drawn once, outside the replicas
-    ignore = {f"gpt2_mlp_up@{r}" for r in range(1, synth.MAX_REPLICAS)}
-    shared = _shared_streams(rec, ignore)
+    shared = _shared_streams(rec)
     assert not shared, f"streams drawn by more than one tensor: {shared}"
 
 
