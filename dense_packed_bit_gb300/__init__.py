@@ -20,16 +20,17 @@ __all__ = [
     "mm_gemm_packed2", "mm_gemm_packed2_ex", "mm_gemv_packed4", "mm_gemv_packed4_ex",
     "mm_check_device_error", "mm_gemm_f32_splitk", "mm_gemm_f32_splitk_workspace", "mm_gemm_f32_splitk_noalloc",
     "MM_SPLITK_NOALLOC_MAX_FLOATS", "mm_gemm_f32_bias_act", "MM_ACT_NONE", "MM_ACT_GELU_TANH",
-    "mm_gemv_packed2_strided_batched", "mm_gemm_f32_bias_act_splitk", "mm_gemm_f32_split_plan",
+    "mm_gemv_packed2_strided_batched", "mm_gemv_packed2_strided_batched_ex", "mm_gemm_f32_bias_act_splitk",
+    "mm_gemm_f32_split_plan",
     "mm_probe_bounded_wait",
     "MM_OK", "MM_ERR_INVALID_ARG", "MM_ERR_UNSUPPORTED", "MM_ERR_CUDA", "MM_ERR_TIMEOUT",
     "MM_GEMM_AUTO", "MM_GEMM_FFMA", "MM_GEMM_TF32X3",
-    "MM_DEQ_AUTO", "MM_DEQ_SELECT", "MM_DEQ_AFFINE", "MM_DEQ_MMA", "MM_DEQ_FP8", "MM_DEQ_TC",
+    "MM_DEQ_AUTO", "MM_DEQ_SELECT", "MM_DEQ_AFFINE", "MM_DEQ_MMA", "MM_DEQ_FP8", "MM_DEQ_TC", "MM_DEQ_MXF4",
 ]
 
 MM_OK, MM_ERR_INVALID_ARG, MM_ERR_UNSUPPORTED, MM_ERR_CUDA, MM_ERR_TIMEOUT = 0, 1, 2, 3, 4
 MM_GEMM_AUTO, MM_GEMM_FFMA, MM_GEMM_TF32X3 = 0, 1, 2
-MM_DEQ_AUTO, MM_DEQ_SELECT, MM_DEQ_AFFINE, MM_DEQ_MMA, MM_DEQ_FP8, MM_DEQ_TC = 0, 1, 2, 3, 4, 5
+MM_DEQ_AUTO, MM_DEQ_SELECT, MM_DEQ_AFFINE, MM_DEQ_MMA, MM_DEQ_FP8, MM_DEQ_TC, MM_DEQ_MXF4 = 0, 1, 2, 3, 4, 5, 6
 MM_SPLITK_NOALLOC_MAX_FLOATS = 4194304  # floats of the static split-K scratch (16 MiB), as in mm.h
 MM_ACT_NONE, MM_ACT_GELU_TANH = 0, 1
 
@@ -86,6 +87,8 @@ SIGNATURES = {
                                      _P], ctypes.c_int),
     "mm_gemv_packed2_strided_batched": ([_P, _I64, _P, _I64, _P, _I64, _P, _I64, _I64, _I64, _I64, _P, _P],
                                         ctypes.c_int),
+    "mm_gemv_packed2_strided_batched_ex": ([_P, _I64, _P, _I64, _P, _I64, _P, _I64, _I64, _I64, _I64, _P, _P,
+                                            ctypes.POINTER(GemvOpts)], ctypes.c_int),
     "mm_probe_bounded_wait": ([_I, ctypes.c_uint64, _P, _P], ctypes.c_int),
 }
 
@@ -205,6 +208,16 @@ def mm_gemv_packed2_strided_batched(codes, codes_stride, scales, scales_stride, 
     _check(load_library().mm_gemv_packed2_strided_batched(
         _ptr(codes), codes_stride, _ptr(scales), scales_stride, _ptr(x), x_stride, _ptr(y), y_stride, batch, rows,
         cols, _codebook(codebook), _stream(stream)))
+
+
+def mm_gemv_packed2_strided_batched_ex(codes, codes_stride, scales, scales_stride, x, x_stride, y, y_stride, batch,
+                                       rows, cols, codebook, stream=None, *, dequant=0, rows_per_lane=0):
+    """mm_gemv_packed2_strided_batched with a decode choice (dequant: 0, MM_DEQ_AFFINE or MM_DEQ_MXF4;
+    rows_per_lane: 127-row tiles per CTA for MM_DEQ_MXF4, 0 = automatic)."""
+    o = GemvOpts(0, rows_per_lane, 0, dequant, 0, 0, 0, -1)
+    _check(load_library().mm_gemv_packed2_strided_batched_ex(
+        _ptr(codes), codes_stride, _ptr(scales), scales_stride, _ptr(x), x_stride, _ptr(y), y_stride, batch, rows,
+        cols, _codebook(codebook), _stream(stream), ctypes.byref(o)))
 
 
 def mm_gemm_f32_bias_act(transA, transB, M, N, K, A, lda, B, ldb, bias, act, C, ldc, stream=None):

@@ -316,6 +316,7 @@ bool gemv_vec_supported(const PackedArgs &a) {
 }
 
 cudaError_t launch_gemv_packed2(const PackedArgs &a, const GemvConfig &cfg, cudaStream_t st) {
+    if (cfg.dequant == 6) return launch_gemv_mxf4(a, cfg, st);
     if (cfg.dequant == 5) return launch_gemv_tc(a, cfg, st);
     if (cfg.dequant == kDeqAffine && cfg.staging) return launch_gemv_rows(a, cfg, st);
     if (cfg.dequant == 4) return launch_gemv_fp8(a, cfg, st);

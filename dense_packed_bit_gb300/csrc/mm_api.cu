@@ -381,7 +381,7 @@ mm_status mm_gemv_packed2_ex(const uint8_t *codes, const uint16_t *scales, const
     // automatic decode, by measurement on GB300 (12,288 x 1,536): the SIMT affine decode is the
     // fastest both for independent calls (bound by issue throughput) and for chained ones
     if (cfg.dequant == MM_DEQ_AUTO) cfg.dequant = affine ? MM_DEQ_AFFINE : MM_DEQ_SELECT;
-    if (cfg.dequant < MM_DEQ_SELECT || cfg.dequant > MM_DEQ_TC)
+    if (cfg.dequant < MM_DEQ_SELECT || cfg.dequant > MM_DEQ_MXF4)
         return fail(MM_ERR_INVALID_ARG, "unknown dequant %d", cfg.dequant);
     if (cfg.dequant != MM_DEQ_SELECT && !affine)
         return fail(MM_ERR_INVALID_ARG, "affine decode needs codebook[c] == codebook[0] + c*(codebook[1]-codebook[0])");
@@ -396,7 +396,17 @@ mm_status mm_gemv_packed2_ex(const uint8_t *codes, const uint16_t *scales, const
         !(cfg.dequant == MM_DEQ_MMA && mm::gemv_tma_supported(a)) &&
         !(cfg.dequant == MM_DEQ_AFFINE && mm::gemv_rows_supported(a)))
         return fail(MM_ERR_INVALID_ARG, "staging needs the affine or tensor-core decode, cols %% 512 == 0, cols <= 4096 and 16-byte aligned codes and x");
-    if (cfg.dequant == MM_DEQ_TC) {
+    if (cfg.dequant == MM_DEQ_MXF4) {
+        // 127 rows per tile and CTA-wide roles fix split and warps; rows_per_lane counts the
+        // tiles a CTA multiplies (automatic: 1)
+        if (!mm::gemv_mxf4_supported(a))
+            return fail(MM_ERR_INVALID_ARG, "fp4 tensor-core decode needs cols %% 512 == 0, cols <= 4096 and 16-byte aligned codes");
+        if (cfg.split || cfg.warps || cfg.staging > 0)
+            return fail(MM_ERR_INVALID_ARG, "split, warps and staging are fixed by the fp4 tensor-core decode");
+        if (cfg.rows_per_lane < 0 || cfg.rows_per_lane > 64)
+            return fail(MM_ERR_INVALID_ARG, "rows_per_lane (127-row tiles per CTA) must be 0..64 with the fp4 tensor-core decode");
+        cfg.blocks_per_cta = cfg.rows_per_lane ? cfg.rows_per_lane : 1;
+    } else if (cfg.dequant == MM_DEQ_TC) {
         // 127 rows per tile and CTA-wide roles fix split and warps; rows_per_lane counts the
         // tiles a CTA multiplies (automatic: 1)
         if (!mm::gemv_tc_supported(a))
@@ -489,6 +499,22 @@ mm_status mm_gemv_packed2_strided_batched(const uint8_t *codes, int64_t codes_st
                                           int64_t scales_stride, const uint16_t *x, int64_t x_stride, float *y,
                                           int64_t y_stride, int64_t batch, int64_t rows, int64_t cols,
                                           const float codebook[4], mm_stream_t stream) {
+    return mm_gemv_packed2_strided_batched_ex(codes, codes_stride, scales, scales_stride, x, x_stride, y, y_stride,
+                                              batch, rows, cols, codebook, stream, nullptr);
+}
+
+mm_status mm_gemv_packed2_strided_batched_ex(const uint8_t *codes, int64_t codes_stride, const uint16_t *scales,
+                                             int64_t scales_stride, const uint16_t *x, int64_t x_stride, float *y,
+                                             int64_t y_stride, int64_t batch, int64_t rows, int64_t cols,
+                                             const float codebook[4], mm_stream_t stream, const mm_gemv_opts *opts) {
+    int dequant = opts ? opts->dequant : MM_DEQ_AUTO;
+    const int tiles = opts ? opts->rows_per_lane : 0;
+    if (opts && (opts->split || opts->warps || opts->pdl || opts->weights_static || opts->independent ||
+                 opts->staging > 0))
+        return fail(MM_ERR_INVALID_ARG, "the batched GEMV takes only dequant and rows_per_lane options");
+    if (dequant != MM_DEQ_AUTO && dequant != MM_DEQ_AFFINE && dequant != MM_DEQ_MXF4)
+        return fail(MM_ERR_INVALID_ARG, "the batched GEMV decode must be MM_DEQ_AUTO, MM_DEQ_AFFINE or MM_DEQ_MXF4");
+    if (tiles < 0 || tiles > 4096) return fail(MM_ERR_INVALID_ARG, "rows_per_lane (tiles per CTA) must be 0..4096");
     if (batch < 1) return fail(MM_ERR_INVALID_ARG, "batch must be >= 1 (got %lld)", (long long)batch);
     mm_status s = check_packed(codes, scales, x, y, 1, rows, cols, codebook);
     if (s != MM_OK) return s;
@@ -510,11 +536,21 @@ mm_status mm_gemv_packed2_strided_batched(const uint8_t *codes, int64_t codes_st
     mm::PackedBatch p{codes, codes_stride, scales, scales_stride, x, x_stride, y, y_stride, batch, rows, cols,
                       {codebook[0], codebook[1], codebook[2], codebook[3]}};
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    if (dequant == MM_DEQ_MXF4 && !mm::gemv_batched_mxf4_supported(p))
+        return fail(MM_ERR_INVALID_ARG, "the fp4 tensor-core decode needs an affine codebook, cols %% 512 == 0, "
+                                        "cols <= 4096 and 16-byte aligned codes and codes_stride");
+    if (dequant == MM_DEQ_MXF4) {
+        const cudaError_t e = mm::launch_gemv_batched_mxf4(p, tiles, st);
+        if (e != cudaSuccess) return cuda_fail(e, "batched gemv launch");
+        return ok();
+    }
     if (mm::gemv_batched_supported(p)) {
         const cudaError_t e = mm::launch_gemv_batched(p, st);
         if (e != cudaSuccess) return cuda_fail(e, "batched gemv launch");
         return ok();
     }
+    if (dequant == MM_DEQ_AFFINE && !mm::codebook_is_affine(codebook))
+        return fail(MM_ERR_INVALID_ARG, "affine decode needs codebook[c] == codebook[0] + c*(codebook[1]-codebook[0])");
     // shapes the one-launch kernel does not take: one call per matrix
     for (int64_t b = 0; b < batch; ++b) {
         s = mm_gemv_packed2_ex(codes + b * codes_stride, scales + b * scales_stride, x + b * x_stride,
@@ -647,6 +683,9 @@ mm_status mm_check_device_error(mm_stream_t stream) {
     const unsigned int u4 = mm::gemv4_take_device_error(&e);
     if (e != cudaSuccess) return cuda_fail(e, "mm_check_device_error");
     if (u4 != 0) return fail(MM_ERR_TIMEOUT, "a bounded device wait ran out in the 4-bit GEMV (code %u)", u4);
+    const unsigned int x4 = mm::gemv_mxf4_take_device_error(&e);
+    if (e != cudaSuccess) return cuda_fail(e, "mm_check_device_error");
+    if (x4 != 0) return fail(MM_ERR_TIMEOUT, "a bounded device wait ran out in the fp4 tensor-core GEMV (code %u)", x4);
     const unsigned int u = mm::gemv_tc_take_device_error(&e);
     if (e != cudaSuccess) return cuda_fail(e, "mm_check_device_error");
     if (u != 0) return fail(MM_ERR_TIMEOUT, "a bounded device wait ran out in the tcgen05 GEMV (code %u)", u);

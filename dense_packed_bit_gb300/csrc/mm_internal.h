@@ -94,6 +94,14 @@ unsigned int gemv_fp8_take_device_error(cudaError_t *err);
 bool gemv_rows_supported(const PackedArgs &a);
 cudaError_t launch_gemv_rows(const PackedArgs &a, const GemvConfig &cfg, cudaStream_t s);
 unsigned int gemv_rows_take_device_error(cudaError_t *err);
+// 2-bit GEMV on tcgen05 with packed fp4 operands (kind::mxf4): codes in TMEM as e2m1 c/2, x as 14
+// exact e2m1 digit pieces; affine codebook, cols % 512 == 0, cols <= 4096, 16-byte aligned codes.
+// The batched form runs a strided batch in one launch (tiles_per_cta 0: automatic).
+bool gemv_mxf4_supported(const PackedArgs &a);
+bool gemv_batched_mxf4_supported(const PackedBatch &p);
+cudaError_t launch_gemv_mxf4(const PackedArgs &a, const GemvConfig &cfg, cudaStream_t s);
+cudaError_t launch_gemv_batched_mxf4(const PackedBatch &p, int tiles_per_cta, cudaStream_t s);
+unsigned int gemv_mxf4_take_device_error(cudaError_t *err);
 bool gemv_tc_supported(const PackedArgs &a);
 cudaError_t launch_gemv_tc(const PackedArgs &a, const GemvConfig &cfg, cudaStream_t s);
 unsigned int gemv_tc_take_device_error(cudaError_t *err);

@@ -5,7 +5,7 @@
     python -m dense_packed_bit_gb300.profile_case gemv --reps 3 --split 0 --rows 1 --warps 0 --dequant 2 --staging 1
     python -m dense_packed_bit_gb300.profile_case gemv4 --reps 3 [--staging 1 --rows 1 --independent 1]
     python -m dense_packed_bit_gb300.profile_case ternary --reps 1 [--tile 2] [--pdl 2: pdl + static weights]
-    python -m dense_packed_bit_gb300.profile_case gemv_batched --reps 2 --matrices 16
+    python -m dense_packed_bit_gb300.profile_case gemv_batched --reps 2 --matrices 16 [--dequant 6 --tiles 0]
     python -m dense_packed_bit_gb300.profile_case gemv_t --reps 3 --matrices 8   (1,536 x 12,288, automatic)
 
 One warm-up launch precedes the `reps` launches.  No timing is done here:
@@ -33,6 +33,7 @@ def main(argv=None):
     ap.add_argument("--dequant", type=int, default=0)
     ap.add_argument("--independent", type=int, default=0)
     ap.add_argument("--staging", type=int, default=0)
+    ap.add_argument("--tiles", type=int, default=0, help="batched fp4 decode: 127-row tiles per CTA (0: automatic)")
     a = ap.parse_args(argv)
 
     import torch
@@ -100,8 +101,8 @@ def main(argv=None):
         x = torch.from_numpy(c.X.reshape(-1)).to(dev)
         y = torch.empty((n, 12288), dtype=torch.float32, device=dev)
         for _ in range(1 + a.reps):
-            mm.mm_gemv_packed2_strided_batched(codes, 12288 * 384, scales, 12288, x, 0, y, 12288, n, 12288, 1536,
-                                               c.codebook)
+            mm.mm_gemv_packed2_strided_batched_ex(codes, 12288 * 384, scales, 12288, x, 0, y, 12288, n, 12288, 1536,
+                                                  c.codebook, dequant=a.dequant, rows_per_lane=a.tiles)
     else:
         layers = []
         for layer in range(16):

@@ -286,12 +286,23 @@ enum {
                             operands, x is split exactly into e5m2 pieces, and the
                             multiply-adds run as mma.sync m16n8k32 (fp8 in, fp32 accumulate);
                             code rows are staged by TMA, one warp per 256-field slab */
-    MM_DEQ_TC = 5        /* same affine condition, cols % 512 == 0, cols <= 8192, 16-byte
+    MM_DEQ_TC = 5,       /* same affine condition, cols % 512 == 0, cols <= 8192, 16-byte
                             aligned codes and x: the e4m3 field bytes are written to tensor
                             memory as the A operand of tcgen05.mma kind::f8f6f4 (M = 128,
                             K = 32), x as exact e5m2 pieces is the B operand in shared memory,
                             fp32 accumulation in tensor memory; 127 rows per tile, the 128th
                             lane forms sum x with the same MMAs */
+    MM_DEQ_MXF4 = 6      /* same affine condition, cols % 512 == 0, cols <= 4096, 16-byte
+                            aligned codes: a 2-bit field in the low bits of a nibble is the
+                            e2m1 value c/2, so two integer ops per eight fields write the codes
+                            to tensor memory as the packed-fp4 A operand of tcgen05.mma
+                            kind::mxf4 (M = 128, N = 16, K = 64, unit block scales); x * 2^24
+                            is split into 14 balanced radix-8 digits, each digit/2 an exact
+                            e2m1 value, as 14 B columns, so every per-digit sum is exact and
+                            the only rounding is the fp32 sum over the digits; 127 rows per
+                            tile, the 128th lane forms the digit sums of x.  A non-finite x
+                            gives NaN in every output.  rows_per_lane: 127-row tiles per CTA
+                            (0 = 1); split, warps and staging must be 0 (staging may be -1) */
 };
 
 typedef struct {
@@ -388,6 +399,23 @@ mm_status mm_gemv_packed2_strided_batched(const uint8_t *codes, int64_t codes_st
                                           int64_t y_stride, int64_t batch, int64_t rows,
                                           int64_t cols, const float codebook[4],
                                           mm_stream_t stream);
+
+/*
+ * mm_gemv_packed2_strided_batched with a decode choice.  opts: NULL (automatic), or a
+ * mm_gemv_opts whose dequant is MM_DEQ_AUTO, MM_DEQ_AFFINE (the staged SIMT affine
+ * kernel, as the automatic choice) or MM_DEQ_MXF4 (one launch of the fp4 tensor-core
+ * decode over the whole batch: its requirements, plus codes_stride % 16 == 0; each CTA
+ * takes rows_per_lane consecutive 127-row tiles of the batch, 0 = spread over two CTAs
+ * per SM); every other field 0 (staging may be -1).  Each y_b then equals bit for bit
+ * the single MM_DEQ_MXF4 call's.  Errors: as mm_gemv_packed2_strided_batched, plus
+ * MM_ERR_INVALID_ARG for other options or a decode the shape does not allow.
+ */
+mm_status mm_gemv_packed2_strided_batched_ex(const uint8_t *codes, int64_t codes_stride,
+                                             const uint16_t *scales, int64_t scales_stride,
+                                             const uint16_t *x, int64_t x_stride, float *y,
+                                             int64_t y_stride, int64_t batch, int64_t rows,
+                                             int64_t cols, const float codebook[4],
+                                             mm_stream_t stream, const mm_gemv_opts *opts);
 
 /* ------------------------------------------------------------------ 4-bit GEMV */
 

@@ -107,3 +107,59 @@ def test_batched_gemv_single_matrix_and_unaligned_stride_fallback(oracle):
         cb_ = flat[b * (rows * rb + 1): b * (rows * rb + 1) + rows * rb].reshape(rows, rb)
         ref, T = oracle.packed_gemm(cb_, sc[b], x[0].reshape(1, cols), rows, cols, CB2)
         check_bound(yh[b], ref[0], T[0], f"unaligned stride, matrix {b}")
+
+
+def run_batched_mxf4(codes, scales, x, rows, cols, cb, shared_x, tiles=0):
+    batch, rtot, rb = codes.shape
+    dc, ds, dx = to_dev(codes), to_dev(scales), to_dev(x)
+    dy = empty_f32((batch, rtot))
+    mm.mm_gemv_packed2_strided_batched_ex(dc, rtot * rb, ds, rtot, dx, 0 if shared_x else cols, dy, rtot, batch,
+                                          rows, cols, cb, dequant=mm.MM_DEQ_MXF4, rows_per_lane=tiles)
+    mm.mm_check_device_error()
+    return to_host(dy)
+
+
+@pytest.mark.parametrize("tiles", [0, 1, 3, 40])
+@pytest.mark.parametrize("shared_x", [True, False])
+@pytest.mark.parametrize("batch,rows,cols,pad", [(8, 12288, 1536, 0), (3, 1000, 512, 24), (1, 129, 4096, 0),
+                                                 (200, 65, 1024, 0), (37, 300, 2048, 4)])
+def test_batched_gemv_mxf4_parity_and_bitwise_equal_to_single_calls(oracle, batch, rows, cols, pad, shared_x, tiles):
+    # one launch of the fp4 tensor-core decode over the batch; CTAs whose run of tiles spans
+    # several matrices rebuild their x pieces at each matrix when x is not shared
+    codes, scales, x = make_batch(batch, rows, cols, seed=batch + rows + cols + 5, shared_x=shared_x, pad_rows=pad)
+    y = run_batched_mxf4(codes, scales, x, rows, cols, CB2, shared_x, tiles)
+    for b in range(batch):
+        xb = x[0 if shared_x else b]
+        ref, T = oracle.packed_gemm(codes[b, :rows], scales[b, :rows], xb.reshape(1, cols), rows, cols, CB2)
+        check_bound(y[b, :rows], ref[0], T[0], f"matrix {b}")
+        assert np.all(np.isnan(y[b, rows:])), "write into the padding rows of y"
+    for b in sorted({0, batch // 2, batch - 1}):
+        dc, ds = to_dev(np.ascontiguousarray(codes[b, :rows])), to_dev(np.ascontiguousarray(scales[b, :rows]))
+        dx = to_dev(np.ascontiguousarray(x[0 if shared_x else b]))
+        dy = empty_f32((rows,))
+        mm.mm_gemv_packed2_ex(dc, ds, dx, dy, rows, cols, CB2, dequant=mm.MM_DEQ_MXF4)
+        assert np.array_equal(to_host(dy).view(np.uint32), y[b, :rows].view(np.uint32)), f"matrix {b} not bitwise equal"
+
+
+def test_batched_gemv_mxf4_zero_entry_rows_exact():
+    batch, rows, cols = 5, 256, 1536
+    codes, scales, x = make_batch(batch, rows, cols, seed=4, shared_x=False)
+    codes[:, ::7, :] = 0xAA  # every field = 2
+    y = run_batched_mxf4(codes, scales, x, rows, cols, CB2, False)
+    assert np.all(y[:, ::7] == 0.0)
+
+
+def test_batched_gemv_mxf4_refusals():
+    rows, cols = 100, 1536
+    codes, scales, x = make_batch(2, rows, cols, seed=9, shared_x=True)
+    with pytest.raises(mm.MMError):  # not affine
+        run_batched_mxf4(codes, scales, x, rows, cols, CB_ODD, True)
+    with pytest.raises(mm.MMError):  # cols not a multiple of 512
+        c2, s2, x2 = make_batch(2, rows, 1000, seed=9, shared_x=True)
+        run_batched_mxf4(c2, s2, x2, rows, 1000, CB2, True)
+    dc, ds, dx = to_dev(codes), to_dev(scales), to_dev(x)
+    dy = empty_f32((2, rows))
+    for kw in (dict(dequant=mm.MM_DEQ_FP8), dict(dequant=mm.MM_DEQ_MXF4, rows_per_lane=-1)):
+        with pytest.raises(mm.MMError):
+            mm.mm_gemv_packed2_strided_batched_ex(dc, rows * cols // 4, ds, rows, dx, 0, dy, rows, 2, rows, cols,
+                                                  CB2, **kw)

@@ -49,6 +49,7 @@ VARIANTS = [
     ("mma_sync_staged", 2, 12288, 1536, dict(dequant=3, staging=1)),
     ("fp8_mma_sync", 2, 12288, 1536, dict(dequant=4)),
     ("tcgen05", 2, 12288, 1536, dict(dequant=5)),
+    ("mxf4", 2, 12288, 1536, dict(dequant=6)),
     ("transposed", 2, 1536, 12288, dict()),
     ("staged_4bit", 4, 12288, 1536, dict(staging=1)),
     ("generic_4bit", 4, 12288, 1536, dict(staging=0)),

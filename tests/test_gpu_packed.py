@@ -529,11 +529,82 @@ def test_gemv_tcgen05(oracle, rows, cols, mode, tiles):
     check_bound(y, ref[0], T[0], f"{rows}x{cols} {mode} tiles {tiles}")
 
 
+@pytest.mark.parametrize("rows", [1, 126, 127, 128, 254, 255, 1000, 1100])
+@pytest.mark.parametrize("cols", [512, 1024, 1536, 2048, 4096])
+@pytest.mark.parametrize("mode", FP8_MODES, ids=["serial", "chained", "independent"])
+@pytest.mark.parametrize("tiles", [0, 1, 2, 5])
+def test_gemv_mxf4(oracle, rows, cols, mode, tiles):
+    # packed e2m1 codes in tensor memory x 14 exact e2m1 digit pieces of x, tcgen05.mma
+    # kind::mxf4; 127-row tiles (the 128th lane forms the digit sums), several tiles per CTA,
+    # ragged last tiles
+    codes, scales, x = rand_case(rows, cols, seed=rows * 17 + cols)
+    y = gemv(codes, scales, x, rows, cols, CB2, dequant=6, rows_per_lane=tiles, **mode)
+    ref, T = oracle.packed_gemm(codes, scales, x, rows, cols, CB2)
+    check_bound(y, ref[0], T[0], f"{rows}x{cols} {mode} tiles {tiles}")
+
+
+def test_gemv_mxf4_full_rotation_every_output(oracle):
+    # all 64 matrices of the 12,288 x 1,536 rotation, independent calls, every output
+    import torch
+    dev = torch.device("cuda:0")
+    for i in range(64):
+        c = synth.gemv_2bit_12288x1536(i)
+        y = gemv(c.codes, c.scales, c.X, c.rows, c.cols, c.codebook, dequant=6, pdl=1, independent=1)
+        ref, T = oracle.packed_gemm(c.codes, c.scales, c.X, c.rows, c.cols, c.codebook)
+        check_bound(y, ref[0], T[0], f"matrix {i}")
+
+
+@pytest.mark.parametrize("cb", [CB2, np.array([-1, 0, 1, 2], np.float32), np.array([0, 0.5, 1, 1.5], np.float32),
+                                np.array([3, 1, -1, -3], np.float32)])
+def test_gemv_mxf4_other_affine_codebooks(oracle, cb):
+    rows, cols = 1000, 2048
+    codes, scales, x = rand_case(rows, cols, seed=88)
+    y = gemv(codes, scales, x, rows, cols, cb, dequant=6)
+    ref, T = oracle.packed_gemm(codes, scales, x, rows, cols, cb)
+    check_bound(y, ref[0], T[0], f"codebook {cb.tolist()}")
+
+
+def test_gemv_mxf4_extreme_activations(oracle):
+    # the largest finite fp16 and the smallest subnormals in one vector, both signs, every
+    # digit position of the split: the result still meets the bound
+    rows, cols = 300, 1536
+    codes, scales, _ = rand_case(rows, cols, seed=91)
+    rng = np.random.default_rng(91)
+    pool = np.array([0x7BFF, 0xFBFF, 0x0001, 0x8001, 0x03FF, 0x0400, 0x3C00, 0x7800, 0x5555, 0x2AAA], np.uint16)
+    x = pool[rng.integers(0, len(pool), cols)]
+    y = gemv(codes, scales, x, rows, cols, CB2, dequant=6)
+    ref, T = oracle.packed_gemm(codes, scales, x, rows, cols, CB2)
+    check_bound(y, ref[0], T[0], "extremes")
+
+
+def test_gemv_mxf4_non_finite_x_gives_nan():
+    rows, cols = 300, 1024
+    codes, scales, x = rand_case(rows, cols, seed=92)
+    for bad in (0x7C00, 0xFC00, 0x7E00):
+        xb = x.copy()
+        xb[0, 517] = bad
+        y = gemv(codes, scales, xb, rows, cols, CB2, dequant=6)
+        assert np.all(np.isnan(y)), hex(bad)
+
+
+def test_gemv_mxf4_options_refused():
+    rows, cols = 256, 1024
+    codes, scales, x = rand_case(rows, cols, seed=93)
+    for opts in (dict(split=4), dict(warps=4), dict(staging=1), dict(rows_per_lane=65)):
+        with pytest.raises(mm.MMError):
+            gemv(codes, scales, x, rows, cols, CB2, dequant=6, **opts)
+    with pytest.raises(mm.MMError):  # cols not a multiple of 512
+        c2, s2, x2 = rand_case(rows, 768, seed=94)
+        gemv(c2, s2, x2, rows, 768, CB2, dequant=6)
+    with pytest.raises(mm.MMError):  # not affine
+        gemv(codes, scales, x, rows, cols, CB_ODD, dequant=6)
+
+
 def _fp16_values(bits):
     return np.array(bits, np.uint16).view(np.float16).astype(np.float64)
 
 
-@pytest.mark.parametrize("dequant", [4, 5])
+@pytest.mark.parametrize("dequant", [4, 5, 6])
 def test_gemv_fp8_one_hot_every_window(oracle, dequant):
     # x = v e_k for values on both sides of the 2^-6 window boundary, subnormals, the
     # largest finite fp16 and negative values: y_r must be exactly fp32(scale_r * cb * v)
@@ -551,7 +622,7 @@ def test_gemv_fp8_one_hot_every_window(oracle, dequant):
             assert np.array_equal(y, expect), (k, hex(bits))
 
 
-@pytest.mark.parametrize("dequant", [4, 5])
+@pytest.mark.parametrize("dequant", [4, 5, 6])
 def test_gemv_fp8_integer_activations_bit_exact(oracle, dequant):
     rows, cols = 500, 1536
     codes, _, _ = rand_case(rows, cols, seed=78)
@@ -563,7 +634,7 @@ def test_gemv_fp8_integer_activations_bit_exact(oracle, dequant):
     check_exact(y, ref[0], "integer x")
 
 
-@pytest.mark.parametrize("dequant", [4, 5])
+@pytest.mark.parametrize("dequant", [4, 5, 6])
 def test_gemv_fp8_wide_dynamic_range(oracle, dequant):
     # activations spread over every fp16 binade, subnormals included, both signs
     rows, cols = 257, 2048
@@ -577,7 +648,7 @@ def test_gemv_fp8_wide_dynamic_range(oracle, dequant):
 
 @pytest.mark.parametrize("cb,zero_code", [(CB2, 2), (np.array([-1, 0, 1, 2], np.float32), 1),
                                           (np.array([0, 0.5, 1, 1.5], np.float32), 0)])
-@pytest.mark.parametrize("dequant", [4, 5])
+@pytest.mark.parametrize("dequant", [4, 5, 6])
 def test_gemv_fp8_zero_rows_at_every_position(oracle, cb, zero_code, dequant):
     # rows whose fields all hold the zero entry sit at every position of the 16-row MMA
     # blocks, between random rows: their outputs must be exactly 0
@@ -592,7 +663,7 @@ def test_gemv_fp8_zero_rows_at_every_position(oracle, cb, zero_code, dequant):
         check_bound(y, ref[0], T[0], "zero rows")
 
 
-@pytest.mark.parametrize("dequant", [4, 5])
+@pytest.mark.parametrize("dequant", [4, 5, 6])
 def test_gemv_fp8_deterministic(dequant):
     c = synth.gemv_2bit_12288x1536(5)
     y1 = gemv(c.codes, c.scales, c.X, c.rows, c.cols, c.codebook, dequant=dequant, pdl=1, independent=1)
