@@ -886,11 +886,13 @@ def main_mm(args):
                              "us_per_matrix": per_mat_gemvb_s * 1e6,
                              "mode": "the 64-matrix rotation (288 MiB) as one mm_gemv_packed2_strided_batched "
                                      "launch per step, one shared x",
+                             "kernel": "gemv2_mxf4_kernel (automatic: codes as packed e2m1 in tensor memory, x as "
+                                       "14 exact e2m1 digit pieces, tcgen05.mma kind::mxf4)",
                              "roofline": {"bound": "hbm", "achieved": GEMV_TOTAL_BYTES / per_mat_gemvb_s / 1e9,
                                           "peak": peaks["hbm_gbs"], "unit": "GB/s",
                                           "frac": GEMV_TOTAL_BYTES / per_mat_gemvb_s / 1e9 / peaks["hbm_gbs"],
                                           "weight_frac": GEMV_WEIGHT_BYTES / per_mat_gemvb_s / 1e9 / peaks["hbm_gbs"],
-                                          "traffic": traffic_for("gemv2_batched"), "peak_source": peaks_src}}},
+                                          "traffic": traffic_for("gemv2_mxf4_batched"), "peak_source": peaks_src}}},
         "ternary": {"value": tern_tflops, "unit": "TFLOP/s", "ms_per_block": tern_total_s / args.steps * 1e3,
                     "us_per_product": tern_total_s / args.steps / (2 * N_LAYERS) * 1e6,
                     "kernel": "gemm_packed2_tcr_kernel (automatic token tile and cluster split)", "opts": TERN_OPTS,

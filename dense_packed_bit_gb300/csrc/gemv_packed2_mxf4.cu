@@ -74,14 +74,15 @@ constexpr int LANES = 128, TR = 127;  // TMEM lanes per tile; weight rows per ti
 constexpr int BOXB = 128 * LANES;     // bytes of one code box: 128 bytes (512 fields) x 128 rows
 constexpr int NPIECE = 14;            // radix-8 digits of x * 2^24
 constexpr int NCOL = 16;              // MMA N: the pieces and two zero columns
-constexpr int ASTAGES = 4;            // TMEM stages of A, 256 fields (32 columns) each
-constexpr int TMEM_COLS = 256;        // D [0,64) (tile buffer db, issuer p at 16 (2 db + p)), SFA [64,72),
-                                      // SFB [72,80), A [128,256)
-constexpr int D_COL = 0, SFA_COL = 64, SFB_COL = 72, A_COL = 128;
-constexpr int NWG = 2;                // decode warpgroups and MMA issuers, taking alternate stages
-constexpr int NDEC = 128 * NWG, NTHREADS = NDEC + 32 * (1 + NWG), NBUILD = NDEC + 32 * NWG;
-constexpr int PRODUCER_WARP = 4 * NWG, MMA_WARP = PRODUCER_WARP + 1;  // MMA warps MMA_WARP + p, p < NWG
-constexpr int SRING = 4;              // tiles whose scales the producer has staged in shared memory
+constexpr int NWG = 4;                // tile pipelines per CTA (one CTA per SM), one decode warpgroup each
+constexpr int ASLOTS = 3;             // TMEM stages of A per pipeline, 256 fields (32 columns) each
+constexpr int MAX_RING = 3;           // code boxes per pipeline in shared memory (a 1,536-field tile: 3)
+constexpr int TMEM_COLS = 512;        // SFA [0,8), SFB [8,16), accumulator of pipeline w [16 + 16 w, +16),
+                                      // A stages of pipeline w [128 + 96 w, +96)
+constexpr int SFA_COL = 0, SFB_COL = 8, D_COL = 16, A_COL = 128, A_SPAN = 32 * ASLOTS;
+constexpr int NDEC = 128 * NWG, NTHREADS = NDEC + 32 * (2 + NWG), NBUILD = NDEC + 32 * NWG;
+constexpr int PRODUCER_WARP = 4 * NWG, MMA_WARP = PRODUCER_WARP + 1;  // MMA warp of pipeline w: MMA_WARP + w
+constexpr int SCALE_WARP = MMA_WARP + NWG;
 // kind::mxf4 instruction descriptor: A and B e2m1 (code 1), N >> 3 at bit 17, ue8m0 block
 // scales (bit 23), M >> 4 at bit 24, scale-factor ids 0, K = 64
 constexpr uint32_t IDESC = (1u << 7) | (1u << 10) | ((uint32_t)(NCOL >> 3) << 17) | (1u << 23) | ((128u >> 4) << 24);
@@ -252,55 +253,62 @@ __device__ __forceinline__ bool bar_red_or(int id, int nthreads, bool pred) {
     return r != 0;
 }
 
+// Barriers of one tile pipeline.  All counters of a pipeline are sequence numbers over the
+// tiles it has taken (k-th tile: parity k & 1 for the per-tile barriers).
+struct Pipe {
+    uint64_t bfull[MAX_RING], bempty[MAX_RING];  // code boxes: TMA -> decode
+    uint64_t afull[ASLOTS], aempty[ASLOTS];      // TMEM A stages: decode -> MMA
+    uint64_t dfull, dempty;                      // accumulator: MMA -> epilogue
+    uint64_t sfull, sempty;                      // the tile's scales: producer -> epilogue
+    float sx[NPIECE];                            // the piece sums of the tile (TMEM lane 127)
+    uint16_t sbuf[128];                          // the scales of the tile's 127 rows
+};
+
 struct Bars {
-    uint64_t dfull[2], dempty[2];
-    uint64_t afull[ASTAGES], aempty[ASTAGES];
-    uint64_t sfull[SRING], sempty[SRING];
+    Pipe pipe[NWG];
     uint64_t last;
     uint32_t tmem_slot;
     int fail;
-    float sx[2][NPIECE];
-    uint16_t sbuf[SRING][128];  // the scales of a tile's 127 rows, staged by the producer warp
-    uint64_t bfull[1];          // [bring], followed by bempty[bring]
 };
 
-__global__ void __launch_bounds__(NTHREADS, 2) gemv2_mxf4_kernel(const __grid_constant__ CUtensorMap tmC,
-                                                             const Mxf4Args a, const int prefetch,
-                                                             const int tiles_per_cta, const int bring) {
+// A CTA takes the tiles g0 .. g0 + my_tiles - 1 (of all matrices of the batch, in order).  A
+// segment is a run of them that shares one x (the whole run when x is shared); within a segment
+// pipeline w takes the segment's tiles w, w + NWG, w + 2 NWG, ..
+__global__ void __launch_bounds__(NTHREADS, 1) gemv2_mxf4_kernel(const __grid_constant__ CUtensorMap tmC,
+                                                                const Mxf4Args a, const int prefetch,
+                                                                const int tiles_per_cta, const int ring) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = smem_aligned<1024>(smem_raw);
     const int cols = (int)a.cols;
     const int nbox = cols >> 9;  // code boxes per tile
-    const int nst = cols >> 8;   // 256-field stages per tile
-    uint8_t *boxes = smem;                                  // [bring][128 rows][128 B]
-    uint8_t *btile = boxes + (size_t)bring * BOXB;          // cols * 8 bytes
+    const int nst = cols >> 8;   // 256-field stages per tile (two per box)
+    uint8_t *boxes = smem;                                                   // [NWG][ring][128 rows][128 B]
+    uint8_t *btile = boxes + (size_t)NWG * ring * BOXB;                     // cols * 8 bytes
     uint16_t *xs = reinterpret_cast<uint16_t *>(btile + (size_t)cols * 8);  // cols fp16
     Bars *bb = reinterpret_cast<Bars *>(xs + cols);
-    uint64_t *bfull = bb->bfull, *bempty = bb->bfull + bring;
     volatile int *fail = &bb->fail;
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int64_t ntiles = (a.rows + TR - 1) / TR;
-    const int64_t total = ntiles * a.batch;
-    const int64_t g0 = (int64_t)blockIdx.x * tiles_per_cta;
-    const int my_tiles = (int)min((int64_t)tiles_per_cta, total - g0);
+    const int ntiles = (int)((a.rows + TR - 1) / TR);  // tiles per matrix; ntiles * batch < 2^31
+    const int total = ntiles * (int)a.batch;
+    const int g0 = (int)blockIdx.x * tiles_per_cta;
+    const int my_tiles = min(tiles_per_cta, total - g0);
 
     if (tid == 0) {
-        for (int i = 0; i < 2; ++i) {
-            mbar_init(&bb->dfull[i], NWG);  // each MMA issuer commits its share of the tile
-            mbar_init(&bb->dempty[i], 4);  // the four warps of the tile's epilogue warpgroup
-        }
-        for (int i = 0; i < ASTAGES; ++i) {
-            mbar_init(&bb->afull[i], 4);   // the four warps of the stage's warpgroup
-            mbar_init(&bb->aempty[i], 1);
-        }
-        for (int i = 0; i < bring; ++i) {
-            mbar_init(&bfull[i], 1);
-            mbar_init(&bempty[i], NDEC / 32);  // every decode warp reads half a box
-        }
-        for (int i = 0; i < SRING; ++i) {
-            mbar_init(&bb->sfull[i], 32);  // every producer lane stores its share of the scales
-            mbar_init(&bb->sempty[i], 4);  // the epilogue warpgroup's four warps
+        for (int w = 0; w < NWG; ++w) {
+            Pipe &pp = bb->pipe[w];
+            for (int i = 0; i < ring; ++i) {
+                mbar_init(&pp.bfull[i], 1);
+                mbar_init(&pp.bempty[i], 4);  // the pipeline's four decode warps
+            }
+            for (int i = 0; i < ASLOTS; ++i) {
+                mbar_init(&pp.afull[i], 4);
+                mbar_init(&pp.aempty[i], 1);
+            }
+            mbar_init(&pp.dfull, 1);
+            mbar_init(&pp.dempty, 4);
+            mbar_init(&pp.sfull, 32);  // every producer lane stores its share of the scales
+            mbar_init(&pp.sempty, 4);
         }
         mbar_init(&bb->last, NWG);
         bb->fail = 0;
@@ -329,56 +337,143 @@ __global__ void __launch_bounds__(NTHREADS, 2) gemv2_mxf4_kernel(const __grid_co
     // had completed long before
     auto spin = [&](uint64_t *bar, uint32_t parity, unsigned code) -> bool {
         if (*fail) return false;
-        if (mbar_wait(bar, parity)) return true;
-        *fail = 1;
-        atomicExch(&g_gemv_mxf4_err, code);
-        return false;
+        if (mbar_try_wait(bar, parity)) return true;
+        const unsigned long long t0 = global_ns();
+        while (!mbar_try_wait(bar, parity)) {
+            __nanosleep(32);
+            if (global_ns() - t0 > kWaitLimitNs) {
+                *fail = 1;
+                atomicExch(&g_gemv_mxf4_err, code);
+                return false;
+            }
+        }
+        return true;
+    };
+    // waits of the roles off the decode's critical path (MMA issuers, producer, scales): they
+    // sleep between tries, so that their polling leaves the issue slots to the decode warps
+    auto nap = [&](uint64_t *bar, uint32_t parity, unsigned code) -> bool {
+        if (*fail) return false;
+        if (mbar_try_wait(bar, parity)) return true;
+        const unsigned long long t0 = global_ns();
+        unsigned ns = 32;
+        while (!mbar_try_wait(bar, parity)) {
+            __nanosleep(ns);
+            ns = ns < 256 ? 2 * ns : 256;
+            if (global_ns() - t0 > kWaitLimitNs) {
+                *fail = 1;
+                atomicExch(&g_gemv_mxf4_err, code);
+                return false;
+            }
+        }
+        return true;
+    };
+    auto seg_len = [&](int t) -> int {  // tiles from CTA tile t that share its x
+        int seg = my_tiles - t;
+        if (a.x_stride != 0) {
+            const int gt = g0 + t;
+            seg = min(seg, (gt / ntiles + 1) * ntiles - gt);
+        }
+        return seg;
     };
 
-    const int total_boxes = my_tiles * nbox;
-    if (warp == PRODUCER_WARP) {
-        // ------------------------------------------------------------ TMA producer
+    if (warp == SCALE_WARP) {
+        // ------------------------------------------------------------ scales
+        // each tile's 127 scales into its pipeline's buffer, in the order the pipelines take
+        // their tiles, so that no decode warp ever waits on a global load (a tile's epilogue
+        // comes long after its first stage)
+        int kbase[NWG];
+#pragma unroll
+        for (int w = 0; w < NWG; ++w) kbase[w] = 0;
+        bool ok = true;
+        for (int t = 0; t < my_tiles && ok;) {
+            const int seg = seg_len(t);
+            for (int rd = 0; rd * NWG < seg && ok; ++rd) {
+#pragma unroll
+                for (int w = 0; w < NWG; ++w) {
+                    if (rd * NWG + w >= seg || !ok) continue;
+                    Pipe &pp = bb->pipe[w];
+                    const int k = kbase[w] + rd;
+                    bool oks = true;
+                    if (lane == 0 && k >= 1) oks = nap(&pp.sempty, (k - 1) & 1, kDevErrWaitEmpty);
+                    ok = __shfl_sync(0xffffffffu, oks, 0);
+                    if (!ok) continue;
+                    const int gt = g0 + t + rd * NWG + w, mt = gt / ntiles, row0 = (gt - mt * ntiles) * TR;
+                    const uint16_t *sc = a.scales + (int64_t)mt * a.scales_stride;
+                    uint16_t v4[4];
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) {
+                        const int e = lane + 32 * i;
+                        const int64_t rr = (int64_t)row0 + e;
+                        v4[i] = (e < TR && rr < a.rows) ? __ldg(sc + rr) : (uint16_t)0;
+                    }
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) pp.sbuf[lane + 32 * i] = v4[i];
+                    mbar_arrive(&pp.sfull);
+                }
+            }
+#pragma unroll
+            for (int w = 0; w < NWG; ++w) kbase[w] += seg > w ? (seg - w + NWG - 1) / NWG : 0;
+            t += seg;
+        }
+    } else if (warp == PRODUCER_WARP) {
+        // ------------------------------------------------------------ producer
         // codes may be loaded before the wait on the previous kernel unless they may be
         // written by it (prefetch 0)
         if (prefetch == 0) pdl_wait();
         if (lane == 0) tma_prefetch_desc(&tmC);
-        int issued = 0;
-        for (; issued < total_boxes; ++issued) {
-            const int slot = issued % bring;
-            bool okp = true;
-            if (lane == 0 && issued >= bring) okp = wait(&bempty[slot], ((issued / bring) - 1) & 1, kDevErrWaitEmpty);
-            if (!__shfl_sync(0xffffffffu, okp, 0)) break;
-            const int tl = issued / nbox;  // tile of this CTA
-            const int gt = (int)g0 + tl, mt = gt / (int)ntiles, row0 = (gt - mt * (int)ntiles) * TR;
-            if (lane == 0) {
-                mbar_arrive_expect_tx(&bfull[slot], (uint32_t)BOXB);
-                tma_load_3d(boxes + (size_t)slot * BOXB, &tmC, &bfull[slot], (issued % nbox) * 128, row0, mt);
-            }
-            if (issued % nbox == nbox - 1) {
-                // the tile's scales, loaded once its boxes are on their way (its epilogue comes
-                // after all of them), so that no decode warp ever waits on a global load
-                const int ss = tl % SRING;
-                bool oks = true;
-                if (lane == 0 && tl >= SRING) oks = wait(&bb->sempty[ss], ((tl / SRING) - 1) & 1, kDevErrWaitEmpty);
-                if (!__shfl_sync(0xffffffffu, oks, 0)) break;
-                const uint16_t *sc = a.scales + (int64_t)mt * a.scales_stride;
+        int kbase[NWG], nq[NWG];  // tiles each pipeline took in earlier segments; boxes issued to it
+        int pslot[NWG], pphase[NWG];  // the ring slot of a pipeline's next box, and that slot's use parity
 #pragma unroll
-                for (int i = lane; i < 128; i += 32) {
-                    const int64_t rr = (int64_t)row0 + i;
-                    bb->sbuf[ss][i] = (i < TR && rr < a.rows) ? __ldg(sc + rr) : (uint16_t)0;
+        for (int w = 0; w < NWG; ++w) kbase[w] = nq[w] = pslot[w] = pphase[w] = 0;
+        bool ok = true;
+        for (int t = 0; t < my_tiles && ok;) {
+            const int seg = seg_len(t);
+            for (int rd = 0; rd * NWG < seg && ok; ++rd) {
+                for (int b = 0; b < nbox && ok; ++b) {
+#pragma unroll
+                    for (int w = 0; w < NWG; ++w) {
+                        if (rd * NWG + w >= seg || !ok) continue;
+                        Pipe &pp = bb->pipe[w];
+                        const int q = nq[w];  // this pipeline's box number
+                        const int slot = pslot[w];
+                        bool okp = true;
+                        if (lane == 0 && q >= ring) okp = nap(&pp.bempty[slot], pphase[w] ^ 1, kDevErrWaitEmpty);
+                        ok = __shfl_sync(0xffffffffu, okp, 0);
+                        if (!ok) continue;
+                        const int gt = g0 + t + rd * NWG + w, mt = gt / ntiles, row0 = (gt - mt * ntiles) * TR;
+                        if (lane == 0) {
+                            mbar_arrive_expect_tx(&pp.bfull[slot], (uint32_t)BOXB);
+                            tma_load_3d(boxes + ((size_t)w * ring + slot) * BOXB, &tmC, &pp.bfull[slot], b * 128, row0,
+                                        mt);
+                        }
+                        nq[w] = q + 1;
+                        if (++pslot[w] == ring) {
+                            pslot[w] = 0;
+                            pphase[w] ^= 1;
+                        }
+                    }
                 }
-                mbar_arrive(&bb->sfull[ss]);
             }
+#pragma unroll
+            for (int w = 0; w < NWG; ++w) kbase[w] += seg > w ? (seg - w + NWG - 1) / NWG : 0;
+            t += seg;
         }
         // every issued copy lands before the CTA can exit
-        if (lane == 0)
-            for (int gb = max(0, issued - bring); gb < issued; ++gb)
-                if (!mbar_wait_sleep(&bfull[gb % bring], (gb / bring) & 1)) atomicExch(&g_gemv_mxf4_err, kDevErrDrain);
+        if (lane == 0) {
+#pragma unroll
+            for (int w = 0; w < NWG; ++w)
+                for (int q = max(0, nq[w] - ring); q < nq[w]; ++q)
+                    if (!mbar_wait_sleep(&bb->pipe[w].bfull[q % ring], (q / ring) & 1))
+                        atomicExch(&g_gemv_mxf4_err, kDevErrDrain);
+        }
         if (prefetch == 2) pdl_launch_dependents();
     } else {
-        // ------------------------------------------------------------ B builders: decode warps + MMA warp
-        const int bt = warp >= MMA_WARP ? NDEC + 32 * (warp - MMA_WARP) + lane : tid;
+        // ------------------------------------------------------------ B builders: decode + MMA warps
+        const bool is_mma = warp >= MMA_WARP;  // (the scale warp took the branch above)
+        const int w = is_mma ? warp - MMA_WARP : warp >> 2;  // this warp's pipeline
+        const int bt = is_mma ? NDEC + 32 * (warp - MMA_WARP) + lane : tid;
         const uint32_t lane_base = (uint32_t)(32 * (warp & 3)) << 16;
+        Pipe &pp = bb->pipe[w];
         if (warp < 4) {  // unit block scales of A and B in this warp's lanes
             tmem_st8(tmem + lane_base + SFA_COL, kUnitScales);
             tmem_st8(tmem + lane_base + SFB_COL, kUnitScales);
@@ -390,78 +485,86 @@ __global__ void __launch_bounds__(NTHREADS, 2) gemv2_mxf4_kernel(const __grid_co
         // the next call may launch once this one has passed its wait: at most one chained call
         // runs ahead (its weight loads) instead of a queue of parked ones
         if (prefetch == 2 || warp == MMA_WARP) pdl_launch_dependents();
-        // decode role state (warps 0-3)
         const int r = tid & 127;  // TMEM lane = tile row
-        const int wg = tid >> 7;  // decode warpgroup (warps 0-3, 4-7)
+        const uint32_t a_base = tmem + A_COL + A_SPAN * w, d_tm = tmem + D_COL + 16 * w;
         const uint32_t b_base = smem_u32(btile);
-        int t = 0;  // tiles of this CTA started
-        while (t < my_tiles) {
-            const int64_t mat = (g0 + t) / ntiles;  // the matrix whose x the B tile holds
-            int seg = my_tiles - t;                  // tiles sharing this x
-            if (a.x_stride != 0) seg = (int)min((int64_t)seg, (mat + 1) * ntiles - (g0 + t));
-            stage_x(a.x + mat * a.x_stride, xs, cols, bt, NBUILD);
+        const uint8_t *myboxes = boxes + (size_t)w * ring * BOXB;
+        int kbase = 0;  // tiles this pipeline took in earlier segments
+        // ring positions, carried over tiles and segments: the MMA issuer's next A stage and its
+        // use parity; the decode's current box (slot, fill parity) and next A stage
+        int m_aslot = 0, m_aphase = 0;
+        int d_bslot = -1, d_bphase = 0, d_aslot = 0, d_aphase = 0, d_g = 0;
+        for (int t = 0; t < my_tiles;) {
+            const int seg = seg_len(t);
+            const int mat = (g0 + t) / ntiles;  // the matrix whose x the B tile holds
+            stage_x(a.x + (int64_t)mat * a.x_stride, xs, cols, bt, NBUILD);
             bar_sync(2, NBUILD);
             const bool finite = build_b_tile(xs, btile, cols, bt, NBUILD);
             fence_proxy_async_smem();
             tc_fence_before_sync();
             const bool nonfinite = bar_red_or(1, NBUILD, !finite);
             tc_fence_after_sync();
-            if (warp >= MMA_WARP) {
-                // -------------------------------------------------------- MMA issuers
-                // Issuer p multiplies the stages s = p, p + 2, .. (those of decode warpgroup p)
-                // into its own accumulator of the tile; the epilogue adds the two (exactly).
-                const int p = warp - MMA_WARP;
+            const int nk = seg > w ? (seg - w + NWG - 1) / NWG : 0;  // tiles of this segment for pipeline w
+            if (is_mma) {
+                // -------------------------------------------------------- MMA issuer of pipeline w
                 if (lane == 0) {
                     bool ok = true;
-                    for (int tt = t; tt < t + seg && ok; ++tt) {
-                        const int db = tt & 1;
-                        if (tt >= 2 && !spin(&bb->dempty[db], ((tt >> 1) - 1) & 1, kDevErrWaitEmpty)) break;
-                        const uint32_t d = tmem + D_COL + 16 * (2 * db + p);
-                        for (int s = p; s < nst; s += NWG) {
-                            const int g = tt * nst + s;
-                            const int as = g % ASTAGES;
-                            if (!spin(&bb->afull[as], (g / ASTAGES) & 1, kDevErrWaitFull)) {
+                    for (int kk = 0; kk < nk && ok; ++kk) {
+                        const int k = kbase + kk;
+                        if (k >= 1 && !nap(&pp.dempty, (k - 1) & 1, kDevErrWaitEmpty)) break;
+                        for (int s = 0; s < nst; ++s) {
+                            const int as = m_aslot;
+                            const bool got = nap(&pp.afull[as], m_aphase, kDevErrWaitFull);
+                            if (++m_aslot == ASLOTS) {
+                                m_aslot = 0;
+                                m_aphase ^= 1;
+                            }
+                            if (!got) {
                                 ok = false;
                                 break;
                             }
                             tc_fence_after_sync();
 #pragma unroll
-                            for (int k = 0; k < 4; ++k)
-                                umma_mxf4_tmem_a(d, tmem + A_COL + 32 * as + 8 * k,
-                                                 sdesc_kmajor_sw128(b_base + s * 2048 + 32 * k), tmem + SFA_COL,
-                                                 tmem + SFB_COL, (s > p || k > 0) ? 1u : 0u);
-                            umma_commit(&bb->aempty[as]);
+                            for (int k4 = 0; k4 < 4; ++k4)
+                                umma_mxf4_tmem_a(d_tm, a_base + 32 * as + 8 * k4,
+                                                 sdesc_kmajor_sw128(b_base + s * 2048 + 32 * k4), tmem + SFA_COL,
+                                                 tmem + SFB_COL, (s > 0 || k4 > 0) ? 1u : 0u);
+                            umma_commit(&pp.aempty[as]);
                         }
-                        if (ok) umma_commit(&bb->dfull[db]);
+                        if (ok) umma_commit(&pp.dfull);
                     }
                 }
                 __syncwarp();
             } else {
-                // -------------------------------------------------------- decode + epilogue
-                // Warpgroup wg decodes the stages s = wg, wg + 2, .. of every tile (a box's two
-                // stages go to the two warpgroups) and runs the epilogue of the tiles tt with
-                // tt % 2 == wg, so one warpgroup's epilogue overlaps the other's decode.
+                // -------------------------------------------------------- decode + epilogue of pipeline w
                 const float c0 = a.c0, two_d = 2.0f * a.d;
-                for (int tt = t; tt < t + seg; ++tt) {
-                    const int64_t gt = g0 + tt;
-                    const int64_t mt = gt / ntiles;  // this tile's matrix (a shared x spans several)
-                    const int64_t row = (gt % ntiles) * TR + r;
-                    const bool mine = (tt & 1) == wg;  // this warpgroup's epilogue
-                    const bool real = mine && r < TR && row < a.rows;
+                for (int kk = 0; kk < nk; ++kk) {
+                    const int k = kbase + kk;
+                    const int gt = g0 + t + w + kk * NWG;
+                    const int mt = gt / ntiles;
+                    const int64_t row = (int64_t)(gt - mt * ntiles) * TR + r;
+                    const bool real = r < TR && row < a.rows;
                     bool ok = __all_sync(0xffffffffu, *fail == 0);  // warp-uniform from here on
-                    // each stage's TMEM store completes while the warpgroup decodes its next
-                    // stage: the stage is handed to the MMA warp one decode later
+                    // each stage's TMEM store completes while the next stage is decoded: the
+                    // stage is handed to the MMA warp one decode later (the last one at once)
                     bool pend = false;
                     int pas = 0;
-                    for (int s = wg; s < nst && ok; s += NWG) {
-                        const int g = tt * nst + s;  // stage of this CTA
-                        const int gbx = g >> 1;      // code box of this CTA (two stages each)
-                        const int bs = gbx % bring;
-                        ok = __all_sync(0xffffffffu, spin(&bfull[bs], (gbx / bring) & 1, kDevErrWaitFull));
-                        const int as = g % ASTAGES;
-                        if (ok && g >= ASTAGES)
-                            ok = __all_sync(0xffffffffu,
-                                            spin(&bb->aempty[as], ((g / ASTAGES) - 1) & 1, kDevErrWaitMma));
+                    for (int s = 0; s < nst && ok; ++s) {
+                        if ((s & 1) == 0) {  // a new box
+                            if (++d_bslot == ring) {
+                                d_bslot = 0;
+                                d_bphase ^= 1;
+                            }
+                            ok = __all_sync(0xffffffffu, spin(&pp.bfull[d_bslot], d_bphase, kDevErrWaitFull));
+                        }
+                        const int slot = d_bslot, as = d_aslot;
+                        if (ok && d_g >= ASLOTS)
+                            ok = __all_sync(0xffffffffu, spin(&pp.aempty[as], d_aphase ^ 1, kDevErrWaitMma));
+                        ++d_g;
+                        if (++d_aslot == ASLOTS) {
+                            d_aslot = 0;
+                            d_aphase ^= 1;
+                        }
                         if (!ok) break;
                         uint32_t v[32];
                         if (r == TR) {
@@ -469,28 +572,30 @@ __global__ void __launch_bounds__(NTHREADS, 2) gemv2_mxf4_kernel(const __grid_co
                             for (int i = 0; i < 32; ++i) v[i] = kOnesRow;
                         } else {
                             // 64 code bytes of this row: 16-byte chunks 4(s&1) .. 4(s&1)+3 of the box
-                            const uint8_t *rowp = boxes + (size_t)bs * BOXB + r * 128;
+                            const uint8_t *rowp = myboxes + (size_t)slot * BOXB + r * 128;
                             const int ch = 4 * (s & 1);
 #pragma unroll
                             for (int i = 0; i < 4; ++i) {
-                                const uint4 q = *reinterpret_cast<const uint4 *>(rowp + (((ch + i) ^ (r & 7)) << 4));
-                                const uint32_t w[4] = {q.x, q.y, q.z, q.w};
+                                const uint4 c4 = *reinterpret_cast<const uint4 *>(rowp + (((ch + i) ^ (r & 7)) << 4));
+                                const uint32_t cw[4] = {c4.x, c4.y, c4.z, c4.w};
 #pragma unroll
                                 for (int j = 0; j < 4; ++j) {
-                                    v[8 * i + 2 * j] = w[j] & 0x33333333u;
-                                    v[8 * i + 2 * j + 1] = (w[j] >> 2) & 0x33333333u;
+                                    v[8 * i + 2 * j] = cw[j] & 0x33333333u;
+                                    v[8 * i + 2 * j + 1] = (cw[j] >> 2) & 0x33333333u;
                                 }
                             }
                         }
-                        __syncwarp();  // this warp is done reading its half of the box
-                        if (lane == 0) mbar_arrive(&bempty[bs]);
+                        if (s & 1) {  // this warp is done reading the box
+                            __syncwarp();
+                            if (lane == 0) mbar_arrive(&pp.bempty[slot]);
+                        }
                         if (pend) {
                             tmem_wait_st();
                             tc_fence_before_sync();
                             __syncwarp();
-                            if (lane == 0) mbar_arrive(&bb->afull[pas]);
+                            if (lane == 0) mbar_arrive(&pp.afull[pas]);
                         }
-                        tmem_st32(tmem + lane_base + A_COL + 32 * as, v);
+                        tmem_st32(a_base + lane_base + 32 * as, v);
                         pend = true;
                         pas = as;
                     }
@@ -498,49 +603,44 @@ __global__ void __launch_bounds__(NTHREADS, 2) gemv2_mxf4_kernel(const __grid_co
                         tmem_wait_st();
                         tc_fence_before_sync();
                         __syncwarp();
-                        if (lane == 0 && ok) mbar_arrive(&bb->afull[pas]);
+                        if (lane == 0 && ok) mbar_arrive(&pp.afull[pas]);
                     }
-                    if (!mine) continue;
-                    // epilogue of tile tt: its scales, staged by the producer warp
-                    const int ss = tt % SRING;
-                    if (ok) ok = __all_sync(0xffffffffu, spin(&bb->sfull[ss], (tt / SRING) & 1, kDevErrWaitFull));
-                    const float scl = ok ? __half2float(__ushort_as_half(bb->sbuf[ss][r])) : 0.f;
+                    // epilogue: the tile's scales (staged by the producer) and accumulator
+                    if (ok) ok = __all_sync(0xffffffffu, spin(&pp.sfull, k & 1, kDevErrWaitFull));
+                    const float scl = ok ? __half2float(__ushort_as_half(pp.sbuf[r])) : 0.f;
                     __syncwarp();
-                    if (lane == 0 && ok) mbar_arrive(&bb->sempty[ss]);
-                    const int db = tt & 1;
+                    if (lane == 0 && ok) mbar_arrive(&pp.sempty);
                     float v[16];
-                    if (ok) ok = __all_sync(0xffffffffu, spin(&bb->dfull[db], (tt >> 1) & 1, kDevErrWaitMma));
+                    if (ok) ok = __all_sync(0xffffffffu, spin(&pp.dfull, k & 1, kDevErrWaitMma));
                     if (ok) {
-                        float v1[16];
                         tc_fence_after_sync();
-                        tmem_ld16(tmem + lane_base + D_COL + 32 * db, v);
-                        tmem_ld16(tmem + lane_base + D_COL + 32 * db + 16, v1);
+                        tmem_ld16(d_tm + lane_base, v);
                         tc_fence_before_sync();
-#pragma unroll
-                        for (int j = 0; j < NPIECE; ++j) v[j] = __fadd_rn(v[j], v1[j]);  // exact: both are small multiples of 1/4
                     }
                     __syncwarp();
-                    if (lane == 0 && ok) mbar_arrive(&bb->dempty[db]);
+                    if (lane == 0 && ok) mbar_arrive(&pp.dempty);
                     if (r == TR) {
 #pragma unroll
-                        for (int j = 0; j < NPIECE; ++j) bb->sx[db][j] = ok ? v[j] : 0.f;
+                        for (int j = 0; j < NPIECE; ++j) pp.sx[j] = ok ? v[j] : 0.f;
                     }
-                    bar_sync(3 + wg, 128);  // the piece sums of this tile are in shared memory
+                    bar_sync(3 + w, 128);  // the piece sums of this tile are in shared memory
                     if (!*fail && real) {
                         float acc = 0.f;
 #pragma unroll
                         for (int j = 0; j < NPIECE; ++j) {
-                            const float p = __fmaf_rn(two_d, v[j], __fmul_rn(c0, bb->sx[db][j]));
+                            const float p = __fmaf_rn(two_d, v[j], __fmul_rn(c0, pp.sx[j]));
                             acc = __fmaf_rn(p, __int_as_float((127 + 3 * j - 23) << 23), acc);
                         }
-                        a.y[mt * a.y_stride + row] = nonfinite ? __int_as_float(0x7FC00000) : __fmul_rn(scl, acc);
+                        a.y[(int64_t)mt * a.y_stride + row] =
+                            nonfinite ? __int_as_float(0x7FC00000) : __fmul_rn(scl, acc);
                     }
                 }
             }
             bar_sync(2, NBUILD);  // every MMA reading this B tile has completed (epilogues waited for them)
+            kbase += nk;
             t += seg;
         }
-        if (warp >= MMA_WARP && lane == 0) {
+        if (is_mma && lane == 0) {
             // every issued MMA completes before TMEM is released
             umma_commit(&bb->last);
             if (!mbar_wait_sleep(&bb->last, 0)) atomicExch(&g_gemv_mxf4_err, kDevErrWaitMma);
@@ -551,8 +651,8 @@ __global__ void __launch_bounds__(NTHREADS, 2) gemv2_mxf4_kernel(const __grid_co
     if (warp == PRODUCER_WARP) tmem_dealloc(tmem, TMEM_COLS);
 }
 
-size_t mxf4_smem_bytes(int64_t cols, int bring) {
-    return 1024 + (size_t)bring * BOXB + (size_t)cols * 10 + sizeof(Bars) + (size_t)2 * bring * 8;
+size_t mxf4_smem_bytes(int64_t cols, int ring) {
+    return 1024 + (size_t)NWG * ring * BOXB + (size_t)cols * 10 + sizeof(Bars);
 }
 
 cudaError_t launch_mxf4(const Mxf4Args &m, const void *codes, int64_t codes_stride, int pdl, int prefetch,
@@ -572,27 +672,24 @@ cudaError_t launch_mxf4(const Mxf4Args &m, const void *codes, int64_t codes_stri
     if (attr_err != cudaSuccess) return attr_err;
     const int64_t ntiles = (m.rows + TR - 1) / TR;
     const int64_t total = ntiles * m.batch;
-    const int tpc = tiles_per_cta > 0 ? tiles_per_cta : 1;
+    const int tpc = tiles_per_cta > 0 ? tiles_per_cta : NWG;
     const int nbox = (int)(m.cols / 512);
-    // code-box ring: a whole tile when a CTA has one, else up to 6 boxes, within 110 KiB so that
-    // two CTAs share an SM (their 256 TMEM columns each also fit)
-    int bring = std::min<int64_t>(tpc == 1 ? nbox : 6, (int64_t)tpc * nbox);
-    bring = std::max(bring, 2);
-    while (bring > 2 && mxf4_smem_bytes(m.cols, bring) > 110 * 1024) --bring;
-    if (mxf4_smem_bytes(m.cols, bring) > 227 * 1024) return cudaErrorNotSupported;
+    // code boxes per pipeline: a whole tile of boxes when shared memory holds them, at least two
+    int ring = std::min(MAX_RING, std::max(nbox, 2));
+    while (ring > 2 && mxf4_smem_bytes(m.cols, ring) > 227 * 1024) --ring;
+    if (mxf4_smem_bytes(m.cols, ring) > 227 * 1024) return cudaErrorNotSupported;
     cudaLaunchConfig_t lc = {};
     lc.gridDim = dim3((unsigned)((total + tpc - 1) / tpc));
     lc.blockDim = dim3(NTHREADS);
-    // at least 76 KiB per CTA: no more than two CTAs share an SM, so their TMEM allocations
-    // (256 columns each) always fit in the SM's 512 columns
-    lc.dynamicSmemBytes = std::max<size_t>(mxf4_smem_bytes(m.cols, bring), 76 * 1024);
+    // at least 116 KiB: one CTA per SM, whose 512 TMEM columns are the SM's whole tensor memory
+    lc.dynamicSmemBytes = std::max<size_t>(mxf4_smem_bytes(m.cols, ring), 116 * 1024);
     lc.stream = st;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[0].val.programmaticStreamSerializationAllowed = pdl ? 1 : 0;
     lc.attrs = attr;
     lc.numAttrs = 1;
-    return cudaLaunchKernelEx(&lc, gemv2_mxf4_kernel, tm, m, prefetch, tpc, bring);
+    return cudaLaunchKernelEx(&lc, gemv2_mxf4_kernel, tm, m, prefetch, tpc, ring);
 }
 
 }  // namespace
@@ -622,11 +719,12 @@ cudaError_t launch_gemv_batched_mxf4(const PackedBatch &p, int tiles_per_cta, cu
                      p.cb[1] - p.cb[0]};
     int tpc = tiles_per_cta;
     if (tpc <= 0) {
-        // one run of tiles per CTA, two CTAs per SM
+        // one run of tiles per CTA and SM, a multiple of the pipelines
         int dev = 0, sms = 152;
         if (cudaGetDevice(&dev) == cudaSuccess) cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
         const int64_t total = ((p.rows + TR - 1) / TR) * p.batch;
-        tpc = (int)std::max<int64_t>(1, (total + 2 * sms - 1) / (2 * sms));
+        tpc = (int)std::max<int64_t>(NWG, (total + sms - 1) / sms);
+        tpc = (tpc + NWG - 1) / NWG * NWG;
     }
     return launch_mxf4(m, p.codes, p.codes_stride, 0, 0, tpc, st);
 }

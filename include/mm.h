@@ -301,8 +301,9 @@ enum {
                             e2m1 value, as 14 B columns, so every per-digit sum is exact and
                             the only rounding is the fp32 sum over the digits; 127 rows per
                             tile, the 128th lane forms the digit sums of x.  A non-finite x
-                            gives NaN in every output.  rows_per_lane: 127-row tiles per CTA
-                            (0 = 1); split, warps and staging must be 0 (staging may be -1) */
+                            gives NaN in every output.  rows_per_lane: 127-row tiles per CTA,
+                            which multiplies four at a time (0 = 4); split, warps and staging
+                            must be 0 (staging may be -1) */
 };
 
 typedef struct {
@@ -385,10 +386,11 @@ mm_status mm_gemm_packed2_ex(const uint8_t *codes, const uint16_t *scales, const
  * matrix b's codes at codes + b * codes_stride (bytes), its scales at scales +
  * b * scales_stride, its x at x + b * x_stride (x_stride 0: one x for every matrix)
  * and its y at y + b * y_stride (entries).  With an affine codebook, cols % 512 ==
- * 0, cols <= 4096, 16-byte aligned codes and x, codes_stride % 16 == 0 and
- * x_stride % 8 == 0 the whole batch runs in one launch (a persistent grid streaming
- * 128-row blocks of every matrix), and each y_b equals bit for bit the staged
- * single call's; other shapes run one call per matrix.  Same tolerance as
+ * 0, cols <= 4096, 16-byte aligned codes and codes_stride % 16 == 0 the whole batch
+ * runs in one launch of the fp4 tensor-core decode (MM_DEQ_MXF4; each y_b equals bit for
+ * bit the single MM_DEQ_MXF4 call's); failing that, with 16-byte aligned x and x_stride %
+ * 8 == 0, one launch of the staged SIMT affine kernel (each y_b equals bit for bit the
+ * staged single call's); other shapes run one call per matrix.  Same tolerance as
  * mm_gemv_packed2.  Errors: as mm_gemv_packed2, plus MM_ERR_INVALID_ARG for batch
  * < 1, a negative stride, strides that do not cover one matrix (batch > 1), or any
  * y overlapping any input.
@@ -403,11 +405,11 @@ mm_status mm_gemv_packed2_strided_batched(const uint8_t *codes, int64_t codes_st
 /*
  * mm_gemv_packed2_strided_batched with a decode choice.  opts: NULL (automatic), or a
  * mm_gemv_opts whose dequant is MM_DEQ_AUTO, MM_DEQ_AFFINE (the staged SIMT affine
- * kernel, as the automatic choice) or MM_DEQ_MXF4 (one launch of the fp4 tensor-core
- * decode over the whole batch: its requirements, plus codes_stride % 16 == 0; each CTA
- * takes rows_per_lane consecutive 127-row tiles of the batch, 0 = spread over two CTAs
- * per SM); every other field 0 (staging may be -1).  Each y_b then equals bit for bit
- * the single MM_DEQ_MXF4 call's.  Errors: as mm_gemv_packed2_strided_batched, plus
+ * kernel when the shape allows) or MM_DEQ_MXF4 (one launch of the fp4 tensor-core
+ * decode over the whole batch: its requirements, plus codes_stride % 16 == 0; each CTA,
+ * one per SM, takes rows_per_lane consecutive 127-row tiles of the batch, four at a
+ * time, 0 = spread evenly over the SMs); every other field 0 (staging may be -1).  Each
+ * y_b then equals bit for bit the single MM_DEQ_MXF4 call's.  Errors: as mm_gemv_packed2_strided_batched, plus
  * MM_ERR_INVALID_ARG for other options or a decode the shape does not allow.
  */
 mm_status mm_gemv_packed2_strided_batched_ex(const uint8_t *codes, int64_t codes_stride,

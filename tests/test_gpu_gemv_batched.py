@@ -35,12 +35,16 @@ def make_batch(batch, rows, cols, seed, shared_x, pad_rows=0):
     return codes, scales, x
 
 
-def run_batched(codes, scales, x, rows, cols, cb, shared_x):
+def run_batched(codes, scales, x, rows, cols, cb, shared_x, dequant=None):
     batch, rtot, rb = codes.shape
     dc, ds, dx = to_dev(codes), to_dev(scales), to_dev(x)
     dy = empty_f32((batch, rtot))
-    mm.mm_gemv_packed2_strided_batched(dc, rtot * rb, ds, rtot, dx, 0 if shared_x else cols, dy, rtot, batch, rows,
-                                       cols, cb)
+    if dequant is None:
+        mm.mm_gemv_packed2_strided_batched(dc, rtot * rb, ds, rtot, dx, 0 if shared_x else cols, dy, rtot, batch,
+                                           rows, cols, cb)
+    else:
+        mm.mm_gemv_packed2_strided_batched_ex(dc, rtot * rb, ds, rtot, dx, 0 if shared_x else cols, dy, rtot, batch,
+                                              rows, cols, cb, dequant=dequant)
     mm.mm_check_device_error()
     return to_host(dy)
 
@@ -49,8 +53,10 @@ def run_batched(codes, scales, x, rows, cols, cb, shared_x):
 @pytest.mark.parametrize("batch,rows,cols,pad", [(8, 12288, 1536, 0), (3, 1000, 512, 24), (1, 129, 4096, 0),
                                                  (200, 65, 1024, 0), (37, 300, 2048, 4)])
 def test_batched_gemv_parity_and_bitwise_equal_to_single_calls(oracle, batch, rows, cols, pad, shared_x):
+    # the staged SIMT affine kernel over the whole batch (the automatic choice takes the fp4
+    # tensor-core decode, tested below)
     codes, scales, x = make_batch(batch, rows, cols, seed=batch + rows + cols, shared_x=shared_x, pad_rows=pad)
-    y = run_batched(codes, scales, x, rows, cols, CB2, shared_x)
+    y = run_batched(codes, scales, x, rows, cols, CB2, shared_x, dequant=mm.MM_DEQ_AFFINE)
     for b in range(batch):
         xb = x[0 if shared_x else b]
         ref, T = oracle.packed_gemm(codes[b, :rows], scales[b, :rows], xb.reshape(1, cols), rows, cols, CB2)
@@ -163,3 +169,17 @@ def test_batched_gemv_mxf4_refusals():
         with pytest.raises(mm.MMError):
             mm.mm_gemv_packed2_strided_batched_ex(dc, rows * cols // 4, ds, rows, dx, 0, dy, rows, 2, rows, cols,
                                                   CB2, **kw)
+
+
+def test_batched_gemv_automatic_takes_the_fp4_decode(oracle):
+    # without options the batch runs the fp4 tensor-core decode: bit for bit the single calls'
+    batch, rows, cols = 6, 1000, 1536
+    codes, scales, x = make_batch(batch, rows, cols, seed=17, shared_x=False)
+    y = run_batched(codes, scales, x, rows, cols, CB2, False)
+    for b in range(batch):
+        dc, ds, dx = to_dev(np.ascontiguousarray(codes[b])), to_dev(np.ascontiguousarray(scales[b])), to_dev(x[b])
+        dy = empty_f32((rows,))
+        mm.mm_gemv_packed2_ex(dc, ds, dx, dy, rows, cols, CB2, dequant=mm.MM_DEQ_MXF4)
+        assert np.array_equal(to_host(dy).view(np.uint32), y[b].view(np.uint32)), f"matrix {b}"
+        ref, T = oracle.packed_gemm(codes[b], scales[b], x[b].reshape(1, cols), rows, cols, CB2)
+        check_bound(y[b], ref[0], T[0], f"matrix {b}")
