@@ -43,7 +43,7 @@ _P, _I64, _I = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int
 
 
 class GemmOpts(ctypes.Structure):
-    _fields_ = [("path", ctypes.c_int), ("tile", ctypes.c_int), ("reserved", ctypes.c_int * 6)]
+    _fields_ = [("path", ctypes.c_int), ("tile", ctypes.c_int), ("splitk", ctypes.c_int), ("reserved", ctypes.c_int * 5)]
 
 
 class GemvOpts(ctypes.Structure):
@@ -166,8 +166,8 @@ def mm_gemm_f32(transA, transB, M, N, K, A, lda, B, ldb, C, ldc, stream=None):
                                       _ptr(C), ldc, _stream(stream)))
 
 
-def mm_gemm_f32_ex(transA, transB, M, N, K, A, lda, B, ldb, C, ldc, stream=None, *, path=0, tile=0):
-    o = GemmOpts(path, tile)
+def mm_gemm_f32_ex(transA, transB, M, N, K, A, lda, B, ldb, C, ldc, stream=None, *, path=0, tile=0, splitk=0):
+    o = GemmOpts(path, tile, splitk)
     _check(load_library().mm_gemm_f32_ex(int(transA), int(transB), M, N, K, _ptr(A), lda, _ptr(B), ldb,
                                          _ptr(C), ldc, _stream(stream), ctypes.byref(o)))
 

@@ -108,6 +108,16 @@ mm_status check_packed4(const uint8_t *codes, const uint16_t *scales, const uint
     return MM_OK;
 }
 
+// A product with few rows of C: the 3xTF32 kernel's 128 x 256 tiles would occupy at most a
+// quarter of the SMs, so the cluster split-K FFMA kernel keeps more of the GPU busy (64 x 3072
+// x 768 on GB300: measured against the 3xTF32 kernel's 12 tiles).
+bool skinny_auto(int64_t M, int64_t N) {
+    if (M > 64) return false;
+    int dev = 0, sms = 152;
+    if (cudaGetDevice(&dev) == cudaSuccess) cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    return ((N + 255) / 256) * 4 <= sms;
+}
+
 }  // namespace
 
 extern "C" {
@@ -139,22 +149,32 @@ mm_status mm_gemm_f32_ex(int transA, int transB, int64_t M, int64_t N, int64_t K
         if (path < MM_GEMM_AUTO || path > MM_GEMM_TF32X3) return fail(MM_ERR_INVALID_ARG, "unknown path %d", path);
     }
     const int tile = opts ? opts->tile : 0;
+    const int splitk = opts ? opts->splitk : 0;
     if ((path == MM_GEMM_TF32X3 || path == MM_GEMM_AUTO) && (tile < 0 || tile > 3))
         return fail(MM_ERR_INVALID_ARG,
                     "3xTF32 tile must be 0 (automatic), 1 (two-stage), 2 (warp-specialised) or 3 (CTA pairs)");
+    if (path == MM_GEMM_FFMA && tile != 0 && tile != 4)
+        return fail(MM_ERR_INVALID_ARG, "FFMA tile must be 0 (TMA-staged 128 x 128) or 4 (few rows, K split in a cluster)");
+    if (splitk < 0 || splitk > 8 || (splitk != 0 && !(path == MM_GEMM_FFMA && tile == 4)))
+        return fail(MM_ERR_INVALID_ARG, "splitk is 0, or 1..8 with the FFMA tile 4");
     mm_status s = check_device();
     if (s != MM_OK) return s;
 
     mm::GemmArgs g{transA, transB, M, N, K, A, lda, B, ldb, C, ldc};
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
     cudaError_t e;
+    if ((path == MM_GEMM_FFMA && tile == 4) || (path == MM_GEMM_AUTO && tile == 0 && skinny_auto(M, N))) {
+        e = mm::launch_gemm_skinny(g, splitk, st);
+        if (e != cudaSuccess) return cuda_fail(e, "gemm launch");
+        return ok();
+    }
     if (path == MM_GEMM_TF32X3 && !mm::gemm_tf32x3_supported(g))
         return fail(MM_ERR_INVALID_ARG, "3xTF32 path needs 16-byte aligned A, B and lda, ldb multiples of 4");
     if ((path == MM_GEMM_TF32X3 || path == MM_GEMM_AUTO) && mm::gemm_tf32x3_supported(g))
         // automatic: CTA pairs (256-row tiles) once M fills them, one CTA per 128-row tile below that
         e = tile == 1 ? mm::launch_gemm_tf32x3(g, st)
                       : mm::launch_gemm_tf32x3_ws(g, (tile == 3 || (tile == 0 && M > 128)) ? 1 : 0, st);
-    else if (mm::gemm_ffma_supported(g)) e = mm::launch_gemm_ffma(g, opts ? opts->tile : 0, st);
+    else if (mm::gemm_ffma_supported(g)) e = mm::launch_gemm_ffma(g, 0, st);
     else if (path == MM_GEMM_FFMA || path == MM_GEMM_AUTO) e = mm::launch_gemm_simple(g, st);
     else e = cudaErrorNotSupported;
     if (e != cudaSuccess) return cuda_fail(e, "gemm launch");
@@ -317,9 +337,11 @@ mm_status mm_gemm_f32_bias_act(int transA, int transB, int64_t M, int64_t N, int
     g.bias = bias;
     g.act = act;
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
-    // the warp-specialised 3xTF32 kernel when TMA can describe the operands, else the plain tiled one
-    cudaError_t e = mm::gemm_tf32x3_supported(g) ? mm::launch_gemm_tf32x3_ws(g, M > 128 ? 1 : 0, st)
-                                                 : mm::launch_gemm_simple(g, st);
+    // few rows: the cluster split-K FFMA kernel; else the warp-specialised 3xTF32 kernel when TMA can
+    // describe the operands, else the plain tiled one
+    cudaError_t e = skinny_auto(M, N)               ? mm::launch_gemm_skinny(g, 0, st)
+                    : mm::gemm_tf32x3_supported(g) ? mm::launch_gemm_tf32x3_ws(g, M > 128 ? 1 : 0, st)
+                                                   : mm::launch_gemm_simple(g, st);
     if (e != cudaSuccess) return cuda_fail(e, "gemm launch");
     return ok();
 }

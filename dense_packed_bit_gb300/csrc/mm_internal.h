@@ -170,6 +170,13 @@ __device__ __forceinline__ float gelu_tanh_f(float z) {
 // Plain shared-memory tiled FFMA kernel: any sizes, strides and alignment.
 cudaError_t launch_gemm_simple(const GemmArgs &g, cudaStream_t s);
 
+// FFMA kernel for few rows of C: 64 x 64 tiles whose K range is split over a thread-block
+// cluster of `split` CTAs (0: automatic), partial tiles added in rank order through
+// distributed shared memory; any sizes, strides and alignment, no workspace.
+int gemm_skinny_split(int64_t M, int64_t N, int64_t K, int sms);
+bool gemm_skinny_supported(const GemmArgs &g);
+cudaError_t launch_gemm_skinny(const GemmArgs &g, int split, cudaStream_t s);
+
 // TMA-staged register-blocked FFMA kernel.  Needs 16-byte aligned A, B and
 // leading dimensions that are multiples of 4.  Returns cudaErrorNotSupported
 // when the arguments do not fit.

@@ -1,6 +1,7 @@
 """Run one hot-path kernel a few times on one workload, for profiler captures.
 
     python -m dense_packed_bit_gb300.profile_case gemm --layout nn --size 2048 --reps 3
+    python -m dense_packed_bit_gb300.profile_case c1 --reps 3 [--path 1 --tile 4 --split 8]   (64 x 768 x 3072 NN)
     python -m dense_packed_bit_gb300.profile_case gemv --reps 3 [--split 8 --rows 4 --warps 8 --dequant 2 --independent 1]
     python -m dense_packed_bit_gb300.profile_case gemv --reps 3 --split 0 --rows 1 --warps 0 --dequant 2 --staging 1
     python -m dense_packed_bit_gb300.profile_case gemv4 --reps 3 [--staging 1 --rows 1 --independent 1]
@@ -19,7 +20,7 @@ import sys
 
 def main(argv=None):
     ap = argparse.ArgumentParser()
-    ap.add_argument("op", choices=["gemm", "gemv", "gemv4", "ternary", "gemv_batched", "gemv_t"])
+    ap.add_argument("op", choices=["gemm", "c1", "gemv", "gemv4", "ternary", "gemv_batched", "gemv_t"])
     ap.add_argument("--layout", default="nn", choices=["nn", "nt", "tn"])
     ap.add_argument("--size", type=int, default=2048)
     ap.add_argument("--path", type=int, default=0)
@@ -52,6 +53,13 @@ def main(argv=None):
         C = torch.empty((n, n), dtype=torch.float32, device=dev)
         for _ in range(1 + a.reps):
             mm.mm_gemm_f32_ex(tA, tB, n, n, n, A, n, B, n, C, n, path=a.path, tile=a.tile)
+    elif a.op == "c1":
+        c = synth.gpt2_mlp_up_64x768x3072()
+        A, B = torch.from_numpy(c.A).to(dev), torch.from_numpy(c.B).to(dev)
+        C = torch.empty((c.M, c.N), dtype=torch.float32, device=dev)
+        for _ in range(1 + a.reps):
+            mm.mm_gemm_f32_ex(0, 0, c.M, c.N, c.K, A, c.K, B, c.N, C, c.N, path=a.path, tile=a.tile,
+                              splitk=a.split if a.path == 1 and a.tile == 4 else 0)
     elif a.op == "gemv":
         codes, scales = [], []
         for i in range(a.matrices):

@@ -261,8 +261,15 @@ typedef struct {
                       tile per CTA, two stages; 2 = persistent warp-specialised kernel,
                       128 x 256 tiles; 3 = the same with pairs of CTAs (a cluster of 2)
                       sharing 256 x 256 tiles.  Automatic: 3 when M > 128, else 2.
-                      Other values are refused. */
-    int reserved[6];
+                      MM_GEMM_FFMA: 4 = the kernel for few rows of C (64 x 64 FFMA tiles
+                      whose K range is split over a thread-block cluster of `splitk` CTAs,
+                      partial tiles added in rank order through distributed shared memory:
+                      no workspace, any alignment).  Automatic (MM_GEMM_AUTO, tile 0): this
+                      kernel when M <= 64 and the 3xTF32 kernel's 128 x 256 tiles would
+                      occupy at most a quarter of the SMs.  Other values are refused. */
+    int splitk;    /* MM_GEMM_FFMA tile 4: CTAs of the cluster sharing K, 1..8; 0 = automatic
+                      (about three CTAs per SM); other paths: must be 0 */
+    int reserved[5];
 } mm_gemm_opts;
 
 mm_status mm_gemm_f32_ex(int transA, int transB, int64_t M, int64_t N, int64_t K,

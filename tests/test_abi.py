@@ -89,6 +89,15 @@ def test_gemm_bad_tf32x3_tile(lib, path, tile):
     assert st == mm.MM_ERR_INVALID_ARG and b"tile" in lib.mm_last_error()
 
 
+@pytest.mark.parametrize("path,tile,splitk", [(1, 3, 0), (1, 5, 0), (1, 4, 9), (1, 4, -1), (1, 0, 2), (0, 0, 2),
+                                              (2, 2, 1)])
+def test_gemm_bad_ffma_tile_or_split(lib, path, tile, splitk):
+    # the few-rows FFMA kernel is tile 4 of the FFMA path; only it takes a cluster split (1..8)
+    o = mm.GemmOpts(path, tile, splitk)
+    st = lib.mm_gemm_f32_ex(0, 0, 8, 8, 8, FAKE, 8, FAKE + 4096, 8, FAKE + 8192, 8, None, ctypes.byref(o))
+    assert st == mm.MM_ERR_INVALID_ARG
+
+
 def test_gemm_splitk_workspace_size(lib):
     out = ctypes.c_int64(-1)
     assert lib.mm_gemm_f32_splitk_workspace(64, 3072, 768, 4, ctypes.byref(out)) == mm.MM_OK

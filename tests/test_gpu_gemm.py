@@ -330,3 +330,52 @@ def test_training_set_through_the_bench_split_path(oracle):
         ref, T = oracle.gemm_at(c.transA, c.transB, c.K, c.A, c.B, ii, jj)
         worst = check_bound(C[ii, jj], ref, T, c.name + " bench split path")
         print(f"{c.name} (split {plans[n]}): {len(ii)} outputs, worst |err|/T = {worst:.3e}")
+
+
+
+# ------------------------------------------------------------------ few rows: K split over a cluster
+
+@pytest.mark.parametrize("splitk", [0, 1, 2, 3, 5, 8])
+@pytest.mark.parametrize("layout", list(LAYOUTS))
+@pytest.mark.parametrize("shape", [(64, 3072, 768), (1, 1, 1), (7, 130, 45), (64, 200, 1000), (33, 64, 31),
+                                   (100, 257, 300)])
+def test_gemm_skinny_parity(oracle, splitk, layout, shape):
+    # 64 x 64 FFMA tiles, K cut over a thread-block cluster, partial tiles added in rank order
+    # through distributed shared memory; ragged M, N and K, rows beyond 64 (a second row of
+    # tiles), padded leading dimensions; columns past N stay untouched
+    tA, tB = LAYOUTS[layout]
+    M, N, K = shape
+    A, B = stored(tA, tB, M, N, K, seed=2100 + M + N + K)
+    Ap = np.zeros((A.shape[0], A.shape[1] + 3), np.float32); Ap[:, :A.shape[1]] = A
+    Bp = np.zeros((B.shape[0], B.shape[1] + 1), np.float32); Bp[:, :B.shape[1]] = B
+    dA, dB = to_dev(Ap), to_dev(Bp)
+    dC = empty_f32((M, N + 5))
+    mm.mm_gemm_f32_ex(tA, tB, M, N, K, dA, Ap.shape[1], dB, Bp.shape[1], dC, N + 5, path=mm.MM_GEMM_FFMA, tile=4,
+                      splitk=splitk)
+    mm.mm_check_device_error()
+    C = to_host(dC)
+    ref, T = oracle.gemm(tA, tB, M, N, K, A, B)
+    check_bound(C[:, :N], ref, T, f"skinny split {splitk} {layout} {shape}")
+    assert np.all(np.isnan(C[:, N:])), "columns past N were written"
+
+
+def test_gemm_skinny_is_automatic_for_few_rows_and_deterministic(oracle):
+    # the GPT-2 MLP up-projection at 64 tokens through mm_gemm_f32 takes the few-rows kernel:
+    # the same bits as the explicit tile-4 call, on every call; small integers are exact
+    c = synth.gpt2_mlp_up_64x768x3072()
+    dA, dB = to_dev(c.A), to_dev(c.B)
+    outs = []
+    for explicit in (False, True, False):
+        dC = empty_f32((c.M, c.N))
+        if explicit:
+            mm.mm_gemm_f32_ex(0, 0, c.M, c.N, c.K, dA, c.K, dB, c.N, dC, c.N, path=mm.MM_GEMM_FFMA, tile=4)
+        else:
+            mm.mm_gemm_f32(0, 0, c.M, c.N, c.K, dA, c.K, dB, c.N, dC, c.N)
+        outs.append(to_host(dC))
+    assert np.array_equal(outs[0].view(np.uint32), outs[1].view(np.uint32))
+    assert np.array_equal(outs[0].view(np.uint32), outs[2].view(np.uint32))
+    ref, T = oracle.gemm(0, 0, c.M, c.N, c.K, c.A, c.B)
+    check_bound(outs[0], ref, T, "automatic few-rows path")
+    A, B = stored(1, 1, 48, 1000, 777, seed=5, kind="int")
+    C = run(1, 1, 48, 1000, 777, A, B)
+    check_exact(C, oracle.gemm(1, 1, 48, 1000, 777, A, B)[0], "few rows, integers")
