@@ -19,7 +19,9 @@
 //
 // Loads: each chunk of op(A) (64 x 32) and op(B) (32 x 64) is copied by the 256
 // threads with the stored matrix's contiguous dimension fastest (coalesced for
-// every layout) by 4-byte cp.async into shared tiles of a 4-stage ring, kept in the
+// every layout) by cp.async -- 16 bytes per copy when both operands are 16-byte
+// aligned with leading dimensions a multiple of four, else 4 -- into shared tiles
+// of a 4-stage ring, kept in the
 // stored orientation (conflict-free copies), three chunks in flight while one is
 // multiplied.
 //
@@ -51,11 +53,18 @@ __device__ __forceinline__ void cp_async4(void *dst, const float *src, int src_b
     asm volatile("cp.async.ca.shared.global [%0], [%1], 4, %2;" ::"r"(smem_u32(dst)), "l"(src), "r"(src_bytes)
                  : "memory");
 }
+// 16-byte asynchronous copy; the bytes past src_bytes (0, 4, 8, 12 or 16) are zero-filled
+__device__ __forceinline__ void cp_async16(void *dst, const float *src, int src_bytes) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(smem_u32(dst)), "l"(src), "r"(src_bytes)
+                 : "memory");
+}
 __device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
 template <int N>
 __device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory"); }
 
-template <bool TA, bool TB>
+// VEC: both operands are 16-byte aligned with leading dimensions a multiple of four floats,
+// so every group of four elements along the stored contiguous dimension is one 16-byte copy
+template <bool TA, bool TB, bool VEC>
 __global__ void __launch_bounds__(NT) gemm_skinny_kernel(const GemmArgs g, const int chunks_per_rank) {
     extern __shared__ __align__(16) float sm[];
     // each operand chunk is kept in its stored orientation, so that a warp's copies land on
@@ -74,7 +83,34 @@ __global__ void __launch_bounds__(NT) gemm_skinny_kernel(const GemmArgs g, const
 
     // chunk c of op(A) and op(B) into stage st: element e = tid + 256 i of each 64 x 32 block,
     // the stored matrix's contiguous dimension fastest; elements outside the matrices read 0
+    // the 16-byte groups: group e = tid + 256 i (i = 0, 1) of each operand chunk, rows of 8
+    // groups when k is the contiguous dimension, of 16 groups when m (n) is
+    auto issue_vec = [&](int64_t c, int st) {
+        const int64_t k0 = c * SKC;
+        float *as = Abuf + st * OPF, *bs = Bbuf + st * OPF;
+#pragma unroll
+        for (int i = 0; i < 2; ++i) {
+            const int e = tid + NT * i;
+            int mm, kk, nn, kb;
+            if (TA) { kk = e >> 4; mm = (e & 15) * 4; } else { mm = e >> 3; kk = (e & 7) * 4; }
+            if (TB) { nn = e >> 3; kb = (e & 7) * 4; } else { kb = e >> 4; nn = (e & 15) * 4; }
+            const int64_t m = m0 + mm, ka = k0 + kk, n = n0 + nn, kq = k0 + kb;
+            // elements of the group inside the matrix (a prefix of the group)
+            const int64_t ra = TA ? (ka < g.K ? g.M - m : 0) : (m < g.M ? g.K - ka : 0);
+            const int64_t rb = TB ? (n < g.N ? g.K - kq : 0) : (kq < g.K ? g.N - n : 0);
+            const int ba = ra <= 0 ? 0 : ra >= 4 ? 16 : (int)ra * 4;
+            const int bb = rb <= 0 ? 0 : rb >= 4 ? 16 : (int)rb * 4;
+            float *da = TA ? as + kk * SB + mm : as + mm * KP + kk;
+            float *db = TB ? bs + nn * KP + kb : bs + kb * SB + nn;
+            cp_async16(da, ba ? (TA ? g.A + ka * g.lda + m : g.A + m * g.lda + ka) : g.A, ba);
+            cp_async16(db, bb ? (TB ? g.B + n * g.ldb + kq : g.B + kq * g.ldb + n) : g.B, bb);
+        }
+    };
     auto issue = [&](int64_t c, int st) {
+        if (VEC) {
+            issue_vec(c, st);
+            return;
+        }
         const int64_t k0 = c * SKC;
         float *as = Abuf + st * OPF, *bs = Bbuf + st * OPF;
 #pragma unroll
@@ -219,18 +255,31 @@ cudaError_t launch_gemm_skinny(const GemmArgs &g, int split, cudaStream_t st) {
     static std::once_flag once;
     static cudaError_t attr_err = cudaSuccess;
     std::call_once(once, [] {
-        const void *k[4] = {(const void *)gemm_skinny_kernel<false, false>, (const void *)gemm_skinny_kernel<false, true>,
-                            (const void *)gemm_skinny_kernel<true, false>, (const void *)gemm_skinny_kernel<true, true>};
+        const void *k[8] = {(const void *)gemm_skinny_kernel<false, false, false>,
+                            (const void *)gemm_skinny_kernel<false, true, false>,
+                            (const void *)gemm_skinny_kernel<true, false, false>,
+                            (const void *)gemm_skinny_kernel<true, true, false>,
+                            (const void *)gemm_skinny_kernel<false, false, true>,
+                            (const void *)gemm_skinny_kernel<false, true, true>,
+                            (const void *)gemm_skinny_kernel<true, false, true>,
+                            (const void *)gemm_skinny_kernel<true, true, true>};
         for (const void *f : k) {
             const cudaError_t e = cudaFuncSetAttribute(f, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
             if (e != cudaSuccess) attr_err = e;
         }
     });
     if (attr_err != cudaSuccess) return attr_err;
-    if (g.transA && g.transB) return cudaLaunchKernelEx(&lc, gemm_skinny_kernel<true, true>, g, per);
-    if (g.transA) return cudaLaunchKernelEx(&lc, gemm_skinny_kernel<true, false>, g, per);
-    if (g.transB) return cudaLaunchKernelEx(&lc, gemm_skinny_kernel<false, true>, g, per);
-    return cudaLaunchKernelEx(&lc, gemm_skinny_kernel<false, false>, g, per);
+    const bool vec = ((uintptr_t)g.A % 16 == 0) && ((uintptr_t)g.B % 16 == 0) && g.lda % 4 == 0 && g.ldb % 4 == 0;
+    if (vec) {
+        if (g.transA && g.transB) return cudaLaunchKernelEx(&lc, gemm_skinny_kernel<true, true, true>, g, per);
+        if (g.transA) return cudaLaunchKernelEx(&lc, gemm_skinny_kernel<true, false, true>, g, per);
+        if (g.transB) return cudaLaunchKernelEx(&lc, gemm_skinny_kernel<false, true, true>, g, per);
+        return cudaLaunchKernelEx(&lc, gemm_skinny_kernel<false, false, true>, g, per);
+    }
+    if (g.transA && g.transB) return cudaLaunchKernelEx(&lc, gemm_skinny_kernel<true, true, false>, g, per);
+    if (g.transA) return cudaLaunchKernelEx(&lc, gemm_skinny_kernel<true, false, false>, g, per);
+    if (g.transB) return cudaLaunchKernelEx(&lc, gemm_skinny_kernel<false, true, false>, g, per);
+    return cudaLaunchKernelEx(&lc, gemm_skinny_kernel<false, false, false>, g, per);
 }
 
 }  // namespace mm

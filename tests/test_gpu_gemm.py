@@ -339,15 +339,19 @@ def test_training_set_through_the_bench_split_path(oracle):
 @pytest.mark.parametrize("layout", list(LAYOUTS))
 @pytest.mark.parametrize("shape", [(64, 3072, 768), (1, 1, 1), (7, 130, 45), (64, 200, 1000), (33, 64, 31),
                                    (100, 257, 300)])
-def test_gemm_skinny_parity(oracle, splitk, layout, shape):
+@pytest.mark.parametrize("aligned", [False, True])
+def test_gemm_skinny_parity(oracle, splitk, layout, shape, aligned):
     # 64 x 64 FFMA tiles, K cut over a thread-block cluster, partial tiles added in rank order
     # through distributed shared memory; ragged M, N and K, rows beyond 64 (a second row of
-    # tiles), padded leading dimensions; columns past N stay untouched
+    # tiles), padded leading dimensions -- a multiple of four floats (16-byte copies) or odd
+    # (4-byte copies); columns past N stay untouched
     tA, tB = LAYOUTS[layout]
     M, N, K = shape
     A, B = stored(tA, tB, M, N, K, seed=2100 + M + N + K)
-    Ap = np.zeros((A.shape[0], A.shape[1] + 3), np.float32); Ap[:, :A.shape[1]] = A
-    Bp = np.zeros((B.shape[0], B.shape[1] + 1), np.float32); Bp[:, :B.shape[1]] = B
+    lda = (A.shape[1] + 3) // 4 * 4 + 4 if aligned else A.shape[1] + 1 + A.shape[1] % 2
+    ldb = (B.shape[1] + 3) // 4 * 4 + 8 if aligned else B.shape[1] + 3 + B.shape[1] % 2
+    Ap = np.zeros((A.shape[0], lda), np.float32); Ap[:, :A.shape[1]] = A
+    Bp = np.zeros((B.shape[0], ldb), np.float32); Bp[:, :B.shape[1]] = B
     dA, dB = to_dev(Ap), to_dev(Bp)
     dC = empty_f32((M, N + 5))
     mm.mm_gemm_f32_ex(tA, tB, M, N, K, dA, Ap.shape[1], dB, Bp.shape[1], dC, N + 5, path=mm.MM_GEMM_FFMA, tile=4,
