@@ -864,13 +864,18 @@ def main_mm(args):
         "gpt2_mlp_up_64": {"metric": "fp32 GEMM TFLOP/s, 64 x 768 x 3072 NN (one mm_gemm_f32 call, L2 flushed)",
                            "value": world * C1_FLOP * args.steps / c1_total_s / 1e12, "unit": "TFLOP/s",
                            "us_per_call": c1_total_s / args.steps * 1e6,
-                           "roofline": {"bound": "hbm", "achieved": C1_BYTES / (c1_total_s / args.steps) / 1e9,
-                                        "peak": peaks["hbm_gbs"], "unit": "GB/s",
-                                        "frac": C1_BYTES / (c1_total_s / args.steps) / 1e9 / peaks["hbm_gbs"],
-                                        "floor_us": C1_BYTES / peaks["hbm_gbs"] / 1e3, "traffic": None,
-                                        "peak_source": peaks_src,
+                           "roofline": {"bound": "alu", "kernel": "gemm_skinny_kernel",
+                                        "achieved": C1_FLOP / (c1_total_s / args.steps) / 1e12,
+                                        "peak": fp32_peak_max, "unit": "TFLOP/s",
+                                        "frac": C1_FLOP / (c1_total_s / args.steps) / 1e12 / fp32_peak_max,
+                                        "traffic": traffic_for("gemm_skinny"),
+                                        "peak_source": f"{sms} SMs x 128 FP32 lanes x 2 flop x "
+                                                       f"{peaks.get('sm_max_mhz', 2070.0):.0f} MHz",
+                                        "hbm_floor_us": C1_BYTES / peaks["hbm_gbs"] / 1e3,
+                                        "fp32_floor_us": C1_FLOP / fp32_peak_max / 1e6,
                                         "note": "302 MFLOP over 10.42 MB (A, B read once, C written): 29 flop per "
-                                                "byte, below the 3xTF32 ridge, so HBM bounds it"}},
+                                                "byte, above the FP32 SIMT ridge (about 12), so the FP32 pipe "
+                                                "bounds this FFMA kernel"}},
         "gemv": {"metric": "2-bit 12288x1536 GEMV weight GB/s", "value": gemv_gbs, "unit": "GB/s",
                  "us_per_call": per_call_gemv_s * 1e6,
                  "mode": "64 independent back-to-back calls over the rotation",

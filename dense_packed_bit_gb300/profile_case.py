@@ -1,9 +1,12 @@
 """Run one hot-path kernel a few times on one workload, for profiler captures.
 
     python -m dense_packed_bit_gb300.profile_case gemm --layout nn --size 2048 --reps 3
+    python -m dense_packed_bit_gb300.profile_case gemm --size 2048 --path 1 --misalign 1   (lda = ldb = ldc = n + 1)
     python -m dense_packed_bit_gb300.profile_case c1 --reps 3 [--path 1 --tile 4 --split 8]   (64 x 768 x 3072 NN)
+    python -m dense_packed_bit_gb300.profile_case c1 --reps 3 --path 2 --split 4   (workspace K slices + reduce)
     python -m dense_packed_bit_gb300.profile_case gemv --reps 3 [--split 8 --rows 4 --warps 8 --dequant 2 --independent 1]
     python -m dense_packed_bit_gb300.profile_case gemv --reps 3 --split 0 --rows 1 --warps 0 --dequant 2 --staging 1
+    python -m dense_packed_bit_gb300.profile_case gemv --reps 3 --misalign 1   (codes one byte off 16-byte alignment)
     python -m dense_packed_bit_gb300.profile_case gemv4 --reps 3 [--staging 1 --rows 1 --independent 1]
     python -m dense_packed_bit_gb300.profile_case ternary --reps 1 [--tile 2] [--pdl 2: pdl + static weights]
     python -m dense_packed_bit_gb300.profile_case gemv_batched --reps 2 --matrices 16 [--dequant 6 --tiles 0]
@@ -33,7 +36,8 @@ def main(argv=None):
     ap.add_argument("--pdl", type=int, default=1)
     ap.add_argument("--dequant", type=int, default=0)
     ap.add_argument("--independent", type=int, default=0)
-    ap.add_argument("--staging", type=int, default=0)
+    ap.add_argument("--staging", type=int, default=None, help="gemv: default 0; gemv4: default automatic")
+    ap.add_argument("--misalign", type=int, default=0, help="gemm: leading dimensions n + 1; gemv: codes at an odd address")
     ap.add_argument("--tiles", type=int, default=0, help="batched fp4 decode: 127-row tiles per CTA (0: automatic)")
     a = ap.parse_args(argv)
 
@@ -48,23 +52,36 @@ def main(argv=None):
     if a.op == "gemm":
         n = a.size
         tA, tB = {"nn": (0, 0), "nt": (0, 1), "tn": (1, 0)}[a.layout]
-        A = torch.from_numpy(synth.normal_f32(1, (n, n), 0.02)).to(dev)
-        B = torch.from_numpy(synth.normal_f32(2, (n, n), 0.02)).to(dev)
-        C = torch.empty((n, n), dtype=torch.float32, device=dev)
+        ld = n + 1 if a.misalign else n
+        A = torch.zeros((n, ld), dtype=torch.float32, device=dev)
+        B = torch.zeros((n, ld), dtype=torch.float32, device=dev)
+        A[:, :n] = torch.from_numpy(synth.normal_f32(1, (n, n), 0.02)).to(dev)
+        B[:, :n] = torch.from_numpy(synth.normal_f32(2, (n, n), 0.02)).to(dev)
+        C = torch.empty((n, ld), dtype=torch.float32, device=dev)
         for _ in range(1 + a.reps):
-            mm.mm_gemm_f32_ex(tA, tB, n, n, n, A, n, B, n, C, n, path=a.path, tile=a.tile)
+            mm.mm_gemm_f32_ex(tA, tB, n, n, n, A, ld, B, ld, C, ld, path=a.path, tile=a.tile)
     elif a.op == "c1":
         c = synth.gpt2_mlp_up_64x768x3072()
         A, B = torch.from_numpy(c.A).to(dev), torch.from_numpy(c.B).to(dev)
         C = torch.empty((c.M, c.N), dtype=torch.float32, device=dev)
-        for _ in range(1 + a.reps):
+        if a.path == 2 and a.split > 1:
+            wsf = mm.mm_gemm_f32_splitk_workspace(c.M, c.N, c.K, a.split)
+            ws = torch.empty((max(wsf, 1),), dtype=torch.float32, device=dev)
+            for _ in range(1 + a.reps):
+                mm.mm_gemm_f32_splitk(0, 0, c.M, c.N, c.K, A, c.K, B, c.N, C, c.N, a.split, ws, wsf)
+        for _ in range(1 + a.reps if not (a.path == 2 and a.split > 1) else 0):
             mm.mm_gemm_f32_ex(0, 0, c.M, c.N, c.K, A, c.K, B, c.N, C, c.N, path=a.path, tile=a.tile,
                               splitk=a.split if a.path == 1 and a.tile == 4 else 0)
     elif a.op == "gemv":
         codes, scales = [], []
         for i in range(a.matrices):
             c = synth.gemv_2bit_12288x1536(i)
-            codes.append(torch.from_numpy(c.codes).to(dev))
+            if a.misalign:
+                buf = torch.empty((c.codes.size + 1,), dtype=torch.uint8, device=dev)
+                buf[1:] = torch.from_numpy(c.codes.reshape(-1)).to(dev)
+                codes.append(buf[1:])
+            else:
+                codes.append(torch.from_numpy(c.codes).to(dev))
             scales.append(torch.from_numpy(c.scales).to(dev))
         x = torch.from_numpy(c.X.reshape(-1)).to(dev)
         y = torch.empty((a.matrices, 12288), dtype=torch.float32, device=dev)
@@ -73,7 +90,7 @@ def main(argv=None):
             mm.mm_gemv_packed2_ex(codes[i], scales[i], x, y[i], 12288, 1536, c.codebook, split=a.split,
                                   rows_per_lane=a.rows, warps=a.warps, dequant=a.dequant, pdl=a.pdl,
                                   weights_static=a.pdl and not a.independent, independent=a.independent,
-                                  staging=a.staging)
+                                  staging=a.staging or 0)
     elif a.op == "gemv_t":
         codes, scales = [], []
         for i in range(a.matrices):
@@ -96,7 +113,7 @@ def main(argv=None):
         for r in range(1 + a.reps):
             i = r % a.matrices
             mm.mm_gemv_packed4_ex(codes[i], scales[i], x, y[i], 12288, 1536, c.codebook, pdl=a.pdl,
-                                  independent=a.independent, staging=a.staging if a.staging else -1,
+                                  independent=a.independent, staging=-1 if a.staging is None else a.staging,
                                   blocks=a.rows if a.staging else 0)
     elif a.op == "gemv_batched":
         n = a.matrices
