@@ -10,7 +10,10 @@
 // accumulation order along k.
 //
 // GB300 design: a CTA computes a 128 x 128 tile of C with 8 consumer warps
-// (8 x 8 outputs per thread, 128-bit shared loads) and one producer warp that
+// (8 x 8 outputs per thread, 128-bit shared loads, the multiply-adds as packed
+// f32x2 FMAs where an operand read along m or n supplies the pairs -- two
+// outputs per instruction, each rounded once as by FFMA: identical bits, at
+// 2048^3 NN 13 %, TN 8 % and TT 14 % faster) and one producer warp that
 // streams 128 x 32 k-slabs of A and B into a 4-stage shared-memory ring with
 // TMA, each stage guarded by a "full" mbarrier (TMA transaction bytes) and an
 // "empty" mbarrier (one arrival per consumer thread).  Operands whose
@@ -160,12 +163,34 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                     b[4][kk] = v1.x; b[5][kk] = v1.y; b[6][kk] = v1.z; b[7][kk] = v1.w;
                 }
             }
+            // Packed f32x2 FMAs pair the outputs along the operand whose values one 16-byte shared
+            // load already leaves in adjacent registers: B read along n pairs columns (2 jp, 2 jp + 1),
+            // A read along m pairs rows; with both read along k, packing would cost a move per pair
+            // and plain FFMAs measured faster.
+            if constexpr (!B_KC) {
 #pragma unroll
-            for (int kk = 0; kk < 4; ++kk)
+                for (int kk = 0; kk < 4; ++kk)
 #pragma unroll
-                for (int i = 0; i < 8; ++i)
+                    for (int i = 0; i < 8; ++i)
 #pragma unroll
-                    for (int j = 0; j < 8; ++j) acc[i][j] = fmaf(a[i][kk], b[j][kk], acc[i][j]);
+                        for (int jp = 0; jp < 4; ++jp)
+                            fma2_bcast(acc[i][2 * jp], acc[i][2 * jp + 1], a[i][kk], b[2 * jp][kk], b[2 * jp + 1][kk]);
+            } else if constexpr (!A_KC) {
+#pragma unroll
+                for (int kk = 0; kk < 4; ++kk)
+#pragma unroll
+                    for (int j = 0; j < 8; ++j)
+#pragma unroll
+                        for (int ip = 0; ip < 4; ++ip)
+                            fma2_bcast(acc[2 * ip][j], acc[2 * ip + 1][j], b[j][kk], a[2 * ip][kk], a[2 * ip + 1][kk]);
+            } else {
+#pragma unroll
+                for (int kk = 0; kk < 4; ++kk)
+#pragma unroll
+                    for (int i = 0; i < 8; ++i)
+#pragma unroll
+                        for (int j = 0; j < 8; ++j) acc[i][j] = fmaf(a[i][kk], b[j][kk], acc[i][j]);
+            }
         }
         mbar_arrive(&empty[s]);
     }

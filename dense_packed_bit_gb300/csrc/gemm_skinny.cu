@@ -165,12 +165,29 @@ __global__ void __launch_bounds__(NT) gemm_skinny_kernel(const GemmArgs g, const
                     b[t][0] = v.x, b[t][1] = v.y, b[t][2] = v.z, b[t][3] = v.w;
                 }
             }
+            // packed f32x2 FMAs (two outputs per instruction, each rounded once) pair columns when
+            // op(B) is read along n, rows when op(A) is read along m; plain FFMAs otherwise
 #pragma unroll
-            for (int t = 0; t < 4; ++t)
+            for (int t = 0; t < 4; ++t) {
+                if constexpr (!TB) {
 #pragma unroll
-                for (int i = 0; i < 4; ++i)
+                    for (int i = 0; i < 4; ++i)
 #pragma unroll
-                    for (int jj = 0; jj < 4; ++jj) acc[i][jj] = fmaf(a[i][t], b[t][jj], acc[i][jj]);
+                        for (int jp = 0; jp < 2; ++jp)
+                            fma2_bcast(acc[i][2 * jp], acc[i][2 * jp + 1], a[i][t], b[t][2 * jp], b[t][2 * jp + 1]);
+                } else if constexpr (TA) {
+#pragma unroll
+                    for (int jj = 0; jj < 4; ++jj)
+#pragma unroll
+                        for (int ip = 0; ip < 2; ++ip)
+                            fma2_bcast(acc[2 * ip][jj], acc[2 * ip + 1][jj], b[t][jj], a[2 * ip][t], a[2 * ip + 1][t]);
+                } else {
+#pragma unroll
+                    for (int i = 0; i < 4; ++i)
+#pragma unroll
+                        for (int jj = 0; jj < 4; ++jj) acc[i][jj] = fmaf(a[i][t], b[t][jj], acc[i][jj]);
+                }
+            }
         }
     }
     cp_async_wait<0>();

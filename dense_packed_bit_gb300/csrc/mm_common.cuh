@@ -265,4 +265,18 @@ __device__ __forceinline__ float2 ffma2(float2 a, float2 b, float2 c) {
     return *reinterpret_cast<float2 *>(&D);
 }
 
+// (d0, d1) += a * (b0, b1): two independent fp32 FMAs, each rounded once, in one packed
+// f32x2 instruction (half the issue slots of two FFMAs; the same bits)
+__device__ __forceinline__ void fma2_bcast(float &d0, float &d1, float a, float b0, float b1) {
+    unsigned long long A, B, D;
+    asm("mov.b64 %0, {%1, %1};" : "=l"(A) : "r"(__float_as_uint(a)));
+    asm("mov.b64 %0, {%1, %2};" : "=l"(B) : "r"(__float_as_uint(b0)), "r"(__float_as_uint(b1)));
+    asm("mov.b64 %0, {%1, %2};" : "=l"(D) : "r"(__float_as_uint(d0)), "r"(__float_as_uint(d1)));
+    asm("fma.rn.f32x2 %0, %1, %2, %0;" : "+l"(D) : "l"(A), "l"(B));
+    unsigned lo, hi;
+    asm("mov.b64 {%0, %1}, %2;" : "=r"(lo), "=r"(hi) : "l"(D));
+    d0 = __uint_as_float(lo);
+    d1 = __uint_as_float(hi);
+}
+
 }  // namespace mm
