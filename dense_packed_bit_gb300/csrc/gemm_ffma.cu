@@ -45,6 +45,8 @@ struct FfmaParams {
     int M, N, K;
     float *C;
     int64_t ldc;
+    const float *bias;  // C = act(op(A) op(B) + bias): bias per column or null, act 1 = GELU (tanh)
+    int act;
 };
 
 // A_KC: the A tile sits in shared memory as [m][k] (k contiguous, 128-byte
@@ -197,6 +199,18 @@ __global__ void __launch_bounds__(NTHREADS, 1)
 
     // ---------------------------------------------------- epilogue (masked)
     const bool vec_ok = !B_KC && (p.ldc % 4 == 0) && ((reinterpret_cast<uintptr_t>(p.C) & 15) == 0);
+    if (p.bias || p.act) {
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+            const int n = n0 + colB[j];
+            const float bj = (p.bias && n < p.N) ? __ldg(p.bias + n) : 0.f;
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                const float z = acc[i][j] + bj;
+                acc[i][j] = p.act ? gelu_tanh_f(z) : z;
+            }
+        }
+    }
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
         const int m = m0 + rowA[i];
@@ -261,7 +275,7 @@ cudaError_t launch_gemm_ffma(const GemmArgs &g, int tile, cudaStream_t s) {
         e = make_tmap_2d(&tb, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, g.B, g.K, g.N, g.ldb * 4, BK, BN,
                          CU_TENSOR_MAP_SWIZZLE_128B);
     if (e != cudaSuccess) return e;
-    FfmaParams p{(int)g.M, (int)g.N, (int)g.K, g.C, g.ldc};
+    FfmaParams p{(int)g.M, (int)g.N, (int)g.K, g.C, g.ldc, g.bias, g.act};
     if (!g.transA && !g.transB) return launch_ffma<true, false>(ta, tb, p, s);
     if (!g.transA && g.transB) return launch_ffma<true, true>(ta, tb, p, s);
     if (g.transA && !g.transB) return launch_ffma<false, false>(ta, tb, p, s);

@@ -696,7 +696,19 @@ cudaError_t launch_gemm_tf32x3_ws_splitk(const GemmArgs &g, int pair, int ksplit
 // Automatic K split.  Tiles that leave more than half of the persistent grid idle: split-K,
 // as many slices as keep every tile's slices within one wave, at least 4 slabs of 16 per
 // slice, at most 16.  Several waves of tiles with a costly partial last wave: stream-K.
+static int gemm_splitk_auto_shape(int64_t M, int64_t N, int64_t K, int pair, int sms);
+
+// The shape's choice (below), raised to the K slices that keep every accumulation within the
+// 3xTF32 accuracy margin: a K longer than kTf32x3MaxK never runs stream-K nor one slice.
 int gemm_splitk_auto(int64_t M, int64_t N, int64_t K, int pair, int sms) {
+    const int64_t need = (K + kTf32x3MaxK - 1) / kTf32x3MaxK;
+    const int s = gemm_splitk_auto_shape(M, N, K, pair, sms);
+    if (need <= 1) return s;
+    const int64_t r = s == kStreamK || s < need ? need : s;
+    return r > 16 ? 16 : (int)r;
+}
+
+static int gemm_splitk_auto_shape(int64_t M, int64_t N, int64_t K, int pair, int sms) {
     const int cg = pair ? 2 : 1;
     const int64_t tiles = ((M + 128 * cg - 1) / (128 * cg)) * ((N + 255) / 256);
     const int64_t kt = (K + BK - 1) / BK;

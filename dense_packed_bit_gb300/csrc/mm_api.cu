@@ -170,7 +170,12 @@ mm_status mm_gemm_f32_ex(int transA, int transB, int64_t M, int64_t N, int64_t K
     }
     if (path == MM_GEMM_TF32X3 && !mm::gemm_tf32x3_supported(g))
         return fail(MM_ERR_INVALID_ARG, "3xTF32 path needs 16-byte aligned A, B and lda, ldb multiples of 4");
-    if ((path == MM_GEMM_TF32X3 || path == MM_GEMM_AUTO) && mm::gemm_tf32x3_supported(g))
+    // beyond the 3xTF32 accuracy margin: refused when asked for, the FFMA kernels when automatic
+    const bool long_k = K > mm::kTf32x3MaxK;
+    if (long_k && (path == MM_GEMM_TF32X3 || (path == MM_GEMM_AUTO && tile != 0)))
+        return fail(MM_ERR_INVALID_ARG, "3xTF32 needs K <= %lld (its accuracy margin), got K=%lld",
+                    (long long)mm::kTf32x3MaxK, (long long)K);
+    if ((path == MM_GEMM_TF32X3 || path == MM_GEMM_AUTO) && !long_k && mm::gemm_tf32x3_supported(g))
         // automatic: CTA pairs (256-row tiles) once M fills them, one CTA per 128-row tile below that
         e = tile == 1 ? mm::launch_gemm_tf32x3(g, st)
                       : mm::launch_gemm_tf32x3_ws(g, (tile == 3 || (tile == 0 && M > 128)) ? 1 : 0, st);
@@ -193,13 +198,20 @@ namespace {
 // The split a split-K call uses and the workspace it needs: `splitk` itself when given (1..16
 // slices, -1 stream-K), else the automatic choice for the tile shape the call runs (CTA pairs
 // when M > 128).  Stream-K sizes depend on the SM count, so they query the device.
+// A split whose every accumulation stays within the 3xTF32 accuracy margin (K slices of at most
+// kTf32x3MaxK; stream-K segments never exceed K).  Any other split runs the FFMA kernel unsplit,
+// needing no workspace.
+bool split_within_margin(int64_t K, int sk) {
+    return sk == mm::kStreamK ? K <= mm::kTf32x3MaxK : (K + sk - 1) / sk <= mm::kTf32x3MaxK;
+}
+
 mm_status resolve_splitk(int64_t M, int64_t N, int64_t K, int splitk, int *out, int64_t *floats) {
     if (splitk < -1 || splitk > 16)
         return fail(MM_ERR_INVALID_ARG, "splitk must be 0 (automatic), 1..16 (slices) or -1 (stream-K)");
     const int pair = M > 128 ? 1 : 0;
     if (splitk > 0) {
         *out = (int)(splitk > (K + 15) / 16 ? (K + 15) / 16 : splitk);
-        *floats = mm::gemm_splitk_workspace_floats(M, N, K, pair, *out, 0);
+        *floats = split_within_margin(K, *out) ? mm::gemm_splitk_workspace_floats(M, N, K, pair, *out, 0) : 0;
         return MM_OK;
     }
     mm_status s = check_device();
@@ -209,7 +221,7 @@ mm_status resolve_splitk(int64_t M, int64_t N, int64_t K, int splitk, int *out, 
     if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
     if (e != cudaSuccess) return cuda_fail(e, "cudaDeviceGetAttribute");
     *out = splitk == mm::kStreamK ? mm::kStreamK : mm::gemm_splitk_auto(M, N, K, pair, sms);
-    *floats = mm::gemm_splitk_workspace_floats(M, N, K, pair, *out, sms);
+    *floats = split_within_margin(K, *out) ? mm::gemm_splitk_workspace_floats(M, N, K, pair, *out, sms) : 0;
     return MM_OK;
 }
 
@@ -286,8 +298,11 @@ mm_status gemm_splitk_impl(int transA, int transB, int64_t M, int64_t N, int64_t
     g.act = act;
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
     cudaError_t e;
-    // operands TMA cannot describe take the unsplit general kernel (the workspace is unused)
-    if (mm::gemm_tf32x3_supported(g)) e = mm::launch_gemm_tf32x3_ws_splitk(g, M > 128 ? 1 : 0, sk, workspace, st);
+    // operands TMA cannot describe take the unsplit general kernel, and a split whose slices would
+    // exceed the 3xTF32 accuracy margin the unsplit FFMA kernel (the workspace is then unused)
+    if (mm::gemm_tf32x3_supported(g) && split_within_margin(K, sk))
+        e = mm::launch_gemm_tf32x3_ws_splitk(g, M > 128 ? 1 : 0, sk, workspace, st);
+    else if (mm::gemm_ffma_supported(g)) e = mm::launch_gemm_ffma(g, 0, st);
     else e = mm::launch_gemm_simple(g, st);
     if (e != cudaSuccess) return cuda_fail(e, "gemm launch");
     return ok();
@@ -339,9 +354,12 @@ mm_status mm_gemm_f32_bias_act(int transA, int transB, int64_t M, int64_t N, int
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
     // few rows: the cluster split-K FFMA kernel; else the warp-specialised 3xTF32 kernel when TMA can
     // describe the operands, else the plain tiled one
-    cudaError_t e = skinny_auto(M, N)               ? mm::launch_gemm_skinny(g, 0, st)
-                    : mm::gemm_tf32x3_supported(g) ? mm::launch_gemm_tf32x3_ws(g, M > 128 ? 1 : 0, st)
-                                                   : mm::launch_gemm_simple(g, st);
+    // (a K beyond the 3xTF32 accuracy margin: the TMA-staged FFMA kernel)
+    const bool long_k = K > mm::kTf32x3MaxK;
+    cudaError_t e = skinny_auto(M, N)                           ? mm::launch_gemm_skinny(g, 0, st)
+                    : !long_k && mm::gemm_tf32x3_supported(g) ? mm::launch_gemm_tf32x3_ws(g, M > 128 ? 1 : 0, st)
+                    : mm::gemm_ffma_supported(g)               ? mm::launch_gemm_ffma(g, 0, st)
+                                                               : mm::launch_gemm_simple(g, st);
     if (e != cudaSuccess) return cuda_fail(e, "gemm launch");
     return ok();
 }
@@ -362,9 +380,16 @@ mm_status mm_gemm_f32_splitk_noalloc(int transA, int transB, int64_t M, int64_t 
     mm_status s = mm_gemm_f32_splitk_workspace(M, N, K, splitk, &need);
     if (s != MM_OK) return s;
     if (!splitk && need > mm::kSplitkStaticFloats) {
-        // the automatic split does not fit the scratch (stream-K of a large product): no split
-        splitk = 1;
-        need = 0;
+        // the automatic split does not fit the scratch: K slices take the most slices that fit (no
+        // split below two); stream-K (one partial tile per CTA of a large product) runs unsplit
+        int sk = 1;
+        int64_t auto_need = 0;
+        s = resolve_splitk(M, N, K, 0, &sk, &auto_need);
+        if (s != MM_OK) return s;
+        const int64_t fit = mm::kSplitkStaticFloats / (M * N);
+        splitk = (sk > 1 && fit >= 2) ? (int)(fit < sk ? fit : sk) : 1;
+        s = mm_gemm_f32_splitk_workspace(M, N, K, splitk, &need);
+        if (s != MM_OK) return s;
     }
     if (need > mm::kSplitkStaticFloats)
         return fail(MM_ERR_INVALID_ARG,

@@ -195,6 +195,13 @@ cudaError_t launch_gemm_tf32x3_ws(const GemmArgs &g, int pair, cudaStream_t s);
 // 16-byte aligned), then summed in slice order into C by a second kernel.
 // ksplit == kStreamK: stream-K instead, ws holding the units' partial-tile slots and flags.
 constexpr int kStreamK = -1;
+
+// Longest K one 3xTF32 accumulation may cover.  The tensor core's fp32 accumulation error
+// grows like sqrt(K): worst |C - C_ref| / sum_k |a_ik b_kj| measured 3.3e-6 at K = 2048 and
+// 5.2e-6 at K = 8192 (N(0, 0.02) operands), so about 7.4e-6 at 16,384 and past the 1e-5
+// bound near 3e4.  A longer K runs the FFMA kernels (fp32 FMA, one rounding per step) or,
+// in the split entry points, K slices of at most this length added in fp32.
+constexpr int64_t kTf32x3MaxK = 16384;
 cudaError_t launch_gemm_tf32x3_ws_splitk(const GemmArgs &g, int pair, int ksplit, float *ws, cudaStream_t s);
 int gemm_splitk_auto(int64_t M, int64_t N, int64_t K, int pair, int sms);
 int64_t gemm_splitk_workspace_floats(int64_t M, int64_t N, int64_t K, int pair, int split, int sms);

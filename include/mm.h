@@ -89,6 +89,11 @@ const char *mm_last_error(void);
 
 /*
  * Dense fp32 GEMM, C = op(A) . op(B).  M, N, K >= 1.
+ * Kernel: M <= 64 with few output tiles, the few-rows FFMA kernel; else the 3xTF32
+ * tensor-core kernel when A and B are 16-byte aligned with lda, ldb multiples of 4
+ * and K <= 16384 (its accuracy margin: the tensor core's fp32 accumulation error
+ * grows like sqrt(K) and would pass the bound near K = 3e4); else the TMA-staged
+ * FFMA kernel, or the plain tiled one for operands TMA cannot describe.
  * Errors: MM_ERR_INVALID_ARG for a null pointer, a dimension < 1, a leading
  * dimension below the stored width, or C overlapping A or B.
  */
@@ -182,7 +187,11 @@ mm_status mm_gemm_f32_bias_act_splitk(int transA, int transB, int64_t M, int64_t
  * splitk = 0: automatic (no split when the tiles fill the GPU, stream-K when they
  * fill more than half of it, split slices otherwise).  Results are
  * bit-reproducible run to run; they may differ from mm_gemm_f32 in the last bits,
- * by summation order.  Same bound |C - C_exact| <= 1e-5 sum|a b|.
+ * by summation order.  Same bound |C - C_exact| <= 1e-5 sum|a b|.  Every 3xTF32
+ * accumulation stays within K <= 16384 (mm_gemm_f32): the automatic split uses at
+ * least ceil(K / 16384) slices, and a split that would exceed it (fewer slices,
+ * stream-K with K > 16384, or K beyond 16 slices of 16384) runs the TMA-staged FFMA
+ * kernel unsplit, with a workspace need of 0.
  *
  * workspace: caller-owned device memory, 16-byte aligned, at least the number of
  * floats mm_gemm_f32_splitk_workspace reports for the same M, N, K, splitk
@@ -224,16 +233,20 @@ mm_status mm_gemm_f32_splitk(int transA, int transB, int64_t M, int64_t N, int64
  *
  * Same arguments, result and errors as mm_gemm_f32_splitk, plus
  * MM_ERR_INVALID_ARG when a given split needs more than
- * MM_SPLITK_NOALLOC_MAX_FLOATS floats (splitk * M * N); an automatic split
- * that would need more is replaced by no split.  splitk = -1 is refused.  The first call on a
- * device looks up the array's device address (cudaGetSymbolAddress, with that
- * device current); make that first call before any stream capture.  Every call
- * shares the one array and leaves its partial tiles there.  The caller clears
- * nothing: a call writes every partial tile before reading it, and when the
- * automatic split is stream-K the call itself zeroes (cudaMemsetAsync on
- * `stream`) the hand-over flags it keeps in the array.  Calls whose kernels overlap on
- * the GPU (on different streams, or from different threads) race on the array
- * and may return wrong results: serialise them.
+ * MM_SPLITK_NOALLOC_MAX_FLOATS floats (splitk * M * N).  An automatic split that
+ * would need more takes the most K slices that fit (at least two; M * N * slices
+ * <= MM_SPLITK_NOALLOC_MAX_FLOATS), and otherwise runs unsplit; an automatic
+ * stream-K split (one 128 x 256 partial tile per CTA: about 5M floats on a
+ * 152-SM GB300) never fits and so runs unsplit.  splitk = -1 is refused.  The
+ * first call on a device looks up the array's device address
+ * (cudaGetSymbolAddress, with that device current) and caches it for the life of
+ * the process: make that first call before any stream capture, and do not call
+ * this entry point on a device after cudaDeviceReset of that device (the cached
+ * address would be stale).  Every call shares the one array and leaves its partial
+ * tiles there.  The caller clears nothing: a call writes every partial tile before
+ * reading it.  Calls whose kernels overlap on the GPU (on different streams, or
+ * from different threads) race on the array and may return wrong results:
+ * serialise them.
  */
 #define MM_SPLITK_NOALLOC_MAX_FLOATS 4194304
 mm_status mm_gemm_f32_splitk_noalloc(int transA, int transB, int64_t M, int64_t N, int64_t K,

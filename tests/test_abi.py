@@ -340,6 +340,11 @@ def test_gemm_bias_act_splitk_argument_errors(lib, case):
     ((64, 3072, 768), 12, 12 * 64 * 3072),
     # 2 tiles: 76 slices would be too thin, capped at K / 64 = 8 slices
     ((100, 300, 500), 8, 8 * 100 * 300),
+    # K past the 3xTF32 margin of 16384: at least ceil(K / 16384) slices, never stream-K nor none
+    ((4096, 4096, 16384), -1, 2 * 76 * 32768 + 152),
+    ((4096, 4096, 32768), 2, 2 * 4096 * 4096),
+    ((8192, 8192, 20000), 2, 2 * 8192 * 8192),
+    ((4096, 4096, 40000), 3, 3 * 4096 * 4096),
 ])
 def test_gemm_split_plan(shape, split, floats):
     mm.load_library()
@@ -360,3 +365,13 @@ def test_probe_bounded_wait_argument_errors(lib, arrive, limit, out):
     # arrive 0 / 1; limit 1 us .. 0.1 s, so the probe can never hold a GPU long; out 8-byte aligned
     st = lib.mm_probe_bounded_wait(arrive, limit, out, None)
     assert st == mm.MM_ERR_INVALID_ARG, lib.mm_last_error()
+
+
+@pytest.mark.parametrize("K,splitk,floats", [
+    (16384, 1, 0), (16384, 2, 2 * 256 * 256),
+    # slices longer than 16384 would break the 3xTF32 margin: such a split runs unsplit, no workspace
+    (40000, 2, 0), (40000, 3, 3 * 256 * 256), (300000, 16, 0),
+])
+def test_split_workspace_respects_the_k_margin(K, splitk, floats):
+    mm.load_library()
+    assert mm.mm_gemm_f32_splitk_workspace(256, 256, K, splitk) == floats

@@ -177,3 +177,24 @@ def test_bias_act_padded_leading_dims(oracle, layout):
     Y, T, Z = oracle.gemm_bias_act(tA, tB, M, N, K, A, B, bias, 1, lda=A.shape[1], ldb=B.shape[1])
     check(got[:, :N], Y, T, Z, f"{layout} padded")
     assert np.all(np.isnan(got[:, N:])), "write into the padding of C"
+
+
+@pytest.mark.parametrize("M", [48, 1024])
+def test_gelu_epilogue_within_the_activation_term_alone(oracle, M):
+    # K = 1, A = z_r (row r), B = 1 and bias_j = j 2^-12 make every pre-activation z = z_r + bias_j
+    # exact in fp32 (z_r multiples of 2^-6 in [-12, 12]; 3xTF32's hi + lo split of z_r adds back to
+    # z_r), so the whole error is the fp32 activation's: it must fit the bound's activation term
+    # 2^-20 (1 + |z|) with the GEMM term 1.13e-5 T left out.  M = 48 takes the few-rows kernel,
+    # M = 1024 the 3xTF32 one.
+    N = 64
+    zr = np.round((-12.0 + 24.0 * np.arange(M) / (M - 1)) * 64.0) / 64.0
+    A = zr.astype(np.float32).reshape(M, 1)
+    B = np.ones((1, N), np.float32)
+    bias = (np.arange(N) * 2.0 ** -12).astype(np.float32)
+    Y, T, Z = oracle.gemm_bias_act(0, 0, M, N, 1, A, B, bias, act=1)
+    assert np.array_equal(Z.astype(np.float32).astype(np.float64), Z), "pre-activations exact in fp32"
+    got = run(0, 0, M, N, 1, A, B, bias, 1).astype(np.float64)
+    err = np.abs(got - Y)
+    bound = 2.0 ** -20 * (1.0 + np.abs(Z))
+    assert np.all(err <= bound), f"worst {float(np.max(err / bound)):.3f} of the activation term"
+    print(f"M={M}: worst error {float(np.max(err / bound)):.4f} of 2^-20 (1 + |z|)")

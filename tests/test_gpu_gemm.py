@@ -383,3 +383,64 @@ def test_gemm_skinny_is_automatic_for_few_rows_and_deterministic(oracle):
     A, B = stored(1, 1, 48, 1000, 777, seed=5, kind="int")
     C = run(1, 1, 48, 1000, 777, A, B)
     check_exact(C, oracle.gemm(1, 1, 48, 1000, 777, A, B)[0], "few rows, integers")
+
+
+# ------------------------------------------------------------------ the 3xTF32 accuracy margin on K
+
+def test_tf32x3_k_margin_boundary(oracle):
+    # K = 16384 is the longest 3xTF32 accumulation: taken when asked for, and automatically; past it
+    # (16388: still a multiple of 4, so that TMA could describe the operands) an explicit 3xTF32
+    # request is refused while the automatic path runs the FFMA kernel -- both within the bound.
+    # N(0, 0.02) operands, the distribution the margin was measured on.
+    M, N = 256, 192
+    for K in (16384, 16388):
+        A = synth.normal_f32(6100 + K, (M, K), 0.02)
+        B = synth.normal_f32(6200 + K, (K, N), 0.02)
+        ref, T = oracle.gemm(0, 0, M, N, K, A, B)
+        C = run(0, 0, M, N, K, A, B)
+        check_bound(C, ref, T, f"automatic path, K={K}")
+        if K <= 16384:
+            check_bound(run(0, 0, M, N, K, A, B, path=mm.MM_GEMM_TF32X3), ref, T, f"3xTF32, K={K}")
+        else:
+            with pytest.raises(mm.MMError, match="3xTF32 needs K <= 16384"):
+                run(0, 0, M, N, K, A, B, path=mm.MM_GEMM_TF32X3)
+            check_bound(run(0, 0, M, N, K, A, B, path=mm.MM_GEMM_FFMA), ref, T, f"FFMA, K={K}")
+
+
+def test_bias_act_beyond_the_k_margin(oracle):
+    # bias + GELU with K past the margin: the TMA-staged FFMA kernel with its fused epilogue
+    M, N, K = 160, 130, 16400
+    A = synth.normal_f32(6301, (M, K), 0.02)
+    B = synth.normal_f32(6302, (K, N), 0.02)
+    bias = synth.normal_f32(6303, (N,), 0.02)
+    for act in (0, 1):
+        Y, T, Z = oracle.gemm_bias_act(0, 0, M, N, K, A, B, bias, act)
+        dC = empty_f32((M, N))
+        mm.mm_gemm_f32_bias_act(0, 0, M, N, K, to_dev(A), K, to_dev(B), N, to_dev(bias), act, dC, N)
+        mm.mm_check_device_error()
+        got = to_host(dC).astype(np.float64)
+        bound = 1.13e-5 * T + 2.0 ** -20 * (1.0 + np.abs(Z))
+        assert np.all(np.abs(got - Y) <= bound), f"act {act}: worst {np.max(np.abs(got - Y) / bound):.3f} of the bound"
+
+
+def test_splitk_keeps_every_slice_within_the_k_margin(oracle):
+    import torch
+    # K = 40000 on one output tile: the automatic split takes at least 3 slices of <= 16384; an
+    # explicit 2-slice split would leave 20000-long slices, so it runs the FFMA kernel unsplit and
+    # needs no workspace; stream-K likewise
+    M, N, K = 128, 256, 40000
+    A = synth.normal_f32(6401, (M, K), 0.02)
+    B = synth.normal_f32(6402, (K, N), 0.02)
+    ref, T = oracle.gemm(0, 0, M, N, K, A, B)
+    dA, dB = to_dev(A), to_dev(B)
+    auto_split, _ = mm.mm_gemm_f32_split_plan(M, N, K, 152)
+    assert auto_split >= 3
+    for splitk in (0, 2, 3, -1):
+        need = mm.mm_gemm_f32_splitk_workspace(M, N, K, splitk)
+        if splitk in (2, -1):
+            assert need == 0
+        ws = torch.full((max(need, 1),), float("nan"), dtype=torch.float32, device=dA.device)
+        dC = empty_f32((M, N))
+        mm.mm_gemm_f32_splitk(0, 0, M, N, K, dA, K, dB, N, dC, N, splitk, ws if need else None, need)
+        mm.mm_check_device_error()
+        check_bound(to_host(dC), ref, T, f"split {splitk}, K={K}")

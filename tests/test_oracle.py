@@ -443,6 +443,31 @@ def test_gelu_tanh_matches_erf_form(oracle):
     assert np.abs(wrong_cubic - exact).max() > 5e-3
 
 
+def test_gelu_tanh_matches_the_library_tanh_gelu(oracle):
+    # PyTorch's own GELU in its tanh form (an independent implementation of GPT-2's published
+    # activation), in fp64 on the CPU: agreement to rounding, so a slip in either constant at any
+    # of its printed digits fails -- shown on two planted slips
+    import torch
+    z = np.linspace(-12.0, 12.0, 24001)
+    lib = torch.nn.functional.gelu(torch.from_numpy(z), approximate="tanh").numpy()
+    # (where 1 + tanh(u) cancels, below z = -7, the two evaluations differ by rounding, < 1e-15)
+    assert np.allclose(oracle.gelu_tanh(z), lib, rtol=1e-13, atol=1e-14)
+
+    def planted(c, a):  # the tanh form with given constants, for the planted slips only
+        return 0.5 * z * (1.0 + np.tanh(c * (z + a * z ** 3)))
+    c0 = np.sqrt(2.0 / np.pi)
+    for c, a in ((c0, 0.04472), (c0 * (1 + 1e-5), 0.044715)):
+        assert not np.allclose(planted(c, a), lib, rtol=1e-13, atol=1e-14), (c, a)
+
+
+def test_gelu_tanh_small_z_series_fixes_the_scale(oracle):
+    # z/2 (1 + tanh(c z + ...)) = z/2 + (c/2) z^2 + O(z^4): the z^2 coefficient is 1/sqrt(2 pi), the
+    # exact GELU's (z Phi(z) = z/2 + z^2/sqrt(2 pi) + ...), which fixes c = sqrt(2/pi)
+    for z in (1e-3, -1e-3, 2e-4):
+        coef = (float(oracle.gelu_tanh(z)) - z / 2) / z ** 2
+        assert abs(coef * np.sqrt(2 * np.pi) - 1.0) < 1e-5
+
+
 def test_gelu_tanh_special_values(oracle):
     g = oracle.gelu_tanh(np.array([0.0, 10.0, -10.0, 30.0]))
     assert g[0] == 0.0 and g[1] == 10.0 and g[2] == 0.0 and g[3] == 30.0

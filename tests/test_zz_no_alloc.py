@@ -79,3 +79,32 @@ def test_noalloc_automatic_split_falls_back_when_scratch_is_small(oracle):
     jj = np.concatenate([np.tile(np.arange(N), 2), rng.integers(0, N, 3000)])
     ref, T = oracle.gemm_at(0, 0, K, A, B, ii, jj)
     check_bound(got[ii, jj], ref, T, "4096^3 through the static-scratch entry point")
+
+
+def test_noalloc_automatic_split_takes_the_most_slices_that_fit(oracle):
+    # 128 x 12288 x 4096: the automatic split is 3 K slices (48 tiles on 152 SMs), 4.7M floats, more
+    # than the scratch holds; the entry point then takes the 2 slices that fit (3.1M floats) rather
+    # than no split
+    M, N, K = 128, 12288, 4096
+    assert mm.mm_gemm_f32_split_plan(M, N, K, 152)[0] == 3
+    assert 3 * M * N > mm.MM_SPLITK_NOALLOC_MAX_FLOATS >= 2 * M * N
+    A = synth.normal_f32(4400, (M, K), 0.02)
+    B = synth.normal_f32(4401, (K, N), 0.02)
+    dA, dB = to_dev(A), to_dev(B)
+    C = empty_f32((M, N))
+    mm.mm_gemm_f32_splitk_noalloc(0, 0, M, N, K, dA, K, dB, N, C, N, 0)
+    mm.mm_check_device_error()
+    got = to_host(C)
+    # bit-identical to the workspace entry point's explicit 2-slice split (same kernels, same order)
+    import torch
+    need = mm.mm_gemm_f32_splitk_workspace(M, N, K, 2)
+    ws = torch.empty((need,), dtype=torch.float32, device=dA.device)
+    C2 = empty_f32((M, N))
+    mm.mm_gemm_f32_splitk(0, 0, M, N, K, dA, K, dB, N, C2, N, 2, ws, need)
+    mm.mm_check_device_error()
+    assert np.array_equal(got.view(np.uint32), to_host(C2).view(np.uint32))
+    rng = np.random.default_rng(4)
+    ii = np.concatenate([np.repeat([0, M - 1], N), rng.integers(0, M, 3000)])
+    jj = np.concatenate([np.tile(np.arange(N), 2), rng.integers(0, N, 3000)])
+    ref, T = oracle.gemm_at(0, 0, K, A, B, ii, jj)
+    check_bound(got[ii, jj], ref, T, "128 x 12288 x 4096 through the static-scratch entry point")
