@@ -11,7 +11,7 @@ it, for every decode of mm_gemv_packed2_ex:
   TMA-staged affine: 128-row blocks per CTA (eight warps split K);
   mma.sync decodes: warps per row x 16-row blocks per warp, or 64-row blocks per
   CTA when staged;
-  fp8 / tcgen05 / fp4 tensor-core decodes: row blocks or 127-row tiles per CTA;
+  fp8 mma.sync, tcgen05 fp8 and tcgen05 fp4 decodes: row blocks or 127-row tiles per CTA;
   the batched fp4 launch: tiles per CTA.
 
 Each configuration runs the 64 distinct seeded matrices (288 MiB, more than L2)
@@ -50,7 +50,7 @@ def configs():
     for blocks in (1, 2, 4, 8):
         out.append(("fp8 mma.sync", dict(dequant=4, rows_per_lane=blocks)))
     for tiles in (1, 2, 4):
-        out.append(("tcgen05 f16", dict(dequant=5, rows_per_lane=tiles)))
+        out.append(("tcgen05 fp8", dict(dequant=5, rows_per_lane=tiles)))
     for tiles in (1, 2, 4):
         out.append(("tcgen05 mxf4", dict(dequant=6, rows_per_lane=tiles)))
     return out
