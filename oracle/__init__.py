@@ -1,4 +1,4 @@
-"""CPU oracle for the dense fp32 GEMM and the packed 2-bit GEMV / skinny GEMM.
+"""CPU oracle for the dense fp32 GEMM, the packed 2-bit GEMV / skinny GEMM and attention.
 
 TEST INFRASTRUCTURE.  Only the tests, the smoke check and the bench's CPU
 baseline leg may import this package.  The product library never loads it and
@@ -14,9 +14,12 @@ textbook small products, exact integer products against numpy int64 matmul,
 the fp16 decoder against numpy's float16 for all 65,536 patterns, the unpacker
 against a hand-written byte table and a pack/unpack round trip, and the packed
 GEMM against dense products of explicitly decoded weights; the GELU of the fused
-epilogue (gelu_tanh, gemm_bias_act) against its odd-part identity, the
-library's normal CDF (z Phi(z), which the tanh form approximates) and special
-values, and the bias broadcast on a zero product.
+epilogue (gelu_tanh, gemm_bias_act) against the library's fp64 tanh GELU, its
+small-z series, its odd-part identity, the library's normal CDF and special
+values, and the bias broadcast on a zero product; attention (attention.c)
+against the library's fp64 scaled-dot-product attention, log-sum-exp and
+autograd gradients, the uniform-weights closed form (Q = 0) and the causal
+first row.
 """
 from __future__ import annotations
 
@@ -29,17 +32,18 @@ import numpy as np
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 _SRC = os.path.join(_HERE, "oracle.c")
+_SRCS = (_SRC, os.path.join(_HERE, "attention.c"))
 _LIB = os.path.join(_HERE, "liboracle.so")
 _lock = threading.Lock()
 _lib = None
 
 
 def build(force: bool = False) -> str:
-    """Compile oracle.c into oracle/liboracle.so with gcc (plain -O2, portable)."""
-    if force or not os.path.exists(_LIB) or os.path.getmtime(_LIB) < os.path.getmtime(_SRC):
+    """Compile oracle.c and attention.c into oracle/liboracle.so with gcc (plain -O2, portable)."""
+    if force or not os.path.exists(_LIB) or any(os.path.getmtime(_LIB) < os.path.getmtime(f) for f in _SRCS):
         tmp = _LIB + f".tmp{os.getpid()}"
         subprocess.check_call(["gcc", "-O2", "-std=c11", "-fPIC", "-shared", "-pthread",
-                               "-o", tmp, _SRC, "-lm"])
+                               "-o", tmp, *_SRCS, "-lm"])
         os.replace(tmp, _LIB)
     return _LIB
 
@@ -65,6 +69,9 @@ def _load():
             lib.orc_pack4.argtypes = [P, I64, I64, P]
             lib.orc_packed4_gemm.argtypes = [P, P, P, I64, I64, I64, P, P, P, I]
             lib.orc_packed4_gemm_at.argtypes = [P, P, P, I64, P, I64, P, P, P, P]
+            D = ctypes.c_double
+            lib.orc_attention_fwd.argtypes = [P, P, P, I64, I64, I64, I, D, P, P, P, I]
+            lib.orc_attention_bwd.argtypes = [P, P, P, P, I64, I64, I64, I, D, P, P, P, P, P, P, I]
             _lib = lib
     return _lib
 
@@ -245,3 +252,40 @@ def packed4_gemm_at(codes, scales, X, cols: int, codebook, mm, rr):
     lib.orc_packed4_gemm_at(_ptr(codes), _ptr(scales), _ptr(X), cols, _ptr(cb), len(mm),
                             _ptr(mm), _ptr(rr), _ptr(Y), _ptr(T))
     return Y, T
+
+
+# ------------------------------------------------------------------ attention (attention.c)
+
+def attention_fwd(Q, K, V, causal: int, scale: float, threads: int | None = None):
+    """(O, L, TO) of softmax(scale Q K^T (+ causal mask)) V per head, in fp64.
+
+    Q, K, V: fp32 arrays of shape (heads, T, D).  L[h, i] = log sum_k exp(S[h, i, k]) (the
+    log-sum-exp of the row's scaled, unmasked scores); TO = sum_k P |V|, the bound scale.
+    scale is taken as given (pass the fp32 value the GPU multiplies by)."""
+    lib = _load()
+    Q = np.ascontiguousarray(Q, dtype=np.float32)
+    K = np.ascontiguousarray(K, dtype=np.float32)
+    V = np.ascontiguousarray(V, dtype=np.float32)
+    BH, T, D = Q.shape
+    assert K.shape == Q.shape and V.shape == Q.shape
+    O = np.empty((BH, T, D), dtype=np.float64)
+    L = np.empty((BH, T), dtype=np.float64)
+    TO = np.empty((BH, T, D), dtype=np.float64)
+    lib.orc_attention_fwd(_ptr(Q), _ptr(K), _ptr(V), BH, T, D, int(causal), float(scale), _ptr(O), _ptr(L),
+                          _ptr(TO), threads or default_threads())
+    return O, L, TO
+
+
+def attention_bwd(Q, K, V, dO, causal: int, scale: float, threads: int | None = None):
+    """(dQ, dK, dV, TdQ, TdK, TdV): the gradients of sum(O * dO) with respect to Q, K and V,
+    in fp64, with their bound scales (see attention.c)."""
+    lib = _load()
+    Q = np.ascontiguousarray(Q, dtype=np.float32)
+    K = np.ascontiguousarray(K, dtype=np.float32)
+    V = np.ascontiguousarray(V, dtype=np.float32)
+    dO = np.ascontiguousarray(dO, dtype=np.float32)
+    BH, T, D = Q.shape
+    out = [np.empty((BH, T, D), dtype=np.float64) for _ in range(6)]
+    lib.orc_attention_bwd(_ptr(Q), _ptr(K), _ptr(V), _ptr(dO), BH, T, D, int(causal), float(scale),
+                          *[_ptr(a) for a in out], threads or default_threads())
+    return tuple(out)

@@ -494,3 +494,77 @@ def test_gemm_bias_act_without_bias_is_gemm(oracle):
     C, T = oracle.gemm(0, 0, 33, 21, 17, A, B)
     Y, T2, Z = oracle.gemm_bias_act(0, 0, 33, 21, 17, A, B, None, act=0)
     assert np.array_equal(Y, C) and np.array_equal(T2, T) and np.array_equal(Z, C)
+
+
+# ------------------------------------------------------------------ attention ("Flash Attention 2")
+
+def _attn_inputs(seed, BH, T, D):
+    rng = np.random.default_rng(seed)
+    return [rng.standard_normal((BH, T, D)).astype(np.float32) for _ in range(4)]
+
+
+@pytest.mark.parametrize("causal", [0, 1])
+@pytest.mark.parametrize("shape", [(2, 37, 16), (1, 64, 64), (3, 5, 8)])
+def test_attention_fwd_matches_the_library_attention(oracle, causal, shape):
+    # PyTorch's own scaled-dot-product attention and log-sum-exp, in fp64 on the CPU (independent
+    # implementations of the definition): agreement to rounding
+    import torch
+    BH, T, D = shape
+    Q, K, V, _ = _attn_inputs(11 + T, BH, T, D)
+    scale = np.float32(1.0 / np.sqrt(D))
+    O, L, TO = oracle.attention_fwd(Q, K, V, causal, float(scale))
+    q, k, v = (torch.from_numpy(a.astype(np.float64)) for a in (Q, K, V))
+    ref = torch.nn.functional.scaled_dot_product_attention(q, k, v, is_causal=bool(causal), scale=float(scale))
+    assert np.allclose(O, ref.numpy(), rtol=1e-12, atol=1e-13)
+    S = float(scale) * (q @ k.transpose(1, 2))
+    if causal:
+        S = S.masked_fill(torch.triu(torch.ones(T, T, dtype=torch.bool), 1), float("-inf"))
+    assert np.allclose(L, torch.logsumexp(S, dim=-1).numpy(), rtol=1e-13, atol=1e-13)
+    assert np.all(TO >= np.abs(O) - 1e-12)
+
+
+@pytest.mark.parametrize("causal", [0, 1])
+def test_attention_bwd_matches_library_autograd(oracle, causal):
+    # the gradients of sum(O * dO) by PyTorch autograd through its fp64 attention
+    import torch
+    BH, T, D = 2, 33, 16
+    Q, K, V, dO = _attn_inputs(21 + causal, BH, T, D)
+    scale = float(np.float32(0.3))
+    dQ, dK, dV, TdQ, TdK, TdV = oracle.attention_bwd(Q, K, V, dO, causal, scale)
+    q, k, v = (torch.from_numpy(a.astype(np.float64)).requires_grad_(True) for a in (Q, K, V))
+    out = torch.nn.functional.scaled_dot_product_attention(q, k, v, is_causal=bool(causal), scale=scale)
+    (out * torch.from_numpy(dO.astype(np.float64))).sum().backward()
+    for mine, ref, name in ((dQ, q.grad, "dQ"), (dK, k.grad, "dK"), (dV, v.grad, "dV")):
+        assert np.allclose(mine, ref.numpy(), rtol=1e-11, atol=1e-12), name
+    for g, t in ((dQ, TdQ), (dK, TdK), (dV, TdV)):
+        assert np.all(t >= np.abs(g) - 1e-12)
+
+
+def test_attention_uniform_closed_form(oracle):
+    # Q = 0: every score is 0, so a causal row i weighs keys 0..i equally -- O_i is the mean of
+    # V_0..V_i and L_i = log(i + 1); without the mask every row is the mean of all of V, L = log T
+    BH, T, D = 2, 12, 8
+    _, K, V, _ = _attn_inputs(31, BH, T, D)
+    Q = np.zeros_like(K)
+    O, L, _ = oracle.attention_fwd(Q, K, V, 1, 0.7)
+    means = np.cumsum(V.astype(np.float64), axis=1) / np.arange(1, T + 1).reshape(1, T, 1)
+    assert np.allclose(O, means, rtol=0, atol=1e-14)
+    assert np.allclose(L, np.log(np.arange(1, T + 1)).reshape(1, T), rtol=0, atol=1e-15)
+    O2, L2, _ = oracle.attention_fwd(Q, K, V, 0, 0.7)
+    assert np.allclose(O2, np.broadcast_to(V.astype(np.float64).mean(axis=1, keepdims=True), O2.shape), atol=1e-14)
+    assert np.allclose(L2, np.log(T), atol=1e-15)
+
+
+def test_attention_first_causal_row_and_magnitudes(oracle):
+    # a causal first row sees only key 0: O_0 = V_0 exactly and L_0 = its one score; with V >= 0
+    # the bound scale TO equals O
+    BH, T, D = 3, 10, 8
+    Q, K, V, _ = _attn_inputs(41, BH, T, D)
+    scale = 0.25
+    O, L, TO = oracle.attention_fwd(Q, K, V, 1, scale)
+    assert np.array_equal(O[:, 0], V[:, 0].astype(np.float64))
+    s00 = scale * np.einsum("hd,hd->h", Q[:, 0].astype(np.float64), K[:, 0].astype(np.float64))
+    assert np.allclose(L[:, 0], s00, rtol=0, atol=1e-15)
+    Vp = np.abs(V)
+    O, _, TO = oracle.attention_fwd(Q, K, Vp, 1, scale)
+    assert np.allclose(TO, O, rtol=1e-15, atol=0)
