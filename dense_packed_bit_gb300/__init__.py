@@ -22,7 +22,7 @@ __all__ = [
     "MM_SPLITK_NOALLOC_MAX_FLOATS", "mm_gemm_f32_bias_act", "MM_ACT_NONE", "MM_ACT_GELU_TANH",
     "mm_gemv_packed2_strided_batched", "mm_gemv_packed2_strided_batched_ex", "mm_gemm_f32_bias_act_splitk",
     "mm_gemm_f32_split_plan",
-    "mm_probe_bounded_wait",
+    "mm_probe_bounded_wait", "mm_attention_fwd", "mm_attention_bwd",
     "MM_OK", "MM_ERR_INVALID_ARG", "MM_ERR_UNSUPPORTED", "MM_ERR_CUDA", "MM_ERR_TIMEOUT",
     "MM_GEMM_AUTO", "MM_GEMM_FFMA", "MM_GEMM_TF32X3",
     "MM_DEQ_AUTO", "MM_DEQ_SELECT", "MM_DEQ_AFFINE", "MM_DEQ_MMA", "MM_DEQ_FP8", "MM_DEQ_TC", "MM_DEQ_MXF4",
@@ -90,6 +90,9 @@ SIGNATURES = {
     "mm_gemv_packed2_strided_batched_ex": ([_P, _I64, _P, _I64, _P, _I64, _P, _I64, _I64, _I64, _I64, _P, _P,
                                             ctypes.POINTER(GemvOpts)], ctypes.c_int),
     "mm_probe_bounded_wait": ([_I, ctypes.c_uint64, _P, _P], ctypes.c_int),
+    "mm_attention_fwd": ([_P, _P, _P, _P, _P, _I64, _I64, _I64, _I, ctypes.c_float, _P], ctypes.c_int),
+    "mm_attention_bwd": ([_P, _P, _P, _P, _P, _P, _P, _P, _P, _I64, _I64, _I64, _I, ctypes.c_float, _P],
+                         ctypes.c_int),
 }
 
 
@@ -277,3 +280,16 @@ def mm_gemv_packed4_ex(codes, scales, x, y, rows, cols, codebook, stream=None, *
     o = Gemv4Opts(blocks, pdl, weights_static, independent, staging)
     _check(load_library().mm_gemv_packed4_ex(_ptr(codes), _ptr(scales), _ptr(x), _ptr(y), rows, cols,
                                              _codebook(codebook, 16), _stream(stream), ctypes.byref(o)))
+
+
+def mm_attention_fwd(Q, K, V, O, L, heads, T, D, causal, scale, stream=None):
+    """O = softmax(scale Q K^T (+ causal mask)) V per head, L = the rows' log-sum-exp; [heads][T][D] fp32."""
+    _check(load_library().mm_attention_fwd(_ptr(Q), _ptr(K), _ptr(V), _ptr(O), _ptr(L), heads, T, D, int(causal),
+                                           float(scale), _stream(stream)))
+
+
+def mm_attention_bwd(Q, K, V, O, dO, L, dQ, dK, dV, heads, T, D, causal, scale, stream=None):
+    """Gradients of sum(O * dO) with respect to Q, K, V, from the forward's O and L."""
+    _check(load_library().mm_attention_bwd(_ptr(Q), _ptr(K), _ptr(V), _ptr(O), _ptr(dO), _ptr(L), _ptr(dQ),
+                                           _ptr(dK), _ptr(dV), heads, T, D, int(causal), float(scale),
+                                           _stream(stream)))

@@ -744,6 +744,71 @@ mm_status mm_check_device_error(mm_stream_t stream) {
     return ok();
 }
 
+namespace {
+
+// shape, pointers and overlaps of an attention call; nin inputs, nout outputs of `per` floats
+// each (L-shaped tensors, heads x T, are listed with their own sizes)
+mm_status check_attention(int64_t heads, int64_t T, int64_t D, int causal, float scale, const void *const *in,
+                          const uint64_t *in_bytes, int nin, void *const *out, const uint64_t *out_bytes, int nout) {
+    if (heads < 1 || T < 1 || D < 1)
+        return fail(MM_ERR_INVALID_ARG, "heads, T, D must be >= 1 (got %lld, %lld, %lld)", (long long)heads,
+                    (long long)T, (long long)D);
+    if (causal != 0 && causal != 1) return fail(MM_ERR_INVALID_ARG, "causal must be 0 or 1");
+    if (!std::isfinite(scale)) return fail(MM_ERR_INVALID_ARG, "scale is not finite");
+    for (int i = 0; i < nin; ++i)
+        if (!in[i] || (reinterpret_cast<uintptr_t>(in[i]) & 3)) return fail(MM_ERR_INVALID_ARG, "NULL or misaligned input %d", i);
+    for (int i = 0; i < nout; ++i)
+        if (!out[i] || (reinterpret_cast<uintptr_t>(out[i]) & 3))
+            return fail(MM_ERR_INVALID_ARG, "NULL or misaligned output %d", i);
+    if (!mm::attention_supported(heads, T, D))
+        return fail(MM_ERR_UNSUPPORTED, "attention supports D = 64, 1 <= T <= 2^24, heads <= 65535 (got D=%lld)",
+                    (long long)D);
+    for (int i = 0; i < nout; ++i) {
+        for (int j = 0; j < nin; ++j)
+            if (overlap(out[i], out_bytes[i], in[j], in_bytes[j])) return fail(MM_ERR_INVALID_ARG, "an output overlaps an input");
+        for (int j = 0; j < i; ++j)
+            if (overlap(out[i], out_bytes[i], out[j], out_bytes[j])) return fail(MM_ERR_INVALID_ARG, "two outputs overlap");
+    }
+    return MM_OK;
+}
+
+}  // namespace
+
+mm_status mm_attention_fwd(const float *Q, const float *K, const float *V, float *O, float *L, int64_t heads,
+                           int64_t T, int64_t D, int causal, float scale, mm_stream_t stream) {
+    const uint64_t nb = (uint64_t)heads * (uint64_t)T * (uint64_t)D * 4, lb = (uint64_t)heads * (uint64_t)T * 4;
+    const void *in[3] = {Q, K, V};
+    const uint64_t inb[3] = {nb, nb, nb};
+    void *out[2] = {O, L};
+    const uint64_t outb[2] = {nb, lb};
+    mm_status s = check_attention(heads, T, D, causal, scale, in, inb, 3, out, outb, 2);
+    if (s != MM_OK) return s;
+    s = check_device();
+    if (s != MM_OK) return s;
+    const cudaError_t e =
+        mm::launch_attention_fwd(Q, K, V, O, L, heads, T, causal, scale, reinterpret_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "attention forward launch");
+    return ok();
+}
+
+mm_status mm_attention_bwd(const float *Q, const float *K, const float *V, const float *O, const float *dO,
+                           const float *L, float *dQ, float *dK, float *dV, int64_t heads, int64_t T, int64_t D,
+                           int causal, float scale, mm_stream_t stream) {
+    const uint64_t nb = (uint64_t)heads * (uint64_t)T * (uint64_t)D * 4, lb = (uint64_t)heads * (uint64_t)T * 4;
+    const void *in[6] = {Q, K, V, O, dO, L};
+    const uint64_t inb[6] = {nb, nb, nb, nb, nb, lb};
+    void *out[3] = {dQ, dK, dV};
+    const uint64_t outb[3] = {nb, nb, nb};
+    mm_status s = check_attention(heads, T, D, causal, scale, in, inb, 6, out, outb, 3);
+    if (s != MM_OK) return s;
+    s = check_device();
+    if (s != MM_OK) return s;
+    const cudaError_t e = mm::launch_attention_bwd(Q, K, V, O, dO, L, dQ, dK, dV, heads, T, causal, scale,
+                                                   reinterpret_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "attention backward launch");
+    return ok();
+}
+
 mm_status mm_probe_bounded_wait(int arrive, uint64_t limit_ns, uint64_t *out, mm_stream_t stream) {
     if (arrive != 0 && arrive != 1) return fail(MM_ERR_INVALID_ARG, "arrive must be 0 or 1");
     if (limit_ns < 1000 || limit_ns > 100000000)

@@ -194,6 +194,14 @@ cudaError_t launch_gemm_tf32x3_ws(const GemmArgs &g, int pair, cudaStream_t s);
 // Split-K form: ksplit slices per output tile computed into ws (ksplit * M * N floats,
 // 16-byte aligned), then summed in slice order into C by a second kernel.
 // ksplit == kStreamK: stream-K instead, ws holding the units' partial-tile slots and flags.
+// Attention (attention_fa2.cu): [heads][T][64] fp32, forward O and L, backward dQ/dK/dV.
+bool attention_supported(int64_t heads, int64_t T, int64_t D);
+cudaError_t launch_attention_fwd(const float *Q, const float *K, const float *V, float *O, float *L, int64_t heads,
+                                 int64_t T, int causal, float scale, cudaStream_t st);
+cudaError_t launch_attention_bwd(const float *Q, const float *K, const float *V, const float *O, const float *dO,
+                                 const float *L, float *dQ, float *dK, float *dV, int64_t heads, int64_t T, int causal,
+                                 float scale, cudaStream_t st);
+
 constexpr int kStreamK = -1;
 
 // Longest K one 3xTF32 accumulation may cover.  The tensor core's fp32 accumulation error

@@ -145,6 +145,38 @@ mm_status mm_check_device_error(mm_stream_t stream);
 mm_status mm_probe_bounded_wait(int arrive, uint64_t limit_ns, uint64_t *out, mm_stream_t stream);
 
 /*
+ * Scaled dot-product attention of a GPT-2 training step, in the Flash-Attention-2
+ * form of "I built a GPT-2 in the browser, then made it 2.6x-12.1x faster",
+ * section "Flash Attention 2": per head, S = scale * Q K^T (keys after the query
+ * masked when causal = 1), P = softmax over each row of S, O = P V, and
+ * L[i] = log sum_k exp(S[i][k]) (the forward's m + log(l)), from which the
+ * backward rebuilds P without storing it.
+ *
+ * Q, K, V, O (and dO, dQ, dK, dV): heads x T x D fp32, row-major, contiguous
+ * (a batch of B sequences of H heads is heads = B * H); L: heads x T fp32.  All
+ * device memory owned by the caller, 4-byte aligned; outputs must not overlap
+ * inputs or each other.  D = 64 (GPT-2's head dimension); T >= 1; causal 0 or
+ * 1; scale finite (usually 1 / sqrt(D)).  Asynchronous on `stream`.
+ *
+ * mm_attention_fwd writes O and L.  mm_attention_bwd takes the forward's O and L
+ * and the gradient dO of a loss with respect to O, and writes dQ, dK, dV
+ * (every element, so their contents on entry do not matter).  Every output is a
+ * sum in a fixed order: bit-reproducible run to run.  Bound, per output, against
+ * the fp64 definition: |err| <= 1e-5 * T_out, T_out the sum of the magnitudes of
+ * the terms of the output's last contraction with the earlier sums taken in
+ * magnitude (O: sum_k P |V|; dV: sum_i P |dO|; dQ, dK: scale sum P (|dP| + |D|)
+ * |K| or |Q|, |dP| = sum_d |dO V|, |D| = sum_d |dO O|); L within 1e-5 (1 + |L|).
+ * Errors: MM_ERR_INVALID_ARG for NULL or misaligned pointers, sizes < 1, causal
+ * not 0/1, a non-finite scale or overlapping outputs; MM_ERR_UNSUPPORTED for
+ * D != 64 or T > 2^24 or heads > 65535.
+ */
+mm_status mm_attention_fwd(const float *Q, const float *K, const float *V, float *O, float *L, int64_t heads,
+                           int64_t T, int64_t D, int causal, float scale, mm_stream_t stream);
+mm_status mm_attention_bwd(const float *Q, const float *K, const float *V, const float *O, const float *dO,
+                           const float *L, float *dQ, float *dK, float *dV, int64_t heads, int64_t T, int64_t D,
+                           int causal, float scale, mm_stream_t stream);
+
+/*
  * GPT-2's linear layer with its MLP activation fused into the GEMM epilogue:
  *     C = act(op(A) . op(B) + bias),   bias[n] added to column n of every row.
  * bias: N fp32 values in device memory, or NULL for none.  act: MM_ACT_NONE or

@@ -375,3 +375,40 @@ def test_probe_bounded_wait_argument_errors(lib, arrive, limit, out):
 def test_split_workspace_respects_the_k_margin(K, splitk, floats):
     mm.load_library()
     assert mm.mm_gemm_f32_splitk_workspace(256, 256, K, splitk) == floats
+
+
+# ------------------------------------------------------------------ attention
+
+_AN = 2 * 16 * 64 * 4  # bytes of one [2][16][64] fp32 tensor
+
+
+@pytest.mark.parametrize("case,status", [
+    (dict(heads=0), mm.MM_ERR_INVALID_ARG), (dict(T=0), mm.MM_ERR_INVALID_ARG), (dict(D=0), mm.MM_ERR_INVALID_ARG),
+    (dict(causal=2), mm.MM_ERR_INVALID_ARG), (dict(scale=float("nan")), mm.MM_ERR_INVALID_ARG),
+    (dict(scale=float("inf")), mm.MM_ERR_INVALID_ARG), (dict(Q=None), mm.MM_ERR_INVALID_ARG),
+    (dict(V=None), mm.MM_ERR_INVALID_ARG), (dict(L=None), mm.MM_ERR_INVALID_ARG), (dict(O=None), mm.MM_ERR_INVALID_ARG),
+    (dict(K=FAKE + 5 * _AN + 2), mm.MM_ERR_INVALID_ARG),            # misaligned
+    (dict(O=FAKE + 64), mm.MM_ERR_INVALID_ARG),                     # O overlaps Q
+    (dict(L=FAKE + 3 * _AN + 16), mm.MM_ERR_INVALID_ARG),           # L overlaps O
+    (dict(D=32), mm.MM_ERR_UNSUPPORTED), (dict(D=128), mm.MM_ERR_UNSUPPORTED),
+])
+def test_attention_fwd_argument_errors(lib, case, status):
+    a = dict(Q=FAKE, K=FAKE + _AN, V=FAKE + 2 * _AN, O=FAKE + 3 * _AN, L=FAKE + 4 * _AN, heads=2, T=16, D=64,
+             causal=1, scale=0.125)
+    a.update(case)
+    st = mm.load_library().mm_attention_fwd(a["Q"], a["K"], a["V"], a["O"], a["L"], a["heads"], a["T"], a["D"],
+                                            a["causal"], a["scale"], None)
+    assert st == status, lib.mm_last_error()
+    assert lib.mm_last_error()
+
+
+@pytest.mark.parametrize("case", [
+    dict(dQ=None), dict(dO=None), dict(dK=FAKE + 64), dict(dV=FAKE + 6 * _AN + 64), dict(L=FAKE + 7 * _AN + 4),
+])
+def test_attention_bwd_argument_errors(lib, case):
+    a = dict(Q=FAKE, K=FAKE + _AN, V=FAKE + 2 * _AN, O=FAKE + 3 * _AN, dO=FAKE + 4 * _AN, L=FAKE + 5 * _AN,
+             dQ=FAKE + 6 * _AN, dK=FAKE + 7 * _AN, dV=FAKE + 8 * _AN)
+    a.update(case)
+    st = mm.load_library().mm_attention_bwd(a["Q"], a["K"], a["V"], a["O"], a["dO"], a["L"], a["dQ"], a["dK"],
+                                            a["dV"], 2, 16, 64, 1, 0.125, None)
+    assert st == mm.MM_ERR_INVALID_ARG, lib.mm_last_error()
