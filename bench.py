@@ -38,6 +38,7 @@ import argparse
 import hashlib
 import json
 import os
+import math
 import statistics
 import subprocess
 import sys
@@ -64,6 +65,10 @@ C1_FLOP = 2.0 * C1_M * C1_N * C1_K  # 302 MFLOP
 C1_BYTES = 4 * (C1_M * C1_K + C1_K * C1_N + C1_M * C1_N)  # 10.42 MB: A and B read once, C written
 C1_CALLS = 8  # distinct problems per step, one mm_gemm_f32 call each, all cold after the L2 flush
 TERN_FLOP_PER_LAYER = 2 * (2.0 * 222 * 3072 * 768)
+ATTN_HEADS, ATTN_T, ATTN_D = 32, 512, 64  # causal self-attention, B = 4 x H = 8 heads
+# algorithmic flops of a forward + backward: the forward's S = Q K^T and O = P V, the backward's
+# dV, dP, dQ, dK, each 2 D flops per allowed (query, key) pair (T (T + 1) / 2 of them, causal)
+ATTN_FLOP = 6 * 2.0 * ATTN_HEADS * (ATTN_T * (ATTN_T + 1) // 2) * ATTN_D
 N_GEMV = 64
 N_LAYERS = 16
 WORKLOAD = ("gpt2_mlp_up_64x768x3072_fp32_nn + square_2048_fp32_gemm_nn_nt_tn + gemv2bit_12288x1536_rotation64 + "
@@ -227,7 +232,7 @@ class Workload:
         # that a change of the inputs shows in the report
         sha = {k: synth.Digest() for k in ("gpt2_mlp_up_64", "square_2048", "gemv2_rotation64", "gemv4_rotation64",
                                            "gemv2_t_rotation64", "ternary_encoder", "training_set",
-                                           "gpt2_mlp_bias_gelu")}
+                                           "gpt2_mlp_bias_gelu", "gpt2_attention")}
         self.c1 = []
         for j in range(C1_CALLS):
             c1 = synth.gpt2_mlp_up_64x768x3072(replica=rep * C1_CALLS + j)
@@ -294,6 +299,13 @@ class Workload:
                                       scales=torch.from_numpy(c.scales).to(device),
                                       X=torch.from_numpy(c.X).to(device),
                                       Y=torch.empty((c.X.shape[0], c.rows), dtype=torch.float32, device=device)))
+        at = synth.gpt2_attention_4x8x512x64(replica=rep)
+        assert (at.heads, at.T, at.D) == (ATTN_HEADS, ATTN_T, ATTN_D)
+        sha["gpt2_attention"].update(at.Q, at.K, at.V, at.dO)
+        self.attn = dict(case=at, **{n: torch.from_numpy(getattr(at, n)).to(device) for n in ("Q", "K", "V", "dO")},
+                         **{n: torch.empty((ATTN_HEADS, ATTN_T, ATTN_D), dtype=torch.float32, device=device)
+                            for n in ("O", "dQ", "dK", "dV")},
+                         L=torch.empty((ATTN_HEADS, ATTN_T), dtype=torch.float32, device=device))
         # training-shape set: forward C = A B, dA = dC B^T, dB = A^T dC (N(0, 0.02)), through the
         # split entry point with its automatic choice and one shared workspace
         self.train = list(synth.training_set_8192_all(replica=rep))
@@ -412,6 +424,13 @@ def capture_phases(w: Workload, stream):
             mm.mm_gemm_f32_splitk(c.transA, c.transB, c.M, c.N, c.K, a, a.shape[1], b, b.shape[1], out, c.N, 0,
                                   w.train_ws, w.train_ws_floats)
 
+    def attn():
+        a = w.attn
+        scale = 1.0 / math.sqrt(ATTN_D)
+        mm.mm_attention_fwd(a["Q"], a["K"], a["V"], a["O"], a["L"], ATTN_HEADS, ATTN_T, ATTN_D, 1, scale)
+        mm.mm_attention_bwd(a["Q"], a["K"], a["V"], a["O"], a["dO"], a["L"], a["dQ"], a["dK"], a["dV"], ATTN_HEADS,
+                            ATTN_T, ATTN_D, 1, scale)
+
     def mlp():
         mm.mm_gemm_f32_bias_act_splitk(0, 0, MLP_M, MLP_N, MLP_K, w.mlp_x, MLP_K, w.mlp_w, MLP_N, w.mlp_b,
                                        mm.MM_ACT_GELU_TANH, w.mlp_y, MLP_N, 0, w.mlp_ws, w.mlp_ws_floats)
@@ -425,7 +444,7 @@ def capture_phases(w: Workload, stream):
     graphs = {}
     for name, fn in (("c1", c1), ("gemm", gemm), ("gemv", gemv(GEMV_INDEP, GEMV_INDEP_STREAMS)), ("gemv_c", gemv_chain),
                      ("tern", tern), ("gemv4", gemv4), ("gemvt", gemvt), ("train", train), ("mlp", mlp),
-                     ("gemv_b", gemv_batched)):
+                     ("gemv_b", gemv_batched), ("attn", attn)):
         with torch.cuda.stream(stream):
             fn()  # warm the kernels' one-time setup outside capture
         torch.cuda.synchronize()
@@ -436,11 +455,11 @@ def capture_phases(w: Workload, stream):
     return graphs
 
 
-LAUNCHES_PER_STEP = C1_CALLS + 3 + 4 * N_GEMV + 2 * N_LAYERS + 3 + 1 + 1  # C1, 2048^3, GEMVs, encoder, training set, MLP, batched
+LAUNCHES_PER_STEP = C1_CALLS + 3 + 4 * N_GEMV + 2 * N_LAYERS + 3 + 1 + 1 + 3  # C1, 2048^3, GEMVs, encoder, training set, MLP, batched, attention
 
 
-PHASES = ("c1", "gemm", "gemv", "gemv_c", "tern", "gemv4", "gemvt", "train", "mlp", "gemv_b")
-L2_COLD = ("c1", "gemm")  # phases whose operands fit in L2: a 512 MiB write evicts them first
+PHASES = ("c1", "gemm", "gemv", "gemv_c", "tern", "gemv4", "gemvt", "train", "mlp", "gemv_b", "attn")
+L2_COLD = ("c1", "gemm", "attn")  # phases whose operands fit in L2: a 512 MiB write evicts them first
 
 
 def run_step(w: Workload, graphs, ev, stream):
@@ -701,6 +720,25 @@ def bench_parity(w) -> dict:
         worst = max(worst, parity_ratio(Ym[r0:r0 + 64], ref, bound))
     out["gpt2_mlp_up_bias_gelu"] = {"worst": worst, "outputs": 128 * MLP_N,
                                     "note": "|err| / (1.13 T + 2^-20 (1 + |z|) / 1e-5)"}
+
+    # attention: heads 0 and 31 in full, O, L and the three gradients, each against its bound scale
+    # times the head's tolerance 1e-5 + 2 gamma_D A (the fp32 scores' rounding, passed on by the
+    # softmax), reported as a fraction of 1e-5 like the others
+    at = w.attn["case"]
+    hs = [0, ATTN_HEADS - 1]
+    scale = float(np.float32(1.0 / math.sqrt(ATTN_D)))
+    Qa, Ka = np.abs(at.Q[hs].astype(np.float64)), np.abs(at.K[hs].astype(np.float64))
+    A = scale * np.max(np.einsum("hid,hkd->hik", Qa, Ka), axis=(1, 2))
+    tol = (1e-5 + 2.0 * ATTN_D * 2.0 ** -24 * A).reshape(-1, 1, 1)
+    Or, Lr, TO = oracle.attention_fwd(at.Q[hs], at.K[hs], at.V[hs], at.causal, scale)
+    rq, rk, rv, tq, tk, tv = oracle.attention_bwd(at.Q[hs], at.K[hs], at.V[hs], at.dO[hs], at.causal, scale)
+    got = {n: w.attn[n].cpu().numpy()[hs] for n in ("O", "L", "dQ", "dK", "dV")}
+    worst = 0.0
+    for n, ref, T in (("O", Or, TO), ("dQ", rq, tq), ("dK", rk, tk), ("dV", rv, tv)):
+        worst = max(worst, parity_ratio(got[n], ref, T * tol / PARITY_TOL))
+    worst = max(worst, parity_ratio(got["L"], Lr, (1.0 + np.abs(Lr)) * tol[:, :, 0] / PARITY_TOL))
+    out["gpt2_attention"] = {"worst": worst, "outputs": int(2 * ATTN_T * (4 * ATTN_D + 1)),
+                             "note": "heads 0 and 31: |err| / (T (1e-5 + 2 gamma_D A) / 1e-5)"}
     ok = all(v["worst"] <= PARITY_TOL for v in out.values())
     return {"what": "max |y_gpu - y_oracle| / sum_k |term_k| over the outputs the timed phases left, per workload",
             "tol": PARITY_TOL, "ok": bool(ok), "workloads": out, "seconds": time.perf_counter() - t0}
@@ -808,6 +846,7 @@ def main_mm(args):
     train_total_s = total_s("train")
     mlp_total_s = total_s("mlp")
     gemvb_total_s = total_s("gemv_b")
+    attn_total_s = total_s("attn")
     per_mat_gemvb_s = gemvb_total_s / (args.steps * N_GEMV)
     wall = reduce_max(wall, dev)
 
@@ -819,7 +858,7 @@ def main_mm(args):
     per_call_gemv4_s = gemv4_total_s / (args.steps * N_GEMV)
     per_call_gemvt_s = gemvt_total_s / (args.steps * N_GEMV)
     step_ms = (c1_total_s + gemm_total_s + gemv_total_s + gemvc_total_s + tern_total_s + gemv4_total_s + gemvt_total_s +
-               train_total_s + mlp_total_s + gemvb_total_s) / args.steps * 1e3
+               train_total_s + mlp_total_s + gemvb_total_s + attn_total_s) / args.steps * 1e3
 
     peaks, peaks_src = measured_peaks()
     props = torch.cuda.get_device_properties(dev)
@@ -908,6 +947,19 @@ def main_mm(args):
                                           "frac": GEMV_TOTAL_BYTES / per_mat_gemvb_s / 1e9 / peaks["hbm_gbs"],
                                           "weight_frac": GEMV_WEIGHT_BYTES / per_mat_gemvb_s / 1e9 / peaks["hbm_gbs"],
                                           "traffic": traffic_for("gemv2_mxf4_batched"), "peak_source": peaks_src}}},
+        "gpt2_attention": {"metric": "causal attention forward + backward TFLOP/s (algorithmic), 32 heads x 512 x 64",
+                           "value": world * ATTN_FLOP * args.steps / attn_total_s / 1e12, "unit": "TFLOP/s",
+                           "us_per_step": attn_total_s / args.steps * 1e6,
+                           "kernels": "attn_fwd_kernel, attn_bwd_dkdv_kernel, attn_bwd_dq_kernel (fp32 FFMA)",
+                           "roofline": {"bound": "alu", "achieved": ATTN_FLOP * args.steps / attn_total_s / 1e12,
+                                        "peak": fp32_peak_max, "unit": "TFLOP/s",
+                                        "frac": ATTN_FLOP * args.steps / attn_total_s / 1e12 / fp32_peak_max,
+                                        "traffic": traffic_for("attn_fwd"),
+                                        "peak_source": f"{sms} SMs x 128 FP32 lanes x 2 flop x "
+                                                       f"{peaks.get('sm_max_mhz', 2070.0):.0f} MHz",
+                                        "note": "algorithmic flops: S, O forward, dV, dP, dQ, dK backward over the "
+                                                "allowed (causal) pairs; the kernels also recompute S and dP for "
+                                                "the dQ pass and compute the diagonal tiles in full"}},
         "ternary": {"value": tern_tflops, "unit": "TFLOP/s", "ms_per_block": tern_total_s / args.steps * 1e3,
                     "us_per_product": tern_total_s / args.steps / (2 * N_LAYERS) * 1e6,
                     "kernel": "gemm_packed2_tcr_kernel (automatic token tile and cluster split)", "opts": TERN_OPTS,

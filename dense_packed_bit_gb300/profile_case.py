@@ -11,6 +11,7 @@
     python -m dense_packed_bit_gb300.profile_case ternary --reps 1 [--tile 2] [--pdl 2: pdl + static weights]
     python -m dense_packed_bit_gb300.profile_case gemv_batched --reps 2 --matrices 16 [--dequant 6 --tiles 0]
     python -m dense_packed_bit_gb300.profile_case gemv_t --reps 3 --matrices 8   (1,536 x 12,288, automatic)
+    python -m dense_packed_bit_gb300.profile_case attn --reps 2   (causal attention 32 x 512 x 64, forward + backward)
 
 One warm-up launch precedes the `reps` launches.  No timing is done here:
 numbers come from the profiler or from bench.py.
@@ -23,7 +24,7 @@ import sys
 
 def main(argv=None):
     ap = argparse.ArgumentParser()
-    ap.add_argument("op", choices=["gemm", "c1", "gemv", "gemv4", "ternary", "gemv_batched", "gemv_t"])
+    ap.add_argument("op", choices=["gemm", "c1", "gemv", "gemv4", "ternary", "gemv_batched", "gemv_t", "attn"])
     ap.add_argument("--layout", default="nn", choices=["nn", "nt", "tn"])
     ap.add_argument("--size", type=int, default=2048)
     ap.add_argument("--path", type=int, default=0)
@@ -72,6 +73,14 @@ def main(argv=None):
         for _ in range(1 + a.reps if not (a.path == 2 and a.split > 1) else 0):
             mm.mm_gemm_f32_ex(0, 0, c.M, c.N, c.K, A, c.K, B, c.N, C, c.N, path=a.path, tile=a.tile,
                               splitk=a.split if a.path == 1 and a.tile == 4 else 0)
+    elif a.op == "attn":
+        c = synth.gpt2_attention_4x8x512x64()
+        Q, K, V, dO = (torch.from_numpy(getattr(c, n)).to(dev) for n in ("Q", "K", "V", "dO"))
+        O, dQ, dK, dV = (torch.empty_like(Q) for _ in range(4))
+        L = torch.empty((c.heads, c.T), dtype=torch.float32, device=dev)
+        for _ in range(1 + a.reps):
+            mm.mm_attention_fwd(Q, K, V, O, L, c.heads, c.T, c.D, c.causal, 0.125)
+            mm.mm_attention_bwd(Q, K, V, O, dO, L, dQ, dK, dV, c.heads, c.T, c.D, c.causal, 0.125)
     elif a.op == "gemv":
         codes, scales = [], []
         for i in range(a.matrices):

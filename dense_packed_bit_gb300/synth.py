@@ -292,6 +292,28 @@ def training_set_8192_all(replica: int = 0) -> tuple:
 
 
 @dataclass
+class AttentionCase:
+    name: str
+    heads: int
+    T: int
+    D: int
+    causal: int
+    Q: np.ndarray  # (heads, T, D) fp32
+    K: np.ndarray
+    V: np.ndarray
+    dO: np.ndarray  # gradient of the loss with respect to O
+
+
+def gpt2_attention_4x8x512x64(replica: int = 0) -> AttentionCase:
+    """Causal self-attention of a GPT-2 training step at the shape of "I built a GPT-2 in the
+    browser", section "Flash Attention 2" (B = 4 sequences, H = 8 heads, T = 512), head dimension
+    64 (GPT-2's): Q, K, V and the incoming gradient dO N(0, 1) fp32, heads = B H = 32."""
+    shape = (32, 512, 64)
+    Q, K, V, dO = (normal_f32(_seed(9, t, 0, replica), shape, 1.0) for t in (1, 2, 3, 4))
+    return AttentionCase("gpt2_attention_b4_h8_t512_d64_causal", 32, 512, 64, 1, Q, K, V, dO)
+
+
+@dataclass
 class PackedCase:
     name: str
     rows: int

@@ -80,6 +80,7 @@ def _all_workloads(rec, replicas=(0,)):
         for which in ("fwd", "dA", "dB"):
             run("training_set" + sfx, lambda: synth.training_set_8192(which, replica=r))
         run("training_set_all" + sfx, lambda: synth.training_set_8192_all(replica=r))
+        run("gpt2_attention" + sfx, lambda: synth.gpt2_attention_4x8x512x64(replica=r))
     return out
 
 
