@@ -11,21 +11,32 @@
 // Layout: Q, K, V, O, dO, dQ, dK, dV are [heads][T][64] fp32 row-major (a batch
 // of B sequences of H heads is B H heads), L is [heads][T] fp32 (natural log).
 //
-// GB300 form.  A CTA of 256 threads owns a 64-row tile; K/V (or Q/dO) tiles of
-// 64 rows pass through shared memory, rows padded to 65 words so that every
-// access of the products below -- by rows or by columns -- falls on distinct
-// banks or is a broadcast.  Thread (ty, tx) = (tid / 16, tid % 16) holds
-// outputs (ty + 16 r, tx + 16 c), r, c = 0..3, of every 64 x 64 product, so
-// the 16 threads of a half-warp hold whole rows: the softmax's row maximum and
-// row sum are 4-step shuffles within the half-warp.  Scores are kept in base-2
-// units (scale * log2(e) folded into one multiply), so each probability is one
-// exp2.
+// GB300 form.  A CTA of 256 threads owns a 64-row tile; 64-row tiles of the
+// other operands pass through shared memory.  Every 64 x 64 x 64 product
+// C[i][j] += sum_t A[i][t] B[t][j] reads its operands as A^T and B, both stored
+// [t][...] with rows padded to 68 words: thread (ty, tx) = (tid / 16, tid % 16)
+// holds C[4 ty + r][4 tx + c] and reads per t one 16-byte vector of each
+// (A^T's shared by the half-warp, a broadcast), multiplying with packed f32x2
+// FMAs.  So a tile is stored in whichever orientation its products read it --
+// "natural" [row][d] or "transposed" [d][row] (the copy does the transpose) --
+// and the probabilities P and dS are written from registers in the orientation
+// the next product needs.  The 16 threads of a half-warp hold whole rows of S:
+// the softmax's row maximum and row sum are 4-step shuffles within it.  Scores
+// are kept in base-2 units (scale * log2(e) folded into one multiply), so each
+// probability is one exp2.
+//
+// Tiles stream through two shared-memory buffers by 4-byte cp.async, the next
+// block's copies in flight while the current one is multiplied.  With a causal
+// mask query tile j meets j + 1 key blocks, so a CTA takes the tile pair
+// (j, n - 1 - j): every CTA then does n + 1 blocks of work (n tiles per head)
+// instead of 1 .. n.
 //
 // The backward is split in two kernels so that every gradient is a sum in a
-// fixed order (no atomics): one CTA per key tile accumulates dK and dV over the
-// query tiles, one CTA per query tile accumulates dQ over the key tiles; both
-// rebuild P and dS = P (dP - D) with D_i = dO_i . O_i from identical products,
-// in identical order.  Causal attention skips the blocks above the diagonal.
+// fixed order (no atomics): one CTA per key tile (pair) accumulates dK and dV
+// over the query tiles, one CTA per query tile (pair) accumulates dQ over the
+// key tiles; both rebuild S, P and dS = P (dP - D), D_i = dO_i . O_i, from
+// identical products in identical order.  Causal attention skips the blocks
+// above the diagonal.
 #include "mm_common.cuh"
 #include "mm_internal.h"
 
@@ -35,38 +46,53 @@ namespace mm {
 
 namespace {
 
-constexpr int HD = 64;     // head dimension
-constexpr int BT = 64;     // rows per tile (queries or keys)
-constexpr int TS = BT + 1; // padded shared-memory row
+constexpr int HD = 64;      // head dimension
+constexpr int BT = 64;      // rows per tile (queries or keys)
+constexpr int TS = BT + 4;  // padded shared-memory row: 16-byte aligned, 4 banks of skew
 constexpr int TILE = BT * TS;
 constexpr int NT = 256;
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 
-// acc[r][c] += sum_t a(ty + 16 r, t) b(t, tx + 16 c), t = 0..63 in order
-template <class FA, class FB>
-__device__ __forceinline__ void mm64(float (&acc)[4][4], int ty, int tx, FA a, FB b) {
-#pragma unroll 4
+// acc[r][c] += sum_t At[t][4 ty + r] B[t][4 tx + c], t = 0..63 in order
+__device__ __forceinline__ void mm64(float (&acc)[4][4], const float *At, const float *B, int ty, int tx) {
+#pragma unroll 8
     for (int t = 0; t < BT; ++t) {
-        float av[4], bv[4];
+        const float4 a = *reinterpret_cast<const float4 *>(At + t * TS + 4 * ty);
+        const float4 b = *reinterpret_cast<const float4 *>(B + t * TS + 4 * tx);
+        const float av[4] = {a.x, a.y, a.z, a.w};
 #pragma unroll
-        for (int r = 0; r < 4; ++r) av[r] = a(ty + 16 * r, t);
-#pragma unroll
-        for (int c = 0; c < 4; ++c) bv[c] = b(t, tx + 16 * c);
-#pragma unroll
-        for (int r = 0; r < 4; ++r)
-#pragma unroll
-            for (int c = 0; c < 4; ++c) acc[r][c] = fmaf(av[r], bv[c], acc[r][c]);
+        for (int r = 0; r < 4; ++r) {
+            fma2_bcast(acc[r][0], acc[r][1], av[r], b.x, b.y);
+            fma2_bcast(acc[r][2], acc[r][3], av[r], b.z, b.w);
+        }
     }
 }
 
-// rows row0 .. row0 + 63 of a [T][64] matrix into a padded tile; rows past T read 0
+__device__ __forceinline__ void cp_async4(float *dst, const float *src, int src_bytes) {
+    asm volatile("cp.async.ca.shared.global [%0], [%1], 4, %2;" ::"r"(smem_u32(dst)), "l"(src), "r"(src_bytes)
+                 : "memory");
+}
+__device__ __forceinline__ void cp_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+__device__ __forceinline__ void cp_wait_all() { asm volatile("cp.async.wait_group 0;" ::: "memory"); }
+
+// rows row0 .. row0 + 63 of a [T][64] matrix into a tile, asynchronously (the caller commits
+// and waits), natural ([row][d]) or transposed ([d][row]); rows past T read 0 (not read)
+template <bool TRANS>
 __device__ __forceinline__ void load_tile(float *dst, const float *src, int64_t row0, int T) {
     for (int e = threadIdx.x; e < BT * HD; e += NT) {
         const int r = e >> 6, d = e & 63;
         const int64_t row = row0 + r;
-        dst[r * TS + d] = row < T ? __ldg(src + row * HD + d) : 0.f;
+        cp_async4(dst + (TRANS ? d * TS + r : r * TS + d), row < T ? src + row * HD + d : src, row < T ? 4 : 0);
     }
+}
+
+// the query (or key) tiles of CTA b: tile b alone, or with a causal mask the pair (b, n - 1 - b)
+__device__ __forceinline__ int tiles_of(int b, int n, int causal, int (&t)[2]) {
+    t[0] = b;
+    if (!causal) return 1;
+    t[1] = n - 1 - b;
+    return t[1] != b ? 2 : 1;
 }
 
 __device__ __forceinline__ float half_max(float v) {
@@ -92,202 +118,264 @@ __device__ __forceinline__ bool allowed(int i, int k, int T, int causal) {
     return i < T && k < T && (!causal || k <= i);
 }
 
-// ---------------------------------------------------------------- forward
-__global__ void __launch_bounds__(NT, 3) attn_fwd_kernel(const AttnArgs a) {
-    extern __shared__ float sm[];
-    float *Qs = sm, *Ks = sm + TILE, *Vs = sm + 2 * TILE, *Ps = sm + 3 * TILE;
-    const int ty = threadIdx.x >> 4, tx = threadIdx.x & 15;
-    const int T = a.T;
-    const int64_t head = blockIdx.y;
-    const int q0 = blockIdx.x * BT;
-    const float *Qh = a.Q + head * T * HD, *Kh = a.K + head * T * HD, *Vh = a.V + head * T * HD;
-    load_tile(Qs, Qh, q0, T);
-
-    float m[4], l[4], o[4][4];
+// tile value v[r][c] (row 4 ty + r, column 4 tx + c) into a natural or a transposed tile
+__device__ __forceinline__ void store_n(float *dst, const float (&v)[4][4], int ty, int tx) {
 #pragma unroll
-    for (int r = 0; r < 4; ++r) {
-        m[r] = -INFINITY;
-        l[r] = 0.f;
+    for (int r = 0; r < 4; ++r)
+        *reinterpret_cast<float4 *>(dst + (4 * ty + r) * TS + 4 * tx) = make_float4(v[r][0], v[r][1], v[r][2], v[r][3]);
+}
+__device__ __forceinline__ void store_t(float *dst, const float (&v)[4][4], int ty, int tx) {
 #pragma unroll
-        for (int c = 0; c < 4; ++c) o[r][c] = 0.f;
-    }
-    const int kend = a.causal ? min(T, q0 + BT) : T;  // keys past the tile's last query are masked
-    for (int k0 = 0; k0 < kend; k0 += BT) {
-        __syncthreads();  // the previous block's K, V and P are no longer read
-        load_tile(Ks, Kh, k0, T);
-        load_tile(Vs, Vh, k0, T);
-        __syncthreads();
-        float s[4][4] = {};
-        mm64(s, ty, tx, [&](int i, int t) { return Qs[i * TS + t]; }, [&](int t, int j) { return Ks[j * TS + t]; });
-#pragma unroll
-        for (int r = 0; r < 4; ++r) {
-            const int i = q0 + ty + 16 * r;
-            float mx = -INFINITY;
-#pragma unroll
-            for (int c = 0; c < 4; ++c) {
-                const int k = k0 + tx + 16 * c;
-                s[r][c] = allowed(i, k, T, a.causal) ? s[r][c] * a.scale2 : -INFINITY;
-                mx = fmaxf(mx, s[r][c]);
-            }
-            const float mnew = fmaxf(m[r], half_max(mx));
-            // a row with no allowed key yet (only rows past T) keeps zero weights
-            const float alpha = mnew == -INFINITY ? 1.f : exp2f(m[r] - mnew);
-            float ls = 0.f;
-#pragma unroll
-            for (int c = 0; c < 4; ++c) {
-                const float p = mnew == -INFINITY ? 0.f : exp2f(s[r][c] - mnew);
-                Ps[(ty + 16 * r) * TS + tx + 16 * c] = p;
-                ls += p;
-                o[r][c] *= alpha;
-            }
-            l[r] = l[r] * alpha + ls;
-            m[r] = mnew;
-        }
-        __syncthreads();  // P complete
-        mm64(o, ty, tx, [&](int i, int t) { return Ps[i * TS + t]; }, [&](int t, int d) { return Vs[t * TS + d]; });
-    }
-#pragma unroll
-    for (int r = 0; r < 4; ++r) {
-        const int i = q0 + ty + 16 * r;
-        const float lrow = half_sum(l[r]);
-        if (i >= T) continue;
-        const float inv = 1.f / lrow;
-        float *orow = a.Out + (head * T + i) * HD;
-#pragma unroll
-        for (int c = 0; c < 4; ++c) orow[tx + 16 * c] = o[r][c] * inv;
-        if (tx == 0) a.Lout[head * T + i] = (m[r] + log2f(lrow)) * kLn2;
-    }
+    for (int c = 0; c < 4; ++c)
+        *reinterpret_cast<float4 *>(dst + (4 * tx + c) * TS + 4 * ty) = make_float4(v[0][c], v[1][c], v[2][c], v[3][c]);
 }
 
-// D_i = dO_i . O_i for the thread's rows ty + 16 r of the tile at q0 (dOs holds the dO tile)
-__device__ __forceinline__ void row_dots(const AttnArgs &a, int64_t head, int q0, const float *dOs, int ty, int tx,
-                                         float (&Drow)[4]) {
+// D_i = dO_i . O_i for rows i = q0 + 4 ty + r (global dO and O, 4 columns per thread)
+__device__ __forceinline__ void row_dots(const AttnArgs &a, int64_t head, int q0, int ty, int tx, float (&Drow)[4]) {
 #pragma unroll
     for (int r = 0; r < 4; ++r) {
-        const int i = q0 + ty + 16 * r;
+        const int i = q0 + 4 * ty + r;
         float p = 0.f;
         if (i < a.T) {
-            const float *orow = a.O + (head * a.T + i) * HD;
+            const int64_t base = (head * a.T + i) * HD + 4 * tx;
 #pragma unroll
-            for (int c = 0; c < 4; ++c) p = fmaf(dOs[(ty + 16 * r) * TS + tx + 16 * c], __ldg(orow + tx + 16 * c), p);
+            for (int c = 0; c < 4; ++c) p = fmaf(__ldg(a.dO + base + c), __ldg(a.O + base + c), p);
         }
         Drow[r] = half_sum(p);
     }
 }
 
-// P and dS of the (query tile q0, key tile k0) block, into Ps and dSs as [i][k]
-__device__ __forceinline__ void probs_and_dS(const AttnArgs &a, int q0, int k0, const float *Qs, const float *dOs,
-                                             const float *Ks, const float *Vs, const float (&L2)[4],
-                                             const float (&Drow)[4], float *Ps, float *dSs, int ty, int tx) {
-    float s[4][4] = {}, dp[4][4] = {};
-    mm64(s, ty, tx, [&](int i, int t) { return Qs[i * TS + t]; }, [&](int t, int j) { return Ks[j * TS + t]; });
-    mm64(dp, ty, tx, [&](int i, int t) { return dOs[i * TS + t]; }, [&](int t, int j) { return Vs[j * TS + t]; });
+// P and dS of the block (query tile q0, key tile k0) in registers, from S = Q K^T and
+// dP = dO V^T (Qt, Kt, dOt, Vt transposed tiles)
+__device__ __forceinline__ void probs_and_dS(const AttnArgs &a, int q0, int k0, const float *Qt, const float *Kt,
+                                             const float *dOt, const float *Vt, const float (&L2)[4],
+                                             const float (&Drow)[4], float (&p)[4][4], float (&ds)[4][4], int ty,
+                                             int tx) {
+    float dp[4][4] = {};
+#pragma unroll
+    for (int r = 0; r < 4; ++r)
+#pragma unroll
+        for (int c = 0; c < 4; ++c) p[r][c] = 0.f;
+    mm64(p, Qt, Kt, ty, tx);
+    mm64(dp, dOt, Vt, ty, tx);
 #pragma unroll
     for (int r = 0; r < 4; ++r) {
-        const int i = q0 + ty + 16 * r;
+        const int i = q0 + 4 * ty + r;
 #pragma unroll
         for (int c = 0; c < 4; ++c) {
-            const int k = k0 + tx + 16 * c;
-            const float p = allowed(i, k, a.T, a.causal) ? exp2f(s[r][c] * a.scale2 - L2[r]) : 0.f;
-            Ps[(ty + 16 * r) * TS + tx + 16 * c] = p;
-            dSs[(ty + 16 * r) * TS + tx + 16 * c] = p * (dp[r][c] - Drow[r]);
+            const int k = k0 + 4 * tx + c;
+            p[r][c] = allowed(i, k, a.T, a.causal) ? exp2f(p[r][c] * a.scale2 - L2[r]) : 0.f;
+            ds[r][c] = p[r][c] * (dp[r][c] - Drow[r]);
+        }
+    }
+}
+
+__device__ __forceinline__ void load_L2(const AttnArgs &a, int64_t head, int q0, int ty, float (&L2)[4]) {
+#pragma unroll
+    for (int r = 0; r < 4; ++r) {
+        const int i = q0 + 4 * ty + r;
+        L2[r] = i < a.T ? __ldg(a.L + head * a.T + i) * kLog2e : 0.f;
+    }
+}
+
+// ---------------------------------------------------------------- forward
+__global__ void __launch_bounds__(NT, 2) attn_fwd_kernel(const AttnArgs a) {
+    extern __shared__ __align__(16) float sm[];
+    float *Qt = sm, *Pt = sm + TILE, *KV = sm + 2 * TILE;  // KV: [2 buffers][Kt, V]
+    const int ty = threadIdx.x >> 4, tx = threadIdx.x & 15;
+    const int T = a.T;
+    const int64_t head = blockIdx.y;
+    const float *Qh = a.Q + head * T * HD, *Kh = a.K + head * T * HD, *Vh = a.V + head * T * HD;
+    int tl[2];
+    const int nt = tiles_of(blockIdx.x, (T + BT - 1) / BT, a.causal, tl);
+    for (int w = 0; w < nt; ++w) {
+        const int q0 = tl[w] * BT;
+        __syncthreads();  // the previous tile's buffers are no longer read
+        load_tile<true>(Qt, Qh, q0, T);
+        load_tile<true>(KV, Kh, 0, T);
+        load_tile<false>(KV + TILE, Vh, 0, T);
+        cp_commit();
+        float m[4], l[4], o[4][4];
+#pragma unroll
+        for (int r = 0; r < 4; ++r) {
+            m[r] = -INFINITY;
+            l[r] = 0.f;
+#pragma unroll
+            for (int c = 0; c < 4; ++c) o[r][c] = 0.f;
+        }
+        const int kend = a.causal ? min(T, q0 + BT) : T;  // keys past the tile's last query are masked
+        for (int k0 = 0, buf = 0; k0 < kend; k0 += BT, buf ^= 1) {
+            cp_wait_all();
+            __syncthreads();  // this block's K, V (and Q) landed; the other buffer and P are free
+            if (k0 + BT < kend) {
+                load_tile<true>(KV + (buf ^ 1) * 2 * TILE, Kh, k0 + BT, T);
+                load_tile<false>(KV + (buf ^ 1) * 2 * TILE + TILE, Vh, k0 + BT, T);
+            }
+            cp_commit();
+            const float *Kt = KV + buf * 2 * TILE, *Vs = Kt + TILE;
+            float s[4][4] = {};
+            mm64(s, Qt, Kt, ty, tx);
+#pragma unroll
+            for (int r = 0; r < 4; ++r) {
+                const int i = q0 + 4 * ty + r;
+                float mx = -INFINITY;
+#pragma unroll
+                for (int c = 0; c < 4; ++c) {
+                    const int k = k0 + 4 * tx + c;
+                    s[r][c] = allowed(i, k, T, a.causal) ? s[r][c] * a.scale2 : -INFINITY;
+                    mx = fmaxf(mx, s[r][c]);
+                }
+                const float mnew = fmaxf(m[r], half_max(mx));
+                // a row with no allowed key yet (only rows past T) keeps zero weights
+                const float alpha = mnew == -INFINITY ? 1.f : exp2f(m[r] - mnew);
+                float ls = 0.f;
+#pragma unroll
+                for (int c = 0; c < 4; ++c) {
+                    s[r][c] = mnew == -INFINITY ? 0.f : exp2f(s[r][c] - mnew);  // now P
+                    ls += s[r][c];
+                    o[r][c] *= alpha;
+                }
+                l[r] = l[r] * alpha + ls;
+                m[r] = mnew;
+            }
+            store_t(Pt, s, ty, tx);
+            __syncthreads();  // P complete
+            mm64(o, Pt, Vs, ty, tx);
+        }
+        cp_wait_all();  // (an empty group when the last block had no successor)
+#pragma unroll
+        for (int r = 0; r < 4; ++r) {
+            const int i = q0 + 4 * ty + r;
+            const float lrow = half_sum(l[r]);
+            if (i >= T) continue;
+            const float inv = 1.f / lrow;
+            float *orow = a.Out + (head * T + i) * HD + 4 * tx;
+#pragma unroll
+            for (int c = 0; c < 4; ++c) orow[c] = o[r][c] * inv;
+            if (tx == 0) a.Lout[head * T + i] = (m[r] + log2f(lrow)) * kLn2;
         }
     }
 }
 
 // ---------------------------------------------------------------- backward: dK, dV per key tile
-__global__ void __launch_bounds__(NT, 2) attn_bwd_dkdv_kernel(const AttnArgs a) {
-    extern __shared__ float sm[];
-    float *Ks = sm, *Vs = sm + TILE, *Qs = sm + 2 * TILE, *dOs = sm + 3 * TILE, *Ps = sm + 4 * TILE,
-          *dSs = sm + 5 * TILE;
+__global__ void __launch_bounds__(NT, 1) attn_bwd_dkdv_kernel(const AttnArgs a) {
+    extern __shared__ __align__(16) float sm[];
+    // Kt, Vt; P, dS (natural); [2 buffers][Qt, Q, dOt, dO]
+    float *Kt = sm, *Vt = sm + TILE, *Pn = sm + 2 * TILE, *dSn = sm + 3 * TILE, *QD = sm + 4 * TILE;
     const int ty = threadIdx.x >> 4, tx = threadIdx.x & 15;
     const int T = a.T;
     const int64_t head = blockIdx.y;
-    const int k0 = blockIdx.x * BT;
     const int64_t off = head * T * HD;
-    load_tile(Ks, a.K + off, k0, T);
-    load_tile(Vs, a.V + off, k0, T);
-    float dv[4][4] = {}, dk[4][4] = {};
-    // causal: query tiles from the one holding row k0 on (earlier queries see none of these keys)
-    for (int q0 = a.causal ? k0 : 0; q0 < T; q0 += BT) {
-        __syncthreads();  // the previous tile's Q, dO, P and dS are no longer read
-        load_tile(Qs, a.Q + off, q0, T);
-        load_tile(dOs, a.dO + off, q0, T);
-        __syncthreads();
-        float L2[4], Drow[4];
+    auto load_q = [&](float *dst, int q0) {
+        load_tile<true>(dst, a.Q + off, q0, T);
+        load_tile<false>(dst + TILE, a.Q + off, q0, T);
+        load_tile<true>(dst + 2 * TILE, a.dO + off, q0, T);
+        load_tile<false>(dst + 3 * TILE, a.dO + off, q0, T);
+    };
+    int tl[2];
+    const int nt = tiles_of(blockIdx.x, (T + BT - 1) / BT, a.causal, tl);
+    for (int w = 0; w < nt; ++w) {
+        const int k0 = tl[w] * BT;
+        // causal: query tiles from the one holding row k0 on (earlier queries see none of these keys)
+        const int qstart = a.causal ? k0 : 0;
+        __syncthreads();  // the previous key tile's buffers are no longer read
+        load_tile<true>(Kt, a.K + off, k0, T);
+        load_tile<true>(Vt, a.V + off, k0, T);
+        load_q(QD, qstart);
+        cp_commit();
+        float dv[4][4] = {}, dk[4][4] = {};
+        for (int q0 = qstart, buf = 0; q0 < T; q0 += BT, buf ^= 1) {
+            cp_wait_all();
+            __syncthreads();  // this tile's Q, dO landed; the other buffer, P and dS are free
+            if (q0 + BT < T) load_q(QD + (buf ^ 1) * 4 * TILE, q0 + BT);
+            cp_commit();
+            const float *Qt = QD + buf * 4 * TILE, *Qn = Qt + TILE, *dOt = Qt + 2 * TILE, *dOn = Qt + 3 * TILE;
+            float L2[4], Drow[4], p[4][4], ds[4][4];
+            load_L2(a, head, q0, ty, L2);
+            row_dots(a, head, q0, ty, tx, Drow);
+            probs_and_dS(a, q0, k0, Qt, Kt, dOt, Vt, L2, Drow, p, ds, ty, tx);
+            store_n(Pn, p, ty, tx);
+            store_n(dSn, ds, ty, tx);
+            __syncthreads();  // P and dS complete
+            mm64(dv, Pn, dOn, ty, tx);   // dV[k][d] += sum_i P[i][k] dO[i][d]
+            mm64(dk, dSn, Qn, ty, tx);   // dK[k][d] += sum_i dS[i][k] Q[i][d]
+        }
+        cp_wait_all();
 #pragma unroll
         for (int r = 0; r < 4; ++r) {
-            const int i = q0 + ty + 16 * r;
-            L2[r] = i < T ? __ldg(a.L + head * T + i) * kLog2e : 0.f;
-        }
-        row_dots(a, head, q0, dOs, ty, tx, Drow);
-        probs_and_dS(a, q0, k0, Qs, dOs, Ks, Vs, L2, Drow, Ps, dSs, ty, tx);
-        __syncthreads();  // P and dS complete
-        mm64(dv, ty, tx, [&](int k, int t) { return Ps[t * TS + k]; }, [&](int t, int d) { return dOs[t * TS + d]; });
-        mm64(dk, ty, tx, [&](int k, int t) { return dSs[t * TS + k]; }, [&](int t, int d) { return Qs[t * TS + d]; });
-    }
+            const int k = k0 + 4 * ty + r;
+            if (k >= T) continue;
 #pragma unroll
-    for (int r = 0; r < 4; ++r) {
-        const int k = k0 + ty + 16 * r;
-        if (k >= T) continue;
-#pragma unroll
-        for (int c = 0; c < 4; ++c) {
-            a.dV[off + (int64_t)k * HD + tx + 16 * c] = dv[r][c];
-            a.dK[off + (int64_t)k * HD + tx + 16 * c] = dk[r][c] * a.scale;
+            for (int c = 0; c < 4; ++c) {
+                a.dV[off + (int64_t)k * HD + 4 * tx + c] = dv[r][c];
+                a.dK[off + (int64_t)k * HD + 4 * tx + c] = dk[r][c] * a.scale;
+            }
         }
     }
 }
 
 // ---------------------------------------------------------------- backward: dQ per query tile
-__global__ void __launch_bounds__(NT, 2) attn_bwd_dq_kernel(const AttnArgs a) {
-    extern __shared__ float sm[];
-    float *Qs = sm, *dOs = sm + TILE, *Ks = sm + 2 * TILE, *Vs = sm + 3 * TILE, *dSs = sm + 4 * TILE,
-          *Ps = sm + 5 * TILE;
+__global__ void __launch_bounds__(NT, 1) attn_bwd_dq_kernel(const AttnArgs a) {
+    extern __shared__ __align__(16) float sm[];
+    // Qt, dOt; dS (transposed); [2 buffers][Kt, Vt, K]
+    float *Qt = sm, *dOt = sm + TILE, *dSt = sm + 2 * TILE, *KV = sm + 3 * TILE;
     const int ty = threadIdx.x >> 4, tx = threadIdx.x & 15;
     const int T = a.T;
     const int64_t head = blockIdx.y;
-    const int q0 = blockIdx.x * BT;
     const int64_t off = head * T * HD;
-    load_tile(Qs, a.Q + off, q0, T);
-    load_tile(dOs, a.dO + off, q0, T);
-    __syncthreads();
-    float L2[4], Drow[4];
+    auto load_k = [&](float *dst, int k0) {
+        load_tile<true>(dst, a.K + off, k0, T);
+        load_tile<true>(dst + TILE, a.V + off, k0, T);
+        load_tile<false>(dst + 2 * TILE, a.K + off, k0, T);
+    };
+    int tl[2];
+    const int nt = tiles_of(blockIdx.x, (T + BT - 1) / BT, a.causal, tl);
+    for (int w = 0; w < nt; ++w) {
+        const int q0 = tl[w] * BT;
+        __syncthreads();  // the previous query tile's buffers are no longer read
+        load_tile<true>(Qt, a.Q + off, q0, T);
+        load_tile<true>(dOt, a.dO + off, q0, T);
+        load_k(KV, 0);
+        cp_commit();
+        float L2[4], Drow[4];
+        load_L2(a, head, q0, ty, L2);
+        row_dots(a, head, q0, ty, tx, Drow);
+        float dq[4][4] = {};
+        const int kend = a.causal ? min(T, q0 + BT) : T;
+        for (int k0 = 0, buf = 0; k0 < kend; k0 += BT, buf ^= 1) {
+            cp_wait_all();
+            __syncthreads();  // this block's K, V landed; the other buffer and dS are free
+            if (k0 + BT < kend) load_k(KV + (buf ^ 1) * 3 * TILE, k0 + BT);
+            cp_commit();
+            const float *Kt = KV + buf * 3 * TILE, *Vt = Kt + TILE, *Kn = Kt + 2 * TILE;
+            float p[4][4], ds[4][4];
+            probs_and_dS(a, q0, k0, Qt, Kt, dOt, Vt, L2, Drow, p, ds, ty, tx);
+            store_t(dSt, ds, ty, tx);
+            __syncthreads();  // dS complete
+            mm64(dq, dSt, Kn, ty, tx);  // dQ[i][d] += sum_k dS[i][k] K[k][d]
+        }
+        cp_wait_all();
 #pragma unroll
-    for (int r = 0; r < 4; ++r) {
-        const int i = q0 + ty + 16 * r;
-        L2[r] = i < T ? __ldg(a.L + head * T + i) * kLog2e : 0.f;
-    }
-    row_dots(a, head, q0, dOs, ty, tx, Drow);
-    float dq[4][4] = {};
-    const int kend = a.causal ? min(T, q0 + BT) : T;
-    for (int k0 = 0; k0 < kend; k0 += BT) {
-        __syncthreads();  // the previous block's K, V and dS are no longer read
-        load_tile(Ks, a.K + off, k0, T);
-        load_tile(Vs, a.V + off, k0, T);
-        __syncthreads();
-        probs_and_dS(a, q0, k0, Qs, dOs, Ks, Vs, L2, Drow, Ps, dSs, ty, tx);
-        __syncthreads();  // dS complete
-        mm64(dq, ty, tx, [&](int i, int t) { return dSs[i * TS + t]; }, [&](int t, int d) { return Ks[t * TS + d]; });
-    }
+        for (int r = 0; r < 4; ++r) {
+            const int i = q0 + 4 * ty + r;
+            if (i >= T) continue;
 #pragma unroll
-    for (int r = 0; r < 4; ++r) {
-        const int i = q0 + ty + 16 * r;
-        if (i >= T) continue;
-#pragma unroll
-        for (int c = 0; c < 4; ++c) a.dQ[off + (int64_t)i * HD + tx + 16 * c] = dq[r][c] * a.scale;
+            for (int c = 0; c < 4; ++c) a.dQ[off + (int64_t)i * HD + 4 * tx + c] = dq[r][c] * a.scale;
+        }
     }
 }
 
-constexpr int FWD_SMEM = 4 * TILE * 4;  // Q, K, V, P
-constexpr int BWD_SMEM = 6 * TILE * 4;  // six tiles
+constexpr int FWD_SMEM = 6 * TILE * 4;    // Qt, Pt, two buffers of Kt and V
+constexpr int DKDV_SMEM = 12 * TILE * 4;  // Kt, Vt, P, dS, two buffers of Qt, Q, dOt, dO
+constexpr int DQ_SMEM = 9 * TILE * 4;     // Qt, dOt, dSt, two buffers of Kt, Vt, K
 
 cudaError_t set_smem_once() {
     static cudaError_t err = [] {
         cudaError_t e = cudaFuncSetAttribute(attn_fwd_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, FWD_SMEM);
         if (e == cudaSuccess)
-            e = cudaFuncSetAttribute(attn_bwd_dkdv_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, BWD_SMEM);
+            e = cudaFuncSetAttribute(attn_bwd_dkdv_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, DKDV_SMEM);
         if (e == cudaSuccess)
-            e = cudaFuncSetAttribute(attn_bwd_dq_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, BWD_SMEM);
+            e = cudaFuncSetAttribute(attn_bwd_dq_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, DQ_SMEM);
         return e;
     }();
     return err;
@@ -305,7 +393,8 @@ cudaError_t launch_attention_fwd(const float *Q, const float *K, const float *V,
     if (e != cudaSuccess) return e;
     AttnArgs a{Q, K, V, nullptr, nullptr, nullptr, O, L, nullptr, nullptr, nullptr, (int)T, causal, scale,
                scale * kLog2e};
-    const dim3 grid((unsigned)((T + BT - 1) / BT), (unsigned)heads);
+    const int n = (int)((T + BT - 1) / BT);
+    const dim3 grid((unsigned)(causal ? (n + 1) / 2 : n), (unsigned)heads);
     attn_fwd_kernel<<<grid, NT, FWD_SMEM, st>>>(a);
     return cudaGetLastError();
 }
@@ -316,11 +405,12 @@ cudaError_t launch_attention_bwd(const float *Q, const float *K, const float *V,
     const cudaError_t e = set_smem_once();
     if (e != cudaSuccess) return e;
     AttnArgs a{Q, K, V, O, dO, L, nullptr, nullptr, dQ, dK, dV, (int)T, causal, scale, scale * kLog2e};
-    const dim3 grid((unsigned)((T + BT - 1) / BT), (unsigned)heads);
-    attn_bwd_dkdv_kernel<<<grid, NT, BWD_SMEM, st>>>(a);
+    const int n = (int)((T + BT - 1) / BT);
+    const dim3 grid((unsigned)(causal ? (n + 1) / 2 : n), (unsigned)heads);
+    attn_bwd_dkdv_kernel<<<grid, NT, DKDV_SMEM, st>>>(a);
     cudaError_t e2 = cudaGetLastError();
     if (e2 != cudaSuccess) return e2;
-    attn_bwd_dq_kernel<<<grid, NT, BWD_SMEM, st>>>(a);
+    attn_bwd_dq_kernel<<<grid, NT, DQ_SMEM, st>>>(a);
     return cudaGetLastError();
 }
 
