@@ -69,6 +69,26 @@ __device__ __forceinline__ void mm64(float (&acc)[4][4], const float *At, const 
     }
 }
 
+// two independent products in one loop (twice the independent FMA chains per step)
+__device__ __forceinline__ void mm64_2(float (&c1)[4][4], const float *At1, const float *B1, float (&c2)[4][4],
+                                       const float *At2, const float *B2, int ty, int tx) {
+#pragma unroll 4
+    for (int t = 0; t < BT; ++t) {
+        const float4 a1 = *reinterpret_cast<const float4 *>(At1 + t * TS + 4 * ty);
+        const float4 b1 = *reinterpret_cast<const float4 *>(B1 + t * TS + 4 * tx);
+        const float4 a2 = *reinterpret_cast<const float4 *>(At2 + t * TS + 4 * ty);
+        const float4 b2 = *reinterpret_cast<const float4 *>(B2 + t * TS + 4 * tx);
+        const float av1[4] = {a1.x, a1.y, a1.z, a1.w}, av2[4] = {a2.x, a2.y, a2.z, a2.w};
+#pragma unroll
+        for (int r = 0; r < 4; ++r) {
+            fma2_bcast(c1[r][0], c1[r][1], av1[r], b1.x, b1.y);
+            fma2_bcast(c2[r][0], c2[r][1], av2[r], b2.x, b2.y);
+            fma2_bcast(c1[r][2], c1[r][3], av1[r], b1.z, b1.w);
+            fma2_bcast(c2[r][2], c2[r][3], av2[r], b2.z, b2.w);
+        }
+    }
+}
+
 __device__ __forceinline__ void cp_async4(float *dst, const float *src, int src_bytes) {
     asm volatile("cp.async.ca.shared.global [%0], [%1], 4, %2;" ::"r"(smem_u32(dst)), "l"(src), "r"(src_bytes)
                  : "memory");
@@ -156,8 +176,7 @@ __device__ __forceinline__ void probs_and_dS(const AttnArgs &a, int q0, int k0, 
     for (int r = 0; r < 4; ++r)
 #pragma unroll
         for (int c = 0; c < 4; ++c) p[r][c] = 0.f;
-    mm64(p, Qt, Kt, ty, tx);
-    mm64(dp, dOt, Vt, ty, tx);
+    mm64_2(p, Qt, Kt, dp, dOt, Vt, ty, tx);
 #pragma unroll
     for (int r = 0; r < 4; ++r) {
         const int i = q0 + 4 * ty + r;
@@ -179,82 +198,118 @@ __device__ __forceinline__ void load_L2(const AttnArgs &a, int64_t head, int q0,
 }
 
 // ---------------------------------------------------------------- forward
-__global__ void __launch_bounds__(NT, 2) attn_fwd_kernel(const AttnArgs a) {
+// The online-softmax update of one query tile for one key block: scores s (rows 4 ty + r of the
+// tile at q0, keys k0 + 4 tx + c) in, probabilities out (in s); state m, l, o rescaled.
+__device__ __forceinline__ void softmax_step(const AttnArgs &a, int q0, int k0, float (&s)[4][4], float (&m)[4],
+                                             float (&l)[4], float (&o)[4][4], int ty, int tx) {
+#pragma unroll
+    for (int r = 0; r < 4; ++r) {
+        const int i = q0 + 4 * ty + r;
+        float mx = -INFINITY;
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+            const int k = k0 + 4 * tx + c;
+            s[r][c] = allowed(i, k, a.T, a.causal) ? s[r][c] * a.scale2 : -INFINITY;
+            mx = fmaxf(mx, s[r][c]);
+        }
+        const float mnew = fmaxf(m[r], half_max(mx));
+        // a row with no allowed key yet (only rows past T) keeps zero weights
+        const float alpha = mnew == -INFINITY ? 1.f : exp2f(m[r] - mnew);
+        float ls = 0.f;
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+            s[r][c] = mnew == -INFINITY ? 0.f : exp2f(s[r][c] - mnew);  // now P
+            ls += s[r][c];
+            o[r][c] *= alpha;
+        }
+        l[r] = l[r] * alpha + ls;
+        m[r] = mnew;
+    }
+}
+
+__device__ __forceinline__ void store_out(const AttnArgs &a, int64_t head, int q0, const float (&m)[4],
+                                          const float (&l)[4], const float (&o)[4][4], int ty, int tx) {
+#pragma unroll
+    for (int r = 0; r < 4; ++r) {
+        const int i = q0 + 4 * ty + r;
+        const float lrow = half_sum(l[r]);
+        if (i >= a.T) continue;
+        const float inv = 1.f / lrow;
+        float *orow = a.Out + (head * a.T + i) * HD + 4 * tx;
+#pragma unroll
+        for (int c = 0; c < 4; ++c) orow[c] = o[r][c] * inv;
+        if (tx == 0) a.Lout[head * a.T + i] = (m[r] + log2f(lrow)) * kLn2;
+    }
+}
+
+// A CTA walks the key blocks once for its tile (pair): with a causal mask the lower tile of a
+// pair (j < n - 1 - j) needs blocks 0 .. j, the upper one 0 .. n - 1 - j; both share every K
+// and V block they have in common, and their two products per block run as independent chains.
+__global__ void __launch_bounds__(NT, 1) attn_fwd_kernel(const AttnArgs a) {
     extern __shared__ __align__(16) float sm[];
-    float *Qt = sm, *Pt = sm + TILE, *KV = sm + 2 * TILE;  // KV: [2 buffers][Kt, V]
+    // Qt of tile 0 and 1, Pt of tile 0 and 1, [2 buffers][Kt, V]
+    float *Qt0 = sm, *Qt1 = sm + TILE, *Pt0 = sm + 2 * TILE, *Pt1 = sm + 3 * TILE, *KV = sm + 4 * TILE;
     const int ty = threadIdx.x >> 4, tx = threadIdx.x & 15;
     const int T = a.T;
     const int64_t head = blockIdx.y;
     const float *Qh = a.Q + head * T * HD, *Kh = a.K + head * T * HD, *Vh = a.V + head * T * HD;
     int tl[2];
     const int nt = tiles_of(blockIdx.x, (T + BT - 1) / BT, a.causal, tl);
-    for (int w = 0; w < nt; ++w) {
-        const int q0 = tl[w] * BT;
-        __syncthreads();  // the previous tile's buffers are no longer read
-        load_tile<true>(Qt, Qh, q0, T);
-        load_tile<true>(KV, Kh, 0, T);
-        load_tile<false>(KV + TILE, Vh, 0, T);
+    const int q0a = tl[0] * BT, q0b = nt == 2 ? tl[1] * BT : q0a;
+    // keys past a tile's last query are masked (causal)
+    const int kend_a = a.causal ? min(T, q0a + BT) : T, kend_b = a.causal ? min(T, q0b + BT) : T;
+    const int kend = max(kend_a, kend_b);
+    load_tile<true>(Qt0, Qh, q0a, T);
+    if (nt == 2) load_tile<true>(Qt1, Qh, q0b, T);
+    load_tile<true>(KV, Kh, 0, T);
+    load_tile<false>(KV + TILE, Vh, 0, T);
+    cp_commit();
+    float m0[4], l0[4], o0[4][4], m1[4], l1[4], o1[4][4];
+#pragma unroll
+    for (int r = 0; r < 4; ++r) {
+        m0[r] = m1[r] = -INFINITY;
+        l0[r] = l1[r] = 0.f;
+#pragma unroll
+        for (int c = 0; c < 4; ++c) o0[r][c] = o1[r][c] = 0.f;
+    }
+    for (int k0 = 0, buf = 0; k0 < kend; k0 += BT, buf ^= 1) {
+        cp_wait_all();
+        __syncthreads();  // this block's K, V (and Q) landed; the other buffer and P are free
+        if (k0 + BT < kend) {
+            load_tile<true>(KV + (buf ^ 1) * 2 * TILE, Kh, k0 + BT, T);
+            load_tile<false>(KV + (buf ^ 1) * 2 * TILE + TILE, Vh, k0 + BT, T);
+        }
         cp_commit();
-        float m[4], l[4], o[4][4];
-#pragma unroll
-        for (int r = 0; r < 4; ++r) {
-            m[r] = -INFINITY;
-            l[r] = 0.f;
-#pragma unroll
-            for (int c = 0; c < 4; ++c) o[r][c] = 0.f;
+        const float *Kt = KV + buf * 2 * TILE, *Vs = Kt + TILE;
+        const bool two = nt == 2 && k0 < kend_b, one = k0 < kend_a;  // block-uniform
+        float s0[4][4] = {}, s1[4][4] = {};
+        if (one && two) {
+            mm64_2(s0, Qt0, Kt, s1, Qt1, Kt, ty, tx);
+        } else if (one) {
+            mm64(s0, Qt0, Kt, ty, tx);
+        } else {
+            mm64(s1, Qt1, Kt, ty, tx);
         }
-        const int kend = a.causal ? min(T, q0 + BT) : T;  // keys past the tile's last query are masked
-        for (int k0 = 0, buf = 0; k0 < kend; k0 += BT, buf ^= 1) {
-            cp_wait_all();
-            __syncthreads();  // this block's K, V (and Q) landed; the other buffer and P are free
-            if (k0 + BT < kend) {
-                load_tile<true>(KV + (buf ^ 1) * 2 * TILE, Kh, k0 + BT, T);
-                load_tile<false>(KV + (buf ^ 1) * 2 * TILE + TILE, Vh, k0 + BT, T);
-            }
-            cp_commit();
-            const float *Kt = KV + buf * 2 * TILE, *Vs = Kt + TILE;
-            float s[4][4] = {};
-            mm64(s, Qt, Kt, ty, tx);
-#pragma unroll
-            for (int r = 0; r < 4; ++r) {
-                const int i = q0 + 4 * ty + r;
-                float mx = -INFINITY;
-#pragma unroll
-                for (int c = 0; c < 4; ++c) {
-                    const int k = k0 + 4 * tx + c;
-                    s[r][c] = allowed(i, k, T, a.causal) ? s[r][c] * a.scale2 : -INFINITY;
-                    mx = fmaxf(mx, s[r][c]);
-                }
-                const float mnew = fmaxf(m[r], half_max(mx));
-                // a row with no allowed key yet (only rows past T) keeps zero weights
-                const float alpha = mnew == -INFINITY ? 1.f : exp2f(m[r] - mnew);
-                float ls = 0.f;
-#pragma unroll
-                for (int c = 0; c < 4; ++c) {
-                    s[r][c] = mnew == -INFINITY ? 0.f : exp2f(s[r][c] - mnew);  // now P
-                    ls += s[r][c];
-                    o[r][c] *= alpha;
-                }
-                l[r] = l[r] * alpha + ls;
-                m[r] = mnew;
-            }
-            store_t(Pt, s, ty, tx);
-            __syncthreads();  // P complete
-            mm64(o, Pt, Vs, ty, tx);
+        if (one) {
+            softmax_step(a, q0a, k0, s0, m0, l0, o0, ty, tx);
+            store_t(Pt0, s0, ty, tx);
         }
-        cp_wait_all();  // (an empty group when the last block had no successor)
-#pragma unroll
-        for (int r = 0; r < 4; ++r) {
-            const int i = q0 + 4 * ty + r;
-            const float lrow = half_sum(l[r]);
-            if (i >= T) continue;
-            const float inv = 1.f / lrow;
-            float *orow = a.Out + (head * T + i) * HD + 4 * tx;
-#pragma unroll
-            for (int c = 0; c < 4; ++c) orow[c] = o[r][c] * inv;
-            if (tx == 0) a.Lout[head * T + i] = (m[r] + log2f(lrow)) * kLn2;
+        if (two) {
+            softmax_step(a, q0b, k0, s1, m1, l1, o1, ty, tx);
+            store_t(Pt1, s1, ty, tx);
+        }
+        __syncthreads();  // P complete
+        if (one && two) {
+            mm64_2(o0, Pt0, Vs, o1, Pt1, Vs, ty, tx);
+        } else if (one) {
+            mm64(o0, Pt0, Vs, ty, tx);
+        } else {
+            mm64(o1, Pt1, Vs, ty, tx);
         }
     }
+    cp_wait_all();  // (an empty group when the last block had no successor)
+    store_out(a, head, q0a, m0, l0, o0, ty, tx);
+    if (nt == 2) store_out(a, head, q0b, m1, l1, o1, ty, tx);
 }
 
 // ---------------------------------------------------------------- backward: dK, dV per key tile
@@ -297,8 +352,8 @@ __global__ void __launch_bounds__(NT, 1) attn_bwd_dkdv_kernel(const AttnArgs a) 
             store_n(Pn, p, ty, tx);
             store_n(dSn, ds, ty, tx);
             __syncthreads();  // P and dS complete
-            mm64(dv, Pn, dOn, ty, tx);   // dV[k][d] += sum_i P[i][k] dO[i][d]
-            mm64(dk, dSn, Qn, ty, tx);   // dK[k][d] += sum_i dS[i][k] Q[i][d]
+            // dV[k][d] += sum_i P[i][k] dO[i][d], dK[k][d] += sum_i dS[i][k] Q[i][d]
+            mm64_2(dv, Pn, dOn, dk, dSn, Qn, ty, tx);
         }
         cp_wait_all();
 #pragma unroll
@@ -365,7 +420,7 @@ __global__ void __launch_bounds__(NT, 1) attn_bwd_dq_kernel(const AttnArgs a) {
     }
 }
 
-constexpr int FWD_SMEM = 6 * TILE * 4;    // Qt, Pt, two buffers of Kt and V
+constexpr int FWD_SMEM = 8 * TILE * 4;    // Qt and Pt of both tiles, two buffers of Kt and V
 constexpr int DKDV_SMEM = 12 * TILE * 4;  // Kt, Vt, P, dS, two buffers of Qt, Q, dOt, dO
 constexpr int DQ_SMEM = 9 * TILE * 4;     // Qt, dOt, dSt, two buffers of Kt, Vt, K
 
