@@ -35,22 +35,24 @@
 // scale.  A row whose fields all hold the zero entry c_z has D_j = (c_z/2) S_j
 // and gives y == 0 exactly.  A non-finite x makes every y of that matrix NaN.
 //
-// Roles (11 warps).  Two decode warpgroups (warps 0-3, 4-7) take the
-// 256-field stages of a tile alternately, each thread one TMEM lane (row): it
-// reads its row's code bytes from the box in shared memory, stores the two
-// words per code word to a TMEM stage with tcgen05.st, and hands the stage to
-// the MMA warp one decode later (the store completes meanwhile).  Warp 8 is
-// the producer: lane 0 issues the TMA copies of the code boxes (128 bytes x
-// 128 rows, 128-byte swizzle) into a ring, and after a tile's last box the
-// warp loads that tile's scales into a small shared ring, so that no decode
-// warp ever waits on a global load.  Warps 9 and 10 lane 0 each issue the MMAs
-// of one warpgroup's stages into their own accumulator of the tile and commit
-// each stage to the barrier that frees its TMEM stage; the epilogue adds the
-// two accumulators (exactly: both are small multiples of 1/4).  Two tile
-// buffers let the epilogue of a tile, run by warpgroup (tile % 2), overlap the
-// next tile.  The decode warps and the MMA warps build the B tile, once per
-// matrix.  A CTA takes a contiguous run of the (matrix, tile) pairs of a
-// strided batch.
+// Roles.  One CTA per SM holds three independent tile pipelines.  Pipeline w has
+// its own decode warpgroup (128 threads, one per TMEM lane: thread r reads its
+// row's code bytes from the box in shared memory and stores the two words per
+// code word to one of four TMEM A stages with tcgen05.st, handing the stage to
+// the MMA warp as soon as the store has completed), its own MMA issuer warp
+// (lane 0 issues the four MMAs of each stage into the pipeline's accumulator
+// and commits them to the barrier that frees the stage), its code-box ring and
+// its accumulator; the same warpgroup runs the tile's epilogue.  One producer
+// warp issues the TMA copies of every pipeline's code boxes (128 bytes x 128
+// rows, 128-byte swizzle) in the order the pipelines take their tiles; one
+// scale warp stages each tile's 127 scales in shared memory, so that no decode
+// warp ever waits on a global load.  The decode and MMA warps build the B
+// tile once per matrix (once per launch when the batch shares x).  A CTA takes
+// a contiguous run of the (matrix, tile) pairs of a strided batch; pipeline w
+// takes its tiles w, w + 3, ...  Measured on the 64-matrix rotation: three
+// pipelines with four A stages each and the immediate hand-off 0.97-1.00 us per
+// matrix, four pipelines with three stages 1.00-1.02, the earlier hand-off one
+// decode later 1.03-1.06.
 //
 // Requirements: cols % 512 == 0, cols <= 4096, 16-byte aligned codes (and
 // codes stride), an affine codebook.
@@ -74,11 +76,11 @@ constexpr int LANES = 128, TR = 127;  // TMEM lanes per tile; weight rows per ti
 constexpr int BOXB = 128 * LANES;     // bytes of one code box: 128 bytes (512 fields) x 128 rows
 constexpr int NPIECE = 14;            // radix-8 digits of x * 2^24
 constexpr int NCOL = 16;              // MMA N: the pieces and two zero columns
-constexpr int NWG = 4;                // tile pipelines per CTA (one CTA per SM), one decode warpgroup each
-constexpr int ASLOTS = 3;             // TMEM stages of A per pipeline, 256 fields (32 columns) each
+constexpr int NWG = 3;                // tile pipelines per CTA (one CTA per SM), one decode warpgroup each
+constexpr int ASLOTS = 4;             // TMEM stages of A per pipeline, 256 fields (32 columns) each
 constexpr int MAX_RING = 3;           // code boxes per pipeline in shared memory (a 1,536-field tile: 3)
 constexpr int TMEM_COLS = 512;        // SFA [0,8), SFB [8,16), accumulator of pipeline w [16 + 16 w, +16),
-                                      // A stages of pipeline w [128 + 96 w, +96)
+                                      // A stages of pipeline w [128 + 128 w, +128)
 constexpr int SFA_COL = 0, SFB_COL = 8, D_COL = 16, A_COL = 128, A_SPAN = 32 * ASLOTS;
 constexpr int NDEC = 128 * NWG, NTHREADS = NDEC + 32 * (2 + NWG), NBUILD = NDEC + 32 * NWG;
 constexpr int PRODUCER_WARP = 4 * NWG, MMA_WARP = PRODUCER_WARP + 1;  // MMA warp of pipeline w: MMA_WARP + w
@@ -545,10 +547,6 @@ __global__ void __launch_bounds__(NTHREADS, 1) gemv2_mxf4_kernel(const __grid_co
                     const int64_t row = (int64_t)(gt - mt * ntiles) * TR + r;
                     const bool real = r < TR && row < a.rows;
                     bool ok = __all_sync(0xffffffffu, *fail == 0);  // warp-uniform from here on
-                    // each stage's TMEM store completes while the next stage is decoded: the
-                    // stage is handed to the MMA warp one decode later (the last one at once)
-                    bool pend = false;
-                    int pas = 0;
                     for (int s = 0; s < nst && ok; ++s) {
                         if ((s & 1) == 0) {  // a new box
                             if (++d_bslot == ring) {
@@ -589,21 +587,14 @@ __global__ void __launch_bounds__(NTHREADS, 1) gemv2_mxf4_kernel(const __grid_co
                             __syncwarp();
                             if (lane == 0) mbar_arrive(&pp.bempty[slot]);
                         }
-                        if (pend) {
-                            tmem_wait_st();
-                            tc_fence_before_sync();
-                            __syncwarp();
-                            if (lane == 0) mbar_arrive(&pp.afull[pas]);
-                        }
+                        // the stage goes to the MMA warp as soon as its store has completed (handing
+                        // it over one decode later, to overlap the store, measured slower: the MMAs
+                        // then started a stage later and the A stages ran out first)
                         tmem_st32(a_base + lane_base + 32 * as, v);
-                        pend = true;
-                        pas = as;
-                    }
-                    if (pend) {
                         tmem_wait_st();
                         tc_fence_before_sync();
                         __syncwarp();
-                        if (lane == 0 && ok) mbar_arrive(&pp.afull[pas]);
+                        if (lane == 0) mbar_arrive(&pp.afull[as]);
                     }
                     // epilogue: the tile's scales (staged by the producer) and accumulator
                     if (ok) ok = __all_sync(0xffffffffu, spin(&pp.sfull, k & 1, kDevErrWaitFull));

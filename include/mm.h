@@ -354,7 +354,7 @@ enum {
                             the only rounding is the fp32 sum over the digits; 127 rows per
                             tile, the 128th lane forms the digit sums of x.  A non-finite x
                             gives NaN in every output.  rows_per_lane: 127-row tiles per CTA,
-                            which multiplies four at a time (0 = 4); split, warps and staging
+                            which multiplies three at a time (0 = 3); split, warps and staging
                             must be 0 (staging may be -1) */
 };
 
