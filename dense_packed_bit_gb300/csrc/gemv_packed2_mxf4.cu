@@ -54,7 +54,7 @@
 // matrix, four pipelines with three stages 1.00-1.02, the earlier hand-off one
 // decode later 1.03-1.06.
 //
-// Requirements: cols % 512 == 0, cols <= 4096, 16-byte aligned codes (and
+// Requirements: cols % 512 == 0, cols <= 12,800, 16-byte aligned codes (and
 // codes stride), an affine codebook.
 #include "mm_common.cuh"
 #include "mm_internal.h"
@@ -646,6 +646,8 @@ size_t mxf4_smem_bytes(int64_t cols, int ring) {
     return 1024 + (size_t)NWG * ring * BOXB + (size_t)cols * 10 + sizeof(Bars);
 }
 
+constexpr int64_t kMxf4MaxCols = 12800;
+
 cudaError_t launch_mxf4(const Mxf4Args &m, const void *codes, int64_t codes_stride, int pdl, int prefetch,
                         int tiles_per_cta, cudaStream_t st) {
     const int64_t rowbytes = m.cols / 4;
@@ -685,8 +687,11 @@ cudaError_t launch_mxf4(const Mxf4Args &m, const void *codes, int64_t codes_stri
 
 }  // namespace
 
+// cols: a multiple of 512 whose x digit tile, x and two code boxes per pipeline fit shared memory
+// (cols <= 12,800: the transposed 1,536 x 12,288 shape included); every per-digit sum stays exact
+// (multiples of 1/4 below 3 cols < 2^22)
 bool gemv_mxf4_supported(const PackedArgs &a) {
-    return a.cols % 512 == 0 && a.cols <= 4096 && (reinterpret_cast<uintptr_t>(a.codes) % 16) == 0 &&
+    return a.cols % 512 == 0 && a.cols <= kMxf4MaxCols && (reinterpret_cast<uintptr_t>(a.codes) % 16) == 0 &&
            a.rows < ((int64_t)1 << 31) - 128 && codebook_is_affine(a.cb);
 }
 

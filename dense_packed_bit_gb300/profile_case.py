@@ -11,6 +11,7 @@
     python -m dense_packed_bit_gb300.profile_case ternary --reps 1 [--tile 2] [--pdl 2: pdl + static weights]
     python -m dense_packed_bit_gb300.profile_case gemv_batched --reps 2 --matrices 16 [--dequant 6 --tiles 0]
     python -m dense_packed_bit_gb300.profile_case gemv_t --reps 3 --matrices 8   (1,536 x 12,288, automatic)
+    python -m dense_packed_bit_gb300.profile_case gemv_t --reps 3 --matrices 4 --dequant 6 --rows 3   (fp4 decode)
     python -m dense_packed_bit_gb300.profile_case attn --reps 2   (causal attention 32 x 512 x 64, forward + backward)
 
 One warm-up launch precedes the `reps` launches.  No timing is done here:
@@ -110,7 +111,9 @@ def main(argv=None):
         y = torch.empty((a.matrices, 1536), dtype=torch.float32, device=dev)
         for r in range(1 + a.reps):
             i = r % a.matrices
-            mm.mm_gemv_packed2_ex(codes[i], scales[i], x, y[i], 1536, 12288, c.codebook, pdl=1, independent=1)
+            # --dequant 6: the fp4 decode with --rows tiles of 127 rows per CTA; else the automatic decode
+            opts = dict(dequant=6, rows_per_lane=a.rows) if a.dequant == 6 else {}
+            mm.mm_gemv_packed2_ex(codes[i], scales[i], x, y[i], 1536, 12288, c.codebook, pdl=1, independent=1, **opts)
     elif a.op == "gemv4":
         codes, scales = [], []
         for i in range(a.matrices):

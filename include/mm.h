@@ -344,7 +344,7 @@ enum {
                             K = 32), x as exact e5m2 pieces is the B operand in shared memory,
                             fp32 accumulation in tensor memory; 127 rows per tile, the 128th
                             lane forms sum x with the same MMAs */
-    MM_DEQ_MXF4 = 6      /* same affine condition, cols % 512 == 0, cols <= 4096, 16-byte
+    MM_DEQ_MXF4 = 6      /* same affine condition, cols % 512 == 0, cols <= 12800, 16-byte
                             aligned codes: a 2-bit field in the low bits of a nibble is the
                             e2m1 value c/2, so two integer ops per eight fields write the codes
                             to tensor memory as the packed-fp4 A operand of tcgen05.mma
@@ -438,7 +438,7 @@ mm_status mm_gemm_packed2_ex(const uint8_t *codes, const uint16_t *scales, const
  * matrix b's codes at codes + b * codes_stride (bytes), its scales at scales +
  * b * scales_stride, its x at x + b * x_stride (x_stride 0: one x for every matrix)
  * and its y at y + b * y_stride (entries).  With an affine codebook, cols % 512 ==
- * 0, cols <= 4096, 16-byte aligned codes and codes_stride % 16 == 0 the whole batch
+ * 0, cols <= 12800, 16-byte aligned codes and codes_stride % 16 == 0 the whole batch
  * runs in one launch of the fp4 tensor-core decode (MM_DEQ_MXF4; each y_b equals bit for
  * bit the single MM_DEQ_MXF4 call's); failing that, with 16-byte aligned x and x_stride %
  * 8 == 0, one launch of the staged SIMT affine kernel (each y_b equals bit for bit the

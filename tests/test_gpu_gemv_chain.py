@@ -51,6 +51,7 @@ VARIANTS = [
     ("tcgen05", 2, 12288, 1536, dict(dequant=5)),
     ("mxf4", 2, 12288, 1536, dict(dequant=6)),
     ("transposed", 2, 1536, 12288, dict()),
+    ("mxf4_transposed", 2, 1536, 12288, dict(dequant=6)),
     ("staged_4bit", 4, 12288, 1536, dict(staging=1)),
     ("generic_4bit", 4, 12288, 1536, dict(staging=0)),
 ]

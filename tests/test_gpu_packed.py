@@ -530,7 +530,7 @@ def test_gemv_tcgen05(oracle, rows, cols, mode, tiles):
 
 
 @pytest.mark.parametrize("rows", [1, 126, 127, 128, 254, 255, 1000, 1100])
-@pytest.mark.parametrize("cols", [512, 1024, 1536, 2048, 4096])
+@pytest.mark.parametrize("cols", [512, 1024, 1536, 2048, 4096, 8192, 12288, 12800])
 @pytest.mark.parametrize("mode", FP8_MODES, ids=["serial", "chained", "independent"])
 @pytest.mark.parametrize("tiles", [0, 1, 2, 5])
 def test_gemv_mxf4(oracle, rows, cols, mode, tiles):
@@ -552,6 +552,24 @@ def test_gemv_mxf4_full_rotation_every_output(oracle):
         y = gemv(c.codes, c.scales, c.X, c.rows, c.cols, c.codebook, dequant=6, pdl=1, independent=1)
         ref, T = oracle.packed_gemm(c.codes, c.scales, c.X, c.rows, c.cols, c.codebook)
         check_bound(y, ref[0], T[0], f"matrix {i}")
+
+
+def test_gemv_mxf4_transposed_rotation_every_output(oracle):
+    # the transposed shape (1,536 rows x 12,288 fields: 13 tiles of 127 rows, 48 stages each) on
+    # the fp4 decode, 8 of its 64 matrices as independent calls, every output
+    for i in range(0, 64, 8):
+        c = synth.gemv_2bit_1536x12288(i)
+        y = gemv(c.codes, c.scales, c.X, c.rows, c.cols, c.codebook, dequant=6, rows_per_lane=5, pdl=1, independent=1)
+        ref, T = oracle.packed_gemm(c.codes, c.scales, c.X, c.rows, c.cols, c.codebook)
+        check_bound(y, ref[0], T[0], f"transposed matrix {i}")
+
+
+def test_gemv_mxf4_refuses_columns_past_the_shared_memory_plan():
+    import torch
+    rows, cols = 8, 13312
+    codes, scales, x = rand_case(rows, cols, seed=3)
+    with pytest.raises(mm.MMError, match="cols <= 12800"):
+        gemv(codes, scales, x, rows, cols, CB2, dequant=6)
 
 
 @pytest.mark.parametrize("cb", [CB2, np.array([-1, 0, 1, 2], np.float32), np.array([0, 0.5, 1, 1.5], np.float32),
