@@ -923,18 +923,19 @@ def main_mm(args):
                            "us_per_call": c1_call_s * 1e6,
                            "calls": f"{C1_CALLS} distinct seeded problems per step, back to back in one graph "
                                     "after the L2 flush (every operand cold)",
-                           "roofline": {"bound": "alu", "kernel": "gemm_skinny_kernel",
-                                        "achieved": C1_FLOP / c1_call_s / 1e12,
-                                        "peak": fp32_peak_max, "unit": "TFLOP/s",
-                                        "frac": C1_FLOP / c1_call_s / 1e12 / fp32_peak_max,
-                                        "traffic": traffic_for("gemm_skinny"),
-                                        "peak_source": f"{sms} SMs x 128 FP32 lanes x 2 flop x "
-                                                       f"{peaks.get('sm_max_mhz', 2070.0):.0f} MHz",
+                           "roofline": {"bound": "hbm", "kernel": "gemm_skinny_tc_kernel",
+                                        "achieved": C1_BYTES / c1_call_s / 1e9,
+                                        "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                                        "frac": C1_BYTES / c1_call_s / 1e9 / peaks["hbm_gbs"],
+                                        "traffic": traffic_for("gemm_skinny_tc"), "peak_source": peaks_src,
                                         "hbm_floor_us": C1_BYTES / peaks["hbm_gbs"] / 1e3,
                                         "fp32_floor_us": C1_FLOP / fp32_peak_max / 1e6,
+                                        "frac_of_fp32_simt_peak": C1_FLOP / c1_call_s / 1e12 / fp32_peak_max,
                                         "note": "302 MFLOP over 10.42 MB (A, B read once, C written): 29 flop per "
-                                                "byte, above the FP32 SIMT ridge (about 12), so the FP32 pipe "
-                                                "bounds this FFMA kernel"}},
+                                                "byte, below the 3xTF32 ridge (316 TFLOP/s / 6.8 TB/s = 47), so "
+                                                "HBM bounds the tensor-core kernel; a single cold 11 us call is "
+                                                "latency-bound (DRAM latency of its first slabs, the cluster "
+                                                "reduction), far from either floor"}},
         "gemv": {"metric": "2-bit 12288x1536 GEMV weight GB/s", "value": gemv_gbs, "unit": "GB/s",
                  "us_per_call": per_call_gemv_s * 1e6,
                  "mode": f"64 independent back-to-back calls over the rotation, {GEMV_INDEP_STREAMS} streams",

@@ -42,6 +42,7 @@
 #include "mm_common.cuh"
 #include "mm_internal.h"
 #include "tcgen05.cuh"
+#include "tf32x3_split.cuh"
 #include "tmap.h"
 
 #include <mutex>
@@ -142,48 +143,6 @@ __device__ __forceinline__ bool seg_next(const WsParams &p, int KT, int cid, int
     u.s = 0;
     cur += u.kt1 - u.kt0;
     return true;
-}
-
-__device__ __forceinline__ float lo_part(float a) {
-    return __fsub_rn(a, __uint_as_float(__float_as_uint(a) & 0xFFFFE000u));
-}
-
-__device__ __forceinline__ float4 lo_part4(float4 v) {
-    return make_float4(lo_part(v.x), lo_part(v.y), lo_part(v.z), lo_part(v.w));
-}
-
-// K-contiguous operand: the lo tile at the same (swizzled) offsets as the raw tile.
-template <int BYTES>
-__device__ __forceinline__ void lo_in_place_layout(const uint8_t *raw, uint8_t *lo, int ct) {
-    constexpr int N4 = BYTES / 16, R = (N4 + NCONV - 1) / NCONV;
-    float4 v[R];
-#pragma unroll
-    for (int i = 0; i < R; ++i)
-        if (N4 % NCONV == 0 || ct + i * NCONV < N4) v[i] = *reinterpret_cast<const float4 *>(raw + (ct + i * NCONV) * 16);
-#pragma unroll
-    for (int i = 0; i < R; ++i)
-        if (N4 % NCONV == 0 || ct + i * NCONV < N4) *reinterpret_cast<float4 *>(lo + (ct + i * NCONV) * 16) = lo_part4(v[i]);
-}
-
-// M/N-contiguous operand: raw [k][r] (BK rows of ROWS fp32, unswizzled) -> K-major
-// 64-byte-swizzled hi and lo tiles, row r, 16-byte chunk c at chunk c ^ ((r >> 1) & 3).
-// A warp covers 32 consecutive r: each column read is one 128-byte row segment and
-// each 8-lane phase of the 16-byte stores hits 8 distinct bank groups.
-template <int ROWS>
-__device__ __forceinline__ void split_transpose(const uint8_t *raw, uint8_t *hi, uint8_t *lo, int ct) {
-    const float *src = reinterpret_cast<const float *>(raw);
-    constexpr int TASKS = ROWS * (BK / 4), R = (TASKS + NCONV - 1) / NCONV;
-#pragma unroll
-    for (int i = 0; i < R; ++i) {
-        const int idx = ct + i * NCONV;
-        if (TASKS % NCONV != 0 && idx >= TASKS) break;
-        const int r = idx % ROWS, c = idx / ROWS;
-        const float4 v = make_float4(src[(4 * c + 0) * ROWS + r], src[(4 * c + 1) * ROWS + r],
-                                     src[(4 * c + 2) * ROWS + r], src[(4 * c + 3) * ROWS + r]);
-        const int off = r * 64 + ((c ^ ((r >> 1) & 3)) << 4);
-        *reinterpret_cast<float4 *>(hi + off) = v;
-        *reinterpret_cast<float4 *>(lo + off) = lo_part4(v);
-    }
 }
 
 // Record an error and raise the abort flag of this CTA and, in a pair, of its peer.
@@ -391,10 +350,10 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                     break;
                 }
                 uint8_t *st = smem + s * STAGE_BYTES;
-                if (A_KC) lo_in_place_layout<A_BYTES>(st + P::RAW_A, st + P::LO_A, ct);
-                else split_transpose<BM>(st + P::RAW_A, st + P::HI_A, st + P::LO_A, ct);
-                if (B_KC) lo_in_place_layout<P::B_BYTES>(st + P::RAW_B, st + P::LO_B, ct);
-                else split_transpose<BNC>(st + P::RAW_B, st + P::HI_B, st + P::LO_B, ct);
+                if (A_KC) tf32x3::lo_in_place_layout<A_BYTES, NCONV>(st + P::RAW_A, st + P::LO_A, ct);
+                else tf32x3::split_transpose<BM, NCONV>(st + P::RAW_A, st + P::HI_A, st + P::LO_A, ct);
+                if (B_KC) tf32x3::lo_in_place_layout<P::B_BYTES, NCONV>(st + P::RAW_B, st + P::LO_B, ct);
+                else tf32x3::split_transpose<BNC, NCONV>(st + P::RAW_B, st + P::HI_B, st + P::LO_B, ct);
                 fence_proxy_async_smem();
                 __syncwarp();
                 if (lane == 0) arrive_leader<CG>(&conv[s]);

@@ -109,8 +109,8 @@ mm_status check_packed4(const uint8_t *codes, const uint16_t *scales, const uint
 }
 
 // A product with few rows of C: the 3xTF32 kernel's 128 x 256 tiles would occupy at most a
-// quarter of the SMs, so the cluster split-K FFMA kernel keeps more of the GPU busy (64 x 3072
-// x 768 on GB300: measured against the 3xTF32 kernel's 12 tiles).
+// quarter of the SMs, so a few-rows kernel whose K range is split over a cluster keeps more of
+// the GPU busy (64 x 3072 x 768 on GB300: measured against the 3xTF32 kernel's 12 tiles).
 bool skinny_auto(int64_t M, int64_t N) {
     if (M > 64) return false;
     int dev = 0, sms = 152;
@@ -150,21 +150,32 @@ mm_status mm_gemm_f32_ex(int transA, int transB, int64_t M, int64_t N, int64_t K
     }
     const int tile = opts ? opts->tile : 0;
     const int splitk = opts ? opts->splitk : 0;
-    if ((path == MM_GEMM_TF32X3 || path == MM_GEMM_AUTO) && (tile < 0 || tile > 3))
-        return fail(MM_ERR_INVALID_ARG,
-                    "3xTF32 tile must be 0 (automatic), 1 (two-stage), 2 (warp-specialised) or 3 (CTA pairs)");
+    if ((path == MM_GEMM_TF32X3 && (tile < 0 || tile > 4)) || (path == MM_GEMM_AUTO && (tile < 0 || tile > 3)))
+        return fail(MM_ERR_INVALID_ARG, "3xTF32 tile must be 0 (automatic), 1 (two-stage), 2 (warp-specialised), "
+                                        "3 (CTA pairs) or 4 (few rows, K split in a cluster; 3xTF32 path only)");
     if (path == MM_GEMM_FFMA && tile != 0 && tile != 4)
         return fail(MM_ERR_INVALID_ARG, "FFMA tile must be 0 (TMA-staged 128 x 128) or 4 (few rows, K split in a cluster)");
-    if (splitk < 0 || splitk > 8 || (splitk != 0 && !(path == MM_GEMM_FFMA && tile == 4)))
-        return fail(MM_ERR_INVALID_ARG, "splitk is 0, or 1..8 with the FFMA tile 4");
+    if (splitk < 0 || splitk > 8 || (splitk != 0 && !((path == MM_GEMM_FFMA || path == MM_GEMM_TF32X3) && tile == 4)))
+        return fail(MM_ERR_INVALID_ARG, "splitk is 0, or 1..8 with tile 4 (FFMA or 3xTF32)");
     mm_status s = check_device();
     if (s != MM_OK) return s;
 
     mm::GemmArgs g{transA, transB, M, N, K, A, lda, B, ldb, C, ldc};
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
     cudaError_t e;
+    if (path == MM_GEMM_TF32X3 && tile == 4) {
+        if (!mm::gemm_skinny_tc_supported(g))
+            return fail(MM_ERR_INVALID_ARG, "3xTF32 tile 4 needs M <= 64, K <= %lld, 16-byte aligned A, B and lda, "
+                                            "ldb multiples of 4", (long long)mm::kTf32x3MaxK);
+        e = mm::launch_gemm_skinny_tc(g, splitk, st);
+        if (e != cudaSuccess) return cuda_fail(e, "gemm launch");
+        return ok();
+    }
     if ((path == MM_GEMM_FFMA && tile == 4) || (path == MM_GEMM_AUTO && tile == 0 && skinny_auto(M, N))) {
-        e = mm::launch_gemm_skinny(g, splitk, st);
+        // automatic: the tensor-core few-rows kernel where its operand rules and the 3xTF32 K
+        // margin allow, else the FFMA one (any alignment, any K)
+        e = path == MM_GEMM_AUTO && mm::gemm_skinny_tc_supported(g) ? mm::launch_gemm_skinny_tc(g, 0, st)
+                                                                    : mm::launch_gemm_skinny(g, splitk, st);
         if (e != cudaSuccess) return cuda_fail(e, "gemm launch");
         return ok();
     }
@@ -352,11 +363,13 @@ mm_status mm_gemm_f32_bias_act(int transA, int transB, int64_t M, int64_t N, int
     g.bias = bias;
     g.act = act;
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
-    // few rows: the cluster split-K FFMA kernel; else the warp-specialised 3xTF32 kernel when TMA can
+    // few rows: the cluster split-K kernels (tensor cores where TMA can describe the operands and K
+    // is within the 3xTF32 margin, else FFMA); else the warp-specialised 3xTF32 kernel when TMA can
     // describe the operands, else the plain tiled one
     // (a K beyond the 3xTF32 accuracy margin: the TMA-staged FFMA kernel)
     const bool long_k = K > mm::kTf32x3MaxK;
-    cudaError_t e = skinny_auto(M, N)                           ? mm::launch_gemm_skinny(g, 0, st)
+    cudaError_t e = skinny_auto(M, N) && mm::gemm_skinny_tc_supported(g) ? mm::launch_gemm_skinny_tc(g, 0, st)
+                    : skinny_auto(M, N)                           ? mm::launch_gemm_skinny(g, 0, st)
                     : !long_k && mm::gemm_tf32x3_supported(g) ? mm::launch_gemm_tf32x3_ws(g, M > 128 ? 1 : 0, st)
                     : mm::gemm_ffma_supported(g)               ? mm::launch_gemm_ffma(g, 0, st)
                                                                : mm::launch_gemm_simple(g, st);
@@ -714,6 +727,9 @@ mm_status mm_check_device_error(mm_stream_t stream) {
     const unsigned int zw = mm::gemm_tf32x3_ws_take_device_error(&e);
     if (e != cudaSuccess) return cuda_fail(e, "mm_check_device_error");
     if (zw != 0) return fail(MM_ERR_TIMEOUT, "a bounded device wait ran out in the warp-specialised 3xTF32 GEMM (code %u)", zw);
+    const unsigned int sk = mm::gemm_skinny_tc_take_device_error(&e);
+    if (e != cudaSuccess) return cuda_fail(e, "mm_check_device_error");
+    if (sk != 0) return fail(MM_ERR_TIMEOUT, "a bounded device wait ran out in the few-rows 3xTF32 GEMM (code %u)", sk);
     const unsigned int tw = mm::gemm_packed2_tcw_take_device_error(&e);
     if (e != cudaSuccess) return cuda_fail(e, "mm_check_device_error");
     if (tw != 0) return fail(MM_ERR_TIMEOUT, "a bounded device wait ran out in the tensor-core packed GEMM, tile 2 (code %u)", tw);

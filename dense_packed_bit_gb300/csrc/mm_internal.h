@@ -177,6 +177,15 @@ int gemm_skinny_split(int64_t M, int64_t N, int64_t K, int sms);
 bool gemm_skinny_supported(const GemmArgs &g);
 cudaError_t launch_gemm_skinny(const GemmArgs &g, int split, cudaStream_t s);
 
+// Few rows of C on the tensor cores (3xTF32): C computed transposed with 128 columns of C per
+// CTA as the MMA's M and the rows (M <= 64) as its N, the K range split over a (split, 1, 1)
+// cluster (0: automatic), partial tiles added in rank order through distributed shared
+// memory.  Needs the 3xTF32 operand rules and K <= kTf32x3MaxK.
+int gemm_skinny_tc_split(int64_t M, int64_t N, int64_t K, int sms);
+bool gemm_skinny_tc_supported(const GemmArgs &g);
+cudaError_t launch_gemm_skinny_tc(const GemmArgs &g, int split, cudaStream_t s);
+unsigned int gemm_skinny_tc_take_device_error(cudaError_t *err);
+
 // TMA-staged register-blocked FFMA kernel.  Needs 16-byte aligned A, B and
 // leading dimensions that are multiples of 4.  Returns cudaErrorNotSupported
 // when the arguments do not fit.

@@ -4,6 +4,7 @@
     python -m dense_packed_bit_gb300.profile_case gemm --size 2048 --path 1 --misalign 1   (lda = ldb = ldc = n + 1)
     python -m dense_packed_bit_gb300.profile_case c1 --reps 3 [--path 1 --tile 4 --split 8]   (64 x 768 x 3072 NN)
     python -m dense_packed_bit_gb300.profile_case c1 --reps 3 --path 2 --split 4   (workspace K slices + reduce)
+    python -m dense_packed_bit_gb300.profile_case c1 --reps 3 --path 2 --tile 4 --split 0   (few rows, tensor cores)
     python -m dense_packed_bit_gb300.profile_case gemv --reps 3 [--split 8 --rows 4 --warps 8 --dequant 2 --independent 1]
     python -m dense_packed_bit_gb300.profile_case gemv --reps 3 --split 0 --rows 1 --warps 0 --dequant 2 --staging 1
     python -m dense_packed_bit_gb300.profile_case gemv --reps 3 --misalign 1   (codes one byte off 16-byte alignment)
@@ -66,14 +67,15 @@ def main(argv=None):
         c = synth.gpt2_mlp_up_64x768x3072()
         A, B = torch.from_numpy(c.A).to(dev), torch.from_numpy(c.B).to(dev)
         C = torch.empty((c.M, c.N), dtype=torch.float32, device=dev)
-        if a.path == 2 and a.split > 1:
+        workspace_split = a.path == 2 and a.tile != 4 and a.split > 1
+        if workspace_split:
             wsf = mm.mm_gemm_f32_splitk_workspace(c.M, c.N, c.K, a.split)
             ws = torch.empty((max(wsf, 1),), dtype=torch.float32, device=dev)
             for _ in range(1 + a.reps):
                 mm.mm_gemm_f32_splitk(0, 0, c.M, c.N, c.K, A, c.K, B, c.N, C, c.N, a.split, ws, wsf)
-        for _ in range(1 + a.reps if not (a.path == 2 and a.split > 1) else 0):
+        for _ in range(0 if workspace_split else 1 + a.reps):
             mm.mm_gemm_f32_ex(0, 0, c.M, c.N, c.K, A, c.K, B, c.N, C, c.N, path=a.path, tile=a.tile,
-                              splitk=a.split if a.path == 1 and a.tile == 4 else 0)
+                              splitk=a.split if a.tile == 4 and a.path in (1, 2) else 0)
     elif a.op == "attn":
         c = synth.gpt2_attention_4x8x512x64()
         Q, K, V, dO = (torch.from_numpy(getattr(c, n)).to(dev) for n in ("Q", "K", "V", "dO"))

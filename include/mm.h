@@ -89,8 +89,10 @@ const char *mm_last_error(void);
 
 /*
  * Dense fp32 GEMM, C = op(A) . op(B).  M, N, K >= 1.
- * Kernel: M <= 64 with few output tiles, the few-rows FFMA kernel; else the 3xTF32
- * tensor-core kernel when A and B are 16-byte aligned with lda, ldb multiples of 4
+ * Kernel: M <= 64 with few output tiles, a few-rows kernel whose K range is split
+ * over a thread-block cluster -- on the tensor cores (3xTF32) when A and B are
+ * 16-byte aligned with lda, ldb multiples of 4 and K <= 16384, else in FFMA; else
+ * the 3xTF32 tensor-core kernel when A and B are 16-byte aligned with lda, ldb multiples of 4
  * and K <= 16384 (its accuracy margin: the tensor core's fp32 accumulation error
  * grows like sqrt(K) and would pass the bound near K = 3e4); else the TMA-staged
  * FFMA kernel, or the plain tiled one for operands TMA cannot describe.
@@ -306,14 +308,23 @@ typedef struct {
                       tile per CTA, two stages; 2 = persistent warp-specialised kernel,
                       128 x 256 tiles; 3 = the same with pairs of CTAs (a cluster of 2)
                       sharing 256 x 256 tiles.  Automatic: 3 when M > 128, else 2.
+                      MM_GEMM_TF32X3 only: 4 = few rows of C on the tensor cores (M <= 64,
+                      K <= 16384: C computed transposed, 128 columns of C per CTA as the
+                      MMA's M and the rows as its N, the K range split over a cluster of
+                      `splitk` CTAs whose partial tiles are added in rank order through
+                      distributed shared memory; no workspace).
                       MM_GEMM_FFMA: 4 = the kernel for few rows of C (64 x 64 FFMA tiles
                       whose K range is split over a thread-block cluster of `splitk` CTAs,
                       partial tiles added in rank order through distributed shared memory:
-                      no workspace, any alignment).  Automatic (MM_GEMM_AUTO, tile 0): this
-                      kernel when M <= 64 and the 3xTF32 kernel's 128 x 256 tiles would
-                      occupy at most a quarter of the SMs.  Other values are refused. */
-    int splitk;    /* MM_GEMM_FFMA tile 4: CTAs of the cluster sharing K, 1..8; 0 = automatic
-                      (about three CTAs per SM); other paths: must be 0 */
+                      no workspace, any alignment).  Automatic (MM_GEMM_AUTO, tile 0): the
+                      3xTF32 tile 4 when M <= 64, the 3xTF32 kernel's 128 x 256 tiles would
+                      occupy at most a quarter of the SMs and its operand rules and K margin
+                      hold; the FFMA tile 4 for such a product otherwise.  Other values are
+                      refused. */
+    int splitk;    /* tile 4 (MM_GEMM_FFMA or MM_GEMM_TF32X3): CTAs of the cluster sharing
+                      K, 1..8; 0 = automatic (FFMA: about three CTAs per SM; 3xTF32: as many
+                      as keep every 128-column tile's cluster within one wave, at least two
+                      16-deep K slabs each); other paths: must be 0 */
     int reserved[5];
 } mm_gemm_opts;
 

@@ -363,26 +363,94 @@ def test_gemm_skinny_parity(oracle, splitk, layout, shape, aligned):
     assert np.all(np.isnan(C[:, N:])), "columns past N were written"
 
 
-def test_gemm_skinny_is_automatic_for_few_rows_and_deterministic(oracle):
-    # the GPT-2 MLP up-projection at 64 tokens through mm_gemm_f32 takes the few-rows kernel:
-    # the same bits as the explicit tile-4 call, on every call; small integers are exact
-    c = synth.gpt2_mlp_up_64x768x3072()
-    dA, dB = to_dev(c.A), to_dev(c.B)
+def _few_rows_calls(c, lda, ldb, explicit_path):
+    """Automatic, explicit tile 4 on `explicit_path`, automatic again: three C arrays."""
+    Ap = np.zeros((c.M, lda), np.float32); Ap[:, :c.K] = c.A
+    Bp = np.zeros((c.K, ldb), np.float32); Bp[:, :c.N] = c.B
+    dA, dB = to_dev(Ap), to_dev(Bp)
     outs = []
     for explicit in (False, True, False):
         dC = empty_f32((c.M, c.N))
         if explicit:
-            mm.mm_gemm_f32_ex(0, 0, c.M, c.N, c.K, dA, c.K, dB, c.N, dC, c.N, path=mm.MM_GEMM_FFMA, tile=4)
+            mm.mm_gemm_f32_ex(0, 0, c.M, c.N, c.K, dA, lda, dB, ldb, dC, c.N, path=explicit_path, tile=4)
         else:
-            mm.mm_gemm_f32(0, 0, c.M, c.N, c.K, dA, c.K, dB, c.N, dC, c.N)
+            mm.mm_gemm_f32(0, 0, c.M, c.N, c.K, dA, lda, dB, ldb, dC, c.N)
+        mm.mm_check_device_error()
         outs.append(to_host(dC))
+    return outs
+
+
+@pytest.mark.parametrize("kernel", ["tensor_cores", "ffma"])
+def test_gemm_skinny_is_automatic_for_few_rows_and_deterministic(oracle, kernel):
+    # the GPT-2 MLP up-projection at 64 tokens through mm_gemm_f32 takes a few-rows kernel: the
+    # 3xTF32 one when TMA can describe the operands (leading dimensions multiples of four), the
+    # FFMA one otherwise (odd leading dimensions) -- the same bits as the explicit tile-4 call of
+    # that path, on every call; small integers are exact
+    c = synth.gpt2_mlp_up_64x768x3072()
+    tc = kernel == "tensor_cores"
+    outs = _few_rows_calls(c, c.K if tc else c.K + 1, c.N if tc else c.N + 3,
+                           mm.MM_GEMM_TF32X3 if tc else mm.MM_GEMM_FFMA)
     assert np.array_equal(outs[0].view(np.uint32), outs[1].view(np.uint32))
     assert np.array_equal(outs[0].view(np.uint32), outs[2].view(np.uint32))
     ref, T = oracle.gemm(0, 0, c.M, c.N, c.K, c.A, c.B)
-    check_bound(outs[0], ref, T, "automatic few-rows path")
-    A, B = stored(1, 1, 48, 1000, 777, seed=5, kind="int")
-    C = run(1, 1, 48, 1000, 777, A, B)
-    check_exact(C, oracle.gemm(1, 1, 48, 1000, 777, A, B)[0], "few rows, integers")
+    check_bound(outs[0], ref, T, f"automatic few-rows path ({kernel})")
+    for tA, tB, K in ((1, 1, 777), (0, 1, 776), (1, 0, 300)):
+        A, B = stored(tA, tB, 48, 1000, K, seed=5 + K, kind="int")
+        C = run(tA, tB, 48, 1000, K, A, B)
+        check_exact(C, oracle.gemm(tA, tB, 48, 1000, K, A, B)[0], f"few rows, integers, layout {tA}{tB}, K={K}")
+
+
+# ------------------------------------------------------------------ few rows on the tensor cores
+
+@pytest.mark.parametrize("splitk", [0, 1, 2, 3, 6, 8])
+@pytest.mark.parametrize("layout", list(LAYOUTS))
+@pytest.mark.parametrize("shape", [(64, 3072, 768), (1, 1, 1), (7, 130, 45), (64, 200, 1000), (33, 64, 31),
+                                   (17, 257, 300), (64, 128, 16)])
+@pytest.mark.parametrize("ldc_pad", [4, 5])
+def test_gemm_skinny_tc_parity(oracle, splitk, layout, shape, ldc_pad):
+    # 3xTF32 on tcgen05 with C computed transposed (128 columns of C per CTA as the MMA's M, the
+    # rows as its N), K cut over a cluster of `splitk` CTAs (a rank without K slabs adds zeros),
+    # partial tiles added in rank order through distributed shared memory; ragged M, N and K,
+    # padded leading dimensions (multiples of four floats), rows of C a multiple of four floats
+    # apart (16-byte stores) or not; columns past N stay untouched
+    tA, tB = LAYOUTS[layout]
+    M, N, K = shape
+    A, B = stored(tA, tB, M, N, K, seed=3100 + M + N + K)
+    lda = (A.shape[1] + 3) // 4 * 4 + 4
+    ldb = (B.shape[1] + 3) // 4 * 4 + 8
+    Ap = np.zeros((A.shape[0], lda), np.float32); Ap[:, :A.shape[1]] = A
+    Bp = np.zeros((B.shape[0], ldb), np.float32); Bp[:, :B.shape[1]] = B
+    dA, dB = to_dev(Ap), to_dev(Bp)
+    ldc = N + ldc_pad
+    dC = empty_f32((M, ldc))
+    mm.mm_gemm_f32_ex(tA, tB, M, N, K, dA, lda, dB, ldb, dC, ldc, path=mm.MM_GEMM_TF32X3, tile=4, splitk=splitk)
+    mm.mm_check_device_error()
+    C = to_host(dC)
+    ref, T = oracle.gemm(tA, tB, M, N, K, A, B)
+    check_bound(C[:, :N], ref, T, f"tensor-core few rows split {splitk} {layout} {shape} ldc N+{ldc_pad}")
+    assert np.all(np.isnan(C[:, N:])), "columns past N were written"
+
+
+def test_gemm_skinny_tc_k_margin_and_refusals(oracle):
+    # K at the 3xTF32 margin runs on the tensor cores within the bound; one slab past it, the
+    # automatic call takes the FFMA few-rows kernel, and the explicit tile 4 is refused, as are
+    # M > 64 and leading dimensions TMA cannot describe
+    M, N = 16, 256
+    for K in (16384, 16388):
+        A, B = stored(0, 0, M, N, K, seed=K)
+        C = run(0, 0, M, N, K, A, B)
+        ref, T = oracle.gemm(0, 0, M, N, K, A, B)
+        check_bound(C, ref, T, f"few rows, K={K}")
+    C = run(0, 0, M, N, 16384, A[:, :16384].copy(), B[:16384].copy(), path=(mm.MM_GEMM_TF32X3, 4))
+    ref, T = oracle.gemm(0, 0, M, N, 16384, A[:, :16384], B[:16384])
+    check_bound(C, ref, T, "tile 4 at the K margin")
+    import torch
+    z = torch.zeros(((16388 + 4) * 300,), device="cuda")
+    out = torch.empty((65 * 256,), device="cuda")
+    for (m, k, lda, ldb) in ((16, 16388, 16388, 256), (65, 64, 64, 256), (16, 64, 65, 256), (16, 64, 64, 258)):
+        with pytest.raises(mm.MMError) as e:
+            mm.mm_gemm_f32_ex(0, 0, m, 256, k, z, lda, z, ldb, out, 256, path=mm.MM_GEMM_TF32X3, tile=4)
+        assert e.value.status == mm.MM_ERR_INVALID_ARG
 
 
 # ------------------------------------------------------------------ the 3xTF32 accuracy margin on K
