@@ -15,7 +15,7 @@
 // tile is the hi operand, a lo pass writes the lo tile, and each 8-deep k-step
 // issues hi.hi + hi.lo + lo.hi.
 //
-// Roles (192 threads, one CTA per SM):
+// Roles (320 threads, one CTA per SM):
 //   warp 0      one thread issues the TMA loads of each 16-deep slab of the CTA's K
 //               share into a landing ring of 12 slabs: op(B)^T as 128 columns x 16
 //               (K-major with the 64-byte swizzle when B is stored transposed, else an
@@ -24,7 +24,7 @@
 //   warp 1      allocates 64 tensor-memory columns; one thread issues 2 x 3
 //               tcgen05.mma kind::tf32 (M = 128, N = 64, K = 8) per slab and commits
 //               each slab to the barrier that frees its operand stage;
-//   warps 2-5   the lo pass of each slab: the landed boxes become K-major hi and lo
+//   warps 2-9   the lo pass of each slab: the landed boxes become K-major hi and lo
 //               tiles in one of three operand stages (M/N-contiguous boxes transposed)
 //               and the landing slot goes back to the TMA thread at once, so that a
 //               CTA's whole K share is in flight from the start (a timeline of the
@@ -57,7 +57,7 @@ namespace {
 constexpr int FM = 128;                  // columns of C per CTA: the MMA's M, one per TMEM lane
 constexpr int TN = 64;                   // rows of C (at most 64): the MMA's N
 constexpr int BK = tf32x3::BK;           // fp32 of K per slab
-constexpr int NCONV = 128;               // lo-pass and epilogue threads (warps 2-5)
+constexpr int NCONV = 256;               // lo-pass and epilogue threads (warps 2-9)
 constexpr int WARP_TMA = 0, WARP_MMA = 1, WARP_CONV0 = 2;
 constexpr int NTHREADS = 64 + NCONV;
 constexpr int TMEM_COLS = 64;            // the accumulator: TN fp32 columns
@@ -295,15 +295,15 @@ __global__ void __launch_bounds__(NTHREADS, 1)
             }
         }
         // ---------------------------------------------------------------- partial tile
-        // the warp of lane quarter q reads TMEM lanes 32 q .. 32 q + 31 (columns f of C); after
-        // a failure the tile is written as zeros, so that the peers read defined values
+        // the warp of lane quarter q reads TMEM lanes 32 q .. 32 q + 31 (columns f of C), the
+        // rows of C of its half; after a failure the tile is written as zeros, so that the peers
+        // read defined values
         if (!mbar_wait_sleep(accf, 0)) fail(kDevErrWaitMma);
         tc_fence_after_sync();
         {
             const int q = warp & 3, f = 32 * q + lane;
             const bool have = nk > 0 && !*fail_flag;
-#pragma unroll
-            for (int c0 = 0; c0 < TN; c0 += 32) {
+            for (int c0 = 32 * ((warp - WARP_CONV0) / 4); c0 < TN; c0 += 32 * (NCONV / 128)) {
                 float v[32];
                 if (have) {
                     tmem_ld32(tmem + ((uint32_t)(32 * q) << 16) + (uint32_t)c0, v);
@@ -324,7 +324,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     if (!*fail_flag) {
         // ---------------------------------------------------------------- reduction and C
         // CTA `rank` owns the float4 tasks [lo, hi) of the tile's rows x 32 column quads, taken
-        // by all 192 threads; a warp's lanes take consecutive quads, i.e. 512 contiguous bytes
+        // by all 320 threads; a warp's lanes take consecutive quads, i.e. 512 contiguous bytes
         // of a row of C.  (Pushing each CTA's rows to their owner with one bulk copy per peer
         // instead measured slower: 12.8 against 11.2 us per 64 x 768 x 3072 call.)
         const int rows = p.M < TN ? p.M : TN;
