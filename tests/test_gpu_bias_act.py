@@ -179,6 +179,30 @@ def test_bias_act_padded_leading_dims(oracle, layout):
     assert np.all(np.isnan(got[:, N:])), "write into the padding of C"
 
 
+@pytest.mark.parametrize("act", [0, 1])
+@pytest.mark.parametrize("layout", list(LAYOUTS))
+@pytest.mark.parametrize("shape", [(17, 257, 300), (64, 130, 48), (1, 5, 8), (40, 1000, 777), (63, 128, 16)])
+def test_bias_act_few_rows_tensor_cores(oracle, shape, layout, act):
+    # M <= 64 with leading dimensions a multiple of four: the few-rows 3xTF32 kernel (C computed
+    # transposed, K split over a cluster), whose reduction applies bias and GELU to the summed
+    # partial tiles; ragged N and K, a padded C whose pad stays untouched
+    tA, tB = LAYOUTS[layout]
+    M, N, K = shape
+    lda = (M if tA else K) + 3
+    ldb = (K if tB else N) + 3
+    lda, ldb = lda + (-lda) % 4, ldb + (-ldb) % 4
+    A, B = operands(tA, tB, M, N, K, seed=91 + M + N + K + 7 * act, lda=lda, ldb=ldb)
+    bias = synth.normal_f32(35 + N, (N,), 1.0)
+    dA, dB, db = to_dev(A), to_dev(B), to_dev(bias)
+    dC = empty_f32((M, N + 5))
+    mm.mm_gemm_f32_bias_act(tA, tB, M, N, K, dA, A.shape[1], dB, B.shape[1], db, act, dC, N + 5)
+    mm.mm_check_device_error()
+    got = to_host(dC)
+    Y, T, Z = oracle.gemm_bias_act(tA, tB, M, N, K, A, B, bias, act, lda=A.shape[1], ldb=B.shape[1])
+    check(got[:, :N], Y, T, Z, f"few rows {layout} {shape} act={act}")
+    assert np.all(np.isnan(got[:, N:])), "write into the padding of C"
+
+
 @pytest.mark.parametrize("M", [48, 1024])
 def test_gelu_epilogue_within_the_activation_term_alone(oracle, M):
     # K = 1, A = z_r (row r), B = 1 and bias_j = j 2^-12 make every pre-activation z = z_r + bias_j
