@@ -70,7 +70,12 @@ ATTN_HEADS, ATTN_T, ATTN_D = 32, 512, 64  # causal self-attention, B = 4 x H = 8
 # dV, dP, dQ, dK, each 2 D flops per allowed (query, key) pair (T (T + 1) / 2 of them, causal)
 ATTN_FLOP = 6 * 2.0 * ATTN_HEADS * (ATTN_T * (ATTN_T + 1) // 2) * ATTN_D
 N_GEMV = 64
-GEMV_B_LAUNCHES = 4  # the rotation as this many back-to-back strided-batched launches per step
+GEMV_B_LAUNCHES = 8  # the rotation as this many back-to-back strided-batched launches per step
+# each launch writes its own y and reads nothing another writes, so it is launched independent
+# (programmatic dependent launch without the wait): the next launch's CTAs take the SMs that the
+# current one's last CTAs leave idle; measured, 4 launches: 0.957 -> 0.927 us per matrix (74 -> 76%
+# of HBM), 8 launches: 0.945 -> 0.911 (75 -> 78%)
+GEMV_B_OPTS = dict(dequant=6, pdl=1, independent=1)
 N_LAYERS = 16
 WORKLOAD = ("gpt2_mlp_up_64x768x3072_fp32_nn + square_2048_fp32_gemm_nn_nt_tn + gemv2bit_12288x1536_rotation64 + "
             "ternary_encoder_16x(222x768x3072,222x3072x768) + gemv4bit_12288x1536_rotation64 + "
@@ -266,7 +271,7 @@ class Workload:
             self.gemv_scales.append(self.gemv_scales_all[i])
             x = c.X
             self.gemv_cb = c.codebook
-        self.gemv_yb = torch.empty((N_GEMV, 12288), dtype=torch.float32, device=device)
+        self.gemv_yb = torch.empty((GEMV_B_LAUNCHES, N_GEMV, 12288), dtype=torch.float32, device=device)
         sha["gemv2_rotation64"].update(x)
         self.gemv_x = torch.from_numpy(x.reshape(-1)).to(device)
         self.gemv_y = torch.empty((N_GEMV, 12288), dtype=torch.float32, device=device)
@@ -413,9 +418,9 @@ def capture_phases(w: Workload, stream):
             mm.mm_gemm_f32(0, 0, C1_M, C1_N, C1_K, g["A"], C1_K, g["B"], C1_N, g["C"], C1_N)
 
     def gemv_batched():
-        for _ in range(GEMV_B_LAUNCHES):
-            mm.mm_gemv_packed2_strided_batched(w.gemv_codes_all, 12288 * 384, w.gemv_scales_all, 12288, w.gemv_x, 0,
-                                               w.gemv_yb, 12288, N_GEMV, 12288, 1536, w.gemv_cb)
+        for j in range(GEMV_B_LAUNCHES):
+            mm.mm_gemv_packed2_strided_batched_ex(w.gemv_codes_all, 12288 * 384, w.gemv_scales_all, 12288, w.gemv_x, 0,
+                                                  w.gemv_yb[j], 12288, N_GEMV, 12288, 1536, w.gemv_cb, **GEMV_B_OPTS)
 
     def gemv4():
         cur = torch.cuda.current_stream()
@@ -664,7 +669,11 @@ def bench_parity(w) -> dict:
     codes = w.gemv_codes_all.cpu().numpy()
     scales = w.gemv_scales_all.cpu().numpy().view(np.uint16)
     x = w.gemv_x.cpu().numpy().view(np.uint16)
-    y, yb, yc = w.gemv_y.cpu().numpy(), w.gemv_yb.cpu().numpy(), w.gemv_yc.cpu().numpy()
+    y, yb, yc = w.gemv_y.cpu().numpy(), w.gemv_yb[-1].cpu().numpy(), w.gemv_yc.cpu().numpy()
+    # the batched launches of a step compute the same rotation: every one must hold the same bits
+    yb_all = w.gemv_yb.cpu().numpy()
+    batched_same = bool(all(np.array_equal(yb_all[j].view(np.uint32), yb.view(np.uint32))
+                            for j in range(GEMV_B_LAUNCHES)))
     worst = worst_b = 0.0
     chain_worst, chain_checked = 0.0, 0
     for i in range(N_GEMV):
@@ -679,7 +688,8 @@ def bench_parity(w) -> dict:
             chain_worst = max(chain_worst, parity_ratio(yc[i], rc[0], Tc[0]))
             chain_checked += 1
     out["gemv2_rotation64"] = {"worst": worst, "outputs": N_GEMV * 12288}
-    out["gemv2_batched"] = {"worst": worst_b, "outputs": N_GEMV * 12288}
+    out["gemv2_batched"] = {"worst": worst_b if batched_same else float("inf"), "outputs": N_GEMV * 12288,
+                            "launches_bit_identical": batched_same}
     out["gemv2_chain"] = {"worst": chain_worst, "calls_checked": chain_checked,
                           "note": "later calls read the previous call's fp32 bits as fp16; calls whose x "
                                   "holds inf or NaN patterns are not compared"}
@@ -983,7 +993,9 @@ def main_mm(args):
                  "batched": {"value": world * GEMV_WEIGHT_BYTES / per_mat_gemvb_s / 1e9, "unit": "GB/s",
                              "us_per_matrix": per_mat_gemvb_s * 1e6,
                              "mode": f"the 64-matrix rotation (288 MiB) as one mm_gemv_packed2_strided_batched "
-                                     f"launch, {GEMV_B_LAUNCHES} launches back to back per step, one shared x",
+                                     f"launch, {GEMV_B_LAUNCHES} launches back to back per step, one shared x, each "
+                                     f"into its own y, launched independent (programmatic dependent launch)",
+                             "opts": GEMV_B_OPTS,
                              "kernel": "gemv2_mxf4_kernel (automatic: codes as packed e2m1 in tensor memory, x as "
                                        "14 exact e2m1 digit pieces, tcgen05.mma kind::mxf4)",
                              "roofline": {"bound": "hbm", "achieved": GEMV_TOTAL_BYTES / per_mat_gemvb_s / 1e9,

@@ -214,10 +214,12 @@ def mm_gemv_packed2_strided_batched(codes, codes_stride, scales, scales_stride, 
 
 
 def mm_gemv_packed2_strided_batched_ex(codes, codes_stride, scales, scales_stride, x, x_stride, y, y_stride, batch,
-                                       rows, cols, codebook, stream=None, *, dequant=0, rows_per_lane=0):
+                                       rows, cols, codebook, stream=None, *, dequant=0, rows_per_lane=0, pdl=0,
+                                       weights_static=0, independent=0):
     """mm_gemv_packed2_strided_batched with a decode choice (dequant: 0, MM_DEQ_AFFINE or MM_DEQ_MXF4;
-    rows_per_lane: 127-row tiles per CTA for MM_DEQ_MXF4, 0 = automatic)."""
-    o = GemvOpts(0, rows_per_lane, 0, dequant, 0, 0, 0, -1)
+    rows_per_lane: 127-row tiles per CTA for MM_DEQ_MXF4, 0 = automatic; pdl / weights_static /
+    independent: programmatic dependent launch options of the fp4 decode)."""
+    o = GemvOpts(0, rows_per_lane, 0, dequant, pdl, weights_static, independent, -1)
     _check(load_library().mm_gemv_packed2_strided_batched_ex(
         _ptr(codes), codes_stride, _ptr(scales), scales_stride, _ptr(x), x_stride, _ptr(y), y_stride, batch, rows,
         cols, _codebook(codebook), _stream(stream), ctypes.byref(o)))

@@ -709,7 +709,7 @@ cudaError_t launch_gemv_mxf4(const PackedArgs &a, const GemvConfig &cfg, cudaStr
     return launch_mxf4(m, a.codes, 0, cfg.pdl, prefetch, cfg.blocks_per_cta, st);
 }
 
-cudaError_t launch_gemv_batched_mxf4(const PackedBatch &p, int tiles_per_cta, cudaStream_t st) {
+cudaError_t launch_gemv_batched_mxf4(const PackedBatch &p, int tiles_per_cta, const GemvConfig &cfg, cudaStream_t st) {
     if (!gemv_batched_mxf4_supported(p)) return cudaErrorNotSupported;
     const Mxf4Args m{p.scales, p.scales_stride, p.x, p.x_stride, p.y, p.y_stride, p.batch, p.rows, p.cols, p.cb[0],
                      p.cb[1] - p.cb[0]};
@@ -722,7 +722,8 @@ cudaError_t launch_gemv_batched_mxf4(const PackedBatch &p, int tiles_per_cta, cu
         tpc = (int)std::max<int64_t>(NWG, (total + sms - 1) / sms);
         tpc = (tpc + NWG - 1) / NWG * NWG;
     }
-    return launch_mxf4(m, p.codes, p.codes_stride, 0, 0, tpc, st);
+    const int prefetch = !cfg.pdl ? 0 : cfg.independent ? 2 : cfg.weights_static ? 1 : 0;
+    return launch_mxf4(m, p.codes, p.codes_stride, cfg.pdl, prefetch, tpc, st);
 }
 
 unsigned int gemv_mxf4_take_device_error(cudaError_t *err) {

@@ -569,9 +569,19 @@ mm_status mm_gemv_packed2_strided_batched_ex(const uint8_t *codes, int64_t codes
                                              const float codebook[4], mm_stream_t stream, const mm_gemv_opts *opts) {
     int dequant = opts ? opts->dequant : MM_DEQ_AUTO;
     const int tiles = opts ? opts->rows_per_lane : 0;
-    if (opts && (opts->split || opts->warps || opts->pdl || opts->weights_static || opts->independent ||
-                 opts->staging > 0))
-        return fail(MM_ERR_INVALID_ARG, "the batched GEMV takes only dequant and rows_per_lane options");
+    if (opts && (opts->split || opts->warps || opts->staging > 0))
+        return fail(MM_ERR_INVALID_ARG,
+                    "the batched GEMV takes only dequant, rows_per_lane, pdl, weights_static and independent options");
+    mm::GemvConfig cfg{0, 0, 0, 0, 0, 0, 0, -1, 0};  // no programmatic launch unless asked for
+    if (opts) {
+        cfg.pdl = opts->pdl;
+        cfg.weights_static = opts->weights_static;
+        cfg.independent = opts->independent;
+    }
+    if ((cfg.pdl != 0 && cfg.pdl != 1) || (cfg.weights_static != 0 && cfg.weights_static != 1) ||
+        (cfg.independent != 0 && cfg.independent != 1))
+        return fail(MM_ERR_INVALID_ARG, "pdl, weights_static and independent must be 0 or 1");
+    const bool launch_opts = cfg.pdl || cfg.weights_static || cfg.independent;
     if (dequant != MM_DEQ_AUTO && dequant != MM_DEQ_AFFINE && dequant != MM_DEQ_MXF4)
         return fail(MM_ERR_INVALID_ARG, "the batched GEMV decode must be MM_DEQ_AUTO, MM_DEQ_AFFINE or MM_DEQ_MXF4");
     if (tiles < 0 || tiles > 4096) return fail(MM_ERR_INVALID_ARG, "rows_per_lane (tiles per CTA) must be 0..4096");
@@ -602,10 +612,12 @@ mm_status mm_gemv_packed2_strided_batched_ex(const uint8_t *codes, int64_t codes
     // automatic: the fp4 tensor-core decode, measured fastest for a batch in one launch on GB300
     // (64 x 12,288 x 1,536: 0.975 us per matrix against 1.42 for the staged SIMT affine kernel)
     if (dequant == MM_DEQ_MXF4 || (dequant == MM_DEQ_AUTO && mm::gemv_batched_mxf4_supported(p))) {
-        const cudaError_t e = mm::launch_gemv_batched_mxf4(p, tiles, st);
+        const cudaError_t e = mm::launch_gemv_batched_mxf4(p, tiles, cfg, st);
         if (e != cudaSuccess) return cuda_fail(e, "batched gemv launch");
         return ok();
     }
+    if (launch_opts)
+        return fail(MM_ERR_INVALID_ARG, "pdl, weights_static and independent need the fp4 tensor-core batched decode");
     if (mm::gemv_batched_supported(p)) {
         const cudaError_t e = mm::launch_gemv_batched(p, st);
         if (e != cudaSuccess) return cuda_fail(e, "batched gemv launch");

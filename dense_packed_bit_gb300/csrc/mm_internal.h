@@ -100,7 +100,8 @@ unsigned int gemv_rows_take_device_error(cudaError_t *err);
 bool gemv_mxf4_supported(const PackedArgs &a);
 bool gemv_batched_mxf4_supported(const PackedBatch &p);
 cudaError_t launch_gemv_mxf4(const PackedArgs &a, const GemvConfig &cfg, cudaStream_t s);
-cudaError_t launch_gemv_batched_mxf4(const PackedBatch &p, int tiles_per_cta, cudaStream_t s);
+// cfg: pdl, weights_static and independent as for a single call (the batch is one kernel)
+cudaError_t launch_gemv_batched_mxf4(const PackedBatch &p, int tiles_per_cta, const GemvConfig &cfg, cudaStream_t s);
 unsigned int gemv_mxf4_take_device_error(cudaError_t *err);
 bool gemv_tc_supported(const PackedArgs &a);
 cudaError_t launch_gemv_tc(const PackedArgs &a, const GemvConfig &cfg, cudaStream_t s);

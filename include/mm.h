@@ -470,10 +470,15 @@ mm_status mm_gemv_packed2_strided_batched(const uint8_t *codes, int64_t codes_st
  * mm_gemv_opts whose dequant is MM_DEQ_AUTO, MM_DEQ_AFFINE (the staged SIMT affine
  * kernel when the shape allows) or MM_DEQ_MXF4 (one launch of the fp4 tensor-core
  * decode over the whole batch: its requirements, plus codes_stride % 16 == 0; each CTA,
- * one per SM, takes rows_per_lane consecutive 127-row tiles of the batch, four at a
- * time, 0 = spread evenly over the SMs); every other field 0 (staging may be -1).  Each
- * y_b then equals bit for bit the single MM_DEQ_MXF4 call's.  Errors: as mm_gemv_packed2_strided_batched, plus
- * MM_ERR_INVALID_ARG for other options or a decode the shape does not allow.
+ * one per SM, takes rows_per_lane consecutive 127-row tiles of the batch, three at a
+ * time, 0 = spread evenly over the SMs).  With the fp4 decode, pdl, weights_static and
+ * independent mean what they mean for one mm_gemv_packed2_ex call, the batch being one
+ * kernel: independent = 1 promises that nothing this launch reads or writes is written by
+ * the kernel before it in the stream, so that launch runs without waiting for it and
+ * back-to-back batched launches overlap their first and last CTAs.  Every other field 0
+ * (staging may be -1).  Each y_b then equals bit for bit the single MM_DEQ_MXF4 call's.
+ * Errors: as mm_gemv_packed2_strided_batched, plus MM_ERR_INVALID_ARG for other options,
+ * launch options without the fp4 decode, or a decode the shape does not allow.
  */
 mm_status mm_gemv_packed2_strided_batched_ex(const uint8_t *codes, int64_t codes_stride,
                                              const uint16_t *scales, int64_t scales_stride,

@@ -165,7 +165,9 @@ def test_batched_gemv_mxf4_refusals():
         run_batched_mxf4(c2, s2, x2, rows, 1000, CB2, True)
     dc, ds, dx = to_dev(codes), to_dev(scales), to_dev(x)
     dy = empty_f32((2, rows))
-    for kw in (dict(dequant=mm.MM_DEQ_FP8), dict(dequant=mm.MM_DEQ_MXF4, rows_per_lane=-1)):
+    for kw in (dict(dequant=mm.MM_DEQ_FP8), dict(dequant=mm.MM_DEQ_MXF4, rows_per_lane=-1),
+               dict(dequant=mm.MM_DEQ_AFFINE, pdl=1), dict(dequant=mm.MM_DEQ_MXF4, pdl=2),
+               dict(dequant=mm.MM_DEQ_MXF4, independent=3)):
         with pytest.raises(mm.MMError):
             mm.mm_gemv_packed2_strided_batched_ex(dc, rows * cols // 4, ds, rows, dx, 0, dy, rows, 2, rows, cols,
                                                   CB2, **kw)

@@ -119,3 +119,78 @@ def test_gemv_chain_reads_and_writes_after_its_predecessor(oracle, variant, weig
         ref3, T3 = _oracle(oracle, bits, codes[2], ones, x3, rows, cols, cb)
         worst = check_bound(to_host(Q)[:rows], ref3, T3, f"{name}: call 3 read call 2's y (repeat {rep})")
     print(f"{name} weights_static={weights_static}: call 3 worst |err|/T = {worst:.3e}")
+
+
+@pytest.mark.parametrize("weights_static", [0, 1])
+def test_batched_fp4_chain_reads_and_writes_after_its_predecessor(oracle, weights_static):
+    # the same three-call chain through the strided-batched fp4 launch (two matrices per call,
+    # a shared x): with programmatic dependent launch each batched kernel may start while the
+    # previous one runs, and must still read x and write y only after it
+    import torch
+    batch, rows, cols = 2, 12288, 1536
+    rb = cols // 4
+    opts = dict(dequant=mm.MM_DEQ_MXF4, pdl=1, weights_static=weights_static)
+    rng = np.random.default_rng(77 + weights_static)
+    codes = [np.stack([_codes(2, rows, cols, 900 + 10 * i + b) for b in range(batch)]) for i in range(3)]
+    ones = np.full((batch, rows), 0x3C00, np.uint16)
+    x1 = rng.integers(-1, 2, size=cols).astype(np.float16).view(np.uint16)
+    x2 = rng.integers(-1, 2, size=cols).astype(np.float16).view(np.uint16)
+    nfl = max(batch * rows, (cols + 1) // 2)
+    P, Q = empty_f32((nfl,)), empty_f32((nfl,))
+    y1 = empty_f32((batch * rows,))
+    dc = [to_dev(c) for c in codes]
+    ds = to_dev(ones)
+    x1_t = torch.from_numpy(x1.view(np.int16)).to(P.device)
+    x2_t = torch.from_numpy(x2.view(np.int16)).to(P.device)
+    Px = P.view(torch.int16)[:cols]
+    Qx = Q.view(torch.int16)[:cols]
+
+    def call(i, x, y):
+        mm.mm_gemv_packed2_strided_batched_ex(dc[i], rows * rb, ds, rows, x, 0, y, rows, batch, rows, cols, CB2,
+                                              **opts)
+
+    ref1 = [_oracle(oracle, 2, codes[0][b], ones[b], x1, rows, cols, CB2)[0] for b in range(batch)]
+    ref2 = [_oracle(oracle, 2, codes[1][b], ones[b], x2, rows, cols, CB2)[0] for b in range(batch)]
+    assert np.all(np.abs(ref2[0]) < 2048), "y2 must read as finite fp16 values"
+    for rep in range(3):
+        P.fill_(float("nan"))
+        Q.fill_(float("nan"))
+        Px.copy_(x1_t)
+        Qx.copy_(x2_t)
+        call(0, Px, y1)
+        call(1, Qx, P[:batch * rows])
+        call(2, Px, Q[:batch * rows])
+        mm.mm_check_device_error()
+        y1h, Ph, Qh = to_host(y1), to_host(P), to_host(Q)
+        for b in range(batch):
+            check_exact(y1h[b * rows:(b + 1) * rows], ref1[b], f"batched call 1, matrix {b}")
+            check_exact(Ph[b * rows:(b + 1) * rows], ref2[b], f"batched call 2, matrix {b}")
+        x3 = Ph.view(np.uint16)[:cols].copy()
+        assert np.all(np.isfinite(x3.view(np.float16)))
+        for b in range(batch):
+            ref3, T3 = _oracle(oracle, 2, codes[2][b], ones[b], x3, rows, cols, CB2)
+            check_bound(Qh[b * rows:(b + 1) * rows], ref3, T3, f"batched call 3, matrix {b} (repeat {rep})")
+
+
+def test_batched_fp4_independent_launches_same_bits():
+    # back-to-back batched launches with independent = 1 (no wait on the previous kernel), each
+    # into its own y: the same bits as plain launches
+    import torch
+    batch, rows, cols = 8, 4000, 1536
+    rb = cols // 4
+    codes = np.stack([_codes(2, rows, cols, 950 + b) for b in range(batch)])
+    scales = synth.uniform_f16_bits(951, (batch, rows), 0.005, 0.05)
+    x = synth.normal_f16_bits(952, (cols,))
+    dc, ds, dx = to_dev(codes), to_dev(scales), to_dev(x)
+    plain = empty_f32((batch, rows))
+    mm.mm_gemv_packed2_strided_batched_ex(dc, rows * rb, ds, rows, dx, 0, plain, rows, batch, rows, cols, CB2,
+                                          dequant=mm.MM_DEQ_MXF4)
+    ref = to_host(plain)
+    for opts in (dict(pdl=1), dict(pdl=1, weights_static=1), dict(pdl=1, independent=1)):
+        ys = [empty_f32((batch, rows)) for _ in range(4)]
+        for y in ys:
+            mm.mm_gemv_packed2_strided_batched_ex(dc, rows * rb, ds, rows, dx, 0, y, rows, batch, rows, cols, CB2,
+                                                  dequant=mm.MM_DEQ_MXF4, **opts)
+        mm.mm_check_device_error()
+        for j, y in enumerate(ys):
+            assert np.array_equal(to_host(y).view(np.uint32), ref.view(np.uint32)), f"{opts}: launch {j}"
