@@ -256,6 +256,10 @@ class Workload:
                                   C=torch.empty((c.M, c.N), dtype=torch.float32, device=device),
                                   C_ffma=torch.empty((c.M, c.N), dtype=torch.float32, device=device),
                                   hA=A, hB=B))
+        import dense_packed_bit_gb300 as mm
+        # the FFMA phase runs through the split entry point: its stream-K tail's workspace
+        self.ffma_ws_floats = mm.mm_gemm_f32_splitk_workspace_ex(2048, 2048, 2048, 0, path=mm.MM_GEMM_FFMA)
+        self.ffma_ws = torch.empty(max(self.ffma_ws_floats, 4), dtype=torch.float32, device=device)
         # the rotation as one contiguous [64, 12288, 384] buffer: the per-call phases take views,
         # the batched phase the whole buffer
         self.gemv_codes_all = torch.empty((N_GEMV, 12288, 384), dtype=torch.uint8, device=device)
@@ -383,11 +387,13 @@ def capture_phases(w: Workload, stream):
                               g["B"].shape[1], g["C"], c.N, path=a.gemm_path)
 
     def gemm_ffma():
-        # the same three products on the FFMA path (the TMA-staged register-blocked kernel)
+        # the same three products on the FFMA path (the TMA-staged register-blocked kernel), with
+        # its stream-K tail (the automatic split of mm_gemm_f32_splitk_ex for this path)
         for g in w.gemm:
             c = g["case"]
-            mm.mm_gemm_f32_ex(c.transA, c.transB, c.M, c.N, c.K, g["A"], g["A"].shape[1], g["B"],
-                              g["B"].shape[1], g["C_ffma"], c.N, path=mm.MM_GEMM_FFMA)
+            mm.mm_gemm_f32_splitk_ex(c.transA, c.transB, c.M, c.N, c.K, g["A"], g["A"].shape[1], g["B"],
+                                     g["B"].shape[1], g["C_ffma"], c.N, 0, w.ffma_ws, w.ffma_ws_floats,
+                                     path=mm.MM_GEMM_FFMA)
 
     side = torch.cuda.Stream(device=stream.device)
     sides = [side] + [torch.cuda.Stream(device=stream.device) for _ in range(GEMV_INDEP_STREAMS - 2)]
@@ -947,7 +953,9 @@ def main_mm(args):
                    "gemm_path": args.gemm_path, "parallelism": f"replicas x{world}"},
         "gemm_ms_per_step": gemm_total_s / args.steps * 1e3,
         "square_2048_ffma": {"metric": "fp32 GEMM TFLOP/s, 2048^3 NN + NT + TN on the FFMA path "
-                                       "(mm_gemm_f32_ex, MM_GEMM_FFMA: TMA-staged 8x8 register blocks, packed f32x2 FMAs)",
+                                       "(mm_gemm_f32_splitk_ex, MM_GEMM_FFMA, automatic split: TMA-staged 8x8 "
+                                       "register blocks, packed f32x2 FMAs, stream-K tail)",
+                             "workspace_floats": w.ffma_ws_floats,
                              "value": world * 3 * GEMM_FLOP * args.steps / gemm_ffma_total_s / 1e12, "unit": "TFLOP/s",
                              "us_per_product": gemm_ffma_total_s / args.steps / 3 * 1e6,
                              "roofline": {"bound": "alu", "kernel": "gemm_ffma_kernel",
@@ -958,7 +966,9 @@ def main_mm(args):
                                           "peak_source": f"{sms} SMs x 128 FP32 lanes x 2 flop x "
                                                          f"{peaks.get('sm_max_mhz', 2070.0):.0f} MHz",
                                           "note": "256 tiles of 128 x 128 at one CTA per SM are 1.68 waves on 152 "
-                                                  "SMs: the SMs are busy ~83% of the time, the FMA pipe ~78% of that"}},
+                                                  "SMs: the first 152 tiles run whole, the k-steps of the other 104 "
+                                                  "are cut evenly over 152 CTAs (stream-K tail), whose partial tiles "
+                                                  "ffma_sk_reduce_kernel adds in K order"}},
         "gpt2_mlp_up_64": {"metric": "fp32 GEMM TFLOP/s, 64 x 768 x 3072 NN (one mm_gemm_f32 call, L2 flushed)",
                            "value": world * C1_FLOP / c1_call_s / 1e12, "unit": "TFLOP/s",
                            "us_per_call": c1_call_s * 1e6,
@@ -1058,7 +1068,8 @@ def main_mm(args):
         "roofline": roof,
         "phases": phases,
         "clocks": clk,
-        "gpu_launches": LAUNCHES_PER_STEP * args.steps,
+        # the FFMA phase's products add a reduce launch each when their stream-K tail runs
+        "gpu_launches": (LAUNCHES_PER_STEP + (3 if w.ffma_ws_floats else 0)) * args.steps,
         "wall_s": wall,
     }
     if rank == 0:

@@ -21,7 +21,7 @@ __all__ = [
     "mm_check_device_error", "mm_gemm_f32_splitk", "mm_gemm_f32_splitk_workspace", "mm_gemm_f32_splitk_noalloc",
     "MM_SPLITK_NOALLOC_MAX_FLOATS", "mm_gemm_f32_bias_act", "MM_ACT_NONE", "MM_ACT_GELU_TANH",
     "mm_gemv_packed2_strided_batched", "mm_gemv_packed2_strided_batched_ex", "mm_gemm_f32_bias_act_splitk",
-    "mm_gemm_f32_split_plan",
+    "mm_gemm_f32_split_plan", "mm_gemm_f32_splitk_ex", "mm_gemm_f32_splitk_workspace_ex", "mm_gemm_f32_split_plan_ex",
     "mm_probe_bounded_wait", "mm_attention_fwd", "mm_attention_bwd",
     "MM_OK", "MM_ERR_INVALID_ARG", "MM_ERR_UNSUPPORTED", "MM_ERR_CUDA", "MM_ERR_TIMEOUT",
     "MM_GEMM_AUTO", "MM_GEMM_FFMA", "MM_GEMM_TF32X3",
@@ -83,6 +83,11 @@ SIGNATURES = {
                                    ctypes.c_int),
     "mm_gemm_f32_bias_act": ([_I, _I, _I64, _I64, _I64, _P, _I64, _P, _I64, _P, _I, _P, _I64, _P], ctypes.c_int),
     "mm_gemm_f32_split_plan": ([_I64, _I64, _I64, _I, _P, _P], ctypes.c_int),
+    "mm_gemm_f32_splitk_ex": ([_I, _I, _I64, _I64, _I64, _P, _I64, _P, _I64, _P, _I64, _I, _P, _I64, _P,
+                               ctypes.POINTER(GemmOpts)], ctypes.c_int),
+    "mm_gemm_f32_splitk_workspace_ex": ([_I64, _I64, _I64, _I, ctypes.POINTER(GemmOpts),
+                                         ctypes.POINTER(ctypes.c_int64)], ctypes.c_int),
+    "mm_gemm_f32_split_plan_ex": ([_I64, _I64, _I64, _I, ctypes.POINTER(GemmOpts), _P, _P], ctypes.c_int),
     "mm_gemm_f32_bias_act_splitk": ([_I, _I, _I64, _I64, _I64, _P, _I64, _P, _I64, _P, _I, _P, _I64, _I, _P, _I64,
                                      _P], ctypes.c_int),
     "mm_gemv_packed2_strided_batched": ([_P, _I64, _P, _I64, _P, _I64, _P, _I64, _I64, _I64, _I64, _P, _P],
@@ -194,6 +199,33 @@ def mm_gemm_f32_split_plan(M, N, K, sms):
     sk = ctypes.c_int(0)
     fl = ctypes.c_int64(0)
     _check(load_library().mm_gemm_f32_split_plan(M, N, K, int(sms), ctypes.byref(sk), ctypes.byref(fl)))
+    return sk.value, fl.value
+
+
+def mm_gemm_f32_splitk_ex(transA, transB, M, N, K, A, lda, B, ldb, C, ldc, splitk, workspace, workspace_floats,
+                          stream=None, *, path=0, tile=0, opt_splitk=0):
+    """mm_gemm_f32_splitk with a kernel choice (path 1: the FFMA kernel and its stream-K tail)."""
+    o = GemmOpts(path, tile, opt_splitk)
+    _check(load_library().mm_gemm_f32_splitk_ex(int(transA), int(transB), M, N, K, _ptr(A), lda, _ptr(B), ldb,
+                                                _ptr(C), ldc, int(splitk), _ptr(workspace), int(workspace_floats),
+                                                _stream(stream), ctypes.byref(o)))
+
+
+def mm_gemm_f32_splitk_workspace_ex(M, N, K, splitk=0, *, path=0, tile=0, opt_splitk=0) -> int:
+    """Floats of workspace mm_gemm_f32_splitk_ex needs for these sizes, split and options."""
+    o = GemmOpts(path, tile, opt_splitk)
+    out = ctypes.c_int64(0)
+    _check(load_library().mm_gemm_f32_splitk_workspace_ex(M, N, K, int(splitk), ctypes.byref(o), ctypes.byref(out)))
+    return out.value
+
+
+def mm_gemm_f32_split_plan_ex(M, N, K, sms, *, path=0, tile=0, opt_splitk=0):
+    """(splitk, workspace_floats) of mm_gemm_f32_splitk_ex's automatic split for `sms` SMs; no device needed."""
+    o = GemmOpts(path, tile, opt_splitk)
+    sk = ctypes.c_int(0)
+    fl = ctypes.c_int64(0)
+    _check(load_library().mm_gemm_f32_split_plan_ex(M, N, K, int(sms), ctypes.byref(o), ctypes.byref(sk),
+                                                    ctypes.byref(fl)))
     return sk.value, fl.value
 
 

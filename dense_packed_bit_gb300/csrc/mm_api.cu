@@ -236,9 +236,81 @@ mm_status resolve_splitk(int64_t M, int64_t N, int64_t K, int splitk, int *out, 
     return MM_OK;
 }
 
+// The FFMA path's split: none (splitk 1), or the stream-K tail of the TMA-staged FFMA kernel
+// (0: when the last wave is at most kFfmaStreamKAutoTailPct % full; -1: whenever there is one).
+mm_status resolve_ffma_split(int64_t M, int64_t N, int64_t K, int splitk, int sms, mm::FfmaStreamKPlan *plan) {
+    *plan = mm::FfmaStreamKPlan{};
+    if (splitk < -1 || splitk > 1)
+        return fail(MM_ERR_INVALID_ARG, "FFMA path: splitk must be 0 (automatic), 1 (no split) or -1 (stream-K tail)");
+    if (splitk != 1)
+        mm::ffma_streamk_plan(M, N, K, sms, splitk == mm::kStreamK ? 100 : mm::kFfmaStreamKAutoTailPct, plan);
+    return MM_OK;
+}
+
+// The path of a split call's options: MM_GEMM_AUTO or MM_GEMM_FFMA, tile and splitk fields 0.
+mm_status split_path(const mm_gemm_opts *opts, int *path) {
+    *path = MM_GEMM_AUTO;
+    if (!opts) return MM_OK;
+    if (opts->path != MM_GEMM_AUTO && opts->path != MM_GEMM_FFMA)
+        return fail(MM_ERR_INVALID_ARG, "split entry points take path 0 (automatic) or 1 (FFMA), got %d", opts->path);
+    if (opts->tile != 0 || opts->splitk != 0)
+        return fail(MM_ERR_INVALID_ARG, "split entry points take opts.tile = 0 and opts.splitk = 0");
+    *path = opts->path;
+    return MM_OK;
+}
+
+int device_sms(mm_status *st) {
+    *st = check_device();
+    if (*st != MM_OK) return 0;
+    int dev = 0, sms = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    if (e != cudaSuccess) *st = cuda_fail(e, "cudaDeviceGetAttribute");
+    return sms;
+}
+
 }  // namespace
 
 extern "C" {
+
+mm_status mm_gemm_f32_split_plan_ex(int64_t M, int64_t N, int64_t K, int sms, const mm_gemm_opts *opts,
+                                    int *splitk, int64_t *workspace_floats) {
+    if (!splitk || !workspace_floats) return fail(MM_ERR_INVALID_ARG, "NULL output");
+    if (M < 1 || N < 1 || K < 1) return fail(MM_ERR_INVALID_ARG, "M, N, K must be >= 1");
+    if (sms < 2) return fail(MM_ERR_INVALID_ARG, "sms must be >= 2 (got %d)", sms);
+    int path = MM_GEMM_AUTO;
+    mm_status s = split_path(opts, &path);
+    if (s != MM_OK) return s;
+    if (path == MM_GEMM_AUTO) return mm_gemm_f32_split_plan(M, N, K, sms, splitk, workspace_floats);
+    mm::FfmaStreamKPlan plan;
+    s = resolve_ffma_split(M, N, K, 0, sms, &plan);
+    if (s != MM_OK) return s;
+    *splitk = plan.sk_ctas ? mm::kStreamK : 1;
+    *workspace_floats = plan.workspace_floats;
+    return ok();
+}
+
+mm_status mm_gemm_f32_splitk_workspace_ex(int64_t M, int64_t N, int64_t K, int splitk, const mm_gemm_opts *opts,
+                                          int64_t *floats) {
+    if (!floats) return fail(MM_ERR_INVALID_ARG, "floats is NULL");
+    if (M < 1 || N < 1 || K < 1) return fail(MM_ERR_INVALID_ARG, "M, N, K must be >= 1");
+    int path = MM_GEMM_AUTO;
+    mm_status s = split_path(opts, &path);
+    if (s != MM_OK) return s;
+    if (path == MM_GEMM_AUTO) return mm_gemm_f32_splitk_workspace(M, N, K, splitk, floats);
+    if (splitk < -1 || splitk > 1)
+        return fail(MM_ERR_INVALID_ARG, "FFMA path: splitk must be 0 (automatic), 1 (no split) or -1 (stream-K tail)");
+    int sms = 0;
+    if (splitk != 1) {
+        sms = device_sms(&s);
+        if (s != MM_OK) return s;
+    }
+    mm::FfmaStreamKPlan plan;
+    s = resolve_ffma_split(M, N, K, splitk, sms, &plan);
+    if (s != MM_OK) return s;
+    *floats = plan.workspace_floats;
+    return ok();
+}
 
 mm_status mm_gemm_f32_split_plan(int64_t M, int64_t N, int64_t K, int sms, int *splitk,
                                  int64_t *workspace_floats) {
@@ -267,7 +339,8 @@ namespace {
 // the split GEMM of mm_gemm_f32_splitk, with the linear layer's bias and activation
 mm_status gemm_splitk_impl(int transA, int transB, int64_t M, int64_t N, int64_t K, const float *A, int64_t lda,
                            const float *B, int64_t ldb, const float *bias, int act, float *C, int64_t ldc, int splitk,
-                           float *workspace, int64_t workspace_floats, mm_stream_t stream) {
+                           float *workspace, int64_t workspace_floats, mm_stream_t stream,
+                           const mm_gemm_opts *opts = nullptr) {
     if ((transA != 0 && transA != 1) || (transB != 0 && transB != 1))
         return fail(MM_ERR_INVALID_ARG, "transA/transB must be 0 or 1");
     if (M < 1 || N < 1 || K < 1)
@@ -295,9 +368,39 @@ mm_status gemm_splitk_impl(int transA, int transB, int64_t M, int64_t N, int64_t
             overlap(workspace, wb, C, cb))
             return fail(MM_ERR_INVALID_ARG, "workspace overlaps A, B or C");
     }
+    int path = MM_GEMM_AUTO;
+    mm_status s = split_path(opts, &path);
+    if (s != MM_OK) return s;
+    if (path == MM_GEMM_FFMA) {
+        // the TMA-staged FFMA kernel, with its stream-K tail when the split asks for one
+        if (splitk < -1 || splitk > 1)
+            return fail(MM_ERR_INVALID_ARG, "FFMA path: splitk must be 0 (automatic), 1 (no split) or -1 (stream-K tail)");
+        int sms = 0;
+        if (splitk != 1) {
+            sms = device_sms(&s);
+            if (s != MM_OK) return s;
+        }
+        mm::FfmaStreamKPlan plan;
+        s = resolve_ffma_split(M, N, K, splitk, sms, &plan);
+        if (s != MM_OK) return s;
+        if (plan.workspace_floats > 0 && (!workspace || workspace_floats < plan.workspace_floats))
+            return fail(MM_ERR_INVALID_ARG, "workspace of %lld floats needed (FFMA stream-K tail)",
+                        (long long)plan.workspace_floats);
+        s = check_device();
+        if (s != MM_OK) return s;
+        mm::GemmArgs g{transA, transB, M, N, K, A, lda, B, ldb, C, ldc};
+        g.bias = bias;
+        g.act = act;
+        cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+        const cudaError_t e = !mm::gemm_ffma_supported(g) ? mm::launch_gemm_simple(g, st)
+                              : plan.sk_ctas               ? mm::launch_gemm_ffma_streamk(g, plan, workspace, st)
+                                                           : mm::launch_gemm_ffma(g, 0, st);
+        if (e != cudaSuccess) return cuda_fail(e, "gemm launch");
+        return ok();
+    }
     int sk = 1;
     int64_t need = 0;
-    mm_status s = resolve_splitk(M, N, K, splitk, &sk, &need);
+    s = resolve_splitk(M, N, K, splitk, &sk, &need);
     if (s != MM_OK) return s;
     if (need > 0 && (!workspace || workspace_floats < need))
         return fail(MM_ERR_INVALID_ARG, "workspace of %lld floats needed (%s)", (long long)need,
@@ -328,6 +431,14 @@ mm_status mm_gemm_f32_splitk(int transA, int transB, int64_t M, int64_t N, int64
                              int64_t workspace_floats, mm_stream_t stream) {
     return gemm_splitk_impl(transA, transB, M, N, K, A, lda, B, ldb, nullptr, MM_ACT_NONE, C, ldc, splitk, workspace,
                             workspace_floats, stream);
+}
+
+mm_status mm_gemm_f32_splitk_ex(int transA, int transB, int64_t M, int64_t N, int64_t K, const float *A,
+                                int64_t lda, const float *B, int64_t ldb, float *C, int64_t ldc, int splitk,
+                                float *workspace, int64_t workspace_floats, mm_stream_t stream,
+                                const mm_gemm_opts *opts) {
+    return gemm_splitk_impl(transA, transB, M, N, K, A, lda, B, ldb, nullptr, MM_ACT_NONE, C, ldc, splitk, workspace,
+                            workspace_floats, stream, opts);
 }
 
 mm_status mm_gemm_f32_bias_act_splitk(int transA, int transB, int64_t M, int64_t N, int64_t K, const float *A,

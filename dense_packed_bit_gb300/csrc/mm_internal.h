@@ -193,6 +193,23 @@ unsigned int gemm_skinny_tc_take_device_error(cudaError_t *err);
 bool gemm_ffma_supported(const GemmArgs &g);
 cudaError_t launch_gemm_ffma(const GemmArgs &g, int tile, cudaStream_t s);
 
+// The same kernel with a stream-K tail: the first dp_tiles 128 x 128 tiles whole, one per CTA,
+// then the k-steps of the remaining tiles cut evenly over sk_ctas CTAs (each share shorter than
+// one tile's K range), whose partial tiles (two workspace slots of 128 x 128 floats per CTA) a
+// second kernel adds in K order into C (no bias or activation).  ffma_streamk_plan gives the split for `ctas` resident
+// CTAs (one per SM: the kernel's shared memory admits one), splitting a last wave of at most
+// max_tail_pct % of the CTAs; false = no tail to split (the plan is then zero and the plain
+// launch runs).
+constexpr int kFfmaStreamKMinSteps = 8;     // k-steps of 32 per share, at least
+constexpr int kFfmaStreamKAutoTailPct = 85; // automatic: a last wave fuller than this runs as it is
+struct FfmaStreamKPlan {
+    int tiles_n, dp_tiles, sk_ctas;
+    int64_t sk_iters;          // k-steps of the tail tiles, laid end to end
+    int64_t workspace_floats;  // 2 * sk_ctas * 128 * 128
+};
+bool ffma_streamk_plan(int64_t M, int64_t N, int64_t K, int ctas, int max_tail_pct, FfmaStreamKPlan *plan);
+cudaError_t launch_gemm_ffma_streamk(const GemmArgs &g, const FfmaStreamKPlan &plan, float *ws, cudaStream_t s);
+
 // 3xTF32 tcgen05 kernels: same operand requirements as the FFMA TMA kernel.
 // launch_gemm_tf32x3: one 128 x 128 tile per CTA, two stages, all threads split
 // and wait together; launch_gemm_tf32x3_ws: persistent, warp-specialised,

@@ -30,7 +30,7 @@ def main(argv=None):
     ap.add_argument("--layout", default="nn", choices=["nn", "nt", "tn"])
     ap.add_argument("--size", type=int, default=2048)
     ap.add_argument("--path", type=int, default=0)
-    ap.add_argument("--tile", type=int, default=0)
+    ap.add_argument("--tile", type=int, default=0, help="gemm --path 1 --tile 5: the FFMA kernel's stream-K tail")
     ap.add_argument("--reps", type=int, default=3)
     ap.add_argument("--matrices", type=int, default=64)
     ap.add_argument("--split", type=int, default=8)
@@ -61,7 +61,13 @@ def main(argv=None):
         A[:, :n] = torch.from_numpy(synth.normal_f32(1, (n, n), 0.02)).to(dev)
         B[:, :n] = torch.from_numpy(synth.normal_f32(2, (n, n), 0.02)).to(dev)
         C = torch.empty((n, ld), dtype=torch.float32, device=dev)
-        for _ in range(1 + a.reps):
+        if a.path == 1 and a.tile == 5:
+            # the FFMA kernel with its stream-K tail (mm_gemm_f32_splitk_ex, automatic split)
+            wsf = mm.mm_gemm_f32_splitk_workspace_ex(n, n, n, 0, path=1)
+            ws = torch.empty((max(wsf, 1),), dtype=torch.float32, device=dev)
+            for _ in range(1 + a.reps):
+                mm.mm_gemm_f32_splitk_ex(tA, tB, n, n, n, A, ld, B, ld, C, ld, 0, ws, wsf, path=1)
+        for _ in range(0 if (a.path == 1 and a.tile == 5) else 1 + a.reps):
             mm.mm_gemm_f32_ex(tA, tB, n, n, n, A, ld, B, ld, C, ld, path=a.path, tile=a.tile)
     elif a.op == "c1":
         c = synth.gpt2_mlp_up_64x768x3072()

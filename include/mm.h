@@ -332,6 +332,46 @@ mm_status mm_gemm_f32_ex(int transA, int transB, int64_t M, int64_t N, int64_t K
                          const float *A, int64_t lda, const float *B, int64_t ldb,
                          float *C, int64_t ldc, mm_stream_t stream, const mm_gemm_opts *opts);
 
+/*
+ * mm_gemm_f32_splitk with a choice of kernel.  opts NULL, or opts->path MM_GEMM_AUTO:
+ * exactly mm_gemm_f32_splitk.  opts->path MM_GEMM_FFMA: the TMA-staged register-blocked
+ * FFMA kernel ("I built a GPT-2 in the browser...", section "The kernel sweep": shared
+ * tiles and register blocks; "More Stumbling...", "Four answers per worker": one fixed
+ * accumulation order), 128 x 128 tiles, one CTA per SM.  When the tiles do not fill a
+ * whole number of waves, the last wave is partly idle (2048^2: 256 tiles on 152 SMs);
+ * with a stream-K tail the first floor(T / SMs) * SMs tiles run whole and the k-steps
+ * of the rest, laid end to end, are cut evenly over one CTA per SM, each share leaving
+ * its partial tiles (at most two) in the workspace, and a second kernel adds each
+ * tile's partial tiles in K order into C.  splitk: 0 = a tail when the last wave is
+ * at most 85% full, -1 = a tail whenever there is one, 1 = none; other values are
+ * refused for this path.  A share is at least 8 k-steps of 32 and at most one tile's
+ * K range, or there is no tail.  opts->tile and opts->splitk must be 0.
+ * Workspace: mm_gemm_f32_splitk_workspace_ex with the same opts (2 x SMs x 128 x 128
+ * floats with a tail, else 0); same rules as mm_gemm_f32_splitk.  Results are
+ * bit-reproducible run to run; with a tail they may differ from the unsplit kernel
+ * in the last bits (summation order).  Bound |C - C_exact| <= 1e-5 sum|a b| for any
+ * K (fp32 FMA, one rounding per step).  Operands TMA cannot describe run the plain
+ * tiled kernel unsplit.  Errors: as mm_gemm_f32_splitk, plus MM_ERR_INVALID_ARG for
+ * an unknown path, nonzero opts->tile or opts->splitk, or an FFMA splitk outside -1..1.
+ */
+mm_status mm_gemm_f32_splitk_ex(int transA, int transB, int64_t M, int64_t N, int64_t K,
+                                const float *A, int64_t lda, const float *B, int64_t ldb,
+                                float *C, int64_t ldc, int splitk, float *workspace,
+                                int64_t workspace_floats, mm_stream_t stream,
+                                const mm_gemm_opts *opts);
+
+/* The workspace mm_gemm_f32_splitk_ex needs for the same M, N, K, splitk and opts (the
+ * device's SM count decides the FFMA tail).  Errors as mm_gemm_f32_splitk_workspace, plus
+ * those of mm_gemm_f32_splitk_ex's options. */
+mm_status mm_gemm_f32_splitk_workspace_ex(int64_t M, int64_t N, int64_t K, int splitk,
+                                          const mm_gemm_opts *opts, int64_t *floats);
+
+/* mm_gemm_f32_split_plan for mm_gemm_f32_splitk_ex's automatic split (splitk = 0) on a GPU
+ * with `sms` SMs, without touching a device; for the FFMA path *splitk = -1 (a stream-K
+ * tail) or 1 (none). */
+mm_status mm_gemm_f32_split_plan_ex(int64_t M, int64_t N, int64_t K, int sms, const mm_gemm_opts *opts,
+                                    int *splitk, int64_t *workspace_floats);
+
 enum {
     MM_DEQ_AUTO = 0,     /* MM_DEQ_AFFINE (TMA-staged when the shape allows), MM_DEQ_SELECT
                             when the codebook is not affine: the fastest measured on GB300 for

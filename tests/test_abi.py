@@ -412,3 +412,102 @@ def test_attention_bwd_argument_errors(lib, case):
     st = mm.load_library().mm_attention_bwd(a["Q"], a["K"], a["V"], a["O"], a["dO"], a["L"], a["dQ"], a["dK"],
                                             a["dV"], 2, 16, 64, 1, 0.125, None)
     assert st == mm.MM_ERR_INVALID_ARG, lib.mm_last_error()
+
+
+# ------------------------------------------------------------------ FFMA stream-K tail
+
+def _ffma_tail(M, N, K, sms, max_pct=85):
+    """The documented rule of the FFMA path's stream-K tail: 128 x 128 tiles, k-steps of 32, one
+    CTA per SM; the last wave's tiles (if at most max_pct % of a wave) split over at most `sms`
+    shares of >= 8 k-steps, each no longer than one tile's K range.  None = no tail."""
+    tn, T, KT = -(-N // 128), -(-M // 128) * -(-N // 128), -(-K // 32)
+    rem = T % sms
+    if rem == 0 or rem * 100 > sms * max_pct:
+        return None
+    I = rem * KT
+    sk = min(I // 8, sms)
+    if sk < rem or sk < 2:
+        return None
+    return dict(T=T, KT=KT, dp=T - rem, rem=rem, sk=sk, I=I)
+
+
+def _cover(t):
+    """Every k-step of every tail tile in exactly one share, every share in at most two tiles
+    (its workspace slots 2j, 2j + 1), and the CTAs the reduce kernel visits for tile u (the
+    shares holding its first and last k-step and those between) are exactly those covering u."""
+    KT, I, sk = t["KT"], t["I"], t["sk"]
+    seen = [[] for _ in range(t["rem"])]
+    for j in range(sk):
+        s, e = j * I // sk, (j + 1) * I // sk
+        assert e - s >= 8
+        tiles = list(range(s // KT, (e - 1) // KT + 1))
+        assert len(tiles) <= 2
+        for q, u in enumerate(tiles):
+            lo, hi = max(s, u * KT), min(e, (u + 1) * KT)
+            seen[u].append((lo, hi, j, 2 * j + q))
+    for u, pieces in enumerate(seen):
+        assert pieces[0][0] == u * KT and pieces[-1][1] == (u + 1) * KT
+        assert all(a[1] == b[0] for a, b in zip(pieces, pieces[1:]))  # contiguous, in K order
+        cta_of = lambda i: ((i + 1) * sk + I - 1) // I - 1
+        ja, jb = cta_of(u * KT), cta_of((u + 1) * KT - 1)
+        assert [p[2] for p in pieces] == list(range(ja, jb + 1))
+        assert [p[3] for p in pieces] == [2 * j + (u - (j * I // sk) // KT) for j in range(ja, jb + 1)]
+
+
+@pytest.mark.parametrize("shape", [(2048, 2048, 2048), (4096, 4096, 4096), (8192, 8192, 2048), (500, 700, 3000),
+                                   (130, 260, 1000), (1700, 1650, 300), (1664, 1664, 300), (1664, 1664, 96),
+                                   (2432, 2176, 200), (64, 3072, 768), (1, 1, 1), (129, 129, 257),
+                                   (19456, 256, 24), (8192, 2048, 8192)])
+@pytest.mark.parametrize("sms", [152, 148, 7])
+def test_ffma_stream_k_plan(shape, sms):
+    mm.load_library()
+    t = _ffma_tail(*shape, sms)
+    sk, floats = mm.mm_gemm_f32_split_plan_ex(*shape, sms, path=mm.MM_GEMM_FFMA)
+    if t is None:
+        assert (sk, floats) == (1, 0)
+        return
+    assert (sk, floats) == (-1, 2 * t["sk"] * 128 * 128)
+    _cover(t)
+
+
+def test_ffma_stream_k_plan_on_the_bench_shape():
+    # 2048^2: 256 tiles on 152 SMs, a last wave of 104 tiles (68%): 152 whole tiles, then
+    # 104 x 64 k-steps cut into 152 shares of 43-44 k-steps, two 64 KiB slots per CTA
+    t = _ffma_tail(2048, 2048, 2048, 152)
+    assert (t["dp"], t["rem"], t["sk"], t["I"]) == (152, 104, 152, 6656)
+    mm.load_library()
+    assert mm.mm_gemm_f32_split_plan_ex(2048, 2048, 2048, 152, path=mm.MM_GEMM_FFMA) == (-1, 2 * 152 * 16384)
+    # the automatic path keeps its own plan (no split on CTA pairs at 2048^3)
+    assert mm.mm_gemm_f32_split_plan_ex(2048, 2048, 2048, 152) == mm.mm_gemm_f32_split_plan(2048, 2048, 2048, 152)
+
+
+@pytest.mark.parametrize("opts,splitk", [((2, 0, 0), 0), ((3, 0, 0), 0), ((1, 4, 0), 0), ((1, 0, 2), 0),
+                                         ((0, 1, 0), 0), ((1, 0, 0), 2), ((1, 0, 0), -2), ((1, 0, 0), 16)])
+def test_ffma_stream_k_refusals(lib, opts, splitk):
+    # split entry points take path 0 or 1 with opts.tile = opts.splitk = 0; the FFMA path takes
+    # splitk -1, 0 or 1: every other request is refused before any device call
+    o = mm.GemmOpts(*opts)
+    st = lib.mm_gemm_f32_splitk_ex(0, 0, 64, 64, 256, FAKE, 256, FAKE + 0x20000, 64, FAKE + 0x40000, 64, splitk,
+                                   FAKE + 0x100000, 1 << 20, None, ctypes.byref(o))
+    assert st == mm.MM_ERR_INVALID_ARG, lib.mm_last_error()
+    out = ctypes.c_int64(-1)
+    if opts[0] != 1 or opts[1] or opts[2] or splitk not in (-1, 0, 1):
+        assert lib.mm_gemm_f32_splitk_workspace_ex(64, 64, 256, splitk, ctypes.byref(o),
+                                                   ctypes.byref(out)) in (mm.MM_ERR_INVALID_ARG,)
+    if opts[0] != 1 or opts[1] or opts[2]:
+        sk = ctypes.c_int(0)
+        assert lib.mm_gemm_f32_split_plan_ex(64, 64, 256, 152, ctypes.byref(o), ctypes.byref(sk),
+                                             ctypes.byref(out)) == mm.MM_ERR_INVALID_ARG
+
+
+def test_ffma_stream_k_workspace_checks(lib):
+    # the tail needs 2 x SMs x 128 x 128 floats; without a device the size cannot be known, so a
+    # call that asks for no split needs none and a NULL workspace passes validation up to the
+    # device check
+    o = mm.GemmOpts(1, 0, 0)
+    out = ctypes.c_int64(-1)
+    assert lib.mm_gemm_f32_splitk_workspace_ex(2048, 2048, 2048, 1, ctypes.byref(o), ctypes.byref(out)) == mm.MM_OK
+    assert out.value == 0
+    st = lib.mm_gemm_f32_splitk_ex(0, 0, 64, 64, 256, FAKE, 256, FAKE + 0x20000, 64, FAKE + 0x40000, 64, 0,
+                                   FAKE + 0x100004, 1 << 20, None, ctypes.byref(o))
+    assert st == mm.MM_ERR_INVALID_ARG  # a misaligned workspace

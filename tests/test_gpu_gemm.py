@@ -512,3 +512,73 @@ def test_splitk_keeps_every_slice_within_the_k_margin(oracle):
         mm.mm_gemm_f32_splitk(0, 0, M, N, K, dA, K, dB, N, dC, N, splitk, ws if need else None, need)
         mm.mm_check_device_error()
         check_bound(to_host(dC), ref, T, f"split {splitk}, K={K}")
+
+
+# ------------------------------------------------------------------ FFMA kernel with a stream-K tail
+
+def run_ffma_sk(tA, tB, M, N, K, A, B, splitk=0, lda=None, ldb=None, ldc=None, fill=float("nan")):
+    import torch
+    lda = lda or A.shape[1]
+    ldb = ldb or B.shape[1]
+    ldc = ldc or N
+    dA, dB = to_dev(A), to_dev(B)
+    dC = empty_f32((M, ldc))
+    n = mm.mm_gemm_f32_splitk_workspace_ex(M, N, K, splitk, path=mm.MM_GEMM_FFMA)
+    ws = torch.full((max(n, 1),), fill, dtype=torch.float32, device=dA.device)  # contents must not matter
+    mm.mm_gemm_f32_splitk_ex(tA, tB, M, N, K, dA, lda, dB, ldb, dC, ldc, splitk, ws if n else None, n,
+                             path=mm.MM_GEMM_FFMA)
+    mm.mm_check_device_error()
+    return to_host(dC), n
+
+
+@pytest.mark.parametrize("splitk", [0, -1, 1])
+@pytest.mark.parametrize("layout", list(LAYOUTS))
+@pytest.mark.parametrize("shape", [(500, 700, 3000), (130, 260, 1000), (1700, 1650, 300), (1664, 1664, 300),
+                                   (2432, 2176, 200), (129, 129, 257)])
+def test_ffma_stream_k_parity(oracle, splitk, layout, shape):
+    # fewer tiles than SMs (every tile split), a short last wave after a whole one (the
+    # first 152 tiles whole, the rest split), a K too short for a split, ragged tiles and K
+    tA, tB = LAYOUTS[layout]
+    M, N, K = shape
+    A, B = stored(tA, tB, M, N, K, seed=1500 + M + N + K)
+    Ap = np.zeros((A.shape[0], (A.shape[1] + 3) // 4 * 4), np.float32); Ap[:, :A.shape[1]] = A
+    Bp = np.zeros((B.shape[0], (B.shape[1] + 3) // 4 * 4), np.float32); Bp[:, :B.shape[1]] = B
+    C, n = run_ffma_sk(tA, tB, M, N, K, Ap, Bp, splitk, lda=Ap.shape[1], ldb=Bp.shape[1], ldc=N + 2)
+    if splitk == 1:
+        assert n == 0
+    ref, T = oracle.gemm(tA, tB, M, N, K, A, B)
+    check_bound(C[:, :N], ref, T, f"FFMA stream-K {splitk} {layout} {shape} (workspace {n})")
+    assert np.all(np.isnan(C[:, N:])), "columns past N were written"
+
+
+@pytest.mark.parametrize("layout", ["nn", "nt", "tn"])
+def test_square_2048_ffma_stream_k_all_outputs(oracle, layout):
+    # the bench's FFMA phase: 256 tiles on 152 SMs, 152 whole and 104 split over 152 CTAs
+    c = synth.square_2048(layout)
+    C, n = run_ffma_sk(c.transA, c.transB, c.M, c.N, c.K, c.A, c.B, 0)
+    assert n > 0
+    ref, T = oracle.gemm(c.transA, c.transB, c.M, c.N, c.K, c.A, c.B)
+    worst = check_bound(C, ref, T, c.name + " FFMA stream-K")
+    print(f"{c.name} FFMA stream-K: worst |err|/T = {worst:.3e}")
+
+
+def test_ffma_stream_k_deterministic_and_integer_exact(oracle):
+    # integers: every partial sum exact, so the split tiles equal the oracle bit for bit; two
+    # runs with different workspace contents give the same bits
+    M, N, K = 1700, 1650, 600
+    A, B = stored(0, 1, M, N, K, seed=93, kind="int")
+    ref, _ = oracle.gemm(0, 1, M, N, K, A, B)
+    c1, n = run_ffma_sk(0, 1, M, N, K, A, B, -1)
+    c2, _ = run_ffma_sk(0, 1, M, N, K, A, B, -1, fill=-7.0)
+    assert n > 0
+    check_exact(c1, ref, "FFMA stream-K integers")
+    assert np.array_equal(c1.view(np.uint32), c2.view(np.uint32))
+
+
+def test_ffma_stream_k_unaligned_operands_take_general_path(oracle):
+    M, N, K = 1700, 1650, 301
+    A, B = stored(0, 0, M, N, K, seed=6)
+    Ap = np.zeros((M, K + 3), np.float32); Ap[:, :K] = A
+    C, _ = run_ffma_sk(0, 0, M, N, K, Ap, B, -1, lda=K + 3)
+    ref, T = oracle.gemm(0, 0, M, N, K, A, B)
+    check_bound(C, ref, T, "FFMA stream-K request, general path")
