@@ -1,6 +1,7 @@
 """Split-width sweep of the 2-bit GEMV decodes on the 12,288 x 1,536 rotation.
 
     python -m dense_packed_bit_gb300.sweep_gemv [--matrices 64] [--reps 15] [--json out.json]
+    python -m dense_packed_bit_gb300.sweep_gemv --streams-sweep [--reps 15]
 
 "Kernel 0112", section "The four variants", sweeps how many threads share one
 row's dot product (4, 16, 32).  This sweeps the same knob, and the ones around
@@ -21,6 +22,12 @@ replay gives microseconds per call and weight GB/s (4,718,592 code bytes per
 call) against the copy bandwidth in MEASURED_PEAKS.json when present.  A
 configuration the library refuses is listed as such.  Timing only: parity of
 every decode is the test suite's job.
+
+--streams-sweep: independent calls of the decodes the bench times, spread over 2, 4
+or 8 streams, by 127-row tiles per CTA (fp4 tensor-core decode, 12,288 x 1,536 and
+the transposed 1,536 x 12,288), 128-row blocks per CTA (TMA-staged SIMT decode) and
+64-row blocks per CTA (4-bit table decode, 32 matrices of 9 MiB); fraction of HBM on
+all the call's bytes.
 """
 from __future__ import annotations
 
@@ -61,7 +68,10 @@ def main(argv=None):
     ap.add_argument("--matrices", type=int, default=64)
     ap.add_argument("--reps", type=int, default=15)
     ap.add_argument("--json", default=None)
+    ap.add_argument("--streams-sweep", action="store_true")
     a = ap.parse_args(argv)
+    if a.streams_sweep:
+        return streams_sweep(a.reps)
 
     import numpy as np
     import torch
@@ -144,6 +154,103 @@ def main(argv=None):
               + (f"  {r['frac_hbm_total_bytes']:.3f} of HBM" if hbm else ""), flush=True)
     if a.json:
         json.dump(rows, open(a.json, "w"), indent=1)
+    return 0
+
+
+def streams_sweep(reps):
+    import numpy as np
+    import torch
+
+    import dense_packed_bit_gb300 as mm
+    from dense_packed_bit_gb300 import build, synth
+
+    build.build()
+    mm.load_library()
+    dev = torch.device("cuda:0")
+    hbm = 6772.5
+    peaks_path = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "MEASURED_PEAKS.json")
+    if os.path.exists(peaks_path):
+        hbm = json.load(open(peaks_path)).get("hbm_gbs") or hbm
+    streams = [torch.cuda.Stream(device=dev) for _ in range(8)]
+    main_st = streams[0]
+
+    def timed(fn, n):
+        try:
+            with torch.cuda.stream(main_st):
+                fn()
+        except mm.MMError:
+            torch.cuda.synchronize()
+            return float("nan")
+        torch.cuda.synchronize()
+        mm.mm_check_device_error()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=main_st):
+            fn()
+        ts = []
+        for _ in range(reps):
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            with torch.cuda.stream(main_st):
+                e0.record(main_st)
+                g.replay()
+                e1.record(main_st)
+            torch.cuda.synchronize()
+            ts.append(e0.elapsed_time(e1) * 1e3 / n)
+        mm.mm_check_device_error()
+        return float(np.median(ts))
+
+    def indep(call, n, ns):
+        def f():
+            cur = torch.cuda.current_stream()
+            sts = [cur] + streams[1:ns]
+            for s in sts[1:]:
+                s.wait_stream(cur)
+            for i in range(n):
+                call(i, sts[i % ns])
+            for s in sts[1:]:
+                cur.wait_stream(s)
+        return f
+
+    def load(fn, n):
+        cs = [fn(i) for i in range(n)]
+        codes = torch.stack([torch.from_numpy(c.codes) for c in cs]).to(dev)
+        scales = torch.stack([torch.from_numpy(c.scales.view("int16")) for c in cs]).to(dev)
+        return codes, scales, torch.from_numpy(cs[0].X.reshape(-1)).to(dev), cs[0].codebook
+
+    def report(label, us, nbytes):
+        print(f"{label:52s} {us:7.3f} us/call  {nbytes / us / 1e3 / hbm:.3f} of HBM", flush=True)
+
+    n = 64
+    total2 = 12288 * 384 + 12288 * 2 + 1536 * 2 + 12288 * 4
+    codes, scales, x, cb = load(synth.gemv_2bit_12288x1536, n)
+    y = torch.empty((n, 12288), dtype=torch.float32, device=dev)
+    for ns in (2, 4, 8):
+        for t in (6, 8, 10, 12, 15, 20, 25, 33, 49):
+            call = lambda i, s, t=t: mm.mm_gemv_packed2_ex(codes[i], scales[i], x, y[i], 12288, 1536, cb, s, pdl=1,
+                                                           independent=1, dequant=6, rows_per_lane=t)
+            report(f"12288x1536 fp4 decode, {t} tiles/CTA, {ns} streams", timed(indep(call, n, ns), n), total2)
+        for b in (2, 3, 4, 6):
+            call = lambda i, s, b=b: mm.mm_gemv_packed2_ex(codes[i], scales[i], x, y[i], 12288, 1536, cb, s, pdl=1,
+                                                           independent=1, dequant=2, staging=1, rows_per_lane=b)
+            report(f"12288x1536 staged SIMT, {b} blocks/CTA, {ns} streams", timed(indep(call, n, ns), n), total2)
+    del codes, scales
+    codes, scales, x, cb = load(synth.gemv_2bit_1536x12288, n)
+    y = torch.empty((n, 1536), dtype=torch.float32, device=dev)
+    total_t = 1536 * 3072 + 1536 * 2 + 12288 * 2 + 1536 * 4
+    for ns in (4, 8):
+        for t in (1, 2, 3, 4, 5, 7):
+            call = lambda i, s, t=t: mm.mm_gemv_packed2_ex(codes[i], scales[i], x, y[i], 1536, 12288, cb, s, pdl=1,
+                                                           independent=1, dequant=6, rows_per_lane=t)
+            report(f"1536x12288 fp4 decode, {t} tiles/CTA, {ns} streams", timed(indep(call, n, ns), n), total_t)
+    del codes, scales
+    n4 = 32
+    codes, scales, x, cb = load(synth.gemv_4bit_12288x1536, n4)
+    y = torch.empty((n4, 12288), dtype=torch.float32, device=dev)
+    total4 = 12288 * 768 + 12288 * 2 + 1536 * 2 + 12288 * 4
+    for ns in (2, 4, 8):
+        for b in (1, 2, 3):
+            call = lambda i, s, b=b: mm.mm_gemv_packed4_ex(codes[i], scales[i], x, y[i], 12288, 1536, cb, s,
+                                                           staging=1, blocks=b, pdl=1, independent=1)
+            report(f"12288x1536 4-bit table, {b} blocks/CTA, {ns} streams", timed(indep(call, n4, ns), n4), total4)
     return 0
 
 
