@@ -394,7 +394,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                     const int t = tb + u * LANES_T;
 #pragma unroll
                     for (int r = 0; r < S; ++r)
-                        if (t < p.ntok) v[u][r] = ld_cluster_v4(peer[r] + (uint32_t)(t * PSTR * 4));
+                        if (t < p.ntok && t0 + t < p.M && ok) v[u][r] = ld_cluster_v4(peer[r] + (uint32_t)(t * PSTR * 4));
                 }
 #pragma unroll
                 for (int u = 0; u < TB; ++u) {
@@ -421,9 +421,12 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                 }
             }
         }
-        // peers keep their shared memory alive until every CTA has read it (nothing to publish)
+        // peers keep their shared memory alive until every CTA has read it.  The arrive has
+        // release semantics so that it waits for this CTA's remote loads to be performed: a
+        // load whose value goes unused (a token past M) must not still be reading a peer's
+        // shared memory when that peer passes the barrier and exits.
         __syncwarp();
-        asm volatile("barrier.cluster.arrive.relaxed.aligned;\n\tbarrier.cluster.wait.aligned;" ::: "memory");
+        cluster_sync();
     }
     tc_fence_before_sync();
     __syncthreads();

@@ -348,11 +348,11 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                     float4 v[TB];
 #pragma unroll
                     for (int u = 0; u < TB; ++u)
-                        if (tb + u < p.ntok)
+                        if (tb + u < p.ntok && t0 + tb + u < p.M)
                             v[u] = ld_cluster_v4(cluster_map(base + (uint32_t)((tb + u) * PST * 4), (uint32_t)q));
 #pragma unroll
                     for (int u = 0; u < TB; ++u)
-                        if (tb + u < p.ntok) {
+                        if (tb + u < p.ntok && t0 + tb + u < p.M) {
                             acc[u].x += v[u].x;
                             acc[u].y += v[u].y;
                             acc[u].z += v[u].z;
@@ -371,8 +371,11 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                 }
             }
         }
-        // peers keep their shared memory alive until every CTA has read it (nothing to publish)
-        asm volatile("barrier.cluster.arrive.relaxed.aligned;\n\tbarrier.cluster.wait.aligned;" ::: "memory");
+        // peers keep their shared memory alive until every CTA has read it.  The arrive has
+        // release semantics so that it waits for this CTA's remote loads to be performed: a
+        // load whose value goes unused (a token past M) must not still be reading a peer's
+        // shared memory when that peer passes the barrier and exits.
+        cluster_sync();
     }
     tc_fence_before_sync();
     __syncthreads();
