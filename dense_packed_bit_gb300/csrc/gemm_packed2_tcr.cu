@@ -375,30 +375,37 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         }
         __syncwarp();
         cluster_sync();  // every partial tile is staged and visible to the cluster
+        // CTA z adds, for its FM / S features and every token, the S partials in rank order;
+        // thread (g, tl) takes 4 features and every LANES_T-th token, TB tokens per batch, and
+        // LANES_T * TB = 128 tokens per pass: at most two passes (ntok <= 256).  The sums are
+        // kept in registers; the CTA arrives at the closing cluster barrier (release: its remote
+        // loads have been performed, so no peer can pass the barrier and exit while one of them
+        // still reads its shared memory) before it stores Y, so the release does not wait for
+        // the global stores.
+        constexpr int FS = FM / S, GROUPS = FS / 4, LANES_T = NDEC / GROUPS, TB = 16 / S;
+        static_assert(LANES_T * TB == 128, "two passes cover 256 tokens");
+        const int d = tid - 64;
+        const int g = d % GROUPS, tl = d / GROUPS;
+        const int fl = z * FS + 4 * g;
+        float4 res[2][TB];
         if (warp >= WARP_DEC0) {
-            // CTA z adds, for its FM / S features and every token, the S partials in rank order;
-            // thread (g, tl) takes 4 features and every lanes_t-th token, TB tokens per batch
-            constexpr int FS = FM / S, GROUPS = FS / 4, LANES_T = NDEC / GROUPS, TB = 16 / S;
-            const int d = tid - 64;
-            const int g = d % GROUPS, tl = d / GROUPS;
-            const int fl = z * FS + 4 * g;
-            const float4 sc = *reinterpret_cast<const float4 *>(sscale + fl);
             const uint32_t base = smem_u32(part) + (uint32_t)(fl * 4);
             uint32_t peer[S];
 #pragma unroll
             for (int r = 0; r < S; ++r) peer[r] = cluster_map(base, (uint32_t)r);
-            for (int tb = tl; tb < p.ntok; tb += LANES_T * TB) {
+#pragma unroll
+            for (int it = 0; it < 2; ++it) {
                 float4 v[TB][S];
 #pragma unroll
                 for (int u = 0; u < TB; ++u) {
-                    const int t = tb + u * LANES_T;
+                    const int t = tl + it * 128 + u * LANES_T;
 #pragma unroll
                     for (int r = 0; r < S; ++r)
                         if (t < p.ntok && t0 + t < p.M && ok) v[u][r] = ld_cluster_v4(peer[r] + (uint32_t)(t * PSTR * 4));
                 }
 #pragma unroll
                 for (int u = 0; u < TB; ++u) {
-                    const int t = tb + u * LANES_T;
+                    const int t = tl + it * 128 + u * LANES_T;
                     if (t >= p.ntok || t0 + t >= p.M || !ok) continue;
                     float4 acc = v[u][0];
 #pragma unroll
@@ -408,8 +415,23 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                         acc.z += v[u][r].z;
                         acc.w += v[u][r].w;
                     }
-                    const int fg = f0 + fl;
+                    res[it][u] = acc;
+                }
+            }
+        }
+        __syncwarp();
+        cluster_arrive();
+        if (warp >= WARP_DEC0) {
+            const float4 sc = *reinterpret_cast<const float4 *>(sscale + fl);
+            const int fg = f0 + fl;
+#pragma unroll
+            for (int it = 0; it < 2; ++it)
+#pragma unroll
+                for (int u = 0; u < TB; ++u) {
+                    const int t = tl + it * 128 + u * LANES_T;
+                    if (t >= p.ntok || t0 + t >= p.M || !ok) continue;
                     float *yrow = p.y + (int64_t)(t0 + t) * p.rows + fg;
+                    const float4 acc = res[it][u];
                     const float r4[4] = {acc.x * sc.x, acc.y * sc.y, acc.z * sc.z, acc.w * sc.w};
                     if (p.vec && fg + 3 < p.rows) {
                         *reinterpret_cast<float4 *>(yrow) = make_float4(r4[0], r4[1], r4[2], r4[3]);
@@ -419,14 +441,9 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                             if (fg + j < p.rows) yrow[j] = r4[j];
                     }
                 }
-            }
         }
-        // peers keep their shared memory alive until every CTA has read it.  The arrive has
-        // release semantics so that it waits for this CTA's remote loads to be performed: a
-        // load whose value goes unused (a token past M) must not still be reading a peer's
-        // shared memory when that peer passes the barrier and exits.
         __syncwarp();
-        cluster_sync();
+        cluster_wait();
     }
     tc_fence_before_sync();
     __syncthreads();
